@@ -1,0 +1,14 @@
+"""GB300-native (sm_103a) Attention Residuals read operator.
+
+The hot path lives in libattnres_gb300.so (C ABI: include/attnres.h); this
+package is its thin Python binding plus seeded workload generators.
+"""
+from .ops import (  # noqa: F401
+    EPS_DEFAULT,
+    attnres,
+    attnres_bwd,
+    attnres_bwd_workspace_bytes,
+    attnres_check_device_error,
+    attnres_fwd,
+    attnres_plan_info,
+)

@@ -1,0 +1,109 @@
+"""ctypes view of the C ABI declared in include/attnres.h.
+
+Argument marshalling only: every step of the operator runs in the CUDA
+library.  Loading fails loudly when the library has not been built.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+MAX_S = 128
+MAX_D = 8192
+DEFAULT_SPLIT_N = 16384
+
+STATUS = {
+    0: "ATTNRES_OK",
+    1: "ATTNRES_ERR_INVALID_ARG",
+    2: "ATTNRES_ERR_ALIGNMENT",
+    3: "ATTNRES_ERR_UNSUPPORTED",
+    4: "ATTNRES_ERR_WORKSPACE",
+    5: "ATTNRES_ERR_CUDA",
+    6: "ATTNRES_ERR_DEVICE",
+}
+
+EXPORTED = [
+    "attnres_fwd",
+    "attnres_bwd",
+    "attnres_bwd_workspace_bytes",
+    "attnres_check_device_error",
+    "attnres_status_string",
+    "attnres_plan_info",
+]
+
+
+class AttnresParams(ctypes.Structure):
+    _fields_ = [
+        ("S", ctypes.c_int32),
+        ("D", ctypes.c_int32),
+        ("R", ctypes.c_int32),
+        ("key_offset", ctypes.c_int32),
+        ("N", ctypes.c_int64),
+        ("eps", ctypes.c_float),
+        ("scale", ctypes.c_float),
+        ("out_norm", ctypes.c_int32),
+        ("split_n_threshold", ctypes.c_int32),
+        ("src_ld", ctypes.c_int64),
+        ("src", ctypes.c_void_p * MAX_S),
+    ]
+
+
+class AttnresError(RuntimeError):
+    def __init__(self, code: int, where: str):
+        self.code = code
+        self.name = STATUS.get(code, str(code))
+        msg = _status_string(code)
+        super().__init__(f"{where}: {self.name}: {msg}")
+
+
+_lock = threading.Lock()
+_lib = None
+
+
+def library_path() -> str:
+    from .build import LIB_PATH
+    return LIB_PATH
+
+
+def load(path: str | None = None):
+    """Load the library (no build, no fallback)."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        p = path or library_path()
+        if not os.path.exists(p):
+            raise RuntimeError(
+                f"AttnRes CUDA library not found at {p}; build it with "
+                "`python -m attention_residuals_gb300.build` (needs nvcc for sm_103a)")
+        lib = ctypes.CDLL(p)
+        P = ctypes.POINTER(AttnresParams)
+        vp, fp, i64, sz = ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int64, ctypes.c_size_t
+        lib.attnres_fwd.restype = ctypes.c_int
+        lib.attnres_fwd.argtypes = [P, vp, vp, vp, fp, fp, fp, fp, vp, vp]
+        lib.attnres_bwd_workspace_bytes.restype = sz
+        lib.attnres_bwd_workspace_bytes.argtypes = [P]
+        lib.attnres_bwd.restype = ctypes.c_int
+        lib.attnres_bwd.argtypes = [P, vp, vp, vp, fp, fp, fp, fp, vp,
+                                    ctypes.POINTER(ctypes.c_void_p), i64, vp, fp, vp, fp, vp, sz, vp]
+        lib.attnres_check_device_error.restype = ctypes.c_int
+        lib.attnres_check_device_error.argtypes = []
+        lib.attnres_status_string.restype = ctypes.c_char_p
+        lib.attnres_status_string.argtypes = [ctypes.c_int]
+        lib.attnres_plan_info.restype = ctypes.c_int
+        lib.attnres_plan_info.argtypes = [P, ctypes.POINTER(ctypes.c_int64)]
+        _lib = lib
+        return lib
+
+
+def _status_string(code: int) -> str:
+    try:
+        return load().attnres_status_string(int(code)).decode()
+    except Exception:  # pragma: no cover - only when the library itself is missing
+        return STATUS.get(code, "unknown")
+
+
+def check(code: int, where: str):
+    if code != 0:
+        raise AttnresError(code, where)

@@ -1,0 +1,322 @@
+// attnres_api.cu -- the C ABI: argument validation, launch planning and
+// workspace sizing for the AttnRes read operator (include/attnres.h).
+#include <cmath>
+#include <cstring>
+
+#include "attnres.h"
+#include "kernels.cuh"
+
+namespace attnres {
+namespace {
+
+struct DeviceInfo {
+    int sm_count = 0;
+    int smem_optin = 0;
+};
+
+// Per-device properties, queried once.
+bool device_info(DeviceInfo* out) {
+    static DeviceInfo cache[64];
+    static bool have[64] = {false};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) return false;
+    if (dev < 64 && have[dev]) {
+        *out = cache[dev];
+        return true;
+    }
+    DeviceInfo d;
+    if (cudaDeviceGetAttribute(&d.sm_count, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+        return false;
+    if (cudaDeviceGetAttribute(&d.smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) !=
+        cudaSuccess)
+        return false;
+    if (dev < 64) {
+        cache[dev] = d;
+        have[dev] = true;
+    }
+    *out = d;
+    return true;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+bool aligned4(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
+
+int next_pow2(int x) {
+    int p = 1;
+    while (p < x) p <<= 1;
+    return p;
+}
+
+attnres_status check_shape(const attnres_params* p) {
+    if (!p) return ATTNRES_ERR_INVALID_ARG;
+    if (p->S < 1 || p->S > ATTNRES_MAX_S) return ATTNRES_ERR_INVALID_ARG;
+    if (p->D < 8 || p->D > ATTNRES_MAX_D) return ATTNRES_ERR_INVALID_ARG;
+    if (p->D % 8 != 0) return ATTNRES_ERR_ALIGNMENT;
+    if (p->R < 1 || p->R > p->D) return ATTNRES_ERR_INVALID_ARG;
+    if (p->key_offset < 0 || p->key_offset > p->D - p->R) return ATTNRES_ERR_INVALID_ARG;
+    if (p->N < 0) return ATTNRES_ERR_INVALID_ARG;
+    if (p->out_norm != 0 && p->out_norm != 1) return ATTNRES_ERR_INVALID_ARG;
+    if (!std::isfinite(p->eps) || p->eps < 0.0f) return ATTNRES_ERR_INVALID_ARG;
+    if (!std::isfinite(p->scale)) return ATTNRES_ERR_INVALID_ARG;
+    if (p->src_ld < p->D) return ATTNRES_ERR_INVALID_ARG;
+    if (p->src_ld % 8 != 0) return ATTNRES_ERR_ALIGNMENT;
+    if (p->N == 0) return ATTNRES_OK;  // nothing is read: pointers may be NULL
+    for (int s = 0; s < p->S; ++s) {
+        if (!p->src[s]) return ATTNRES_ERR_INVALID_ARG;
+        if (!aligned16(p->src[s])) return ATTNRES_ERR_ALIGNMENT;
+    }
+    return ATTNRES_OK;
+}
+
+attnres_status make_plan(const attnres_params* p, Plan* plan) {
+    DeviceInfo dev;
+    if (!device_info(&dev)) return ATTNRES_ERR_CUDA;
+    Plan pl{};
+    const int ncv = p->D / 8;
+    pl.vpt = ncv <= 256 ? 1 : (ncv <= 512 ? 2 : 4);
+    pl.ncw = (ncv + 32 * pl.vpt - 1) / (32 * pl.vpt);
+    if (pl.ncw < 1 || pl.ncw > kMaxConsumerWarps) return ATTNRES_ERR_UNSUPPORTED;
+    pl.slot_bytes = static_cast<int>(align_up(static_cast<uint32_t>(p->D) * 2u, 128u));
+    pl.s_pad = static_cast<int>(align_up(static_cast<uint32_t>(p->S), 4u));
+    // Ring depth: as many row slots as the backward layout (the larger) fits.
+    int slots = 0;
+    for (int k = kMaxSlots; k >= 1; --k) {
+        if (make_layout(k, pl.slot_bytes, pl.ncw, pl.s_pad, true).total <=
+            static_cast<uint32_t>(dev.smem_optin)) {
+            slots = k;
+            break;
+        }
+    }
+    if (slots < 4) return ATTNRES_ERR_UNSUPPORTED;
+    pl.slots = slots;
+    pl.smem_fwd = make_layout(slots, pl.slot_bytes, pl.ncw, pl.s_pad, false).total;
+    pl.smem_bwd = make_layout(slots, pl.slot_bytes, pl.ncw, pl.s_pad, true).total;
+    // Forward groups keep their rows resident: at most half the ring each.
+    int gp = next_pow2(p->S);
+    if (gp < 2) gp = 2;
+    if (gp > 16) gp = 16;
+    while (gp > 2 && 2 * (gp < p->S ? gp : p->S) > slots) gp >>= 1;
+    pl.gp_fwd = gp;
+    int gpb = next_pow2(p->S);
+    if (gpb < 2) gpb = 2;
+    if (gpb > 16) gpb = 16;
+    pl.gp_bwd = gpb;
+    pl.resident = (p->S + 1 + p->out_norm) <= slots ? 1 : 0;
+    const int thr = p->split_n_threshold > 0 ? p->split_n_threshold : ATTNRES_DEFAULT_SPLIT_N;
+    pl.split = p->N >= thr ? 1 : 0;
+    long long grid = dev.sm_count;
+    if (p->N < grid) grid = p->N;
+    if (grid < 1) grid = 1;
+    pl.grid = static_cast<int>(grid);
+    pl.ngroups = (pl.grid + kGroupTicket - 1) / kGroupTicket;
+    const size_t W = static_cast<size_t>(p->R) + (p->out_norm ? static_cast<size_t>(p->D) : 0u);
+    size_t off = align_up(static_cast<uint32_t>((pl.ngroups + 1) * 4), 256u);
+    pl.ws_part_off = off;
+    off += align_up(static_cast<uint32_t>(pl.grid * W * 4), 256u);
+    pl.ws_gpart_off = off;
+    off += static_cast<size_t>(pl.ngroups) * W * 4;
+    pl.ws_bytes = p->N == 0 ? 0 : off;
+    *plan = pl;
+    return ATTNRES_OK;
+}
+
+bool ranges_overlap(const void* a, size_t na, const void* b, size_t nb) {
+    const uintptr_t x = reinterpret_cast<uintptr_t>(a), y = reinterpret_cast<uintptr_t>(b);
+    return x < y + nb && y < x + na;
+}
+
+}  // namespace
+}  // namespace attnres
+
+using namespace attnres;
+
+extern "C" {
+
+const char* attnres_status_string(attnres_status s) {
+    switch (s) {
+        case ATTNRES_OK: return "ok";
+        case ATTNRES_ERR_INVALID_ARG: return "invalid argument (size, flag or NULL pointer)";
+        case ATTNRES_ERR_ALIGNMENT: return "alignment: rows must start on 16-byte boundaries, D and row strides multiples of 8";
+        case ATTNRES_ERR_UNSUPPORTED: return "unsupported configuration for this build";
+        case ATTNRES_ERR_WORKSPACE: return "workspace missing or too small";
+        case ATTNRES_ERR_CUDA: return "CUDA runtime error";
+        case ATTNRES_ERR_DEVICE: return "a kernel gave up waiting on a shared-memory barrier";
+        default: return "unknown status";
+    }
+}
+
+attnres_status attnres_plan_info(const attnres_params* p, int64_t out[8]) {
+    attnres_status st = check_shape(p);
+    if (st != ATTNRES_OK) return st;
+    if (!out) return ATTNRES_ERR_INVALID_ARG;
+    Plan pl;
+    st = make_plan(p, &pl);
+    if (st != ATTNRES_OK) return st;
+    out[0] = pl.grid;
+    out[1] = pl.ncw;
+    out[2] = pl.vpt;
+    out[3] = pl.slots;
+    out[4] = pl.gp_fwd;
+    out[5] = pl.resident;
+    out[6] = static_cast<int64_t>(pl.smem_bwd);
+    out[7] = pl.split;
+    return ATTNRES_OK;
+}
+
+attnres_status attnres_fwd(const attnres_params* p, const void* q, const void* w_o, void* y,
+                           float* alpha, float* rstd, float* logit, float* o_rstd, void* o_pre,
+                           void* stream) {
+    attnres_status st = check_shape(p);
+    if (st != ATTNRES_OK) return st;
+    if (p->N == 0) return ATTNRES_OK;
+    if (!q || !y || !alpha || !rstd || !logit) return ATTNRES_ERR_INVALID_ARG;
+    if (p->out_norm && (!w_o || !o_rstd || !o_pre)) return ATTNRES_ERR_INVALID_ARG;
+    if (!aligned16(y) || !aligned4(alpha) || !aligned4(rstd) || !aligned4(logit))
+        return ATTNRES_ERR_ALIGNMENT;
+    if (p->out_norm && (!aligned16(o_pre) || !aligned4(o_rstd))) return ATTNRES_ERR_ALIGNMENT;
+    if ((reinterpret_cast<uintptr_t>(q) & 1u) || (w_o && (reinterpret_cast<uintptr_t>(w_o) & 1u)))
+        return ATTNRES_ERR_ALIGNMENT;
+    Plan pl;
+    st = make_plan(p, &pl);
+    if (st != ATTNRES_OK) return st;
+    FwdArgs a;
+    std::memset(&a, 0, sizeof a);
+    for (int s = 0; s < p->S; ++s) a.src[s] = p->src[s];
+    a.N = p->N;
+    a.src_ld = p->src_ld;
+    a.S = p->S;
+    a.D = p->D;
+    a.R = p->R;
+    a.ko = p->key_offset;
+    a.out_norm = p->out_norm;
+    a.eps = p->eps;
+    a.scale = p->scale;
+    a.slots = pl.slots;
+    a.slot_bytes = pl.slot_bytes;
+    a.ncw = pl.ncw;
+    a.s_pad = pl.s_pad;
+    a.q = static_cast<const uint16_t*>(q);
+    a.w_o = static_cast<const uint16_t*>(w_o);
+    a.y = static_cast<uint16_t*>(y);
+    a.alpha = alpha;
+    a.rstd = rstd;
+    a.logit = logit;
+    a.o_rstd = o_rstd;
+    a.o_pre = static_cast<uint16_t*>(o_pre);
+    return launch_fwd(pl, a, static_cast<cudaStream_t>(stream)) == cudaSuccess ? ATTNRES_OK
+                                                                              : ATTNRES_ERR_CUDA;
+}
+
+size_t attnres_bwd_workspace_bytes(const attnres_params* p) {
+    if (check_shape(p) != ATTNRES_OK) return 0;
+    Plan pl;
+    if (make_plan(p, &pl) != ATTNRES_OK) return 0;
+    return pl.ws_bytes;
+}
+
+attnres_status attnres_bwd(const attnres_params* p, const void* q, const void* w_o, const void* dy,
+                           const float* alpha, const float* rstd, const float* logit,
+                           const float* o_rstd, const void* o_pre, void* const* dsrc,
+                           int64_t dsrc_ld, void* dq, float* dq_f32, void* dw_o, float* dw_o_f32,
+                           void* workspace, size_t workspace_bytes, void* stream) {
+    attnres_status st = check_shape(p);
+    if (st != ATTNRES_OK) return st;
+    if (p->N == 0) {
+        // Empty sums: dq and dw_o are zero; nothing else is touched.
+        if (!dq || (p->out_norm && !dw_o)) return ATTNRES_ERR_INVALID_ARG;
+        cudaStream_t s0 = static_cast<cudaStream_t>(stream);
+        if (cudaMemsetAsync(dq, 0, static_cast<size_t>(p->R) * 2, s0) != cudaSuccess ||
+            (dq_f32 && cudaMemsetAsync(dq_f32, 0, static_cast<size_t>(p->R) * 4, s0) != cudaSuccess) ||
+            (dw_o && cudaMemsetAsync(dw_o, 0, static_cast<size_t>(p->D) * 2, s0) != cudaSuccess) ||
+            (dw_o_f32 && cudaMemsetAsync(dw_o_f32, 0, static_cast<size_t>(p->D) * 4, s0) != cudaSuccess))
+            return ATTNRES_ERR_CUDA;
+        return ATTNRES_OK;
+    }
+    if (!q || !dy || !alpha || !rstd || !logit || !dsrc || !dq) return ATTNRES_ERR_INVALID_ARG;
+    if (p->out_norm && (!w_o || !o_rstd || !o_pre || !dw_o)) return ATTNRES_ERR_INVALID_ARG;
+    if (dsrc_ld < p->D) return ATTNRES_ERR_INVALID_ARG;
+    if (dsrc_ld % 8 != 0) return ATTNRES_ERR_ALIGNMENT;
+    if (!aligned16(dy) || !aligned4(alpha) || !aligned4(rstd) || !aligned4(logit))
+        return ATTNRES_ERR_ALIGNMENT;
+    if (p->out_norm && (!aligned16(o_pre) || !aligned4(o_rstd))) return ATTNRES_ERR_ALIGNMENT;
+    if ((reinterpret_cast<uintptr_t>(q) & 1u) || (reinterpret_cast<uintptr_t>(dq) & 1u) ||
+        (dq_f32 && !aligned4(dq_f32)) || (dw_o && (reinterpret_cast<uintptr_t>(dw_o) & 1u)) ||
+        (dw_o_f32 && !aligned4(dw_o_f32)) || (w_o && (reinterpret_cast<uintptr_t>(w_o) & 1u)))
+        return ATTNRES_ERR_ALIGNMENT;
+    const size_t n_rows = static_cast<size_t>(p->N);
+    const size_t d_bytes = n_rows == 0 ? 0 : ((n_rows - 1) * static_cast<size_t>(dsrc_ld) + p->D) * 2;
+    const size_t s_bytes = n_rows == 0 ? 0 : ((n_rows - 1) * static_cast<size_t>(p->src_ld) + p->D) * 2;
+    for (int s = 0; s < p->S; ++s) {
+        if (!dsrc[s]) return ATTNRES_ERR_INVALID_ARG;
+        if (!aligned16(dsrc[s])) return ATTNRES_ERR_ALIGNMENT;
+    }
+    {
+        for (int s = 0; s < p->S; ++s) {
+            for (int t = 0; t < p->S; ++t) {
+                if (t != s && ranges_overlap(dsrc[s], d_bytes, dsrc[t], d_bytes))
+                    return ATTNRES_ERR_INVALID_ARG;
+                if (ranges_overlap(dsrc[s], d_bytes, p->src[t], s_bytes)) return ATTNRES_ERR_INVALID_ARG;
+            }
+        }
+    }
+    Plan pl;
+    st = make_plan(p, &pl);
+    if (st != ATTNRES_OK) return st;
+    if (!workspace || workspace_bytes < pl.ws_bytes) return ATTNRES_ERR_WORKSPACE;
+    if (!aligned16(workspace)) return ATTNRES_ERR_ALIGNMENT;
+    BwdArgs a;
+    std::memset(&a, 0, sizeof a);
+    for (int s = 0; s < p->S; ++s) {
+        a.src[s] = p->src[s];
+        a.dsrc[s] = dsrc[s];
+    }
+    a.N = p->N;
+    a.src_ld = p->src_ld;
+    a.dsrc_ld = dsrc_ld;
+    a.S = p->S;
+    a.D = p->D;
+    a.R = p->R;
+    a.ko = p->key_offset;
+    a.out_norm = p->out_norm;
+    a.eps = p->eps;
+    a.scale = p->scale;
+    a.slots = pl.slots;
+    a.slot_bytes = pl.slot_bytes;
+    a.ncw = pl.ncw;
+    a.s_pad = pl.s_pad;
+    a.resident = pl.resident;
+    a.split = pl.split;
+    a.ngroups = pl.ngroups;
+    a.q = static_cast<const uint16_t*>(q);
+    a.w_o = static_cast<const uint16_t*>(w_o);
+    a.dy = static_cast<const uint16_t*>(dy);
+    a.alpha = alpha;
+    a.rstd = rstd;
+    a.logit = logit;
+    a.o_rstd = o_rstd;
+    a.o_pre = static_cast<const uint16_t*>(o_pre);
+    unsigned char* ws = static_cast<unsigned char*>(workspace);
+    a.tickets = reinterpret_cast<unsigned*>(ws);
+    a.part = reinterpret_cast<float*>(ws + pl.ws_part_off);
+    a.gpart = reinterpret_cast<float*>(ws + pl.ws_gpart_off);
+    a.dq = static_cast<uint16_t*>(dq);
+    a.dq_f32 = dq_f32;
+    a.dw_o = static_cast<uint16_t*>(dw_o);
+    a.dw_o_f32 = dw_o_f32;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (!pl.split) {
+        if (cudaMemsetAsync(a.tickets, 0, static_cast<size_t>(pl.ngroups + 1) * 4, s) != cudaSuccess)
+            return ATTNRES_ERR_CUDA;
+    }
+    return launch_bwd(pl, a, s) == cudaSuccess ? ATTNRES_OK : ATTNRES_ERR_CUDA;
+}
+
+attnres_status attnres_check_device_error(void) {
+    if (cudaDeviceSynchronize() != cudaSuccess) return ATTNRES_ERR_CUDA;
+    const unsigned f = take_fwd_error();
+    const unsigned b = take_bwd_error();
+    if (f == 0xffffffffu || b == 0xffffffffu) return ATTNRES_ERR_CUDA;
+    return (f || b) ? ATTNRES_ERR_DEVICE : ATTNRES_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,137 @@
+// kernels.cuh -- kernel arguments, shared-memory layout and launch plan of
+// the AttnRes forward/backward kernels (internal to the library).
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "attnres.h"
+
+namespace attnres {
+
+constexpr int kMaxConsumerWarps = 8;
+constexpr int kMaxThreads = (kMaxConsumerWarps + 1) * 32;  // + one producer warp
+constexpr int kMaxSlots = 64;
+constexpr int kTokSlots = 4;      // token-statistics ring depth (backward)
+constexpr int kGroupTicket = 12;  // CTAs per first-level group of the in-kernel reduction
+constexpr int kReduceStride = 32; // floats per warp in the reduction scratch
+
+// Where a bounded wait gave up (value recorded in g_device_error).
+enum WaitSite : unsigned {
+    kSiteFwdProducer = 1,
+    kSiteFwdConsumer = 2,
+    kSiteBwdProducer = 3,
+    kSiteBwdConsumer = 4,
+    kSiteBwdTokStat = 5,
+    kSiteDrain = 6,
+};
+
+// Launch plan: one persistent CTA per SM; `ncw` consumer warps each own
+// `vpt` 16-byte column vectors of every row; a ring of `slots` row buffers
+// of `slot_bytes` each is filled by one producer thread with 1-D TMA copies.
+struct Plan {
+    int grid;
+    int ncw;
+    int vpt;
+    int slots;
+    int slot_bytes;
+    int gp_fwd;       // sources per forward group (power of two)
+    int gp_bwd;       // sources per backward dot-pass group (power of two)
+    int resident;     // backward keeps a token's rows between its two passes
+    int split;        // backward reduction via the finalize kernel
+    int s_pad;        // S rounded up to 4
+    size_t smem_fwd;
+    size_t smem_bwd;
+    size_t ws_bytes;  // backward workspace
+    size_t ws_part_off, ws_gpart_off;
+    int ngroups;
+};
+
+// Byte offsets inside the dynamic shared memory of one CTA.
+struct SmemLayout {
+    uint32_t ring, full, empty, tfull, tempty, red, tok, coef, misc, total;
+};
+
+__host__ __device__ inline uint32_t align_up(uint32_t x, uint32_t a) { return (x + a - 1) / a * a; }
+
+// coef holds per-token vectors: forward z[s_pad], rstd[s_pad], group
+// coefficients 2 x 64; backward alpha[s_pad], c1[s_pad], c2[s_pad], da[s_pad].
+__host__ __device__ inline SmemLayout make_layout(int slots, int slot_bytes, int ncw, int s_pad,
+                                                  bool backward) {
+    SmemLayout L;
+    uint32_t off = 0;
+    L.ring = off;
+    off += static_cast<uint32_t>(slots) * static_cast<uint32_t>(slot_bytes);
+    off = align_up(off, 16);
+    L.full = off;
+    off += 8u * slots;
+    L.empty = off;
+    off += 8u * slots;
+    L.tfull = off;
+    off += backward ? 8u * kTokSlots : 0u;
+    L.tempty = off;
+    off += backward ? 8u * kTokSlots : 0u;
+    off = align_up(off, 16);
+    L.red = off;
+    off += 2u * ncw * kReduceStride * 4u;
+    L.tok = off;
+    off += backward ? static_cast<uint32_t>(kTokSlots) * (3u * s_pad + 4u) * 4u : 0u;
+    L.coef = off;
+    off += backward ? 4u * s_pad * 4u : (2u * s_pad + 2u * 64u) * 4u;
+    L.misc = off;  // abort flag, ticket flags
+    off += 16u;
+    L.total = align_up(off, 128);
+    return L;
+}
+
+struct FwdArgs {
+    const void* src[ATTNRES_MAX_S];
+    long long N;
+    long long src_ld;
+    int S, D, R, ko, out_norm;
+    float eps, scale;
+    int slots, slot_bytes, ncw, s_pad;
+    const uint16_t* q;
+    const uint16_t* w_o;
+    uint16_t* y;
+    float* alpha;
+    float* rstd;
+    float* logit;
+    float* o_rstd;
+    uint16_t* o_pre;
+};
+
+struct BwdArgs {
+    const void* src[ATTNRES_MAX_S];
+    void* dsrc[ATTNRES_MAX_S];
+    long long N;
+    long long src_ld, dsrc_ld;
+    int S, D, R, ko, out_norm;
+    float eps, scale;
+    int slots, slot_bytes, ncw, s_pad, resident, split, ngroups;
+    const uint16_t* q;
+    const uint16_t* w_o;
+    const uint16_t* dy;
+    const float* alpha;
+    const float* rstd;
+    const float* logit;
+    const float* o_rstd;
+    const uint16_t* o_pre;
+    float* part;        // [grid][R + Dw] per-CTA partial sums (Dw = out_norm ? D : 0)
+    float* gpart;       // [ngroups][R + Dw] group sums (in-kernel reduction)
+    unsigned* tickets;  // [ngroups + 1] zeroed before launch (in-kernel reduction)
+    uint16_t* dq;
+    float* dq_f32;
+    uint16_t* dw_o;
+    float* dw_o_f32;
+};
+
+// Host-side launchers (return a CUDA error code) and the per-kernel records
+// of failed waits (read and cleared; 0 = none).
+unsigned take_fwd_error();
+unsigned take_bwd_error();
+cudaError_t launch_fwd(const Plan& plan, const FwdArgs& a, cudaStream_t stream);
+cudaError_t launch_bwd(const Plan& plan, const BwdArgs& a, cudaStream_t stream);
+
+}  // namespace attnres

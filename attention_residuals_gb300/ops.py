@@ -1,0 +1,283 @@
+"""Python binding of the C ABI (same names), plus the autograd operator.
+
+PyTorch provides device memory, the current stream and autograd plumbing;
+the binding only marshals pointers and sizes.  Every step of the operator
+("Fast Attention Residuals", section "Equation", with the optional output
+RMSNorm of "[Perf] Parallelize AttnRes long-sequence reduction") runs in the
+CUDA library.  There is no CPU path: CPU tensors are rejected.
+"""
+from __future__ import annotations
+
+import ctypes
+from dataclasses import dataclass
+from typing import List, Optional, Sequence, Union
+
+import torch
+
+from . import _lib
+
+EPS_DEFAULT = 2.0 ** -23
+Sources = Union[torch.Tensor, Sequence[torch.Tensor]]
+
+
+# --------------------------------------------------------------------------
+# Source marshalling
+# --------------------------------------------------------------------------
+@dataclass
+class _SourceView:
+    rows: List[torch.Tensor]   # S tensors viewed as [N, D] with a common row stride
+    packed: bool
+    lead_shape: tuple          # leading (token) shape of one source
+    N: int
+    D: int
+    ld: int
+
+
+def _as_rows(t: torch.Tensor, D: int) -> torch.Tensor:
+    if t.shape[-1] != D:
+        raise ValueError("every source must have the same last dimension D")
+    if t.dim() == 1:
+        t = t.unsqueeze(0)
+    r = t.reshape(-1, D) if t.is_contiguous() else None
+    if r is None:
+        try:
+            r = t.view(-1, D)
+        except RuntimeError:
+            r = None
+    if r is None or r.stride(1) != 1 or (r.shape[0] > 1 and r.stride(0) < D):
+        r = t.contiguous().view(-1, D)
+    return r
+
+
+def _source_view(values: Sources) -> _SourceView:
+    if isinstance(values, torch.Tensor):
+        if values.dim() < 2:
+            raise ValueError("packed values must be [S, ..., D]")
+        S, D = values.shape[0], values.shape[-1]
+        lead = tuple(values.shape[1:-1])
+        rows = [_as_rows(values[s], D) for s in range(S)]
+        packed = True
+    else:
+        vals = list(values)
+        if not vals:
+            raise ValueError("need at least one source")
+        D = vals[0].shape[-1]
+        lead = tuple(vals[0].shape[:-1])
+        for v in vals:
+            if tuple(v.shape[:-1]) != lead:
+                raise ValueError("all sources must have the same shape")
+        rows = [_as_rows(v, D) for v in vals]
+        packed = False
+    for r in rows:
+        if r.dtype != torch.bfloat16:
+            raise TypeError("sources must be torch.bfloat16")
+        if not r.is_cuda:
+            raise TypeError("sources must be CUDA tensors (the operator has no CPU path)")
+    N = rows[0].shape[0]
+    lds = {int(r.stride(0)) if r.shape[0] > 1 else D for r in rows}
+    if len(lds) != 1 or any(r.data_ptr() % 16 for r in rows) or next(iter(lds)) % 8:
+        rows = [r.contiguous() for r in rows]
+        lds = {D}
+    return _SourceView(rows=rows, packed=packed, lead_shape=lead, N=N, D=D, ld=next(iter(lds)))
+
+
+def make_params(view: _SourceView, R: int, *, key_offset: Optional[int], eps: float, scale: float,
+                out_norm: bool, split_n_threshold: int = 0) -> _lib.AttnresParams:
+    S = len(view.rows)
+    if S > _lib.MAX_S:
+        raise ValueError(f"at most {_lib.MAX_S} sources")
+    p = _lib.AttnresParams()
+    p.S = S
+    p.D = view.D
+    p.R = int(R)
+    p.key_offset = view.D - int(R) if key_offset is None else int(key_offset)
+    p.N = view.N
+    p.eps = float(eps)
+    p.scale = float(scale)
+    p.out_norm = 1 if out_norm else 0
+    p.split_n_threshold = int(split_n_threshold)
+    p.src_ld = view.ld
+    for s, r in enumerate(view.rows):
+        p.src[s] = r.data_ptr()
+    return p
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream) -> ctypes.c_void_p:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream))
+
+
+def _check_vec(t: Optional[torch.Tensor], n: int, name: str):
+    if t is None:
+        return None
+    if t.dtype != torch.bfloat16 or not t.is_cuda or t.numel() != n:
+        raise TypeError(f"{name} must be a CUDA bf16 tensor with {n} elements")
+    return t.contiguous()
+
+
+# --------------------------------------------------------------------------
+# C-ABI mirrors
+# --------------------------------------------------------------------------
+def attnres_plan_info(values: Sources, R: int, *, key_offset=None, out_norm=False,
+                      split_n_threshold=0) -> dict:
+    view = _source_view(values)
+    p = make_params(view, R, key_offset=key_offset, eps=EPS_DEFAULT, scale=1.0, out_norm=out_norm,
+                    split_n_threshold=split_n_threshold)
+    out = (ctypes.c_int64 * 8)()
+    _lib.check(_lib.load().attnres_plan_info(ctypes.byref(p), out), "attnres_plan_info")
+    keys = ["grid", "consumer_warps", "vectors_per_thread", "ring_slots", "fwd_group",
+            "bwd_resident", "bwd_smem_bytes", "bwd_split"]
+    return dict(zip(keys, list(out)))
+
+
+def attnres_bwd_workspace_bytes(params: _lib.AttnresParams) -> int:
+    return int(_lib.load().attnres_bwd_workspace_bytes(ctypes.byref(params)))
+
+
+def attnres_check_device_error() -> None:
+    _lib.check(_lib.load().attnres_check_device_error(), "attnres_check_device_error")
+
+
+def attnres_fwd(values: Sources, q: torch.Tensor, *, w_o: Optional[torch.Tensor] = None,
+                eps: float = EPS_DEFAULT, scale: float = 1.0, key_offset: Optional[int] = None,
+                stream=None, out: Optional[dict] = None) -> dict:
+    """Forward read.  Returns y [..., D] bf16 and the saved statistics
+    alpha/rstd/logit [N, S] f32, o_rstd [N] f32 and o_pre [N, D] bf16 (the
+    last two only with w_o).  ``out`` may supply preallocated tensors."""
+    view = _source_view(values)
+    R = q.numel()
+    q = _check_vec(q, R, "q")
+    w_o = _check_vec(w_o, view.D, "w_o")
+    p = make_params(view, R, key_offset=key_offset, eps=eps, scale=scale, out_norm=w_o is not None)
+    dev = view.rows[0].device
+    S, N, D = len(view.rows), view.N, view.D
+    o = dict(out or {})
+    y = o.get("y")
+    if y is None:
+        y = torch.empty((N, D), dtype=torch.bfloat16, device=dev)
+    f32 = dict(dtype=torch.float32, device=dev)
+    alpha = o.get("alpha") if o.get("alpha") is not None else torch.empty((N, S), **f32)
+    rstd = o.get("rstd") if o.get("rstd") is not None else torch.empty((N, S), **f32)
+    logit = o.get("logit") if o.get("logit") is not None else torch.empty((N, S), **f32)
+    o_rstd = o_pre = None
+    if w_o is not None:
+        o_rstd = o.get("o_rstd") if o.get("o_rstd") is not None else torch.empty((N,), **f32)
+        o_pre = o.get("o_pre") if o.get("o_pre") is not None else torch.empty((N, D), dtype=torch.bfloat16, device=dev)
+    rc = _lib.load().attnres_fwd(ctypes.byref(p), _ptr(q), _ptr(w_o), _ptr(y), _ptr(alpha),
+                                 _ptr(rstd), _ptr(logit), _ptr(o_rstd), _ptr(o_pre), _stream(stream))
+    _lib.check(rc, "attnres_fwd")
+    return {"y": y.view(*view.lead_shape, D) if view.lead_shape else y.view(D),
+            "alpha": alpha, "rstd": rstd, "logit": logit, "o_rstd": o_rstd, "o_pre": o_pre,
+            "params": p, "view": view}
+
+
+def attnres_bwd(values: Sources, q: torch.Tensor, dy: torch.Tensor, saved: dict, *,
+                w_o: Optional[torch.Tensor] = None, eps: float = EPS_DEFAULT, scale: float = 1.0,
+                key_offset: Optional[int] = None, split_n_threshold: int = 0, stream=None,
+                dvalues: Optional[Sources] = None, workspace: Optional[torch.Tensor] = None) -> dict:
+    """Backward.  ``saved`` is attnres_fwd's result for the same sources.
+    Returns dvalues (packed [S, ..., D] if the sources were packed, else a
+    list), dq/dw_o in bf16 and fp32."""
+    view = saved.get("view") or _source_view(values)
+    R = q.numel()
+    q = _check_vec(q, R, "q")
+    w_o = _check_vec(w_o, view.D, "w_o")
+    p = make_params(view, R, key_offset=key_offset, eps=eps, scale=scale, out_norm=w_o is not None,
+                    split_n_threshold=split_n_threshold)
+    S, N, D = len(view.rows), view.N, view.D
+    dev = view.rows[0].device
+    if dy.dtype != torch.bfloat16 or not dy.is_cuda or dy.numel() != N * D:
+        raise TypeError("dy must be a CUDA bf16 tensor shaped like the output")
+    dy2 = dy.reshape(N, D).contiguous()
+    if dvalues is None:
+        if view.packed:
+            dpacked = torch.empty((S, N, D), dtype=torch.bfloat16, device=dev)
+            drows = [dpacked[s] for s in range(S)]
+        else:
+            dpacked = None
+            drows = [torch.empty((N, D), dtype=torch.bfloat16, device=dev) for _ in range(S)]
+    else:
+        if isinstance(dvalues, torch.Tensor):
+            dpacked = dvalues
+            drows = [dvalues[s].reshape(N, D) for s in range(S)]
+        else:
+            dpacked = None
+            drows = [d.reshape(N, D) for d in dvalues]
+    dld = int(drows[0].stride(0)) if N > 1 else D
+    dptrs = (ctypes.c_void_p * S)(*[r.data_ptr() for r in drows])
+    dq = torch.empty((R,), dtype=torch.bfloat16, device=dev)
+    dq32 = torch.empty((R,), dtype=torch.float32, device=dev)
+    dw = dw32 = None
+    if w_o is not None:
+        dw = torch.empty((D,), dtype=torch.bfloat16, device=dev)
+        dw32 = torch.empty((D,), dtype=torch.float32, device=dev)
+    need = attnres_bwd_workspace_bytes(p)
+    if workspace is None or workspace.numel() < need:
+        workspace = torch.empty((max(need, 16),), dtype=torch.uint8, device=dev)
+    rc = _lib.load().attnres_bwd(
+        ctypes.byref(p), _ptr(q), _ptr(w_o), _ptr(dy2), _ptr(saved["alpha"]), _ptr(saved["rstd"]),
+        _ptr(saved["logit"]), _ptr(saved.get("o_rstd")), _ptr(saved.get("o_pre")), dptrs,
+        ctypes.c_int64(dld), _ptr(dq), _ptr(dq32), _ptr(dw), _ptr(dw32), _ptr(workspace),
+        ctypes.c_size_t(workspace.numel()), _stream(stream))
+    _lib.check(rc, "attnres_bwd")
+    shape = (*view.lead_shape, D)
+    if dpacked is not None:
+        dv = dpacked.view(S, *shape)
+    else:
+        dv = [r.view(*shape) for r in drows]
+    return {"dvalues": dv, "dq": dq, "dq_f32": dq32, "dw_o": dw, "dw_o_f32": dw32}
+
+
+# --------------------------------------------------------------------------
+# Autograd operator
+# --------------------------------------------------------------------------
+class _AttnResFn(torch.autograd.Function):
+    @staticmethod
+    def forward(ctx, q, w_o, cfg, *sources):
+        eps, scale, key_offset, packed = cfg
+        vals = sources[0] if packed else list(sources)
+        r = attnres_fwd(vals, q, w_o=w_o, eps=eps, scale=scale, key_offset=key_offset)
+        ctx.cfg = cfg
+        ctx.view = r["view"]
+        ctx.params = r["params"]
+        ctx.save_for_backward(q, w_o, r["alpha"], r["rstd"], r["logit"],
+                              r["o_rstd"], r["o_pre"], *sources)
+        return r["y"]
+
+    @staticmethod
+    def backward(ctx, dy):
+        q, w_o, alpha, rstd, logit, o_rstd, o_pre, *sources = ctx.saved_tensors
+        eps, scale, key_offset, packed = ctx.cfg
+        vals = sources[0] if packed else list(sources)
+        saved = {"alpha": alpha, "rstd": rstd, "logit": logit, "o_rstd": o_rstd, "o_pre": o_pre,
+                 "view": ctx.view}
+        g = attnres_bwd(vals, q, dy.to(torch.bfloat16), saved, w_o=w_o, eps=eps, scale=scale,
+                        key_offset=key_offset)
+        dq = g["dq"].view_as(q)
+        dw = g["dw_o"].view_as(w_o) if w_o is not None else None
+        if packed:
+            return (dq, dw, None, g["dvalues"])
+        return (dq, dw, None, *g["dvalues"])
+
+
+def attnres(values: Sources, query: torch.Tensor, *, eps: float = EPS_DEFAULT, scale: float = 1.0,
+            out_norm_weight: Optional[torch.Tensor] = None,
+            key_offset: Optional[int] = None) -> torch.Tensor:
+    """AttnRes read: mix S ordered full-width sources with a softmax over
+    scale * <query, RMSNorm(key slice)> and return one [..., D] bf16 residual.
+
+    values: packed [S, ..., D] bf16 or an ordered list/tuple of [..., D]
+    tensors (a shared source may appear more than once; its gradients add).
+    query: [R], 1 <= R <= D.  key_offset: first key channel (default D - R,
+    the final R coordinates).  out_norm_weight: optional [D] weight of an
+    output RMSNorm."""
+    packed = isinstance(values, torch.Tensor)
+    cfg = (float(eps), float(scale), key_offset, packed)
+    if packed:
+        return _AttnResFn.apply(query, out_norm_weight, cfg, values)
+    return _AttnResFn.apply(query, out_norm_weight, cfg, *values)

@@ -1,0 +1,174 @@
+/*
+ * attnres.h -- C ABI of the GB300 (sm_103a) Attention Residuals read operator.
+ *
+ * The operator ("Fast Attention Residuals", sections "Quickstart" and
+ * "Equation"): for every token n and S ordered full-width residual sources
+ * v_s[n, 0:D] (bf16),
+ *
+ *   t_s   = v_s[n, key_offset : key_offset + R]      implicit key slice
+ *   r_s   = 1 / sqrt(mean(t_s^2) + eps)              key reciprocal RMS ("rstd")
+ *   z_s   = scale * r_s * <t_s, q>                   routing logit
+ *   a_s   = softmax_s(z)                             routing weight ("alpha")
+ *   o     = sum_s a_s * v_s[n, 0:D]
+ *   y     = o                                        (out_norm == 0)
+ *   y     = o * o_rstd * w_o, o_rstd = 1/sqrt(mean(o^2) + eps)   (out_norm == 1)
+ *
+ * The optional output RMSNorm and the statistics saved for backward reuse
+ * (o_rstd next to the pre-norm output o_pre) follow "[Perf] Parallelize
+ * AttnRes long-sequence reduction", Summary.  The page's canonical key slice
+ * is the final R channels (key_offset = D - R); any 0 <= key_offset <= D - R
+ * is accepted.  Standard AttnRes is R == D; sliced low-rank routing is R < D
+ * ("Fast Attention Residuals", section "Sliced LR-AttnRes").
+ *
+ * The backward returns dvalues, dq and dw_o; dq and dw_o are sums over all N
+ * tokens.  For N >= split_n_threshold (default 16384, the page's threshold)
+ * the per-CTA FP32 partial sums are combined by a separate finalize kernel;
+ * shorter inputs finish the reduction inside the backward kernel (the last
+ * CTA of each group, then the last group, add the partials).  Both orders are
+ * fixed, so dq and dw_o are bitwise reproducible run to run.
+ *
+ * Conventions for every entry point:
+ *  - All tensor pointers are DEVICE pointers of the current CUDA device,
+ *    except the attnres_params struct and the dsrc pointer array, which live
+ *    in host memory and are read during the call only.
+ *  - The caller owns every buffer, including the backward workspace.  The
+ *    library allocates no device memory.
+ *  - Calls are asynchronous on `stream` (a cudaStream_t, NULL = legacy
+ *    default stream) and never synchronise the host.
+ *  - Arguments are validated before anything is enqueued; on any error
+ *    nothing is launched and the status says why.
+ *  - bf16 is IEEE bfloat16 stored as uint16_t bit patterns.
+ *  - Rows: every source row, dy row, y row and dvalues row starts on a
+ *    16-byte boundary and D is a multiple of 8.
+ */
+#ifndef ATTNRES_H_
+#define ATTNRES_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define ATTNRES_MAX_S 128      /* most sources one call accepts           */
+#define ATTNRES_MAX_D 8192     /* widest row one call accepts             */
+#define ATTNRES_DEFAULT_SPLIT_N 16384
+
+typedef enum {
+    ATTNRES_OK = 0,
+    ATTNRES_ERR_INVALID_ARG = 1,  /* a size, flag or pointer is out of range      */
+    ATTNRES_ERR_ALIGNMENT = 2,    /* a pointer or row stride breaks 16-byte rows  */
+    ATTNRES_ERR_UNSUPPORTED = 3,  /* legal shape this build does not handle       */
+    ATTNRES_ERR_WORKSPACE = 4,    /* workspace NULL or smaller than required      */
+    ATTNRES_ERR_CUDA = 5,         /* a CUDA runtime call or launch failed         */
+    ATTNRES_ERR_DEVICE = 6        /* a kernel reported a failed wait (see below)  */
+} attnres_status;
+
+/*
+ * Shape and source description shared by forward and backward.
+ *   S            number of sources, 1 <= S <= ATTNRES_MAX_S
+ *   D            row width, 8 <= D <= ATTNRES_MAX_D, D % 8 == 0
+ *   R            key rank, 1 <= R <= D
+ *   key_offset   first key channel, 0 <= key_offset <= D - R
+ *   N            tokens (B*T*H flattened), N >= 0; N == 0 is a no-op
+ *   eps          added to the mean square inside the root (default 2^-23)
+ *   scale        logit multiplier applied after key normalisation (default 1)
+ *   out_norm     0 or 1: apply the output RMSNorm with weight w_o
+ *   split_n_threshold  N at or above which the backward uses the finalize
+ *                kernel; <= 0 selects ATTNRES_DEFAULT_SPLIT_N
+ *   src_ld       element stride between consecutive token rows of each
+ *                source, src_ld >= D, src_ld % 8 == 0
+ *   src[s]       device pointer to source s, row n at src[s] + n * src_ld
+ *                (bf16, 16-byte aligned).  The same pointer may appear more
+ *                than once (a shared source read twice).
+ */
+typedef struct {
+    int32_t S;
+    int32_t D;
+    int32_t R;
+    int32_t key_offset;
+    int64_t N;
+    float eps;
+    float scale;
+    int32_t out_norm;
+    int32_t split_n_threshold;
+    int64_t src_ld;
+    const void* src[ATTNRES_MAX_S];
+} attnres_params;
+
+/*
+ * Forward.  Outputs (device, caller-allocated, fully overwritten):
+ *   y       bf16 [N, D] contiguous
+ *   alpha   f32  [N, S]  routing weights a_s
+ *   rstd    f32  [N, S]  key reciprocal RMS r_s
+ *   logit   f32  [N, S]  routing logits z_s
+ *   o_rstd  f32  [N]     output reciprocal RMS; required iff out_norm, else ignored
+ *   o_pre   bf16 [N, D]  pre-norm mixture o; required iff out_norm, else ignored
+ *   q       bf16 [R]     query;  w_o bf16 [D], required iff out_norm
+ * alpha, rstd, logit, o_rstd and o_pre are what attnres_bwd consumes.
+ * Errors: INVALID_ARG (sizes, NULL pointers), ALIGNMENT (16-byte rows),
+ * UNSUPPORTED (no kernel configuration fits), CUDA (launch failure).
+ */
+attnres_status attnres_fwd(const attnres_params* p, const void* q, const void* w_o,
+                           void* y, float* alpha, float* rstd, float* logit,
+                           float* o_rstd, void* o_pre, void* stream);
+
+/*
+ * Bytes of device workspace attnres_bwd needs for these params on the
+ * current device (0 when N == 0).  Depends on S, D, R, N, out_norm,
+ * split_n_threshold and the device's SM count only.
+ */
+size_t attnres_bwd_workspace_bytes(const attnres_params* p);
+
+/*
+ * Backward.  Inputs: q, w_o (iff out_norm), dy bf16 [N, D] contiguous, and
+ * the forward's alpha, rstd, logit, o_rstd and o_pre for the same sources.
+ * Outputs (written, never accumulated):
+ *   dsrc       host array of S device pointers; dsrc[s] receives the
+ *              gradient of source s, bf16 rows at dsrc[s] + n * dsrc_ld
+ *              (dsrc_ld >= D, % 8 == 0, 16-byte aligned rows).  Entries must
+ *              be distinct and must not overlap any source or each other.
+ *              Shared (repeated) sources get one gradient per occurrence; the
+ *              caller adds them.
+ *   dq         bf16 [R];   dq_f32   f32 [R] (may be NULL)
+ *   dw_o       bf16 [D];   dw_o_f32 f32 [D] (may be NULL); required iff out_norm
+ *   workspace  device scratch of at least attnres_bwd_workspace_bytes(p)
+ *              bytes, 16-byte aligned; contents on entry are ignored.
+ * Errors: as attnres_fwd, plus WORKSPACE.
+ */
+attnres_status attnres_bwd(const attnres_params* p, const void* q, const void* w_o,
+                           const void* dy, const float* alpha, const float* rstd,
+                           const float* logit, const float* o_rstd, const void* o_pre,
+                           void* const* dsrc, int64_t dsrc_ld, void* dq, float* dq_f32,
+                           void* dw_o, float* dw_o_f32, void* workspace,
+                           size_t workspace_bytes, void* stream);
+
+/*
+ * Kernels bound every wait on a shared-memory barrier.  A wait that runs out
+ * of time makes the kernel record a nonzero code here and finish without
+ * further waiting (its outputs are then garbage).  This call synchronises
+ * the device, returns ATTNRES_ERR_DEVICE and clears the record if one was
+ * set, ATTNRES_OK otherwise.
+ */
+attnres_status attnres_check_device_error(void);
+
+/* Static description of a status code; never NULL. */
+const char* attnres_status_string(attnres_status s);
+
+/*
+ * Launch plan the library would use for these params on the current device
+ * (for tests and benchmarks; no launch happens).  Fills out[0..7] with:
+ * grid CTAs, consumer warps, vectors per thread, ring slots, forward group
+ * size, backward resident flag (1 = source rows stay in shared memory
+ * between the two backward passes), dynamic shared memory bytes of the
+ * backward kernel, and the backward reduction path (0 = in-kernel,
+ * 1 = finalize kernel).
+ */
+attnres_status attnres_plan_info(const attnres_params* p, int64_t out[8]);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* ATTNRES_H_ */
