@@ -101,7 +101,7 @@ attnres_status make_plan(const attnres_params* p, Plan* plan) {
     if (gpb < 2) gpb = 2;
     if (gpb > 16) gpb = 16;
     pl.gp_bwd = gpb;
-    pl.resident = (p->S + 1 + p->out_norm) <= slots ? 1 : 0;
+    pl.resident = (p->S + 1) <= slots ? 1 : 0;
     const int thr = p->split_n_threshold > 0 ? p->split_n_threshold : ATTNRES_DEFAULT_SPLIT_N;
     pl.split = p->N >= thr ? 1 : 0;
     long long grid = dev.sm_count;
@@ -164,16 +164,18 @@ attnres_status attnres_plan_info(const attnres_params* p, int64_t out[8]) {
 }
 
 attnres_status attnres_fwd(const attnres_params* p, const void* q, const void* w_o, void* y,
-                           float* alpha, float* rstd, float* logit, float* o_rstd, void* o_pre,
+                           float* alpha, float* rstd, float* logit, float* o_rstd, float* o_pre,
                            void* stream) {
     attnres_status st = check_shape(p);
     if (st != ATTNRES_OK) return st;
     if (p->N == 0) return ATTNRES_OK;
     if (!q || !y || !alpha || !rstd || !logit) return ATTNRES_ERR_INVALID_ARG;
-    if (p->out_norm && (!w_o || !o_rstd || !o_pre)) return ATTNRES_ERR_INVALID_ARG;
+    if (p->out_norm && (!w_o || !o_rstd)) return ATTNRES_ERR_INVALID_ARG;
+    if (!p->out_norm && o_pre) return ATTNRES_ERR_INVALID_ARG;
     if (!aligned16(y) || !aligned4(alpha) || !aligned4(rstd) || !aligned4(logit))
         return ATTNRES_ERR_ALIGNMENT;
-    if (p->out_norm && (!aligned16(o_pre) || !aligned4(o_rstd))) return ATTNRES_ERR_ALIGNMENT;
+    if (p->out_norm && !aligned4(o_rstd)) return ATTNRES_ERR_ALIGNMENT;
+    if (o_pre && !aligned16(o_pre)) return ATTNRES_ERR_ALIGNMENT;
     if ((reinterpret_cast<uintptr_t>(q) & 1u) || (w_o && (reinterpret_cast<uintptr_t>(w_o) & 1u)))
         return ATTNRES_ERR_ALIGNMENT;
     Plan pl;
@@ -202,7 +204,7 @@ attnres_status attnres_fwd(const attnres_params* p, const void* q, const void* w
     a.rstd = rstd;
     a.logit = logit;
     a.o_rstd = o_rstd;
-    a.o_pre = static_cast<uint16_t*>(o_pre);
+    a.o_pre = p->out_norm ? o_pre : nullptr;
     return launch_fwd(pl, a, static_cast<cudaStream_t>(stream)) == cudaSuccess ? ATTNRES_OK
                                                                               : ATTNRES_ERR_CUDA;
 }
@@ -216,7 +218,7 @@ size_t attnres_bwd_workspace_bytes(const attnres_params* p) {
 
 attnres_status attnres_bwd(const attnres_params* p, const void* q, const void* w_o, const void* dy,
                            const float* alpha, const float* rstd, const float* logit,
-                           const float* o_rstd, const void* o_pre, void* const* dsrc,
+                           const float* o_rstd, const float* o_pre, void* const* dsrc,
                            int64_t dsrc_ld, void* dq, float* dq_f32, void* dw_o, float* dw_o_f32,
                            void* workspace, size_t workspace_bytes, void* stream) {
     attnres_status st = check_shape(p);
@@ -233,12 +235,14 @@ attnres_status attnres_bwd(const attnres_params* p, const void* q, const void* w
         return ATTNRES_OK;
     }
     if (!q || !dy || !alpha || !rstd || !logit || !dsrc || !dq) return ATTNRES_ERR_INVALID_ARG;
-    if (p->out_norm && (!w_o || !o_rstd || !o_pre || !dw_o)) return ATTNRES_ERR_INVALID_ARG;
+    if (p->out_norm && (!w_o || !o_rstd || !dw_o)) return ATTNRES_ERR_INVALID_ARG;
+    if (!p->out_norm && o_pre) return ATTNRES_ERR_INVALID_ARG;
     if (dsrc_ld < p->D) return ATTNRES_ERR_INVALID_ARG;
     if (dsrc_ld % 8 != 0) return ATTNRES_ERR_ALIGNMENT;
     if (!aligned16(dy) || !aligned4(alpha) || !aligned4(rstd) || !aligned4(logit))
         return ATTNRES_ERR_ALIGNMENT;
-    if (p->out_norm && (!aligned16(o_pre) || !aligned4(o_rstd))) return ATTNRES_ERR_ALIGNMENT;
+    if (p->out_norm && !aligned4(o_rstd)) return ATTNRES_ERR_ALIGNMENT;
+    if (o_pre && !aligned16(o_pre)) return ATTNRES_ERR_ALIGNMENT;
     if ((reinterpret_cast<uintptr_t>(q) & 1u) || (reinterpret_cast<uintptr_t>(dq) & 1u) ||
         (dq_f32 && !aligned4(dq_f32)) || (dw_o && (reinterpret_cast<uintptr_t>(dw_o) & 1u)) ||
         (dw_o_f32 && !aligned4(dw_o_f32)) || (w_o && (reinterpret_cast<uintptr_t>(w_o) & 1u)))
@@ -294,7 +298,7 @@ attnres_status attnres_bwd(const attnres_params* p, const void* q, const void* w
     a.rstd = rstd;
     a.logit = logit;
     a.o_rstd = o_rstd;
-    a.o_pre = static_cast<const uint16_t*>(o_pre);
+    a.o_pre = o_pre;
     unsigned char* ws = static_cast<unsigned char*>(workspace);
     a.tickets = reinterpret_cast<unsigned*>(ws);
     a.part = reinterpret_cast<float*>(ws + pl.ws_part_off);

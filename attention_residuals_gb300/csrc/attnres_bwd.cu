@@ -1,10 +1,11 @@
 // attnres_bwd.cu -- backward kernel and dq/dw_o finalize of the Attention
 // Residuals read operator.
 //
-// Per token, with the forward's saved alpha, rstd, logit (and o_rstd, o_pre
-// when the output RMSNorm is on; "[Perf] Parallelize AttnRes long-sequence
+// Per token, with the forward's saved alpha, rstd, logit (and o_rstd when the
+// output RMSNorm is on; "[Perf] Parallelize AttnRes long-sequence
 // reduction", Summary):
-//   out-norm:  yhat = o_pre * o_rstd, dw_o += dy * yhat, g = dy * w_o,
+//   out-norm:  o = sum_s alpha_s v_s (rebuilt in FP32, or the caller's FP32
+//              copy), yhat = o * o_rstd, dw_o += dy * yhat, g = dy * w_o,
 //              do = o_rstd * (g - yhat * <g, yhat> / D);   else do = dy
 //   da_s  = <do, v_s>,   delta = sum_s alpha_s da_s,  dz_s = alpha_s (da_s - delta)
 //   dv_s  = alpha_s do  +  on key channels: c1_s q + c2_s t_s
@@ -15,11 +16,11 @@
 // GB300 mapping.  As in the forward, one persistent CTA per SM, a producer
 // thread filling a shared-memory row ring with 1-D TMA copies, and consumer
 // threads that own fixed 16-byte column vectors.  Per token the ring
-// receives dy, o_pre (out-norm) and the S source rows.  When the S rows fit
-// next to the next token's rows ("resident"), each source row is read from
-// HBM once: the dot pass and the write pass both read it from shared memory.
-// Otherwise the producer streams the key slices a second time (served from
-// L2 when it still holds them).  The saved per-token statistics arrive
+// receives dy and the S source rows.  When the S rows fit in the ring
+// ("resident"), each source row is read from HBM once: the o rebuild (with
+// the output norm), the dot pass and the write pass all read it from shared
+// memory.  Otherwise the producer streams the rows once per pass (served
+// from L2 when it still holds them), and the write pass gets key slices only.  The saved per-token statistics arrive
 // through small cp.async copies into a separate 4-deep ring.
 //
 // dq and dw_o: every consumer thread owns the same columns for every token,
@@ -131,22 +132,26 @@ __global__ void __launch_bounds__(kMaxThreads, 1) attnres_bwd_kernel(const __gri
                 tphase ^= 1u;
             }
             if (lane == 0) {
-                const int nrows = 1 + a.out_norm + S + (a.resident ? 0 : S);
+                // Row schedule of one token: dy; then, when o must be rebuilt
+                // from streamed rows, S rows for that pass; S rows for the dot
+                // pass (in resident mode these also serve the other passes);
+                // when streaming, S key slices for the write pass.
+                const int pass_a = (a.out_norm && !a.o_pre && !a.resident) ? S : 0;
+                const int pass_c = a.resident ? 0 : S;
+                const int nrows = 1 + pass_a + S + pass_c;
                 for (int r = 0; r < nrows; ++r) {
                     const unsigned char* src;
                     uint32_t off = 0, bytes = row_bytes;
                     if (r == 0) {
                         src = reinterpret_cast<const unsigned char*>(a.dy + n * D);
-                    } else if (a.out_norm && r == 1) {
-                        src = reinterpret_cast<const unsigned char*>(a.o_pre + n * D);
                     } else {
-                        int s = r - 1 - a.out_norm;
-                        const bool second = s >= S;
-                        if (second) {
-                            s -= S;
+                        int s = r - 1;
+                        if (s >= pass_a) s -= pass_a;  // rows of the o pass come first
+                        if (r - 1 >= pass_a + S) {      // write-pass key slices
                             off = key_off_b;
                             bytes = key_bytes;
                         }
+                        if (s >= S) s -= S;
                         src = static_cast<const unsigned char*>(a.src[s]) + (n * a.src_ld) * 2 + off;
                     }
                     if (!mbar_wait(empty + slot, phase ^ 1u, abort_flag, &g_bwd_error, kSiteBwdProducer)) break;
@@ -216,28 +221,77 @@ __global__ void __launch_bounds__(kMaxThreads, 1) attnres_bwd_kernel(const __gri
         advance(slot, phase, slots);
         const unsigned char* dy_row = ring + static_cast<size_t>(dy_slot) * a.slot_bytes;
         if (a.out_norm) {
-            const int op_slot = slot;
-            mbar_wait(full + slot, phase, abort_flag, &g_bwd_error, kSiteBwdConsumer);
-            advance(slot, phase, slots);
-            const unsigned char* op_row = ring + static_cast<size_t>(op_slot) * a.slot_bytes;
+            // o = sum_s alpha_s v_s in FP32: from the caller's saved copy, or
+            // rebuilt from the source rows (resident: the rows the dot pass
+            // uses next; streaming: a dedicated pass of rows).
+            float o[VPT][8];
+            if (a.o_pre) {
+                const float* prow = a.o_pre + n * static_cast<long long>(D);
+#pragma unroll
+                for (int i = 0; i < VPT; ++i) {
+                    if (vi[i].col >= 0) {
+                        const uint4 lo = ld_global_nc_v4(prow + 8 * vi[i].col);
+                        const uint4 hi = ld_global_nc_v4(prow + 8 * vi[i].col + 4);
+                        o[i][0] = __uint_as_float(lo.x); o[i][1] = __uint_as_float(lo.y);
+                        o[i][2] = __uint_as_float(lo.z); o[i][3] = __uint_as_float(lo.w);
+                        o[i][4] = __uint_as_float(hi.x); o[i][5] = __uint_as_float(hi.y);
+                        o[i][6] = __uint_as_float(hi.z); o[i][7] = __uint_as_float(hi.w);
+                    }
+                }
+            } else {
+#pragma unroll
+                for (int i = 0; i < VPT; ++i)
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) o[i][e] = 0.0f;
+                int aslot = slot;
+                uint32_t aphase = phase;
+                for (int s = 0; s < S; ++s) {
+                    mbar_wait(full + aslot, aphase, abort_flag, &g_bwd_error, kSiteBwdConsumer);
+                    const unsigned char* row = ring + static_cast<size_t>(aslot) * a.slot_bytes;
+                    const float al = tk[s];
+#pragma unroll
+                    for (int i = 0; i < VPT; ++i) {
+                        if (vi[i].col >= 0) {
+                            float x[8];
+                            unpack8(ld_shared_v4(row + vi[i].col * 16), x);
+#pragma unroll
+                            for (int e = 0; e < 8; ++e) o[i][e] = fmaf(al, x[e], o[i][e]);
+                        }
+                    }
+                    if (!a.resident) {
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(empty + aslot);
+                    }
+                    advance(aslot, aphase, slots);
+                }
+                if (!a.resident) {  // the streamed o-pass rows are consumed
+                    slot = aslot;
+                    phase = aphase;
+                }
+            }
             const float rho = tk[3 * s_pad];
             float gy = 0.0f;
 #pragma unroll
             for (int i = 0; i < VPT; ++i) {
                 if (vi[i].col >= 0) {
-                    float g[8], yh[8];
+                    float g[8];
                     unpack8(ld_shared_v4(dy_row + vi[i].col * 16), g);
-                    unpack8(ld_shared_v4(op_row + vi[i].col * 16), yh);
 #pragma unroll
                     for (int e = 0; e < 8; ++e) {
-                        yh[e] *= rho;
-                        dw_acc[i][e] = fmaf(g[e], yh[e], dw_acc[i][e]);
+                        const float yh = o[i][e] * rho;
+                        o[i][e] = yh;
+                        dw_acc[i][e] = fmaf(g[e], yh, dw_acc[i][e]);
                         g[e] *= wf[i][e];
-                        gy = fmaf(g[e], yh[e], gy);
+                        gy = fmaf(g[e], yh, gy);
                         dout[i][e] = g[e];
                     }
+                } else {
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) dout[i][e] = 0.0f;
                 }
             }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(empty + dy_slot);
             gy = warp_sum(gy);
             if (lane == 0) red[(rbuf * ncw + warp) * kReduceStride] = gy;
             named_bar_sync(1, nct);
@@ -246,20 +300,9 @@ __global__ void __launch_bounds__(kMaxThreads, 1) attnres_bwd_kernel(const __gri
             rbuf ^= 1;
             const float cg = tot * inv_d;
 #pragma unroll
-            for (int i = 0; i < VPT; ++i) {
-                if (vi[i].col >= 0) {
-                    float yh[8];
-                    unpack8(ld_shared_v4(op_row + vi[i].col * 16), yh);
+            for (int i = 0; i < VPT; ++i)
 #pragma unroll
-                    for (int e = 0; e < 8; ++e)
-                        dout[i][e] = rho * fmaf(-(yh[e] * rho), cg, dout[i][e]);
-                }
-            }
-            __syncwarp();
-            if (lane == 0) {
-                mbar_arrive(empty + dy_slot);
-                mbar_arrive(empty + op_slot);
-            }
+                for (int e = 0; e < 8; ++e) dout[i][e] = rho * fmaf(-o[i][e], cg, dout[i][e]);
         } else {
 #pragma unroll
             for (int i = 0; i < VPT; ++i) {

@@ -18,6 +18,7 @@
 // softmax maximum and denominator, and a second pass over the same
 // resident rows adds the weighted rows into FP32 registers before the slots
 // are released.  The output norm needs one more CTA reduction per token.
+// The pre-norm mixture o is written (FP32) only when the caller asks for it.
 // This is a bandwidth-bound per-token reduction: no tensor cores.
 #include <cfloat>
 
@@ -270,7 +271,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1) attnres_fwd_kernel(const __gri
             if (threadIdx.x == 0) a.o_rstd[n] = rho;
         }
         uint16_t* yrow = a.y + n * static_cast<long long>(a.D);
-        uint16_t* prow = a.out_norm ? a.o_pre + n * static_cast<long long>(a.D) : nullptr;
+        float* prow = a.o_pre ? a.o_pre + n * static_cast<long long>(a.D) : nullptr;
 #pragma unroll
         for (int i = 0; i < VPT; ++i) {
             if (vi[i].col >= 0) {
@@ -278,7 +279,14 @@ __global__ void __launch_bounds__(kMaxThreads, 1) attnres_fwd_kernel(const __gri
 #pragma unroll
                 for (int e = 0; e < 8; ++e) yv[e] = acc[i][e] * rho * wf[i][e];
                 st_global_cs_v4(yrow + 8 * vi[i].col, pack8(yv));
-                if (a.out_norm) st_global_cs_v4(prow + 8 * vi[i].col, pack8(acc[i]));
+                if (prow) {
+                    const uint4 lo = make_uint4(__float_as_uint(acc[i][0]), __float_as_uint(acc[i][1]),
+                                                __float_as_uint(acc[i][2]), __float_as_uint(acc[i][3]));
+                    const uint4 hi = make_uint4(__float_as_uint(acc[i][4]), __float_as_uint(acc[i][5]),
+                                                __float_as_uint(acc[i][6]), __float_as_uint(acc[i][7]));
+                    st_global_cs_v4(prow + 8 * vi[i].col, lo);
+                    st_global_cs_v4(prow + 8 * vi[i].col + 4, hi);
+                }
             }
         }
         if (warp == 0) {

@@ -99,7 +99,7 @@ struct FwdArgs {
     float* rstd;
     float* logit;
     float* o_rstd;
-    uint16_t* o_pre;
+    float* o_pre;       // optional FP32 [N, D] pre-norm mixture
 };
 
 struct BwdArgs {
@@ -117,7 +117,7 @@ struct BwdArgs {
     const float* rstd;
     const float* logit;
     const float* o_rstd;
-    const uint16_t* o_pre;
+    const float* o_pre;  // optional FP32 [N, D]; NULL = recompute o from the sources
     float* part;        // [grid][R + Dw] per-CTA partial sums (Dw = out_norm ? D : 0)
     float* gpart;       // [ngroups][R + Dw] group sums (in-kernel reduction)
     unsigned* tickets;  // [ngroups + 1] zeroed before launch (in-kernel reduction)

@@ -123,16 +123,22 @@ def _check_vec(t: Optional[torch.Tensor], n: int, name: str):
 # --------------------------------------------------------------------------
 # C-ABI mirrors
 # --------------------------------------------------------------------------
+_PLAN_KEYS = ["grid", "consumer_warps", "vectors_per_thread", "ring_slots", "fwd_group",
+              "bwd_resident", "bwd_smem_bytes", "bwd_split"]
+
+
+def _plan(p: _lib.AttnresParams) -> dict:
+    out = (ctypes.c_int64 * 8)()
+    _lib.check(_lib.load().attnres_plan_info(ctypes.byref(p), out), "attnres_plan_info")
+    return dict(zip(_PLAN_KEYS, list(out)))
+
+
 def attnres_plan_info(values: Sources, R: int, *, key_offset=None, out_norm=False,
                       split_n_threshold=0) -> dict:
     view = _source_view(values)
     p = make_params(view, R, key_offset=key_offset, eps=EPS_DEFAULT, scale=1.0, out_norm=out_norm,
                     split_n_threshold=split_n_threshold)
-    out = (ctypes.c_int64 * 8)()
-    _lib.check(_lib.load().attnres_plan_info(ctypes.byref(p), out), "attnres_plan_info")
-    keys = ["grid", "consumer_warps", "vectors_per_thread", "ring_slots", "fwd_group",
-            "bwd_resident", "bwd_smem_bytes", "bwd_split"]
-    return dict(zip(keys, list(out)))
+    return _plan(p)
 
 
 def attnres_bwd_workspace_bytes(params: _lib.AttnresParams) -> int:
@@ -145,10 +151,13 @@ def attnres_check_device_error() -> None:
 
 def attnres_fwd(values: Sources, q: torch.Tensor, *, w_o: Optional[torch.Tensor] = None,
                 eps: float = EPS_DEFAULT, scale: float = 1.0, key_offset: Optional[int] = None,
-                stream=None, out: Optional[dict] = None) -> dict:
+                save_o_pre: Optional[bool] = None, stream=None, out: Optional[dict] = None) -> dict:
     """Forward read.  Returns y [..., D] bf16 and the saved statistics
-    alpha/rstd/logit [N, S] f32, o_rstd [N] f32 and o_pre [N, D] bf16 (the
-    last two only with w_o).  ``out`` may supply preallocated tensors."""
+    alpha/rstd/logit [N, S] f32 and, with w_o, o_rstd [N] f32 and optionally
+    the FP32 pre-norm mixture o_pre [N, D].  save_o_pre=None saves o_pre only
+    when the backward cannot keep a token's rows resident (then it spares the
+    backward a pass over the sources).  ``out`` may supply preallocated
+    tensors."""
     view = _source_view(values)
     R = q.numel()
     q = _check_vec(q, R, "q")
@@ -167,7 +176,10 @@ def attnres_fwd(values: Sources, q: torch.Tensor, *, w_o: Optional[torch.Tensor]
     o_rstd = o_pre = None
     if w_o is not None:
         o_rstd = o.get("o_rstd") if o.get("o_rstd") is not None else torch.empty((N,), **f32)
-        o_pre = o.get("o_pre") if o.get("o_pre") is not None else torch.empty((N, D), dtype=torch.bfloat16, device=dev)
+        if save_o_pre is None:
+            save_o_pre = N > 0 and not _plan(p)["bwd_resident"]
+        if save_o_pre:
+            o_pre = o.get("o_pre") if o.get("o_pre") is not None else torch.empty((N, D), **f32)
     rc = _lib.load().attnres_fwd(ctypes.byref(p), _ptr(q), _ptr(w_o), _ptr(y), _ptr(alpha),
                                  _ptr(rstd), _ptr(logit), _ptr(o_rstd), _ptr(o_pre), _stream(stream))
     _lib.check(rc, "attnres_fwd")

@@ -1,0 +1,443 @@
+#!/usr/bin/env python3
+"""Benchmark of the AttnRes read operator, forward + backward, on GB300.
+
+One step = attnres_fwd + attnres_bwd (every step of the hot path: key
+statistics, softmax routing, weighted read, output RMSNorm, dot pass,
+dvalues write, dq/dw_o partial sums and their finalize) over one batch of
+the long-sequence workload S=10 sources, N=32768 tokens, D=4096, bf16,
+output RMSNorm on (the shape of the first row of the benchmark table in
+"[Perf] Parallelize AttnRes long-sequence reduction", Test plan).
+
+The metric is effective HBM bandwidth: the algorithmic bytes one step must
+move (sources read in the forward and again in the backward, dvalues
+written, y written, dy read, saved statistics and the FP32 partial sums)
+divided by the measured step time.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Prints ONE JSON line on rank 0.  With --gpus N > 1 run it under
+torch.distributed.run: every rank processes its own full batch (weak
+scaling, no collective inside the timed region).  --impl reference times
+the FP64 CPU oracle on the host cores instead (rank 0 only).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "AttnRes fwd+bwd ms and effective HBM GB/s (% of roofline), bf16, 1×GB300"
+WORKLOAD_CFG = 3
+FALLBACK_HBM_GBS = 6800.0
+PROFILE_TRAFFIC = os.path.join(ROOT, "profiles", "attnres_bwd_traffic.json")
+
+
+# --------------------------------------------------------------------------
+# Byte model
+# --------------------------------------------------------------------------
+def algorithmic_bytes(S, N, D, R, out_norm, P):
+    """Bytes each kernel must move (bf16 = 2 B, fp32 = 4 B): the forward reads
+    the sources and writes y plus the per-token statistics; the backward reads
+    the sources again, reads dy and the statistics, writes dvalues and moves
+    the FP32 partial sums of dq/dw_o (P rows written, then read)."""
+    v = S * N * D * 2
+    row = N * D * 2
+    stats = 3 * N * S * 4 + (N * 4 if out_norm else 0)
+    fwd = v + row + stats
+    W = R + (D if out_norm else 0)
+    bwd = 2 * v + row + stats + 2 * P * W * 4
+    return {"fwd": fwd, "bwd": bwd, "total": fwd + bwd}
+
+
+def kernel_sources_hash():
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "attention_residuals_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(name.encode())
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def read_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            peaks = json.load(f)
+        for key in ("hbm_gbs", "hbm_GBs", "hbm_copy_gbs", "hbm"):
+            if key in peaks and isinstance(peaks[key], (int, float)):
+                return float(peaks[key]), "measured"
+    except Exception:
+        pass
+    return FALLBACK_HBM_GBS, "fallback"
+
+
+def profiled_traffic(config_key):
+    """DRAM bytes per backward launch from the committed ncu summary, only if
+    the kernel sources are unchanged since that capture."""
+    try:
+        with open(PROFILE_TRAFFIC) as f:
+            doc = json.load(f)
+        if doc.get("sources_hash") == kernel_sources_hash() and doc.get("config") == config_key:
+            return doc.get("traffic_bytes_per_launch")
+    except Exception:
+        pass
+    return None
+
+
+# --------------------------------------------------------------------------
+# Clock sampling during the timed region
+# --------------------------------------------------------------------------
+class ClockSampler:
+    FIELDS = ("timestamp,clocks.sm,clocks.max.sm,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.lines = []
+        self.t0 = self.t1 = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "50"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.reader = threading.Thread(target=self._read, daemon=True)
+            self.reader.start()
+        except Exception:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append((time.time(), line.strip()))
+
+    def mark(self, which):
+        if which == "begin":
+            self.t0 = time.time()
+        else:
+            self.t1 = time.time()
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.12)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        rows = []
+        for ts, line in self.lines:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 8:
+                continue
+            rows.append((ts, parts))
+        inside = [r for r in rows if self.t0 is not None and self.t0 <= r[0] <= (self.t1 or 1e30)]
+        used = inside if inside else rows[-3:]
+        sm = [float(p[1]) for _, p in used if p[1].replace(".", "").isdigit()]
+        smax = [float(p[2]) for _, p in used if p[2].replace(".", "").isdigit()]
+        reasons = set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for _, p in used:
+            for k, name in enumerate(names):
+                if p[4 + k].lower().startswith("active"):
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples_in_window": len(inside)}
+
+
+# --------------------------------------------------------------------------
+# Distributed helpers
+# --------------------------------------------------------------------------
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+# --------------------------------------------------------------------------
+# Reference arm: the FP64 oracle on the host cores
+# --------------------------------------------------------------------------
+def oracle_sample(sample_tokens, seed=0):
+    from attention_residuals_gb300.workloads import make_workload
+    return make_workload(WORKLOAD_CFG, N=sample_tokens, seed=WORKLOAD_CFG + 1000 * seed)
+
+
+def time_oracle(wl, repeats=1):
+    from oracle import attnres_oracle
+    cores = os.cpu_count() or 1
+    times = []
+    for _ in range(repeats):
+        t = time.perf_counter()
+        attnres_oracle(wl.values, wl.q, w_o=wl.w_o, dy=wl.dy, key_offset=wl.key_offset,
+                       nthreads=cores, want_dvalues=True)
+        times.append(time.perf_counter() - t)
+    return times, cores
+
+
+def run_reference(args):
+    world, rank, _ = dist_env()
+    if rank != 0:
+        return 0
+    from oracle import build_oracle
+    build_oracle()
+    sample = args.ref_tokens
+    wl = oracle_sample(sample)
+    b = algorithmic_bytes(wl.S, sample, wl.D, wl.R, wl.out_norm, 1)["total"]
+    small = oracle_sample(16)
+    for _ in range(args.warmup):  # untimed warm-up steps on a small sample
+        time_oracle(small, repeats=1)
+    times, cores = time_oracle(wl, repeats=max(1, args.steps))
+    t = sum(times) / len(times)
+    gbs = b / t / 1e9
+    line = {
+        "metric": METRIC, "value": gbs, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": t * 1e3 * (32768 / sample),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "impl": "reference",
+        "config": {"workload": "S=10 N=32768 D=4096 R=4096 out-norm (long-sequence)",
+                   "sample_tokens": sample},
+        "cpu_baseline": {"value": gbs, "unit": "GB/s", "cores": cores, "kind": "oracle",
+                         "sample": f"{sample} of 32768 tokens per step, fwd+bwd in FP64; "
+                                   "ms_per_step scaled to the full 32768 tokens"},
+        "e2e": {"value": gbs, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# --------------------------------------------------------------------------
+# Our arm
+# --------------------------------------------------------------------------
+def run_ours(args):
+    import torch
+
+    world, rank, local = dist_env()
+    if not torch.cuda.is_available():
+        print(json.dumps({"error": "no CUDA device"}))
+        return 1
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    pg = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+        pg = dist
+
+    from attention_residuals_gb300 import _lib, attnres_bwd, attnres_fwd, attnres_plan_info
+    from attention_residuals_gb300.build import build
+    from attention_residuals_gb300.workloads import make_workload
+    build()
+    _lib.load()
+
+    # CPU baseline sample is generated before any GPU work (rank 0, N=1 only).
+    cpu_wl = oracle_sample(args.cpu_tokens) if (rank == 0 and world == 1 and not args.no_cpu) else None
+
+    wl = make_workload(WORKLOAD_CFG, N=args.tokens, seed=WORKLOAD_CFG + 1000 * rank, device=str(dev))
+    S, N, D, R = wl.S, wl.N, wl.D, wl.R
+    v, q, w, dy = wl.values, wl.q, wl.w_o, wl.dy
+    info = attnres_plan_info(v, R, key_offset=wl.key_offset, out_norm=wl.out_norm)
+    P = info["grid"]
+    nbytes = algorithmic_bytes(S, N, D, R, wl.out_norm, P)
+
+    # Preallocated outputs and workspace: the timed step allocates nothing.
+    f32 = dict(dtype=torch.float32, device=dev)
+    out = {"y": torch.empty((N, D), dtype=torch.bfloat16, device=dev),
+           "alpha": torch.empty((N, S), **f32), "rstd": torch.empty((N, S), **f32),
+           "logit": torch.empty((N, S), **f32), "o_rstd": torch.empty((N,), **f32)}
+    dv = torch.empty_like(v)
+    ws = torch.empty((64 << 20,), dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        f = attnres_fwd(v, q, w_o=w, key_offset=wl.key_offset, out=out, stream=stream)
+        b = attnres_bwd(v, q, dy, f, w_o=w, key_offset=wl.key_offset, workspace=ws, dvalues=dv,
+                        stream=stream)
+        return f, b
+
+    for _ in range(max(3, args.warmup)):
+        step()
+    torch.cuda.synchronize()
+
+    K = args.steps
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
+    e_start = torch.cuda.Event(enable_timing=True)
+    e_end = torch.cuda.Event(enable_timing=True)
+    sampler = ClockSampler(local)
+    sampler.start()
+    time.sleep(0.3)
+    if pg is not None:
+        pg.barrier()
+    torch.cuda.synchronize()
+    sampler.mark("begin")
+    e_start.record(stream)
+    for k in range(K):
+        ev[k][0].record(stream)
+        f = attnres_fwd(v, q, w_o=w, key_offset=wl.key_offset, out=out, stream=stream)
+        ev[k][1].record(stream)
+        attnres_bwd(v, q, dy, f, w_o=w, key_offset=wl.key_offset, workspace=ws, dvalues=dv,
+                    stream=stream)
+        ev[k][2].record(stream)
+    e_end.record(stream)
+    torch.cuda.synchronize()
+    sampler.mark("end")
+    if pg is not None:
+        pg.barrier()
+    clocks = sampler.stop()
+    total_ms = e_start.elapsed_time(e_end)
+    fwd_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in ev)
+    bwd_ms = statistics.mean(e[1].elapsed_time(e[2]) for e in ev)
+    ms_step = total_ms / K
+    if pg is not None:
+        t = torch.tensor([ms_step, fwd_ms, bwd_ms], device=dev)
+        pg.all_reduce(t, op=pg.ReduceOp.MAX)
+        ms_step, fwd_ms, bwd_ms = [float(x) for x in t.tolist()]
+
+    # ---------------------------------------------------------- end to end
+    e2e = None
+    if not args.no_e2e:
+        hv = torch.empty(v.shape, dtype=v.dtype, pin_memory=True)
+        hv.copy_(v)
+        hq = q.cpu().pin_memory()
+        hw = w.cpu().pin_memory()
+        hdy = torch.empty(dy.shape, dtype=dy.dtype, pin_memory=True)
+        hdy.copy_(dy)
+        hy = torch.empty((N, D), dtype=torch.bfloat16, pin_memory=True)
+        hdv = torch.empty(v.shape, dtype=v.dtype, pin_memory=True)
+        hdq = torch.empty((R,), dtype=torch.bfloat16, pin_memory=True)
+        hdw = torch.empty((D,), dtype=torch.bfloat16, pin_memory=True)
+        dv_in = torch.empty_like(v)
+        dq_in = torch.empty_like(q)
+        dw_in = torch.empty_like(w)
+        ddy = torch.empty_like(dy)
+
+        def e2e_step():
+            dv_in.copy_(hv, non_blocking=True)
+            dq_in.copy_(hq, non_blocking=True)
+            dw_in.copy_(hw, non_blocking=True)
+            ddy.copy_(hdy, non_blocking=True)
+            f = attnres_fwd(dv_in, dq_in, w_o=dw_in, key_offset=wl.key_offset, out=out,
+                            stream=stream)
+            b = attnres_bwd(dv_in, dq_in, ddy, f, w_o=dw_in, key_offset=wl.key_offset,
+                            workspace=ws, dvalues=dv, stream=stream)
+            hy.copy_(out["y"], non_blocking=True)
+            hdv.copy_(dv, non_blocking=True)
+            hdq.copy_(b["dq"], non_blocking=True)
+            hdw.copy_(b["dw_o"], non_blocking=True)
+
+        e2e_step()
+        torch.cuda.synchronize()
+        KE = max(1, min(args.e2e_steps, K))
+        s0 = torch.cuda.Event(enable_timing=True)
+        s1 = torch.cuda.Event(enable_timing=True)
+        if pg is not None:
+            pg.barrier()
+        torch.cuda.synchronize()
+        s0.record(stream)
+        for _ in range(KE):
+            e2e_step()
+        s1.record(stream)
+        torch.cuda.synchronize()
+        e2e_ms = s0.elapsed_time(s1) / KE
+        if pg is not None:
+            t = torch.tensor([e2e_ms], device=dev)
+            pg.all_reduce(t, op=pg.ReduceOp.MAX)
+            e2e_ms = float(t.item())
+        h2d = (hv.numel() + hq.numel() + hw.numel() + hdy.numel()) * 2
+        d2h = (hy.numel() + hdv.numel() + hdq.numel() + hdw.numel()) * 2
+        e2e = {"value": world * nbytes["total"] / (e2e_ms * 1e-3) / 1e9, "unit": "GB/s",
+               "ms_per_step": e2e_ms, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+        del hv, hdv
+
+    # ---------------------------------------------------------- CPU baseline
+    cpu = None
+    if cpu_wl is not None:
+        times, cores = time_oracle(cpu_wl, repeats=1)
+        cb = algorithmic_bytes(S, args.cpu_tokens, D, R, wl.out_norm, 1)["total"]
+        cpu = {"value": cb / times[0] / 1e9, "unit": "GB/s", "cores": cores, "kind": "oracle",
+               "sample": f"{args.cpu_tokens} of {N} tokens of the same workload, fwd+bwd in "
+                         f"FP64 ({times[0]:.1f} s)"}
+
+    if rank != 0:
+        if pg is not None:
+            pg.destroy_process_group()
+        return 0
+
+    peak, peak_kind = read_peak()
+    achieved = nbytes["bwd"] / (bwd_ms * 1e-3) / 1e9
+    value = world * nbytes["total"] / (ms_step * 1e-3) / 1e9
+    launches_per_step = 2 + (1 if info["bwd_split"] else 0)
+    line = {
+        "metric": METRIC,
+        "value": value,
+        "unit": "GB/s",
+        "n_gpus": world,
+        "steps": K,
+        "warmup": max(3, args.warmup),
+        "ms_per_step": ms_step,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic",
+        "config": {"workload": "S=10 N=32768 D=4096 R=4096 key_offset=0 out-norm bf16 "
+                               "(long-sequence, split-N reduction)",
+                   "bytes_per_step": nbytes["total"],
+                   "fwd_ms": fwd_ms, "bwd_ms": bwd_ms,
+                   "frac_of_peak_step": value / world / peak,
+                   "l2": "inputs larger than L2 (2.7 GB of sources per step); no flush",
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+                   "plan": info},
+        "roofline": {"bound": "hbm", "kernel": "attnres_bwd_kernel (+ finalize)",
+                     "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak, "peak_kind": f"{peak_kind} HBM copy bandwidth",
+                     "traffic": profiled_traffic("cfg3")},
+        "clocks": clocks,
+        "gpu_launches": launches_per_step * K,
+        "e2e": e2e,
+        "cpu_baseline": cpu,
+    }
+    print(json.dumps(line), flush=True)
+    if pg is not None:
+        pg.destroy_process_group()
+    return 0
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=300)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--e2e-steps", type=int, default=5)
+    ap.add_argument("--cpu-tokens", type=int, default=8192)
+    ap.add_argument("--ref-tokens", type=int, default=1024)
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--tokens", type=int, default=None,
+                    help="fewer tokens of the same workload (profiling captures only)")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -13,9 +13,9 @@
  *   y     = o                                        (out_norm == 0)
  *   y     = o * o_rstd * w_o, o_rstd = 1/sqrt(mean(o^2) + eps)   (out_norm == 1)
  *
- * The optional output RMSNorm and the statistics saved for backward reuse
- * (o_rstd next to the pre-norm output o_pre) follow "[Perf] Parallelize
- * AttnRes long-sequence reduction", Summary.  The page's canonical key slice
+ * The optional output RMSNorm and the statistic saved for backward reuse
+ * (the output reciprocal RMS o_rstd) follow "[Perf] Parallelize AttnRes
+ * long-sequence reduction", Summary.  The page's canonical key slice
  * is the final R channels (key_offset = D - R); any 0 <= key_offset <= D - R
  * is accepted.  Standard AttnRes is R == D; sliced low-rank routing is R < D
  * ("Fast Attention Residuals", section "Sliced LR-AttnRes").
@@ -104,15 +104,20 @@ typedef struct {
  *   rstd    f32  [N, S]  key reciprocal RMS r_s
  *   logit   f32  [N, S]  routing logits z_s
  *   o_rstd  f32  [N]     output reciprocal RMS; required iff out_norm, else ignored
- *   o_pre   bf16 [N, D]  pre-norm mixture o; required iff out_norm, else ignored
+ *   o_pre   f32  [N, D]  optional (NULL allowed; must be NULL without out_norm):
+ *                        the pre-norm mixture o.  The backward rebuilds o from
+ *                        the sources when it is NULL, which is free when the
+ *                        backward keeps a token's rows in shared memory
+ *                        (attnres_plan_info slot 5) and costs one more pass
+ *                        over the sources otherwise.
  *   q       bf16 [R]     query;  w_o bf16 [D], required iff out_norm
- * alpha, rstd, logit, o_rstd and o_pre are what attnres_bwd consumes.
+ * alpha, rstd, logit, o_rstd (and o_pre) are what attnres_bwd consumes.
  * Errors: INVALID_ARG (sizes, NULL pointers), ALIGNMENT (16-byte rows),
  * UNSUPPORTED (no kernel configuration fits), CUDA (launch failure).
  */
 attnres_status attnres_fwd(const attnres_params* p, const void* q, const void* w_o,
                            void* y, float* alpha, float* rstd, float* logit,
-                           float* o_rstd, void* o_pre, void* stream);
+                           float* o_rstd, float* o_pre, void* stream);
 
 /*
  * Bytes of device workspace attnres_bwd needs for these params on the
@@ -123,7 +128,8 @@ size_t attnres_bwd_workspace_bytes(const attnres_params* p);
 
 /*
  * Backward.  Inputs: q, w_o (iff out_norm), dy bf16 [N, D] contiguous, and
- * the forward's alpha, rstd, logit, o_rstd and o_pre for the same sources.
+ * the forward's alpha, rstd, logit, o_rstd and (optional, may be NULL) o_pre
+ * for the same sources.
  * Outputs (written, never accumulated):
  *   dsrc       host array of S device pointers; dsrc[s] receives the
  *              gradient of source s, bf16 rows at dsrc[s] + n * dsrc_ld
@@ -139,7 +145,7 @@ size_t attnres_bwd_workspace_bytes(const attnres_params* p);
  */
 attnres_status attnres_bwd(const attnres_params* p, const void* q, const void* w_o,
                            const void* dy, const float* alpha, const float* rstd,
-                           const float* logit, const float* o_rstd, const void* o_pre,
+                           const float* logit, const float* o_rstd, const float* o_pre,
                            void* const* dsrc, int64_t dsrc_ld, void* dq, float* dq_f32,
                            void* dw_o, float* dw_o_f32, void* workspace,
                            size_t workspace_bytes, void* stream);

@@ -77,15 +77,36 @@ def test_token_counts(N):
     check_backward(bwd, ref, out_norm=True, tag=f"N={N}")
 
 
-def test_streaming_backward_many_sources():
-    # 64 rows of 8 KB do not fit the ring next to dy/o_pre: the backward
-    # streams the key slices twice instead of keeping them resident.
+@pytest.mark.parametrize("save_o_pre", [None, False, True])
+def test_streaming_backward_many_sources(save_o_pre):
+    # 64 rows of 8 KB do not fit the ring: the backward streams the rows once
+    # per pass (o rebuild unless o_pre was saved, dot pass, key slices).
     wl = make_random(64, 90, 4096, 1024, key_offset=1024, out_norm=True, seed=64)
-    info = attnres_plan_info(cuda_copy(wl)[0], 1024, key_offset=1024, out_norm=True)
+    v, q, w, dy = cuda_copy(wl)
+    info = attnres_plan_info(v, 1024, key_offset=1024, out_norm=True)
     assert info["bwd_resident"] == 0
-    fwd, bwd, ref = run_both(wl)
+    fwd = attnres_fwd(v, q, w_o=w, key_offset=1024, save_o_pre=save_o_pre)
+    assert (fwd["o_pre"] is not None) == (save_o_pre is not False)
+    bwd = attnres_bwd(v, q, dy, fwd, w_o=w, key_offset=1024)
+    torch.cuda.synchronize()
+    ref = attnres_oracle(wl.values, wl.q, w_o=wl.w_o, dy=wl.dy, key_offset=1024)
     check_forward(fwd, ref, out_norm=True, tag="S64 streaming")
     check_backward(bwd, ref, out_norm=True, tag="S64 streaming")
+    if fwd["o_pre"] is not None:
+        o_ref = ref["y"] / (wl.w_o.double().numpy() * ref["o_rstd"][:, None])
+        assert rel_l2(to_np(fwd["o_pre"]), o_ref) < 1e-5
+
+
+def test_resident_backward_with_saved_o_pre():
+    wl = make_random(10, 120, 4096, out_norm=True, seed=65)
+    v, q, w, dy = cuda_copy(wl)
+    assert attnres_plan_info(v, 4096, key_offset=0, out_norm=True)["bwd_resident"] == 1
+    fwd = attnres_fwd(v, q, w_o=w, key_offset=0, save_o_pre=True)
+    assert fwd["o_pre"] is not None and fwd["o_pre"].dtype == torch.float32
+    bwd = attnres_bwd(v, q, dy, fwd, w_o=w, key_offset=0)
+    torch.cuda.synchronize()
+    ref = attnres_oracle(wl.values, wl.q, w_o=wl.w_o, dy=wl.dy, key_offset=0)
+    check_backward(bwd, ref, out_norm=True, tag="resident + o_pre")
 
 
 @pytest.mark.parametrize("thr", [1, 10 ** 9])
@@ -159,8 +180,8 @@ def test_poisoned_outputs_and_workspace():
            "rstd": torch.full((N, S), nan, device="cuda"),
            "logit": torch.full((N, S), nan, device="cuda"),
            "o_rstd": torch.full((N,), nan, device="cuda"),
-           "o_pre": torch.full((N, D), nan, dtype=torch.bfloat16, device="cuda")}
-    fwd = attnres_fwd(v, q, w_o=w, key_offset=0, out=out)
+           "o_pre": torch.full((N, D), nan, device="cuda")}
+    fwd = attnres_fwd(v, q, w_o=w, key_offset=0, out=out, save_o_pre=True)
     ref = attnres_oracle(wl.values, wl.q, w_o=wl.w_o, dy=wl.dy, key_offset=0)
     for thr in (1, 10 ** 9):
         ws = torch.full((1 << 22,), 0xFF, dtype=torch.uint8, device="cuda")
@@ -191,7 +212,7 @@ def test_cuda_graph_replay():
     attnres_bwd(v, q, dy, fwd0, w_o=w, key_offset=0, workspace=ws, dvalues=dv)
     torch.cuda.synchronize()
     s = torch.cuda.Stream()
-    out = {k: torch.empty_like(fwd0[k]) for k in ("y", "alpha", "rstd", "logit", "o_rstd", "o_pre")}
+    out = {k: torch.empty_like(fwd0[k]) for k in ("y", "alpha", "rstd", "logit", "o_rstd")}
     g = torch.cuda.CUDAGraph()
     with torch.cuda.stream(s):
         with torch.cuda.graph(g, stream=s):
