@@ -41,12 +41,6 @@ bool device_info(DeviceInfo* out) {
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 bool aligned4(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
 
-int next_pow2(int x) {
-    int p = 1;
-    while (p < x) p <<= 1;
-    return p;
-}
-
 attnres_status check_shape(const attnres_params* p) {
     if (!p) return ATTNRES_ERR_INVALID_ARG;
     if (p->S < 1 || p->S > ATTNRES_MAX_S) return ATTNRES_ERR_INVALID_ARG;
@@ -92,15 +86,10 @@ attnres_status make_plan(const attnres_params* p, Plan* plan) {
     pl.smem_fwd = make_layout(slots, pl.slot_bytes, pl.ncw, pl.s_pad, false).total;
     pl.smem_bwd = make_layout(slots, pl.slot_bytes, pl.ncw, pl.s_pad, true).total;
     // Forward groups keep their rows resident: at most half the ring each.
-    int gp = next_pow2(p->S);
-    if (gp < 2) gp = 2;
-    if (gp > 16) gp = 16;
-    while (gp > 2 && 2 * (gp < p->S ? gp : p->S) > slots) gp >>= 1;
-    pl.gp_fwd = gp;
-    int gpb = next_pow2(p->S);
-    if (gpb < 2) gpb = 2;
-    if (gpb > 16) gpb = 16;
-    pl.gp_bwd = gpb;
+    int g = p->S < kMaxGroup ? p->S : kMaxGroup;
+    if (g > slots / 2) g = slots / 2;
+    if (g < 1) g = 1;
+    pl.group = g;
     pl.resident = (p->S + 1) <= slots ? 1 : 0;
     const int thr = p->split_n_threshold > 0 ? p->split_n_threshold : ATTNRES_DEFAULT_SPLIT_N;
     pl.split = p->N >= thr ? 1 : 0;
@@ -156,7 +145,7 @@ attnres_status attnres_plan_info(const attnres_params* p, int64_t out[8]) {
     out[1] = pl.ncw;
     out[2] = pl.vpt;
     out[3] = pl.slots;
-    out[4] = pl.gp_fwd;
+    out[4] = pl.group;
     out[5] = pl.resident;
     out[6] = static_cast<int64_t>(pl.smem_bwd);
     out[7] = pl.split;
@@ -197,6 +186,7 @@ attnres_status attnres_fwd(const attnres_params* p, const void* q, const void* w
     a.slot_bytes = pl.slot_bytes;
     a.ncw = pl.ncw;
     a.s_pad = pl.s_pad;
+    a.group = pl.group;
     a.q = static_cast<const uint16_t*>(q);
     a.w_o = static_cast<const uint16_t*>(w_o);
     a.y = static_cast<uint16_t*>(y);

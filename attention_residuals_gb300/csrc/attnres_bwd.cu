@@ -43,11 +43,6 @@ namespace {
 // First failed wait of any backward launch (0 = none).
 __device__ unsigned int g_bwd_error = 0;
 
-struct VecInfo {
-    int col;
-    unsigned kmask;
-};
-
 __device__ __forceinline__ void advance(int& slot, uint32_t& phase, int slots) {
     if (++slot == slots) {
         slot = 0;
@@ -55,9 +50,15 @@ __device__ __forceinline__ void advance(int& slot, uint32_t& phase, int slots) {
     }
 }
 
+__device__ __forceinline__ int ring_add(int slot, int k, int slots) {
+    const int r = slot + k;
+    return r >= slots ? r - slots : r;
+}
+
 __device__ __forceinline__ float ldcg_f32(const float* p) { return __ldcg(p); }
 
-template <int VPT, int GP>
+// KEYALL: every channel is a key channel (R == D), so no per-vector masks.
+template <int VPT, bool KEYALL>
 __global__ void __launch_bounds__(kMaxThreads, 1) attnres_bwd_kernel(const __grid_constant__ BwdArgs a) {
     extern __shared__ __align__(128) unsigned char smem[];
     const int ncw = a.ncw;
@@ -70,15 +71,16 @@ __global__ void __launch_bounds__(kMaxThreads, 1) attnres_bwd_kernel(const __gri
     uint64_t* empty = reinterpret_cast<uint64_t*>(smem + L.empty);
     uint64_t* tfull = reinterpret_cast<uint64_t*>(smem + L.tfull);
     uint64_t* tempty = reinterpret_cast<uint64_t*>(smem + L.tempty);
-    float* red = reinterpret_cast<float*>(smem + L.red);
+    float* red = reinterpret_cast<float*>(smem + L.red);  // [2][ncw][red_stride]
     float* tok = reinterpret_cast<float*>(smem + L.tok);  // [kTokSlots][3*s_pad + 4]
     float* cA = reinterpret_cast<float*>(smem + L.coef);  // alpha_s
-    float* c1 = cA + s_pad;
-    float* c2 = c1 + s_pad;
+    float* c1 = cA + s_pad;                               // rstd_s dz_s
+    float* c2 = c1 + s_pad;                               // -rstd_s^2 dz_s z_s / R
     float* da_all = c2 + s_pad;
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L.misc);
     volatile int* ticket_flag = abort_flag + 1;
     const int tstride = 3 * s_pad + 4;
+    const int red_stride = L.red_stride;
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -105,7 +107,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1) attnres_bwd_kernel(const __gri
         // ------------------------------------------------------ producer
         const uint64_t pol = policy_evict_first();
         const uint32_t row_bytes = static_cast<uint32_t>(D) * 2u;
-        // Key slice of the second pass: only the key channels when they
+        // Key slice of the write pass: only the key channels when they
         // start and end on 16-byte boundaries, else the whole row.
         const bool key_only = ((a.ko & 7) == 0) && ((a.R & 7) == 0);
         const uint32_t key_off_b = key_only ? static_cast<uint32_t>(a.ko) * 2u : 0u;
@@ -178,31 +180,41 @@ __global__ void __launch_bounds__(kMaxThreads, 1) attnres_bwd_kernel(const __gri
     // ---------------------------------------------------------- consumers
     const int ncv = D >> 3;
     const int ko = a.ko, kend = a.ko + a.R;
-    VecInfo vi[VPT];
-    float qf[VPT][8];
-    float wf[VPT][8];
-    float dq_acc[VPT][8];
-    float dw_acc[VPT][8];
+    int col[VPT];
+    unsigned kmask[VPT];
+    float2 qs[VPT][4];     // scale * q at the owned key channels, 0 elsewhere
+    uint4 wb[VPT];         // output-norm weight bits
+    float2 dq_acc[VPT][4];
+    float2 dw_acc[VPT][4];
 #pragma unroll
     for (int i = 0; i < VPT; ++i) {
         const int c = threadIdx.x + i * nct;
-        vi[i].col = c < ncv ? c : -1;
+        col[i] = c < ncv ? c : -1;
         unsigned m = 0;
+        uint32_t ww[4];
 #pragma unroll
-        for (int e = 0; e < 8; ++e) {
-            const int j = 8 * c + e;
-            const bool in_key = vi[i].col >= 0 && j >= ko && j < kend;
-            m |= in_key ? (1u << e) : 0u;
-            qf[i][e] = in_key ? a.scale * bf16_bits_to_float(a.q[j - ko]) : 0.0f;
-            wf[i][e] = (a.out_norm && vi[i].col >= 0) ? bf16_bits_to_float(a.w_o[j]) : 1.0f;
-            dq_acc[i][e] = 0.0f;
-            dw_acc[i][e] = 0.0f;
+        for (int k = 0; k < 4; ++k) {
+            float qv[2];
+            uint32_t wv = 0;
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                const int j = 8 * c + 2 * k + h;
+                const bool in_key = col[i] >= 0 && j >= ko && j < kend;
+                m |= in_key ? (1u << (2 * k + h)) : 0u;
+                qv[h] = in_key ? a.scale * bf16_bits_to_float(a.q[j - ko]) : 0.0f;
+                const uint32_t wh = (a.out_norm && col[i] >= 0) ? a.w_o[j] : 0x3f80u;
+                wv |= wh << (16 * h);
+            }
+            qs[i][k] = make_float2(qv[0], qv[1]);
+            ww[k] = wv;
+            dq_acc[i][k] = make_float2(0.0f, 0.0f);
+            dw_acc[i][k] = make_float2(0.0f, 0.0f);
         }
-        vi[i].kmask = m;
+        kmask[i] = m;
+        wb[i] = make_uint4(ww[0], ww[1], ww[2], ww[3]);
     }
     const float inv_r = 1.0f / static_cast<float>(a.R);
     const float inv_d = 1.0f / static_cast<float>(D);
-    constexpr int SH = 5 - log2_const<GP>();
 
     int slot = 0;
     uint32_t phase = 0;
@@ -214,55 +226,77 @@ __global__ void __launch_bounds__(kMaxThreads, 1) attnres_bwd_kernel(const __gri
         mbar_wait(tfull + ts, tphase, abort_flag, &g_bwd_error, kSiteBwdTokStat);
         const float* tk = tok + ts * tstride;
 
+        // ---- dy into registers; its slot is free again at once
+        uint4 dyv[VPT];
+        {
+            mbar_wait(full + slot, phase, abort_flag, &g_bwd_error, kSiteBwdConsumer);
+            const unsigned char* dy_row = ring + static_cast<size_t>(slot) * a.slot_bytes;
+#pragma unroll
+            for (int i = 0; i < VPT; ++i)
+                dyv[i] = col[i] >= 0 ? ld_shared_v4(dy_row + col[i] * 16) : make_uint4(0u, 0u, 0u, 0u);
+            __syncwarp();
+            if (lane == 0) mbar_arrive(empty + slot);
+            advance(slot, phase, slots);
+        }
+
         // ---- gradient wrt the mixture o (kept in registers)
-        float dout[VPT][8];
-        const int dy_slot = slot;
-        mbar_wait(full + slot, phase, abort_flag, &g_bwd_error, kSiteBwdConsumer);
-        advance(slot, phase, slots);
-        const unsigned char* dy_row = ring + static_cast<size_t>(dy_slot) * a.slot_bytes;
+        float2 dout[VPT][4];
         if (a.out_norm) {
-            // o = sum_s alpha_s v_s in FP32: from the caller's saved copy, or
+            // o = sum_s alpha_s v_s in FP32: the caller's saved copy, or
             // rebuilt from the source rows (resident: the rows the dot pass
             // uses next; streaming: a dedicated pass of rows).
-            float o[VPT][8];
+            float2 o[VPT][4];
             if (a.o_pre) {
                 const float* prow = a.o_pre + n * static_cast<long long>(D);
 #pragma unroll
                 for (int i = 0; i < VPT; ++i) {
-                    if (vi[i].col >= 0) {
-                        const uint4 lo = ld_global_nc_v4(prow + 8 * vi[i].col);
-                        const uint4 hi = ld_global_nc_v4(prow + 8 * vi[i].col + 4);
-                        o[i][0] = __uint_as_float(lo.x); o[i][1] = __uint_as_float(lo.y);
-                        o[i][2] = __uint_as_float(lo.z); o[i][3] = __uint_as_float(lo.w);
-                        o[i][4] = __uint_as_float(hi.x); o[i][5] = __uint_as_float(hi.y);
-                        o[i][6] = __uint_as_float(hi.z); o[i][7] = __uint_as_float(hi.w);
+                    if (col[i] >= 0) {
+                        const uint4 lo = ld_global_nc_v4(prow + 8 * col[i]);
+                        const uint4 hi = ld_global_nc_v4(prow + 8 * col[i] + 4);
+                        o[i][0] = make_float2(__uint_as_float(lo.x), __uint_as_float(lo.y));
+                        o[i][1] = make_float2(__uint_as_float(lo.z), __uint_as_float(lo.w));
+                        o[i][2] = make_float2(__uint_as_float(hi.x), __uint_as_float(hi.y));
+                        o[i][3] = make_float2(__uint_as_float(hi.z), __uint_as_float(hi.w));
+                    } else {
+#pragma unroll
+                        for (int k = 0; k < 4; ++k) o[i][k] = make_float2(0.0f, 0.0f);
                     }
                 }
             } else {
 #pragma unroll
                 for (int i = 0; i < VPT; ++i)
 #pragma unroll
-                    for (int e = 0; e < 8; ++e) o[i][e] = 0.0f;
+                    for (int k = 0; k < 4; ++k) o[i][k] = make_float2(0.0f, 0.0f);
                 int aslot = slot;
                 uint32_t aphase = phase;
+                if (a.resident) {
+                    for (int s = 0; s < S; ++s) {
+                        mbar_wait(full + aslot, aphase, abort_flag, &g_bwd_error, kSiteBwdConsumer);
+                        advance(aslot, aphase, slots);
+                    }
+                    aslot = slot;
+                }
+#pragma unroll 2
                 for (int s = 0; s < S; ++s) {
-                    mbar_wait(full + aslot, aphase, abort_flag, &g_bwd_error, kSiteBwdConsumer);
+                    if (!a.resident) mbar_wait(full + aslot, aphase, abort_flag, &g_bwd_error, kSiteBwdConsumer);
                     const unsigned char* row = ring + static_cast<size_t>(aslot) * a.slot_bytes;
                     const float al = tk[s];
+                    const float2 al2 = make_float2(al, al);
 #pragma unroll
                     for (int i = 0; i < VPT; ++i) {
-                        if (vi[i].col >= 0) {
-                            float x[8];
-                            unpack8(ld_shared_v4(row + vi[i].col * 16), x);
+                        if (col[i] >= 0) {
+                            const uint4 xv = ld_shared_v4(row + col[i] * 16);
 #pragma unroll
-                            for (int e = 0; e < 8; ++e) o[i][e] = fmaf(al, x[e], o[i][e]);
+                            for (int k = 0; k < 4; ++k) o[i][k] = ffma2(al2, bf2_to_f2(u4_get(xv, k)), o[i][k]);
                         }
                     }
                     if (!a.resident) {
                         __syncwarp();
                         if (lane == 0) mbar_arrive(empty + aslot);
+                        advance(aslot, aphase, slots);
+                    } else {
+                        aslot = ring_add(aslot, 1, slots);
                     }
-                    advance(aslot, aphase, slots);
                 }
                 if (!a.resident) {  // the streamed o-pass rows are consumed
                     slot = aslot;
@@ -270,101 +304,103 @@ __global__ void __launch_bounds__(kMaxThreads, 1) attnres_bwd_kernel(const __gri
                 }
             }
             const float rho = tk[3 * s_pad];
-            float gy = 0.0f;
+            const float2 rho2 = make_float2(rho, rho);
+            float2 gy2 = make_float2(0.0f, 0.0f);
 #pragma unroll
             for (int i = 0; i < VPT; ++i) {
-                if (vi[i].col >= 0) {
-                    float g[8];
-                    unpack8(ld_shared_v4(dy_row + vi[i].col * 16), g);
 #pragma unroll
-                    for (int e = 0; e < 8; ++e) {
-                        const float yh = o[i][e] * rho;
-                        o[i][e] = yh;
-                        dw_acc[i][e] = fmaf(g[e], yh, dw_acc[i][e]);
-                        g[e] *= wf[i][e];
-                        gy = fmaf(g[e], yh, gy);
-                        dout[i][e] = g[e];
-                    }
-                } else {
-#pragma unroll
-                    for (int e = 0; e < 8; ++e) dout[i][e] = 0.0f;
+                for (int k = 0; k < 4; ++k) {
+                    const float2 yh = fmul2(o[i][k], rho2);
+                    const float2 g = bf2_to_f2(u4_get(dyv[i], k));
+                    o[i][k] = yh;
+                    dw_acc[i][k] = ffma2(g, yh, dw_acc[i][k]);
+                    const float2 gw = fmul2(g, bf2_to_f2(u4_get(wb[i], k)));
+                    gy2 = ffma2(gw, yh, gy2);
+                    dout[i][k] = gw;
                 }
             }
-            __syncwarp();
-            if (lane == 0) mbar_arrive(empty + dy_slot);
-            gy = warp_sum(gy);
-            if (lane == 0) red[(rbuf * ncw + warp) * kReduceStride] = gy;
+            const float gy = warp_sum(gy2.x + gy2.y);
+            if (lane == 0) red[(rbuf * ncw + warp) * red_stride] = gy;
             named_bar_sync(1, nct);
             float tot = 0.0f;
-            for (int w = 0; w < ncw; ++w) tot += red[(rbuf * ncw + w) * kReduceStride];
+            for (int w = 0; w < ncw; ++w) tot += red[(rbuf * ncw + w) * red_stride];
             rbuf ^= 1;
-            const float cg = tot * inv_d;
+            const float ncg = -tot * inv_d;
+            const float2 ncg2 = make_float2(ncg, ncg);
 #pragma unroll
             for (int i = 0; i < VPT; ++i)
 #pragma unroll
-                for (int e = 0; e < 8; ++e) dout[i][e] = rho * fmaf(-o[i][e], cg, dout[i][e]);
+                for (int k = 0; k < 4; ++k) dout[i][k] = fmul2(rho2, ffma2(o[i][k], ncg2, dout[i][k]));
         } else {
 #pragma unroll
-            for (int i = 0; i < VPT; ++i) {
-                if (vi[i].col >= 0) {
-                    unpack8(ld_shared_v4(dy_row + vi[i].col * 16), dout[i]);
-                } else {
+            for (int i = 0; i < VPT; ++i)
 #pragma unroll
-                    for (int e = 0; e < 8; ++e) dout[i][e] = 0.0f;
-                }
-            }
-            __syncwarp();
-            if (lane == 0) mbar_arrive(empty + dy_slot);
+                for (int k = 0; k < 4; ++k) dout[i][k] = bf2_to_f2(u4_get(dyv[i], k));
         }
 
-        // ---- dot pass: da_s = <do, v_s>
+        // ---- dot pass: da_s = <do, v_s>, four rows at a time
         const int v_slot0 = slot;
         const uint32_t v_phase0 = phase;
-        for (int g0 = 0; g0 < S; g0 += GP) {
-            const int gs = min(GP, S - g0);
-            float part[GP];
+        if (a.resident) {
+            int ws = slot;
+            uint32_t wp = phase;
+            for (int s = 0; s < S; ++s) {  // completed phases return at once
+                mbar_wait(full + ws, wp, abort_flag, &g_bwd_error, kSiteBwdConsumer);
+                advance(ws, wp, slots);
+            }
+        }
+        float* redw = red + (rbuf * ncw + warp) * red_stride;
+        for (int c0 = 0; c0 < S; c0 += 4) {
+            const int cn = min(4, S - c0);
+            if (!a.resident) {
+                int ws = slot;
+                uint32_t wp = phase;
+                for (int r = 0; r < cn; ++r) {
+                    mbar_wait(full + ws, wp, abort_flag, &g_bwd_error, kSiteBwdConsumer);
+                    advance(ws, wp, slots);
+                }
+            }
+            float part[4];
 #pragma unroll
-            for (int k = 0; k < GP; ++k) part[k] = 0.0f;
-#pragma unroll
-            for (int s = 0; s < GP; ++s) {
-                if (s < gs) {
-                    mbar_wait(full + slot, phase, abort_flag, &g_bwd_error, kSiteBwdConsumer);
-                    const unsigned char* row = ring + static_cast<size_t>(slot) * a.slot_bytes;
-                    float d = 0.0f;
+            for (int r = 0; r < 4; ++r) {
+                float2 d2 = make_float2(0.0f, 0.0f);
+                if (r < cn) {
+                    const unsigned char* row =
+                        ring + static_cast<size_t>(ring_add(a.resident ? v_slot0 : slot, (a.resident ? c0 : 0) + r, slots)) *
+                                   a.slot_bytes;
 #pragma unroll
                     for (int i = 0; i < VPT; ++i) {
-                        if (vi[i].col >= 0) {
-                            float x[8];
-                            unpack8(ld_shared_v4(row + vi[i].col * 16), x);
+                        if (col[i] >= 0) {
+                            const uint4 xv = ld_shared_v4(row + col[i] * 16);
 #pragma unroll
-                            for (int e = 0; e < 8; ++e) d = fmaf(dout[i][e], x[e], d);
+                            for (int k = 0; k < 4; ++k) d2 = ffma2(dout[i][k], bf2_to_f2(u4_get(xv, k)), d2);
                         }
                     }
-                    part[s] = d;
-                    if (!a.resident) {
-                        __syncwarp();
-                        if (lane == 0) mbar_arrive(empty + slot);
-                    }
+                }
+                part[r] = d2.x + d2.y;
+            }
+            if (!a.resident) {
+                __syncwarp();
+                for (int r = 0; r < cn; ++r) {
+                    if (lane == 0) mbar_arrive(empty + slot);
                     advance(slot, phase, slots);
                 }
             }
-            warp_reduce_scatter<GP>(part, lane);
-            if ((lane & ((1 << SH) - 1)) == 0)
-                red[(rbuf * ncw + warp) * kReduceStride + (lane >> SH)] = part[0];
-            named_bar_sync(1, nct);
-            if (warp == 0 && lane < gs) {
-                float d = 0.0f;
-                for (int w = 0; w < ncw; ++w) d += red[(rbuf * ncw + w) * kReduceStride + lane];
-                da_all[g0 + lane] = d;
-            }
-            rbuf ^= 1;
+            warp_reduce_scatter<4>(part, lane);
+            // lane l holds element l >> 3
+            if ((lane & 7) == 0 && c0 + (lane >> 3) < S) redw[c0 + (lane >> 3)] = part[0];
         }
+        named_bar_sync(1, nct);
 
         // ---- per-source coefficients (warp 0)
         if (warp == 0) {
-            __syncwarp();
             float part_delta = 0.0f;
-            for (int s = lane; s < S; s += 32) part_delta = fmaf(tk[s], da_all[s], part_delta);
+            for (int s = lane; s < S; s += 32) {
+                float d = 0.0f;
+                for (int w = 0; w < ncw; ++w) d += red[(rbuf * ncw + w) * red_stride + s];
+                da_all[s] = d;
+                part_delta = fmaf(tk[s], d, part_delta);
+            }
             const float delta = warp_sum(part_delta);
             for (int s = lane; s < S; s += 32) {
                 const float al = tk[s];
@@ -372,12 +408,13 @@ __global__ void __launch_bounds__(kMaxThreads, 1) attnres_bwd_kernel(const __gri
                 const float z = tk[2 * s_pad + s];
                 const float dz = al * (da_all[s] - delta);
                 cA[s] = al;
-                c1[s] = r * dz;  // qf carries `scale`, so c1 * qf = rstd * scale * dz * q
+                c1[s] = r * dz;  // qs carries `scale`, so c1 * qs = rstd * scale * dz * q
                 c2[s] = -(r * r) * dz * z * inv_r;
             }
             __syncwarp();
             if (lane == 0) mbar_arrive(tempty + ts);
         }
+        rbuf ^= 1;
         if (++ts == kTokSlots) {
             ts = 0;
             tphase ^= 1u;
@@ -389,33 +426,36 @@ __global__ void __launch_bounds__(kMaxThreads, 1) attnres_bwd_kernel(const __gri
             slot = v_slot0;
             phase = v_phase0;
         }
+#pragma unroll 2
         for (int s = 0; s < S; ++s) {
             if (!a.resident) mbar_wait(full + slot, phase, abort_flag, &g_bwd_error, kSiteBwdConsumer);
             const unsigned char* row = ring + static_cast<size_t>(slot) * a.slot_bytes;
             const float al = cA[s];
             const float k1 = c1[s];
             const float k2 = c2[s];
+            const float2 al2 = make_float2(al, al), k12 = make_float2(k1, k1), k22 = make_float2(k2, k2);
             uint16_t* drow = static_cast<uint16_t*>(a.dsrc[s]) + n * a.dsrc_ld;
 #pragma unroll
             for (int i = 0; i < VPT; ++i) {
-                if (vi[i].col >= 0) {
-                    float dv[8];
+                if (col[i] >= 0) {
+                    float2 dv[4];
 #pragma unroll
-                    for (int e = 0; e < 8; ++e) dv[e] = al * dout[i][e];
-                    if (vi[i].kmask) {
-                        float x[8];
-                        unpack8(ld_shared_v4(row + vi[i].col * 16), x);
-                        if (vi[i].kmask != 0xffu) {
+                    for (int k = 0; k < 4; ++k) dv[k] = fmul2(al2, dout[i][k]);
+                    if (KEYALL || kmask[i] != 0u) {
+                        const uint4 xv = ld_shared_v4(row + col[i] * 16);
 #pragma unroll
-                            for (int e = 0; e < 8; ++e) x[e] = ((vi[i].kmask >> e) & 1u) ? x[e] : 0.0f;
-                        }
-#pragma unroll
-                        for (int e = 0; e < 8; ++e) {
-                            dv[e] = fmaf(k1, qf[i][e], fmaf(k2, x[e], dv[e]));
-                            dq_acc[i][e] = fmaf(k1, x[e], dq_acc[i][e]);
+                        for (int k = 0; k < 4; ++k) {
+                            float2 x = bf2_to_f2(u4_get(xv, k));
+                            if (!KEYALL && kmask[i] != 0xffu) {
+                                if (!((kmask[i] >> (2 * k)) & 1u)) x.x = 0.0f;
+                                if (!((kmask[i] >> (2 * k + 1)) & 1u)) x.y = 0.0f;
+                            }
+                            dv[k] = ffma2(k12, qs[i][k], ffma2(k22, x, dv[k]));
+                            dq_acc[i][k] = ffma2(k12, x, dq_acc[i][k]);
                         }
                     }
-                    st_global_cs_v4(drow + 8 * vi[i].col, pack8(dv));
+                    st_global_cs_v4(drow + 8 * col[i],
+                                    make_uint4(pack_f2(dv[0]), pack_f2(dv[1]), pack_f2(dv[2]), pack_f2(dv[3])));
                 }
             }
             __syncwarp();
@@ -431,13 +471,15 @@ __global__ void __launch_bounds__(kMaxThreads, 1) attnres_bwd_kernel(const __gri
     float* my_part = a.part + static_cast<size_t>(blockIdx.x) * W;
 #pragma unroll
     for (int i = 0; i < VPT; ++i) {
-        if (vi[i].col >= 0) {
+        if (col[i] >= 0) {
 #pragma unroll
             for (int e = 0; e < 8; ++e) {
-                const int j = 8 * vi[i].col + e;
+                const int j = 8 * col[i] + e;
+                const float dqv = (e & 1) ? dq_acc[i][e >> 1].y : dq_acc[i][e >> 1].x;
+                const float dwv = (e & 1) ? dw_acc[i][e >> 1].y : dw_acc[i][e >> 1].x;
                 // dq = scale * sum_s dz_s k_s = scale * sum_s c1_s t_s
-                if ((vi[i].kmask >> e) & 1u) my_part[j - ko] = a.scale * dq_acc[i][e];
-                if (a.out_norm) my_part[R + j] = dw_acc[i][e];
+                if ((kmask[i] >> e) & 1u) my_part[j - ko] = a.scale * dqv;
+                if (a.out_norm) my_part[R + j] = dwv;
             }
         }
     }
@@ -512,9 +554,9 @@ __global__ void __launch_bounds__(256) attnres_finalize_kernel(const float* __re
     }
 }
 
-template <int VPT, int GP>
+template <int VPT, bool KEYALL>
 cudaError_t launch_bwd_t(const Plan& plan, const BwdArgs& a, cudaStream_t stream) {
-    auto kern = attnres_bwd_kernel<VPT, GP>;
+    auto kern = attnres_bwd_kernel<VPT, KEYALL>;
     cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                            static_cast<int>(plan.smem_bwd));
     if (err != cudaSuccess) return err;
@@ -528,14 +570,9 @@ cudaError_t launch_bwd_t(const Plan& plan, const BwdArgs& a, cudaStream_t stream
 }
 
 template <int VPT>
-cudaError_t dispatch_gp(const Plan& plan, const BwdArgs& a, cudaStream_t stream) {
-    switch (plan.gp_bwd) {
-        case 2: return launch_bwd_t<VPT, 2>(plan, a, stream);
-        case 4: return launch_bwd_t<VPT, 4>(plan, a, stream);
-        case 8: return launch_bwd_t<VPT, 8>(plan, a, stream);
-        case 16: return launch_bwd_t<VPT, 16>(plan, a, stream);
-        default: return cudaErrorInvalidConfiguration;
-    }
+cudaError_t dispatch_key(const Plan& plan, const BwdArgs& a, cudaStream_t stream) {
+    return (a.R == a.D) ? launch_bwd_t<VPT, true>(plan, a, stream)
+                        : launch_bwd_t<VPT, false>(plan, a, stream);
 }
 
 }  // namespace
@@ -549,9 +586,9 @@ unsigned take_bwd_error() {
 
 cudaError_t launch_bwd(const Plan& plan, const BwdArgs& a, cudaStream_t stream) {
     switch (plan.vpt) {
-        case 1: return dispatch_gp<1>(plan, a, stream);
-        case 2: return dispatch_gp<2>(plan, a, stream);
-        case 4: return dispatch_gp<4>(plan, a, stream);
+        case 1: return dispatch_key<1>(plan, a, stream);
+        case 2: return dispatch_key<2>(plan, a, stream);
+        case 4: return dispatch_key<4>(plan, a, stream);
         default: return cudaErrorInvalidConfiguration;
     }
 }

@@ -12,13 +12,14 @@
 // (one cp.async.bulk per row, completion counted on an mbarrier).  Consumer
 // thread t owns the 16-byte column vectors t, t + 32*ncw, ... of every row,
 // so each warp reads 512 contiguous bytes per shared load.  Sources are taken
-// in groups of GP: one pass over the group's rows accumulates the key
-// sum-of-squares and the query dot, a warp reduce-scatter plus one
-// cross-warp step yields the group's logits, warp 0 updates the running
-// softmax maximum and denominator, and a second pass over the same
-// resident rows adds the weighted rows into FP32 registers before the slots
-// are released.  The output norm needs one more CTA reduction per token.
-// The pre-norm mixture o is written (FP32) only when the caller asks for it.
+// in groups of up to 32 rows that stay resident together: the consumers wait
+// for the whole group, then pass 1 accumulates the key sum of squares and
+// the query dot four rows at a time (packed FP32 FMAs, independent chains),
+// each four-row chunk ends with a warp reduce-scatter, one cross-warp step
+// gives the group's logits, warp 0 updates the running softmax maximum and
+// denominator, and pass 2 adds the weighted rows into FP32 registers and
+// releases the slots.  The output norm needs one more CTA reduction per
+// token.  The pre-norm mixture o is written (FP32) only when asked for.
 // This is a bandwidth-bound per-token reduction: no tensor cores.
 #include <cfloat>
 
@@ -32,11 +33,6 @@ namespace {
 // First failed wait of any forward launch (0 = none).
 __device__ unsigned int g_fwd_error = 0;
 
-struct VecInfo {
-    int col;          // 16-byte column vector index, -1 when not owned
-    unsigned kmask;   // bit e: channel 8*col+e lies in the key slice
-};
-
 __device__ __forceinline__ void advance(int& slot, uint32_t& phase, int slots) {
     if (++slot == slots) {
         slot = 0;
@@ -44,7 +40,13 @@ __device__ __forceinline__ void advance(int& slot, uint32_t& phase, int slots) {
     }
 }
 
-template <int VPT, int GP>
+__device__ __forceinline__ int ring_add(int slot, int k, int slots) {
+    const int r = slot + k;
+    return r >= slots ? r - slots : r;
+}
+
+// KEYALL: every channel is a key channel (R == D), so no per-vector masks.
+template <int VPT, bool KEYALL>
 __global__ void __launch_bounds__(kMaxThreads, 1) attnres_fwd_kernel(const __grid_constant__ FwdArgs a) {
     extern __shared__ __align__(128) unsigned char smem[];
     const int ncw = a.ncw;
@@ -54,11 +56,12 @@ __global__ void __launch_bounds__(kMaxThreads, 1) attnres_fwd_kernel(const __gri
     unsigned char* ring = smem + L.ring;
     uint64_t* full = reinterpret_cast<uint64_t*>(smem + L.full);
     uint64_t* empty = reinterpret_cast<uint64_t*>(smem + L.empty);
-    float* red = reinterpret_cast<float*>(smem + L.red);
-    float* zall = reinterpret_cast<float*>(smem + L.coef);
-    float* rall = zall + a.s_pad;
+    float* red = reinterpret_cast<float*>(smem + L.red);     // [2][ncw][red_stride]
+    float* zall = reinterpret_cast<float*>(smem + L.coef);  // [s_pad]
+    float* rall = zall + a.s_pad;                           // [s_pad]
     float* coef = rall + a.s_pad;  // [2][64]: e_s (s < 32), corr at 32, 1/l at 33
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L.misc);
+    const int red_stride = L.red_stride;
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -110,93 +113,108 @@ __global__ void __launch_bounds__(kMaxThreads, 1) attnres_fwd_kernel(const __gri
     // ---------------------------------------------------------- consumers
     const int ncv = a.D >> 3;
     const int ko = a.ko, kend = a.ko + a.R;
-    VecInfo vi[VPT];
-    float qf[VPT][8];
-    float wf[VPT][8];
+    int col[VPT];
+    unsigned kmask[VPT];   // bit e: channel 8*col+e lies in the key slice
+    uint4 qb[VPT];         // query bits at the owned channels (0 outside the key)
+    uint4 wb[VPT];         // output-norm weight bits (1.0 without the norm)
 #pragma unroll
     for (int i = 0; i < VPT; ++i) {
         const int c = threadIdx.x + i * nct;
-        vi[i].col = c < ncv ? c : -1;
+        col[i] = c < ncv ? c : -1;
         unsigned m = 0;
+        uint32_t qw[4], ww[4];
 #pragma unroll
-        for (int e = 0; e < 8; ++e) {
-            const int j = 8 * c + e;
-            const bool in_key = vi[i].col >= 0 && j >= ko && j < kend;
-            m |= in_key ? (1u << e) : 0u;
-            qf[i][e] = in_key ? bf16_bits_to_float(a.q[j - ko]) : 0.0f;
-            wf[i][e] = (a.out_norm && vi[i].col >= 0) ? bf16_bits_to_float(a.w_o[j]) : 1.0f;
+        for (int k = 0; k < 4; ++k) {
+            uint32_t qv = 0, wv = 0;
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                const int j = 8 * c + 2 * k + h;
+                const bool in_key = col[i] >= 0 && j >= ko && j < kend;
+                m |= in_key ? (1u << (2 * k + h)) : 0u;
+                const uint32_t qh = in_key ? a.q[j - ko] : 0u;
+                const uint32_t wh = (a.out_norm && col[i] >= 0) ? a.w_o[j] : 0x3f80u;
+                qv |= qh << (16 * h);
+                wv |= wh << (16 * h);
+            }
+            qw[k] = qv;
+            ww[k] = wv;
         }
-        vi[i].kmask = m;
+        kmask[i] = m;
+        qb[i] = make_uint4(qw[0], qw[1], qw[2], qw[3]);
+        wb[i] = make_uint4(ww[0], ww[1], ww[2], ww[3]);
     }
     const float inv_r = 1.0f / static_cast<float>(a.R);
     const float inv_d = 1.0f / static_cast<float>(a.D);
-    constexpr int K2 = 2 * GP;
-    constexpr int SH = 5 - log2_const<K2>();
+    const int G = a.group;  // rows per group (<= 32, <= slots)
 
     int slot = 0;
     uint32_t phase = 0;
     int rbuf = 0;
 
     for (long long n = blockIdx.x; n < N; n += gridDim.x) {
-        float acc[VPT][8];
+        float2 acc[VPT][4];
 #pragma unroll
         for (int i = 0; i < VPT; ++i)
 #pragma unroll
-            for (int e = 0; e < 8; ++e) acc[i][e] = 0.0f;
+            for (int k = 0; k < 4; ++k) acc[i][k] = make_float2(0.0f, 0.0f);
         float m_run = -FLT_MAX;  // meaningful in warp 0
         float l_run = 0.0f;
         int cbuf = 0;
 
-        for (int g0 = 0; g0 < S; g0 += GP) {
-            const int gs = min(GP, S - g0);
+        for (int g0 = 0; g0 < S; g0 += G) {
+            const int gs = min(G, S - g0);
             const int gslot = slot;
-            const uint32_t gphase = phase;
-            float part[K2];
+            // wait for the whole group, then compute without interruptions
+            for (int s = 0; s < gs; ++s) {
+                mbar_wait(full + slot, phase, abort_flag, &g_fwd_error, kSiteFwdConsumer);
+                advance(slot, phase, slots);
+            }
+            float* redw = red + (rbuf * ncw + warp) * red_stride;
+            // pass 1: key sum of squares and query dot, four rows at a time
+            for (int c0 = 0; c0 < gs; c0 += 4) {
+                float part[8];
 #pragma unroll
-            for (int k = 0; k < K2; ++k) part[k] = 0.0f;
-            // pass 1: key sum of squares and query dot per source
+                for (int r = 0; r < 4; ++r) {
+                    float2 ss2 = make_float2(0.0f, 0.0f), qt2 = make_float2(0.0f, 0.0f);
+                    if (c0 + r < gs) {
+                        const unsigned char* row =
+                            ring + static_cast<size_t>(ring_add(gslot, c0 + r, slots)) * a.slot_bytes;
 #pragma unroll
-            for (int s = 0; s < GP; ++s) {
-                if (s < gs) {
-                    mbar_wait(full + slot, phase, abort_flag, &g_fwd_error, kSiteFwdConsumer);
-                    const unsigned char* row = ring + static_cast<size_t>(slot) * a.slot_bytes;
-                    float ss = 0.0f, qt = 0.0f;
+                        for (int i = 0; i < VPT; ++i) {
+                            if (KEYALL ? (col[i] >= 0) : (kmask[i] != 0u)) {
+                                const uint4 xv = ld_shared_v4(row + col[i] * 16);
 #pragma unroll
-                    for (int i = 0; i < VPT; ++i) {
-                        if (vi[i].kmask) {
-                            float x[8];
-                            unpack8(ld_shared_v4(row + vi[i].col * 16), x);
-                            if (vi[i].kmask == 0xffu) {
-#pragma unroll
-                                for (int e = 0; e < 8; ++e) {
-                                    ss = fmaf(x[e], x[e], ss);
-                                    qt = fmaf(qf[i][e], x[e], qt);
-                                }
-                            } else {
-#pragma unroll
-                                for (int e = 0; e < 8; ++e) {
-                                    const float xm = ((vi[i].kmask >> e) & 1u) ? x[e] : 0.0f;
-                                    ss = fmaf(xm, xm, ss);
-                                    qt = fmaf(qf[i][e], xm, qt);
+                                for (int k = 0; k < 4; ++k) {
+                                    float2 x = bf2_to_f2(u4_get(xv, k));
+                                    if (!KEYALL && kmask[i] != 0xffu) {
+                                        if (!((kmask[i] >> (2 * k)) & 1u)) x.x = 0.0f;
+                                        if (!((kmask[i] >> (2 * k + 1)) & 1u)) x.y = 0.0f;
+                                    }
+                                    ss2 = ffma2(x, x, ss2);
+                                    qt2 = ffma2(bf2_to_f2(u4_get(qb[i], k)), x, qt2);
                                 }
                             }
                         }
                     }
-                    part[s] = ss;
-                    part[GP + s] = qt;
-                    advance(slot, phase, slots);
+                    part[r] = ss2.x + ss2.y;
+                    part[4 + r] = qt2.x + qt2.y;
+                }
+                warp_reduce_scatter<8>(part, lane);
+                // lane l now holds element l >> 2: rows 0..3 sum-of-squares, then dots
+                if ((lane & 3) == 0) {
+                    const int idx = lane >> 2;
+                    const int r = idx & 3;
+                    if (c0 + r < gs) redw[(idx >> 2) * 32 + c0 + r] = part[0];
                 }
             }
-            warp_reduce_scatter<K2>(part, lane);
-            if ((lane & ((1 << SH) - 1)) == 0)
-                red[(rbuf * ncw + warp) * kReduceStride + (lane >> SH)] = part[0];
             named_bar_sync(1, nct);
             if (warp == 0) {
                 float ss = 0.0f, qt = 0.0f;
                 if (lane < gs) {
                     for (int w = 0; w < ncw; ++w) {
-                        ss += red[(rbuf * ncw + w) * kReduceStride + lane];
-                        qt += red[(rbuf * ncw + w) * kReduceStride + GP + lane];
+                        const float* rw = red + (rbuf * ncw + w) * red_stride;
+                        ss += rw[lane];
+                        qt += rw[32 + lane];
                     }
                 }
                 const float r = rsqrtf(fmaf(ss, inv_r, a.eps));
@@ -221,71 +239,72 @@ __global__ void __launch_bounds__(kMaxThreads, 1) attnres_fwd_kernel(const __gri
             named_bar_sync(1, nct);
             // pass 2: rescale the running sum and add this group's weighted rows
             const float corr = coef[cbuf * 64 + 32];
+            const float2 corr2 = make_float2(corr, corr);
 #pragma unroll
             for (int i = 0; i < VPT; ++i)
 #pragma unroll
-                for (int e = 0; e < 8; ++e) acc[i][e] *= corr;
-            slot = gslot;
-            phase = gphase;
+                for (int k = 0; k < 4; ++k) acc[i][k] = fmul2(acc[i][k], corr2);
+            int sl = gslot;
+#pragma unroll 2
+            for (int s = 0; s < gs; ++s) {
+                const float es = coef[cbuf * 64 + s];
+                const float2 es2 = make_float2(es, es);
+                const unsigned char* row = ring + static_cast<size_t>(sl) * a.slot_bytes;
 #pragma unroll
-            for (int s = 0; s < GP; ++s) {
-                if (s < gs) {
-                    const float es = coef[cbuf * 64 + s];
-                    const unsigned char* row = ring + static_cast<size_t>(slot) * a.slot_bytes;
+                for (int i = 0; i < VPT; ++i) {
+                    if (col[i] >= 0) {
+                        const uint4 xv = ld_shared_v4(row + col[i] * 16);
 #pragma unroll
-                    for (int i = 0; i < VPT; ++i) {
-                        if (vi[i].col >= 0) {
-                            float x[8];
-                            unpack8(ld_shared_v4(row + vi[i].col * 16), x);
-#pragma unroll
-                            for (int e = 0; e < 8; ++e) acc[i][e] = fmaf(es, x[e], acc[i][e]);
-                        }
+                        for (int k = 0; k < 4; ++k) acc[i][k] = ffma2(es2, bf2_to_f2(u4_get(xv, k)), acc[i][k]);
                     }
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(empty + slot);
-                    advance(slot, phase, slots);
                 }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(empty + sl);
+                sl = ring_add(sl, 1, slots);
             }
             cbuf ^= 1;
         }
         const float inv_l = coef[(cbuf ^ 1) * 64 + 33];
+        const float2 inv_l2 = make_float2(inv_l, inv_l);
         float rho = 1.0f;
 #pragma unroll
         for (int i = 0; i < VPT; ++i)
 #pragma unroll
-            for (int e = 0; e < 8; ++e) acc[i][e] *= inv_l;
+            for (int k = 0; k < 4; ++k) acc[i][k] = fmul2(acc[i][k], inv_l2);
         if (a.out_norm) {
-            float ss = 0.0f;
+            float2 ss2 = make_float2(0.0f, 0.0f);
 #pragma unroll
             for (int i = 0; i < VPT; ++i)
-                if (vi[i].col >= 0)
+                if (col[i] >= 0)
 #pragma unroll
-                    for (int e = 0; e < 8; ++e) ss = fmaf(acc[i][e], acc[i][e], ss);
-            ss = warp_sum(ss);
-            if (lane == 0) red[(rbuf * ncw + warp) * kReduceStride] = ss;
+                    for (int k = 0; k < 4; ++k) ss2 = ffma2(acc[i][k], acc[i][k], ss2);
+            const float ss = warp_sum(ss2.x + ss2.y);
+            if (lane == 0) red[(rbuf * ncw + warp) * red_stride] = ss;
             named_bar_sync(1, nct);
             float tot = 0.0f;
-            for (int w = 0; w < ncw; ++w) tot += red[(rbuf * ncw + w) * kReduceStride];
+            for (int w = 0; w < ncw; ++w) tot += red[(rbuf * ncw + w) * red_stride];
             rbuf ^= 1;
             rho = rsqrtf(fmaf(tot, inv_d, a.eps));
             if (threadIdx.x == 0) a.o_rstd[n] = rho;
         }
         uint16_t* yrow = a.y + n * static_cast<long long>(a.D);
         float* prow = a.o_pre ? a.o_pre + n * static_cast<long long>(a.D) : nullptr;
+        const float2 rho2 = make_float2(rho, rho);
 #pragma unroll
         for (int i = 0; i < VPT; ++i) {
-            if (vi[i].col >= 0) {
-                float yv[8];
+            if (col[i] >= 0) {
+                uint32_t yw[4];
 #pragma unroll
-                for (int e = 0; e < 8; ++e) yv[e] = acc[i][e] * rho * wf[i][e];
-                st_global_cs_v4(yrow + 8 * vi[i].col, pack8(yv));
+                for (int k = 0; k < 4; ++k)
+                    yw[k] = pack_f2(fmul2(fmul2(acc[i][k], rho2), bf2_to_f2(u4_get(wb[i], k))));
+                st_global_cs_v4(yrow + 8 * col[i], make_uint4(yw[0], yw[1], yw[2], yw[3]));
                 if (prow) {
-                    const uint4 lo = make_uint4(__float_as_uint(acc[i][0]), __float_as_uint(acc[i][1]),
-                                                __float_as_uint(acc[i][2]), __float_as_uint(acc[i][3]));
-                    const uint4 hi = make_uint4(__float_as_uint(acc[i][4]), __float_as_uint(acc[i][5]),
-                                                __float_as_uint(acc[i][6]), __float_as_uint(acc[i][7]));
-                    st_global_cs_v4(prow + 8 * vi[i].col, lo);
-                    st_global_cs_v4(prow + 8 * vi[i].col + 4, hi);
+                    st_global_cs_v4(prow + 8 * col[i],
+                                    make_uint4(__float_as_uint(acc[i][0].x), __float_as_uint(acc[i][0].y),
+                                               __float_as_uint(acc[i][1].x), __float_as_uint(acc[i][1].y)));
+                    st_global_cs_v4(prow + 8 * col[i] + 4,
+                                    make_uint4(__float_as_uint(acc[i][2].x), __float_as_uint(acc[i][2].y),
+                                               __float_as_uint(acc[i][3].x), __float_as_uint(acc[i][3].y)));
                 }
             }
         }
@@ -301,9 +320,9 @@ __global__ void __launch_bounds__(kMaxThreads, 1) attnres_fwd_kernel(const __gri
     }
 }
 
-template <int VPT, int GP>
+template <int VPT, bool KEYALL>
 cudaError_t launch_fwd_t(const Plan& plan, const FwdArgs& a, cudaStream_t stream) {
-    auto kern = attnres_fwd_kernel<VPT, GP>;
+    auto kern = attnres_fwd_kernel<VPT, KEYALL>;
     cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                            static_cast<int>(plan.smem_fwd));
     if (err != cudaSuccess) return err;
@@ -312,14 +331,9 @@ cudaError_t launch_fwd_t(const Plan& plan, const FwdArgs& a, cudaStream_t stream
 }
 
 template <int VPT>
-cudaError_t dispatch_gp(const Plan& plan, const FwdArgs& a, cudaStream_t stream) {
-    switch (plan.gp_fwd) {
-        case 2: return launch_fwd_t<VPT, 2>(plan, a, stream);
-        case 4: return launch_fwd_t<VPT, 4>(plan, a, stream);
-        case 8: return launch_fwd_t<VPT, 8>(plan, a, stream);
-        case 16: return launch_fwd_t<VPT, 16>(plan, a, stream);
-        default: return cudaErrorInvalidConfiguration;
-    }
+cudaError_t dispatch_key(const Plan& plan, const FwdArgs& a, cudaStream_t stream) {
+    return (a.R == a.D) ? launch_fwd_t<VPT, true>(plan, a, stream)
+                        : launch_fwd_t<VPT, false>(plan, a, stream);
 }
 
 }  // namespace
@@ -333,9 +347,9 @@ unsigned take_fwd_error() {
 
 cudaError_t launch_fwd(const Plan& plan, const FwdArgs& a, cudaStream_t stream) {
     switch (plan.vpt) {
-        case 1: return dispatch_gp<1>(plan, a, stream);
-        case 2: return dispatch_gp<2>(plan, a, stream);
-        case 4: return dispatch_gp<4>(plan, a, stream);
+        case 1: return dispatch_key<1>(plan, a, stream);
+        case 2: return dispatch_key<2>(plan, a, stream);
+        case 4: return dispatch_key<4>(plan, a, stream);
         default: return cudaErrorInvalidConfiguration;
     }
 }

@@ -137,6 +137,26 @@ __device__ __forceinline__ uint4 pack8(const float (&f)[8]) {
     return r;
 }
 
+// bf16 pair (low half = lower address) -> packed FP32 pair.
+__device__ __forceinline__ float2 bf2_to_f2(uint32_t w) {
+    return make_float2(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u));
+}
+
+// Packed FP32 fused multiply-add (one FFMA2 on sm_100 and later).
+__device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c) { return __ffma2_rn(a, b, c); }
+
+__device__ __forceinline__ float2 fmul2(float2 a, float2 b) { return __fmul2_rn(a, b); }
+
+__device__ __forceinline__ uint32_t pack_f2(float2 v) {
+    uint32_t r;
+    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(v.y), "f"(v.x));
+    return r;
+}
+
+__device__ __forceinline__ uint32_t u4_get(const uint4& v, int k) {
+    return k == 0 ? v.x : (k == 1 ? v.y : (k == 2 ? v.z : v.w));
+}
+
 __device__ __forceinline__ float bf16_bits_to_float(uint16_t h) {
     return __uint_as_float(static_cast<uint32_t>(h) << 16);
 }

@@ -15,7 +15,7 @@ constexpr int kMaxThreads = (kMaxConsumerWarps + 1) * 32;  // + one producer war
 constexpr int kMaxSlots = 64;
 constexpr int kTokSlots = 4;      // token-statistics ring depth (backward)
 constexpr int kGroupTicket = 12;  // CTAs per first-level group of the in-kernel reduction
-constexpr int kReduceStride = 32; // floats per warp in the reduction scratch
+constexpr int kMaxGroup = 32;     // forward rows reduced together
 
 // Where a bounded wait gave up (value recorded in g_device_error).
 enum WaitSite : unsigned {
@@ -36,8 +36,7 @@ struct Plan {
     int vpt;
     int slots;
     int slot_bytes;
-    int gp_fwd;       // sources per forward group (power of two)
-    int gp_bwd;       // sources per backward dot-pass group (power of two)
+    int group;        // forward rows resident and reduced together (<= kMaxGroup)
     int resident;     // backward keeps a token's rows between its two passes
     int split;        // backward reduction via the finalize kernel
     int s_pad;        // S rounded up to 4
@@ -51,6 +50,7 @@ struct Plan {
 // Byte offsets inside the dynamic shared memory of one CTA.
 struct SmemLayout {
     uint32_t ring, full, empty, tfull, tempty, red, tok, coef, misc, total;
+    int red_stride;  // floats per warp in the reduction scratch
 };
 
 __host__ __device__ inline uint32_t align_up(uint32_t x, uint32_t a) { return (x + a - 1) / a * a; }
@@ -74,7 +74,8 @@ __host__ __device__ inline SmemLayout make_layout(int slots, int slot_bytes, int
     off += backward ? 8u * kTokSlots : 0u;
     off = align_up(off, 16);
     L.red = off;
-    off += 2u * ncw * kReduceStride * 4u;
+    L.red_stride = s_pad > 64 ? s_pad : 64;
+    off += 2u * ncw * static_cast<uint32_t>(L.red_stride) * 4u;
     L.tok = off;
     off += backward ? static_cast<uint32_t>(kTokSlots) * (3u * s_pad + 4u) * 4u : 0u;
     L.coef = off;
@@ -91,7 +92,7 @@ struct FwdArgs {
     long long src_ld;
     int S, D, R, ko, out_norm;
     float eps, scale;
-    int slots, slot_bytes, ncw, s_pad;
+    int slots, slot_bytes, ncw, s_pad, group;
     const uint16_t* q;
     const uint16_t* w_o;
     uint16_t* y;

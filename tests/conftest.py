@@ -26,3 +26,21 @@ def pytest_collection_modifyitems(config, items):
     for item in items:
         if "gpu" in item.keywords:
             item.add_marker(skip)
+
+
+@pytest.fixture(autouse=True)
+def _device_error_word(request):
+    """Every GPU test starts and ends with a clear kernel wait-failure record."""
+    if "gpu" not in request.keywords:
+        yield
+        return
+    import torch
+    if not torch.cuda.is_available():
+        yield
+        return
+    from attention_residuals_gb300 import _lib
+    lib = _lib.load()
+    lib.attnres_check_device_error()  # clear anything left by an earlier test
+    yield
+    rc = lib.attnres_check_device_error()
+    assert rc == 0, f"a kernel gave up waiting during this test (status {rc})"

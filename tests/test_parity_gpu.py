@@ -121,7 +121,7 @@ def test_reduction_paths_deterministic():
     v, q, w, dy = cuda_copy(wl)
     fwd = attnres_fwd(v, q, w_o=w, key_offset=0)
     outs = []
-    for thr in (1, 1, 10 ** 9, 10 ** 9):
+    for thr in (1, 1, 10 ** 9, 10 ** 9):  # finalize kernel twice, in-kernel reduction twice
         b = attnres_bwd(v, q, dy, fwd, w_o=w, key_offset=0, split_n_threshold=thr)
         outs.append((b["dq_f32"].clone(), b["dw_o_f32"].clone(), b["dvalues"].clone()))
     torch.cuda.synchronize()
