@@ -67,9 +67,9 @@ attnres_status make_plan(const attnres_params* p, Plan* plan) {
     if (!device_info(&dev)) return ATTNRES_ERR_CUDA;
     Plan pl{};
     const int ncv = p->D / 8;
-    pl.vpt = ncv <= 256 ? 1 : (ncv <= 512 ? 2 : 4);
+    pl.vpt = ncv <= 32 * max_warps_for(1) ? 1 : 4;
     pl.ncw = (ncv + 32 * pl.vpt - 1) / (32 * pl.vpt);
-    if (pl.ncw < 1 || pl.ncw > kMaxConsumerWarps) return ATTNRES_ERR_UNSUPPORTED;
+    if (pl.ncw < 1 || pl.ncw > max_warps_for(pl.vpt)) return ATTNRES_ERR_UNSUPPORTED;
     pl.slot_bytes = static_cast<int>(align_up(static_cast<uint32_t>(p->D) * 2u, 128u));
     pl.s_pad = static_cast<int>(align_up(static_cast<uint32_t>(p->S), 4u));
     // Ring depth: as many row slots as the backward layout (the larger) fits.

@@ -59,7 +59,7 @@ __device__ __forceinline__ float ldcg_f32(const float* p) { return __ldcg(p); }
 
 // KEYALL: every channel is a key channel (R == D), so no per-vector masks.
 template <int VPT, bool KEYALL>
-__global__ void __launch_bounds__(kMaxThreads, 1) attnres_bwd_kernel(const __grid_constant__ BwdArgs a) {
+__global__ void __launch_bounds__(max_threads_for(VPT), 1) attnres_bwd_kernel(const __grid_constant__ BwdArgs a) {
     extern __shared__ __align__(128) unsigned char smem[];
     const int ncw = a.ncw;
     const int nct = ncw * 32;
@@ -73,10 +73,6 @@ __global__ void __launch_bounds__(kMaxThreads, 1) attnres_bwd_kernel(const __gri
     uint64_t* tempty = reinterpret_cast<uint64_t*>(smem + L.tempty);
     float* red = reinterpret_cast<float*>(smem + L.red);  // [2][ncw][red_stride]
     float* tok = reinterpret_cast<float*>(smem + L.tok);  // [kTokSlots][3*s_pad + 4]
-    float* cA = reinterpret_cast<float*>(smem + L.coef);  // alpha_s
-    float* c1 = cA + s_pad;                               // rstd_s dz_s
-    float* c2 = c1 + s_pad;                               // -rstd_s^2 dz_s z_s / R
-    float* da_all = c2 + s_pad;
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L.misc);
     volatile int* ticket_flag = abort_flag + 1;
     const int tstride = 3 * s_pad + 4;
@@ -95,7 +91,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1) attnres_bwd_kernel(const __gri
         }
         for (int k = 0; k < kTokSlots; ++k) {
             mbar_init(tfull + k, 32);
-            mbar_init(tempty + k, 1);
+            mbar_init(tempty + k, ncw);
         }
         *abort_flag = 0;
         *ticket_flag = 0;
@@ -392,34 +388,45 @@ __global__ void __launch_bounds__(kMaxThreads, 1) attnres_bwd_kernel(const __gri
         }
         named_bar_sync(1, nct);
 
-        // ---- per-source coefficients (warp 0)
-        if (warp == 0) {
+        // ---- per-source coefficients, computed by every warp (identically)
+        // and kept in registers: lane l holds sources l, l+32, l+64, l+96.
+        float cal[4], ck1[4], ck2[4];
+        {
+            float dav[4];
             float part_delta = 0.0f;
-            for (int s = lane; s < S; s += 32) {
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const int s = lane + 32 * j;
                 float d = 0.0f;
-                for (int w = 0; w < ncw; ++w) d += red[(rbuf * ncw + w) * red_stride + s];
-                da_all[s] = d;
-                part_delta = fmaf(tk[s], d, part_delta);
+                if (s < S) {
+                    for (int w = 0; w < ncw; ++w) d += red[(rbuf * ncw + w) * red_stride + s];
+                    part_delta = fmaf(tk[s], d, part_delta);
+                }
+                dav[j] = d;
             }
             const float delta = warp_sum(part_delta);
-            for (int s = lane; s < S; s += 32) {
-                const float al = tk[s];
-                const float r = tk[s_pad + s];
-                const float z = tk[2 * s_pad + s];
-                const float dz = al * (da_all[s] - delta);
-                cA[s] = al;
-                c1[s] = r * dz;  // qs carries `scale`, so c1 * qs = rstd * scale * dz * q
-                c2[s] = -(r * r) * dz * z * inv_r;
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const int s = lane + 32 * j;
+                cal[j] = ck1[j] = ck2[j] = 0.0f;
+                if (s < S) {
+                    const float al = tk[s];
+                    const float r = tk[s_pad + s];
+                    const float z = tk[2 * s_pad + s];
+                    const float dz = al * (dav[j] - delta);
+                    cal[j] = al;
+                    ck1[j] = r * dz;  // qs carries `scale`, so ck1 * qs = rstd * scale * dz * q
+                    ck2[j] = -(r * r) * dz * z * inv_r;
+                }
             }
             __syncwarp();
-            if (lane == 0) mbar_arrive(tempty + ts);
+            if (lane == 0) mbar_arrive(tempty + ts);  // this warp is done with tok[ts]
         }
         rbuf ^= 1;
         if (++ts == kTokSlots) {
             ts = 0;
             tphase ^= 1u;
         }
-        named_bar_sync(1, nct);
 
         // ---- write pass: dv_s rows and dq contributions
         if (a.resident) {
@@ -430,9 +437,10 @@ __global__ void __launch_bounds__(kMaxThreads, 1) attnres_bwd_kernel(const __gri
         for (int s = 0; s < S; ++s) {
             if (!a.resident) mbar_wait(full + slot, phase, abort_flag, &g_bwd_error, kSiteBwdConsumer);
             const unsigned char* row = ring + static_cast<size_t>(slot) * a.slot_bytes;
-            const float al = cA[s];
-            const float k1 = c1[s];
-            const float k2 = c2[s];
+            const int j = s >> 5;
+            const float al = __shfl_sync(0xffffffffu, j == 0 ? cal[0] : j == 1 ? cal[1] : j == 2 ? cal[2] : cal[3], s & 31);
+            const float k1 = __shfl_sync(0xffffffffu, j == 0 ? ck1[0] : j == 1 ? ck1[1] : j == 2 ? ck1[2] : ck1[3], s & 31);
+            const float k2 = __shfl_sync(0xffffffffu, j == 0 ? ck2[0] : j == 1 ? ck2[1] : j == 2 ? ck2[2] : ck2[3], s & 31);
             const float2 al2 = make_float2(al, al), k12 = make_float2(k1, k1), k22 = make_float2(k2, k2);
             uint16_t* drow = static_cast<uint16_t*>(a.dsrc[s]) + n * a.dsrc_ld;
 #pragma unroll
@@ -587,7 +595,6 @@ unsigned take_bwd_error() {
 cudaError_t launch_bwd(const Plan& plan, const BwdArgs& a, cudaStream_t stream) {
     switch (plan.vpt) {
         case 1: return dispatch_key<1>(plan, a, stream);
-        case 2: return dispatch_key<2>(plan, a, stream);
         case 4: return dispatch_key<4>(plan, a, stream);
         default: return cudaErrorInvalidConfiguration;
     }

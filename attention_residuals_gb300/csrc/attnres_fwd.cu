@@ -16,8 +16,9 @@
 // for the whole group, then pass 1 accumulates the key sum of squares and
 // the query dot four rows at a time (packed FP32 FMAs, independent chains),
 // each four-row chunk ends with a warp reduce-scatter, one cross-warp step
-// gives the group's logits, warp 0 updates the running softmax maximum and
-// denominator, and pass 2 adds the weighted rows into FP32 registers and
+// gives the group's logits, every warp updates the running softmax maximum
+// and denominator itself (redundantly, so one CTA barrier per group
+// suffices), and pass 2 adds the weighted rows into FP32 registers and
 // releases the slots.  The output norm needs one more CTA reduction per
 // token.  The pre-norm mixture o is written (FP32) only when asked for.
 // This is a bandwidth-bound per-token reduction: no tensor cores.
@@ -47,7 +48,7 @@ __device__ __forceinline__ int ring_add(int slot, int k, int slots) {
 
 // KEYALL: every channel is a key channel (R == D), so no per-vector masks.
 template <int VPT, bool KEYALL>
-__global__ void __launch_bounds__(kMaxThreads, 1) attnres_fwd_kernel(const __grid_constant__ FwdArgs a) {
+__global__ void __launch_bounds__(max_threads_for(VPT), 1) attnres_fwd_kernel(const __grid_constant__ FwdArgs a) {
     extern __shared__ __align__(128) unsigned char smem[];
     const int ncw = a.ncw;
     const int nct = ncw * 32;
@@ -59,7 +60,6 @@ __global__ void __launch_bounds__(kMaxThreads, 1) attnres_fwd_kernel(const __gri
     float* red = reinterpret_cast<float*>(smem + L.red);     // [2][ncw][red_stride]
     float* zall = reinterpret_cast<float*>(smem + L.coef);  // [s_pad]
     float* rall = zall + a.s_pad;                           // [s_pad]
-    float* coef = rall + a.s_pad;  // [2][64]: e_s (s < 32), corr at 32, 1/l at 33
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L.misc);
     const int red_stride = L.red_stride;
 
@@ -157,9 +157,8 @@ __global__ void __launch_bounds__(kMaxThreads, 1) attnres_fwd_kernel(const __gri
         for (int i = 0; i < VPT; ++i)
 #pragma unroll
             for (int k = 0; k < 4; ++k) acc[i][k] = make_float2(0.0f, 0.0f);
-        float m_run = -FLT_MAX;  // meaningful in warp 0
-        float l_run = 0.0f;
-        int cbuf = 0;
+        float m_run = -FLT_MAX;  // running softmax maximum (same in every warp)
+        float l_run = 0.0f;      // running softmax denominator
 
         for (int g0 = 0; g0 < S; g0 += G) {
             const int gs = min(G, S - g0);
@@ -208,7 +207,12 @@ __global__ void __launch_bounds__(kMaxThreads, 1) attnres_fwd_kernel(const __gri
                 }
             }
             named_bar_sync(1, nct);
-            if (warp == 0) {
+            // Every warp derives the group's logits and softmax update itself
+            // (identical inputs and operations, so identical results), which
+            // saves a second CTA barrier per group.  Lane l holds row g0 + l.
+            float e;
+            float corr;
+            {
                 float ss = 0.0f, qt = 0.0f;
                 if (lane < gs) {
                     for (int w = 0; w < ncw; ++w) {
@@ -220,25 +224,18 @@ __global__ void __launch_bounds__(kMaxThreads, 1) attnres_fwd_kernel(const __gri
                 const float r = rsqrtf(fmaf(ss, inv_r, a.eps));
                 const float z = a.scale * r * qt;
                 const float m_new = fmaxf(m_run, warp_max(lane < gs ? z : -FLT_MAX));
-                const float e = lane < gs ? __expf(z - m_new) : 0.0f;
+                e = lane < gs ? __expf(z - m_new) : 0.0f;
                 const float esum = warp_sum(e);
-                const float corr = __expf(m_run - m_new);
+                corr = __expf(m_run - m_new);
                 l_run = fmaf(l_run, corr, esum);
                 m_run = m_new;
-                if (lane < gs) {
-                    coef[cbuf * 64 + lane] = e;
+                if (warp == 0 && lane < gs) {
                     zall[g0 + lane] = z;
                     rall[g0 + lane] = r;
                 }
-                if (lane == 0) {
-                    coef[cbuf * 64 + 32] = corr;
-                    coef[cbuf * 64 + 33] = 1.0f / l_run;
-                }
             }
             rbuf ^= 1;
-            named_bar_sync(1, nct);
             // pass 2: rescale the running sum and add this group's weighted rows
-            const float corr = coef[cbuf * 64 + 32];
             const float2 corr2 = make_float2(corr, corr);
 #pragma unroll
             for (int i = 0; i < VPT; ++i)
@@ -247,7 +244,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1) attnres_fwd_kernel(const __gri
             int sl = gslot;
 #pragma unroll 2
             for (int s = 0; s < gs; ++s) {
-                const float es = coef[cbuf * 64 + s];
+                const float es = __shfl_sync(0xffffffffu, e, s);
                 const float2 es2 = make_float2(es, es);
                 const unsigned char* row = ring + static_cast<size_t>(sl) * a.slot_bytes;
 #pragma unroll
@@ -262,9 +259,8 @@ __global__ void __launch_bounds__(kMaxThreads, 1) attnres_fwd_kernel(const __gri
                 if (lane == 0) mbar_arrive(empty + sl);
                 sl = ring_add(sl, 1, slots);
             }
-            cbuf ^= 1;
         }
-        const float inv_l = coef[(cbuf ^ 1) * 64 + 33];
+        const float inv_l = 1.0f / l_run;
         const float2 inv_l2 = make_float2(inv_l, inv_l);
         float rho = 1.0f;
 #pragma unroll
@@ -309,10 +305,10 @@ __global__ void __launch_bounds__(kMaxThreads, 1) attnres_fwd_kernel(const __gri
             }
         }
         if (warp == 0) {
-            const float inv_lw = 1.0f / l_run;
+            __syncwarp();
             for (int s = lane; s < S; s += 32) {
                 const float z = zall[s];
-                a.alpha[n * S + s] = __expf(z - m_run) * inv_lw;
+                a.alpha[n * S + s] = __expf(z - m_run) * inv_l;
                 a.rstd[n * S + s] = rall[s];
                 a.logit[n * S + s] = z;
             }
@@ -348,7 +344,6 @@ unsigned take_fwd_error() {
 cudaError_t launch_fwd(const Plan& plan, const FwdArgs& a, cudaStream_t stream) {
     switch (plan.vpt) {
         case 1: return dispatch_key<1>(plan, a, stream);
-        case 2: return dispatch_key<2>(plan, a, stream);
         case 4: return dispatch_key<4>(plan, a, stream);
         default: return cudaErrorInvalidConfiguration;
     }

@@ -46,6 +46,20 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
     return ok != 0;
 }
 
+// As mbar_try_wait, but lets the thread sleep for up to `hint_ns` while the
+// phase is incomplete (it wakes as soon as the phase completes).
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t* bar, uint32_t parity, uint32_t hint_ns) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity), "r"(hint_ns)
+        : "memory");
+    return ok != 0;
+}
+
 __device__ __forceinline__ uint64_t global_timer_ns() {
     uint64_t t;
     asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
@@ -62,8 +76,8 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volati
     if (*abort) return false;
     const uint64_t t0 = global_timer_ns();
     uint32_t spins = 0;
-    while (!mbar_try_wait(bar, parity)) {
-        if (((++spins) & 255u) == 0u) {
+    while (!mbar_try_wait_sleep(bar, parity, 20000u)) {
+        if (((++spins) & 15u) == 0u) {
             if (*abort) return false;
             if (global_timer_ns() - t0 > 2000000000ull) {
                 atomicCAS(err, 0u, where);

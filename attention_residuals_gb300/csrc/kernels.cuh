@@ -10,8 +10,12 @@
 
 namespace attnres {
 
-constexpr int kMaxConsumerWarps = 8;
-constexpr int kMaxThreads = (kMaxConsumerWarps + 1) * 32;  // + one producer warp
+constexpr int kMaxConsumerWarps = 16;
+// Threads per CTA (consumers + one producer warp).  One 16-byte vector per
+// thread allows 16 consumer warps (registers <= 96); wider per-thread
+// footprints keep 8 consumer warps (registers <= 168).
+__host__ __device__ constexpr int max_threads_for(int vpt) { return vpt == 1 ? 17 * 32 : 9 * 32; }
+__host__ __device__ constexpr int max_warps_for(int vpt) { return vpt == 1 ? 16 : 8; }
 constexpr int kMaxSlots = 64;
 constexpr int kTokSlots = 4;      // token-statistics ring depth (backward)
 constexpr int kGroupTicket = 12;  // CTAs per first-level group of the in-kernel reduction
@@ -55,8 +59,8 @@ struct SmemLayout {
 
 __host__ __device__ inline uint32_t align_up(uint32_t x, uint32_t a) { return (x + a - 1) / a * a; }
 
-// coef holds per-token vectors: forward z[s_pad], rstd[s_pad], group
-// coefficients 2 x 64; backward alpha[s_pad], c1[s_pad], c2[s_pad], da[s_pad].
+// coef holds per-token vectors: forward z[s_pad], rstd[s_pad]; backward
+// nothing (its per-source coefficients live in registers).
 __host__ __device__ inline SmemLayout make_layout(int slots, int slot_bytes, int ncw, int s_pad,
                                                   bool backward) {
     SmemLayout L;
@@ -79,7 +83,7 @@ __host__ __device__ inline SmemLayout make_layout(int slots, int slot_bytes, int
     L.tok = off;
     off += backward ? static_cast<uint32_t>(kTokSlots) * (3u * s_pad + 4u) * 4u : 0u;
     L.coef = off;
-    off += backward ? 4u * s_pad * 4u : (2u * s_pad + 2u * 64u) * 4u;
+    off += backward ? 0u : 2u * s_pad * 4u;
     L.misc = off;  // abort flag, ticket flags
     off += 16u;
     L.total = align_up(off, 128);
