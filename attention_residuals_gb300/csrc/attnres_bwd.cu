@@ -71,12 +71,11 @@ __global__ void __launch_bounds__(max_threads_for(VPT), 1) attnres_bwd_kernel(co
     uint64_t* empty = reinterpret_cast<uint64_t*>(smem + L.empty);
     uint64_t* tfull = reinterpret_cast<uint64_t*>(smem + L.tfull);
     uint64_t* tempty = reinterpret_cast<uint64_t*>(smem + L.tempty);
-    float* red = reinterpret_cast<float*>(smem + L.red);  // [2][ncw][red_stride]
+    float* red = reinterpret_cast<float*>(smem + L.red);  // [2][red_rows][kRedPitch]
     float* tok = reinterpret_cast<float*>(smem + L.tok);  // [kTokSlots][3*s_pad + 4]
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L.misc);
     volatile int* ticket_flag = abort_flag + 1;
     const int tstride = 3 * s_pad + 4;
-    const int red_stride = L.red_stride;
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -212,27 +211,57 @@ __global__ void __launch_bounds__(max_threads_for(VPT), 1) attnres_bwd_kernel(co
     const float inv_r = 1.0f / static_cast<float>(a.R);
     const float inv_d = 1.0f / static_cast<float>(D);
 
-    int slot = 0;
-    uint32_t phase = 0;
+    // 32-bit shared addresses; the cursor's row address already includes
+    // this thread's first vector offset.
+    const uint32_t sbase = smem_u32(smem);
+    const uint32_t voff = static_cast<uint32_t>(col[0] < 0 ? 0 : col[0]) * 16u;
+    const uint32_t vstep = static_cast<uint32_t>(nct) * 16u;
+    const uint32_t sb = static_cast<uint32_t>(a.slot_bytes);
+    const uint32_t ring_lo = sbase + L.ring + voff;
+    const uint32_t ring_span = static_cast<uint32_t>(slots) * sb;
+    const uint32_t full_s = sbase + L.full;
+    const uint32_t empty_s = sbase + L.empty;
+    const uint32_t tfull_s = sbase + L.tfull;
+    const uint32_t tempty_s = sbase + L.tempty;
+    const uint32_t red_s = sbase + L.red;
+    const int red_rows = L.red_rows;
+    const int nq = (ncw + 3) >> 2;
+    // this thread's byte offset inside a dvalues row, and the row pitch
+    const long long dld_b = a.dsrc_ld * 2;
+    const long long d_off = static_cast<long long>(col[0] < 0 ? 0 : col[0]) * 16;
+
+    for (int k = threadIdx.x; k < 2 * red_rows * kRedPitch; k += nct) red[k] = 0.0f;
+    named_bar_sync(1, nct);
+
+    auto red_sum = [&](int buf, int row) -> float {
+        const uint32_t base = red_s + static_cast<uint32_t>(((buf * red_rows + row) * kRedPitch) * 4);
+        float t = 0.0f;
+        for (int q4 = 0; q4 < nq; ++q4) {
+            const float4 v = lds128f(base + 16u * q4);
+            t += (v.x + v.y) + (v.z + v.w);
+        }
+        return t;
+    };
+
+    RingCursor cur{ring_lo, 0, 0u};
     int ts = 0;
     uint32_t tphase = 0;
     int rbuf = 0;
 
     for (long long n = blockIdx.x; n < N; n += gridDim.x) {
-        mbar_wait(tfull + ts, tphase, abort_flag, &g_bwd_error, kSiteBwdTokStat);
+        mbar_wait_s(tfull_s + 8u * ts, tphase, abort_flag, &g_bwd_error, kSiteBwdTokStat);
         const float* tk = tok + ts * tstride;
 
         // ---- dy into registers; its slot is free again at once
         uint4 dyv[VPT];
         {
-            mbar_wait(full + slot, phase, abort_flag, &g_bwd_error, kSiteBwdConsumer);
-            const unsigned char* dy_row = ring + static_cast<size_t>(slot) * a.slot_bytes;
+            mbar_wait_s(full_s + 8u * cur.slot, cur.phase, abort_flag, &g_bwd_error, kSiteBwdConsumer);
 #pragma unroll
             for (int i = 0; i < VPT; ++i)
-                dyv[i] = col[i] >= 0 ? ld_shared_v4(dy_row + col[i] * 16) : make_uint4(0u, 0u, 0u, 0u);
+                dyv[i] = col[i] >= 0 ? lds128(cur.row + i * vstep) : make_uint4(0u, 0u, 0u, 0u);
             __syncwarp();
-            if (lane == 0) mbar_arrive(empty + slot);
-            advance(slot, phase, slots);
+            if (lane == 0) mbar_arrive_s(empty_s + 8u * cur.slot);
+            cur.next(sb, slots, ring_lo);
         }
 
         // ---- gradient wrt the mixture o (kept in registers)
@@ -263,41 +292,35 @@ __global__ void __launch_bounds__(max_threads_for(VPT), 1) attnres_bwd_kernel(co
                 for (int i = 0; i < VPT; ++i)
 #pragma unroll
                     for (int k = 0; k < 4; ++k) o[i][k] = make_float2(0.0f, 0.0f);
-                int aslot = slot;
-                uint32_t aphase = phase;
+                RingCursor ac = cur;
                 if (a.resident) {
                     for (int s = 0; s < S; ++s) {
-                        mbar_wait(full + aslot, aphase, abort_flag, &g_bwd_error, kSiteBwdConsumer);
-                        advance(aslot, aphase, slots);
+                        mbar_wait_s(full_s + 8u * ac.slot, ac.phase, abort_flag, &g_bwd_error, kSiteBwdConsumer);
+                        ac.next(sb, slots, ring_lo);
                     }
-                    aslot = slot;
+                    ac = cur;
                 }
 #pragma unroll 2
                 for (int s = 0; s < S; ++s) {
-                    if (!a.resident) mbar_wait(full + aslot, aphase, abort_flag, &g_bwd_error, kSiteBwdConsumer);
-                    const unsigned char* row = ring + static_cast<size_t>(aslot) * a.slot_bytes;
+                    if (!a.resident)
+                        mbar_wait_s(full_s + 8u * ac.slot, ac.phase, abort_flag, &g_bwd_error, kSiteBwdConsumer);
                     const float al = tk[s];
                     const float2 al2 = make_float2(al, al);
 #pragma unroll
                     for (int i = 0; i < VPT; ++i) {
                         if (col[i] >= 0) {
-                            const uint4 xv = ld_shared_v4(row + col[i] * 16);
+                            const uint4 xv = lds128(ac.row + i * vstep);
 #pragma unroll
                             for (int k = 0; k < 4; ++k) o[i][k] = ffma2(al2, bf2_to_f2(u4_get(xv, k)), o[i][k]);
                         }
                     }
                     if (!a.resident) {
                         __syncwarp();
-                        if (lane == 0) mbar_arrive(empty + aslot);
-                        advance(aslot, aphase, slots);
-                    } else {
-                        aslot = ring_add(aslot, 1, slots);
+                        if (lane == 0) mbar_arrive_s(empty_s + 8u * ac.slot);
                     }
+                    ac.next(sb, slots, ring_lo);
                 }
-                if (!a.resident) {  // the streamed o-pass rows are consumed
-                    slot = aslot;
-                    phase = aphase;
-                }
+                if (!a.resident) cur = ac;  // the streamed o-pass rows are consumed
             }
             const float rho = tk[3 * s_pad];
             const float2 rho2 = make_float2(rho, rho);
@@ -316,10 +339,9 @@ __global__ void __launch_bounds__(max_threads_for(VPT), 1) attnres_bwd_kernel(co
                 }
             }
             const float gy = warp_sum(gy2.x + gy2.y);
-            if (lane == 0) red[(rbuf * ncw + warp) * red_stride] = gy;
+            if (lane == 0) red[(rbuf * red_rows) * kRedPitch + warp] = gy;
             named_bar_sync(1, nct);
-            float tot = 0.0f;
-            for (int w = 0; w < ncw; ++w) tot += red[(rbuf * ncw + w) * red_stride];
+            const float tot = red_sum(rbuf, 0);
             rbuf ^= 1;
             const float ncg = -tot * inv_d;
             const float2 ncg2 = make_float2(ncg, ncg);
@@ -335,57 +357,54 @@ __global__ void __launch_bounds__(max_threads_for(VPT), 1) attnres_bwd_kernel(co
         }
 
         // ---- dot pass: da_s = <do, v_s>, four rows at a time
-        const int v_slot0 = slot;
-        const uint32_t v_phase0 = phase;
+        const RingCursor vcur = cur;
         if (a.resident) {
-            int ws = slot;
-            uint32_t wp = phase;
+            RingCursor wc = cur;
             for (int s = 0; s < S; ++s) {  // completed phases return at once
-                mbar_wait(full + ws, wp, abort_flag, &g_bwd_error, kSiteBwdConsumer);
-                advance(ws, wp, slots);
+                mbar_wait_s(full_s + 8u * wc.slot, wc.phase, abort_flag, &g_bwd_error, kSiteBwdConsumer);
+                wc.next(sb, slots, ring_lo);
             }
         }
-        float* redw = red + (rbuf * ncw + warp) * red_stride;
+        RingCursor dc = cur;
         for (int c0 = 0; c0 < S; c0 += 4) {
             const int cn = min(4, S - c0);
             if (!a.resident) {
-                int ws = slot;
-                uint32_t wp = phase;
+                RingCursor wc = dc;
                 for (int r = 0; r < cn; ++r) {
-                    mbar_wait(full + ws, wp, abort_flag, &g_bwd_error, kSiteBwdConsumer);
-                    advance(ws, wp, slots);
+                    mbar_wait_s(full_s + 8u * wc.slot, wc.phase, abort_flag, &g_bwd_error, kSiteBwdConsumer);
+                    wc.next(sb, slots, ring_lo);
                 }
             }
             float part[4];
+            uint32_t rowa = dc.row;
 #pragma unroll
             for (int r = 0; r < 4; ++r) {
                 float2 d2 = make_float2(0.0f, 0.0f);
                 if (r < cn) {
-                    const unsigned char* row =
-                        ring + static_cast<size_t>(ring_add(a.resident ? v_slot0 : slot, (a.resident ? c0 : 0) + r, slots)) *
-                                   a.slot_bytes;
 #pragma unroll
                     for (int i = 0; i < VPT; ++i) {
                         if (col[i] >= 0) {
-                            const uint4 xv = ld_shared_v4(row + col[i] * 16);
+                            const uint4 xv = lds128(rowa + i * vstep);
 #pragma unroll
                             for (int k = 0; k < 4; ++k) d2 = ffma2(dout[i][k], bf2_to_f2(u4_get(xv, k)), d2);
                         }
                     }
+                    rowa += sb;
+                    if (rowa >= ring_lo + ring_span) rowa -= ring_span;
                 }
                 part[r] = d2.x + d2.y;
             }
-            if (!a.resident) {
-                __syncwarp();
-                for (int r = 0; r < cn; ++r) {
-                    if (lane == 0) mbar_arrive(empty + slot);
-                    advance(slot, phase, slots);
-                }
+            __syncwarp();
+            for (int r = 0; r < cn; ++r) {
+                if (!a.resident && lane == 0) mbar_arrive_s(empty_s + 8u * dc.slot);
+                dc.next(sb, slots, ring_lo);
             }
             warp_reduce_scatter<4>(part, lane);
             // lane l holds element l >> 3
-            if ((lane & 7) == 0 && c0 + (lane >> 3) < S) redw[c0 + (lane >> 3)] = part[0];
+            if ((lane & 7) == 0 && c0 + (lane >> 3) < S)
+                red[(rbuf * red_rows + c0 + (lane >> 3)) * kRedPitch + warp] = part[0];
         }
+        if (!a.resident) cur = dc;
         named_bar_sync(1, nct);
 
         // ---- per-source coefficients, computed by every warp (identically)
@@ -399,7 +418,7 @@ __global__ void __launch_bounds__(max_threads_for(VPT), 1) attnres_bwd_kernel(co
                 const int s = lane + 32 * j;
                 float d = 0.0f;
                 if (s < S) {
-                    for (int w = 0; w < ncw; ++w) d += red[(rbuf * ncw + w) * red_stride + s];
+                    d = red_sum(rbuf, s);
                     part_delta = fmaf(tk[s], d, part_delta);
                 }
                 dav[j] = d;
@@ -420,7 +439,7 @@ __global__ void __launch_bounds__(max_threads_for(VPT), 1) attnres_bwd_kernel(co
                 }
             }
             __syncwarp();
-            if (lane == 0) mbar_arrive(tempty + ts);  // this warp is done with tok[ts]
+            if (lane == 0) mbar_arrive_s(tempty_s + 8u * ts);  // this warp is done with tok[ts]
         }
         rbuf ^= 1;
         if (++ts == kTokSlots) {
@@ -429,20 +448,26 @@ __global__ void __launch_bounds__(max_threads_for(VPT), 1) attnres_bwd_kernel(co
         }
 
         // ---- write pass: dv_s rows and dq contributions
-        if (a.resident) {
-            slot = v_slot0;
-            phase = v_phase0;
-        }
+        RingCursor wcur = a.resident ? vcur : cur;
+        char* dbase_n = nullptr;
+        const long long row_off = n * dld_b + d_off;
 #pragma unroll 2
         for (int s = 0; s < S; ++s) {
-            if (!a.resident) mbar_wait(full + slot, phase, abort_flag, &g_bwd_error, kSiteBwdConsumer);
-            const unsigned char* row = ring + static_cast<size_t>(slot) * a.slot_bytes;
-            const int j = s >> 5;
-            const float al = __shfl_sync(0xffffffffu, j == 0 ? cal[0] : j == 1 ? cal[1] : j == 2 ? cal[2] : cal[3], s & 31);
-            const float k1 = __shfl_sync(0xffffffffu, j == 0 ? ck1[0] : j == 1 ? ck1[1] : j == 2 ? ck1[2] : ck1[3], s & 31);
-            const float k2 = __shfl_sync(0xffffffffu, j == 0 ? ck2[0] : j == 1 ? ck2[1] : j == 2 ? ck2[2] : ck2[3], s & 31);
+            if (!a.resident)
+                mbar_wait_s(full_s + 8u * wcur.slot, wcur.phase, abort_flag, &g_bwd_error, kSiteBwdConsumer);
+            float al, k1, k2;
+            if (S <= 32) {
+                al = __shfl_sync(0xffffffffu, cal[0], s);
+                k1 = __shfl_sync(0xffffffffu, ck1[0], s);
+                k2 = __shfl_sync(0xffffffffu, ck2[0], s);
+            } else {
+                const int j = s >> 5;
+                al = __shfl_sync(0xffffffffu, j == 0 ? cal[0] : j == 1 ? cal[1] : j == 2 ? cal[2] : cal[3], s & 31);
+                k1 = __shfl_sync(0xffffffffu, j == 0 ? ck1[0] : j == 1 ? ck1[1] : j == 2 ? ck1[2] : ck1[3], s & 31);
+                k2 = __shfl_sync(0xffffffffu, j == 0 ? ck2[0] : j == 1 ? ck2[1] : j == 2 ? ck2[2] : ck2[3], s & 31);
+            }
             const float2 al2 = make_float2(al, al), k12 = make_float2(k1, k1), k22 = make_float2(k2, k2);
-            uint16_t* drow = static_cast<uint16_t*>(a.dsrc[s]) + n * a.dsrc_ld;
+            dbase_n = static_cast<char*>(a.dsrc[s]) + row_off;
 #pragma unroll
             for (int i = 0; i < VPT; ++i) {
                 if (col[i] >= 0) {
@@ -450,7 +475,7 @@ __global__ void __launch_bounds__(max_threads_for(VPT), 1) attnres_bwd_kernel(co
 #pragma unroll
                     for (int k = 0; k < 4; ++k) dv[k] = fmul2(al2, dout[i][k]);
                     if (KEYALL || kmask[i] != 0u) {
-                        const uint4 xv = ld_shared_v4(row + col[i] * 16);
+                        const uint4 xv = lds128(wcur.row + i * vstep);
 #pragma unroll
                         for (int k = 0; k < 4; ++k) {
                             float2 x = bf2_to_f2(u4_get(xv, k));
@@ -462,14 +487,15 @@ __global__ void __launch_bounds__(max_threads_for(VPT), 1) attnres_bwd_kernel(co
                             dq_acc[i][k] = ffma2(k12, x, dq_acc[i][k]);
                         }
                     }
-                    st_global_cs_v4(drow + 8 * col[i],
+                    st_global_cs_v4(dbase_n + static_cast<long long>(i) * vstep,
                                     make_uint4(pack_f2(dv[0]), pack_f2(dv[1]), pack_f2(dv[2]), pack_f2(dv[3])));
                 }
             }
             __syncwarp();
-            if (lane == 0) mbar_arrive(empty + slot);
-            advance(slot, phase, slots);
+            if (lane == 0) mbar_arrive_s(empty_s + 8u * wcur.slot);
+            wcur.next(sb, slots, ring_lo);
         }
+        cur = wcur;
     }
 
     // ---------------------------------------------- per-CTA partial sums

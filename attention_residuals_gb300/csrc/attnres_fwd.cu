@@ -57,11 +57,10 @@ __global__ void __launch_bounds__(max_threads_for(VPT), 1) attnres_fwd_kernel(co
     unsigned char* ring = smem + L.ring;
     uint64_t* full = reinterpret_cast<uint64_t*>(smem + L.full);
     uint64_t* empty = reinterpret_cast<uint64_t*>(smem + L.empty);
-    float* red = reinterpret_cast<float*>(smem + L.red);     // [2][ncw][red_stride]
+    float* red = reinterpret_cast<float*>(smem + L.red);     // [2][red_rows][kRedPitch]
     float* zall = reinterpret_cast<float*>(smem + L.coef);  // [s_pad]
     float* rall = zall + a.s_pad;                           // [s_pad]
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L.misc);
-    const int red_stride = L.red_stride;
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -147,8 +146,38 @@ __global__ void __launch_bounds__(max_threads_for(VPT), 1) attnres_fwd_kernel(co
     const float inv_d = 1.0f / static_cast<float>(a.D);
     const int G = a.group;  // rows per group (<= 32, <= slots)
 
-    int slot = 0;
-    uint32_t phase = 0;
+    // 32-bit shared addresses; the cursor's row address already includes
+    // this thread's first vector offset.
+    const uint32_t sbase = smem_u32(smem);
+    const uint32_t voff = static_cast<uint32_t>(col[0] < 0 ? 0 : col[0]) * 16u;
+    const uint32_t vstep = static_cast<uint32_t>(nct) * 16u;  // between a thread's vectors
+    const uint32_t sb = static_cast<uint32_t>(a.slot_bytes);
+    const uint32_t ring_lo = sbase + L.ring + voff;
+    const uint32_t ring_span = static_cast<uint32_t>(slots) * sb;
+    const uint32_t full_s = sbase + L.full;
+    const uint32_t empty_s = sbase + L.empty;
+    const uint32_t red_s = sbase + L.red;
+    const int red_rows = L.red_rows;
+    const int nq = (ncw + 3) >> 2;  // 16-byte loads per reduction row
+
+    // warp partials never written stay zero in the reduction scratch
+    for (int k = threadIdx.x; k < 2 * red_rows * kRedPitch; k += nct) red[k] = 0.0f;
+    named_bar_sync(1, nct);
+
+    auto red_addr = [&](int buf, int row, int w) -> uint32_t {
+        return red_s + static_cast<uint32_t>(((buf * red_rows + row) * kRedPitch + w) * 4);
+    };
+    auto red_sum = [&](int buf, int row) -> float {
+        const uint32_t base = red_addr(buf, row, 0);
+        float t = 0.0f;
+        for (int q4 = 0; q4 < nq; ++q4) {
+            const float4 v = lds128f(base + 16u * q4);
+            t += (v.x + v.y) + (v.z + v.w);
+        }
+        return t;
+    };
+
+    RingCursor cur{ring_lo, 0, 0u};
     int rbuf = 0;
 
     for (long long n = blockIdx.x; n < N; n += gridDim.x) {
@@ -162,26 +191,24 @@ __global__ void __launch_bounds__(max_threads_for(VPT), 1) attnres_fwd_kernel(co
 
         for (int g0 = 0; g0 < S; g0 += G) {
             const int gs = min(G, S - g0);
-            const int gslot = slot;
+            const RingCursor gcur = cur;
             // wait for the whole group, then compute without interruptions
             for (int s = 0; s < gs; ++s) {
-                mbar_wait(full + slot, phase, abort_flag, &g_fwd_error, kSiteFwdConsumer);
-                advance(slot, phase, slots);
+                mbar_wait_s(full_s + 8u * cur.slot, cur.phase, abort_flag, &g_fwd_error, kSiteFwdConsumer);
+                cur.next(sb, slots, ring_lo);
             }
-            float* redw = red + (rbuf * ncw + warp) * red_stride;
             // pass 1: key sum of squares and query dot, four rows at a time
+            uint32_t rowa = gcur.row;
             for (int c0 = 0; c0 < gs; c0 += 4) {
                 float part[8];
 #pragma unroll
                 for (int r = 0; r < 4; ++r) {
                     float2 ss2 = make_float2(0.0f, 0.0f), qt2 = make_float2(0.0f, 0.0f);
                     if (c0 + r < gs) {
-                        const unsigned char* row =
-                            ring + static_cast<size_t>(ring_add(gslot, c0 + r, slots)) * a.slot_bytes;
 #pragma unroll
                         for (int i = 0; i < VPT; ++i) {
                             if (KEYALL ? (col[i] >= 0) : (kmask[i] != 0u)) {
-                                const uint4 xv = ld_shared_v4(row + col[i] * 16);
+                                const uint4 xv = lds128(rowa + i * vstep);
 #pragma unroll
                                 for (int k = 0; k < 4; ++k) {
                                     float2 x = bf2_to_f2(u4_get(xv, k));
@@ -194,16 +221,18 @@ __global__ void __launch_bounds__(max_threads_for(VPT), 1) attnres_fwd_kernel(co
                                 }
                             }
                         }
+                        rowa += sb;
+                        if (rowa >= ring_lo + ring_span) rowa -= ring_span;
                     }
                     part[r] = ss2.x + ss2.y;
                     part[4 + r] = qt2.x + qt2.y;
                 }
                 warp_reduce_scatter<8>(part, lane);
-                // lane l now holds element l >> 2: rows 0..3 sum-of-squares, then dots
+                // lane l holds element l >> 2: rows 0..3 sum-of-squares, then dots
                 if ((lane & 3) == 0) {
                     const int idx = lane >> 2;
                     const int r = idx & 3;
-                    if (c0 + r < gs) redw[(idx >> 2) * 32 + c0 + r] = part[0];
+                    if (c0 + r < gs) red[((rbuf * red_rows) + (idx >> 2) * 32 + c0 + r) * kRedPitch + warp] = part[0];
                 }
             }
             named_bar_sync(1, nct);
@@ -215,11 +244,8 @@ __global__ void __launch_bounds__(max_threads_for(VPT), 1) attnres_fwd_kernel(co
             {
                 float ss = 0.0f, qt = 0.0f;
                 if (lane < gs) {
-                    for (int w = 0; w < ncw; ++w) {
-                        const float* rw = red + (rbuf * ncw + w) * red_stride;
-                        ss += rw[lane];
-                        qt += rw[32 + lane];
-                    }
+                    ss = red_sum(rbuf, lane);
+                    qt = red_sum(rbuf, 32 + lane);
                 }
                 const float r = rsqrtf(fmaf(ss, inv_r, a.eps));
                 const float z = a.scale * r * qt;
@@ -241,23 +267,22 @@ __global__ void __launch_bounds__(max_threads_for(VPT), 1) attnres_fwd_kernel(co
             for (int i = 0; i < VPT; ++i)
 #pragma unroll
                 for (int k = 0; k < 4; ++k) acc[i][k] = fmul2(acc[i][k], corr2);
-            int sl = gslot;
+            RingCursor pc = gcur;
 #pragma unroll 2
             for (int s = 0; s < gs; ++s) {
                 const float es = __shfl_sync(0xffffffffu, e, s);
                 const float2 es2 = make_float2(es, es);
-                const unsigned char* row = ring + static_cast<size_t>(sl) * a.slot_bytes;
 #pragma unroll
                 for (int i = 0; i < VPT; ++i) {
                     if (col[i] >= 0) {
-                        const uint4 xv = ld_shared_v4(row + col[i] * 16);
+                        const uint4 xv = lds128(pc.row + i * vstep);
 #pragma unroll
                         for (int k = 0; k < 4; ++k) acc[i][k] = ffma2(es2, bf2_to_f2(u4_get(xv, k)), acc[i][k]);
                     }
                 }
                 __syncwarp();
-                if (lane == 0) mbar_arrive(empty + sl);
-                sl = ring_add(sl, 1, slots);
+                if (lane == 0) mbar_arrive_s(empty_s + 8u * pc.slot);
+                pc.next(sb, slots, ring_lo);
             }
         }
         const float inv_l = 1.0f / l_run;
@@ -275,10 +300,9 @@ __global__ void __launch_bounds__(max_threads_for(VPT), 1) attnres_fwd_kernel(co
 #pragma unroll
                     for (int k = 0; k < 4; ++k) ss2 = ffma2(acc[i][k], acc[i][k], ss2);
             const float ss = warp_sum(ss2.x + ss2.y);
-            if (lane == 0) red[(rbuf * ncw + warp) * red_stride] = ss;
+            if (lane == 0) red[(rbuf * red_rows) * kRedPitch + warp] = ss;
             named_bar_sync(1, nct);
-            float tot = 0.0f;
-            for (int w = 0; w < ncw; ++w) tot += red[(rbuf * ncw + w) * red_stride];
+            const float tot = red_sum(rbuf, 0);
             rbuf ^= 1;
             rho = rsqrtf(fmaf(tot, inv_d, a.eps));
             if (threadIdx.x == 0) a.o_rstd[n] = rho;

@@ -241,4 +241,90 @@ __device__ __forceinline__ constexpr int log2_const() {
     return K <= 1 ? 0 : 1 + log2_const<K / 2>();
 }
 
+
+// ------------------------------------------------ 32-bit shared addressing
+__device__ __forceinline__ void mbar_arrive_s(uint32_t bar) {
+    asm volatile("mbarrier.arrive.release.cta.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_test_s(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+__device__ __forceinline__ bool mbar_test_sleep_s(uint32_t bar, uint32_t parity, uint32_t hint_ns) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity), "r"(hint_ns)
+        : "memory");
+    return ok != 0;
+}
+
+// Bounded wait on a barrier given by its 32-bit shared address (see mbar_wait).
+static __device__ __noinline__ bool mbar_wait_slow_s(uint32_t bar, uint32_t parity, volatile int* abort,
+                                              unsigned* err, unsigned where) {
+    if (*abort) return false;
+    const uint64_t t0 = global_timer_ns();
+    uint32_t spins = 0;
+    while (!mbar_test_sleep_s(bar, parity, 20000u)) {
+        if (((++spins) & 15u) == 0u) {
+            if (*abort) return false;
+            if (global_timer_ns() - t0 > 2000000000ull) {
+                atomicCAS(err, 0u, where);
+                *abort = 1;
+                return false;
+            }
+        }
+    }
+    return true;
+}
+
+__device__ __forceinline__ bool mbar_wait_s(uint32_t bar, uint32_t parity, volatile int* abort,
+                                            unsigned* err, unsigned where) {
+    if (mbar_test_s(bar, parity)) return true;
+    return mbar_wait_slow_s(bar, parity, abort, err, where);
+}
+
+__device__ __forceinline__ uint4 lds128(uint32_t addr) {
+    uint4 v;
+    asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "r"(addr));
+    return v;
+}
+
+__device__ __forceinline__ float4 lds128f(uint32_t addr) {
+    float4 v;
+    asm volatile("ld.shared.v4.f32 {%0,%1,%2,%3}, [%4];"
+                 : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+                 : "r"(addr));
+    return v;
+}
+
+// Position in the shared-memory row ring: row address, slot index, phase.
+struct RingCursor {
+    uint32_t row;
+    int slot;
+    uint32_t phase;
+    __device__ __forceinline__ void next(uint32_t slot_bytes, int slots, uint32_t ring_lo) {
+        row += slot_bytes;
+        if (++slot == slots) {
+            slot = 0;
+            row = ring_lo;
+            phase ^= 1u;
+        }
+    }
+};
+
 }  // namespace attnres

@@ -54,8 +54,13 @@ struct Plan {
 // Byte offsets inside the dynamic shared memory of one CTA.
 struct SmemLayout {
     uint32_t ring, full, empty, tfull, tempty, red, tok, coef, misc, total;
-    int red_stride;  // floats per warp in the reduction scratch
+    int red_rows;  // rows of the reduction scratch (per buffer)
 };
+
+// The reduction scratch is [2 buffers][red_rows][kRedPitch] floats: row =
+// reduced quantity, column = consumer warp.  A pitch of 20 floats lets a lane
+// read one row's 16 warp partials with four conflict-free 16-byte loads.
+constexpr int kRedPitch = 20;
 
 __host__ __device__ inline uint32_t align_up(uint32_t x, uint32_t a) { return (x + a - 1) / a * a; }
 
@@ -78,8 +83,9 @@ __host__ __device__ inline SmemLayout make_layout(int slots, int slot_bytes, int
     off += backward ? 8u * kTokSlots : 0u;
     off = align_up(off, 16);
     L.red = off;
-    L.red_stride = s_pad > 64 ? s_pad : 64;
-    off += 2u * ncw * static_cast<uint32_t>(L.red_stride) * 4u;
+    L.red_rows = s_pad > 64 ? s_pad : 64;
+    off += 2u * static_cast<uint32_t>(L.red_rows) * kRedPitch * 4u;
+    (void)ncw;
     L.tok = off;
     off += backward ? static_cast<uint32_t>(kTokSlots) * (3u * s_pad + 4u) * 4u : 0u;
     L.coef = off;
