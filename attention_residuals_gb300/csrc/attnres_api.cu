@@ -72,25 +72,52 @@ attnres_status make_plan(const attnres_params* p, Plan* plan) {
     if (pl.ncw < 1 || pl.ncw > max_warps_for(pl.vpt)) return ATTNRES_ERR_UNSUPPORTED;
     pl.slot_bytes = static_cast<int>(align_up(static_cast<uint32_t>(p->D) * 2u, 128u));
     pl.s_pad = static_cast<int>(align_up(static_cast<uint32_t>(p->S), 4u));
-    // Ring depth: as many row slots as the backward layout (the larger) fits.
-    int slots = 0;
-    for (int k = kMaxSlots; k >= 1; --k) {
-        if (make_layout(k, pl.slot_bytes, pl.ncw, pl.s_pad, true).total <=
-            static_cast<uint32_t>(dev.smem_optin)) {
-            slots = k;
-            break;
-        }
+    const int S = p->S;
+    const long long sb = pl.slot_bytes;
+    const long long optin = dev.smem_optin;
+    auto fits = [&](int chunks, int rows, int dy, bool bwd) {
+        return make_layout(chunks, rows, pl.slot_bytes, dy, pl.s_pad, bwd).total <= static_cast<uint32_t>(optin);
+    };
+    auto max_chunks = [&](int rows, int dy, bool bwd) {
+        int c = 0;
+        while (c < kMaxChunks && fits(c + 1, rows, dy, bwd)) ++c;
+        return c;
+    };
+    // Forward: a chunk is one softmax group; keep at least four chunks in the
+    // ring so that loads of later groups overlap the current one.
+    {
+        const long long fixed = make_layout(0, 1, pl.slot_bytes, 0, pl.s_pad, false).total + 64;
+        long long gmax = (optin - fixed) / (4 * sb);
+        if (gmax > kMaxGroup) gmax = kMaxGroup;
+        if (gmax < 1) gmax = 1;
+        const int groups = static_cast<int>((S + gmax - 1) / gmax);
+        pl.f_rows = (S + groups - 1) / groups;
+        pl.f_chunks = max_chunks(pl.f_rows, 0, false);
+        if (pl.f_chunks < 2) return ATTNRES_ERR_UNSUPPORTED;
     }
-    if (slots < 4) return ATTNRES_ERR_UNSUPPORTED;
-    pl.slots = slots;
-    pl.smem_fwd = make_layout(slots, pl.slot_bytes, pl.ncw, pl.s_pad, false).total;
-    pl.smem_bwd = make_layout(slots, pl.slot_bytes, pl.ncw, pl.s_pad, true).total;
-    // Forward groups keep their rows resident: at most half the ring each.
-    int g = p->S < kMaxGroup ? p->S : kMaxGroup;
-    if (g > slots / 2) g = slots / 2;
-    if (g < 1) g = 1;
-    pl.group = g;
-    pl.resident = (p->S + 1) <= slots ? 1 : 0;
+    // Backward: dy ring, then either a resident token (its rows in two
+    // chunks, at most ~60% of the ring so the next token can load meanwhile)
+    // or streamed chunks (at least four in the ring).
+    {
+        pl.dy_slots = sb > 8192 ? 2 : 4;
+        const long long fixed = make_layout(0, 1, pl.slot_bytes, pl.dy_slots, pl.s_pad, true).total + 64;
+        const long long avail = optin - fixed;
+        pl.resident = (static_cast<long long>(S) * sb * 10 <= avail * 6) ? 1 : 0;
+        if (pl.resident) {
+            pl.b_rows = S >= 2 ? (S + 1) / 2 : 1;
+        } else {
+            long long g = avail / (4 * sb);
+            if (g > 16) g = 16;
+            if (g < 1) g = 1;
+            pl.b_rows = static_cast<int>(g);
+        }
+        pl.b_chunks = max_chunks(pl.b_rows, pl.dy_slots, true);
+        const int per_token = (S + pl.b_rows - 1) / pl.b_rows;
+        if (pl.resident && pl.b_chunks < per_token + 1) pl.resident = 0;
+        if (!pl.resident && pl.b_chunks < 2) return ATTNRES_ERR_UNSUPPORTED;
+    }
+    pl.smem_fwd = make_layout(pl.f_chunks, pl.f_rows, pl.slot_bytes, 0, pl.s_pad, false).total;
+    pl.smem_bwd = make_layout(pl.b_chunks, pl.b_rows, pl.slot_bytes, pl.dy_slots, pl.s_pad, true).total;
     const int thr = p->split_n_threshold > 0 ? p->split_n_threshold : ATTNRES_DEFAULT_SPLIT_N;
     pl.split = p->N >= thr ? 1 : 0;
     long long grid = dev.sm_count;
@@ -144,8 +171,8 @@ attnres_status attnres_plan_info(const attnres_params* p, int64_t out[8]) {
     out[0] = pl.grid;
     out[1] = pl.ncw;
     out[2] = pl.vpt;
-    out[3] = pl.slots;
-    out[4] = pl.group;
+    out[3] = pl.b_chunks * 1000 + pl.b_rows;
+    out[4] = pl.f_chunks * 1000 + pl.f_rows;
     out[5] = pl.resident;
     out[6] = static_cast<int64_t>(pl.smem_bwd);
     out[7] = pl.split;
@@ -182,11 +209,11 @@ attnres_status attnres_fwd(const attnres_params* p, const void* q, const void* w
     a.out_norm = p->out_norm;
     a.eps = p->eps;
     a.scale = p->scale;
-    a.slots = pl.slots;
+    a.chunks = pl.f_chunks;
+    a.rows = pl.f_rows;
     a.slot_bytes = pl.slot_bytes;
     a.ncw = pl.ncw;
     a.s_pad = pl.s_pad;
-    a.group = pl.group;
     a.q = static_cast<const uint16_t*>(q);
     a.w_o = static_cast<const uint16_t*>(w_o);
     a.y = static_cast<uint16_t*>(y);
@@ -274,7 +301,9 @@ attnres_status attnres_bwd(const attnres_params* p, const void* q, const void* w
     a.out_norm = p->out_norm;
     a.eps = p->eps;
     a.scale = p->scale;
-    a.slots = pl.slots;
+    a.chunks = pl.b_chunks;
+    a.rows = pl.b_rows;
+    a.dy_slots = pl.dy_slots;
     a.slot_bytes = pl.slot_bytes;
     a.ncw = pl.ncw;
     a.s_pad = pl.s_pad;

@@ -15,12 +15,14 @@
 //
 // GB300 mapping.  As in the forward, one persistent CTA per SM, a producer
 // thread filling a shared-memory row ring with 1-D TMA copies, and consumer
-// threads that own fixed 16-byte column vectors.  Per token the ring
-// receives dy and the S source rows.  When the S rows fit in the ring
+// threads that own fixed 16-byte column vectors.  dy rows go through a small
+// ring of their own; source rows through a ring of chunks of G rows with one
+// "full" and one "empty" mbarrier per chunk.  When a token's S rows fit
 // ("resident"), each source row is read from HBM once: the o rebuild (with
 // the output norm), the dot pass and the write pass all read it from shared
-// memory.  Otherwise the producer streams the rows once per pass (served
-// from L2 when it still holds them), and the write pass gets key slices only.  The saved per-token statistics arrive
+// memory, and the write pass releases the chunks.  Otherwise the producer
+// streams the rows once per pass (served from L2 when it still holds them),
+// and the write pass gets key slices only.  The saved per-token statistics arrive
 // through small cp.async copies into a separate 4-deep ring.
 //
 // dq and dw_o: every consumer thread owns the same columns for every token,
@@ -43,18 +45,6 @@ namespace {
 // First failed wait of any backward launch (0 = none).
 __device__ unsigned int g_bwd_error = 0;
 
-__device__ __forceinline__ void advance(int& slot, uint32_t& phase, int slots) {
-    if (++slot == slots) {
-        slot = 0;
-        phase ^= 1u;
-    }
-}
-
-__device__ __forceinline__ int ring_add(int slot, int k, int slots) {
-    const int r = slot + k;
-    return r >= slots ? r - slots : r;
-}
-
 __device__ __forceinline__ float ldcg_f32(const float* p) { return __ldcg(p); }
 
 // KEYALL: every channel is a key channel (R == D), so no per-vector masks.
@@ -63,12 +53,15 @@ __global__ void __launch_bounds__(max_threads_for(VPT), 1) attnres_bwd_kernel(co
     extern __shared__ __align__(128) unsigned char smem[];
     const int ncw = a.ncw;
     const int nct = ncw * 32;
-    const int slots = a.slots;
+    const int K = a.chunks;   // ring depth in chunks
+    const int G = a.rows;     // rows per chunk
+    const int DS = a.dy_slots;
     const int s_pad = a.s_pad;
-    const SmemLayout L = make_layout(slots, a.slot_bytes, ncw, s_pad, true);
-    unsigned char* ring = smem + L.ring;
+    const SmemLayout L = make_layout(K, G, a.slot_bytes, DS, s_pad, true);
     uint64_t* full = reinterpret_cast<uint64_t*>(smem + L.full);
     uint64_t* empty = reinterpret_cast<uint64_t*>(smem + L.empty);
+    uint64_t* dyfull = reinterpret_cast<uint64_t*>(smem + L.dyfull);
+    uint64_t* dyempty = reinterpret_cast<uint64_t*>(smem + L.dyempty);
     uint64_t* tfull = reinterpret_cast<uint64_t*>(smem + L.tfull);
     uint64_t* tempty = reinterpret_cast<uint64_t*>(smem + L.tempty);
     float* red = reinterpret_cast<float*>(smem + L.red);  // [2][red_rows][kRedPitch]
@@ -82,11 +75,18 @@ __global__ void __launch_bounds__(max_threads_for(VPT), 1) attnres_bwd_kernel(co
     const long long N = a.N;
     const int S = a.S;
     const int D = a.D;
+    const uint32_t sb = static_cast<uint32_t>(a.slot_bytes);
+    const uint32_t cb = static_cast<uint32_t>(G) * sb;
+    const int nchunk = (S + G - 1) / G;  // chunks per pass of one token
 
     if (threadIdx.x == 0) {
-        for (int k = 0; k < slots; ++k) {
+        for (int k = 0; k < K; ++k) {
             mbar_init(full + k, 1);
             mbar_init(empty + k, ncw);
+        }
+        for (int k = 0; k < DS; ++k) {
+            mbar_init(dyfull + k, 1);
+            mbar_init(dyempty + k, ncw);
         }
         for (int k = 0; k < kTokSlots; ++k) {
             mbar_init(tfull + k, 32);
@@ -107,11 +107,18 @@ __global__ void __launch_bounds__(max_threads_for(VPT), 1) attnres_bwd_kernel(co
         const bool key_only = ((a.ko & 7) == 0) && ((a.R & 7) == 0);
         const uint32_t key_off_b = key_only ? static_cast<uint32_t>(a.ko) * 2u : 0u;
         const uint32_t key_bytes = key_only ? static_cast<uint32_t>(a.R) * 2u : row_bytes;
-        int slot = 0;
+        // Passes over the source rows per token: resident -> one; streaming
+        // -> (o rebuild when needed), dot pass, write pass (key slices).
+        const int npass = a.resident ? 1 : ((a.out_norm && !a.o_pre) ? 3 : 2);
+        unsigned char* ring = smem + L.ring;
+        unsigned char* dyring = smem + L.dyring;
+        int k = 0;
         uint32_t phase = 0;
+        int dk = 0;
+        uint32_t dphase = 0;
         int ts = 0;
         uint32_t tphase = 0;
-        long long issued = 0;
+        long long issued = 0, dy_issued = 0;
         for (long long n = blockIdx.x; n < N; n += gridDim.x) {
             if (*abort_flag) break;
             // token statistics -> tok[ts] (all 32 lanes arrive on tfull)
@@ -129,44 +136,49 @@ __global__ void __launch_bounds__(max_threads_for(VPT), 1) attnres_bwd_kernel(co
                 tphase ^= 1u;
             }
             if (lane == 0) {
-                // Row schedule of one token: dy; then, when o must be rebuilt
-                // from streamed rows, S rows for that pass; S rows for the dot
-                // pass (in resident mode these also serve the other passes);
-                // when streaming, S key slices for the write pass.
-                const int pass_a = (a.out_norm && !a.o_pre && !a.resident) ? S : 0;
-                const int pass_c = a.resident ? 0 : S;
-                const int nrows = 1 + pass_a + S + pass_c;
-                for (int r = 0; r < nrows; ++r) {
-                    const unsigned char* src;
-                    uint32_t off = 0, bytes = row_bytes;
-                    if (r == 0) {
-                        src = reinterpret_cast<const unsigned char*>(a.dy + n * D);
-                    } else {
-                        int s = r - 1;
-                        if (s >= pass_a) s -= pass_a;  // rows of the o pass come first
-                        if (r - 1 >= pass_a + S) {      // write-pass key slices
-                            off = key_off_b;
-                            bytes = key_bytes;
-                        }
-                        if (s >= S) s -= S;
-                        src = static_cast<const unsigned char*>(a.src[s]) + (n * a.src_ld) * 2 + off;
+                if (mbar_wait(dyempty + dk, dphase ^ 1u, abort_flag, &g_bwd_error, kSiteBwdProducer)) {
+                    mbar_arrive_expect_tx(dyfull + dk, row_bytes);
+                    tma_load_1d(dyring + dk * sb, a.dy + n * D, row_bytes, dyfull + dk, pol);
+                    ++dy_issued;
+                    if (++dk == DS) {
+                        dk = 0;
+                        dphase ^= 1u;
                     }
-                    if (!mbar_wait(empty + slot, phase ^ 1u, abort_flag, &g_bwd_error, kSiteBwdProducer)) break;
-                    mbar_arrive_expect_tx(full + slot, bytes);
-                    tma_load_1d(ring + static_cast<size_t>(slot) * a.slot_bytes + off, src, bytes,
-                                full + slot, pol);
-                    ++issued;
-                    advance(slot, phase, slots);
+                }
+                for (int pass = 0; pass < npass && !*abort_flag; ++pass) {
+                    const bool keys = !a.resident && pass == npass - 1;
+                    const uint32_t off = keys ? key_off_b : 0u;
+                    const uint32_t bytes = keys ? key_bytes : row_bytes;
+                    for (int g0 = 0; g0 < S; g0 += G) {
+                        const int gs = min(G, S - g0);
+                        if (!mbar_wait(empty + k, phase ^ 1u, abort_flag, &g_bwd_error, kSiteBwdProducer)) break;
+                        mbar_arrive_expect_tx(full + k, bytes * static_cast<uint32_t>(gs));
+                        for (int r = 0; r < gs; ++r) {
+                            const unsigned char* src =
+                                static_cast<const unsigned char*>(a.src[g0 + r]) + (n * a.src_ld) * 2 + off;
+                            tma_load_1d(ring + k * cb + r * sb + off, src, bytes, full + k, pol);
+                        }
+                        ++issued;
+                        if (++k == K) {
+                            k = 0;
+                            phase ^= 1u;
+                        }
+                    }
                 }
             }
             __syncwarp();
         }
         asm volatile("cp.async.wait_all;" ::: "memory");
         if (lane == 0 && *abort_flag) {
-            for (int k = 0; k < slots && k < issued; ++k) {
-                const long long fills = (issued - 1 - k) / slots + 1;
+            for (int c = 0; c < K && c < issued; ++c) {
+                const long long fills = (issued - 1 - c) / K + 1;
                 volatile int no_abort = 0;
-                mbar_wait(full + k, static_cast<uint32_t>((fills - 1) & 1), &no_abort, &g_bwd_error, kSiteDrain);
+                mbar_wait(full + c, static_cast<uint32_t>((fills - 1) & 1), &no_abort, &g_bwd_error, kSiteDrain);
+            }
+            for (int c = 0; c < DS && c < dy_issued; ++c) {
+                const long long fills = (dy_issued - 1 - c) / DS + 1;
+                volatile int no_abort = 0;
+                mbar_wait(dyfull + c, static_cast<uint32_t>((fills - 1) & 1), &no_abort, &g_bwd_error, kSiteDrain);
             }
         }
         return;
@@ -188,22 +200,22 @@ __global__ void __launch_bounds__(max_threads_for(VPT), 1) attnres_bwd_kernel(co
         unsigned m = 0;
         uint32_t ww[4];
 #pragma unroll
-        for (int k = 0; k < 4; ++k) {
+        for (int kk = 0; kk < 4; ++kk) {
             float qv[2];
             uint32_t wv = 0;
 #pragma unroll
             for (int h = 0; h < 2; ++h) {
-                const int j = 8 * c + 2 * k + h;
+                const int j = 8 * c + 2 * kk + h;
                 const bool in_key = col[i] >= 0 && j >= ko && j < kend;
-                m |= in_key ? (1u << (2 * k + h)) : 0u;
+                m |= in_key ? (1u << (2 * kk + h)) : 0u;
                 qv[h] = in_key ? a.scale * bf16_bits_to_float(a.q[j - ko]) : 0.0f;
                 const uint32_t wh = (a.out_norm && col[i] >= 0) ? a.w_o[j] : 0x3f80u;
                 wv |= wh << (16 * h);
             }
-            qs[i][k] = make_float2(qv[0], qv[1]);
-            ww[k] = wv;
-            dq_acc[i][k] = make_float2(0.0f, 0.0f);
-            dw_acc[i][k] = make_float2(0.0f, 0.0f);
+            qs[i][kk] = make_float2(qv[0], qv[1]);
+            ww[kk] = wv;
+            dq_acc[i][kk] = make_float2(0.0f, 0.0f);
+            dw_acc[i][kk] = make_float2(0.0f, 0.0f);
         }
         kmask[i] = m;
         wb[i] = make_uint4(ww[0], ww[1], ww[2], ww[3]);
@@ -211,22 +223,22 @@ __global__ void __launch_bounds__(max_threads_for(VPT), 1) attnres_bwd_kernel(co
     const float inv_r = 1.0f / static_cast<float>(a.R);
     const float inv_d = 1.0f / static_cast<float>(D);
 
-    // 32-bit shared addresses; the cursor's row address already includes
-    // this thread's first vector offset.
+    // 32-bit shared addresses (row addresses include this thread's first
+    // vector offset).
     const uint32_t sbase = smem_u32(smem);
     const uint32_t voff = static_cast<uint32_t>(col[0] < 0 ? 0 : col[0]) * 16u;
     const uint32_t vstep = static_cast<uint32_t>(nct) * 16u;
-    const uint32_t sb = static_cast<uint32_t>(a.slot_bytes);
     const uint32_t ring_lo = sbase + L.ring + voff;
-    const uint32_t ring_span = static_cast<uint32_t>(slots) * sb;
+    const uint32_t dy_lo = sbase + L.dyring + voff;
     const uint32_t full_s = sbase + L.full;
     const uint32_t empty_s = sbase + L.empty;
+    const uint32_t dyfull_s = sbase + L.dyfull;
+    const uint32_t dyempty_s = sbase + L.dyempty;
     const uint32_t tfull_s = sbase + L.tfull;
     const uint32_t tempty_s = sbase + L.tempty;
     const uint32_t red_s = sbase + L.red;
     const int red_rows = L.red_rows;
     const int nq = (ncw + 3) >> 2;
-    // this thread's byte offset inside a dvalues row, and the row pitch
     const long long dld_b = a.dsrc_ld * 2;
     const long long d_off = static_cast<long long>(col[0] < 0 ? 0 : col[0]) * 16;
 
@@ -243,7 +255,20 @@ __global__ void __launch_bounds__(max_threads_for(VPT), 1) attnres_bwd_kernel(co
         return t;
     };
 
-    RingCursor cur{ring_lo, 0, 0u};
+    // chunk-ring position (chunk index, fill parity, row-0 address)
+    int ck = 0;
+    uint32_t cphase = 0;
+    uint32_t cbase = ring_lo;
+    auto next_chunk = [&](int& k, uint32_t& ph, uint32_t& base) {
+        base += cb;
+        if (++k == K) {
+            k = 0;
+            ph ^= 1u;
+            base = ring_lo;
+        }
+    };
+    int dk = 0;
+    uint32_t dphase = 0;
     int ts = 0;
     uint32_t tphase = 0;
     int rbuf = 0;
@@ -255,21 +280,30 @@ __global__ void __launch_bounds__(max_threads_for(VPT), 1) attnres_bwd_kernel(co
         // ---- dy into registers; its slot is free again at once
         uint4 dyv[VPT];
         {
-            mbar_wait_s(full_s + 8u * cur.slot, cur.phase, abort_flag, &g_bwd_error, kSiteBwdConsumer);
+            mbar_wait_s(dyfull_s + 8u * dk, dphase, abort_flag, &g_bwd_error, kSiteBwdConsumer);
+            uint32_t dep = 0;
 #pragma unroll
-            for (int i = 0; i < VPT; ++i)
-                dyv[i] = col[i] >= 0 ? lds128(cur.row + i * vstep) : make_uint4(0u, 0u, 0u, 0u);
+            for (int i = 0; i < VPT; ++i) {
+                dyv[i] = col[i] >= 0 ? lds128(dy_lo + dk * sb + i * vstep) : make_uint4(0u, 0u, 0u, 0u);
+                dep ^= dyv[i].x;
+            }
             __syncwarp();
-            if (lane == 0) mbar_arrive_s(empty_s + 8u * cur.slot);
-            cur.next(sb, slots, ring_lo);
+            if (lane == 0) mbar_arrive_after(dyempty_s + 8u * dk, dep);
+            if (++dk == DS) {
+                dk = 0;
+                dphase ^= 1u;
+            }
         }
+        // first chunk of this token's rows (resident: used by every pass)
+        const int tk_ck = ck;
+        const uint32_t tk_phase = cphase, tk_base = cbase;
 
         // ---- gradient wrt the mixture o (kept in registers)
         float2 dout[VPT][4];
         if (a.out_norm) {
             // o = sum_s alpha_s v_s in FP32: the caller's saved copy, or
-            // rebuilt from the source rows (resident: the rows the dot pass
-            // uses next; streaming: a dedicated pass of rows).
+            // rebuilt from the source rows (resident: the rows the other
+            // passes use; streaming: a dedicated pass of chunks).
             float2 o[VPT][4];
             if (a.o_pre) {
                 const float* prow = a.o_pre + n * static_cast<long long>(D);
@@ -284,43 +318,47 @@ __global__ void __launch_bounds__(max_threads_for(VPT), 1) attnres_bwd_kernel(co
                         o[i][3] = make_float2(__uint_as_float(hi.z), __uint_as_float(hi.w));
                     } else {
 #pragma unroll
-                        for (int k = 0; k < 4; ++k) o[i][k] = make_float2(0.0f, 0.0f);
+                        for (int kk = 0; kk < 4; ++kk) o[i][kk] = make_float2(0.0f, 0.0f);
                     }
                 }
             } else {
 #pragma unroll
                 for (int i = 0; i < VPT; ++i)
 #pragma unroll
-                    for (int k = 0; k < 4; ++k) o[i][k] = make_float2(0.0f, 0.0f);
-                RingCursor ac = cur;
-                if (a.resident) {
-                    for (int s = 0; s < S; ++s) {
-                        mbar_wait_s(full_s + 8u * ac.slot, ac.phase, abort_flag, &g_bwd_error, kSiteBwdConsumer);
-                        ac.next(sb, slots, ring_lo);
-                    }
-                    ac = cur;
-                }
+                    for (int kk = 0; kk < 4; ++kk) o[i][kk] = make_float2(0.0f, 0.0f);
+                int k = ck;
+                uint32_t ph = cphase, base = cbase;
+                for (int g0 = 0; g0 < S; g0 += G) {
+                    const int gs = min(G, S - g0);
+                    mbar_wait_s(full_s + 8u * k, ph, abort_flag, &g_bwd_error, kSiteBwdConsumer);
+                    uint32_t dep = 0;
+                    uint32_t rowa = base;
 #pragma unroll 2
-                for (int s = 0; s < S; ++s) {
-                    if (!a.resident)
-                        mbar_wait_s(full_s + 8u * ac.slot, ac.phase, abort_flag, &g_bwd_error, kSiteBwdConsumer);
-                    const float al = tk[s];
-                    const float2 al2 = make_float2(al, al);
+                    for (int r = 0; r < gs; ++r) {
+                        const float al = tk[g0 + r];
+                        const float2 al2 = make_float2(al, al);
 #pragma unroll
-                    for (int i = 0; i < VPT; ++i) {
-                        if (col[i] >= 0) {
-                            const uint4 xv = lds128(ac.row + i * vstep);
+                        for (int i = 0; i < VPT; ++i) {
+                            if (col[i] >= 0) {
+                                const uint4 xv = lds128(rowa + i * vstep);
+                                dep ^= xv.x;
 #pragma unroll
-                            for (int k = 0; k < 4; ++k) o[i][k] = ffma2(al2, bf2_to_f2(u4_get(xv, k)), o[i][k]);
+                                for (int kk = 0; kk < 4; ++kk) o[i][kk] = ffma2(al2, bf2_to_f2(u4_get(xv, kk)), o[i][kk]);
+                            }
                         }
+                        rowa += sb;
                     }
                     if (!a.resident) {
                         __syncwarp();
-                        if (lane == 0) mbar_arrive_s(empty_s + 8u * ac.slot);
+                        if (lane == 0) mbar_arrive_after(empty_s + 8u * k, dep);
                     }
-                    ac.next(sb, slots, ring_lo);
+                    next_chunk(k, ph, base);
                 }
-                if (!a.resident) cur = ac;  // the streamed o-pass rows are consumed
+                if (!a.resident) {  // the streamed o-pass chunks are consumed
+                    ck = k;
+                    cphase = ph;
+                    cbase = base;
+                }
             }
             const float rho = tk[3 * s_pad];
             const float2 rho2 = make_float2(rho, rho);
@@ -328,14 +366,14 @@ __global__ void __launch_bounds__(max_threads_for(VPT), 1) attnres_bwd_kernel(co
 #pragma unroll
             for (int i = 0; i < VPT; ++i) {
 #pragma unroll
-                for (int k = 0; k < 4; ++k) {
-                    const float2 yh = fmul2(o[i][k], rho2);
-                    const float2 g = bf2_to_f2(u4_get(dyv[i], k));
-                    o[i][k] = yh;
-                    dw_acc[i][k] = ffma2(g, yh, dw_acc[i][k]);
-                    const float2 gw = fmul2(g, bf2_to_f2(u4_get(wb[i], k)));
+                for (int kk = 0; kk < 4; ++kk) {
+                    const float2 yh = fmul2(o[i][kk], rho2);
+                    const float2 g = bf2_to_f2(u4_get(dyv[i], kk));
+                    o[i][kk] = yh;
+                    dw_acc[i][kk] = ffma2(g, yh, dw_acc[i][kk]);
+                    const float2 gw = fmul2(g, bf2_to_f2(u4_get(wb[i], kk)));
                     gy2 = ffma2(gw, yh, gy2);
-                    dout[i][k] = gw;
+                    dout[i][kk] = gw;
                 }
             }
             const float gy = warp_sum(gy2.x + gy2.y);
@@ -348,63 +386,59 @@ __global__ void __launch_bounds__(max_threads_for(VPT), 1) attnres_bwd_kernel(co
 #pragma unroll
             for (int i = 0; i < VPT; ++i)
 #pragma unroll
-                for (int k = 0; k < 4; ++k) dout[i][k] = fmul2(rho2, ffma2(o[i][k], ncg2, dout[i][k]));
+                for (int kk = 0; kk < 4; ++kk) dout[i][kk] = fmul2(rho2, ffma2(o[i][kk], ncg2, dout[i][kk]));
         } else {
 #pragma unroll
             for (int i = 0; i < VPT; ++i)
 #pragma unroll
-                for (int k = 0; k < 4; ++k) dout[i][k] = bf2_to_f2(u4_get(dyv[i], k));
+                for (int kk = 0; kk < 4; ++kk) dout[i][kk] = bf2_to_f2(u4_get(dyv[i], kk));
         }
 
-        // ---- dot pass: da_s = <do, v_s>, four rows at a time
-        const RingCursor vcur = cur;
-        if (a.resident) {
-            RingCursor wc = cur;
-            for (int s = 0; s < S; ++s) {  // completed phases return at once
-                mbar_wait_s(full_s + 8u * wc.slot, wc.phase, abort_flag, &g_bwd_error, kSiteBwdConsumer);
-                wc.next(sb, slots, ring_lo);
-            }
-        }
-        RingCursor dc = cur;
-        for (int c0 = 0; c0 < S; c0 += 4) {
-            const int cn = min(4, S - c0);
-            if (!a.resident) {
-                RingCursor wc = dc;
-                for (int r = 0; r < cn; ++r) {
-                    mbar_wait_s(full_s + 8u * wc.slot, wc.phase, abort_flag, &g_bwd_error, kSiteBwdConsumer);
-                    wc.next(sb, slots, ring_lo);
-                }
-            }
-            float part[4];
-            uint32_t rowa = dc.row;
+        // ---- dot pass: da_s = <do, v_s>, four rows at a time per chunk
+        {
+            int k = a.resident ? tk_ck : ck;
+            uint32_t ph = a.resident ? tk_phase : cphase;
+            uint32_t base = a.resident ? tk_base : cbase;
+            for (int g0 = 0; g0 < S; g0 += G) {
+                const int gs = min(G, S - g0);
+                mbar_wait_s(full_s + 8u * k, ph, abort_flag, &g_bwd_error, kSiteBwdConsumer);
+                uint32_t dep = 0;
+                for (int c0 = 0; c0 < gs; c0 += 4) {
+                    float part[4];
 #pragma unroll
-            for (int r = 0; r < 4; ++r) {
-                float2 d2 = make_float2(0.0f, 0.0f);
-                if (r < cn) {
+                    for (int r = 0; r < 4; ++r) {
+                        float2 d2 = make_float2(0.0f, 0.0f);
+                        if (c0 + r < gs) {
+                            const uint32_t rowa = base + static_cast<uint32_t>(c0 + r) * sb;
 #pragma unroll
-                    for (int i = 0; i < VPT; ++i) {
-                        if (col[i] >= 0) {
-                            const uint4 xv = lds128(rowa + i * vstep);
+                            for (int i = 0; i < VPT; ++i) {
+                                if (col[i] >= 0) {
+                                    const uint4 xv = lds128(rowa + i * vstep);
+                                    dep ^= xv.x;
 #pragma unroll
-                            for (int k = 0; k < 4; ++k) d2 = ffma2(dout[i][k], bf2_to_f2(u4_get(xv, k)), d2);
+                                    for (int kk = 0; kk < 4; ++kk) d2 = ffma2(dout[i][kk], bf2_to_f2(u4_get(xv, kk)), d2);
+                                }
+                            }
                         }
+                        part[r] = d2.x + d2.y;
                     }
-                    rowa += sb;
-                    if (rowa >= ring_lo + ring_span) rowa -= ring_span;
+                    warp_reduce_scatter<4>(part, lane);
+                    // lane l holds element l >> 3
+                    if ((lane & 7) == 0 && c0 + (lane >> 3) < gs)
+                        red[(rbuf * red_rows + g0 + c0 + (lane >> 3)) * kRedPitch + warp] = part[0];
                 }
-                part[r] = d2.x + d2.y;
+                if (!a.resident) {
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive_after(empty_s + 8u * k, dep);
+                }
+                next_chunk(k, ph, base);
             }
-            __syncwarp();
-            for (int r = 0; r < cn; ++r) {
-                if (!a.resident && lane == 0) mbar_arrive_s(empty_s + 8u * dc.slot);
-                dc.next(sb, slots, ring_lo);
+            if (!a.resident) {
+                ck = k;
+                cphase = ph;
+                cbase = base;
             }
-            warp_reduce_scatter<4>(part, lane);
-            // lane l holds element l >> 3
-            if ((lane & 7) == 0 && c0 + (lane >> 3) < S)
-                red[(rbuf * red_rows + c0 + (lane >> 3)) * kRedPitch + warp] = part[0];
         }
-        if (!a.resident) cur = dc;
         named_bar_sync(1, nct);
 
         // ---- per-source coefficients, computed by every warp (identically)
@@ -448,54 +482,66 @@ __global__ void __launch_bounds__(max_threads_for(VPT), 1) attnres_bwd_kernel(co
         }
 
         // ---- write pass: dv_s rows and dq contributions
-        RingCursor wcur = a.resident ? vcur : cur;
-        char* dbase_n = nullptr;
-        const long long row_off = n * dld_b + d_off;
+        {
+            int k = a.resident ? tk_ck : ck;
+            uint32_t ph = a.resident ? tk_phase : cphase;
+            uint32_t base = a.resident ? tk_base : cbase;
+            const long long row_off = n * dld_b + d_off;
+            for (int g0 = 0; g0 < S; g0 += G) {
+                const int gs = min(G, S - g0);
+                if (!a.resident) mbar_wait_s(full_s + 8u * k, ph, abort_flag, &g_bwd_error, kSiteBwdConsumer);
+                uint32_t dep = 0;
+                uint32_t rowa = base;
 #pragma unroll 2
-        for (int s = 0; s < S; ++s) {
-            if (!a.resident)
-                mbar_wait_s(full_s + 8u * wcur.slot, wcur.phase, abort_flag, &g_bwd_error, kSiteBwdConsumer);
-            float al, k1, k2;
-            if (S <= 32) {
-                al = __shfl_sync(0xffffffffu, cal[0], s);
-                k1 = __shfl_sync(0xffffffffu, ck1[0], s);
-                k2 = __shfl_sync(0xffffffffu, ck2[0], s);
-            } else {
-                const int j = s >> 5;
-                al = __shfl_sync(0xffffffffu, j == 0 ? cal[0] : j == 1 ? cal[1] : j == 2 ? cal[2] : cal[3], s & 31);
-                k1 = __shfl_sync(0xffffffffu, j == 0 ? ck1[0] : j == 1 ? ck1[1] : j == 2 ? ck1[2] : ck1[3], s & 31);
-                k2 = __shfl_sync(0xffffffffu, j == 0 ? ck2[0] : j == 1 ? ck2[1] : j == 2 ? ck2[2] : ck2[3], s & 31);
-            }
-            const float2 al2 = make_float2(al, al), k12 = make_float2(k1, k1), k22 = make_float2(k2, k2);
-            dbase_n = static_cast<char*>(a.dsrc[s]) + row_off;
+                for (int r = 0; r < gs; ++r) {
+                    const int s = g0 + r;
+                    float al, k1, k2;
+                    if (S <= 32) {
+                        al = __shfl_sync(0xffffffffu, cal[0], s);
+                        k1 = __shfl_sync(0xffffffffu, ck1[0], s);
+                        k2 = __shfl_sync(0xffffffffu, ck2[0], s);
+                    } else {
+                        const int j = s >> 5;
+                        al = __shfl_sync(0xffffffffu, j == 0 ? cal[0] : j == 1 ? cal[1] : j == 2 ? cal[2] : cal[3], s & 31);
+                        k1 = __shfl_sync(0xffffffffu, j == 0 ? ck1[0] : j == 1 ? ck1[1] : j == 2 ? ck1[2] : ck1[3], s & 31);
+                        k2 = __shfl_sync(0xffffffffu, j == 0 ? ck2[0] : j == 1 ? ck2[1] : j == 2 ? ck2[2] : ck2[3], s & 31);
+                    }
+                    const float2 al2 = make_float2(al, al), k12 = make_float2(k1, k1), k22 = make_float2(k2, k2);
+                    char* drow = static_cast<char*>(a.dsrc[s]) + row_off;
 #pragma unroll
-            for (int i = 0; i < VPT; ++i) {
-                if (col[i] >= 0) {
-                    float2 dv[4];
+                    for (int i = 0; i < VPT; ++i) {
+                        if (col[i] >= 0) {
+                            float2 dv[4];
 #pragma unroll
-                    for (int k = 0; k < 4; ++k) dv[k] = fmul2(al2, dout[i][k]);
-                    if (KEYALL || kmask[i] != 0u) {
-                        const uint4 xv = lds128(wcur.row + i * vstep);
+                            for (int kk = 0; kk < 4; ++kk) dv[kk] = fmul2(al2, dout[i][kk]);
+                            if (KEYALL || kmask[i] != 0u) {
+                                const uint4 xv = lds128(rowa + i * vstep);
+                                dep ^= xv.x;
 #pragma unroll
-                        for (int k = 0; k < 4; ++k) {
-                            float2 x = bf2_to_f2(u4_get(xv, k));
-                            if (!KEYALL && kmask[i] != 0xffu) {
-                                if (!((kmask[i] >> (2 * k)) & 1u)) x.x = 0.0f;
-                                if (!((kmask[i] >> (2 * k + 1)) & 1u)) x.y = 0.0f;
+                                for (int kk = 0; kk < 4; ++kk) {
+                                    float2 x = bf2_to_f2(u4_get(xv, kk));
+                                    if (!KEYALL && kmask[i] != 0xffu) {
+                                        if (!((kmask[i] >> (2 * kk)) & 1u)) x.x = 0.0f;
+                                        if (!((kmask[i] >> (2 * kk + 1)) & 1u)) x.y = 0.0f;
+                                    }
+                                    dv[kk] = ffma2(k12, qs[i][kk], ffma2(k22, x, dv[kk]));
+                                    dq_acc[i][kk] = ffma2(k12, x, dq_acc[i][kk]);
+                                }
                             }
-                            dv[k] = ffma2(k12, qs[i][k], ffma2(k22, x, dv[k]));
-                            dq_acc[i][k] = ffma2(k12, x, dq_acc[i][k]);
+                            st_global_cs_v4(drow + static_cast<long long>(i) * vstep,
+                                            make_uint4(pack_f2(dv[0]), pack_f2(dv[1]), pack_f2(dv[2]), pack_f2(dv[3])));
                         }
                     }
-                    st_global_cs_v4(dbase_n + static_cast<long long>(i) * vstep,
-                                    make_uint4(pack_f2(dv[0]), pack_f2(dv[1]), pack_f2(dv[2]), pack_f2(dv[3])));
+                    rowa += sb;
                 }
+                __syncwarp();
+                if (lane == 0) mbar_arrive_after(empty_s + 8u * k, dep);
+                next_chunk(k, ph, base);
             }
-            __syncwarp();
-            if (lane == 0) mbar_arrive_s(empty_s + 8u * wcur.slot);
-            wcur.next(sb, slots, ring_lo);
+            ck = k;
+            cphase = ph;
+            cbase = base;
         }
-        cur = wcur;
     }
 
     // ---------------------------------------------- per-CTA partial sums

@@ -9,11 +9,12 @@
 // GB300 mapping.  One persistent CTA per SM walks tokens n = blockIdx.x,
 // blockIdx.x + gridDim.x, ...  A producer thread streams every source row of
 // the token into a ring of shared-memory row slots with 1-D TMA bulk copies
-// (one cp.async.bulk per row, completion counted on an mbarrier).  Consumer
-// thread t owns the 16-byte column vectors t, t + 32*ncw, ... of every row,
-// so each warp reads 512 contiguous bytes per shared load.  Sources are taken
-// in groups of up to 32 rows that stay resident together: the consumers wait
-// for the whole group, then pass 1 accumulates the key sum of squares and
+// (one cp.async.bulk per row).  The ring is organised in chunks of G rows
+// with one "full" and one "empty" mbarrier each, so waits and releases cost
+// one barrier operation per G rows.  Consumer thread t owns the 16-byte
+// column vectors t, t + 32*ncw, ... of every row, so each warp reads 512
+// contiguous bytes per shared load.  A chunk is one softmax group: the
+// consumers wait for it once, then pass 1 accumulates the key sum of squares and
 // the query dot four rows at a time (packed FP32 FMAs, independent chains),
 // each four-row chunk ends with a warp reduce-scatter, one cross-warp step
 // gives the group's logits, every warp updates the running softmax maximum
@@ -52,9 +53,9 @@ __global__ void __launch_bounds__(max_threads_for(VPT), 1) attnres_fwd_kernel(co
     extern __shared__ __align__(128) unsigned char smem[];
     const int ncw = a.ncw;
     const int nct = ncw * 32;
-    const int slots = a.slots;
-    const SmemLayout L = make_layout(slots, a.slot_bytes, ncw, a.s_pad, false);
-    unsigned char* ring = smem + L.ring;
+    const int K = a.chunks;  // ring depth in chunks
+    const int G = a.rows;    // rows per chunk = softmax group
+    const SmemLayout L = make_layout(K, G, a.slot_bytes, 0, a.s_pad, false);
     uint64_t* full = reinterpret_cast<uint64_t*>(smem + L.full);
     uint64_t* empty = reinterpret_cast<uint64_t*>(smem + L.empty);
     float* red = reinterpret_cast<float*>(smem + L.red);     // [2][red_rows][kRedPitch]
@@ -66,9 +67,11 @@ __global__ void __launch_bounds__(max_threads_for(VPT), 1) attnres_fwd_kernel(co
     const int lane = threadIdx.x & 31;
     const long long N = a.N;
     const int S = a.S;
+    const uint32_t sb = static_cast<uint32_t>(a.slot_bytes);
+    const uint32_t cb = static_cast<uint32_t>(G) * sb;  // chunk bytes
 
     if (threadIdx.x == 0) {
-        for (int k = 0; k < slots; ++k) {
+        for (int k = 0; k < K; ++k) {
             mbar_init(full + k, 1);
             mbar_init(empty + k, ncw);
         }
@@ -82,27 +85,33 @@ __global__ void __launch_bounds__(max_threads_for(VPT), 1) attnres_fwd_kernel(co
         if (lane == 0) {
             const uint64_t pol = policy_evict_first();
             const uint32_t bytes = static_cast<uint32_t>(a.D) * 2u;
-            int slot = 0;
+            unsigned char* ring = smem + L.ring;
+            int k = 0;
             uint32_t phase = 0;
-            long long issued = 0;
+            long long issued = 0;  // chunk fills started
             for (long long n = blockIdx.x; n < N && !*abort_flag; n += gridDim.x) {
-                for (int s = 0; s < S; ++s) {
-                    if (!mbar_wait(empty + slot, phase ^ 1u, abort_flag, &g_fwd_error, kSiteFwdProducer)) break;
-                    mbar_arrive_expect_tx(full + slot, bytes);
-                    const unsigned char* src =
-                        static_cast<const unsigned char*>(a.src[s]) + (n * a.src_ld) * 2;
-                    tma_load_1d(ring + static_cast<size_t>(slot) * a.slot_bytes, src, bytes,
-                                full + slot, pol);
+                for (int g0 = 0; g0 < S; g0 += G) {
+                    const int gs = min(G, S - g0);
+                    if (!mbar_wait(empty + k, phase ^ 1u, abort_flag, &g_fwd_error, kSiteFwdProducer)) break;
+                    mbar_arrive_expect_tx(full + k, bytes * static_cast<uint32_t>(gs));
+                    for (int r = 0; r < gs; ++r) {
+                        const unsigned char* src =
+                            static_cast<const unsigned char*>(a.src[g0 + r]) + (n * a.src_ld) * 2;
+                        tma_load_1d(ring + k * cb + r * sb, src, bytes, full + k, pol);
+                    }
                     ++issued;
-                    advance(slot, phase, slots);
+                    if (++k == K) {
+                        k = 0;
+                        phase ^= 1u;
+                    }
                 }
             }
             if (*abort_flag) {
                 // Let every copy this thread started land before the CTA can exit.
-                for (int k = 0; k < slots && k < issued; ++k) {
-                    const long long fills = (issued - 1 - k) / slots + 1;
+                for (int c = 0; c < K && c < issued; ++c) {
+                    const long long fills = (issued - 1 - c) / K + 1;
                     volatile int no_abort = 0;
-                    mbar_wait(full + k, static_cast<uint32_t>((fills - 1) & 1), &no_abort, &g_fwd_error, kSiteDrain);
+                    mbar_wait(full + c, static_cast<uint32_t>((fills - 1) & 1), &no_abort, &g_fwd_error, kSiteDrain);
                 }
             }
         }
@@ -123,20 +132,20 @@ __global__ void __launch_bounds__(max_threads_for(VPT), 1) attnres_fwd_kernel(co
         unsigned m = 0;
         uint32_t qw[4], ww[4];
 #pragma unroll
-        for (int k = 0; k < 4; ++k) {
+        for (int kk = 0; kk < 4; ++kk) {
             uint32_t qv = 0, wv = 0;
 #pragma unroll
             for (int h = 0; h < 2; ++h) {
-                const int j = 8 * c + 2 * k + h;
+                const int j = 8 * c + 2 * kk + h;
                 const bool in_key = col[i] >= 0 && j >= ko && j < kend;
-                m |= in_key ? (1u << (2 * k + h)) : 0u;
+                m |= in_key ? (1u << (2 * kk + h)) : 0u;
                 const uint32_t qh = in_key ? a.q[j - ko] : 0u;
                 const uint32_t wh = (a.out_norm && col[i] >= 0) ? a.w_o[j] : 0x3f80u;
                 qv |= qh << (16 * h);
                 wv |= wh << (16 * h);
             }
-            qw[k] = qv;
-            ww[k] = wv;
+            qw[kk] = qv;
+            ww[kk] = wv;
         }
         kmask[i] = m;
         qb[i] = make_uint4(qw[0], qw[1], qw[2], qw[3]);
@@ -144,16 +153,13 @@ __global__ void __launch_bounds__(max_threads_for(VPT), 1) attnres_fwd_kernel(co
     }
     const float inv_r = 1.0f / static_cast<float>(a.R);
     const float inv_d = 1.0f / static_cast<float>(a.D);
-    const int G = a.group;  // rows per group (<= 32, <= slots)
 
-    // 32-bit shared addresses; the cursor's row address already includes
-    // this thread's first vector offset.
+    // 32-bit shared addresses; chunk row addresses include this thread's
+    // first vector offset.
     const uint32_t sbase = smem_u32(smem);
     const uint32_t voff = static_cast<uint32_t>(col[0] < 0 ? 0 : col[0]) * 16u;
     const uint32_t vstep = static_cast<uint32_t>(nct) * 16u;  // between a thread's vectors
-    const uint32_t sb = static_cast<uint32_t>(a.slot_bytes);
     const uint32_t ring_lo = sbase + L.ring + voff;
-    const uint32_t ring_span = static_cast<uint32_t>(slots) * sb;
     const uint32_t full_s = sbase + L.full;
     const uint32_t empty_s = sbase + L.empty;
     const uint32_t red_s = sbase + L.red;
@@ -164,11 +170,8 @@ __global__ void __launch_bounds__(max_threads_for(VPT), 1) attnres_fwd_kernel(co
     for (int k = threadIdx.x; k < 2 * red_rows * kRedPitch; k += nct) red[k] = 0.0f;
     named_bar_sync(1, nct);
 
-    auto red_addr = [&](int buf, int row, int w) -> uint32_t {
-        return red_s + static_cast<uint32_t>(((buf * red_rows + row) * kRedPitch + w) * 4);
-    };
     auto red_sum = [&](int buf, int row) -> float {
-        const uint32_t base = red_addr(buf, row, 0);
+        const uint32_t base = red_s + static_cast<uint32_t>(((buf * red_rows + row) * kRedPitch) * 4);
         float t = 0.0f;
         for (int q4 = 0; q4 < nq; ++q4) {
             const float4 v = lds128f(base + 16u * q4);
@@ -177,7 +180,9 @@ __global__ void __launch_bounds__(max_threads_for(VPT), 1) attnres_fwd_kernel(co
         return t;
     };
 
-    RingCursor cur{ring_lo, 0, 0u};
+    int ck = 0;            // current chunk
+    uint32_t cphase = 0;   // its fill parity
+    uint32_t cbase = ring_lo;
     int rbuf = 0;
 
     for (long long n = blockIdx.x; n < N; n += gridDim.x) {
@@ -185,44 +190,37 @@ __global__ void __launch_bounds__(max_threads_for(VPT), 1) attnres_fwd_kernel(co
 #pragma unroll
         for (int i = 0; i < VPT; ++i)
 #pragma unroll
-            for (int k = 0; k < 4; ++k) acc[i][k] = make_float2(0.0f, 0.0f);
+            for (int kk = 0; kk < 4; ++kk) acc[i][kk] = make_float2(0.0f, 0.0f);
         float m_run = -FLT_MAX;  // running softmax maximum (same in every warp)
         float l_run = 0.0f;      // running softmax denominator
 
         for (int g0 = 0; g0 < S; g0 += G) {
             const int gs = min(G, S - g0);
-            const RingCursor gcur = cur;
-            // wait for the whole group, then compute without interruptions
-            for (int s = 0; s < gs; ++s) {
-                mbar_wait_s(full_s + 8u * cur.slot, cur.phase, abort_flag, &g_fwd_error, kSiteFwdConsumer);
-                cur.next(sb, slots, ring_lo);
-            }
+            mbar_wait_s(full_s + 8u * ck, cphase, abort_flag, &g_fwd_error, kSiteFwdConsumer);
             // pass 1: key sum of squares and query dot, four rows at a time
-            uint32_t rowa = gcur.row;
             for (int c0 = 0; c0 < gs; c0 += 4) {
                 float part[8];
 #pragma unroll
                 for (int r = 0; r < 4; ++r) {
                     float2 ss2 = make_float2(0.0f, 0.0f), qt2 = make_float2(0.0f, 0.0f);
                     if (c0 + r < gs) {
+                        const uint32_t rowa = cbase + static_cast<uint32_t>(c0 + r) * sb;
 #pragma unroll
                         for (int i = 0; i < VPT; ++i) {
                             if (KEYALL ? (col[i] >= 0) : (kmask[i] != 0u)) {
                                 const uint4 xv = lds128(rowa + i * vstep);
 #pragma unroll
-                                for (int k = 0; k < 4; ++k) {
-                                    float2 x = bf2_to_f2(u4_get(xv, k));
+                                for (int kk = 0; kk < 4; ++kk) {
+                                    float2 x = bf2_to_f2(u4_get(xv, kk));
                                     if (!KEYALL && kmask[i] != 0xffu) {
-                                        if (!((kmask[i] >> (2 * k)) & 1u)) x.x = 0.0f;
-                                        if (!((kmask[i] >> (2 * k + 1)) & 1u)) x.y = 0.0f;
+                                        if (!((kmask[i] >> (2 * kk)) & 1u)) x.x = 0.0f;
+                                        if (!((kmask[i] >> (2 * kk + 1)) & 1u)) x.y = 0.0f;
                                     }
                                     ss2 = ffma2(x, x, ss2);
-                                    qt2 = ffma2(bf2_to_f2(u4_get(qb[i], k)), x, qt2);
+                                    qt2 = ffma2(bf2_to_f2(u4_get(qb[i], kk)), x, qt2);
                                 }
                             }
                         }
-                        rowa += sb;
-                        if (rowa >= ring_lo + ring_span) rowa -= ring_span;
                     }
                     part[r] = ss2.x + ss2.y;
                     part[4 + r] = qt2.x + qt2.y;
@@ -266,23 +264,31 @@ __global__ void __launch_bounds__(max_threads_for(VPT), 1) attnres_fwd_kernel(co
 #pragma unroll
             for (int i = 0; i < VPT; ++i)
 #pragma unroll
-                for (int k = 0; k < 4; ++k) acc[i][k] = fmul2(acc[i][k], corr2);
-            RingCursor pc = gcur;
+                for (int kk = 0; kk < 4; ++kk) acc[i][kk] = fmul2(acc[i][kk], corr2);
+            uint32_t dep = 0;
+            uint32_t rowa = cbase;
 #pragma unroll 2
-            for (int s = 0; s < gs; ++s) {
-                const float es = __shfl_sync(0xffffffffu, e, s);
+            for (int r = 0; r < gs; ++r) {
+                const float es = __shfl_sync(0xffffffffu, e, r);
                 const float2 es2 = make_float2(es, es);
 #pragma unroll
                 for (int i = 0; i < VPT; ++i) {
                     if (col[i] >= 0) {
-                        const uint4 xv = lds128(pc.row + i * vstep);
+                        const uint4 xv = lds128(rowa + i * vstep);
+                        dep ^= xv.x;
 #pragma unroll
-                        for (int k = 0; k < 4; ++k) acc[i][k] = ffma2(es2, bf2_to_f2(u4_get(xv, k)), acc[i][k]);
+                        for (int kk = 0; kk < 4; ++kk) acc[i][kk] = ffma2(es2, bf2_to_f2(u4_get(xv, kk)), acc[i][kk]);
                     }
                 }
-                __syncwarp();
-                if (lane == 0) mbar_arrive_s(empty_s + 8u * pc.slot);
-                pc.next(sb, slots, ring_lo);
+                rowa += sb;
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive_after(empty_s + 8u * ck, dep);
+            cbase += G * sb;
+            if (++ck == K) {
+                ck = 0;
+                cbase = ring_lo;
+                cphase ^= 1u;
             }
         }
         const float inv_l = 1.0f / l_run;
@@ -291,14 +297,14 @@ __global__ void __launch_bounds__(max_threads_for(VPT), 1) attnres_fwd_kernel(co
 #pragma unroll
         for (int i = 0; i < VPT; ++i)
 #pragma unroll
-            for (int k = 0; k < 4; ++k) acc[i][k] = fmul2(acc[i][k], inv_l2);
+            for (int kk = 0; kk < 4; ++kk) acc[i][kk] = fmul2(acc[i][kk], inv_l2);
         if (a.out_norm) {
             float2 ss2 = make_float2(0.0f, 0.0f);
 #pragma unroll
             for (int i = 0; i < VPT; ++i)
                 if (col[i] >= 0)
 #pragma unroll
-                    for (int k = 0; k < 4; ++k) ss2 = ffma2(acc[i][k], acc[i][k], ss2);
+                    for (int kk = 0; kk < 4; ++kk) ss2 = ffma2(acc[i][kk], acc[i][kk], ss2);
             const float ss = warp_sum(ss2.x + ss2.y);
             if (lane == 0) red[(rbuf * red_rows) * kRedPitch + warp] = ss;
             named_bar_sync(1, nct);
@@ -315,8 +321,8 @@ __global__ void __launch_bounds__(max_threads_for(VPT), 1) attnres_fwd_kernel(co
             if (col[i] >= 0) {
                 uint32_t yw[4];
 #pragma unroll
-                for (int k = 0; k < 4; ++k)
-                    yw[k] = pack_f2(fmul2(fmul2(acc[i][k], rho2), bf2_to_f2(u4_get(wb[i], k))));
+                for (int kk = 0; kk < 4; ++kk)
+                    yw[kk] = pack_f2(fmul2(fmul2(acc[i][kk], rho2), bf2_to_f2(u4_get(wb[i], kk))));
                 st_global_cs_v4(yrow + 8 * col[i], make_uint4(yw[0], yw[1], yw[2], yw[3]));
                 if (prow) {
                     st_global_cs_v4(prow + 8 * col[i],

@@ -312,6 +312,16 @@ __device__ __forceinline__ float4 lds128f(uint32_t addr) {
     return v;
 }
 
+
+// Arrive on a slot's "empty" barrier once the shared-memory loads that read
+// the slot have returned their data: `dep` must be computed from every one
+// of those loads, so the arrive cannot issue while a load is in flight (a
+// later bulk copy into the slot would otherwise race with it).
+__device__ __forceinline__ void mbar_arrive_after(uint32_t bar, uint32_t dep) {
+    asm volatile("mbarrier.arrive.release.cta.shared::cta.b64 _, [%0];" ::"r"(bar), "r"(dep)
+                 : "memory");
+}
+
 // Position in the shared-memory row ring: row address, slot index, phase.
 struct RingCursor {
     uint32_t row;

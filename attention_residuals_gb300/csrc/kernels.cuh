@@ -16,7 +16,7 @@ constexpr int kMaxConsumerWarps = 16;
 // footprints keep 8 consumer warps (registers <= 168).
 __host__ __device__ constexpr int max_threads_for(int vpt) { return vpt == 1 ? 17 * 32 : 9 * 32; }
 __host__ __device__ constexpr int max_warps_for(int vpt) { return vpt == 1 ? 16 : 8; }
-constexpr int kMaxSlots = 64;
+constexpr int kMaxChunks = 32;
 constexpr int kTokSlots = 4;      // token-statistics ring depth (backward)
 constexpr int kGroupTicket = 12;  // CTAs per first-level group of the in-kernel reduction
 constexpr int kMaxGroup = 32;     // forward rows reduced together
@@ -31,29 +31,33 @@ enum WaitSite : unsigned {
     kSiteDrain = 6,
 };
 
-// Launch plan: one persistent CTA per SM; `ncw` consumer warps each own
-// `vpt` 16-byte column vectors of every row; a ring of `slots` row buffers
-// of `slot_bytes` each is filled by one producer thread with 1-D TMA copies.
+// Launch plan: one persistent CTA per SM.  `ncw` consumer warps each own
+// `vpt` 16-byte column vectors of every row.  Source rows stream through a
+// ring of `chunks` chunks; a chunk holds up to `rows` source rows of
+// `slot_bytes` each and has one "full" and one "empty" mbarrier, so waits
+// and releases are per chunk, not per row.  The backward also has a ring of
+// `dy_slots` single-row slots for dy.
 struct Plan {
     int grid;
     int ncw;
     int vpt;
-    int slots;
     int slot_bytes;
-    int group;        // forward rows resident and reduced together (<= kMaxGroup)
-    int resident;     // backward keeps a token's rows between its two passes
-    int split;        // backward reduction via the finalize kernel
-    int s_pad;        // S rounded up to 4
+    int s_pad;
+    int f_rows, f_chunks;    // forward: rows per chunk (= softmax group), ring depth
+    int b_rows, b_chunks;    // backward
+    int dy_slots;
+    int resident;            // backward keeps a token's rows between its passes
+    int split;               // backward reduction via the finalize kernel
     size_t smem_fwd;
     size_t smem_bwd;
-    size_t ws_bytes;  // backward workspace
+    size_t ws_bytes;         // backward workspace
     size_t ws_part_off, ws_gpart_off;
     int ngroups;
 };
 
 // Byte offsets inside the dynamic shared memory of one CTA.
 struct SmemLayout {
-    uint32_t ring, full, empty, tfull, tempty, red, tok, coef, misc, total;
+    uint32_t ring, dyring, full, empty, dyfull, dyempty, tfull, tempty, red, tok, coef, misc, total;
     int red_rows;  // rows of the reduction scratch (per buffer)
 };
 
@@ -64,19 +68,25 @@ constexpr int kRedPitch = 20;
 
 __host__ __device__ inline uint32_t align_up(uint32_t x, uint32_t a) { return (x + a - 1) / a * a; }
 
-// coef holds per-token vectors: forward z[s_pad], rstd[s_pad]; backward
-// nothing (its per-source coefficients live in registers).
-__host__ __device__ inline SmemLayout make_layout(int slots, int slot_bytes, int ncw, int s_pad,
-                                                  bool backward) {
+// Forward: chunk ring, z[s_pad] and rstd[s_pad] of the current token.
+// Backward: chunk ring, dy ring, token-statistics ring.
+__host__ __device__ inline SmemLayout make_layout(int chunks, int rows, int slot_bytes, int dy_slots,
+                                                  int s_pad, bool backward) {
     SmemLayout L;
     uint32_t off = 0;
     L.ring = off;
-    off += static_cast<uint32_t>(slots) * static_cast<uint32_t>(slot_bytes);
+    off += static_cast<uint32_t>(chunks) * static_cast<uint32_t>(rows) * static_cast<uint32_t>(slot_bytes);
+    L.dyring = off;
+    off += backward ? static_cast<uint32_t>(dy_slots) * static_cast<uint32_t>(slot_bytes) : 0u;
     off = align_up(off, 16);
     L.full = off;
-    off += 8u * slots;
+    off += 8u * chunks;
     L.empty = off;
-    off += 8u * slots;
+    off += 8u * chunks;
+    L.dyfull = off;
+    off += backward ? 8u * dy_slots : 0u;
+    L.dyempty = off;
+    off += backward ? 8u * dy_slots : 0u;
     L.tfull = off;
     off += backward ? 8u * kTokSlots : 0u;
     L.tempty = off;
@@ -85,7 +95,6 @@ __host__ __device__ inline SmemLayout make_layout(int slots, int slot_bytes, int
     L.red = off;
     L.red_rows = s_pad > 64 ? s_pad : 64;
     off += 2u * static_cast<uint32_t>(L.red_rows) * kRedPitch * 4u;
-    (void)ncw;
     L.tok = off;
     off += backward ? static_cast<uint32_t>(kTokSlots) * (3u * s_pad + 4u) * 4u : 0u;
     L.coef = off;
@@ -102,7 +111,7 @@ struct FwdArgs {
     long long src_ld;
     int S, D, R, ko, out_norm;
     float eps, scale;
-    int slots, slot_bytes, ncw, s_pad, group;
+    int chunks, rows, slot_bytes, ncw, s_pad;
     const uint16_t* q;
     const uint16_t* w_o;
     uint16_t* y;
@@ -120,7 +129,7 @@ struct BwdArgs {
     long long src_ld, dsrc_ld;
     int S, D, R, ko, out_norm;
     float eps, scale;
-    int slots, slot_bytes, ncw, s_pad, resident, split, ngroups;
+    int chunks, rows, slot_bytes, dy_slots, ncw, s_pad, resident, split, ngroups;
     const uint16_t* q;
     const uint16_t* w_o;
     const uint16_t* dy;

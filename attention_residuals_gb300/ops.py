@@ -123,7 +123,7 @@ def _check_vec(t: Optional[torch.Tensor], n: int, name: str):
 # --------------------------------------------------------------------------
 # C-ABI mirrors
 # --------------------------------------------------------------------------
-_PLAN_KEYS = ["grid", "consumer_warps", "vectors_per_thread", "ring_slots", "fwd_group",
+_PLAN_KEYS = ["grid", "consumer_warps", "vectors_per_thread", "bwd_ring", "fwd_ring",
               "bwd_resident", "bwd_smem_bytes", "bwd_split"]
 
 

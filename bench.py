@@ -395,8 +395,8 @@ def run_ours(args):
         "vs_baseline": None,
         "dtype": "bf16",
         "data": "synthetic",
-        "config": {"workload": "S=10 N=32768 D=4096 R=4096 key_offset=0 out-norm bf16 "
-                               "(long-sequence, split-N reduction)",
+        "config": {"workload": f"S={S} N={N} D={D} R={R} key_offset={wl.key_offset} out-norm bf16 "
+                               f"(long-sequence, {'split-N' if info['bwd_split'] else 'in-kernel'} reduction)",
                    "bytes_per_step": nbytes["total"],
                    "fwd_ms": fwd_ms, "bwd_ms": bwd_ms,
                    "frac_of_peak_step": value / world / peak,

@@ -165,11 +165,12 @@ const char* attnres_status_string(attnres_status s);
 /*
  * Launch plan the library would use for these params on the current device
  * (for tests and benchmarks; no launch happens).  Fills out[0..7] with:
- * grid CTAs, consumer warps, vectors per thread, ring slots, forward group
- * size, backward resident flag (1 = source rows stay in shared memory
- * between the two backward passes), dynamic shared memory bytes of the
- * backward kernel, and the backward reduction path (0 = in-kernel,
- * 1 = finalize kernel).
+ * grid CTAs, consumer warps, 16-byte vectors per thread, the backward ring
+ * (chunks * 1000 + rows per chunk), the forward ring (chunks * 1000 + rows
+ * per chunk = softmax group), the backward resident flag (1 = a token's
+ * source rows stay in shared memory for all backward passes), dynamic
+ * shared memory bytes of the backward kernel, and the backward reduction
+ * path (0 = in-kernel, 1 = finalize kernel).
  */
 attnres_status attnres_plan_info(const attnres_params* p, int64_t out[8]);
 

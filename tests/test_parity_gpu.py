@@ -88,13 +88,33 @@ def test_streaming_backward_many_sources(save_o_pre):
     fwd = attnres_fwd(v, q, w_o=w, key_offset=1024, save_o_pre=save_o_pre)
     assert (fwd["o_pre"] is not None) == (save_o_pre is not False)
     bwd = attnres_bwd(v, q, dy, fwd, w_o=w, key_offset=1024)
+    bwd2 = attnres_bwd(v, q, dy, fwd, w_o=w, key_offset=1024)
     torch.cuda.synchronize()
+    for key in ("dvalues", "dq_f32", "dw_o_f32"):
+        assert torch.equal(bwd[key], bwd2[key]), key
     ref = attnres_oracle(wl.values, wl.q, w_o=wl.w_o, dy=wl.dy, key_offset=1024)
     check_forward(fwd, ref, out_norm=True, tag="S64 streaming")
     check_backward(bwd, ref, out_norm=True, tag="S64 streaming")
     if fwd["o_pre"] is not None:
         o_ref = ref["y"] / (wl.w_o.double().numpy() * ref["o_rstd"][:, None])
         assert rel_l2(to_np(fwd["o_pre"]), o_ref) < 1e-5
+
+
+@pytest.mark.parametrize("S,D,outn", [(24, 8192, True), (40, 6144, False), (130 // 2, 2048, True)])
+def test_streaming_wide_rows_deterministic(S, D, outn):
+    # rows too many to stay resident; 4 vectors per thread for D > 4096
+    wl = make_random(S, 70, D, out_norm=outn, seed=S + D)
+    v, q, w, dy = cuda_copy(wl)
+    info = attnres_plan_info(v, D, key_offset=0, out_norm=outn)
+    fwd = attnres_fwd(v, q, w_o=w, key_offset=0)
+    outs = [attnres_bwd(v, q, dy, fwd, w_o=w, key_offset=0) for _ in range(3)]
+    torch.cuda.synchronize()
+    for b in outs[1:]:
+        assert torch.equal(b["dvalues"], outs[0]["dvalues"])
+        assert torch.equal(b["dq_f32"], outs[0]["dq_f32"])
+    ref = attnres_oracle(wl.values, wl.q, w_o=wl.w_o, dy=wl.dy, key_offset=0)
+    check_forward(fwd, ref, out_norm=outn, tag=f"S{S} D{D} {info}")
+    check_backward(outs[0], ref, out_norm=outn, tag=f"S{S} D{D} {info}")
 
 
 def test_resident_backward_with_saved_o_pre():
