@@ -94,6 +94,11 @@ attnres_status make_plan(const attnres_params* p, Plan* plan) {
         pl.f_rows = (S + groups - 1) / groups;
         pl.f_chunks = max_chunks(pl.f_rows, 0, false);
         if (pl.f_chunks < 2) return ATTNRES_ERR_UNSUPPORTED;
+        // A softmax group spans whole chunks and leaves two chunks loading.
+        int gc = pl.f_chunks - 2;
+        if (gc < 1) gc = 1;
+        while (gc > 1 && gc * pl.f_rows > kMaxGroup) --gc;
+        pl.f_group = gc * pl.f_rows;
     }
     // Backward: dy ring, then either a resident token (its rows in two
     // chunks, at most ~60% of the ring so the next token can load meanwhile)
@@ -211,6 +216,7 @@ attnres_status attnres_fwd(const attnres_params* p, const void* q, const void* w
     a.scale = p->scale;
     a.chunks = pl.f_chunks;
     a.rows = pl.f_rows;
+    a.group = pl.f_group;
     a.slot_bytes = pl.slot_bytes;
     a.ncw = pl.ncw;
     a.s_pad = pl.s_pad;
@@ -294,6 +300,18 @@ attnres_status attnres_bwd(const attnres_params* p, const void* q, const void* w
     a.N = p->N;
     a.src_ld = p->src_ld;
     a.dsrc_ld = dsrc_ld;
+    {
+        // evenly spaced output rows (a packed [S, N, D] gradient) let the
+        // kernel step from one source's row to the next with one add
+        const long long st = p->S > 1 ? static_cast<long long>(reinterpret_cast<uintptr_t>(dsrc[1])) -
+                                            static_cast<long long>(reinterpret_cast<uintptr_t>(dsrc[0]))
+                                      : 0;
+        bool even = p->S > 1 && st != 0;
+        for (int s2 = 2; even && s2 < p->S; ++s2)
+            even = static_cast<long long>(reinterpret_cast<uintptr_t>(dsrc[s2])) -
+                       static_cast<long long>(reinterpret_cast<uintptr_t>(dsrc[s2 - 1])) == st;
+        a.dsrc_stride = even ? st : 0;
+    }
     a.S = p->S;
     a.D = p->D;
     a.R = p->R;

@@ -48,7 +48,8 @@ __device__ unsigned int g_bwd_error = 0;
 __device__ __forceinline__ float ldcg_f32(const float* p) { return __ldcg(p); }
 
 // KEYALL: every channel is a key channel (R == D), so no per-vector masks.
-template <int VPT, bool KEYALL>
+// FULL: every consumer thread owns VPT whole vectors (D == 8 * VPT * 32 * ncw).
+template <int VPT, bool KEYALL, bool FULL>
 __global__ void __launch_bounds__(max_threads_for(VPT), 1) attnres_bwd_kernel(const __grid_constant__ BwdArgs a) {
     extern __shared__ __align__(128) unsigned char smem[];
     const int ncw = a.ncw;
@@ -339,7 +340,7 @@ __global__ void __launch_bounds__(max_threads_for(VPT), 1) attnres_bwd_kernel(co
                         const float2 al2 = make_float2(al, al);
 #pragma unroll
                         for (int i = 0; i < VPT; ++i) {
-                            if (col[i] >= 0) {
+                            if (FULL || col[i] >= 0) {
                                 const uint4 xv = lds128(rowa + i * vstep);
                                 dep ^= xv.x;
 #pragma unroll
@@ -412,7 +413,7 @@ __global__ void __launch_bounds__(max_threads_for(VPT), 1) attnres_bwd_kernel(co
                             const uint32_t rowa = base + static_cast<uint32_t>(c0 + r) * sb;
 #pragma unroll
                             for (int i = 0; i < VPT; ++i) {
-                                if (col[i] >= 0) {
+                                if (FULL || col[i] >= 0) {
                                     const uint4 xv = lds128(rowa + i * vstep);
                                     dep ^= xv.x;
 #pragma unroll
@@ -487,6 +488,8 @@ __global__ void __launch_bounds__(max_threads_for(VPT), 1) attnres_bwd_kernel(co
             uint32_t ph = a.resident ? tk_phase : cphase;
             uint32_t base = a.resident ? tk_base : cbase;
             const long long row_off = n * dld_b + d_off;
+            const long long dstride = a.dsrc_stride;
+            char* dnext = static_cast<char*>(a.dsrc[0]) + row_off;  // used when evenly spaced
             for (int g0 = 0; g0 < S; g0 += G) {
                 const int gs = min(G, S - g0);
                 if (!a.resident) mbar_wait_s(full_s + 8u * k, ph, abort_flag, &g_bwd_error, kSiteBwdConsumer);
@@ -507,10 +510,11 @@ __global__ void __launch_bounds__(max_threads_for(VPT), 1) attnres_bwd_kernel(co
                         k2 = __shfl_sync(0xffffffffu, j == 0 ? ck2[0] : j == 1 ? ck2[1] : j == 2 ? ck2[2] : ck2[3], s & 31);
                     }
                     const float2 al2 = make_float2(al, al), k12 = make_float2(k1, k1), k22 = make_float2(k2, k2);
-                    char* drow = static_cast<char*>(a.dsrc[s]) + row_off;
+                    char* drow = dstride ? dnext : static_cast<char*>(a.dsrc[s]) + row_off;
+                    dnext += dstride;
 #pragma unroll
                     for (int i = 0; i < VPT; ++i) {
-                        if (col[i] >= 0) {
+                        if (FULL || col[i] >= 0) {
                             float2 dv[4];
 #pragma unroll
                             for (int kk = 0; kk < 4; ++kk) dv[kk] = fmul2(al2, dout[i][kk]);
@@ -634,9 +638,9 @@ __global__ void __launch_bounds__(256) attnres_finalize_kernel(const float* __re
     }
 }
 
-template <int VPT, bool KEYALL>
+template <int VPT, bool KEYALL, bool FULL>
 cudaError_t launch_bwd_t(const Plan& plan, const BwdArgs& a, cudaStream_t stream) {
-    auto kern = attnres_bwd_kernel<VPT, KEYALL>;
+    auto kern = attnres_bwd_kernel<VPT, KEYALL, FULL>;
     cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                            static_cast<int>(plan.smem_bwd));
     if (err != cudaSuccess) return err;
@@ -651,8 +655,10 @@ cudaError_t launch_bwd_t(const Plan& plan, const BwdArgs& a, cudaStream_t stream
 
 template <int VPT>
 cudaError_t dispatch_key(const Plan& plan, const BwdArgs& a, cudaStream_t stream) {
-    return (a.R == a.D) ? launch_bwd_t<VPT, true>(plan, a, stream)
-                        : launch_bwd_t<VPT, false>(plan, a, stream);
+    const bool full = (a.D / 8) == VPT * 32 * plan.ncw;
+    if (a.R == a.D)
+        return full ? launch_bwd_t<VPT, true, true>(plan, a, stream) : launch_bwd_t<VPT, true, false>(plan, a, stream);
+    return full ? launch_bwd_t<VPT, false, true>(plan, a, stream) : launch_bwd_t<VPT, false, false>(plan, a, stream);
 }
 
 }  // namespace

@@ -13,8 +13,9 @@
 // with one "full" and one "empty" mbarrier each, so waits and releases cost
 // one barrier operation per G rows.  Consumer thread t owns the 16-byte
 // column vectors t, t + 32*ncw, ... of every row, so each warp reads 512
-// contiguous bytes per shared load.  A chunk is one softmax group: the
-// consumers wait for it once, then pass 1 accumulates the key sum of squares and
+// contiguous bytes per shared load.  A softmax group is a whole number of
+// chunks (the whole token when it fits beside two loading chunks): the
+// consumers wait for its chunks, then pass 1 accumulates the key sum of squares and
 // the query dot four rows at a time (packed FP32 FMAs, independent chains),
 // each four-row chunk ends with a warp reduce-scatter, one cross-warp step
 // gives the group's logits, every warp updates the running softmax maximum
@@ -48,13 +49,15 @@ __device__ __forceinline__ int ring_add(int slot, int k, int slots) {
 }
 
 // KEYALL: every channel is a key channel (R == D), so no per-vector masks.
-template <int VPT, bool KEYALL>
+// FULL: every consumer thread owns VPT whole vectors (D == 8 * VPT * 32 * ncw).
+template <int VPT, bool KEYALL, bool FULL>
 __global__ void __launch_bounds__(max_threads_for(VPT), 1) attnres_fwd_kernel(const __grid_constant__ FwdArgs a) {
     extern __shared__ __align__(128) unsigned char smem[];
     const int ncw = a.ncw;
     const int nct = ncw * 32;
     const int K = a.chunks;  // ring depth in chunks
-    const int G = a.rows;    // rows per chunk = softmax group
+    const int G = a.rows;    // rows per chunk
+    const int GG = a.group;  // softmax group rows (whole chunks)
     const SmemLayout L = make_layout(K, G, a.slot_bytes, 0, a.s_pad, false);
     uint64_t* full = reinterpret_cast<uint64_t*>(smem + L.full);
     uint64_t* empty = reinterpret_cast<uint64_t*>(smem + L.empty);
@@ -194,20 +197,39 @@ __global__ void __launch_bounds__(max_threads_for(VPT), 1) attnres_fwd_kernel(co
         float m_run = -FLT_MAX;  // running softmax maximum (same in every warp)
         float l_run = 0.0f;      // running softmax denominator
 
-        for (int g0 = 0; g0 < S; g0 += G) {
-            const int gs = min(G, S - g0);
-            mbar_wait_s(full_s + 8u * ck, cphase, abort_flag, &g_fwd_error, kSiteFwdConsumer);
-            // pass 1: key sum of squares and query dot, four rows at a time
+        for (int g0 = 0; g0 < S; g0 += GG) {
+            const int gs = min(GG, S - g0);
+            // wait for every chunk of the group (rows [g0, g0 + gs))
+            {
+                int k = ck;
+                uint32_t ph = cphase;
+                for (int r0 = 0; r0 < gs; r0 += G) {
+                    mbar_wait_s(full_s + 8u * k, ph, abort_flag, &g_fwd_error, kSiteFwdConsumer);
+                    if (++k == K) {
+                        k = 0;
+                        ph ^= 1u;
+                    }
+                }
+            }
+            // pass 1: key sum of squares and query dot, four rows at a time;
+            // (rb, ri) walks row addresses across the group's chunks
+            uint32_t rb = cbase;
+            int ri = 0;
             for (int c0 = 0; c0 < gs; c0 += 4) {
                 float part[8];
 #pragma unroll
                 for (int r = 0; r < 4; ++r) {
                     float2 ss2 = make_float2(0.0f, 0.0f), qt2 = make_float2(0.0f, 0.0f);
                     if (c0 + r < gs) {
-                        const uint32_t rowa = cbase + static_cast<uint32_t>(c0 + r) * sb;
+                        const uint32_t rowa = rb + static_cast<uint32_t>(ri) * sb;
+                        if (++ri == G) {
+                            ri = 0;
+                            rb += cb;
+                            if (rb == ring_lo + static_cast<uint32_t>(K) * cb) rb = ring_lo;
+                        }
 #pragma unroll
                         for (int i = 0; i < VPT; ++i) {
-                            if (KEYALL ? (col[i] >= 0) : (kmask[i] != 0u)) {
+                            if (KEYALL ? (FULL || col[i] >= 0) : (kmask[i] != 0u)) {
                                 const uint4 xv = lds128(rowa + i * vstep);
 #pragma unroll
                                 for (int kk = 0; kk < 4; ++kk) {
@@ -259,36 +281,40 @@ __global__ void __launch_bounds__(max_threads_for(VPT), 1) attnres_fwd_kernel(co
                 }
             }
             rbuf ^= 1;
-            // pass 2: rescale the running sum and add this group's weighted rows
+            // pass 2: rescale the running sum and add this group's weighted
+            // rows; each chunk is released once its rows are read
             const float2 corr2 = make_float2(corr, corr);
 #pragma unroll
             for (int i = 0; i < VPT; ++i)
 #pragma unroll
                 for (int kk = 0; kk < 4; ++kk) acc[i][kk] = fmul2(acc[i][kk], corr2);
-            uint32_t dep = 0;
-            uint32_t rowa = cbase;
+            for (int r0 = 0; r0 < gs; r0 += G) {
+                const int rn = min(G, gs - r0);
+                uint32_t dep = 0;
+                uint32_t rowa = cbase;
 #pragma unroll 2
-            for (int r = 0; r < gs; ++r) {
-                const float es = __shfl_sync(0xffffffffu, e, r);
-                const float2 es2 = make_float2(es, es);
+                for (int r = 0; r < rn; ++r) {
+                    const float es = __shfl_sync(0xffffffffu, e, r0 + r);
+                    const float2 es2 = make_float2(es, es);
 #pragma unroll
-                for (int i = 0; i < VPT; ++i) {
-                    if (col[i] >= 0) {
-                        const uint4 xv = lds128(rowa + i * vstep);
-                        dep ^= xv.x;
+                    for (int i = 0; i < VPT; ++i) {
+                        if (FULL || col[i] >= 0) {
+                            const uint4 xv = lds128(rowa + i * vstep);
+                            dep ^= xv.x;
 #pragma unroll
-                        for (int kk = 0; kk < 4; ++kk) acc[i][kk] = ffma2(es2, bf2_to_f2(u4_get(xv, kk)), acc[i][kk]);
+                            for (int kk = 0; kk < 4; ++kk) acc[i][kk] = ffma2(es2, bf2_to_f2(u4_get(xv, kk)), acc[i][kk]);
+                        }
                     }
+                    rowa += sb;
                 }
-                rowa += sb;
-            }
-            __syncwarp();
-            if (lane == 0) mbar_arrive_after(empty_s + 8u * ck, dep);
-            cbase += G * sb;
-            if (++ck == K) {
-                ck = 0;
-                cbase = ring_lo;
-                cphase ^= 1u;
+                __syncwarp();
+                if (lane == 0) mbar_arrive_after(empty_s + 8u * ck, dep);
+                cbase += cb;
+                if (++ck == K) {
+                    ck = 0;
+                    cbase = ring_lo;
+                    cphase ^= 1u;
+                }
             }
         }
         const float inv_l = 1.0f / l_run;
@@ -302,7 +328,7 @@ __global__ void __launch_bounds__(max_threads_for(VPT), 1) attnres_fwd_kernel(co
             float2 ss2 = make_float2(0.0f, 0.0f);
 #pragma unroll
             for (int i = 0; i < VPT; ++i)
-                if (col[i] >= 0)
+                if (FULL || col[i] >= 0)
 #pragma unroll
                     for (int kk = 0; kk < 4; ++kk) ss2 = ffma2(acc[i][kk], acc[i][kk], ss2);
             const float ss = warp_sum(ss2.x + ss2.y);
@@ -318,7 +344,7 @@ __global__ void __launch_bounds__(max_threads_for(VPT), 1) attnres_fwd_kernel(co
         const float2 rho2 = make_float2(rho, rho);
 #pragma unroll
         for (int i = 0; i < VPT; ++i) {
-            if (col[i] >= 0) {
+            if (FULL || col[i] >= 0) {
                 uint32_t yw[4];
 #pragma unroll
                 for (int kk = 0; kk < 4; ++kk)
@@ -346,9 +372,9 @@ __global__ void __launch_bounds__(max_threads_for(VPT), 1) attnres_fwd_kernel(co
     }
 }
 
-template <int VPT, bool KEYALL>
+template <int VPT, bool KEYALL, bool FULL>
 cudaError_t launch_fwd_t(const Plan& plan, const FwdArgs& a, cudaStream_t stream) {
-    auto kern = attnres_fwd_kernel<VPT, KEYALL>;
+    auto kern = attnres_fwd_kernel<VPT, KEYALL, FULL>;
     cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                            static_cast<int>(plan.smem_fwd));
     if (err != cudaSuccess) return err;
@@ -358,8 +384,10 @@ cudaError_t launch_fwd_t(const Plan& plan, const FwdArgs& a, cudaStream_t stream
 
 template <int VPT>
 cudaError_t dispatch_key(const Plan& plan, const FwdArgs& a, cudaStream_t stream) {
-    return (a.R == a.D) ? launch_fwd_t<VPT, true>(plan, a, stream)
-                        : launch_fwd_t<VPT, false>(plan, a, stream);
+    const bool full = (a.D / 8) == VPT * 32 * plan.ncw;
+    if (a.R == a.D)
+        return full ? launch_fwd_t<VPT, true, true>(plan, a, stream) : launch_fwd_t<VPT, true, false>(plan, a, stream);
+    return full ? launch_fwd_t<VPT, false, true>(plan, a, stream) : launch_fwd_t<VPT, false, false>(plan, a, stream);
 }
 
 }  // namespace

@@ -43,7 +43,8 @@ struct Plan {
     int vpt;
     int slot_bytes;
     int s_pad;
-    int f_rows, f_chunks;    // forward: rows per chunk (= softmax group), ring depth
+    int f_rows, f_chunks;    // forward: rows per chunk, ring depth
+    int f_group;             // forward softmax group rows (whole chunks)
     int b_rows, b_chunks;    // backward
     int dy_slots;
     int resident;            // backward keeps a token's rows between its passes
@@ -112,6 +113,7 @@ struct FwdArgs {
     int S, D, R, ko, out_norm;
     float eps, scale;
     int chunks, rows, slot_bytes, ncw, s_pad;
+    int group;          // softmax group rows (a whole number of chunks, <= kMaxGroup)
     const uint16_t* q;
     const uint16_t* w_o;
     uint16_t* y;
@@ -127,6 +129,7 @@ struct BwdArgs {
     void* dsrc[ATTNRES_MAX_S];
     long long N;
     long long src_ld, dsrc_ld;
+    long long dsrc_stride;  // bytes between dsrc[s] and dsrc[s+1] when evenly spaced, else 0
     int S, D, R, ko, out_norm;
     float eps, scale;
     int chunks, rows, slot_bytes, dy_slots, ncw, s_pad, resident, split, ngroups;
