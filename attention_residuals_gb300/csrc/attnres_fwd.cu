@@ -15,13 +15,13 @@
 // column vectors t, t + 32*ncw, ... of every row, so each warp reads 512
 // contiguous bytes per shared load.  A softmax group is a whole number of
 // chunks (the whole token when it fits beside two loading chunks): the
-// consumers wait for its chunks, then pass 1 accumulates the key sum of squares and
-// the query dot four rows at a time (packed FP32 FMAs, independent chains),
-// each four-row chunk ends with a warp reduce-scatter, one cross-warp step
-// gives the group's logits, every warp updates the running softmax maximum
-// and denominator itself (redundantly, so one CTA barrier per group
-// suffices), and pass 2 adds the weighted rows into FP32 registers and
-// releases the slots.  The output norm needs one more CTA reduction per
+// consumers wait for its chunks, then pass 1 gives each row to one warp,
+// which accumulates the row's key sum of squares and query dot with
+// mixed-precision FMAs on the bf16 halves (query in shared memory) and
+// reduces them within the warp; after one CTA barrier every warp updates
+// the running softmax maximum and denominator itself (redundantly, so no
+// second barrier is needed), and pass 2 adds the weighted rows into FP32
+// registers, thread t owning fixed columns, and releases the chunks.  The output norm needs one more CTA reduction per
 // token.  The pre-norm mixture o is written (FP32) only when asked for.
 // This is a bandwidth-bound per-token reduction: no tensor cores.
 #include <cfloat>
@@ -36,21 +36,8 @@ namespace {
 // First failed wait of any forward launch (0 = none).
 __device__ unsigned int g_fwd_error = 0;
 
-__device__ __forceinline__ void advance(int& slot, uint32_t& phase, int slots) {
-    if (++slot == slots) {
-        slot = 0;
-        phase ^= 1u;
-    }
-}
-
-__device__ __forceinline__ int ring_add(int slot, int k, int slots) {
-    const int r = slot + k;
-    return r >= slots ? r - slots : r;
-}
-
-// KEYALL: every channel is a key channel (R == D), so no per-vector masks.
 // FULL: every consumer thread owns VPT whole vectors (D == 8 * VPT * 32 * ncw).
-template <int VPT, bool KEYALL, bool FULL>
+template <int VPT, bool FULL>
 __global__ void __launch_bounds__(max_threads_for(VPT), 1) attnres_fwd_kernel(const __grid_constant__ FwdArgs a) {
     extern __shared__ __align__(128) unsigned char smem[];
     const int ncw = a.ncw;
@@ -125,33 +112,23 @@ __global__ void __launch_bounds__(max_threads_for(VPT), 1) attnres_fwd_kernel(co
     const int ncv = a.D >> 3;
     const int ko = a.ko, kend = a.ko + a.R;
     int col[VPT];
-    unsigned kmask[VPT];   // bit e: channel 8*col+e lies in the key slice
-    uint4 qb[VPT];         // query bits at the owned channels (0 outside the key)
     uint4 wb[VPT];         // output-norm weight bits (1.0 without the norm)
 #pragma unroll
     for (int i = 0; i < VPT; ++i) {
         const int c = threadIdx.x + i * nct;
         col[i] = c < ncv ? c : -1;
-        unsigned m = 0;
-        uint32_t qw[4], ww[4];
+        uint32_t ww[4];
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk) {
-            uint32_t qv = 0, wv = 0;
+            uint32_t wv = 0;
 #pragma unroll
             for (int h = 0; h < 2; ++h) {
                 const int j = 8 * c + 2 * kk + h;
-                const bool in_key = col[i] >= 0 && j >= ko && j < kend;
-                m |= in_key ? (1u << (2 * kk + h)) : 0u;
-                const uint32_t qh = in_key ? a.q[j - ko] : 0u;
                 const uint32_t wh = (a.out_norm && col[i] >= 0) ? a.w_o[j] : 0x3f80u;
-                qv |= qh << (16 * h);
                 wv |= wh << (16 * h);
             }
-            qw[kk] = qv;
             ww[kk] = wv;
         }
-        kmask[i] = m;
-        qb[i] = make_uint4(qw[0], qw[1], qw[2], qw[3]);
         wb[i] = make_uint4(ww[0], ww[1], ww[2], ww[3]);
     }
     const float inv_r = 1.0f / static_cast<float>(a.R);
@@ -169,9 +146,19 @@ __global__ void __launch_bounds__(max_threads_for(VPT), 1) attnres_fwd_kernel(co
     const int red_rows = L.red_rows;
     const int nq = (ncw + 3) >> 2;  // 16-byte loads per reduction row
 
-    // warp partials never written stay zero in the reduction scratch
+    // warp partials never written stay zero in the reduction scratch; the
+    // query goes to shared memory indexed by channel (zero outside the key)
     for (int k = threadIdx.x; k < 2 * red_rows * kRedPitch; k += nct) red[k] = 0.0f;
+    {
+        uint16_t* qsm = reinterpret_cast<uint16_t*>(smem + L.qsm);
+        for (int j = threadIdx.x; j < a.slot_bytes / 2; j += nct)
+            qsm[j] = (j >= ko && j < kend) ? a.q[j - ko] : static_cast<uint16_t>(0);
+    }
     named_bar_sync(1, nct);
+    const uint32_t ring_raw = sbase + L.ring;  // row addresses without a column offset
+    const uint32_t qsm_s = sbase + L.qsm;
+    const int kv0 = ko >> 3, kv1 = (kend + 7) >> 3;  // key vectors of a row
+    const bool key_aligned = ((ko | kend) & 7) == 0;
 
     auto red_sum = [&](int buf, int row) -> float {
         const uint32_t base = red_s + static_cast<uint32_t>(((buf * red_rows + row) * kRedPitch) * 4);
@@ -211,49 +198,55 @@ __global__ void __launch_bounds__(max_threads_for(VPT), 1) attnres_fwd_kernel(co
                     }
                 }
             }
-            // pass 1: key sum of squares and query dot, four rows at a time;
-            // (rb, ri) walks row addresses across the group's chunks
-            uint32_t rb = cbase;
-            int ri = 0;
-            for (int c0 = 0; c0 < gs; c0 += 4) {
-                float part[8];
-#pragma unroll
-                for (int r = 0; r < 4; ++r) {
-                    float2 ss2 = make_float2(0.0f, 0.0f), qt2 = make_float2(0.0f, 0.0f);
-                    if (c0 + r < gs) {
-                        const uint32_t rowa = rb + static_cast<uint32_t>(ri) * sb;
-                        if (++ri == G) {
-                            ri = 0;
-                            rb += cb;
-                            if (rb == ring_lo + static_cast<uint32_t>(K) * cb) rb = ring_lo;
-                        }
-#pragma unroll
-                        for (int i = 0; i < VPT; ++i) {
-                            if (KEYALL ? (FULL || col[i] >= 0) : (kmask[i] != 0u)) {
-                                const uint4 xv = lds128(rowa + i * vstep);
-#pragma unroll
-                                for (int kk = 0; kk < 4; ++kk) {
-                                    float2 x = bf2_to_f2(u4_get(xv, kk));
-                                    if (!KEYALL && kmask[i] != 0xffu) {
-                                        if (!((kmask[i] >> (2 * kk)) & 1u)) x.x = 0.0f;
-                                        if (!((kmask[i] >> (2 * kk + 1)) & 1u)) x.y = 0.0f;
-                                    }
-                                    ss2 = ffma2(x, x, ss2);
-                                    qt2 = ffma2(bf2_to_f2(u4_get(qb[i], kk)), x, qt2);
-                                }
-                            }
-                        }
+            // pass 1: key sum of squares and query dot.  One warp per row
+            // (rows warp, warp + ncw, ...): lanes stride over the row's key
+            // vectors and multiply the bf16 halves directly, then one warp
+            // reduction gives the row's totals.  No cross-warp sums needed.
+            for (int r = warp; r < gs; r += ncw) {
+                int rr = r;
+                int kc = ck;
+                while (rr >= G) {
+                    rr -= G;
+                    if (++kc == K) kc = 0;
+                }
+                const uint32_t row_raw = ring_raw + static_cast<uint32_t>(kc) * cb + static_cast<uint32_t>(rr) * sb;
+                float s0 = 0.0f, s1 = 0.0f, t0 = 0.0f, t1 = 0.0f;
+                float s2 = 0.0f, s3 = 0.0f, t2 = 0.0f, t3 = 0.0f;
+                int v = kv0 + lane;
+                if (key_aligned) {
+                    for (; v + 32 < kv1; v += 64) {
+                        const uint4 x0 = lds128(row_raw + 16u * v);
+                        const uint4 q0 = lds128(qsm_s + 16u * v);
+                        const uint4 x1 = lds128(row_raw + 16u * (v + 32));
+                        const uint4 q1 = lds128(qsm_s + 16u * (v + 32));
+                        bf16_sq_dot(x0, q0, s0, s1, t0, t1);
+                        bf16_sq_dot(x1, q1, s2, s3, t2, t3);
                     }
-                    part[r] = ss2.x + ss2.y;
-                    part[4 + r] = qt2.x + qt2.y;
+                    if (v < kv1) {
+                        const uint4 x0 = lds128(row_raw + 16u * v);
+                        const uint4 q0 = lds128(qsm_s + 16u * v);
+                        bf16_sq_dot(x0, q0, s0, s1, t0, t1);
+                    }
+                } else {
+                    for (; v < kv1; v += 32) {
+                        uint4 x0 = lds128(row_raw + 16u * v);
+                        const uint4 q0 = lds128(qsm_s + 16u * v);
+                        // zero the channels of a boundary vector outside [ko, kend)
+                        uint32_t w[4] = {x0.x, x0.y, x0.z, x0.w};
+#pragma unroll
+                        for (int kk = 0; kk < 4; ++kk) {
+                            const int j = 8 * v + 2 * kk;
+                            if (j < ko || j >= kend) w[kk] &= 0xffff0000u;
+                            if (j + 1 < ko || j + 1 >= kend) w[kk] &= 0x0000ffffu;
+                        }
+                        x0 = make_uint4(w[0], w[1], w[2], w[3]);
+                        bf16_sq_dot(x0, q0, s0, s1, t0, t1);
+                    }
                 }
-                warp_reduce_scatter<8>(part, lane);
-                // lane l holds element l >> 2: rows 0..3 sum-of-squares, then dots
-                if ((lane & 3) == 0) {
-                    const int idx = lane >> 2;
-                    const int r = idx & 3;
-                    if (c0 + r < gs) red[((rbuf * red_rows) + (idx >> 2) * 32 + c0 + r) * kRedPitch + warp] = part[0];
-                }
+                float part[2] = {(s0 + s1) + (s2 + s3), (t0 + t1) + (t2 + t3)};
+                warp_reduce_scatter<2>(part, lane);
+                // lane 0 holds the sum of squares, lane 16 the query dot
+                if ((lane & 15) == 0) red[(rbuf * red_rows + (lane >> 4) * 32 + r) * kRedPitch] = part[0];
             }
             named_bar_sync(1, nct);
             // Every warp derives the group's logits and softmax update itself
@@ -264,8 +257,8 @@ __global__ void __launch_bounds__(max_threads_for(VPT), 1) attnres_fwd_kernel(co
             {
                 float ss = 0.0f, qt = 0.0f;
                 if (lane < gs) {
-                    ss = red_sum(rbuf, lane);
-                    qt = red_sum(rbuf, 32 + lane);
+                    ss = red[(rbuf * red_rows + lane) * kRedPitch];
+                    qt = red[(rbuf * red_rows + 32 + lane) * kRedPitch];
                 }
                 const float r = rsqrtf(fmaf(ss, inv_r, a.eps));
                 const float z = a.scale * r * qt;
@@ -372,9 +365,9 @@ __global__ void __launch_bounds__(max_threads_for(VPT), 1) attnres_fwd_kernel(co
     }
 }
 
-template <int VPT, bool KEYALL, bool FULL>
+template <int VPT, bool FULL>
 cudaError_t launch_fwd_t(const Plan& plan, const FwdArgs& a, cudaStream_t stream) {
-    auto kern = attnres_fwd_kernel<VPT, KEYALL, FULL>;
+    auto kern = attnres_fwd_kernel<VPT, FULL>;
     cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                            static_cast<int>(plan.smem_fwd));
     if (err != cudaSuccess) return err;
@@ -385,9 +378,7 @@ cudaError_t launch_fwd_t(const Plan& plan, const FwdArgs& a, cudaStream_t stream
 template <int VPT>
 cudaError_t dispatch_key(const Plan& plan, const FwdArgs& a, cudaStream_t stream) {
     const bool full = (a.D / 8) == VPT * 32 * plan.ncw;
-    if (a.R == a.D)
-        return full ? launch_fwd_t<VPT, true, true>(plan, a, stream) : launch_fwd_t<VPT, true, false>(plan, a, stream);
-    return full ? launch_fwd_t<VPT, false, true>(plan, a, stream) : launch_fwd_t<VPT, false, false>(plan, a, stream);
+    return full ? launch_fwd_t<VPT, true>(plan, a, stream) : launch_fwd_t<VPT, false>(plan, a, stream);
 }
 
 }  // namespace

@@ -322,6 +322,30 @@ __device__ __forceinline__ void mbar_arrive_after(uint32_t bar, uint32_t dep) {
                  : "memory");
 }
 
+
+// Key statistics of one 16-byte vector of bf16 pairs, on bf16 operands
+// directly (fma.rn.f32.bf16: one FFMA each, exact products, FP32 sums):
+//   s0 += x_lo^2, s1 += x_hi^2, t0 += q_lo*x_lo, t1 += q_hi*x_hi
+// for each of the four 32-bit words of x and q.
+__device__ __forceinline__ void bf16_sq_dot(const uint4& x, const uint4& q, float& s0, float& s1,
+                                            float& t0, float& t1) {
+    asm("{\n\t.reg .b16 xl, xh, ql, qh;\n\t"
+        "mov.b32 {xl, xh}, %4;\n\tmov.b32 {ql, qh}, %8;\n\t"
+        "fma.rn.f32.bf16 %0, xl, xl, %0;\n\tfma.rn.f32.bf16 %1, xh, xh, %1;\n\t"
+        "fma.rn.f32.bf16 %2, ql, xl, %2;\n\tfma.rn.f32.bf16 %3, qh, xh, %3;\n\t"
+        "mov.b32 {xl, xh}, %5;\n\tmov.b32 {ql, qh}, %9;\n\t"
+        "fma.rn.f32.bf16 %0, xl, xl, %0;\n\tfma.rn.f32.bf16 %1, xh, xh, %1;\n\t"
+        "fma.rn.f32.bf16 %2, ql, xl, %2;\n\tfma.rn.f32.bf16 %3, qh, xh, %3;\n\t"
+        "mov.b32 {xl, xh}, %6;\n\tmov.b32 {ql, qh}, %10;\n\t"
+        "fma.rn.f32.bf16 %0, xl, xl, %0;\n\tfma.rn.f32.bf16 %1, xh, xh, %1;\n\t"
+        "fma.rn.f32.bf16 %2, ql, xl, %2;\n\tfma.rn.f32.bf16 %3, qh, xh, %3;\n\t"
+        "mov.b32 {xl, xh}, %7;\n\tmov.b32 {ql, qh}, %11;\n\t"
+        "fma.rn.f32.bf16 %0, xl, xl, %0;\n\tfma.rn.f32.bf16 %1, xh, xh, %1;\n\t"
+        "fma.rn.f32.bf16 %2, ql, xl, %2;\n\tfma.rn.f32.bf16 %3, qh, xh, %3;\n\t}"
+        : "+f"(s0), "+f"(s1), "+f"(t0), "+f"(t1)
+        : "r"(x.x), "r"(x.y), "r"(x.z), "r"(x.w), "r"(q.x), "r"(q.y), "r"(q.z), "r"(q.w));
+}
+
 // Position in the shared-memory row ring: row address, slot index, phase.
 struct RingCursor {
     uint32_t row;

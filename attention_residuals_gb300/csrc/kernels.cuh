@@ -58,7 +58,7 @@ struct Plan {
 
 // Byte offsets inside the dynamic shared memory of one CTA.
 struct SmemLayout {
-    uint32_t ring, dyring, full, empty, dyfull, dyempty, tfull, tempty, red, tok, coef, misc, total;
+    uint32_t ring, dyring, full, empty, dyfull, dyempty, tfull, tempty, red, tok, coef, qsm, misc, total;
     int red_rows;  // rows of the reduction scratch (per buffer)
 };
 
@@ -69,7 +69,8 @@ constexpr int kRedPitch = 20;
 
 __host__ __device__ inline uint32_t align_up(uint32_t x, uint32_t a) { return (x + a - 1) / a * a; }
 
-// Forward: chunk ring, z[s_pad] and rstd[s_pad] of the current token.
+// Forward: chunk ring, z[s_pad] and rstd[s_pad] of the current token, and
+// the query as bf16 indexed by channel (slot_bytes, zero outside the key).
 // Backward: chunk ring, dy ring, token-statistics ring.
 __host__ __device__ inline SmemLayout make_layout(int chunks, int rows, int slot_bytes, int dy_slots,
                                                   int s_pad, bool backward) {
@@ -100,6 +101,9 @@ __host__ __device__ inline SmemLayout make_layout(int chunks, int rows, int slot
     off += backward ? static_cast<uint32_t>(kTokSlots) * (3u * s_pad + 4u) * 4u : 0u;
     L.coef = off;
     off += backward ? 0u : 2u * s_pad * 4u;
+    off = align_up(off, 16);
+    L.qsm = off;
+    off += backward ? 0u : static_cast<uint32_t>(slot_bytes);
     L.misc = off;  // abort flag, ticket flags
     off += 16u;
     L.total = align_up(off, 128);
