@@ -70,6 +70,9 @@ attnres_status make_plan(const attnres_params* p, Plan* plan) {
     pl.vpt = ncv <= 32 * max_warps_for(1) ? 1 : 4;
     pl.ncw = (ncv + 32 * pl.vpt - 1) / (32 * pl.vpt);
     if (pl.ncw < 1 || pl.ncw > max_warps_for(pl.vpt)) return ATTNRES_ERR_UNSUPPORTED;
+    pl.b_vpt = ncv <= 256 ? 1 : (ncv <= 512 ? 2 : 4);
+    pl.b_ncw = (ncv + 32 * pl.b_vpt - 1) / (32 * pl.b_vpt);
+    if (pl.b_ncw < 1 || pl.b_ncw > max_warps_for(pl.b_vpt)) return ATTNRES_ERR_UNSUPPORTED;
     pl.slot_bytes = static_cast<int>(align_up(static_cast<uint32_t>(p->D) * 2u, 128u));
     pl.s_pad = static_cast<int>(align_up(static_cast<uint32_t>(p->S), 4u));
     const int S = p->S;
@@ -174,8 +177,8 @@ attnres_status attnres_plan_info(const attnres_params* p, int64_t out[8]) {
     st = make_plan(p, &pl);
     if (st != ATTNRES_OK) return st;
     out[0] = pl.grid;
-    out[1] = pl.ncw;
-    out[2] = pl.vpt;
+    out[1] = pl.ncw * 1000 + pl.b_ncw;
+    out[2] = pl.vpt * 1000 + pl.b_vpt;
     out[3] = pl.b_chunks * 1000 + pl.b_rows;
     out[4] = pl.f_chunks * 1000 + pl.f_rows;
     out[5] = pl.resident;
@@ -323,7 +326,7 @@ attnres_status attnres_bwd(const attnres_params* p, const void* q, const void* w
     a.rows = pl.b_rows;
     a.dy_slots = pl.dy_slots;
     a.slot_bytes = pl.slot_bytes;
-    a.ncw = pl.ncw;
+    a.ncw = pl.b_ncw;
     a.s_pad = pl.s_pad;
     a.resident = pl.resident;
     a.split = pl.split;

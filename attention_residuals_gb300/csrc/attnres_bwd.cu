@@ -644,7 +644,7 @@ cudaError_t launch_bwd_t(const Plan& plan, const BwdArgs& a, cudaStream_t stream
     cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                            static_cast<int>(plan.smem_bwd));
     if (err != cudaSuccess) return err;
-    kern<<<plan.grid, (plan.ncw + 1) * 32, plan.smem_bwd, stream>>>(a);
+    kern<<<plan.grid, (plan.b_ncw + 1) * 32, plan.smem_bwd, stream>>>(a);
     err = cudaGetLastError();
     if (err != cudaSuccess || !plan.split) return err;
     const int W = a.R + (a.out_norm ? a.D : 0);
@@ -655,7 +655,7 @@ cudaError_t launch_bwd_t(const Plan& plan, const BwdArgs& a, cudaStream_t stream
 
 template <int VPT>
 cudaError_t dispatch_key(const Plan& plan, const BwdArgs& a, cudaStream_t stream) {
-    const bool full = (a.D / 8) == VPT * 32 * plan.ncw;
+    const bool full = (a.D / 8) == VPT * 32 * plan.b_ncw;
     if (a.R == a.D)
         return full ? launch_bwd_t<VPT, true, true>(plan, a, stream) : launch_bwd_t<VPT, true, false>(plan, a, stream);
     return full ? launch_bwd_t<VPT, false, true>(plan, a, stream) : launch_bwd_t<VPT, false, false>(plan, a, stream);
@@ -671,8 +671,9 @@ unsigned take_bwd_error() {
 }
 
 cudaError_t launch_bwd(const Plan& plan, const BwdArgs& a, cudaStream_t stream) {
-    switch (plan.vpt) {
+    switch (plan.b_vpt) {
         case 1: return dispatch_key<1>(plan, a, stream);
+        case 2: return dispatch_key<2>(plan, a, stream);
         case 4: return dispatch_key<4>(plan, a, stream);
         default: return cudaErrorInvalidConfiguration;
     }

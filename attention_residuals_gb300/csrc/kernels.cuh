@@ -13,7 +13,11 @@ namespace attnres {
 constexpr int kMaxConsumerWarps = 16;
 // Threads per CTA (consumers + one producer warp).  One 16-byte vector per
 // thread allows 16 consumer warps (registers <= 96); wider per-thread
-// footprints keep 8 consumer warps (registers <= 168).
+// footprints keep 8 consumer warps (registers <= 168).  The backward keeps
+// more state per column (dq, dw_o, the gradient wrt o) and runs 8 warps
+// with two vectors each for D = 4096: it stays clear of the 96-register
+// limit, where the compiler's spill and rematerialisation choices made its
+// speed unstable.
 __host__ __device__ constexpr int max_threads_for(int vpt) { return vpt == 1 ? 17 * 32 : 9 * 32; }
 __host__ __device__ constexpr int max_warps_for(int vpt) { return vpt == 1 ? 16 : 8; }
 constexpr int kMaxChunks = 32;
@@ -39,8 +43,8 @@ enum WaitSite : unsigned {
 // `dy_slots` single-row slots for dy.
 struct Plan {
     int grid;
-    int ncw;
-    int vpt;
+    int ncw, vpt;            // forward: consumer warps, 16-byte vectors per thread
+    int b_ncw, b_vpt;        // backward
     int slot_bytes;
     int s_pad;
     int f_rows, f_chunks;    // forward: rows per chunk, ring depth

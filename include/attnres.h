@@ -165,7 +165,8 @@ const char* attnres_status_string(attnres_status s);
 /*
  * Launch plan the library would use for these params on the current device
  * (for tests and benchmarks; no launch happens).  Fills out[0..7] with:
- * grid CTAs, consumer warps, 16-byte vectors per thread, the backward ring
+ * grid CTAs, consumer warps (forward * 1000 + backward), 16-byte vectors
+ * per thread (forward * 1000 + backward), the backward ring
  * (chunks * 1000 + rows per chunk), the forward ring (chunks * 1000 + rows
  * per chunk = softmax group), the backward resident flag (1 = a token's
  * source rows stay in shared memory for all backward passes), dynamic
