@@ -7,6 +7,7 @@ from .ops import (  # noqa: F401
     EPS_DEFAULT,
     attnres,
     attnres_bwd,
+    attnres_bwd_noalloc,
     attnres_bwd_workspace_bytes,
     attnres_check_device_error,
     attnres_fwd,

@@ -11,6 +11,7 @@ import threading
 
 MAX_S = 128
 MAX_D = 8192
+NOALLOC_SCRATCH_BYTES = 16 << 20
 DEFAULT_SPLIT_N = 16384
 
 STATUS = {
@@ -26,6 +27,7 @@ STATUS = {
 EXPORTED = [
     "attnres_fwd",
     "attnres_bwd",
+    "attnres_bwd_noalloc",
     "attnres_bwd_workspace_bytes",
     "attnres_check_device_error",
     "attnres_status_string",
@@ -87,6 +89,9 @@ def load(path: str | None = None):
         lib.attnres_bwd.restype = ctypes.c_int
         lib.attnres_bwd.argtypes = [P, vp, vp, vp, fp, fp, fp, fp, vp,
                                     ctypes.POINTER(ctypes.c_void_p), i64, vp, fp, vp, fp, vp, sz, vp]
+        lib.attnres_bwd_noalloc.restype = ctypes.c_int
+        lib.attnres_bwd_noalloc.argtypes = [P, vp, vp, vp, fp, fp, fp, fp, fp,
+                                            ctypes.POINTER(ctypes.c_void_p), i64, vp, fp, vp, fp, vp]
         lib.attnres_check_device_error.restype = ctypes.c_int
         lib.attnres_check_device_error.argtypes = []
         lib.attnres_status_string.restype = ctypes.c_char_p

@@ -2,6 +2,7 @@
 // workspace sizing for the AttnRes read operator (include/attnres.h).
 #include <cmath>
 #include <cstring>
+#include <mutex>
 
 #include "attnres.h"
 #include "kernels.cuh"
@@ -353,6 +354,45 @@ attnres_status attnres_bwd(const attnres_params* p, const void* q, const void* w
             return ATTNRES_ERR_CUDA;
     }
     return launch_bwd(pl, a, s) == cudaSuccess ? ATTNRES_OK : ATTNRES_ERR_CUDA;
+}
+
+// ---------------------------------------------------------------------------
+// Backward without a caller workspace.  Its scratch is this file-scope device
+// array; host code must not use the name as an address (on the host it is a
+// stand-in), so each device's address is looked up once with cudaGetSymbolAddress
+// and handed to attnres_bwd as the workspace.  The tickets that must start at
+// zero are cleared on the caller's stream by attnres_bwd itself.
+// ---------------------------------------------------------------------------
+static __device__ __align__(256) unsigned char g_noalloc_scratch[ATTNRES_NOALLOC_SCRATCH_BYTES];
+
+static void* noalloc_scratch_address(int dev) {
+    static std::mutex mu;
+    static void* addr[64] = {nullptr};
+    if (dev < 0 || dev >= 64) return nullptr;
+    std::lock_guard<std::mutex> lock(mu);
+    if (!addr[dev]) {
+        void* ptr = nullptr;
+        if (cudaGetSymbolAddress(&ptr, g_noalloc_scratch) != cudaSuccess) return nullptr;
+        addr[dev] = ptr;
+    }
+    return addr[dev];
+}
+
+attnres_status attnres_bwd_noalloc(const attnres_params* p, const void* q, const void* w_o,
+                                   const void* dy, const float* alpha, const float* rstd,
+                                   const float* logit, const float* o_rstd, const float* o_pre,
+                                   void* const* dsrc, int64_t dsrc_ld, void* dq, float* dq_f32,
+                                   void* dw_o, float* dw_o_f32, void* stream) {
+    attnres_status st = check_shape(p);
+    if (st != ATTNRES_OK) return st;
+    const size_t need = attnres_bwd_workspace_bytes(p);
+    if (need > ATTNRES_NOALLOC_SCRATCH_BYTES) return ATTNRES_ERR_WORKSPACE;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return ATTNRES_ERR_CUDA;
+    void* scratch = noalloc_scratch_address(dev);
+    if (!scratch) return ATTNRES_ERR_CUDA;
+    return attnres_bwd(p, q, w_o, dy, alpha, rstd, logit, o_rstd, o_pre, dsrc, dsrc_ld, dq, dq_f32,
+                       dw_o, dw_o_f32, scratch, ATTNRES_NOALLOC_SCRATCH_BYTES, stream);
 }
 
 attnres_status attnres_check_device_error(void) {

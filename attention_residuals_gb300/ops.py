@@ -245,6 +245,46 @@ def attnres_bwd(values: Sources, q: torch.Tensor, dy: torch.Tensor, saved: dict,
     return {"dvalues": dv, "dq": dq, "dq_f32": dq32, "dw_o": dw, "dw_o_f32": dw32}
 
 
+def attnres_bwd_noalloc(values: Sources, q: torch.Tensor, dy: torch.Tensor, saved: dict, *,
+                        w_o: Optional[torch.Tensor] = None, eps: float = EPS_DEFAULT,
+                        scale: float = 1.0, key_offset: Optional[int] = None,
+                        split_n_threshold: int = 0, stream=None, dvalues: Optional[Sources] = None,
+                        dq: Optional[torch.Tensor] = None, dq_f32: Optional[torch.Tensor] = None,
+                        dw_o: Optional[torch.Tensor] = None,
+                        dw_o_f32: Optional[torch.Tensor] = None) -> dict:
+    """Backward through the library's fixed scratch array instead of a
+    workspace, for callers that must not allocate device memory during the
+    call (pass every output preallocated).  Calls sharing the array must not
+    overlap on the GPU; see include/attnres.h."""
+    view = saved.get("view") or _source_view(values)
+    R = q.numel()
+    q = _check_vec(q, R, "q")
+    w_o = _check_vec(w_o, view.D, "w_o")
+    p = make_params(view, R, key_offset=key_offset, eps=eps, scale=scale, out_norm=w_o is not None,
+                    split_n_threshold=split_n_threshold)
+    S, N, D = len(view.rows), view.N, view.D
+    dev = view.rows[0].device
+    if dy.dtype != torch.bfloat16 or not dy.is_cuda or dy.numel() != N * D:
+        raise TypeError("dy must be a CUDA bf16 tensor shaped like the output")
+    dy2 = dy.reshape(N, D)
+    if not dy2.is_contiguous():
+        raise ValueError("dy must be contiguous (the no-allocation path makes no copies)")
+    if dvalues is None or dq is None or (w_o is not None and dw_o is None):
+        raise ValueError("the no-allocation path needs preallocated dvalues, dq (and dw_o)")
+    if isinstance(dvalues, torch.Tensor):
+        drows = [dvalues[s].reshape(N, D) for s in range(S)]
+    else:
+        drows = [d.reshape(N, D) for d in dvalues]
+    dld = int(drows[0].stride(0)) if N > 1 else D
+    dptrs = (ctypes.c_void_p * S)(*[r.data_ptr() for r in drows])
+    rc = _lib.load().attnres_bwd_noalloc(
+        ctypes.byref(p), _ptr(q), _ptr(w_o), _ptr(dy2), _ptr(saved["alpha"]), _ptr(saved["rstd"]),
+        _ptr(saved["logit"]), _ptr(saved.get("o_rstd")), _ptr(saved.get("o_pre")), dptrs,
+        ctypes.c_int64(dld), _ptr(dq), _ptr(dq_f32), _ptr(dw_o), _ptr(dw_o_f32), _stream(stream))
+    _lib.check(rc, "attnres_bwd_noalloc")
+    return {"dvalues": dvalues, "dq": dq, "dq_f32": dq_f32, "dw_o": dw_o, "dw_o_f32": dw_o_f32}
+
+
 # --------------------------------------------------------------------------
 # Autograd operator
 # --------------------------------------------------------------------------

@@ -151,6 +151,34 @@ attnres_status attnres_bwd(const attnres_params* p, const void* q, const void* w
                            size_t workspace_bytes, void* stream);
 
 /*
+ * Backward without a caller-supplied workspace (no counterpart in the
+ * papers; it exists for callers that cannot allocate device memory, such as
+ * code running inside a region being captured into a CUDA graph, plugins
+ * that must not touch the allocator of the process hosting them, or
+ * latency-critical paths where cudaMalloc's implicit synchronisation is not
+ * acceptable).  Same arguments and results as attnres_bwd minus the
+ * workspace: the scratch lives in a fixed device array of the library of
+ * ATTNRES_NOALLOC_SCRATCH_BYTES bytes (16 MiB), which every GPU that loads
+ * the library holds until the process exits.
+ *   - Nothing is allocated: no cudaMalloc, cudaFree or allocating library
+ *     call.  The first call on a device looks up the array's device address
+ *     (cudaGetSymbolAddress) with that device current; make that first call
+ *     before any stream capture.
+ *   - Shapes whose scratch (attnres_bwd_workspace_bytes) exceeds the array
+ *     are rejected with ATTNRES_ERR_WORKSPACE before anything is enqueued.
+ *   - All calls share the one array: calls that may overlap on the GPU (other
+ *     streams, other host threads) race and give wrong results; serialise
+ *     them, e.g. on one stream.  The parts of the array that must start at
+ *     zero are cleared by every call on its stream.
+ */
+#define ATTNRES_NOALLOC_SCRATCH_BYTES (16u << 20)
+attnres_status attnres_bwd_noalloc(const attnres_params* p, const void* q, const void* w_o,
+                                   const void* dy, const float* alpha, const float* rstd,
+                                   const float* logit, const float* o_rstd, const float* o_pre,
+                                   void* const* dsrc, int64_t dsrc_ld, void* dq, float* dq_f32,
+                                   void* dw_o, float* dw_o_f32, void* stream);
+
+/*
  * Kernels bound every wait on a shared-memory barrier.  A wait that runs out
  * of time makes the kernel record a nonzero code here and finish without
  * further waiting (its outputs are then garbage).  This call synchronises
