@@ -241,6 +241,7 @@ def run_ours(args):
 
     from attention_residuals_gb300 import _lib, attnres_bwd, attnres_fwd, attnres_plan_info
     from attention_residuals_gb300.build import build
+    from attention_residuals_gb300.dist import max_over_ranks, weak_scaling_throughput
     from attention_residuals_gb300.workloads import make_workload
     build()
     _lib.load()
@@ -303,10 +304,8 @@ def run_ours(args):
     fwd_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in ev)
     bwd_ms = statistics.mean(e[1].elapsed_time(e[2]) for e in ev)
     ms_step = total_ms / K
-    if pg is not None:
-        t = torch.tensor([ms_step, fwd_ms, bwd_ms], device=dev)
-        pg.all_reduce(t, op=pg.ReduceOp.MAX)
-        ms_step, fwd_ms, bwd_ms = [float(x) for x in t.tolist()]
+    if pg is not None:  # the slowest rank sets the step time
+        ms_step, fwd_ms, bwd_ms = max_over_ranks([ms_step, fwd_ms, bwd_ms], device=dev)
 
     # ---------------------------------------------------------- end to end
     e2e = None
@@ -355,12 +354,10 @@ def run_ours(args):
         torch.cuda.synchronize()
         e2e_ms = s0.elapsed_time(s1) / KE
         if pg is not None:
-            t = torch.tensor([e2e_ms], device=dev)
-            pg.all_reduce(t, op=pg.ReduceOp.MAX)
-            e2e_ms = float(t.item())
+            e2e_ms = max_over_ranks([e2e_ms], device=dev)[0]
         h2d = (hv.numel() + hq.numel() + hw.numel() + hdy.numel()) * 2
         d2h = (hy.numel() + hdv.numel() + hdq.numel() + hdw.numel()) * 2
-        e2e = {"value": world * nbytes["total"] / (e2e_ms * 1e-3) / 1e9, "unit": "GB/s",
+        e2e = {"value": weak_scaling_throughput(nbytes["total"], world, e2e_ms), "unit": "GB/s",
                "ms_per_step": e2e_ms, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
         del hv, hdv
 
@@ -380,7 +377,7 @@ def run_ours(args):
 
     peak, peak_kind = read_peak()
     achieved = nbytes["bwd"] / (bwd_ms * 1e-3) / 1e9
-    value = world * nbytes["total"] / (ms_step * 1e-3) / 1e9
+    value = weak_scaling_throughput(nbytes["total"], world, ms_step)
     launches_per_step = 2 + (1 if info["bwd_split"] else 0)
     line = {
         "metric": METRIC,
