@@ -68,12 +68,12 @@ attnres_status make_plan(const attnres_params* p, Plan* plan) {
     if (!device_info(&dev)) return ATTNRES_ERR_CUDA;
     Plan pl{};
     const int ncv = p->D / 8;
-    pl.vpt = ncv <= 32 * max_warps_for(1) ? 1 : 4;
+    // 16-byte vectors per thread so that at most 8 consumer warps cover a row
+    pl.vpt = ncv <= 256 ? 1 : (ncv <= 512 ? 2 : 4);
     pl.ncw = (ncv + 32 * pl.vpt - 1) / (32 * pl.vpt);
-    if (pl.ncw < 1 || pl.ncw > max_warps_for(pl.vpt)) return ATTNRES_ERR_UNSUPPORTED;
-    pl.b_vpt = ncv <= 256 ? 1 : (ncv <= 512 ? 2 : 4);
-    pl.b_ncw = (ncv + 32 * pl.b_vpt - 1) / (32 * pl.b_vpt);
-    if (pl.b_ncw < 1 || pl.b_ncw > max_warps_for(pl.b_vpt)) return ATTNRES_ERR_UNSUPPORTED;
+    if (pl.ncw < 1 || pl.ncw > kMaxConsumerWarps) return ATTNRES_ERR_UNSUPPORTED;
+    pl.b_vpt = pl.vpt;
+    pl.b_ncw = pl.ncw;
     pl.slot_bytes = static_cast<int>(align_up(static_cast<uint32_t>(p->D) * 2u, 128u));
     pl.s_pad = static_cast<int>(align_up(static_cast<uint32_t>(p->S), 4u));
     const int S = p->S;
@@ -87,22 +87,32 @@ attnres_status make_plan(const attnres_params* p, Plan* plan) {
         while (c < kMaxChunks && fits(c + 1, rows, dy, bwd)) ++c;
         return c;
     };
-    // Forward: a chunk is one softmax group; keep at least four chunks in the
-    // ring so that loads of later groups overlap the current one.
+    // Forward: CTAs that share an SM split its shared memory.  A chunk holds
+    // half a token (or less); a softmax group is all chunks but one, which
+    // keeps one chunk loading while the group is read (the other CTA on the
+    // SM overlaps the rest).
     {
+        const int per_sm = fwd_ctas_per_sm(pl.vpt);
+        const long long budget = per_sm > 1 ? (optin / per_sm - 1024) : optin;
+        auto ffits = [&](int chunks, int rows) {
+            return make_layout(chunks, rows, pl.slot_bytes, 0, pl.s_pad, false).total <=
+                   static_cast<uint32_t>(budget);
+        };
         const long long fixed = make_layout(0, 1, pl.slot_bytes, 0, pl.s_pad, false).total + 64;
-        long long gmax = (optin - fixed) / (4 * sb);
+        long long gmax = (budget - fixed) / (2 * sb);
         if (gmax > kMaxGroup) gmax = kMaxGroup;
         if (gmax < 1) gmax = 1;
         const int groups = static_cast<int>((S + gmax - 1) / gmax);
         pl.f_rows = (S + groups - 1) / groups;
-        pl.f_chunks = max_chunks(pl.f_rows, 0, false);
+        pl.f_chunks = 0;
+        while (pl.f_chunks < kMaxChunks && ffits(pl.f_chunks + 1, pl.f_rows)) ++pl.f_chunks;
         if (pl.f_chunks < 2) return ATTNRES_ERR_UNSUPPORTED;
-        // A softmax group spans whole chunks and leaves two chunks loading.
-        int gc = pl.f_chunks - 2;
-        if (gc < 1) gc = 1;
+        int gc = pl.f_chunks - 1;
         while (gc > 1 && gc * pl.f_rows > kMaxGroup) --gc;
         pl.f_group = gc * pl.f_rows;
+        long long fg = static_cast<long long>(per_sm) * dev.sm_count;
+        if (p->N < fg) fg = p->N;
+        pl.fgrid = static_cast<int>(fg < 1 ? 1 : fg);
     }
     // Backward: dy ring, then either a resident token (its rows in two
     // chunks, at most ~60% of the ring so the next token can load meanwhile)

@@ -50,7 +50,7 @@ __device__ __forceinline__ float ldcg_f32(const float* p) { return __ldcg(p); }
 // KEYALL: every channel is a key channel (R == D), so no per-vector masks.
 // FULL: every consumer thread owns VPT whole vectors (D == 8 * VPT * 32 * ncw).
 template <int VPT, bool KEYALL, bool FULL>
-__global__ void __launch_bounds__(max_threads_for(VPT), 1) attnres_bwd_kernel(const __grid_constant__ BwdArgs a) {
+__global__ void __launch_bounds__(kMaxThreads, 1) attnres_bwd_kernel(const __grid_constant__ BwdArgs a) {
     extern __shared__ __align__(128) unsigned char smem[];
     const int ncw = a.ncw;
     const int nct = ncw * 32;

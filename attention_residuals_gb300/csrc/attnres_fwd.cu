@@ -6,8 +6,9 @@
 // RMSNorm whose reciprocal RMS is saved for the backward ("[Perf]
 // Parallelize AttnRes long-sequence reduction", Summary).
 //
-// GB300 mapping.  One persistent CTA per SM walks tokens n = blockIdx.x,
-// blockIdx.x + gridDim.x, ...  A producer thread streams every source row of
+// GB300 mapping.  Persistent CTAs (two per SM when a thread owns at most two
+// vectors, so that one CTA's barrier and softmax phases overlap the other's
+// streaming work) walk tokens n = blockIdx.x, blockIdx.x + gridDim.x, ...  A producer thread streams every source row of
 // the token into a ring of shared-memory row slots with 1-D TMA bulk copies
 // (one cp.async.bulk per row).  The ring is organised in chunks of G rows
 // with one "full" and one "empty" mbarrier each, so waits and releases cost
@@ -38,7 +39,7 @@ __device__ unsigned int g_fwd_error = 0;
 
 // FULL: every consumer thread owns VPT whole vectors (D == 8 * VPT * 32 * ncw).
 template <int VPT, bool FULL>
-__global__ void __launch_bounds__(max_threads_for(VPT), 1) attnres_fwd_kernel(const __grid_constant__ FwdArgs a) {
+__global__ void __launch_bounds__(kMaxThreads, fwd_ctas_per_sm(VPT)) attnres_fwd_kernel(const __grid_constant__ FwdArgs a) {
     extern __shared__ __align__(128) unsigned char smem[];
     const int ncw = a.ncw;
     const int nct = ncw * 32;
@@ -371,7 +372,7 @@ cudaError_t launch_fwd_t(const Plan& plan, const FwdArgs& a, cudaStream_t stream
     cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                            static_cast<int>(plan.smem_fwd));
     if (err != cudaSuccess) return err;
-    kern<<<plan.grid, (plan.ncw + 1) * 32, plan.smem_fwd, stream>>>(a);
+    kern<<<plan.fgrid, (plan.ncw + 1) * 32, plan.smem_fwd, stream>>>(a);
     return cudaGetLastError();
 }
 
@@ -393,6 +394,7 @@ unsigned take_fwd_error() {
 cudaError_t launch_fwd(const Plan& plan, const FwdArgs& a, cudaStream_t stream) {
     switch (plan.vpt) {
         case 1: return dispatch_key<1>(plan, a, stream);
+        case 2: return dispatch_key<2>(plan, a, stream);
         case 4: return dispatch_key<4>(plan, a, stream);
         default: return cudaErrorInvalidConfiguration;
     }

@@ -10,16 +10,13 @@
 
 namespace attnres {
 
-constexpr int kMaxConsumerWarps = 16;
-// Threads per CTA (consumers + one producer warp).  One 16-byte vector per
-// thread allows 16 consumer warps (registers <= 96); wider per-thread
-// footprints keep 8 consumer warps (registers <= 168).  The backward keeps
-// more state per column (dq, dw_o, the gradient wrt o) and runs 8 warps
-// with two vectors each for D = 4096: it stays clear of the 96-register
-// limit, where the compiler's spill and rematerialisation choices made its
-// speed unstable.
-__host__ __device__ constexpr int max_threads_for(int vpt) { return vpt == 1 ? 17 * 32 : 9 * 32; }
-__host__ __device__ constexpr int max_warps_for(int vpt) { return vpt == 1 ? 16 : 8; }
+constexpr int kMaxConsumerWarps = 8;
+// Threads per CTA: up to 8 consumer warps and one producer warp.
+constexpr int kMaxThreads = (kMaxConsumerWarps + 1) * 32;
+// Forward CTAs per SM: with at most two 16-byte vectors per thread two CTAs
+// fit (registers <= 96, half the shared memory each) and each CTA's barrier
+// and softmax phases overlap the other's streaming work; wider rows run one.
+__host__ __device__ constexpr int fwd_ctas_per_sm(int vpt) { return vpt <= 2 ? 2 : 1; }
 constexpr int kMaxChunks = 32;
 constexpr int kTokSlots = 4;      // token-statistics ring depth (backward)
 constexpr int kGroupTicket = 12;  // CTAs per first-level group of the in-kernel reduction
@@ -42,7 +39,8 @@ enum WaitSite : unsigned {
 // and releases are per chunk, not per row.  The backward also has a ring of
 // `dy_slots` single-row slots for dy.
 struct Plan {
-    int grid;
+    int grid;                // backward CTAs (one per SM)
+    int fgrid;               // forward CTAs (fwd_ctas_per_sm per SM)
     int ncw, vpt;            // forward: consumer warps, 16-byte vectors per thread
     int b_ncw, b_vpt;        // backward
     int slot_bytes;

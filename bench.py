@@ -307,6 +307,23 @@ def run_ours(args):
     if pg is not None:  # the slowest rank sets the step time
         ms_step, fwd_ms, bwd_ms = max_over_ranks([ms_step, fwd_ms, bwd_ms], device=dev)
 
+    # --------------------- device copy bandwidth on this GPU (context only)
+    copy_gbs = None
+    if not args.no_copy_probe:
+        src = torch.empty((2 << 30,), dtype=torch.uint8, device=dev)
+        dst = torch.empty_like(src)
+        for _ in range(3):
+            dst.copy_(src)
+        c0 = torch.cuda.Event(enable_timing=True)
+        c1 = torch.cuda.Event(enable_timing=True)
+        c0.record(stream)
+        for _ in range(10):
+            dst.copy_(src)
+        c1.record(stream)
+        torch.cuda.synchronize()
+        copy_gbs = 10 * 2 * src.numel() / (c0.elapsed_time(c1) * 1e-3) / 1e9
+        del src, dst
+
     # ---------------------------------------------------------- end to end
     e2e = None
     if not args.no_e2e:
@@ -397,6 +414,7 @@ def run_ours(args):
                    "bytes_per_step": nbytes["total"],
                    "fwd_ms": fwd_ms, "bwd_ms": bwd_ms,
                    "frac_of_peak_step": value / world / peak,
+                   "device_copy_gbs": copy_gbs,
                    "l2": "inputs larger than L2 (2.7 GB of sources per step); no flush",
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
                    "plan": info},
@@ -426,6 +444,7 @@ def main(argv=None):
     ap.add_argument("--ref-tokens", type=int, default=1024)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--no-copy-probe", action="store_true")
     ap.add_argument("--tokens", type=int, default=None,
                     help="fewer tokens of the same workload (profiling captures only)")
     args = ap.parse_args(argv)
