@@ -1,0 +1,135 @@
+"""torch.library registration of the read operator.
+
+`attnres_gb300::read_fwd` and `attnres_gb300::read_bwd` wrap the C ABI
+calls as custom operators with shape-only ("fake") implementations and an
+autograd formula, so `torch.compile(..., fullgraph=True)` traces through
+`attnres()` without graph breaks and CUDA-graph capture replays the same
+kernels ("Fast Attention Residuals", Quickstart: the read is compiled with
+fullgraph=True and replayed in CUDA graphs).  The operators compute nothing
+themselves: every step runs in the CUDA library.
+
+Values travel as a list: either one packed [S, ..., D] tensor or S separate
+[..., D] tensors; the gradient comes back in the same form (a packed input
+gets one packed gradient, with no stacking copy).
+"""
+from __future__ import annotations
+
+import ctypes
+from typing import List, Optional, Tuple
+
+import torch
+from torch import Tensor
+
+from . import _lib
+from . import ops as _ops
+
+_NS = "attnres_gb300"
+
+
+def _shape_info(values: List[Tensor], R: int) -> Tuple[int, int, int, tuple]:
+    if len(values) == 1 and values[0].dim() >= 2:
+        v = values[0]
+        return v.shape[0], v.shape[-1], 1, tuple(v.shape[1:-1])
+    return len(values), values[0].shape[-1], 0, tuple(values[0].shape[:-1])
+
+
+def _bwd_resident(S: int, D: int, R: int, key_offset: int, out_norm: bool) -> bool:
+    """Whether the backward keeps a token's rows resident (shape-only plan
+    query: an empty token range needs no pointers)."""
+    p = _lib.AttnresParams()
+    p.S, p.D, p.R, p.key_offset, p.N = S, D, R, key_offset, 0
+    p.eps, p.scale, p.out_norm, p.split_n_threshold, p.src_ld = 2.0 ** -23, 1.0, int(out_norm), 0, D
+    out = (ctypes.c_int64 * 8)()
+    rc = _lib.load().attnres_plan_info(ctypes.byref(p), out)
+    return rc == 0 and bool(out[5])
+
+
+def _as_values(values: List[Tensor], packed: int):
+    return values[0] if packed else list(values)
+
+
+@torch.library.custom_op(f"{_NS}::read_fwd", mutates_args=(), device_types="cuda")
+def read_fwd(values: List[Tensor], q: Tensor, w_o: Optional[Tensor], eps: float, scale: float,
+             key_offset: int) -> Tuple[Tensor, Tensor, Tensor, Tensor, Tensor, Tensor]:
+    S, D, packed, lead = _shape_info(values, q.numel())
+    save = w_o is not None and not _bwd_resident(S, D, q.numel(), key_offset, True)
+    r = _ops.attnres_fwd(_as_values(values, packed), q, w_o=w_o, eps=eps, scale=scale,
+                         key_offset=key_offset, save_o_pre=save)
+    dev = q.device
+    empty = torch.empty((0,), dtype=torch.float32, device=dev)
+    o_rstd = r["o_rstd"] if r["o_rstd"] is not None else empty
+    o_pre = r["o_pre"] if r["o_pre"] is not None else empty.clone()
+    return r["y"], r["alpha"], r["rstd"], r["logit"], o_rstd, o_pre
+
+
+@read_fwd.register_fake
+def _(values, q, w_o, eps, scale, key_offset):
+    S, D, packed, lead = _shape_info(values, q.numel())
+    N = 1
+    for d in lead:
+        N *= d
+    f32 = dict(dtype=torch.float32, device=q.device)
+    y = torch.empty((*lead, D), dtype=torch.bfloat16, device=q.device)
+    stats = [torch.empty((N, S), **f32) for _ in range(3)]
+    if w_o is not None:
+        o_rstd = torch.empty((N,), **f32)
+        save = not _bwd_resident(S, D, q.numel(), key_offset, True)
+        o_pre = torch.empty((N, D) if save else (0,), **f32)
+    else:
+        o_rstd = torch.empty((0,), **f32)
+        o_pre = torch.empty((0,), **f32)
+    return y, stats[0], stats[1], stats[2], o_rstd, o_pre
+
+
+@torch.library.custom_op(f"{_NS}::read_bwd", mutates_args=(), device_types="cuda")
+def read_bwd(values: List[Tensor], q: Tensor, w_o: Optional[Tensor], dy: Tensor, alpha: Tensor,
+             rstd: Tensor, logit: Tensor, o_rstd: Tensor, o_pre: Tensor, eps: float, scale: float,
+             key_offset: int) -> Tuple[List[Tensor], Tensor, Tensor]:
+    S, D, packed, lead = _shape_info(values, q.numel())
+    saved = {"alpha": alpha, "rstd": rstd, "logit": logit,
+             "o_rstd": o_rstd if o_rstd.numel() else None,
+             "o_pre": o_pre if o_pre.numel() else None}
+    g = _ops.attnres_bwd(_as_values(values, packed), q, dy.contiguous(), saved, w_o=w_o, eps=eps,
+                         scale=scale, key_offset=key_offset)
+    dv = [g["dvalues"]] if packed else list(g["dvalues"])
+    dw = g["dw_o"] if g["dw_o"] is not None else torch.empty((0,), dtype=torch.bfloat16, device=q.device)
+    return dv, g["dq"].view_as(q), dw
+
+
+@read_bwd.register_fake
+def _(values, q, w_o, dy, alpha, rstd, logit, o_rstd, o_pre, eps, scale, key_offset):
+    dv = [torch.empty_like(v) for v in values]
+    dw = torch.empty_like(w_o) if w_o is not None else torch.empty((0,), dtype=torch.bfloat16,
+                                                                   device=q.device)
+    return dv, torch.empty_like(q), dw
+
+
+def _setup_context(ctx, inputs, output):
+    values, q, w_o, eps, scale, key_offset = inputs
+    y, alpha, rstd, logit, o_rstd, o_pre = output
+    ctx.cfg = (eps, scale, key_offset)
+    ctx.has_w = w_o is not None
+    ctx.nvalues = len(values)
+    ctx.save_for_backward(q, w_o if w_o is not None else q.new_empty((0,)), alpha, rstd, logit,
+                          o_rstd, o_pre, *values)
+
+
+def _backward(ctx, dy, d_alpha, d_rstd, d_logit, d_orstd, d_opre):
+    q, w_o, alpha, rstd, logit, o_rstd, o_pre, *values = ctx.saved_tensors
+    eps, scale, key_offset = ctx.cfg
+    dv, dq, dw = read_bwd(list(values), q, w_o if ctx.has_w else None, dy.to(torch.bfloat16),
+                          alpha, rstd, logit, o_rstd, o_pre, eps, scale, key_offset)
+    return list(dv), dq, (dw if ctx.has_w else None), None, None, None
+
+
+read_fwd.register_autograd(_backward, setup_context=_setup_context)
+
+
+def attnres_op(values, query: Tensor, *, eps: float = _ops.EPS_DEFAULT, scale: float = 1.0,
+               out_norm_weight: Optional[Tensor] = None, key_offset: Optional[int] = None) -> Tensor:
+    """The read through the registered operator (compile- and graph-safe)."""
+    vals = [values] if isinstance(values, Tensor) else list(values)
+    D = vals[0].shape[-1]
+    ko = D - query.numel() if key_offset is None else int(key_offset)
+    y = read_fwd(vals, query, out_norm_weight, float(eps), float(scale), ko)[0]
+    return y

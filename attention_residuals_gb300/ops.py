@@ -288,35 +288,6 @@ def attnres_bwd_noalloc(values: Sources, q: torch.Tensor, dy: torch.Tensor, save
 # --------------------------------------------------------------------------
 # Autograd operator
 # --------------------------------------------------------------------------
-class _AttnResFn(torch.autograd.Function):
-    @staticmethod
-    def forward(ctx, q, w_o, cfg, *sources):
-        eps, scale, key_offset, packed = cfg
-        vals = sources[0] if packed else list(sources)
-        r = attnres_fwd(vals, q, w_o=w_o, eps=eps, scale=scale, key_offset=key_offset)
-        ctx.cfg = cfg
-        ctx.view = r["view"]
-        ctx.params = r["params"]
-        ctx.save_for_backward(q, w_o, r["alpha"], r["rstd"], r["logit"],
-                              r["o_rstd"], r["o_pre"], *sources)
-        return r["y"]
-
-    @staticmethod
-    def backward(ctx, dy):
-        q, w_o, alpha, rstd, logit, o_rstd, o_pre, *sources = ctx.saved_tensors
-        eps, scale, key_offset, packed = ctx.cfg
-        vals = sources[0] if packed else list(sources)
-        saved = {"alpha": alpha, "rstd": rstd, "logit": logit, "o_rstd": o_rstd, "o_pre": o_pre,
-                 "view": ctx.view}
-        g = attnres_bwd(vals, q, dy.to(torch.bfloat16), saved, w_o=w_o, eps=eps, scale=scale,
-                        key_offset=key_offset)
-        dq = g["dq"].view_as(q)
-        dw = g["dw_o"].view_as(w_o) if w_o is not None else None
-        if packed:
-            return (dq, dw, None, g["dvalues"])
-        return (dq, dw, None, *g["dvalues"])
-
-
 def attnres(values: Sources, query: torch.Tensor, *, eps: float = EPS_DEFAULT, scale: float = 1.0,
             out_norm_weight: Optional[torch.Tensor] = None,
             key_offset: Optional[int] = None) -> torch.Tensor:
@@ -327,9 +298,9 @@ def attnres(values: Sources, query: torch.Tensor, *, eps: float = EPS_DEFAULT, s
     tensors (a shared source may appear more than once; its gradients add).
     query: [R], 1 <= R <= D.  key_offset: first key channel (default D - R,
     the final R coordinates).  out_norm_weight: optional [D] weight of an
-    output RMSNorm."""
-    packed = isinstance(values, torch.Tensor)
-    cfg = (float(eps), float(scale), key_offset, packed)
-    if packed:
-        return _AttnResFn.apply(query, out_norm_weight, cfg, values)
-    return _AttnResFn.apply(query, out_norm_weight, cfg, *values)
+    output RMSNorm.  Differentiable in values, query and out_norm_weight;
+    runs through registered torch operators, so torch.compile(fullgraph=True)
+    and CUDA-graph capture work."""
+    from .custom_ops import attnres_op
+    return attnres_op(values, query, eps=eps, scale=scale, out_norm_weight=out_norm_weight,
+                      key_offset=key_offset)
