@@ -11,5 +11,9 @@ from .ops import (  # noqa: F401
     attnres_bwd_workspace_bytes,
     attnres_check_device_error,
     attnres_fwd,
+    attnres_multi,
+    attnres_multi_bwd,
+    attnres_multi_fwd,
+    attnres_multi_plan_info,
     attnres_plan_info,
 )

@@ -11,6 +11,7 @@ import threading
 
 MAX_S = 128
 MAX_D = 8192
+MAX_M = 16
 NOALLOC_SCRATCH_BYTES = 16 << 20
 DEFAULT_SPLIT_N = 16384
 
@@ -32,6 +33,10 @@ EXPORTED = [
     "attnres_check_device_error",
     "attnres_status_string",
     "attnres_plan_info",
+    "attnres_multi_fwd",
+    "attnres_multi_bwd",
+    "attnres_multi_bwd_workspace_bytes",
+    "attnres_multi_plan_info",
 ]
 
 
@@ -48,6 +53,15 @@ class AttnresParams(ctypes.Structure):
         ("split_n_threshold", ctypes.c_int32),
         ("src_ld", ctypes.c_int64),
         ("src", ctypes.c_void_p * MAX_S),
+    ]
+
+
+class AttnresMultiParams(ctypes.Structure):
+    _fields_ = [
+        ("base", AttnresParams),
+        ("M", ctypes.c_int32),
+        ("out_ld_m", ctypes.c_int64),
+        ("out_ld_n", ctypes.c_int64),
     ]
 
 
@@ -98,6 +112,16 @@ def load(path: str | None = None):
         lib.attnres_status_string.argtypes = [ctypes.c_int]
         lib.attnres_plan_info.restype = ctypes.c_int
         lib.attnres_plan_info.argtypes = [P, ctypes.POINTER(ctypes.c_int64)]
+        MP = ctypes.POINTER(AttnresMultiParams)
+        lib.attnres_multi_fwd.restype = ctypes.c_int
+        lib.attnres_multi_fwd.argtypes = [MP, vp, vp, fp, fp, fp, vp]
+        lib.attnres_multi_bwd_workspace_bytes.restype = sz
+        lib.attnres_multi_bwd_workspace_bytes.argtypes = [MP]
+        lib.attnres_multi_bwd.restype = ctypes.c_int
+        lib.attnres_multi_bwd.argtypes = [MP, vp, vp, fp, fp, fp, ctypes.POINTER(ctypes.c_void_p), i64,
+                                          vp, fp, vp, sz, vp]
+        lib.attnres_multi_plan_info.restype = ctypes.c_int
+        lib.attnres_multi_plan_info.argtypes = [MP, ctypes.POINTER(ctypes.c_int64)]
         _lib = lib
         return lib
 

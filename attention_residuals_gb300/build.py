@@ -21,7 +21,8 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 LIB_NAME = "libattnres_gb300.so"
 LIB_PATH = os.path.join(PKG, LIB_NAME)
-SOURCES = ["attnres_fwd.cu", "attnres_bwd.cu", "attnres_api.cu"]
+SOURCES = ["attnres_fwd.cu", "attnres_bwd.cu", "attnres_multi_fwd.cu", "attnres_multi_bwd.cu",
+           "attnres_api.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

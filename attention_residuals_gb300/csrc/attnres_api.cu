@@ -163,6 +163,114 @@ bool ranges_overlap(const void* a, size_t na, const void* b, size_t nb) {
     return x < y + nb && y < x + na;
 }
 
+// Gradient rows: present, 16-byte aligned, disjoint from each other and from
+// every source.
+attnres_status check_dsrc(const attnres_params* p, void* const* dsrc, int64_t dsrc_ld) {
+    if (dsrc_ld < p->D) return ATTNRES_ERR_INVALID_ARG;
+    if (dsrc_ld % 8 != 0) return ATTNRES_ERR_ALIGNMENT;
+    const size_t n_rows = static_cast<size_t>(p->N);
+    const size_t d_bytes = n_rows == 0 ? 0 : ((n_rows - 1) * static_cast<size_t>(dsrc_ld) + p->D) * 2;
+    const size_t s_bytes = n_rows == 0 ? 0 : ((n_rows - 1) * static_cast<size_t>(p->src_ld) + p->D) * 2;
+    for (int s = 0; s < p->S; ++s) {
+        if (!dsrc[s]) return ATTNRES_ERR_INVALID_ARG;
+        if (!aligned16(dsrc[s])) return ATTNRES_ERR_ALIGNMENT;
+    }
+    for (int s = 0; s < p->S; ++s) {
+        for (int t = 0; t < p->S; ++t) {
+            if (t != s && ranges_overlap(dsrc[s], d_bytes, dsrc[t], d_bytes)) return ATTNRES_ERR_INVALID_ARG;
+            if (ranges_overlap(dsrc[s], d_bytes, p->src[t], s_bytes)) return ATTNRES_ERR_INVALID_ARG;
+        }
+    }
+    return ATTNRES_OK;
+}
+
+// ---------------------------------------------------------------- multi-query
+attnres_status check_multi(const attnres_multi_params* p) {
+    if (!p) return ATTNRES_ERR_INVALID_ARG;
+    const attnres_status st = check_shape(&p->base);
+    if (st != ATTNRES_OK) return st;
+    if (p->M < 1 || p->M > ATTNRES_MAX_M) return ATTNRES_ERR_INVALID_ARG;
+    if (p->base.out_norm) return ATTNRES_ERR_UNSUPPORTED;
+    if (p->out_ld_m < 0 || p->out_ld_n < 0) return ATTNRES_ERR_INVALID_ARG;
+    if (p->out_ld_m % 8 != 0 || p->out_ld_n % 8 != 0) return ATTNRES_ERR_ALIGNMENT;
+    return ATTNRES_OK;
+}
+
+int pow2_ceil(int x) {
+    int p = 1;
+    while (p < x) p <<= 1;
+    return p;
+}
+
+// Chunk ring for a resident token: the fewest chunks per token that leave
+// room for one more chunk (so the next token starts loading), then as many
+// chunks as fit; as a last resort the token alone.
+template <typename F>
+bool pick_ring(int S, F&& fits, int* rows, int* chunks) {
+    for (int extra = 1; extra >= 0; --extra) {
+        for (int cpt = 1; cpt <= S; ++cpt) {
+            const int G = (S + cpt - 1) / cpt;
+            if ((S + G - 1) / G != cpt) continue;
+            if (!fits(cpt + extra, G)) continue;
+            int K = cpt + extra;
+            while (K < kMaxChunks && fits(K + 1, G)) ++K;
+            *rows = G;
+            *chunks = K;
+            return true;
+        }
+    }
+    return false;
+}
+
+attnres_status make_multi_plan(const attnres_multi_params* p, MultiPlan* plan) {
+    DeviceInfo dev;
+    if (!device_info(&dev)) return ATTNRES_ERR_CUDA;
+    const attnres_params& b = p->base;
+    MultiPlan pl{};
+    const int ncv = b.D / 8;
+    pl.vpt = ncv <= 256 ? 1 : (ncv <= 512 ? 2 : 4);
+    pl.ncw = (ncv + 32 * pl.vpt - 1) / (32 * pl.vpt);
+    if (pl.ncw < 1 || pl.ncw > kMaxConsumerWarps) return ATTNRES_ERR_UNSUPPORTED;
+    const int M = p->M;
+    const int p2 = pow2_ceil(M);
+    pl.mb_f = p2 < (pl.vpt <= 2 ? 4 : 2) ? p2 : (pl.vpt <= 2 ? 4 : 2);
+    pl.mb_b = p2 < 4 / pl.vpt ? p2 : 4 / pl.vpt;
+    pl.slot_bytes = static_cast<int>(align_up(static_cast<uint32_t>(b.D) * 2u, 128u));
+    pl.s_pad = static_cast<int>(align_up(static_cast<uint32_t>(b.S), 4u));
+    pl.m_pad = static_cast<int>(align_up(static_cast<uint32_t>(M), 4u));
+    pl.kv0 = b.key_offset / 8;
+    pl.nkv = (b.key_offset + b.R + 7) / 8 - pl.kv0;
+    const uint32_t optin = static_cast<uint32_t>(dev.smem_optin);
+    auto ffits = [&](int K, int G) {
+        return make_multi_layout(K, G, pl.slot_bytes, M, 0, pl.s_pad, pl.m_pad, pl.nkv, 0, false).total <= optin;
+    };
+    if (!pick_ring(b.S, ffits, &pl.f_rows, &pl.f_chunks)) return ATTNRES_ERR_UNSUPPORTED;
+    const int nmb = (M + pl.mb_b - 1) / pl.mb_b;
+    const int dq_nkv = nmb > 1 ? pl.nkv : 0;
+    bool ok = false;
+    for (int ds = 2; ds >= 1 && !ok; --ds) {
+        auto bfits = [&](int K, int G) {
+            return make_multi_layout(K, G, pl.slot_bytes, M, ds, pl.s_pad, pl.m_pad, pl.nkv, dq_nkv, true).total <=
+                   optin;
+        };
+        if (pick_ring(b.S, bfits, &pl.b_rows, &pl.b_chunks)) {
+            pl.dy_slots = ds;
+            ok = true;
+        }
+    }
+    if (!ok) return ATTNRES_ERR_UNSUPPORTED;
+    pl.smem_fwd = make_multi_layout(pl.f_chunks, pl.f_rows, pl.slot_bytes, M, 0, pl.s_pad, pl.m_pad, pl.nkv, 0,
+                                    false).total;
+    pl.smem_bwd = make_multi_layout(pl.b_chunks, pl.b_rows, pl.slot_bytes, M, pl.dy_slots, pl.s_pad, pl.m_pad,
+                                    pl.nkv, dq_nkv, true).total;
+    long long grid = dev.sm_count;
+    if (b.N < grid) grid = b.N;
+    pl.grid = static_cast<int>(grid < 1 ? 1 : grid);
+    pl.ws_bytes = b.N == 0 ? 0 : static_cast<size_t>(pl.grid) * M * b.R * 4;
+    *plan = pl;
+    return ATTNRES_OK;
+}
+
 }  // namespace
 }  // namespace attnres
 
@@ -277,8 +385,6 @@ attnres_status attnres_bwd(const attnres_params* p, const void* q, const void* w
     if (!q || !dy || !alpha || !rstd || !logit || !dsrc || !dq) return ATTNRES_ERR_INVALID_ARG;
     if (p->out_norm && (!w_o || !o_rstd || !dw_o)) return ATTNRES_ERR_INVALID_ARG;
     if (!p->out_norm && o_pre) return ATTNRES_ERR_INVALID_ARG;
-    if (dsrc_ld < p->D) return ATTNRES_ERR_INVALID_ARG;
-    if (dsrc_ld % 8 != 0) return ATTNRES_ERR_ALIGNMENT;
     if (!aligned16(dy) || !aligned4(alpha) || !aligned4(rstd) || !aligned4(logit))
         return ATTNRES_ERR_ALIGNMENT;
     if (p->out_norm && !aligned4(o_rstd)) return ATTNRES_ERR_ALIGNMENT;
@@ -287,22 +393,8 @@ attnres_status attnres_bwd(const attnres_params* p, const void* q, const void* w
         (dq_f32 && !aligned4(dq_f32)) || (dw_o && (reinterpret_cast<uintptr_t>(dw_o) & 1u)) ||
         (dw_o_f32 && !aligned4(dw_o_f32)) || (w_o && (reinterpret_cast<uintptr_t>(w_o) & 1u)))
         return ATTNRES_ERR_ALIGNMENT;
-    const size_t n_rows = static_cast<size_t>(p->N);
-    const size_t d_bytes = n_rows == 0 ? 0 : ((n_rows - 1) * static_cast<size_t>(dsrc_ld) + p->D) * 2;
-    const size_t s_bytes = n_rows == 0 ? 0 : ((n_rows - 1) * static_cast<size_t>(p->src_ld) + p->D) * 2;
-    for (int s = 0; s < p->S; ++s) {
-        if (!dsrc[s]) return ATTNRES_ERR_INVALID_ARG;
-        if (!aligned16(dsrc[s])) return ATTNRES_ERR_ALIGNMENT;
-    }
-    {
-        for (int s = 0; s < p->S; ++s) {
-            for (int t = 0; t < p->S; ++t) {
-                if (t != s && ranges_overlap(dsrc[s], d_bytes, dsrc[t], d_bytes))
-                    return ATTNRES_ERR_INVALID_ARG;
-                if (ranges_overlap(dsrc[s], d_bytes, p->src[t], s_bytes)) return ATTNRES_ERR_INVALID_ARG;
-            }
-        }
-    }
+    st = check_dsrc(p, dsrc, dsrc_ld);
+    if (st != ATTNRES_OK) return st;
     Plan pl;
     st = make_plan(p, &pl);
     if (st != ATTNRES_OK) return st;
@@ -412,8 +504,148 @@ attnres_status attnres_check_device_error(void) {
     if (cudaDeviceSynchronize() != cudaSuccess) return ATTNRES_ERR_CUDA;
     const unsigned f = take_fwd_error();
     const unsigned b = take_bwd_error();
-    if (f == 0xffffffffu || b == 0xffffffffu) return ATTNRES_ERR_CUDA;
-    return (f || b) ? ATTNRES_ERR_DEVICE : ATTNRES_OK;
+    const unsigned mf = take_multi_fwd_error();
+    const unsigned mb = take_multi_bwd_error();
+    if (f == 0xffffffffu || b == 0xffffffffu || mf == 0xffffffffu || mb == 0xffffffffu) return ATTNRES_ERR_CUDA;
+    return (f || b || mf || mb) ? ATTNRES_ERR_DEVICE : ATTNRES_OK;
+}
+
+// ---------------------------------------------------------------------------
+// Multi-query read.
+// ---------------------------------------------------------------------------
+attnres_status attnres_multi_plan_info(const attnres_multi_params* p, int64_t out[8]) {
+    attnres_status st = check_multi(p);
+    if (st != ATTNRES_OK) return st;
+    if (!out) return ATTNRES_ERR_INVALID_ARG;
+    MultiPlan pl;
+    st = make_multi_plan(p, &pl);
+    if (st != ATTNRES_OK) return st;
+    out[0] = pl.grid;
+    out[1] = pl.ncw;
+    out[2] = pl.vpt;
+    out[3] = pl.mb_f * 1000 + pl.mb_b;
+    out[4] = pl.f_chunks * 1000 + pl.f_rows;
+    out[5] = pl.b_chunks * 1000 + pl.b_rows;
+    out[6] = pl.dy_slots;
+    out[7] = static_cast<int64_t>(pl.smem_bwd);
+    return ATTNRES_OK;
+}
+
+attnres_status attnres_multi_fwd(const attnres_multi_params* p, const void* q, void* y, float* alpha,
+                                 float* rstd, float* logit, void* stream) {
+    attnres_status st = check_multi(p);
+    if (st != ATTNRES_OK) return st;
+    const attnres_params& b = p->base;
+    if (b.N == 0) return ATTNRES_OK;
+    if (!q || !y || !alpha || !rstd || !logit) return ATTNRES_ERR_INVALID_ARG;
+    if (!aligned16(y) || !aligned4(alpha) || !aligned4(rstd) || !aligned4(logit) ||
+        (reinterpret_cast<uintptr_t>(q) & 1u))
+        return ATTNRES_ERR_ALIGNMENT;
+    MultiPlan pl;
+    st = make_multi_plan(p, &pl);
+    if (st != ATTNRES_OK) return st;
+    MultiFwdArgs a;
+    std::memset(&a, 0, sizeof a);
+    for (int s = 0; s < b.S; ++s) a.src[s] = b.src[s];
+    a.N = b.N;
+    a.src_ld = b.src_ld;
+    a.y_ms = p->out_ld_m;
+    a.y_ns = p->out_ld_n;
+    a.S = b.S;
+    a.D = b.D;
+    a.R = b.R;
+    a.ko = b.key_offset;
+    a.M = p->M;
+    a.eps = b.eps;
+    a.scale = b.scale;
+    a.chunks = pl.f_chunks;
+    a.rows = pl.f_rows;
+    a.slot_bytes = pl.slot_bytes;
+    a.ncw = pl.ncw;
+    a.s_pad = pl.s_pad;
+    a.m_pad = pl.m_pad;
+    a.kv0 = pl.kv0;
+    a.nkv = pl.nkv;
+    a.q = static_cast<const uint16_t*>(q);
+    a.y = static_cast<uint16_t*>(y);
+    a.alpha = alpha;
+    a.rstd = rstd;
+    a.logit = logit;
+    return launch_multi_fwd(pl, a, static_cast<cudaStream_t>(stream)) == cudaSuccess ? ATTNRES_OK
+                                                                                    : ATTNRES_ERR_CUDA;
+}
+
+size_t attnres_multi_bwd_workspace_bytes(const attnres_multi_params* p) {
+    if (check_multi(p) != ATTNRES_OK) return 0;
+    MultiPlan pl;
+    if (make_multi_plan(p, &pl) != ATTNRES_OK) return 0;
+    return pl.ws_bytes;
+}
+
+attnres_status attnres_multi_bwd(const attnres_multi_params* p, const void* q, const void* dy,
+                                 const float* alpha, const float* rstd, const float* logit,
+                                 void* const* dsrc, int64_t dsrc_ld, void* dq, float* dq_f32,
+                                 void* workspace, size_t workspace_bytes, void* stream) {
+    attnres_status st = check_multi(p);
+    if (st != ATTNRES_OK) return st;
+    const attnres_params& b = p->base;
+    cudaStream_t s0 = static_cast<cudaStream_t>(stream);
+    const size_t nq = static_cast<size_t>(p->M) * static_cast<size_t>(b.R);
+    if (!dq) return ATTNRES_ERR_INVALID_ARG;
+    if ((reinterpret_cast<uintptr_t>(dq) & 1u) || (dq_f32 && !aligned4(dq_f32))) return ATTNRES_ERR_ALIGNMENT;
+    if (b.N == 0) {
+        if (cudaMemsetAsync(dq, 0, nq * 2, s0) != cudaSuccess ||
+            (dq_f32 && cudaMemsetAsync(dq_f32, 0, nq * 4, s0) != cudaSuccess))
+            return ATTNRES_ERR_CUDA;
+        return ATTNRES_OK;
+    }
+    if (!q || !dy || !alpha || !rstd || !logit || !dsrc) return ATTNRES_ERR_INVALID_ARG;
+    if (!aligned16(dy) || !aligned4(alpha) || !aligned4(rstd) || !aligned4(logit) ||
+        (reinterpret_cast<uintptr_t>(q) & 1u))
+        return ATTNRES_ERR_ALIGNMENT;
+    st = check_dsrc(&b, dsrc, dsrc_ld);
+    if (st != ATTNRES_OK) return st;
+    MultiPlan pl;
+    st = make_multi_plan(p, &pl);
+    if (st != ATTNRES_OK) return st;
+    if (!workspace || workspace_bytes < pl.ws_bytes) return ATTNRES_ERR_WORKSPACE;
+    if (!aligned16(workspace)) return ATTNRES_ERR_ALIGNMENT;
+    MultiBwdArgs a;
+    std::memset(&a, 0, sizeof a);
+    for (int s = 0; s < b.S; ++s) {
+        a.src[s] = b.src[s];
+        a.dsrc[s] = dsrc[s];
+    }
+    a.N = b.N;
+    a.src_ld = b.src_ld;
+    a.dsrc_ld = dsrc_ld;
+    a.dy_ms = p->out_ld_m;
+    a.dy_ns = p->out_ld_n;
+    a.S = b.S;
+    a.D = b.D;
+    a.R = b.R;
+    a.ko = b.key_offset;
+    a.M = p->M;
+    a.eps = b.eps;
+    a.scale = b.scale;
+    a.chunks = pl.b_chunks;
+    a.rows = pl.b_rows;
+    a.slot_bytes = pl.slot_bytes;
+    a.dy_slots = pl.dy_slots;
+    a.ncw = pl.ncw;
+    a.s_pad = pl.s_pad;
+    a.m_pad = pl.m_pad;
+    a.kv0 = pl.kv0;
+    a.nkv = pl.nkv;
+    a.q = static_cast<const uint16_t*>(q);
+    a.dy = static_cast<const uint16_t*>(dy);
+    a.alpha = alpha;
+    a.rstd = rstd;
+    a.logit = logit;
+    a.part = static_cast<float*>(workspace);
+    a.dq = static_cast<uint16_t*>(dq);
+    a.dq_f32 = dq_f32;
+    return launch_multi_bwd(pl, a, s0) == cudaSuccess ? ATTNRES_OK : ATTNRES_ERR_CUDA;
 }
 
 }  // extern "C"

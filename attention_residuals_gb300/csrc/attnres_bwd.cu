@@ -663,6 +663,12 @@ cudaError_t dispatch_key(const Plan& plan, const BwdArgs& a, cudaStream_t stream
 
 }  // namespace
 
+cudaError_t launch_finalize(const float* part, int P, int R, int W, uint16_t* dq, float* dq_f32,
+                            uint16_t* dw_o, float* dw_o_f32, cudaStream_t stream) {
+    attnres_finalize_kernel<<<(W + 255) / 256, 256, 0, stream>>>(part, P, R, W, dq, dq_f32, dw_o, dw_o_f32);
+    return cudaGetLastError();
+}
+
 unsigned take_bwd_error() {
     unsigned v = 0, zero = 0;
     if (cudaMemcpyFromSymbol(&v, g_bwd_error, sizeof v) != cudaSuccess) return 0xffffffffu;

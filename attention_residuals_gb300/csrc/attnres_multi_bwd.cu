@@ -1,0 +1,607 @@
+// attnres_multi_bwd.cu -- backward kernel of the multi-query read.
+//
+// Each query m is an independent read of the same sources ("Fast Attention
+// Residuals", section "Multi-query AttnRes"), so with the forward's saved
+// alpha_ms, logit z_ms and key statistics r_s (chain rule through section
+// "Equation", per query):
+//   da_ms  = <dy_m, v_s>,  delta_m = sum_s alpha_ms da_ms,
+//   dz_ms  = alpha_ms (da_ms - delta_m)
+//   b_ms   = scale r_s dz_ms,   c_s = -(r_s^2 / R) sum_m dz_ms z_ms
+//   dv_s   = sum_m alpha_ms dy_m  +  on key channels: sum_m b_ms q_m + c_s t_s
+//   dq_m  += sum_s b_ms t_s                      (summed over tokens)
+// The sources feed every query, so their gradient is the sum over queries.
+//
+// GB300 mapping.  One persistent CTA per SM.  A producer warp streams each
+// token's S source rows (1-D TMA into a chunk ring), its M dy rows (one TMA
+// group per token into a dy ring) and its saved statistics (cp.async into a
+// two-slot ring).  The token stays resident for all passes:
+//   dot pass: one warp per source row, lanes over the row's vectors, mixed-
+//             precision bf16 FMAs against every dy row, reduce-scatter per
+//             four queries;
+//   coefficients: after a CTA barrier, one warp per query forms delta_m,
+//             b_ms and its share of c_s into shared tables;
+//   write pass: after a second barrier, thread t owns fixed 16-byte column
+//             vectors; it forms dv_s for every source with the dy rows and
+//             query vectors held in registers (queries in register blocks of
+//             MB when M > MB), stores each row once, and accumulates its dq
+//             columns.
+// dq: with one register block the per-thread dq sums stay in registers for
+// all of the CTA's tokens; with several they accumulate in shared memory.
+// Each CTA writes one FP32 partial row [M * R]; a finalize kernel adds the
+// rows in CTA order (bitwise reproducible).
+#include <cfloat>
+
+#include "device_utils.cuh"
+#include "kernels.cuh"
+
+namespace attnres {
+namespace {
+
+// First failed wait of any multi-query backward launch (0 = none).
+__device__ unsigned int g_multi_bwd_error = 0;
+
+__device__ __forceinline__ float2 key_part(const float2 x, unsigned mask, int kk) {
+    return make_float2((mask >> (2 * kk)) & 1u ? x.x : 0.0f, (mask >> (2 * kk + 1)) & 1u ? x.y : 0.0f);
+}
+
+template <int VPT, int MB>
+__global__ void __launch_bounds__(kMaxThreads, 1) attnres_multi_bwd_kernel(const __grid_constant__ MultiBwdArgs a) {
+    extern __shared__ __align__(128) unsigned char smem[];
+    const int ncw = a.ncw;
+    const int nct = ncw * 32;
+    const int K = a.chunks;
+    const int G = a.rows;
+    const int S = a.S;
+    const int M = a.M;
+    const int DS = a.dy_slots;
+    const int s_pad = a.s_pad, m_pad = a.m_pad;
+    const int nmb = (M + MB - 1) / MB;
+    const MultiLayout L =
+        make_multi_layout(K, G, a.slot_bytes, M, DS, s_pad, m_pad, a.nkv, nmb > 1 ? a.nkv : 0, true);
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem + L.full);
+    uint64_t* empty = reinterpret_cast<uint64_t*>(smem + L.empty);
+    uint64_t* dyfull = reinterpret_cast<uint64_t*>(smem + L.dyfull);
+    uint64_t* dyempty = reinterpret_cast<uint64_t*>(smem + L.dyempty);
+    uint64_t* tfull = reinterpret_cast<uint64_t*>(smem + L.tfull);
+    uint64_t* tempty = reinterpret_cast<uint64_t*>(smem + L.tempty);
+    float* tok = reinterpret_cast<float*>(smem + L.tok);
+    float* da_t = reinterpret_cast<float*>(smem + L.tab);  // [m_pad][s_pad]
+    float* al_t = da_t + m_pad * s_pad;                    // [s_pad][m_pad]
+    float* b_t = al_t + s_pad * m_pad;                     // [s_pad][m_pad]
+    float* zr_t = b_t + s_pad * m_pad;                     // [m_pad][s_pad]
+    float* dqsm = reinterpret_cast<float*>(smem + L.dqsm);  // [M][nkv * 8] (several blocks)
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L.misc);
+    const int tstride = static_cast<int>(L.tstride);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const long long N = a.N;
+    const int D = a.D;
+    const int MS = M * S;
+    const uint32_t sb = static_cast<uint32_t>(a.slot_bytes);
+    const uint32_t cb = static_cast<uint32_t>(G) * sb;
+    const int cpt = (S + G - 1) / G;
+
+    if (threadIdx.x == 0) {
+        for (int k = 0; k < K; ++k) {
+            mbar_init(full + k, 1);
+            mbar_init(empty + k, ncw);
+        }
+        for (int k = 0; k < DS; ++k) {
+            mbar_init(dyfull + k, 1);
+            mbar_init(dyempty + k, ncw);
+        }
+        for (int k = 0; k < kMultiTokSlots; ++k) {
+            mbar_init(tfull + k, 32);
+            mbar_init(tempty + k, ncw);
+        }
+        *abort_flag = 0;
+        mbar_fence_init();
+    }
+    // coefficients of padded queries stay zero; dq sums start at zero
+    for (int i = threadIdx.x; i < 2 * s_pad * m_pad; i += blockDim.x) al_t[i] = 0.0f;
+    if (nmb > 1)
+        for (int i = threadIdx.x; i < M * a.nkv * 8; i += blockDim.x) dqsm[i] = 0.0f;
+    __syncthreads();
+
+    if (warp == ncw) {
+        // ------------------------------------------------------ producer
+        const uint64_t pol = policy_evict_first();
+        const uint32_t row_bytes = static_cast<uint32_t>(D) * 2u;
+        unsigned char* ring = smem + L.ring;
+        unsigned char* dyring = smem + L.dyring;
+        int k = 0;
+        uint32_t phase = 0;
+        int dk = 0;
+        uint32_t dphase = 0;
+        int ts = 0;
+        uint32_t tphase = 0;
+        long long issued = 0, dy_issued = 0;
+        for (long long n = blockIdx.x; n < N; n += gridDim.x) {
+            if (*abort_flag) break;
+            // saved statistics -> tok[ts] (all 32 lanes arrive on tfull)
+            mbar_wait(tempty + ts, tphase ^ 1u, abort_flag, &g_multi_bwd_error, kSiteBwdProducer);
+            float* dst = tok + ts * tstride;
+            for (int e = lane; e < MS; e += 32) {
+                cp_async_4(dst + e, a.alpha + n * MS + e);
+                cp_async_4(dst + MS + e, a.logit + n * MS + e);
+            }
+            for (int e = lane; e < S; e += 32) cp_async_4(dst + 2 * MS + e, a.rstd + n * S + e);
+            cp_async_arrive_noinc(tfull + ts);
+            if (++ts == kMultiTokSlots) {
+                ts = 0;
+                tphase ^= 1u;
+            }
+            if (lane == 0) {
+                if (mbar_wait(dyempty + dk, dphase ^ 1u, abort_flag, &g_multi_bwd_error, kSiteBwdProducer)) {
+                    mbar_arrive_expect_tx(dyfull + dk, row_bytes * static_cast<uint32_t>(M));
+                    for (int m = 0; m < M; ++m)
+                        tma_load_1d(dyring + (dk * M + m) * sb, a.dy + m * a.dy_ms + n * a.dy_ns, row_bytes,
+                                    dyfull + dk, pol);
+                    ++dy_issued;
+                    if (++dk == DS) {
+                        dk = 0;
+                        dphase ^= 1u;
+                    }
+                }
+                for (int g0 = 0; g0 < S && !*abort_flag; g0 += G) {
+                    const int gs = min(G, S - g0);
+                    if (!mbar_wait(empty + k, phase ^ 1u, abort_flag, &g_multi_bwd_error, kSiteBwdProducer)) break;
+                    mbar_arrive_expect_tx(full + k, row_bytes * static_cast<uint32_t>(gs));
+                    for (int r = 0; r < gs; ++r) {
+                        const unsigned char* src =
+                            static_cast<const unsigned char*>(a.src[g0 + r]) + (n * a.src_ld) * 2;
+                        tma_load_1d(ring + k * cb + r * sb, src, row_bytes, full + k, pol);
+                    }
+                    ++issued;
+                    if (++k == K) {
+                        k = 0;
+                        phase ^= 1u;
+                    }
+                }
+            }
+            __syncwarp();
+        }
+        asm volatile("cp.async.wait_all;" ::: "memory");
+        if (lane == 0 && *abort_flag) {
+            for (int c = 0; c < K && c < issued; ++c) {
+                const long long fills = (issued - 1 - c) / K + 1;
+                volatile int no_abort = 0;
+                mbar_wait(full + c, static_cast<uint32_t>((fills - 1) & 1), &no_abort, &g_multi_bwd_error, kSiteDrain);
+            }
+            for (int c = 0; c < DS && c < dy_issued; ++c) {
+                const long long fills = (dy_issued - 1 - c) / DS + 1;
+                volatile int no_abort = 0;
+                mbar_wait(dyfull + c, static_cast<uint32_t>((fills - 1) & 1), &no_abort, &g_multi_bwd_error, kSiteDrain);
+            }
+        }
+        return;
+    }
+
+    // ---------------------------------------------------------- consumers
+    const int ncv = D >> 3;
+    const int ko = a.ko, kend = a.ko + a.R;
+    const int kv0 = a.kv0, nkv = a.nkv;
+    const int kw = nkv * 8;
+    const uint32_t kwb = static_cast<uint32_t>(nkv) * 16u;
+    int col[VPT];
+    int kvi[VPT];        // key vector index within the key window, -1 outside
+    unsigned kmask[VPT];  // key channels of the vector (bit e = channel 8*col + e)
+#pragma unroll
+    for (int i = 0; i < VPT; ++i) {
+        const int c = threadIdx.x + i * nct;
+        col[i] = c < ncv ? c : -1;
+        kvi[i] = (col[i] >= kv0 && col[i] < kv0 + nkv) ? col[i] - kv0 : -1;
+        unsigned m = 0;
+        for (int e = 0; e < 8; ++e) {
+            const int j = 8 * c + e;
+            if (kvi[i] >= 0 && j >= ko && j < kend) m |= 1u << e;
+        }
+        kmask[i] = m;
+    }
+    const float inv_r = 1.0f / static_cast<float>(a.R);
+    const float scale = a.scale;
+
+    const uint32_t sbase = smem_u32(smem);
+    const uint32_t voff = static_cast<uint32_t>(col[0] < 0 ? 0 : col[0]) * 16u;
+    const uint32_t vstep = static_cast<uint32_t>(nct) * 16u;
+    const uint32_t ring_raw = sbase + L.ring;
+    const uint32_t ring_lo = ring_raw + voff;
+    const uint32_t dy_raw = sbase + L.dyring;
+    const uint32_t full_s = sbase + L.full;
+    const uint32_t empty_s = sbase + L.empty;
+    const uint32_t dyfull_s = sbase + L.dyfull;
+    const uint32_t dyempty_s = sbase + L.dyempty;
+    const uint32_t tfull_s = sbase + L.tfull;
+    const uint32_t tempty_s = sbase + L.tempty;
+    const uint32_t qsm_s = sbase + L.qsm;
+    {
+        uint16_t* qsm = reinterpret_cast<uint16_t*>(smem + L.qsm);
+        for (int i = threadIdx.x; i < m_pad * kw; i += nct) {
+            const int m = i / kw;
+            const int c = 8 * kv0 + (i - m * kw);
+            qsm[i] = (m < M && c >= ko && c < kend) ? a.q[static_cast<long long>(m) * a.R + (c - ko)]
+                                                    : static_cast<uint16_t>(0);
+        }
+    }
+    // One register block: the query values at the owned key vectors and the
+    // dq sums live in registers for the whole launch.
+    float2 qf[MB][VPT][4];
+    float2 dqa[MB][VPT][4];
+#pragma unroll
+    for (int j = 0; j < MB; ++j)
+#pragma unroll
+        for (int i = 0; i < VPT; ++i)
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk) {
+                float qv[2];
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    const int e = 2 * kk + h;
+                    const bool in = nmb == 1 && j < M && ((kmask[i] >> e) & 1u);
+                    qv[h] = in ? bf16_bits_to_float(a.q[static_cast<long long>(j) * a.R + (8 * col[i] + e - ko)])
+                               : 0.0f;
+                }
+                qf[j][i][kk] = make_float2(qv[0], qv[1]);
+                dqa[j][i][kk] = make_float2(0.0f, 0.0f);
+            }
+    named_bar_sync(1, nct);
+
+    int ck = 0;
+    uint32_t cphase = 0;
+    int dk = 0;
+    uint32_t dphase = 0;
+    int ts = 0;
+    uint32_t tphase = 0;
+    for (long long n = blockIdx.x; n < N; n += gridDim.x) {
+        {
+            int k = ck;
+            uint32_t ph = cphase;
+            for (int c = 0; c < cpt; ++c) {
+                mbar_wait_s(full_s + 8u * k, ph, abort_flag, &g_multi_bwd_error, kSiteBwdConsumer);
+                if (++k == K) {
+                    k = 0;
+                    ph ^= 1u;
+                }
+            }
+            mbar_wait_s(dyfull_s + 8u * dk, dphase, abort_flag, &g_multi_bwd_error, kSiteBwdConsumer);
+            mbar_wait_s(tfull_s + 8u * ts, tphase, abort_flag, &g_multi_bwd_error, kSiteBwdTokStat);
+        }
+        const uint32_t dyb = dy_raw + static_cast<uint32_t>(dk * M) * sb;
+        // dot pass: da_ms = <dy_m, v_s>, one warp per source row
+        for (int r = warp; r < S; r += ncw) {
+            int kc = ck + r / G;
+            if (kc >= K) kc -= K;
+            const uint32_t row = ring_raw + static_cast<uint32_t>(kc) * cb + static_cast<uint32_t>(r % G) * sb;
+            for (int m4 = 0; m4 < M; m4 += 4) {
+                float t[4][2];
+#pragma unroll
+                for (int j = 0; j < 4; ++j) t[j][0] = t[j][1] = 0.0f;
+                for (int v = lane; v < ncv; v += 32) {
+                    const uint4 x = lds128(row + 16u * v);
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        if (m4 + j < M) {
+                            const uint4 y = lds128(dyb + static_cast<uint32_t>(m4 + j) * sb + 16u * v);
+                            bf16_dot8(x, y, t[j][0], t[j][1]);
+                        }
+                    }
+                }
+                float part[4] = {t[0][0] + t[0][1], t[1][0] + t[1][1], t[2][0] + t[2][1], t[3][0] + t[3][1]};
+                warp_reduce_scatter<4>(part, lane);
+                if ((lane & 7) == 0) {
+                    const int e = lane >> 3;
+                    if (m4 + e < M) da_t[(m4 + e) * s_pad + r] = part[0];
+                }
+            }
+        }
+        named_bar_sync(1, nct);
+        // coefficients: one warp per query, lanes over sources
+        {
+            const float* tk = tok + ts * tstride;
+            for (int m = warp; m < M; m += ncw) {
+                float al[4], da[4], z[4], rs[4];
+                float p = 0.0f;
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const int s = lane + 32 * i;
+                    al[i] = da[i] = z[i] = rs[i] = 0.0f;
+                    if (s < S) {
+                        al[i] = tk[m * S + s];
+                        z[i] = tk[MS + m * S + s];
+                        rs[i] = tk[2 * MS + s];
+                        da[i] = da_t[m * s_pad + s];
+                        p = fmaf(al[i], da[i], p);
+                    }
+                }
+                const float delta = warp_sum(p);
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const int s = lane + 32 * i;
+                    if (s < S) {
+                        const float dz = al[i] * (da[i] - delta);
+                        al_t[s * m_pad + m] = al[i];
+                        b_t[s * m_pad + m] = scale * rs[i] * dz;
+                        zr_t[m * s_pad + s] = -(dz * z[i]) * (rs[i] * rs[i]) * inv_r;
+                    }
+                }
+            }
+        }
+        named_bar_sync(1, nct);
+        if (lane == 0) mbar_arrive_s(tempty_s + 8u * ts);
+
+        // write pass: dv_s for every source row, one store per row
+        if (nmb == 1) {
+            float2 dyf[MB][VPT][4];
+            uint32_t ddep = 0;
+#pragma unroll
+            for (int j = 0; j < MB; ++j)
+#pragma unroll
+                for (int i = 0; i < VPT; ++i) {
+                    uint4 yv = make_uint4(0u, 0u, 0u, 0u);
+                    if (j < M && col[i] >= 0) {
+                        yv = lds128(dyb + static_cast<uint32_t>(j) * sb + voff + i * vstep);
+                        ddep ^= yv.x;
+                    }
+#pragma unroll
+                    for (int kk = 0; kk < 4; ++kk) dyf[j][i][kk] = bf2_to_f2(u4_get(yv, kk));
+                }
+            __syncwarp();
+            if (lane == 0) mbar_arrive_after(dyempty_s + 8u * dk, ddep);
+            int kc = ck;
+            for (int r0 = 0; r0 < S; r0 += G) {
+                const int rn = min(G, S - r0);
+                uint32_t dep = 0;
+                uint32_t rowa = ring_lo + static_cast<uint32_t>(kc) * cb;
+                for (int r = 0; r < rn; ++r) {
+                    const int s = r0 + r;
+                    float2 al2[MB], bl2[MB];
+#pragma unroll
+                    for (int j = 0; j < MB; ++j) {
+                        const float av = al_t[s * m_pad + j], bv = b_t[s * m_pad + j];
+                        al2[j] = make_float2(av, av);
+                        bl2[j] = make_float2(bv, bv);
+                    }
+                    float cs = 0.0f;
+                    for (int m = 0; m < M; ++m) cs += zr_t[m * s_pad + s];
+                    const float2 cs2 = make_float2(cs, cs);
+                    uint16_t* drow = static_cast<uint16_t*>(a.dsrc[s]) + n * a.dsrc_ld;
+#pragma unroll
+                    for (int i = 0; i < VPT; ++i) {
+                        if (col[i] >= 0) {
+                            const uint4 xv = lds128(rowa + i * vstep);
+                            dep ^= xv.x;
+                            float2 o[4];
+#pragma unroll
+                            for (int kk = 0; kk < 4; ++kk) {
+                                o[kk] = fmul2(al2[0], dyf[0][i][kk]);
+#pragma unroll
+                                for (int j = 1; j < MB; ++j) o[kk] = ffma2(al2[j], dyf[j][i][kk], o[kk]);
+                            }
+                            if (kvi[i] >= 0) {
+#pragma unroll
+                                for (int kk = 0; kk < 4; ++kk) {
+                                    const float2 xk = key_part(bf2_to_f2(u4_get(xv, kk)), kmask[i], kk);
+                                    o[kk] = ffma2(cs2, xk, o[kk]);
+#pragma unroll
+                                    for (int j = 0; j < MB; ++j) {
+                                        o[kk] = ffma2(bl2[j], qf[j][i][kk], o[kk]);
+                                        dqa[j][i][kk] = ffma2(bl2[j], xk, dqa[j][i][kk]);
+                                    }
+                                }
+                            }
+                            st_global_cs_v4(drow + 8 * col[i], make_uint4(pack_f2(o[0]), pack_f2(o[1]),
+                                                                          pack_f2(o[2]), pack_f2(o[3])));
+                        }
+                    }
+                    rowa += sb;
+                }
+                __syncwarp();
+                if (lane == 0) mbar_arrive_after(empty_s + 8u * kc, dep);
+                if (++kc == K) kc = 0;
+            }
+        } else {
+            // several register blocks: dy and query vectors come from shared
+            // memory for every row, dq sums go to shared memory afterwards
+            uint32_t ddep = 0;
+            {
+                int kc = ck;
+                for (int r0 = 0; r0 < S; r0 += G) {
+                    const int rn = min(G, S - r0);
+                    uint32_t rowa = ring_lo + static_cast<uint32_t>(kc) * cb;
+                    for (int r = 0; r < rn; ++r) {
+                        const int s = r0 + r;
+                        float cs = 0.0f;
+                        for (int m = 0; m < M; ++m) cs += zr_t[m * s_pad + s];
+                        const float2 cs2 = make_float2(cs, cs);
+                        uint16_t* drow = static_cast<uint16_t*>(a.dsrc[s]) + n * a.dsrc_ld;
+#pragma unroll
+                        for (int i = 0; i < VPT; ++i) {
+                            if (col[i] < 0) continue;
+                            float2 o[4];
+#pragma unroll
+                            for (int kk = 0; kk < 4; ++kk) o[kk] = make_float2(0.0f, 0.0f);
+                            for (int mb = 0; mb < M; mb += MB) {
+#pragma unroll
+                                for (int j = 0; j < MB; ++j) {
+                                    if (mb + j < M) {
+                                        const float av = al_t[s * m_pad + mb + j];
+                                        const float2 al2 = make_float2(av, av);
+                                        const uint4 yv =
+                                            lds128(dyb + static_cast<uint32_t>(mb + j) * sb + voff + i * vstep);
+                                        ddep ^= yv.x;
+#pragma unroll
+                                        for (int kk = 0; kk < 4; ++kk)
+                                            o[kk] = ffma2(al2, bf2_to_f2(u4_get(yv, kk)), o[kk]);
+                                        if (kvi[i] >= 0) {
+                                            const float bv = b_t[s * m_pad + mb + j];
+                                            const float2 bl2 = make_float2(bv, bv);
+                                            const uint4 qv = lds128(qsm_s + static_cast<uint32_t>(mb + j) * kwb +
+                                                                    16u * static_cast<uint32_t>(kvi[i]));
+#pragma unroll
+                                            for (int kk = 0; kk < 4; ++kk)
+                                                o[kk] = ffma2(bl2, bf2_to_f2(u4_get(qv, kk)), o[kk]);
+                                        }
+                                    }
+                                }
+                            }
+                            if (kvi[i] >= 0) {
+                                const uint4 xv = lds128(rowa + i * vstep);
+#pragma unroll
+                                for (int kk = 0; kk < 4; ++kk)
+                                    o[kk] = ffma2(cs2, key_part(bf2_to_f2(u4_get(xv, kk)), kmask[i], kk), o[kk]);
+                            }
+                            st_global_cs_v4(drow + 8 * col[i], make_uint4(pack_f2(o[0]), pack_f2(o[1]),
+                                                                          pack_f2(o[2]), pack_f2(o[3])));
+                        }
+                        rowa += sb;
+                    }
+                    if (++kc == K) kc = 0;
+                }
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive_after(dyempty_s + 8u * dk, ddep);
+            // dq pass: one register block of queries at a time
+            uint32_t dep = 0;
+            for (int mb = 0; mb < M; mb += MB) {
+                float2 dqt[MB][VPT][4];
+#pragma unroll
+                for (int j = 0; j < MB; ++j)
+#pragma unroll
+                    for (int i = 0; i < VPT; ++i)
+#pragma unroll
+                        for (int kk = 0; kk < 4; ++kk) dqt[j][i][kk] = make_float2(0.0f, 0.0f);
+                int kc = ck;
+                for (int r0 = 0; r0 < S; r0 += G) {
+                    const int rn = min(G, S - r0);
+                    uint32_t rowa = ring_lo + static_cast<uint32_t>(kc) * cb;
+                    for (int r = 0; r < rn; ++r) {
+                        const int s = r0 + r;
+                        float2 bl2[MB];
+#pragma unroll
+                        for (int j = 0; j < MB; ++j) {
+                            const float bv = b_t[s * m_pad + mb + j];
+                            bl2[j] = make_float2(bv, bv);
+                        }
+#pragma unroll
+                        for (int i = 0; i < VPT; ++i) {
+                            if (kvi[i] >= 0) {
+                                const uint4 xv = lds128(rowa + i * vstep);
+                                dep ^= xv.x;
+#pragma unroll
+                                for (int kk = 0; kk < 4; ++kk) {
+                                    const float2 xk = key_part(bf2_to_f2(u4_get(xv, kk)), kmask[i], kk);
+#pragma unroll
+                                    for (int j = 0; j < MB; ++j) dqt[j][i][kk] = ffma2(bl2[j], xk, dqt[j][i][kk]);
+                                }
+                            }
+                        }
+                        rowa += sb;
+                    }
+                    if (++kc == K) kc = 0;
+                }
+#pragma unroll
+                for (int j = 0; j < MB; ++j) {
+                    if (mb + j >= M) continue;
+#pragma unroll
+                    for (int i = 0; i < VPT; ++i) {
+                        if (kvi[i] < 0) continue;
+                        float2* d2 = reinterpret_cast<float2*>(dqsm + (mb + j) * kw + 8 * kvi[i]);
+#pragma unroll
+                        for (int kk = 0; kk < 4; ++kk) {
+                            const float2 o = d2[kk];
+                            d2[kk] = make_float2(o.x + dqt[j][i][kk].x, o.y + dqt[j][i][kk].y);
+                        }
+                    }
+                }
+            }
+            // the chunks held every row until the dq pass
+            int kc = ck;
+            for (int c = 0; c < cpt; ++c) {
+                __syncwarp();
+                if (lane == 0) mbar_arrive_after(empty_s + 8u * kc, dep);
+                if (++kc == K) kc = 0;
+            }
+        }
+        for (int c = 0; c < cpt; ++c) {
+            if (++ck == K) {
+                ck = 0;
+                cphase ^= 1u;
+            }
+        }
+        if (++dk == DS) {
+            dk = 0;
+            dphase ^= 1u;
+        }
+        if (++ts == kMultiTokSlots) {
+            ts = 0;
+            tphase ^= 1u;
+        }
+    }
+
+    // this CTA's FP32 partial row: part[cta][m * R + (c - ko)]
+    float* prow = a.part + static_cast<long long>(blockIdx.x) * M * a.R;
+#pragma unroll
+    for (int i = 0; i < VPT; ++i) {
+        if (kvi[i] < 0) continue;
+        for (int m = 0; m < M; ++m) {
+            float v8[8];
+            if (nmb == 1) {
+#pragma unroll
+                for (int j = 0; j < MB; ++j) {
+                    if (j == m) {
+#pragma unroll
+                        for (int kk = 0; kk < 4; ++kk) {
+                            v8[2 * kk] = dqa[j][i][kk].x;
+                            v8[2 * kk + 1] = dqa[j][i][kk].y;
+                        }
+                    }
+                }
+            } else {
+#pragma unroll
+                for (int e = 0; e < 8; ++e) v8[e] = dqsm[m * kw + 8 * kvi[i] + e];
+            }
+#pragma unroll
+            for (int e = 0; e < 8; ++e)
+                if ((kmask[i] >> e) & 1u) prow[m * a.R + (8 * col[i] + e - ko)] = v8[e];
+        }
+    }
+}
+
+template <int VPT, int MB>
+cudaError_t launch_t(const MultiPlan& plan, const MultiBwdArgs& a, cudaStream_t stream) {
+    auto kern = attnres_multi_bwd_kernel<VPT, MB>;
+    cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                           static_cast<int>(plan.smem_bwd));
+    if (err != cudaSuccess) return err;
+    kern<<<plan.grid, (plan.ncw + 1) * 32, plan.smem_bwd, stream>>>(a);
+    err = cudaGetLastError();
+    if (err != cudaSuccess) return err;
+    const int W = a.M * a.R;
+    return launch_finalize(a.part, plan.grid, W, W, const_cast<uint16_t*>(a.dq), a.dq_f32, nullptr, nullptr,
+                           stream);
+}
+
+}  // namespace
+
+unsigned take_multi_bwd_error() {
+    unsigned v = 0, zero = 0;
+    if (cudaMemcpyFromSymbol(&v, g_multi_bwd_error, sizeof v) != cudaSuccess) return 0xffffffffu;
+    if (v) cudaMemcpyToSymbol(g_multi_bwd_error, &zero, sizeof zero);
+    return v;
+}
+
+cudaError_t launch_multi_bwd(const MultiPlan& plan, const MultiBwdArgs& a, cudaStream_t stream) {
+    const int key = plan.vpt * 10 + plan.mb_b;
+    switch (key) {
+        case 11: return launch_t<1, 1>(plan, a, stream);
+        case 12: return launch_t<1, 2>(plan, a, stream);
+        case 14: return launch_t<1, 4>(plan, a, stream);
+        case 21: return launch_t<2, 1>(plan, a, stream);
+        case 22: return launch_t<2, 2>(plan, a, stream);
+        case 41: return launch_t<4, 1>(plan, a, stream);
+        default: return cudaErrorInvalidConfiguration;
+    }
+}
+
+}  // namespace attnres

@@ -346,6 +346,37 @@ __device__ __forceinline__ void bf16_sq_dot(const uint4& x, const uint4& q, floa
         : "r"(x.x), "r"(x.y), "r"(x.z), "r"(x.w), "r"(q.x), "r"(q.y), "r"(q.z), "r"(q.w));
 }
 
+// t0 += x_lo * y_lo, t1 += x_hi * y_hi over the four 32-bit words of two
+// bf16x8 vectors (fma.rn.f32.bf16: exact products, FP32 sums).
+__device__ __forceinline__ void bf16_dot8(const uint4& x, const uint4& y, float& t0, float& t1) {
+    asm("{\n\t.reg .b16 xl, xh, yl, yh;\n\t"
+        "mov.b32 {xl, xh}, %2;\n\tmov.b32 {yl, yh}, %6;\n\t"
+        "fma.rn.f32.bf16 %0, yl, xl, %0;\n\tfma.rn.f32.bf16 %1, yh, xh, %1;\n\t"
+        "mov.b32 {xl, xh}, %3;\n\tmov.b32 {yl, yh}, %7;\n\t"
+        "fma.rn.f32.bf16 %0, yl, xl, %0;\n\tfma.rn.f32.bf16 %1, yh, xh, %1;\n\t"
+        "mov.b32 {xl, xh}, %4;\n\tmov.b32 {yl, yh}, %8;\n\t"
+        "fma.rn.f32.bf16 %0, yl, xl, %0;\n\tfma.rn.f32.bf16 %1, yh, xh, %1;\n\t"
+        "mov.b32 {xl, xh}, %5;\n\tmov.b32 {yl, yh}, %9;\n\t"
+        "fma.rn.f32.bf16 %0, yl, xl, %0;\n\tfma.rn.f32.bf16 %1, yh, xh, %1;\n\t}"
+        : "+f"(t0), "+f"(t1)
+        : "r"(x.x), "r"(x.y), "r"(x.z), "r"(x.w), "r"(y.x), "r"(y.y), "r"(y.z), "r"(y.w));
+}
+
+// s0 += x_lo^2, s1 += x_hi^2 over the four words of a bf16x8 vector.
+__device__ __forceinline__ void bf16_sq8(const uint4& x, float& s0, float& s1) { bf16_dot8(x, x, s0, s1); }
+
+// Zero the bf16 halves of x (channels j0 .. j0+7) outside [lo, hi).
+__device__ __forceinline__ uint4 mask_bf16x8(const uint4& x, int j0, int lo, int hi) {
+    uint32_t w[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+    for (int kk = 0; kk < 4; ++kk) {
+        const int j = j0 + 2 * kk;
+        if (j < lo || j >= hi) w[kk] &= 0xffff0000u;
+        if (j + 1 < lo || j + 1 >= hi) w[kk] &= 0x0000ffffu;
+    }
+    return make_uint4(w[0], w[1], w[2], w[3]);
+}
+
 // Position in the shared-memory row ring: row address, slot index, phase.
 struct RingCursor {
     uint32_t row;

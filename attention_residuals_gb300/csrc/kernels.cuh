@@ -156,6 +156,116 @@ struct BwdArgs {
     float* dw_o_f32;
 };
 
+// ---------------------------------------------------------------------------
+// Multi-query read: M queries share one read of the sources.  A token's S
+// rows stay resident in the chunk ring while every query is served; the
+// backward also keeps the token's M dy rows (a ring of `dy_slots` groups of
+// M rows) and its saved statistics (two slots) in shared memory.
+// ---------------------------------------------------------------------------
+constexpr int kMultiTokSlots = 2;
+
+struct MultiLayout {
+    uint32_t ring, dyring, full, empty, dyfull, dyempty, tfull, tempty, tok, tab, qsm, dqsm, misc, total;
+    uint32_t tstride;  // floats per statistics slot
+};
+
+// Tables (floats).  Forward: ss[s_pad], dot[m_pad][s_pad], alpha[s_pad][m_pad].
+// Backward: da[m_pad][s_pad], alpha[s_pad][m_pad], b[s_pad][m_pad],
+// zr[m_pad][s_pad].  qsm: m_pad query rows of nkv 16-byte vectors (bf16).
+// dqsm (backward, only when the queries take several register blocks): M
+// rows of dq_nkv * 8 FP32 dq partial sums.
+__host__ __device__ inline MultiLayout make_multi_layout(int chunks, int rows, int slot_bytes, int M,
+                                                        int dy_slots, int s_pad, int m_pad, int nkv,
+                                                        int dq_nkv, bool backward) {
+    MultiLayout L;
+    uint32_t off = 0;
+    L.ring = off;
+    off += static_cast<uint32_t>(chunks) * static_cast<uint32_t>(rows) * static_cast<uint32_t>(slot_bytes);
+    L.dyring = off;
+    off += backward ? static_cast<uint32_t>(dy_slots) * static_cast<uint32_t>(M) * static_cast<uint32_t>(slot_bytes) : 0u;
+    off = align_up(off, 16);
+    L.full = off;
+    off += 8u * chunks;
+    L.empty = off;
+    off += 8u * chunks;
+    L.dyfull = off;
+    off += backward ? 8u * dy_slots : 0u;
+    L.dyempty = off;
+    off += backward ? 8u * dy_slots : 0u;
+    L.tfull = off;
+    off += backward ? 8u * kMultiTokSlots : 0u;
+    L.tempty = off;
+    off += backward ? 8u * kMultiTokSlots : 0u;
+    off = align_up(off, 16);
+    L.tstride = align_up(static_cast<uint32_t>(2 * M * s_pad + s_pad), 4u);
+    L.tok = off;
+    off += backward ? kMultiTokSlots * L.tstride * 4u : 0u;
+    L.tab = off;
+    off += (backward ? 4u * m_pad * s_pad : (s_pad + 2u * m_pad * s_pad)) * 4u;
+    off = align_up(off, 16);
+    L.qsm = off;
+    off += static_cast<uint32_t>(m_pad) * static_cast<uint32_t>(nkv) * 16u;
+    L.dqsm = off;
+    off += backward ? static_cast<uint32_t>(M) * static_cast<uint32_t>(dq_nkv) * 32u : 0u;
+    L.misc = off;  // abort flag
+    off += 16u;
+    L.total = align_up(off, 128);
+    return L;
+}
+
+struct MultiPlan {
+    int grid;
+    int ncw, vpt;          // consumer warps, 16-byte vectors per thread
+    int mb_f, mb_b;        // queries per register block (forward / backward)
+    int slot_bytes, s_pad, m_pad;
+    int kv0, nkv;          // key window in 16-byte vectors
+    int f_rows, f_chunks;  // forward chunk ring
+    int b_rows, b_chunks, dy_slots;
+    size_t smem_fwd, smem_bwd;
+    size_t ws_bytes;       // backward workspace: [grid][M * R] FP32 partials
+};
+
+struct MultiFwdArgs {
+    const void* src[ATTNRES_MAX_S];
+    long long N, src_ld;
+    long long y_ms, y_ns;  // elements between queries / tokens of the output
+    int S, D, R, ko, M;
+    float eps, scale;
+    int chunks, rows, slot_bytes, ncw, s_pad, m_pad, kv0, nkv;
+    const uint16_t* q;     // [M][R]
+    uint16_t* y;
+    float* alpha;          // [N][M][S]
+    float* rstd;           // [N][S]
+    float* logit;          // [N][M][S]
+};
+
+struct MultiBwdArgs {
+    const void* src[ATTNRES_MAX_S];
+    void* dsrc[ATTNRES_MAX_S];
+    long long N, src_ld, dsrc_ld;
+    long long dy_ms, dy_ns;
+    int S, D, R, ko, M;
+    float eps, scale;
+    int chunks, rows, slot_bytes, dy_slots, ncw, s_pad, m_pad, kv0, nkv;
+    const uint16_t* q;
+    const uint16_t* dy;
+    const float* alpha;
+    const float* rstd;
+    const float* logit;
+    float* part;           // [grid][M * R]
+    uint16_t* dq;          // [M][R]
+    float* dq_f32;         // [M][R] or NULL
+};
+
+unsigned take_multi_fwd_error();
+unsigned take_multi_bwd_error();
+cudaError_t launch_multi_fwd(const MultiPlan& plan, const MultiFwdArgs& a, cudaStream_t stream);
+cudaError_t launch_multi_bwd(const MultiPlan& plan, const MultiBwdArgs& a, cudaStream_t stream);
+// Column sums of a [P][W] FP32 partial matrix in row order; columns < R go to
+// dq (bf16 + optional FP32), the rest to dw_o.
+cudaError_t launch_finalize(const float* part, int P, int R, int W, uint16_t* dq, float* dq_f32,
+                            uint16_t* dw_o, float* dw_o_f32, cudaStream_t stream);
+
 // Host-side launchers (return a CUDA error code) and the per-kernel records
 // of failed waits (read and cleared; 0 = none).
 unsigned take_fwd_error();

@@ -133,3 +133,79 @@ def attnres_op(values, query: Tensor, *, eps: float = _ops.EPS_DEFAULT, scale: f
     ko = D - query.numel() if key_offset is None else int(key_offset)
     y = read_fwd(vals, query, out_norm_weight, float(eps), float(scale), ko)[0]
     return y
+
+
+# --------------------------------------------------------------------------
+# Multi-query read ("Fast Attention Residuals", section "Multi-query AttnRes")
+# --------------------------------------------------------------------------
+def _multi_out_shape(lead, M: int, D: int, token_major: bool):
+    return (*lead, M, D) if token_major else (M, *lead, D)
+
+
+@torch.library.custom_op(f"{_NS}::read_multi_fwd", mutates_args=(), device_types="cuda")
+def read_multi_fwd(values: List[Tensor], queries: Tensor, eps: float, scale: float, key_offset: int,
+                   token_major: bool) -> Tuple[Tensor, Tensor, Tensor, Tensor]:
+    S, D, packed, lead = _shape_info(values, queries.shape[-1])
+    r = _ops.attnres_multi_fwd(_as_values(values, packed), queries, eps=eps, scale=scale,
+                               key_offset=key_offset, token_major=token_major)
+    return r["y"], r["alpha"], r["rstd"], r["logit"]
+
+
+@read_multi_fwd.register_fake
+def _(values, queries, eps, scale, key_offset, token_major):
+    S, D, packed, lead = _shape_info(values, queries.shape[-1])
+    M = queries.shape[0]
+    N = 1
+    for d in lead:
+        N *= d
+    f32 = dict(dtype=torch.float32, device=queries.device)
+    y = torch.empty(_multi_out_shape(lead, M, D, token_major), dtype=torch.bfloat16,
+                    device=queries.device)
+    return y, torch.empty((N, M, S), **f32), torch.empty((N, S), **f32), torch.empty((N, M, S), **f32)
+
+
+@torch.library.custom_op(f"{_NS}::read_multi_bwd", mutates_args=(), device_types="cuda")
+def read_multi_bwd(values: List[Tensor], queries: Tensor, dy: Tensor, alpha: Tensor, rstd: Tensor,
+                   logit: Tensor, eps: float, scale: float, key_offset: int,
+                   token_major: bool) -> Tuple[List[Tensor], Tensor]:
+    S, D, packed, lead = _shape_info(values, queries.shape[-1])
+    saved = {"alpha": alpha, "rstd": rstd, "logit": logit, "token_major": token_major}
+    g = _ops.attnres_multi_bwd(_as_values(values, packed), queries, dy.contiguous(), saved, eps=eps,
+                               scale=scale, key_offset=key_offset, token_major=token_major)
+    dv = [g["dvalues"]] if packed else list(g["dvalues"])
+    return dv, g["dq"]
+
+
+@read_multi_bwd.register_fake
+def _(values, queries, dy, alpha, rstd, logit, eps, scale, key_offset, token_major):
+    return [torch.empty_like(v) for v in values], torch.empty_like(queries)
+
+
+def _multi_setup_context(ctx, inputs, output):
+    values, queries, eps, scale, key_offset, token_major = inputs
+    y, alpha, rstd, logit = output
+    ctx.cfg = (eps, scale, key_offset, token_major)
+    ctx.save_for_backward(queries, alpha, rstd, logit, *values)
+
+
+def _multi_backward(ctx, dy, d_alpha, d_rstd, d_logit):
+    queries, alpha, rstd, logit, *values = ctx.saved_tensors
+    eps, scale, key_offset, token_major = ctx.cfg
+    dv, dq = read_multi_bwd(list(values), queries, dy.to(torch.bfloat16), alpha, rstd, logit, eps,
+                            scale, key_offset, token_major)
+    return list(dv), dq, None, None, None, None
+
+
+read_multi_fwd.register_autograd(_multi_backward, setup_context=_multi_setup_context)
+
+
+def attnres_multi_op(values, queries: Tensor, *, eps: float = _ops.EPS_DEFAULT, scale: float = 1.0,
+                     key_offset: Optional[int] = None, output_layout: str = "query_major") -> Tensor:
+    """The multi-query read through the registered operator."""
+    if output_layout not in ("query_major", "token_major"):
+        raise ValueError("output_layout must be 'query_major' or 'token_major'")
+    vals = [values] if isinstance(values, Tensor) else list(values)
+    D = vals[0].shape[-1]
+    ko = D - queries.shape[-1] if key_offset is None else int(key_offset)
+    return read_multi_fwd(vals, queries, float(eps), float(scale), ko,
+                          output_layout == "token_major")[0]

@@ -286,6 +286,118 @@ def attnres_bwd_noalloc(values: Sources, q: torch.Tensor, dy: torch.Tensor, save
 
 
 # --------------------------------------------------------------------------
+# Multi-query read ("Fast Attention Residuals", section "Multi-query AttnRes")
+# --------------------------------------------------------------------------
+_MULTI_PLAN_KEYS = ["grid", "consumer_warps", "vectors_per_thread", "query_blocks", "fwd_ring",
+                    "bwd_ring", "dy_slots", "bwd_smem_bytes"]
+
+
+def make_multi_params(view: _SourceView, M: int, R: int, *, key_offset: Optional[int], eps: float,
+                      scale: float, token_major: bool) -> _lib.AttnresMultiParams:
+    mp = _lib.AttnresMultiParams()
+    mp.base = make_params(view, R, key_offset=key_offset, eps=eps, scale=scale, out_norm=False)
+    mp.M = int(M)
+    N, D = view.N, view.D
+    if token_major:             # [N, M, D]
+        mp.out_ld_m, mp.out_ld_n = D, M * D
+    else:                       # [M, N, D]
+        mp.out_ld_m, mp.out_ld_n = N * D, D
+    return mp
+
+
+def _check_queries(queries: torch.Tensor, D: int) -> torch.Tensor:
+    if queries.dim() != 2:
+        raise ValueError("queries must be [M, R]")
+    M, R = queries.shape
+    if not (1 <= M <= _lib.MAX_M) or not (1 <= R <= D):
+        raise ValueError(f"queries must be [M, R] with 1 <= M <= {_lib.MAX_M}, 1 <= R <= D")
+    if queries.dtype != torch.bfloat16 or not queries.is_cuda:
+        raise TypeError("queries must be a CUDA bf16 tensor")
+    return queries.contiguous()
+
+
+def attnres_multi_plan_info(values: Sources, M: int, R: int, *, key_offset=None) -> dict:
+    view = _source_view(values)
+    mp = make_multi_params(view, M, R, key_offset=key_offset, eps=EPS_DEFAULT, scale=1.0,
+                           token_major=False)
+    out = (ctypes.c_int64 * 8)()
+    _lib.check(_lib.load().attnres_multi_plan_info(ctypes.byref(mp), out), "attnres_multi_plan_info")
+    return dict(zip(_MULTI_PLAN_KEYS, list(out)))
+
+
+def attnres_multi_bwd_workspace_bytes(params: _lib.AttnresMultiParams) -> int:
+    return int(_lib.load().attnres_multi_bwd_workspace_bytes(ctypes.byref(params)))
+
+
+def _multi_out_shape(view: _SourceView, M: int, token_major: bool):
+    return (*view.lead_shape, M, view.D) if token_major else (M, *view.lead_shape, view.D)
+
+
+def attnres_multi_fwd(values: Sources, queries: torch.Tensor, *, eps: float = EPS_DEFAULT,
+                      scale: float = 1.0, key_offset: Optional[int] = None, token_major: bool = False,
+                      stream=None) -> dict:
+    """Multi-query forward.  Returns y ([M, ..., D], or [..., M, D] when
+    token_major) and the saved statistics alpha/logit [N, M, S] and
+    rstd [N, S] (f32)."""
+    view = _source_view(values)
+    queries = _check_queries(queries, view.D)
+    M, R = queries.shape
+    mp = make_multi_params(view, M, R, key_offset=key_offset, eps=eps, scale=scale,
+                           token_major=token_major)
+    dev = view.rows[0].device
+    S, N, D = len(view.rows), view.N, view.D
+    y = torch.empty((N, M, D) if token_major else (M, N, D), dtype=torch.bfloat16, device=dev)
+    f32 = dict(dtype=torch.float32, device=dev)
+    alpha = torch.empty((N, M, S), **f32)
+    rstd = torch.empty((N, S), **f32)
+    logit = torch.empty((N, M, S), **f32)
+    rc = _lib.load().attnres_multi_fwd(ctypes.byref(mp), _ptr(queries), _ptr(y), _ptr(alpha),
+                                       _ptr(rstd), _ptr(logit), _stream(stream))
+    _lib.check(rc, "attnres_multi_fwd")
+    return {"y": y.view(_multi_out_shape(view, M, token_major)), "alpha": alpha, "rstd": rstd,
+            "logit": logit, "params": mp, "view": view, "token_major": token_major}
+
+
+def attnres_multi_bwd(values: Sources, queries: torch.Tensor, dy: torch.Tensor, saved: dict, *,
+                      eps: float = EPS_DEFAULT, scale: float = 1.0, key_offset: Optional[int] = None,
+                      token_major: Optional[bool] = None, stream=None,
+                      workspace: Optional[torch.Tensor] = None) -> dict:
+    """Multi-query backward.  ``saved`` is attnres_multi_fwd's result; dy
+    has the output's shape and layout.  Returns dvalues (packed or a list,
+    like the sources; the sum over queries) and dq [M, R] in bf16 and fp32."""
+    view = saved.get("view") or _source_view(values)
+    queries = _check_queries(queries, view.D)
+    M, R = queries.shape
+    tm = saved.get("token_major", False) if token_major is None else token_major
+    mp = make_multi_params(view, M, R, key_offset=key_offset, eps=eps, scale=scale, token_major=tm)
+    S, N, D = len(view.rows), view.N, view.D
+    dev = view.rows[0].device
+    if dy.dtype != torch.bfloat16 or not dy.is_cuda or dy.numel() != M * N * D:
+        raise TypeError("dy must be a CUDA bf16 tensor shaped like the output")
+    dy3 = dy.reshape((N, M, D) if tm else (M, N, D)).contiguous()
+    if view.packed:
+        dpacked = torch.empty((S, N, D), dtype=torch.bfloat16, device=dev)
+        drows = [dpacked[s] for s in range(S)]
+    else:
+        dpacked = None
+        drows = [torch.empty((N, D), dtype=torch.bfloat16, device=dev) for _ in range(S)]
+    dptrs = (ctypes.c_void_p * S)(*[r.data_ptr() for r in drows])
+    dq = torch.empty((M, R), dtype=torch.bfloat16, device=dev)
+    dq32 = torch.empty((M, R), dtype=torch.float32, device=dev)
+    need = attnres_multi_bwd_workspace_bytes(mp)
+    if workspace is None or workspace.numel() < need:
+        workspace = torch.empty((max(need, 16),), dtype=torch.uint8, device=dev)
+    rc = _lib.load().attnres_multi_bwd(
+        ctypes.byref(mp), _ptr(queries), _ptr(dy3), _ptr(saved["alpha"]), _ptr(saved["rstd"]),
+        _ptr(saved["logit"]), dptrs, ctypes.c_int64(D), _ptr(dq), _ptr(dq32), _ptr(workspace),
+        ctypes.c_size_t(workspace.numel()), _stream(stream))
+    _lib.check(rc, "attnres_multi_bwd")
+    shape = (*view.lead_shape, D)
+    dv = dpacked.view(S, *shape) if dpacked is not None else [r.view(*shape) for r in drows]
+    return {"dvalues": dv, "dq": dq, "dq_f32": dq32}
+
+
+# --------------------------------------------------------------------------
 # Autograd operator
 # --------------------------------------------------------------------------
 def attnres(values: Sources, query: torch.Tensor, *, eps: float = EPS_DEFAULT, scale: float = 1.0,
@@ -304,3 +416,16 @@ def attnres(values: Sources, query: torch.Tensor, *, eps: float = EPS_DEFAULT, s
     from .custom_ops import attnres_op
     return attnres_op(values, query, eps=eps, scale=scale, out_norm_weight=out_norm_weight,
                       key_offset=key_offset)
+
+
+def attnres_multi(values: Sources, queries: torch.Tensor, *, eps: float = EPS_DEFAULT,
+                  scale: float = 1.0, key_offset: Optional[int] = None,
+                  output_layout: str = "query_major") -> torch.Tensor:
+    """Multi-query read: M queries [M, R] (1 <= M <= 16) read the same
+    sources, each with its own routing weights and full-width output.
+    Returns [M, ..., D] (output_layout="query_major") or [..., M, D]
+    ("token_major").  Differentiable in values and queries; registered
+    torch operators, so torch.compile(fullgraph=True) and CUDA graphs work."""
+    from .custom_ops import attnres_multi_op
+    return attnres_multi_op(values, queries, eps=eps, scale=scale, key_offset=key_offset,
+                            output_layout=output_layout)

@@ -135,3 +135,68 @@ def make_random(S: int, N: int, D: int, R: Optional[int] = None, *, key_offset: 
     return Workload(name=f"random S{S} N{N} D{D} R{R}", S=S, N=N, D=D, R=R,
                     key_offset=int(key_offset), eps=eps, scale=scale, out_norm=out_norm,
                     values=values, q=q, w_o=w_o, dy=dy)
+
+
+# ---------------------------------------------------------------------------
+# Multi-query reads ("Fast Attention Residuals", section "Multi-query
+# AttnRes": queries [M, R], 1 <= M <= 16, the page's example reads a packed
+# [8, 2, 1024] value tensor with two rank-64 queries; its QK/V fixture routes
+# two roles with two queries).
+# ---------------------------------------------------------------------------
+@dataclass
+class MultiWorkload:
+    name: str
+    S: int
+    N: int
+    D: int
+    R: int
+    M: int
+    key_offset: int
+    eps: float
+    scale: float
+    values: torch.Tensor            # packed [S, N, D] bf16
+    queries: torch.Tensor           # [M, R] bf16
+    dy: torch.Tensor                # [M, N, D] bf16 (query-major)
+
+
+MULTI_CONFIGS = {
+    # the page's multi-query example: values [8, 2, 1024], queries [2, 64]
+    "example": dict(S=8, N=2, D=1024, R=64, M=2, src_scale=None),
+    # two queries over the long-sequence shapes at quarter rank, key in the
+    # final R channels
+    "long": dict(S=10, N=32768, D=4096, R=1024, M=2, src_scale=(0.5, 2.0)),
+}
+
+
+def make_multi(S: int, N: int, D: int, R: int, M: int, *, key_offset: Optional[int] = None,
+               seed: int = 0, src_scale=None, device: str = "cpu", scale: float = 1.0,
+               eps: float = EPS_DEFAULT, name: Optional[str] = None) -> MultiWorkload:
+    """Sources N(0,1) (times one U[lo, hi] scalar per source when src_scale
+    is given), queries N(0,1) * R^-1/2, dy N(0,1); key_offset defaults to
+    the page's final R channels (D - R)."""
+    gen = torch.Generator(device=device)
+    gen.manual_seed(int(seed))
+    values = torch.empty((S, N, D), dtype=torch.bfloat16, device=device)
+    scales = None
+    if src_scale is not None:
+        lo, hi = src_scale
+        scales = lo + (hi - lo) * torch.rand((S,), generator=gen, device=device)
+    for s in range(S):
+        x = _randn((N, D), gen, device)
+        if scales is not None:
+            x *= scales[s]
+        values[s] = x.to(torch.bfloat16)
+    queries = (_randn((M, R), gen, device) * R ** -0.5).to(torch.bfloat16)
+    dy = _randn((M, N, D), gen, device).to(torch.bfloat16)
+    ko = D - R if key_offset is None else int(key_offset)
+    return MultiWorkload(name=name or f"multi S{S} N{N} D{D} R{R} M{M}", S=S, N=N, D=D, R=R, M=M,
+                         key_offset=ko, eps=eps, scale=scale, values=values, queries=queries, dy=dy)
+
+
+def make_multi_workload(key: str, *, N: Optional[int] = None, seed: Optional[int] = None,
+                        device: str = "cpu") -> MultiWorkload:
+    c = MULTI_CONFIGS[key]
+    n = c["N"] if N is None else int(N)
+    return make_multi(c["S"], n, c["D"], c["R"], c["M"], seed=100 + len(key) if seed is None else seed,
+                      src_scale=c["src_scale"], device=device,
+                      name=f"multi-query {key} S{c['S']} N{n} D{c['D']} R{c['R']} M{c['M']}")

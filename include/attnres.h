@@ -203,6 +203,84 @@ const char* attnres_status_string(attnres_status s);
  */
 attnres_status attnres_plan_info(const attnres_params* p, int64_t out[8]);
 
+/* ------------------------------------------------------------------------
+ * Multi-query read ("Fast Attention Residuals", section "Multi-query
+ * AttnRes"): the same sources are read with M queries q_m (bf16 [M][R],
+ * 1 <= M <= ATTNRES_MAX_M); each query has its own routing weights and its
+ * own full-width output,
+ *
+ *   z_ms = scale * r_s * <t_s, q_m>,  a_m = softmax_s(z_m),  y_m = sum_s a_ms v_s
+ *
+ * with the key slice t_s and its reciprocal RMS r_s exactly as above (r_s
+ * does not depend on the query).  The multi-query read has no output norm.
+ * Every source row is read from HBM once per call for all M outputs.  The
+ * gradient of a source is the sum over queries; dq_m sums over tokens.
+ *
+ * Supported range: a token's S source rows stay in shared memory while all
+ * queries are served, and the backward also holds the token's M dy rows and
+ * the queries' key channels.  Shapes where these do not fit the device's
+ * shared memory (roughly (S + M) * D * 2 + M * R * 2 bytes beyond ~220 KB)
+ * return ATTNRES_ERR_UNSUPPORTED before anything is enqueued;
+ * attnres_multi_plan_info tells in advance.
+ * ------------------------------------------------------------------------ */
+#define ATTNRES_MAX_M 16
+
+/*
+ *   base        S, D, R, key_offset, N, eps, scale, src_ld, src as for
+ *               attnres_params; base.out_norm must be 0; split_n_threshold
+ *               is ignored (the multi-query backward always finalizes its
+ *               per-CTA partial sums in a separate kernel, in CTA order).
+ *   M           number of queries, 1 <= M <= ATTNRES_MAX_M
+ *   out_ld_m    element stride between query m and m + 1 of one token, in
+ *               the output y and in the upstream gradient dy
+ *   out_ld_n    element stride between token n and n + 1 of one query
+ *               (both multiples of 8).  Query-major [M, N, D]: out_ld_m =
+ *               N * D, out_ld_n = D; token-major [N, M, D] (the page's
+ *               output_layout="token_major"): out_ld_m = D, out_ld_n = M * D.
+ */
+typedef struct {
+    attnres_params base;
+    int32_t M;
+    int64_t out_ld_m;
+    int64_t out_ld_n;
+} attnres_multi_params;
+
+/*
+ * Multi-query forward.  q bf16 [M][R] contiguous.  Outputs (fully
+ * overwritten): y bf16 rows y + m * out_ld_m + n * out_ld_n (16-byte
+ * aligned), alpha f32 [N][M][S], rstd f32 [N][S], logit f32 [N][M][S].
+ * Errors: INVALID_ARG, ALIGNMENT, UNSUPPORTED (out_norm set, or the shape
+ * does not fit), CUDA.
+ */
+attnres_status attnres_multi_fwd(const attnres_multi_params* p, const void* q, void* y,
+                                 float* alpha, float* rstd, float* logit, void* stream);
+
+/* Bytes of workspace attnres_multi_bwd needs (grid * M * R * 4; 0 when N == 0). */
+size_t attnres_multi_bwd_workspace_bytes(const attnres_multi_params* p);
+
+/*
+ * Multi-query backward.  Inputs: q, dy (bf16 rows at dy + m * out_ld_m +
+ * n * out_ld_n, 16-byte aligned) and the forward's alpha, rstd, logit.
+ * Outputs (written, never accumulated): dsrc[s] as for attnres_bwd (the
+ * sum over all M queries), dq bf16 [M][R], dq_f32 f32 [M][R] (may be NULL).
+ * workspace: at least attnres_multi_bwd_workspace_bytes(p) bytes, 16-byte
+ * aligned.  Errors: as attnres_multi_fwd, plus WORKSPACE.
+ */
+attnres_status attnres_multi_bwd(const attnres_multi_params* p, const void* q, const void* dy,
+                                 const float* alpha, const float* rstd, const float* logit,
+                                 void* const* dsrc, int64_t dsrc_ld, void* dq, float* dq_f32,
+                                 void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * Launch plan of the multi-query kernels (no launch).  out[0..7]: grid CTAs,
+ * consumer warps, 16-byte vectors per thread, queries per register block
+ * (forward * 1000 + backward), forward ring (chunks * 1000 + rows per
+ * chunk), backward ring (chunks * 1000 + rows per chunk), dy slots, and the
+ * backward dynamic shared memory bytes.  UNSUPPORTED when the shape does not
+ * fit.
+ */
+attnres_status attnres_multi_plan_info(const attnres_multi_params* p, int64_t out[8]);
+
 #ifdef __cplusplus
 }
 #endif

@@ -129,3 +129,56 @@ def test_binding_refuses_cpu_tensors():
     q = torch.zeros((64,), dtype=torch.bfloat16)
     with pytest.raises(TypeError):
         attnres_fwd(v, q)
+
+
+# --------------------------------------------------------------- multi-query
+def test_multi_params_struct_layout_matches_header():
+    MP = _lib.AttnresMultiParams
+    base = ctypes.sizeof(_lib.AttnresParams)
+    assert MP.M.offset == base and MP.out_ld_m.offset == base + 8 and MP.out_ld_n.offset == base + 16
+    assert ctypes.sizeof(MP) == base + 24
+
+
+def _mparams(M=2, ld_m=None, ld_n=None, **kw):
+    mp = _lib.AttnresMultiParams()
+    mp.base = _params(**kw)
+    mp.M = M
+    N, D = mp.base.N, mp.base.D
+    mp.out_ld_m = N * D if ld_m is None else ld_m
+    mp.out_ld_n = D if ld_n is None else ld_n
+    return mp
+
+
+MULTI_BAD = BAD + [
+    (dict(M=0), 1), (dict(M=17), 1), (dict(out_norm=1), 3), (dict(ld_m=4), 2), (dict(ld_n=-8), 1),
+]
+
+
+@pytest.mark.parametrize("kw,code", MULTI_BAD)
+def test_multi_forward_rejects_bad_shapes_before_launch(lib, kw, code):
+    mp = _mparams(**kw)
+    fake = ctypes.c_void_p(0x200000)
+    rc = lib.attnres_multi_fwd(ctypes.byref(mp), fake, fake, fake, fake, fake, None)
+    assert rc == code
+
+
+@pytest.mark.parametrize("kw,code", MULTI_BAD)
+def test_multi_backward_rejects_bad_shapes_before_launch(lib, kw, code):
+    mp = _mparams(**kw)
+    fake = ctypes.c_void_p(0x200000)
+    d = (ctypes.c_void_p * 4)(*[0x300000 + i * 0x10000 for i in range(4)])
+    rc = lib.attnres_multi_bwd(ctypes.byref(mp), fake, fake, fake, fake, fake, d, ctypes.c_int64(64),
+                               fake, None, fake, ctypes.c_size_t(1 << 20), None)
+    assert rc == code
+    assert lib.attnres_multi_bwd_workspace_bytes(ctypes.byref(mp)) == 0
+
+
+def test_multi_missing_or_misaligned_pointers_rejected(lib):
+    mp = _mparams()
+    fake = ctypes.c_void_p(0x200000)
+    assert lib.attnres_multi_fwd(ctypes.byref(mp), None, fake, fake, fake, fake, None) == 1
+    assert lib.attnres_multi_fwd(ctypes.byref(mp), fake, ctypes.c_void_p(0x200008), fake, fake, fake,
+                                 None) == 2
+    d = (ctypes.c_void_p * 4)(*[0x300000 + i * 0x10000 for i in range(4)])
+    assert lib.attnres_multi_bwd(ctypes.byref(mp), fake, fake, fake, fake, fake, d, ctypes.c_int64(64),
+                                 None, None, fake, ctypes.c_size_t(1 << 20), None) == 1
