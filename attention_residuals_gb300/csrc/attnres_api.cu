@@ -228,42 +228,86 @@ attnres_status make_multi_plan(const attnres_multi_params* p, MultiPlan* plan) {
     const attnres_params& b = p->base;
     MultiPlan pl{};
     const int ncv = b.D / 8;
-    pl.vpt = ncv <= 256 ? 1 : (ncv <= 512 ? 2 : 4);
-    pl.ncw = (ncv + 32 * pl.vpt - 1) / (32 * pl.vpt);
-    if (pl.ncw < 1 || pl.ncw > kMaxConsumerWarps) return ATTNRES_ERR_UNSUPPORTED;
     const int M = p->M;
     const int p2 = pow2_ceil(M);
-    pl.mb_f = p2 < (pl.vpt <= 2 ? 4 : 2) ? p2 : (pl.vpt <= 2 ? 4 : 2);
-    pl.mb_b = p2 < 4 / pl.vpt ? p2 : 4 / pl.vpt;
     pl.slot_bytes = static_cast<int>(align_up(static_cast<uint32_t>(b.D) * 2u, 128u));
     pl.s_pad = static_cast<int>(align_up(static_cast<uint32_t>(b.S), 4u));
     pl.m_pad = static_cast<int>(align_up(static_cast<uint32_t>(M), 4u));
     pl.kv0 = b.key_offset / 8;
     pl.nkv = (b.key_offset + b.R + 7) / 8 - pl.kv0;
     const uint32_t optin = static_cast<uint32_t>(dev.smem_optin);
-    auto ffits = [&](int K, int G) {
-        return make_multi_layout(K, G, pl.slot_bytes, M, 0, pl.s_pad, pl.m_pad, pl.nkv, 0, false).total <= optin;
-    };
-    if (!pick_ring(b.S, ffits, &pl.f_rows, &pl.f_chunks)) return ATTNRES_ERR_UNSUPPORTED;
+    const long long sb = pl.slot_bytes;
+
+    // Forward: as the single-query forward (two CTAs per SM when a thread owns
+    // at most two vectors), with MB = 4 / (vectors per thread) queries per
+    // pass over a token.  The queries stay in shared memory when they take at
+    // most a quarter of it, else each block's MB queries are reloaded.
+    pl.vpt = ncv <= 256 ? 1 : (ncv <= 512 ? 2 : 4);
+    pl.ncw = (ncv + 32 * pl.vpt - 1) / (32 * pl.vpt);
+    if (pl.ncw < 1 || pl.ncw > kMaxConsumerWarps) return ATTNRES_ERR_UNSUPPORTED;
+    pl.mb_f = p2 < kMultiMaxMB / pl.vpt ? p2 : kMultiMaxMB / pl.vpt;
+    const int nblk = (M + pl.mb_f - 1) / pl.mb_f;
+    bool fok = false;
+    for (int cps = kMultiMaxCtasPerSm; cps >= 1 && !fok; --cps) {
+        if (cps * (pl.ncw + 1) * 32 > 2048) continue;
+        const uint32_t budget = cps > 1 ? optin / cps - 1024 : optin;
+        const uint32_t qall = static_cast<uint32_t>(nblk * pl.mb_f) * static_cast<uint32_t>(pl.nkv) * 16u;
+        const int qrows = qall <= budget / 2 ? nblk * pl.mb_f : pl.mb_f;
+        auto ffits = [&](int chunks, int rows) {
+            return make_multi_fwd_layout(chunks, rows, pl.slot_bytes, pl.s_pad, qrows, pl.nkv).total <= budget;
+        };
+        const long long fixed = make_multi_fwd_layout(0, 1, pl.slot_bytes, pl.s_pad, qrows, pl.nkv).total + 64;
+        if (fixed + 2 * sb > budget) continue;
+        long long gmax = (budget - fixed) / (2 * sb);
+        if (gmax > kMaxGroup) gmax = kMaxGroup;
+        if (gmax < 1) gmax = 1;
+        const int groups = static_cast<int>((b.S + gmax - 1) / gmax);
+        const int rows = (b.S + groups - 1) / groups;
+        int chunks = 0;
+        while (chunks < kMaxChunks && ffits(chunks + 1, rows)) ++chunks;
+        if (chunks < 2) continue;
+        int gc = chunks - 1;
+        while (gc > 1 && gc * rows > kMaxGroup) --gc;
+        pl.f_rows = rows;
+        pl.f_chunks = chunks;
+        pl.f_group = gc * rows;
+        pl.qrows = qrows;
+        pl.smem_fwd = make_multi_fwd_layout(chunks, rows, pl.slot_bytes, pl.s_pad, qrows, pl.nkv).total;
+        // more than one CTA per SM only when the kernel's registers allow it
+        if (cps > 1 && multi_fwd_occupancy(pl) < cps) continue;
+        long long fg = static_cast<long long>(cps) * dev.sm_count;
+        if (b.N < fg) fg = b.N;
+        pl.fgrid = static_cast<int>(fg < 1 ? 1 : fg);
+        fok = true;
+    }
+    if (!fok) return ATTNRES_ERR_UNSUPPORTED;
+
+    // Backward: a token's rows, its dy rows and the queries stay resident.
+    pl.b_vpt = ncv <= 32 * kMultiBwdWarps ? 1 : 2;
+    pl.b_ncw = (ncv + 32 * pl.b_vpt - 1) / (32 * pl.b_vpt);
+    pl.mb_b = p2 < 2 / pl.b_vpt ? p2 : 2 / pl.b_vpt;
     const int nmb = (M + pl.mb_b - 1) / pl.mb_b;
     const int dq_nkv = nmb > 1 ? pl.nkv : 0;
-    bool ok = false;
-    for (int ds = 2; ds >= 1 && !ok; --ds) {
-        auto bfits = [&](int K, int G) {
-            return make_multi_layout(K, G, pl.slot_bytes, M, ds, pl.s_pad, pl.m_pad, pl.nkv, dq_nkv, true).total <=
-                   optin;
-        };
-        if (pick_ring(b.S, bfits, &pl.b_rows, &pl.b_chunks)) {
+    pl.bwd_ok = 0;
+    int bcps = 1;
+    for (int cps = kMultiMaxCtasPerSm; cps >= 1 && !pl.bwd_ok; --cps) {
+        if (cps * (pl.b_ncw + 1) * 32 > 2048 || pl.b_ncw > kMultiBwdWarps) continue;
+        const uint32_t budget = cps > 1 ? optin / cps - 1024 : optin;
+        for (int ds = 2; ds >= 1 && !pl.bwd_ok; --ds) {
+            auto bfits = [&](int K, int G) {
+                return make_multi_layout(K, G, pl.slot_bytes, M, ds, pl.s_pad, pl.m_pad, pl.nkv, dq_nkv, true)
+                           .total <= budget;
+            };
+            if (!pick_ring(b.S, bfits, &pl.b_rows, &pl.b_chunks)) continue;
             pl.dy_slots = ds;
-            ok = true;
+            pl.smem_bwd = make_multi_layout(pl.b_chunks, pl.b_rows, pl.slot_bytes, M, ds, pl.s_pad, pl.m_pad,
+                                            pl.nkv, dq_nkv, true).total;
+            if (cps > 1 && multi_bwd_occupancy(pl) < cps) continue;
+            pl.bwd_ok = 1;
+            bcps = cps;
         }
     }
-    if (!ok) return ATTNRES_ERR_UNSUPPORTED;
-    pl.smem_fwd = make_multi_layout(pl.f_chunks, pl.f_rows, pl.slot_bytes, M, 0, pl.s_pad, pl.m_pad, pl.nkv, 0,
-                                    false).total;
-    pl.smem_bwd = make_multi_layout(pl.b_chunks, pl.b_rows, pl.slot_bytes, M, pl.dy_slots, pl.s_pad, pl.m_pad,
-                                    pl.nkv, dq_nkv, true).total;
-    long long grid = dev.sm_count;
+    long long grid = static_cast<long long>(bcps) * dev.sm_count;
     if (b.N < grid) grid = b.N;
     pl.grid = static_cast<int>(grid < 1 ? 1 : grid);
     pl.ws_bytes = b.N == 0 ? 0 : static_cast<size_t>(pl.grid) * M * b.R * 4;
@@ -520,9 +564,10 @@ attnres_status attnres_multi_plan_info(const attnres_multi_params* p, int64_t ou
     MultiPlan pl;
     st = make_multi_plan(p, &pl);
     if (st != ATTNRES_OK) return st;
-    out[0] = pl.grid;
-    out[1] = pl.ncw;
-    out[2] = pl.vpt;
+    if (!pl.bwd_ok) return ATTNRES_ERR_UNSUPPORTED;
+    out[0] = static_cast<int64_t>(pl.fgrid) * 1000 + pl.grid;
+    out[1] = pl.ncw * 1000 + pl.b_ncw;
+    out[2] = pl.vpt * 1000 + pl.b_vpt;
     out[3] = pl.mb_f * 1000 + pl.mb_b;
     out[4] = pl.f_chunks * 1000 + pl.f_rows;
     out[5] = pl.b_chunks * 1000 + pl.b_rows;
@@ -560,10 +605,11 @@ attnres_status attnres_multi_fwd(const attnres_multi_params* p, const void* q, v
     a.scale = b.scale;
     a.chunks = pl.f_chunks;
     a.rows = pl.f_rows;
+    a.group = pl.f_group;
+    a.qrows = pl.qrows;
     a.slot_bytes = pl.slot_bytes;
     a.ncw = pl.ncw;
     a.s_pad = pl.s_pad;
-    a.m_pad = pl.m_pad;
     a.kv0 = pl.kv0;
     a.nkv = pl.nkv;
     a.q = static_cast<const uint16_t*>(q);
@@ -608,6 +654,7 @@ attnres_status attnres_multi_bwd(const attnres_multi_params* p, const void* q, c
     MultiPlan pl;
     st = make_multi_plan(p, &pl);
     if (st != ATTNRES_OK) return st;
+    if (!pl.bwd_ok) return ATTNRES_ERR_UNSUPPORTED;
     if (!workspace || workspace_bytes < pl.ws_bytes) return ATTNRES_ERR_WORKSPACE;
     if (!aligned16(workspace)) return ATTNRES_ERR_ALIGNMENT;
     MultiBwdArgs a;
@@ -632,7 +679,7 @@ attnres_status attnres_multi_bwd(const attnres_multi_params* p, const void* q, c
     a.rows = pl.b_rows;
     a.slot_bytes = pl.slot_bytes;
     a.dy_slots = pl.dy_slots;
-    a.ncw = pl.ncw;
+    a.ncw = pl.b_ncw;
     a.s_pad = pl.s_pad;
     a.m_pad = pl.m_pad;
     a.kv0 = pl.kv0;

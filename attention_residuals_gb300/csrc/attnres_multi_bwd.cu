@@ -11,7 +11,8 @@
 //   dq_m  += sum_s b_ms t_s                      (summed over tokens)
 // The sources feed every query, so their gradient is the sum over queries.
 //
-// GB300 mapping.  One persistent CTA per SM.  A producer warp streams each
+// GB300 mapping.  One persistent CTA per SM with up to 16 consumer warps
+// (the passes below are latency-bound: more warps hide it).  A producer warp streams each
 // token's S source rows (1-D TMA into a chunk ring), its M dy rows (one TMA
 // group per token into a dy ring) and its saved statistics (cp.async into a
 // two-slot ring).  The token stays resident for all passes:
@@ -45,7 +46,7 @@ __device__ __forceinline__ float2 key_part(const float2 x, unsigned mask, int kk
 }
 
 template <int VPT, int MB>
-__global__ void __launch_bounds__(kMaxThreads, 1) attnres_multi_bwd_kernel(const __grid_constant__ MultiBwdArgs a) {
+__global__ void __launch_bounds__(kMultiBwdThreads, 1) attnres_multi_bwd_kernel(const __grid_constant__ MultiBwdArgs a) {
     extern __shared__ __align__(128) unsigned char smem[];
     const int ncw = a.ncw;
     const int nct = ncw * 32;
@@ -574,12 +575,24 @@ cudaError_t launch_t(const MultiPlan& plan, const MultiBwdArgs& a, cudaStream_t 
     cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                            static_cast<int>(plan.smem_bwd));
     if (err != cudaSuccess) return err;
-    kern<<<plan.grid, (plan.ncw + 1) * 32, plan.smem_bwd, stream>>>(a);
+    kern<<<plan.grid, (plan.b_ncw + 1) * 32, plan.smem_bwd, stream>>>(a);
     err = cudaGetLastError();
     if (err != cudaSuccess) return err;
     const int W = a.M * a.R;
     return launch_finalize(a.part, plan.grid, W, W, const_cast<uint16_t*>(a.dq), a.dq_f32, nullptr, nullptr,
                            stream);
+}
+
+template <int VPT, int MB>
+int occupancy_t(const MultiPlan& plan) {
+    auto kern = attnres_multi_bwd_kernel<VPT, MB>;
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(plan.smem_bwd)) !=
+        cudaSuccess)
+        return 0;
+    int n = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kern, (plan.b_ncw + 1) * 32, plan.smem_bwd) != cudaSuccess)
+        return 0;
+    return n;
 }
 
 }  // namespace
@@ -591,15 +604,21 @@ unsigned take_multi_bwd_error() {
     return v;
 }
 
+int multi_bwd_occupancy(const MultiPlan& plan) {
+    switch (plan.b_vpt * 10 + plan.mb_b) {
+        case 11: return occupancy_t<1, 1>(plan);
+        case 12: return occupancy_t<1, 2>(plan);
+        case 21: return occupancy_t<2, 1>(plan);
+        default: return 0;
+    }
+}
+
 cudaError_t launch_multi_bwd(const MultiPlan& plan, const MultiBwdArgs& a, cudaStream_t stream) {
-    const int key = plan.vpt * 10 + plan.mb_b;
+    const int key = plan.b_vpt * 10 + plan.mb_b;
     switch (key) {
         case 11: return launch_t<1, 1>(plan, a, stream);
         case 12: return launch_t<1, 2>(plan, a, stream);
-        case 14: return launch_t<1, 4>(plan, a, stream);
         case 21: return launch_t<2, 1>(plan, a, stream);
-        case 22: return launch_t<2, 2>(plan, a, stream);
-        case 41: return launch_t<4, 1>(plan, a, stream);
         default: return cudaErrorInvalidConfiguration;
     }
 }

@@ -6,22 +6,28 @@
 // (section "Equation"):
 //   r_s = 1/sqrt(mean(t_s^2) + eps),  z_ms = scale * r_s * <t_s, q_m>,
 //   alpha_m = softmax_s(z_m),          y_m = sum_s alpha_ms v_s.
-// The key statistics r_s do not depend on the query, so they are formed once.
+// The key statistics r_s do not depend on the query, so they are formed once
+// per token.
 //
-// GB300 mapping.  One persistent CTA per SM; a producer thread streams every
-// source row of a token into a ring of shared-memory chunks with 1-D TMA
-// bulk copies, and the token stays resident while all M queries are served,
-// so each source row is read from HBM once for all M outputs.
-//   pass 1: one warp per source row; lanes stride over the key vectors and
-//           accumulate the key sum of squares and the M query dots with
-//           mixed-precision bf16 FMAs (queries in shared memory), then one
-//           reduce-scatter per four queries gives the row's totals.
-//   softmax: after one CTA barrier, one warp per query forms its logits and
-//           weights (lanes over sources) into a shared table.
-//   pass 2: after a second barrier, thread t owns fixed 16-byte column
-//           vectors and accumulates MB outputs at a time in FP32 registers
-//           (packed FFMA2), so each source row is unpacked once per MB
-//           queries; the last block releases each chunk once read.
+// GB300 mapping: the single-query forward's streaming design, serving MB
+// queries per pass over a token.  Persistent CTAs (two per SM when a thread
+// owns at most two vectors, so one CTA's barrier and softmax phases overlap
+// the other's streaming); a producer thread streams the token's rows into a
+// ring of chunks with 1-D TMA bulk copies; the softmax runs online over
+// groups of whole chunks, so a token never has to fit in shared memory.
+//   pass 1: one warp per row; lanes stride over the key vectors and form the
+//           key sum of squares (first block only) and the MB query dots with
+//           mixed-precision bf16 FMAs, then one reduce-scatter per row;
+//   softmax: after one CTA barrier every warp updates the MB running maxima
+//           and denominators itself (identical inputs, identical results),
+//           so no second barrier is needed;
+//   pass 2: thread t owns fixed 16-byte column vectors and accumulates the
+//           MB outputs in FP32 registers (each row unpacked once for all MB
+//           queries, packed FFMA2), releasing each chunk after its rows.
+// With M > MB the queries are served in blocks of MB: a token that fits in
+// one softmax group stays in shared memory for every block; a longer token is
+// streamed once per block, all passes but the last asking L2 to keep the rows
+// (evict_last), so the re-reads are served from L2 and HBM sees each row once.
 // Bandwidth-bound per-token reductions: no tensor cores.
 #include <cfloat>
 
@@ -35,22 +41,37 @@ namespace {
 // First failed wait of any multi-query forward launch (0 = none).
 __device__ unsigned int g_multi_error = 0;
 
+__device__ __forceinline__ uint64_t policy_evict_last() {
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+
 template <int VPT, int MB>
-__global__ void __launch_bounds__(kMaxThreads, 1) attnres_multi_fwd_kernel(const __grid_constant__ MultiFwdArgs a) {
+__global__ void __launch_bounds__(kMaxThreads, multi_fwd_ctas_per_sm(VPT))
+    attnres_multi_fwd_kernel(const __grid_constant__ MultiFwdArgs a) {
+    constexpr int KV = 1 + MB;                     // values reduced per row
+    constexpr int KR = KV <= 2 ? 2 : (KV <= 4 ? 4 : 8);  // reduce-scatter width
     extern __shared__ __align__(128) unsigned char smem[];
     const int ncw = a.ncw;
     const int nct = ncw * 32;
     const int K = a.chunks;
     const int G = a.rows;
+    const int GG = a.group;
     const int S = a.S;
     const int M = a.M;
-    const int s_pad = a.s_pad, m_pad = a.m_pad;
-    const MultiLayout L = make_multi_layout(K, G, a.slot_bytes, M, 0, s_pad, m_pad, a.nkv, 0, false);
+    const int s_pad = a.s_pad;
+    const int nblk = (M + MB - 1) / MB;            // register blocks of queries
+    // A token that fits in one softmax group is loaded once and every block
+    // reads it from shared memory; otherwise it is streamed once per block.
+    const bool one_group = S <= GG;
+    const int npass = one_group ? 1 : nblk;
+    const MultiFwdLayout L = make_multi_fwd_layout(K, G, a.slot_bytes, s_pad, a.qrows, a.nkv);
     uint64_t* full = reinterpret_cast<uint64_t*>(smem + L.full);
     uint64_t* empty = reinterpret_cast<uint64_t*>(smem + L.empty);
-    float* ss_t = reinterpret_cast<float*>(smem + L.tab);  // [s_pad]
-    float* dot_t = ss_t + s_pad;                           // [m_pad][s_pad]
-    float* al_t = dot_t + m_pad * s_pad;                   // [s_pad][m_pad]
+    float* red = reinterpret_cast<float*>(smem + L.red);    // [2][KV][kMaxGroup]
+    float* zall = reinterpret_cast<float*>(smem + L.zall);  // [MB][s_pad]
+    float* rall = reinterpret_cast<float*>(smem + L.rall);  // [s_pad]
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L.misc);
 
     const int warp = threadIdx.x >> 5;
@@ -58,7 +79,6 @@ __global__ void __launch_bounds__(kMaxThreads, 1) attnres_multi_fwd_kernel(const
     const long long N = a.N;
     const uint32_t sb = static_cast<uint32_t>(a.slot_bytes);
     const uint32_t cb = static_cast<uint32_t>(G) * sb;
-    const int cpt = (S + G - 1) / G;  // chunks per token
 
     if (threadIdx.x == 0) {
         for (int k = 0; k < K; ++k) {
@@ -68,37 +88,40 @@ __global__ void __launch_bounds__(kMaxThreads, 1) attnres_multi_fwd_kernel(const
         *abort_flag = 0;
         mbar_fence_init();
     }
-    // weights of padded queries stay zero
-    for (int i = threadIdx.x; i < s_pad * m_pad; i += blockDim.x) al_t[i] = 0.0f;
     __syncthreads();
 
     if (warp == ncw) {
         // ------------------------------------------------------ producer
         if (lane == 0) {
-            const uint64_t pol = policy_evict_first();
+            const uint64_t pol_last = policy_evict_first();
+            const uint64_t pol_keep = policy_evict_last();
             const uint32_t bytes = static_cast<uint32_t>(a.D) * 2u;
             unsigned char* ring = smem + L.ring;
             int k = 0;
             uint32_t phase = 0;
             long long issued = 0;
             for (long long n = blockIdx.x; n < N && !*abort_flag; n += gridDim.x) {
-                for (int g0 = 0; g0 < S; g0 += G) {
-                    const int gs = min(G, S - g0);
-                    if (!mbar_wait(empty + k, phase ^ 1u, abort_flag, &g_multi_error, kSiteFwdProducer)) break;
-                    mbar_arrive_expect_tx(full + k, bytes * static_cast<uint32_t>(gs));
-                    for (int r = 0; r < gs; ++r) {
-                        const unsigned char* src =
-                            static_cast<const unsigned char*>(a.src[g0 + r]) + (n * a.src_ld) * 2;
-                        tma_load_1d(ring + k * cb + r * sb, src, bytes, full + k, pol);
-                    }
-                    ++issued;
-                    if (++k == K) {
-                        k = 0;
-                        phase ^= 1u;
+                for (int b = 0; b < npass && !*abort_flag; ++b) {
+                    const uint64_t pol = b + 1 < npass ? pol_keep : pol_last;
+                    for (int g0 = 0; g0 < S; g0 += G) {
+                        const int gs = min(G, S - g0);
+                        if (!mbar_wait(empty + k, phase ^ 1u, abort_flag, &g_multi_error, kSiteFwdProducer)) break;
+                        mbar_arrive_expect_tx(full + k, bytes * static_cast<uint32_t>(gs));
+                        for (int r = 0; r < gs; ++r) {
+                            const unsigned char* src =
+                                static_cast<const unsigned char*>(a.src[g0 + r]) + (n * a.src_ld) * 2;
+                            tma_load_1d(ring + k * cb + r * sb, src, bytes, full + k, pol);
+                        }
+                        ++issued;
+                        if (++k == K) {
+                            k = 0;
+                            phase ^= 1u;
+                        }
                     }
                 }
             }
             if (*abort_flag) {
+                // Let every copy this thread started land before the CTA can exit.
                 for (int c = 0; c < K && c < issued; ++c) {
                     const long long fills = (issued - 1 - c) / K + 1;
                     volatile int no_abort = 0;
@@ -113,7 +136,9 @@ __global__ void __launch_bounds__(kMaxThreads, 1) attnres_multi_fwd_kernel(const
     const int ncv = a.D >> 3;
     const int ko = a.ko, kend = a.ko + a.R;
     const int kv0 = a.kv0, nkv = a.nkv;
+    const int kw = nkv * 8;
     const uint32_t kwb = static_cast<uint32_t>(nkv) * 16u;  // bytes per query row in shared memory
+    const bool q_once = a.qrows >= M;                      // every query stays in shared memory
     int col[VPT];
 #pragma unroll
     for (int i = 0; i < VPT; ++i) {
@@ -130,112 +155,52 @@ __global__ void __launch_bounds__(kMaxThreads, 1) attnres_multi_fwd_kernel(const
     const uint32_t full_s = sbase + L.full;
     const uint32_t empty_s = sbase + L.empty;
     const uint32_t qsm_s = sbase + L.qsm;
-    {
-        // queries by key channel: row m holds channels 8*kv0 .. 8*(kv0+nkv)
-        uint16_t* qsm = reinterpret_cast<uint16_t*>(smem + L.qsm);
-        const int kw = nkv * 8;
-        for (int i = threadIdx.x; i < m_pad * kw; i += nct) {
-            const int m = i / kw;
-            const int c = 8 * kv0 + (i - m * kw);
-            qsm[i] = (m < M && c >= ko && c < kend) ? a.q[static_cast<long long>(m) * a.R + (c - ko)]
-                                                    : static_cast<uint16_t>(0);
-        }
-    }
-    named_bar_sync(1, nct);
+    uint16_t* qsm = reinterpret_cast<uint16_t*>(smem + L.qsm);
+    // queries m0 .. m0+rows-1 by key channel: row j holds channels
+    // 8*kv0 .. 8*(kv0+nkv), zero outside the key and past M
     const bool key_aligned = ((ko | kend) & 7) == 0;
+    // With an aligned key and a 16-byte aligned query array a query row is
+    // copied as whole 16-byte vectors (the key window is then exactly R).
+    const bool q_vec = key_aligned && (reinterpret_cast<uintptr_t>(a.q) & 15u) == 0;
+    auto load_q = [&](int m0, int rows) {
+        if (q_vec) {
+#pragma unroll 4
+            for (int i = threadIdx.x; i < rows * nkv; i += nct) {
+                const int j = i / nkv;
+                const int m = m0 + j;
+                uint4 w = make_uint4(0u, 0u, 0u, 0u);
+                if (m < M) w = ld_global_nc_v4(a.q + static_cast<long long>(m) * a.R + 8 * (i - j * nkv));
+                *reinterpret_cast<uint4*>(qsm + 8 * i) = w;
+            }
+        } else {
+#pragma unroll 4
+            for (int i = threadIdx.x; i < rows * kw; i += nct) {
+                const int j = i / kw;
+                const int c = 8 * kv0 + (i - j * kw);
+                const int m = m0 + j;
+                qsm[i] = (m < M && c >= ko && c < kend) ? a.q[static_cast<long long>(m) * a.R + (c - ko)]
+                                                        : static_cast<uint16_t>(0);
+            }
+        }
+    };
+    if (q_once) load_q(0, a.qrows);
+    named_bar_sync(1, nct);
 
-    int ck = 0;
-    uint32_t cphase = 0;
+    int ck = 0;            // current chunk
+    uint32_t cphase = 0;   // its fill parity
+    uint32_t cbase = ring_lo;
+    int rbuf = 0;
+
     for (long long n = blockIdx.x; n < N; n += gridDim.x) {
-        {
-            int k = ck;
-            uint32_t ph = cphase;
-            for (int c = 0; c < cpt; ++c) {
-                mbar_wait_s(full_s + 8u * k, ph, abort_flag, &g_multi_error, kSiteFwdConsumer);
-                if (++k == K) {
-                    k = 0;
-                    ph ^= 1u;
-                }
+        for (int b = 0; b < nblk; ++b) {
+            const int m0 = b * MB;
+            const bool first = b == 0;
+            if (!q_once) {
+                // every warp finished the previous block's pass 1 before its last barrier
+                load_q(m0, MB);
+                named_bar_sync(1, nct);
             }
-        }
-        // pass 1: one warp per row, four queries per reduce-scatter
-        for (int r = warp; r < S; r += ncw) {
-            int kc = ck + r / G;
-            if (kc >= K) kc -= K;
-            const uint32_t row = ring_raw + static_cast<uint32_t>(kc) * cb +
-                                 static_cast<uint32_t>(r % G) * sb + 16u * static_cast<uint32_t>(kv0);
-            for (int qb = 0; qb < m_pad; qb += 4) {
-                float s0 = 0.0f, s1 = 0.0f;
-                float t[4][2];
-#pragma unroll
-                for (int j = 0; j < 4; ++j) t[j][0] = t[j][1] = 0.0f;
-                const uint32_t qrow = qsm_s + static_cast<uint32_t>(qb) * kwb;
-                for (int v = lane; v < nkv; v += 32) {
-                    uint4 x = lds128(row + 16u * v);
-                    if (!key_aligned) x = mask_bf16x8(x, 8 * (kv0 + v), ko, kend);
-                    if (qb == 0) bf16_sq8(x, s0, s1);
-#pragma unroll
-                    for (int j = 0; j < 4; ++j) {
-                        const uint4 qv = lds128(qrow + static_cast<uint32_t>(j) * kwb + 16u * v);
-                        bf16_dot8(x, qv, t[j][0], t[j][1]);
-                    }
-                }
-                float part[8] = {s0 + s1, t[0][0] + t[0][1], t[1][0] + t[1][1], t[2][0] + t[2][1],
-                                 t[3][0] + t[3][1], 0.0f, 0.0f, 0.0f};
-                warp_reduce_scatter<8>(part, lane);
-                if ((lane & 3) == 0) {
-                    const int e = lane >> 2;
-                    if (e == 0) {
-                        if (qb == 0) ss_t[r] = part[0];
-                    } else if (e <= 4) {
-                        dot_t[(qb + e - 1) * s_pad + r] = part[0];
-                    }
-                }
-            }
-        }
-        named_bar_sync(1, nct);
-        // softmax: one warp per query, lanes over sources
-        for (int m = warp; m < M; m += ncw) {
-            float z[4], rr[4];
-            float mx = -FLT_MAX;
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                const int s = lane + 32 * i;
-                z[i] = -FLT_MAX;
-                rr[i] = 0.0f;
-                if (s < S) {
-                    rr[i] = rsqrtf(fmaf(ss_t[s], inv_r, a.eps));
-                    z[i] = a.scale * rr[i] * dot_t[m * s_pad + s];
-                    mx = fmaxf(mx, z[i]);
-                }
-            }
-            mx = warp_max(mx);
-            float e[4];
-            float es = 0.0f;
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                e[i] = (lane + 32 * i < S) ? __expf(z[i] - mx) : 0.0f;
-                es += e[i];
-            }
-            const float inv_l = 1.0f / warp_sum(es);
-            float* arow = a.alpha + (n * M + m) * S;
-            float* zrow = a.logit + (n * M + m) * S;
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                const int s = lane + 32 * i;
-                if (s < S) {
-                    const float al = e[i] * inv_l;
-                    al_t[s * m_pad + m] = al;
-                    arow[s] = al;
-                    zrow[s] = z[i];
-                    if (m == 0) a.rstd[n * S + s] = rr[i];
-                }
-            }
-        }
-        named_bar_sync(1, nct);
-        // pass 2: MB outputs at a time; the last block releases the chunks
-        for (int mb = 0; mb < M; mb += MB) {
-            const bool last = mb + MB >= M;
+            const uint32_t qbase = qsm_s + static_cast<uint32_t>(q_once ? m0 : 0) * kwb;
             float2 acc[MB][VPT][4];
 #pragma unroll
             for (int j = 0; j < MB; ++j)
@@ -243,56 +208,175 @@ __global__ void __launch_bounds__(kMaxThreads, 1) attnres_multi_fwd_kernel(const
                 for (int i = 0; i < VPT; ++i)
 #pragma unroll
                     for (int kk = 0; kk < 4; ++kk) acc[j][i][kk] = make_float2(0.0f, 0.0f);
-            int kc = ck;
-            for (int r0 = 0; r0 < S; r0 += G) {
-                const int rn = min(G, S - r0);
-                uint32_t dep = 0;
-                uint32_t rowa = ring_lo + static_cast<uint32_t>(kc) * cb;
-                for (int r = 0; r < rn; ++r) {
-                    const float* al_row = al_t + (r0 + r) * m_pad + mb;
-                    float2 w2[MB];
-#pragma unroll
-                    for (int j = 0; j < MB; ++j) w2[j] = make_float2(al_row[j], al_row[j]);
-#pragma unroll
-                    for (int i = 0; i < VPT; ++i) {
-                        if (col[i] >= 0) {
-                            const uint4 xv = lds128(rowa + i * vstep);
-                            dep ^= xv.x;
-#pragma unroll
-                            for (int kk = 0; kk < 4; ++kk) {
-                                const float2 x2 = bf2_to_f2(u4_get(xv, kk));
-#pragma unroll
-                                for (int j = 0; j < MB; ++j) acc[j][i][kk] = ffma2(w2[j], x2, acc[j][i][kk]);
-                            }
-                        }
-                    }
-                    rowa += sb;
-                }
-                if (last) {
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive_after(empty_s + 8u * kc, dep);
-                }
-                if (++kc == K) kc = 0;
-            }
+            float m_run[MB], l_run[MB];  // running softmax state (same in every warp)
 #pragma unroll
             for (int j = 0; j < MB; ++j) {
-                if (mb + j < M) {
-                    uint16_t* yrow = a.y + static_cast<long long>(mb + j) * a.y_ms + n * a.y_ns;
+                m_run[j] = -FLT_MAX;
+                l_run[j] = 0.0f;
+            }
+
+            const bool load_rows = !one_group || b == 0;          // wait for the rows
+            const bool free_rows = !one_group || b + 1 == nblk;   // release them after pass 2
+            for (int g0 = 0; g0 < S; g0 += GG) {
+                const int gs = min(GG, S - g0);
+                if (load_rows) {
+                    int k = ck;
+                    uint32_t ph = cphase;
+                    for (int r0 = 0; r0 < gs; r0 += G) {
+                        mbar_wait_s(full_s + 8u * k, ph, abort_flag, &g_multi_error, kSiteFwdConsumer);
+                        if (++k == K) {
+                            k = 0;
+                            ph ^= 1u;
+                        }
+                    }
+                }
+                // pass 1: one warp per row
+                for (int r = warp; r < gs; r += ncw) {
+                    int rr = r;
+                    int kc = ck;
+                    while (rr >= G) {
+                        rr -= G;
+                        if (++kc == K) kc = 0;
+                    }
+                    const uint32_t row = ring_raw + static_cast<uint32_t>(kc) * cb + static_cast<uint32_t>(rr) * sb +
+                                         16u * static_cast<uint32_t>(kv0);
+                    float s0 = 0.0f, s1 = 0.0f;
+                    float t[MB][2];
+#pragma unroll
+                    for (int j = 0; j < MB; ++j) t[j][0] = t[j][1] = 0.0f;
+                    for (int v = lane; v < nkv; v += 32) {
+                        uint4 x = lds128(row + 16u * v);
+                        if (!key_aligned) x = mask_bf16x8(x, 8 * (kv0 + v), ko, kend);
+                        if (first) bf16_sq8(x, s0, s1);
+#pragma unroll
+                        for (int j = 0; j < MB; ++j) {
+                            const uint4 qv = lds128(qbase + static_cast<uint32_t>(j) * kwb + 16u * v);
+                            bf16_dot8(x, qv, t[j][0], t[j][1]);
+                        }
+                    }
+                    float part[KR];
+                    part[0] = s0 + s1;
+#pragma unroll
+                    for (int j = 0; j < MB; ++j) part[1 + j] = t[j][0] + t[j][1];
+#pragma unroll
+                    for (int e = KV; e < KR; ++e) part[e] = 0.0f;
+                    warp_reduce_scatter<KR>(part, lane);
+                    constexpr int W = 32 / KR;  // lanes per reduced value
+                    if ((lane & (W - 1)) == 0) {
+                        const int e = lane / W;
+                        if (e < KV) red[(rbuf * KV + e) * kMaxGroup + r] = part[0];
+                    }
+                }
+                named_bar_sync(1, nct);
+                // Every warp updates the running softmax of each of the MB
+                // queries itself; lane l holds row g0 + l.
+                float e[MB], corr[MB];
+                {
+                    float rs = 0.0f;
+                    if (lane < gs)
+                        rs = first ? rsqrtf(fmaf(red[(rbuf * KV) * kMaxGroup + lane], inv_r, a.eps)) : rall[g0 + lane];
+#pragma unroll
+                    for (int j = 0; j < MB; ++j) {
+                        const float qt = lane < gs ? red[(rbuf * KV + 1 + j) * kMaxGroup + lane] : 0.0f;
+                        const float z = a.scale * rs * qt;
+                        const float m_new = fmaxf(m_run[j], warp_max(lane < gs ? z : -FLT_MAX));
+                        e[j] = lane < gs ? __expf(z - m_new) : 0.0f;
+                        const float esum = warp_sum(e[j]);
+                        corr[j] = __expf(m_run[j] - m_new);
+                        l_run[j] = fmaf(l_run[j], corr[j], esum);
+                        m_run[j] = m_new;
+                        if (warp == 0 && lane < gs) zall[j * s_pad + g0 + lane] = z;
+                    }
+                    if (first && warp == 0 && lane < gs) rall[g0 + lane] = rs;
+                }
+                rbuf ^= 1;
+                // pass 2: rescale the running sums and add this group's rows
+#pragma unroll
+                for (int j = 0; j < MB; ++j) {
+                    const float2 c2 = make_float2(corr[j], corr[j]);
+#pragma unroll
+                    for (int i = 0; i < VPT; ++i)
+#pragma unroll
+                        for (int kk = 0; kk < 4; ++kk) acc[j][i][kk] = fmul2(acc[j][i][kk], c2);
+                }
+                int lk = ck;            // chunk cursor of this pass
+                uint32_t lbase = cbase;
+                uint32_t lphase = cphase;
+                for (int r0 = 0; r0 < gs; r0 += G) {
+                    const int rn = min(G, gs - r0);
+                    uint32_t dep = 0;
+                    uint32_t rowa = lbase;
+                    for (int r = 0; r < rn; ++r) {
+                        float2 es2[MB];
+#pragma unroll
+                        for (int j = 0; j < MB; ++j) {
+                            const float es = __shfl_sync(0xffffffffu, e[j], r0 + r);
+                            es2[j] = make_float2(es, es);
+                        }
+#pragma unroll
+                        for (int i = 0; i < VPT; ++i) {
+                            if (col[i] >= 0) {
+                                const uint4 xv = lds128(rowa + i * vstep);
+                                dep ^= xv.x;
+#pragma unroll
+                                for (int kk = 0; kk < 4; ++kk) {
+                                    const float2 x2 = bf2_to_f2(u4_get(xv, kk));
+#pragma unroll
+                                    for (int j = 0; j < MB; ++j) acc[j][i][kk] = ffma2(es2[j], x2, acc[j][i][kk]);
+                                }
+                            }
+                        }
+                        rowa += sb;
+                    }
+                    if (free_rows) {
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive_after(empty_s + 8u * lk, dep);
+                    }
+                    lbase += cb;
+                    if (++lk == K) {
+                        lk = 0;
+                        lbase = ring_lo;
+                        lphase ^= 1u;
+                    }
+                }
+                if (free_rows) {
+                    ck = lk;
+                    cbase = lbase;
+                    cphase = lphase;
+                }
+            }
+            // this block's outputs and statistics
+            float inv_l[MB];
+#pragma unroll
+            for (int j = 0; j < MB; ++j) inv_l[j] = 1.0f / l_run[j];
+#pragma unroll
+            for (int j = 0; j < MB; ++j) {
+                if (m0 + j < M) {
+                    const float2 il2 = make_float2(inv_l[j], inv_l[j]);
+                    uint16_t* yrow = a.y + static_cast<long long>(m0 + j) * a.y_ms + n * a.y_ns;
 #pragma unroll
                     for (int i = 0; i < VPT; ++i) {
                         if (col[i] >= 0) {
                             st_global_cs_v4(yrow + 8 * col[i],
-                                            make_uint4(pack_f2(acc[j][i][0]), pack_f2(acc[j][i][1]),
-                                                       pack_f2(acc[j][i][2]), pack_f2(acc[j][i][3])));
+                                            make_uint4(pack_f2(fmul2(acc[j][i][0], il2)), pack_f2(fmul2(acc[j][i][1], il2)),
+                                                       pack_f2(fmul2(acc[j][i][2], il2)), pack_f2(fmul2(acc[j][i][3], il2))));
                         }
                     }
                 }
             }
-        }
-        for (int c = 0; c < cpt; ++c) {
-            if (++ck == K) {
-                ck = 0;
-                cphase ^= 1u;
+            if (warp == 0) {
+                __syncwarp();
+                for (int s = lane; s < S; s += 32) {
+#pragma unroll
+                    for (int j = 0; j < MB; ++j) {
+                        if (m0 + j < M) {
+                            const float z = zall[j * s_pad + s];
+                            a.alpha[(n * M + m0 + j) * S + s] = __expf(z - m_run[j]) * inv_l[j];
+                            a.logit[(n * M + m0 + j) * S + s] = z;
+                        }
+                    }
+                    if (first) a.rstd[n * S + s] = rall[s];
+                }
             }
         }
     }
@@ -304,8 +388,20 @@ cudaError_t launch_t(const MultiPlan& plan, const MultiFwdArgs& a, cudaStream_t 
     cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                            static_cast<int>(plan.smem_fwd));
     if (err != cudaSuccess) return err;
-    kern<<<plan.grid, (plan.ncw + 1) * 32, plan.smem_fwd, stream>>>(a);
+    kern<<<plan.fgrid, (plan.ncw + 1) * 32, plan.smem_fwd, stream>>>(a);
     return cudaGetLastError();
+}
+
+template <int VPT, int MB>
+int occupancy_t(const MultiPlan& plan) {
+    auto kern = attnres_multi_fwd_kernel<VPT, MB>;
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(plan.smem_fwd)) !=
+        cudaSuccess)
+        return 0;
+    int n = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kern, (plan.ncw + 1) * 32, plan.smem_fwd) != cudaSuccess)
+        return 0;
+    return n;
 }
 
 }  // namespace
@@ -317,6 +413,18 @@ unsigned take_multi_fwd_error() {
     return v;
 }
 
+int multi_fwd_occupancy(const MultiPlan& plan) {
+    switch (plan.vpt * 10 + plan.mb_f) {
+        case 11: return occupancy_t<1, 1>(plan);
+        case 12: return occupancy_t<1, 2>(plan);
+        case 14: return occupancy_t<1, 4>(plan);
+        case 21: return occupancy_t<2, 1>(plan);
+        case 22: return occupancy_t<2, 2>(plan);
+        case 41: return occupancy_t<4, 1>(plan);
+        default: return 0;
+    }
+}
+
 cudaError_t launch_multi_fwd(const MultiPlan& plan, const MultiFwdArgs& a, cudaStream_t stream) {
     const int key = plan.vpt * 10 + plan.mb_f;
     switch (key) {
@@ -325,9 +433,7 @@ cudaError_t launch_multi_fwd(const MultiPlan& plan, const MultiFwdArgs& a, cudaS
         case 14: return launch_t<1, 4>(plan, a, stream);
         case 21: return launch_t<2, 1>(plan, a, stream);
         case 22: return launch_t<2, 2>(plan, a, stream);
-        case 24: return launch_t<2, 4>(plan, a, stream);
         case 41: return launch_t<4, 1>(plan, a, stream);
-        case 42: return launch_t<4, 2>(plan, a, stream);
         default: return cudaErrorInvalidConfiguration;
     }
 }

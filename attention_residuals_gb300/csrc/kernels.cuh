@@ -163,15 +163,20 @@ struct BwdArgs {
 // M rows) and its saved statistics (two slots) in shared memory.
 // ---------------------------------------------------------------------------
 constexpr int kMultiTokSlots = 2;
+// The multi-query backward runs up to 16 consumer warps (one 16-byte vector
+// per thread up to D = 4096) so that more warps hide shared-memory and
+// barrier latency; registers are then capped near 120 per thread.
+constexpr int kMultiBwdWarps = 16;
+constexpr int kMultiBwdThreads = (kMultiBwdWarps + 1) * 32;
 
 struct MultiLayout {
     uint32_t ring, dyring, full, empty, dyfull, dyempty, tfull, tempty, tok, tab, qsm, dqsm, misc, total;
     uint32_t tstride;  // floats per statistics slot
 };
 
-// Tables (floats).  Forward: ss[s_pad], dot[m_pad][s_pad], alpha[s_pad][m_pad].
-// Backward: da[m_pad][s_pad], alpha[s_pad][m_pad], b[s_pad][m_pad],
-// zr[m_pad][s_pad].  qsm: m_pad query rows of nkv 16-byte vectors (bf16).
+// Backward layout.  Tables (floats): da[m_pad][s_pad], alpha[s_pad][m_pad],
+// b[s_pad][m_pad], zr[m_pad][s_pad].  qsm: m_pad query rows of nkv 16-byte
+// vectors (bf16).
 // dqsm (backward, only when the queries take several register blocks): M
 // rows of dq_nkv * 8 FP32 dq partial sums.
 __host__ __device__ inline MultiLayout make_multi_layout(int chunks, int rows, int slot_bytes, int M,
@@ -201,7 +206,7 @@ __host__ __device__ inline MultiLayout make_multi_layout(int chunks, int rows, i
     L.tok = off;
     off += backward ? kMultiTokSlots * L.tstride * 4u : 0u;
     L.tab = off;
-    off += (backward ? 4u * m_pad * s_pad : (s_pad + 2u * m_pad * s_pad)) * 4u;
+    off += 4u * m_pad * s_pad * 4u;
     off = align_up(off, 16);
     L.qsm = off;
     off += static_cast<uint32_t>(m_pad) * static_cast<uint32_t>(nkv) * 16u;
@@ -213,9 +218,57 @@ __host__ __device__ inline MultiLayout make_multi_layout(int chunks, int rows, i
     return L;
 }
 
+// Forward of the multi-query read: streamed like the single-query forward
+// (online softmax over groups of whole chunks), MB queries per pass over a
+// token.  Layout: chunk ring, full/empty mbarriers, pass-1 results
+// [2][1 + kMultiMaxMB][kMaxGroup], logits of the block's queries
+// [kMultiMaxMB][s_pad], key rstd [s_pad], queries [qrows][nkv * 8] bf16.
+constexpr int kMultiMaxMB = 4;
+// Register budget of the forward: two CTAs of up to 288 threads per SM when a
+// thread owns at most two vectors.  The planner may place more CTAs of
+// narrower rows (fewer warps) on an SM when they fit.
+__host__ __device__ constexpr int multi_fwd_ctas_per_sm(int vpt) { return vpt <= 2 ? 2 : 1; }
+constexpr int kMultiMaxCtasPerSm = 4;
+
+struct MultiFwdLayout {
+    uint32_t ring, full, empty, red, zall, rall, qsm, misc, total;
+};
+
+__host__ __device__ inline MultiFwdLayout make_multi_fwd_layout(int chunks, int rows, int slot_bytes, int s_pad,
+                                                               int qrows, int nkv) {
+    MultiFwdLayout L;
+    uint32_t off = 0;
+    L.ring = off;
+    off += static_cast<uint32_t>(chunks) * static_cast<uint32_t>(rows) * static_cast<uint32_t>(slot_bytes);
+    off = align_up(off, 16);
+    L.full = off;
+    off += 8u * chunks;
+    L.empty = off;
+    off += 8u * chunks;
+    off = align_up(off, 16);
+    L.red = off;
+    off += 2u * (1 + kMultiMaxMB) * kMaxGroup * 4u;
+    L.zall = off;
+    off += static_cast<uint32_t>(kMultiMaxMB) * s_pad * 4u;
+    L.rall = off;
+    off += static_cast<uint32_t>(s_pad) * 4u;
+    off = align_up(off, 16);
+    L.qsm = off;
+    off += static_cast<uint32_t>(qrows) * static_cast<uint32_t>(nkv) * 16u;
+    L.misc = off;
+    off += 16u;
+    L.total = align_up(off, 128);
+    return L;
+}
+
 struct MultiPlan {
     int grid;
-    int ncw, vpt;          // consumer warps, 16-byte vectors per thread
+    int fgrid;             // forward CTAs (multi_fwd_ctas_per_sm per SM)
+    int f_group;           // forward softmax group rows (whole chunks, <= kMaxGroup)
+    int qrows;             // query rows held in shared memory by the forward
+    int bwd_ok;            // the backward's resident layout fits
+    int ncw, vpt;          // forward: consumer warps, 16-byte vectors per thread
+    int b_ncw, b_vpt;      // backward
     int mb_f, mb_b;        // queries per register block (forward / backward)
     int slot_bytes, s_pad, m_pad;
     int kv0, nkv;          // key window in 16-byte vectors
@@ -231,7 +284,9 @@ struct MultiFwdArgs {
     long long y_ms, y_ns;  // elements between queries / tokens of the output
     int S, D, R, ko, M;
     float eps, scale;
-    int chunks, rows, slot_bytes, ncw, s_pad, m_pad, kv0, nkv;
+    int chunks, rows, slot_bytes, ncw, s_pad, kv0, nkv;
+    int group;             // softmax group rows (whole chunks)
+    int qrows;             // query rows in shared memory (M, or MB: reloaded per block)
     const uint16_t* q;     // [M][R]
     uint16_t* y;
     float* alpha;          // [N][M][S]
@@ -260,6 +315,9 @@ struct MultiBwdArgs {
 unsigned take_multi_fwd_error();
 unsigned take_multi_bwd_error();
 cudaError_t launch_multi_fwd(const MultiPlan& plan, const MultiFwdArgs& a, cudaStream_t stream);
+// CTAs of the plan's kernel variant that fit on one SM (0 on error).
+int multi_fwd_occupancy(const MultiPlan& plan);
+int multi_bwd_occupancy(const MultiPlan& plan);
 cudaError_t launch_multi_bwd(const MultiPlan& plan, const MultiBwdArgs& a, cudaStream_t stream);
 // Column sums of a [P][W] FP32 partial matrix in row order; columns < R go to
 // dq (bf16 + optional FP32), the rest to dw_o.

@@ -216,12 +216,14 @@ attnres_status attnres_plan_info(const attnres_params* p, int64_t out[8]);
  * Every source row is read from HBM once per call for all M outputs.  The
  * gradient of a source is the sum over queries; dq_m sums over tokens.
  *
- * Supported range: a token's S source rows stay in shared memory while all
- * queries are served, and the backward also holds the token's M dy rows and
- * the queries' key channels.  Shapes where these do not fit the device's
- * shared memory (roughly (S + M) * D * 2 + M * R * 2 bytes beyond ~220 KB)
- * return ATTNRES_ERR_UNSUPPORTED before anything is enqueued;
- * attnres_multi_plan_info tells in advance.
+ * The forward streams each token's rows once per block of queries it holds
+ * in registers (one block for M <= 4 at D <= 2048, M <= 2 at D <= 4096;
+ * later blocks re-read the token from L2), so any S and D are served.  The
+ * backward keeps a token's S source rows, its M dy rows and the queries' key
+ * channels in shared memory; shapes where these do not fit (roughly
+ * (S + 2 * M) * D * 2 + M * R * 2 bytes beyond ~220 KB) return
+ * ATTNRES_ERR_UNSUPPORTED from attnres_multi_bwd (and from
+ * attnres_multi_plan_info) before anything is enqueued.
  * ------------------------------------------------------------------------ */
 #define ATTNRES_MAX_M 16
 
@@ -272,12 +274,13 @@ attnres_status attnres_multi_bwd(const attnres_multi_params* p, const void* q, c
                                  void* workspace, size_t workspace_bytes, void* stream);
 
 /*
- * Launch plan of the multi-query kernels (no launch).  out[0..7]: grid CTAs,
- * consumer warps, 16-byte vectors per thread, queries per register block
- * (forward * 1000 + backward), forward ring (chunks * 1000 + rows per
- * chunk), backward ring (chunks * 1000 + rows per chunk), dy slots, and the
- * backward dynamic shared memory bytes.  UNSUPPORTED when the shape does not
- * fit.
+ * Launch plan of the multi-query kernels (no launch).  out[0..7]: forward
+ * CTAs * 1000 + backward CTAs, consumer warps (forward * 1000 + backward),
+ * 16-byte vectors per thread (forward * 1000 + backward), queries per
+ * register block (forward * 1000 + backward), forward ring (chunks * 1000 +
+ * rows per chunk), backward ring (chunks * 1000 + rows per chunk), dy slots,
+ * and the backward dynamic shared memory bytes.  UNSUPPORTED when the shape
+ * does not fit.
  */
 attnres_status attnres_multi_plan_info(const attnres_multi_params* p, int64_t out[8]);
 

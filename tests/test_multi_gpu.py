@@ -78,6 +78,7 @@ SHAPES = [
     (33, 41, 512, 256, 256, 3),      # more sources than lanes
     (1, 30, 1024, 512, 512, 4),      # one source
     (12, 161, 2048, 512, 1536, 8),   # M = 8
+    (16, 23, 4096, 1024, 3072, 3),   # forward: several softmax groups and two passes per token
 ]
 
 
@@ -136,12 +137,19 @@ def test_multi_empty_input():
     assert torch.count_nonzero(g["dq_f32"]).item() == 0 and g["dq"].shape == (2, 128)
 
 
-def test_multi_unsupported_shape_is_refused():
-    # 64 rows of 16 KB cannot stay resident in shared memory
-    v = torch.zeros((64, 4, 8192), dtype=torch.bfloat16, device="cuda")
-    Q = torch.zeros((16, 8192), dtype=torch.bfloat16, device="cuda")
+def test_multi_forward_streams_large_tokens_backward_refuses_them():
+    # 64 rows of 16 KB cannot stay resident in shared memory: the forward
+    # streams them (one pass per query, queries reloaded per pass), the
+    # backward refuses the shape before launching anything
+    wl = make_multi(64, 5, 8192, 8192, 16, key_offset=0, seed=77)
+    v, Q = wl.values.cuda(), wl.queries.cuda()
+    fwd = attnres_multi_fwd(v, Q, key_offset=0)
+    torch.cuda.synchronize()
+    attnres_check_device_error()
+    ref = attnres_multi_oracle(wl.values, wl.queries, key_offset=0)
+    _check(wl, fwd, None, ref, False, "S64 D8192 M16 forward")
     with pytest.raises(AttnresError) as e:
-        attnres_multi_fwd(v, Q)
+        attnres_multi_bwd(v, Q, wl.dy.cuda(), fwd, key_offset=0)
     assert e.value.name == "ATTNRES_ERR_UNSUPPORTED"
 
 
