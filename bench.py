@@ -1,19 +1,26 @@
 #!/usr/bin/env python3
 """Benchmark of the AttnRes read operator, forward + backward, on GB300.
 
-One step = attnres_fwd + attnres_bwd (every step of the hot path: key
-statistics, softmax routing, weighted read, output RMSNorm, dot pass,
-dvalues write, dq/dw_o partial sums and their finalize) over one batch of
-the long-sequence workload S=10 sources, N=32768 tokens, D=4096, bf16,
-output RMSNorm on (the shape of the first row of the benchmark table in
-"[Perf] Parallelize AttnRes long-sequence reduction", Test plan).
+Default workload (`--workload long`): one step = attnres_fwd + attnres_bwd
+(every step of the hot path: key statistics, softmax routing, weighted read,
+output RMSNorm, dot pass, dvalues write, dq/dw_o partial sums and their
+finalize) over one batch of the long-sequence workload S=10 sources,
+N=32768 tokens, D=4096, bf16, output RMSNorm on (the shape of the first row
+of the benchmark table in "[Perf] Parallelize AttnRes long-sequence
+reduction", Test plan).
+
+`--workload multi`: one step = attnres_multi_fwd + attnres_multi_bwd with
+M=2 queries of rank R=1024 over the same S=10, N=32768, D=4096 sources
+("Fast Attention Residuals", section "Multi-query AttnRes": two queries
+route two roles from one read).
 
 The metric is effective HBM bandwidth: the algorithmic bytes one step must
 move (sources read in the forward and again in the backward, dvalues
-written, y written, dy read, saved statistics and the FP32 partial sums)
-divided by the measured step time.
+written, outputs written, upstream gradients read, saved statistics and the
+FP32 partial sums) divided by the measured step time.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--workload long|multi]
 
 Prints ONE JSON line on rank 0.  With --gpus N > 1 run it under
 torch.distributed.run: every rank processes its own full batch (weak
@@ -40,6 +47,7 @@ METRIC = "AttnRes fwd+bwd ms and effective HBM GB/s (% of roofline), bf16, 1×GB
 WORKLOAD_CFG = 3
 FALLBACK_HBM_GBS = 6800.0
 PROFILE_TRAFFIC = os.path.join(ROOT, "profiles", "attnres_bwd_traffic.json")
+PROFILE_TRAFFIC_MULTI = os.path.join(ROOT, "profiles", "attnres_multi_bwd_traffic.json")
 
 
 # --------------------------------------------------------------------------
@@ -59,12 +67,30 @@ def algorithmic_bytes(S, N, D, R, out_norm, P):
     return {"fwd": fwd, "bwd": bwd, "total": fwd + bwd}
 
 
-def kernel_sources_hash():
+def multi_algorithmic_bytes(S, N, D, R, M, P):
+    """Multi-query read: the forward reads the sources once for all M
+    queries and writes M outputs plus alpha/logit [N, M, S] and rstd [N, S];
+    the backward reads the sources, the M upstream gradients and the
+    statistics, writes dvalues and moves the [P, M*R] FP32 partial sums."""
+    v = S * N * D * 2
+    out = M * N * D * 2
+    stats = (2 * M * S + S) * N * 4
+    fwd = v + out + stats
+    bwd = 2 * v + out + stats + 2 * P * M * R * 4
+    return {"fwd": fwd, "bwd": bwd, "total": fwd + bwd}
+
+
+SINGLE_SOURCES = ["attnres_api.cu", "attnres_bwd.cu", "attnres_fwd.cu", "device_utils.cuh", "kernels.cuh"]
+MULTI_SOURCES = ["attnres_api.cu", "attnres_bwd.cu", "attnres_multi_bwd.cu", "attnres_multi_fwd.cu",
+                 "device_utils.cuh", "kernels.cuh"]
+
+
+def kernel_sources_hash(names=None):
+    """Hash of the kernel sources a profile was captured from (the
+    single-query kernels and what they compile from, by default)."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "attention_residuals_gb300", "csrc")
-    # the single-query kernels and what they compile from
-    names = ["attnres_api.cu", "attnres_bwd.cu", "attnres_fwd.cu", "device_utils.cuh", "kernels.cuh"]
-    for name in names:
+    for name in (names or SINGLE_SOURCES):
         with open(os.path.join(csrc, name), "rb") as f:
             h.update(name.encode())
             h.update(f.read())
@@ -84,13 +110,13 @@ def read_peak():
     return FALLBACK_HBM_GBS, "fallback"
 
 
-def profiled_traffic(config_key):
+def profiled_traffic(config_key, path=PROFILE_TRAFFIC, names=None):
     """DRAM bytes per backward launch from the committed ncu summary, only if
     the kernel sources are unchanged since that capture."""
     try:
-        with open(PROFILE_TRAFFIC) as f:
+        with open(path) as f:
             doc = json.load(f)
-        if doc.get("sources_hash") == kernel_sources_hash() and doc.get("config") == config_key:
+        if doc.get("sources_hash") == kernel_sources_hash(names) and doc.get("config") == config_key:
             return doc.get("traffic_bytes_per_launch")
     except Exception:
         pass
@@ -173,50 +199,223 @@ def dist_env():
 
 
 # --------------------------------------------------------------------------
-# Reference arm: the FP64 oracle on the host cores
+# Workloads: what one step runs, its bytes, its end-to-end variant and its
+# oracle (the CPU baseline and the reference arm)
 # --------------------------------------------------------------------------
-def oracle_sample(sample_tokens, seed=0):
-    from attention_residuals_gb300.workloads import make_workload
-    return make_workload(WORKLOAD_CFG, N=sample_tokens, seed=WORKLOAD_CFG + 1000 * seed)
+class LongRead:
+    """Single-query read on the long-sequence workload (output RMSNorm on)."""
+    key = "long"
+    roofline_kernel = "attnres_bwd_kernel (+ finalize)"
 
+    def __init__(self, tokens=None, seed=0, device="cpu"):
+        from attention_residuals_gb300.workloads import make_workload
+        self.wl = make_workload(WORKLOAD_CFG, N=tokens, seed=WORKLOAD_CFG + 1000 * seed, device=device)
 
-def time_oracle(wl, repeats=1):
-    from oracle import attnres_oracle
-    cores = os.cpu_count() or 1
-    times = []
-    for _ in range(repeats):
+    def bytes_for(self, P):
+        wl = self.wl
+        return algorithmic_bytes(wl.S, wl.N, wl.D, wl.R, wl.out_norm, P)
+
+    def describe(self):
+        wl = self.wl
+        return (f"S={wl.S} N={wl.N} D={wl.D} R={wl.R} key_offset={wl.key_offset} out-norm bf16 "
+                f"(long-sequence)")
+
+    # ---------------------------------------------------------------- GPU
+    def prepare(self, dev):
+        import torch
+        from attention_residuals_gb300 import attnres_plan_info
+        wl = self.wl
+        S, N, D, R = wl.S, wl.N, wl.D, wl.R
+        self.info = attnres_plan_info(wl.values, R, key_offset=wl.key_offset, out_norm=wl.out_norm)
+        self.bytes = self.bytes_for(self.info["grid"])
+        f32 = dict(dtype=torch.float32, device=dev)
+        self.out = {"y": torch.empty((N, D), dtype=torch.bfloat16, device=dev),
+                    "alpha": torch.empty((N, S), **f32), "rstd": torch.empty((N, S), **f32),
+                    "logit": torch.empty((N, S), **f32), "o_rstd": torch.empty((N,), **f32)}
+        self.dv = torch.empty_like(wl.values)
+        self.ws = torch.empty((64 << 20,), dtype=torch.uint8, device=dev)
+        self.launches = 2 + (1 if self.info["bwd_split"] else 0)
+        self.f = None
+
+    def fwd(self, stream, values=None, q=None, w=None):
+        from attention_residuals_gb300 import attnres_fwd
+        wl = self.wl
+        self.f = attnres_fwd(wl.values if values is None else values, wl.q if q is None else q,
+                             w_o=wl.w_o if w is None else w, key_offset=wl.key_offset, out=self.out,
+                             stream=stream)
+        return self.f
+
+    def bwd(self, stream, values=None, q=None, w=None, dy=None):
+        from attention_residuals_gb300 import attnres_bwd
+        wl = self.wl
+        return attnres_bwd(wl.values if values is None else values, wl.q if q is None else q,
+                           wl.dy if dy is None else dy, self.f, w_o=wl.w_o if w is None else w,
+                           key_offset=wl.key_offset, workspace=self.ws, dvalues=self.dv, stream=stream)
+
+    def e2e(self, stream):
+        """A step through the same API from pinned host buffers: inputs copied
+        in, fwd + bwd, every output copied back."""
+        import torch
+        wl = self.wl
+        v, q, w, dy = wl.values, wl.q, wl.w_o, wl.dy
+        N, D, R = wl.N, wl.D, wl.R
+        h = {"v": torch.empty(v.shape, dtype=v.dtype, pin_memory=True), "q": q.cpu().pin_memory(),
+             "w": w.cpu().pin_memory(), "dy": torch.empty(dy.shape, dtype=dy.dtype, pin_memory=True),
+             "y": torch.empty((N, D), dtype=torch.bfloat16, pin_memory=True),
+             "dv": torch.empty(v.shape, dtype=v.dtype, pin_memory=True),
+             "dq": torch.empty((R,), dtype=torch.bfloat16, pin_memory=True),
+             "dw": torch.empty((D,), dtype=torch.bfloat16, pin_memory=True)}
+        h["v"].copy_(v)
+        h["dy"].copy_(dy)
+        d = {"v": torch.empty_like(v), "q": torch.empty_like(q), "w": torch.empty_like(w),
+             "dy": torch.empty_like(dy)}
+
+        def step():
+            for k in ("v", "q", "w", "dy"):
+                d[k].copy_(h[k], non_blocking=True)
+            self.fwd(stream, d["v"], d["q"], d["w"])
+            b = self.bwd(stream, d["v"], d["q"], d["w"], d["dy"])
+            h["y"].copy_(self.out["y"], non_blocking=True)
+            h["dv"].copy_(self.dv, non_blocking=True)
+            h["dq"].copy_(b["dq"], non_blocking=True)
+            h["dw"].copy_(b["dw_o"], non_blocking=True)
+
+        h2d = sum(h[k].numel() for k in ("v", "q", "w", "dy")) * 2
+        d2h = sum(h[k].numel() for k in ("y", "dv", "dq", "dw")) * 2
+        return step, h2d, d2h, h
+
+    def traffic(self):
+        return profiled_traffic("cfg3")
+
+    # ---------------------------------------------------------------- CPU
+    def oracle_seconds(self, cores):
+        from oracle import attnres_oracle
+        wl = self.wl
         t = time.perf_counter()
         attnres_oracle(wl.values, wl.q, w_o=wl.w_o, dy=wl.dy, key_offset=wl.key_offset,
                        nthreads=cores, want_dvalues=True)
-        times.append(time.perf_counter() - t)
-    return times, cores
+        return time.perf_counter() - t
 
 
+class MultiRead:
+    """Multi-query read: two rank-1024 queries over the long-sequence sources."""
+    key = "multi"
+    roofline_kernel = "attnres_multi_bwd_kernel (+ finalize)"
+
+    def __init__(self, tokens=None, seed=0, device="cpu"):
+        from attention_residuals_gb300.workloads import make_multi_workload
+        self.wl = make_multi_workload("long", N=tokens, seed=200 + 1000 * seed, device=device)
+
+    def bytes_for(self, P):
+        wl = self.wl
+        return multi_algorithmic_bytes(wl.S, wl.N, wl.D, wl.R, wl.M, P)
+
+    def describe(self):
+        wl = self.wl
+        return (f"multi-query M={wl.M} S={wl.S} N={wl.N} D={wl.D} R={wl.R} key_offset={wl.key_offset} "
+                f"bf16 (two queries over the long-sequence sources)")
+
+    # ---------------------------------------------------------------- GPU
+    def prepare(self, dev):
+        import torch
+        from attention_residuals_gb300 import attnres_multi_plan_info
+        wl = self.wl
+        self.info = attnres_multi_plan_info(wl.values, wl.M, wl.R, key_offset=wl.key_offset)
+        self.bytes = self.bytes_for(self.info["grid"] % 1000)
+        self.ws = torch.empty((64 << 20,), dtype=torch.uint8, device=dev)
+        self.launches = 3
+        self.f = None
+
+    def fwd(self, stream, values=None, queries=None):
+        from attention_residuals_gb300 import attnres_multi_fwd
+        wl = self.wl
+        self.f = attnres_multi_fwd(wl.values if values is None else values,
+                                   wl.queries if queries is None else queries,
+                                   key_offset=wl.key_offset, stream=stream)
+        return self.f
+
+    def bwd(self, stream, values=None, queries=None, dy=None):
+        from attention_residuals_gb300 import attnres_multi_bwd
+        wl = self.wl
+        return attnres_multi_bwd(wl.values if values is None else values,
+                                 wl.queries if queries is None else queries,
+                                 wl.dy if dy is None else dy, self.f, key_offset=wl.key_offset,
+                                 stream=stream, workspace=self.ws)
+
+    def e2e(self, stream):
+        import torch
+        wl = self.wl
+        v, Q, dy = wl.values, wl.queries, wl.dy
+        h = {"v": torch.empty(v.shape, dtype=v.dtype, pin_memory=True), "q": Q.cpu().pin_memory(),
+             "dy": torch.empty(dy.shape, dtype=dy.dtype, pin_memory=True),
+             "y": torch.empty(dy.shape, dtype=torch.bfloat16, pin_memory=True),
+             "dv": torch.empty(v.shape, dtype=v.dtype, pin_memory=True),
+             "dq": torch.empty(Q.shape, dtype=torch.bfloat16, pin_memory=True)}
+        h["v"].copy_(v)
+        h["dy"].copy_(dy)
+        d = {"v": torch.empty_like(v), "q": torch.empty_like(Q), "dy": torch.empty_like(dy)}
+
+        def step():
+            for k in ("v", "q", "dy"):
+                d[k].copy_(h[k], non_blocking=True)
+            f = self.fwd(stream, d["v"], d["q"])
+            b = self.bwd(stream, d["v"], d["q"], d["dy"])
+            h["y"].copy_(f["y"], non_blocking=True)
+            h["dv"].copy_(b["dvalues"], non_blocking=True)
+            h["dq"].copy_(b["dq"], non_blocking=True)
+
+        h2d = sum(h[k].numel() for k in ("v", "q", "dy")) * 2
+        d2h = sum(h[k].numel() for k in ("y", "dv", "dq")) * 2
+        return step, h2d, d2h, h
+
+    def traffic(self):
+        return profiled_traffic("multi-long", PROFILE_TRAFFIC_MULTI, MULTI_SOURCES)
+
+    # ---------------------------------------------------------------- CPU
+    def oracle_seconds(self, cores):
+        from oracle.multi import attnres_multi_oracle
+        wl = self.wl
+        t = time.perf_counter()
+        attnres_multi_oracle(wl.values, wl.queries, dy=wl.dy, key_offset=wl.key_offset,
+                             nthreads=cores, want_dvalues=True)
+        return time.perf_counter() - t
+
+
+WORKLOADS = {"long": LongRead, "multi": MultiRead}
+FULL_TOKENS = {"long": 32768, "multi": 32768}
+
+
+# --------------------------------------------------------------------------
+# Reference arm: the FP64 oracle on the host cores
+# --------------------------------------------------------------------------
 def run_reference(args):
     world, rank, _ = dist_env()
     if rank != 0:
         return 0
     from oracle import build_oracle
     build_oracle()
+    W = WORKLOADS[args.workload]
     sample = args.ref_tokens
-    wl = oracle_sample(sample)
-    b = algorithmic_bytes(wl.S, sample, wl.D, wl.R, wl.out_norm, 1)["total"]
-    small = oracle_sample(16)
+    wl = W(tokens=sample)
+    n_full = FULL_TOKENS[args.workload]
+    b = wl.bytes_for(1)["total"]
+    cores = os.cpu_count() or 1
+    small = W(tokens=16)
     for _ in range(args.warmup):  # untimed warm-up steps on a small sample
-        time_oracle(small, repeats=1)
-    times, cores = time_oracle(wl, repeats=max(1, args.steps))
+        small.oracle_seconds(cores)
+    times = [wl.oracle_seconds(cores) for _ in range(max(1, args.steps))]
     t = sum(times) / len(times)
     gbs = b / t / 1e9
     line = {
         "metric": METRIC, "value": gbs, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
-        "warmup": args.warmup, "ms_per_step": t * 1e3 * (32768 / sample),
+        "warmup": args.warmup, "ms_per_step": t * 1e3 * (n_full / sample),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic", "impl": "reference",
-        "config": {"workload": "S=10 N=32768 D=4096 R=4096 out-norm (long-sequence)",
+        "config": {"workload": wl.describe().replace(f"N={sample}", f"N={n_full}"),
                    "sample_tokens": sample},
         "cpu_baseline": {"value": gbs, "unit": "GB/s", "cores": cores, "kind": "oracle",
-                         "sample": f"{sample} of 32768 tokens per step, fwd+bwd in FP64; "
-                                   "ms_per_step scaled to the full 32768 tokens"},
+                         "sample": f"{sample} of {n_full} tokens per step, fwd+bwd in FP64; "
+                                   f"ms_per_step scaled to the full {n_full} tokens"},
         "e2e": {"value": gbs, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
@@ -241,40 +440,24 @@ def run_ours(args):
         dist.init_process_group("nccl", device_id=dev)
         pg = dist
 
-    from attention_residuals_gb300 import _lib, attnres_bwd, attnres_fwd, attnres_plan_info
+    from attention_residuals_gb300 import _lib
     from attention_residuals_gb300.build import build
     from attention_residuals_gb300.dist import max_over_ranks, weak_scaling_throughput
-    from attention_residuals_gb300.workloads import make_workload
     build()
     _lib.load()
+    W = WORKLOADS[args.workload]
 
     # CPU baseline sample is generated before any GPU work (rank 0, N=1 only).
-    cpu_wl = oracle_sample(args.cpu_tokens) if (rank == 0 and world == 1 and not args.no_cpu) else None
+    cpu_wl = W(tokens=args.cpu_tokens) if (rank == 0 and world == 1 and not args.no_cpu) else None
 
-    wl = make_workload(WORKLOAD_CFG, N=args.tokens, seed=WORKLOAD_CFG + 1000 * rank, device=str(dev))
-    S, N, D, R = wl.S, wl.N, wl.D, wl.R
-    v, q, w, dy = wl.values, wl.q, wl.w_o, wl.dy
-    info = attnres_plan_info(v, R, key_offset=wl.key_offset, out_norm=wl.out_norm)
-    P = info["grid"]
-    nbytes = algorithmic_bytes(S, N, D, R, wl.out_norm, P)
-
-    # Preallocated outputs and workspace: the timed step allocates nothing.
-    f32 = dict(dtype=torch.float32, device=dev)
-    out = {"y": torch.empty((N, D), dtype=torch.bfloat16, device=dev),
-           "alpha": torch.empty((N, S), **f32), "rstd": torch.empty((N, S), **f32),
-           "logit": torch.empty((N, S), **f32), "o_rstd": torch.empty((N,), **f32)}
-    dv = torch.empty_like(v)
-    ws = torch.empty((64 << 20,), dtype=torch.uint8, device=dev)
+    work = W(tokens=args.tokens, seed=rank, device=str(dev))
+    work.prepare(dev)
+    nbytes = work.bytes
     stream = torch.cuda.current_stream(dev)
 
-    def step():
-        f = attnres_fwd(v, q, w_o=w, key_offset=wl.key_offset, out=out, stream=stream)
-        b = attnres_bwd(v, q, dy, f, w_o=w, key_offset=wl.key_offset, workspace=ws, dvalues=dv,
-                        stream=stream)
-        return f, b
-
     for _ in range(max(3, args.warmup)):
-        step()
+        work.fwd(stream)
+        work.bwd(stream)
     torch.cuda.synchronize()
 
     K = args.steps
@@ -291,10 +474,9 @@ def run_ours(args):
     e_start.record(stream)
     for k in range(K):
         ev[k][0].record(stream)
-        f = attnres_fwd(v, q, w_o=w, key_offset=wl.key_offset, out=out, stream=stream)
+        work.fwd(stream)
         ev[k][1].record(stream)
-        attnres_bwd(v, q, dy, f, w_o=w, key_offset=wl.key_offset, workspace=ws, dvalues=dv,
-                    stream=stream)
+        work.bwd(stream)
         ev[k][2].record(stream)
     e_end.record(stream)
     torch.cuda.synchronize()
@@ -329,35 +511,7 @@ def run_ours(args):
     # ---------------------------------------------------------- end to end
     e2e = None
     if not args.no_e2e:
-        hv = torch.empty(v.shape, dtype=v.dtype, pin_memory=True)
-        hv.copy_(v)
-        hq = q.cpu().pin_memory()
-        hw = w.cpu().pin_memory()
-        hdy = torch.empty(dy.shape, dtype=dy.dtype, pin_memory=True)
-        hdy.copy_(dy)
-        hy = torch.empty((N, D), dtype=torch.bfloat16, pin_memory=True)
-        hdv = torch.empty(v.shape, dtype=v.dtype, pin_memory=True)
-        hdq = torch.empty((R,), dtype=torch.bfloat16, pin_memory=True)
-        hdw = torch.empty((D,), dtype=torch.bfloat16, pin_memory=True)
-        dv_in = torch.empty_like(v)
-        dq_in = torch.empty_like(q)
-        dw_in = torch.empty_like(w)
-        ddy = torch.empty_like(dy)
-
-        def e2e_step():
-            dv_in.copy_(hv, non_blocking=True)
-            dq_in.copy_(hq, non_blocking=True)
-            dw_in.copy_(hw, non_blocking=True)
-            ddy.copy_(hdy, non_blocking=True)
-            f = attnres_fwd(dv_in, dq_in, w_o=dw_in, key_offset=wl.key_offset, out=out,
-                            stream=stream)
-            b = attnres_bwd(dv_in, dq_in, ddy, f, w_o=dw_in, key_offset=wl.key_offset,
-                            workspace=ws, dvalues=dv, stream=stream)
-            hy.copy_(out["y"], non_blocking=True)
-            hdv.copy_(dv, non_blocking=True)
-            hdq.copy_(b["dq"], non_blocking=True)
-            hdw.copy_(b["dw_o"], non_blocking=True)
-
+        e2e_step, h2d, d2h, host = work.e2e(stream)
         e2e_step()
         torch.cuda.synchronize()
         KE = max(1, min(args.e2e_steps, K))
@@ -374,20 +528,19 @@ def run_ours(args):
         e2e_ms = s0.elapsed_time(s1) / KE
         if pg is not None:
             e2e_ms = max_over_ranks([e2e_ms], device=dev)[0]
-        h2d = (hv.numel() + hq.numel() + hw.numel() + hdy.numel()) * 2
-        d2h = (hy.numel() + hdv.numel() + hdq.numel() + hdw.numel()) * 2
         e2e = {"value": weak_scaling_throughput(nbytes["total"], world, e2e_ms), "unit": "GB/s",
                "ms_per_step": e2e_ms, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
-        del hv, hdv
+        del host
 
     # ---------------------------------------------------------- CPU baseline
     cpu = None
     if cpu_wl is not None:
-        times, cores = time_oracle(cpu_wl, repeats=1)
-        cb = algorithmic_bytes(S, args.cpu_tokens, D, R, wl.out_norm, 1)["total"]
-        cpu = {"value": cb / times[0] / 1e9, "unit": "GB/s", "cores": cores, "kind": "oracle",
-               "sample": f"{args.cpu_tokens} of {N} tokens of the same workload, fwd+bwd in "
-                         f"FP64 ({times[0]:.1f} s)"}
+        cores = os.cpu_count() or 1
+        secs = cpu_wl.oracle_seconds(cores)
+        cb = cpu_wl.bytes_for(1)["total"]
+        cpu = {"value": cb / secs / 1e9, "unit": "GB/s", "cores": cores, "kind": "oracle",
+               "sample": f"{args.cpu_tokens} of {work.wl.N} tokens of the same workload, fwd+bwd in "
+                         f"FP64 ({secs:.1f} s)"}
 
     if rank != 0:
         if pg is not None:
@@ -397,7 +550,6 @@ def run_ours(args):
     peak, peak_kind = read_peak()
     achieved = nbytes["bwd"] / (bwd_ms * 1e-3) / 1e9
     value = weak_scaling_throughput(nbytes["total"], world, ms_step)
-    launches_per_step = 2 + (1 if info["bwd_split"] else 0)
     line = {
         "metric": METRIC,
         "value": value,
@@ -411,21 +563,20 @@ def run_ours(args):
         "vs_baseline": None,
         "dtype": "bf16",
         "data": "synthetic",
-        "config": {"workload": f"S={S} N={N} D={D} R={R} key_offset={wl.key_offset} out-norm bf16 "
-                               f"(long-sequence, {'split-N' if info['bwd_split'] else 'in-kernel'} reduction)",
+        "config": {"workload": work.describe(),
                    "bytes_per_step": nbytes["total"],
                    "fwd_ms": fwd_ms, "bwd_ms": bwd_ms,
                    "frac_of_peak_step": value / world / peak,
                    "device_copy_gbs": copy_gbs,
                    "l2": "inputs larger than L2 (2.7 GB of sources per step); no flush",
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
-                   "plan": info},
-        "roofline": {"bound": "hbm", "kernel": "attnres_bwd_kernel (+ finalize)",
+                   "plan": work.info},
+        "roofline": {"bound": "hbm", "kernel": work.roofline_kernel,
                      "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "peak_kind": f"{peak_kind} HBM copy bandwidth",
-                     "traffic": profiled_traffic("cfg3")},
+                     "traffic": work.traffic()},
         "clocks": clocks,
-        "gpu_launches": launches_per_step * K,
+        "gpu_launches": work.launches * K,
         "e2e": e2e,
         "cpu_baseline": cpu,
     }
@@ -441,6 +592,7 @@ def main(argv=None):
     ap.add_argument("--steps", type=int, default=300)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", choices=sorted(WORKLOADS), default="long")
     ap.add_argument("--e2e-steps", type=int, default=5)
     ap.add_argument("--cpu-tokens", type=int, default=8192)
     ap.add_argument("--ref-tokens", type=int, default=1024)

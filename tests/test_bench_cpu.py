@@ -1,0 +1,49 @@
+"""CPU checks of the benchmark's byte models and its reference arm (the FP64
+oracle timed on the host cores), for both workloads."""
+import json
+import subprocess
+import sys
+import os
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+sys.path.insert(0, ROOT)
+
+import bench  # noqa: E402
+
+
+def test_single_byte_model():
+    b = bench.algorithmic_bytes(S=10, N=32768, D=4096, R=4096, out_norm=True, P=152)
+    v = 10 * 32768 * 4096 * 2
+    row = 32768 * 4096 * 2
+    stats = 3 * 32768 * 10 * 4 + 32768 * 4
+    assert b["fwd"] == v + row + stats
+    assert b["bwd"] == 2 * v + row + stats + 2 * 152 * (4096 + 4096) * 4
+    assert b["total"] == b["fwd"] + b["bwd"]
+
+
+def test_multi_byte_model():
+    b = bench.multi_algorithmic_bytes(S=10, N=32768, D=4096, R=1024, M=2, P=152)
+    v = 10 * 32768 * 4096 * 2
+    out = 2 * 32768 * 4096 * 2
+    stats = (2 * 2 * 10 + 10) * 32768 * 4
+    assert b["fwd"] == v + out + stats
+    assert b["bwd"] == 2 * v + out + stats + 2 * 152 * 2 * 1024 * 4
+
+
+@pytest.mark.parametrize("workload", ["long", "multi"])
+def test_reference_arm_prints_one_json_line(workload):
+    r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference",
+                        "--workload", workload, "--steps", "1", "--warmup", "3", "--ref-tokens", "16"],
+                       capture_output=True, text=True, timeout=600, cwd=ROOT)
+    assert r.returncode == 0, r.stderr
+    lines = [ln for ln in r.stdout.splitlines() if ln.strip()]
+    assert len(lines) == 1
+    d = json.loads(lines[0])
+    for k in ("metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step",
+              "higher_is_better", "impl", "cpu_baseline", "e2e", "config"):
+        assert k in d, k
+    assert d["impl"] == "reference" and d["value"] > 0
+    assert d["e2e"]["h2d_bytes_per_step"] == 0
+    assert d["cpu_baseline"]["kind"] == "oracle"
