@@ -6,3 +6,4 @@ this package.  It shares no code with the CUDA library.  See
 """
 from .oracle import attnres_oracle, build_oracle, oracle_library_path  # noqa: F401
 from .multi import attnres_multi_oracle, attnres_selected_oracle  # noqa: F401,E402
+from .partial import attnres_partial_oracle  # noqa: F401,E402
