@@ -16,4 +16,7 @@ from .ops import (  # noqa: F401
     attnres_multi_fwd,
     attnres_multi_plan_info,
     attnres_plan_info,
+    attnres_selected,
+    attnres_selected_bwd,
+    attnres_selected_fwd,
 )

@@ -37,6 +37,11 @@ EXPORTED = [
     "attnres_multi_bwd",
     "attnres_multi_bwd_workspace_bytes",
     "attnres_multi_plan_info",
+    "attnres_selected_fwd",
+    "attnres_selected_bwd",
+    "attnres_selected_bwd_workspace_bytes",
+    "attnres_fwd_partial",
+    "attnres_bwd_partial",
 ]
 
 
@@ -122,6 +127,19 @@ def load(path: str | None = None):
                                           vp, fp, vp, sz, vp]
         lib.attnres_multi_plan_info.restype = ctypes.c_int
         lib.attnres_multi_plan_info.argtypes = [MP, ctypes.POINTER(ctypes.c_int64)]
+        lib.attnres_fwd_partial.restype = ctypes.c_int
+        lib.attnres_fwd_partial.argtypes = [P, vp, vp, vp, i64, vp, i64, vp, fp, fp, fp, fp, vp, vp]
+        lib.attnres_bwd_partial.restype = ctypes.c_int
+        lib.attnres_bwd_partial.argtypes = [P, vp, vp, vp, fp, fp, fp, fp, vp, vp, i64,
+                                            ctypes.POINTER(ctypes.c_void_p), i64, vp, fp, vp, fp, vp, sz, vp]
+        i32 = ctypes.c_int32
+        lib.attnres_selected_fwd.restype = ctypes.c_int
+        lib.attnres_selected_fwd.argtypes = [MP, vp, i32, vp, vp, fp, fp, fp, vp]
+        lib.attnres_selected_bwd_workspace_bytes.restype = sz
+        lib.attnres_selected_bwd_workspace_bytes.argtypes = [MP, i32]
+        lib.attnres_selected_bwd.restype = ctypes.c_int
+        lib.attnres_selected_bwd.argtypes = [MP, vp, i32, vp, vp, fp, fp, fp, ctypes.POINTER(ctypes.c_void_p),
+                                             i64, vp, fp, vp, sz, vp]
         _lib = lib
         return lib
 

@@ -63,7 +63,8 @@ attnres_status check_shape(const attnres_params* p) {
     return ATTNRES_OK;
 }
 
-attnres_status make_plan(const attnres_params* p, Plan* plan) {
+// fused: the forward also streams one added row per token (block-partial sum).
+attnres_status make_plan(const attnres_params* p, Plan* plan, bool fused = false) {
     DeviceInfo dev;
     if (!device_info(&dev)) return ATTNRES_ERR_CUDA;
     Plan pl{};
@@ -95,10 +96,11 @@ attnres_status make_plan(const attnres_params* p, Plan* plan) {
         const int per_sm = fwd_ctas_per_sm(pl.vpt);
         const long long budget = per_sm > 1 ? (optin / per_sm - 1024) : optin;
         auto ffits = [&](int chunks, int rows) {
-            return make_layout(chunks, rows, pl.slot_bytes, 0, pl.s_pad, false).total <=
+            return make_layout(chunks, rows, pl.slot_bytes, fused ? kDeltaSlots : 0, pl.s_pad, false).total <=
                    static_cast<uint32_t>(budget);
         };
-        const long long fixed = make_layout(0, 1, pl.slot_bytes, 0, pl.s_pad, false).total + 64;
+        const long long fixed =
+            make_layout(0, 1, pl.slot_bytes, fused ? kDeltaSlots : 0, pl.s_pad, false).total + 64;
         long long gmax = (budget - fixed) / (2 * sb);
         if (gmax > kMaxGroup) gmax = kMaxGroup;
         if (gmax < 1) gmax = 1;
@@ -138,7 +140,7 @@ attnres_status make_plan(const attnres_params* p, Plan* plan) {
         if (pl.resident && pl.b_chunks < per_token + 1) pl.resident = 0;
         if (!pl.resident && pl.b_chunks < 2) return ATTNRES_ERR_UNSUPPORTED;
     }
-    pl.smem_fwd = make_layout(pl.f_chunks, pl.f_rows, pl.slot_bytes, 0, pl.s_pad, false).total;
+    pl.smem_fwd = make_layout(pl.f_chunks, pl.f_rows, pl.slot_bytes, fused ? kDeltaSlots : 0, pl.s_pad, false).total;
     pl.smem_bwd = make_layout(pl.b_chunks, pl.b_rows, pl.slot_bytes, pl.dy_slots, pl.s_pad, true).total;
     const int thr = p->split_n_threshold > 0 ? p->split_n_threshold : ATTNRES_DEFAULT_SPLIT_N;
     pl.split = p->N >= thr ? 1 : 0;
@@ -222,7 +224,8 @@ bool pick_ring(int S, F&& fits, int* rows, int* chunks) {
     return false;
 }
 
-attnres_status make_multi_plan(const attnres_multi_params* p, MultiPlan* plan) {
+// E > 0: per-token queries selected from an [E, R] bank (dq rows are bank rows).
+attnres_status make_multi_plan(const attnres_multi_params* p, MultiPlan* plan, int E = 0) {
     DeviceInfo dev;
     if (!device_info(&dev)) return ATTNRES_ERR_CUDA;
     const attnres_params& b = p->base;
@@ -287,7 +290,10 @@ attnres_status make_multi_plan(const attnres_multi_params* p, MultiPlan* plan) {
     pl.b_ncw = (ncv + 32 * pl.b_vpt - 1) / (32 * pl.b_vpt);
     pl.mb_b = p2 < 2 / pl.b_vpt ? p2 : 2 / pl.b_vpt;
     const int nmb = (M + pl.mb_b - 1) / pl.mb_b;
-    const int dq_nkv = nmb > 1 ? pl.nkv : 0;
+    const bool regblock = nmb == 1 && E == 0;
+    const int dq_nkv = regblock ? 0 : pl.nkv;
+    const int dq_rows = E > 0 ? E : M;
+    pl.E = E;
     pl.bwd_ok = 0;
     int bcps = 1;
     for (int cps = kMultiMaxCtasPerSm; cps >= 1 && !pl.bwd_ok; --cps) {
@@ -295,13 +301,13 @@ attnres_status make_multi_plan(const attnres_multi_params* p, MultiPlan* plan) {
         const uint32_t budget = cps > 1 ? optin / cps - 1024 : optin;
         for (int ds = 2; ds >= 1 && !pl.bwd_ok; --ds) {
             auto bfits = [&](int K, int G) {
-                return make_multi_layout(K, G, pl.slot_bytes, M, ds, pl.s_pad, pl.m_pad, pl.nkv, dq_nkv, true)
-                           .total <= budget;
+                return make_multi_layout(K, G, pl.slot_bytes, M, ds, pl.s_pad, pl.m_pad, pl.nkv, dq_nkv, true,
+                                         dq_rows).total <= budget;
             };
             if (!pick_ring(b.S, bfits, &pl.b_rows, &pl.b_chunks)) continue;
             pl.dy_slots = ds;
             pl.smem_bwd = make_multi_layout(pl.b_chunks, pl.b_rows, pl.slot_bytes, M, ds, pl.s_pad, pl.m_pad,
-                                            pl.nkv, dq_nkv, true).total;
+                                            pl.nkv, dq_nkv, true, dq_rows).total;
             if (cps > 1 && multi_bwd_occupancy(pl) < cps) continue;
             pl.bwd_ok = 1;
             bcps = cps;
@@ -310,7 +316,7 @@ attnres_status make_multi_plan(const attnres_multi_params* p, MultiPlan* plan) {
     long long grid = static_cast<long long>(bcps) * dev.sm_count;
     if (b.N < grid) grid = b.N;
     pl.grid = static_cast<int>(grid < 1 ? 1 : grid);
-    pl.ws_bytes = b.N == 0 ? 0 : static_cast<size_t>(pl.grid) * M * b.R * 4;
+    pl.ws_bytes = b.N == 0 ? 0 : static_cast<size_t>(pl.grid) * dq_rows * b.R * 4;
     *plan = pl;
     return ATTNRES_OK;
 }
@@ -330,7 +336,7 @@ const char* attnres_status_string(attnres_status s) {
         case ATTNRES_ERR_UNSUPPORTED: return "unsupported configuration for this build";
         case ATTNRES_ERR_WORKSPACE: return "workspace missing or too small";
         case ATTNRES_ERR_CUDA: return "CUDA runtime error";
-        case ATTNRES_ERR_DEVICE: return "a kernel gave up waiting on a shared-memory barrier";
+        case ATTNRES_ERR_DEVICE: return "a kernel reported an error (a failed barrier wait or an out-of-range query id)";
         default: return "unknown status";
     }
 }
@@ -353,12 +359,18 @@ attnres_status attnres_plan_info(const attnres_params* p, int64_t out[8]) {
     return ATTNRES_OK;
 }
 
-attnres_status attnres_fwd(const attnres_params* p, const void* q, const void* w_o, void* y,
-                           float* alpha, float* rstd, float* logit, float* o_rstd, float* o_pre,
-                           void* stream) {
+static attnres_status fwd_impl(const attnres_params* p, const void* q, const void* w_o, const void* delta,
+                               int64_t delta_ld, void* partial_out, int64_t partial_ld, void* y, float* alpha,
+                               float* rstd, float* logit, float* o_rstd, float* o_pre, void* stream) {
     attnres_status st = check_shape(p);
     if (st != ATTNRES_OK) return st;
+    if (delta) {
+        if (!partial_out) return ATTNRES_ERR_INVALID_ARG;
+        if (delta_ld < p->D || partial_ld < p->D) return ATTNRES_ERR_INVALID_ARG;
+        if (delta_ld % 8 != 0 || partial_ld % 8 != 0) return ATTNRES_ERR_ALIGNMENT;
+    }
     if (p->N == 0) return ATTNRES_OK;
+    if (delta && (!aligned16(delta) || !aligned16(partial_out))) return ATTNRES_ERR_ALIGNMENT;
     if (!q || !y || !alpha || !rstd || !logit) return ATTNRES_ERR_INVALID_ARG;
     if (p->out_norm && (!w_o || !o_rstd)) return ATTNRES_ERR_INVALID_ARG;
     if (!p->out_norm && o_pre) return ATTNRES_ERR_INVALID_ARG;
@@ -369,7 +381,7 @@ attnres_status attnres_fwd(const attnres_params* p, const void* q, const void* w
     if ((reinterpret_cast<uintptr_t>(q) & 1u) || (w_o && (reinterpret_cast<uintptr_t>(w_o) & 1u)))
         return ATTNRES_ERR_ALIGNMENT;
     Plan pl;
-    st = make_plan(p, &pl);
+    st = make_plan(p, &pl, delta != nullptr);
     if (st != ATTNRES_OK) return st;
     FwdArgs a;
     std::memset(&a, 0, sizeof a);
@@ -397,8 +409,28 @@ attnres_status attnres_fwd(const attnres_params* p, const void* q, const void* w
     a.logit = logit;
     a.o_rstd = o_rstd;
     a.o_pre = p->out_norm ? o_pre : nullptr;
+    a.delta = static_cast<const uint16_t*>(delta);
+    a.delta_ld = delta_ld;
+    a.partial_out = static_cast<uint16_t*>(partial_out);
+    a.partial_ld = partial_ld;
     return launch_fwd(pl, a, static_cast<cudaStream_t>(stream)) == cudaSuccess ? ATTNRES_OK
                                                                               : ATTNRES_ERR_CUDA;
+}
+
+attnres_status attnres_fwd(const attnres_params* p, const void* q, const void* w_o, void* y,
+                           float* alpha, float* rstd, float* logit, float* o_rstd, float* o_pre,
+                           void* stream) {
+    return fwd_impl(p, q, w_o, nullptr, 0, nullptr, 0, y, alpha, rstd, logit, o_rstd, o_pre, stream);
+}
+
+attnres_status attnres_fwd_partial(const attnres_params* p, const void* q, const void* w_o,
+                                   const void* delta, int64_t delta_ld, void* partial_out,
+                                   int64_t partial_ld, void* y, float* alpha, float* rstd,
+                                   float* logit, float* o_rstd, float* o_pre, void* stream) {
+    if (!delta && p && p->N > 0) return ATTNRES_ERR_INVALID_ARG;
+    if (!delta) return check_shape(p);
+    return fwd_impl(p, q, w_o, delta, delta_ld, partial_out, partial_ld, y, alpha, rstd, logit, o_rstd, o_pre,
+                    stream);
 }
 
 size_t attnres_bwd_workspace_bytes(const attnres_params* p) {
@@ -408,12 +440,14 @@ size_t attnres_bwd_workspace_bytes(const attnres_params* p) {
     return pl.ws_bytes;
 }
 
-attnres_status attnres_bwd(const attnres_params* p, const void* q, const void* w_o, const void* dy,
-                           const float* alpha, const float* rstd, const float* logit,
-                           const float* o_rstd, const float* o_pre, void* const* dsrc,
-                           int64_t dsrc_ld, void* dq, float* dq_f32, void* dw_o, float* dw_o_f32,
-                           void* workspace, size_t workspace_bytes, void* stream) {
+static attnres_status bwd_impl(const attnres_params* p, const void* q, const void* w_o, const void* dy,
+                               const float* alpha, const float* rstd, const float* logit,
+                               const float* o_rstd, const float* o_pre, const void* g_last, int64_t g_ld,
+                               void* const* dsrc, int64_t dsrc_ld, void* dq, float* dq_f32, void* dw_o,
+                               float* dw_o_f32, void* workspace, size_t workspace_bytes, void* stream) {
     attnres_status st = check_shape(p);
+    if (g_last && (g_ld < p->D)) return ATTNRES_ERR_INVALID_ARG;
+    if (g_last && (g_ld % 8 != 0 || !aligned16(g_last))) return ATTNRES_ERR_ALIGNMENT;
     if (st != ATTNRES_OK) return st;
     if (p->N == 0) {
         // Empty sums: dq and dw_o are zero; nothing else is touched.
@@ -497,12 +531,33 @@ attnres_status attnres_bwd(const attnres_params* p, const void* q, const void* w
     a.dq_f32 = dq_f32;
     a.dw_o = static_cast<uint16_t*>(dw_o);
     a.dw_o_f32 = dw_o_f32;
+    a.dlast_add = static_cast<const uint16_t*>(g_last);
+    a.dlast_add_ld = g_ld;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     if (!pl.split) {
         if (cudaMemsetAsync(a.tickets, 0, static_cast<size_t>(pl.ngroups + 1) * 4, s) != cudaSuccess)
             return ATTNRES_ERR_CUDA;
     }
     return launch_bwd(pl, a, s) == cudaSuccess ? ATTNRES_OK : ATTNRES_ERR_CUDA;
+}
+
+attnres_status attnres_bwd(const attnres_params* p, const void* q, const void* w_o, const void* dy,
+                           const float* alpha, const float* rstd, const float* logit,
+                           const float* o_rstd, const float* o_pre, void* const* dsrc,
+                           int64_t dsrc_ld, void* dq, float* dq_f32, void* dw_o, float* dw_o_f32,
+                           void* workspace, size_t workspace_bytes, void* stream) {
+    return bwd_impl(p, q, w_o, dy, alpha, rstd, logit, o_rstd, o_pre, nullptr, 0, dsrc, dsrc_ld, dq, dq_f32,
+                    dw_o, dw_o_f32, workspace, workspace_bytes, stream);
+}
+
+attnres_status attnres_bwd_partial(const attnres_params* p, const void* q, const void* w_o, const void* dy,
+                                   const float* alpha, const float* rstd, const float* logit,
+                                   const float* o_rstd, const float* o_pre, const void* g_partial,
+                                   int64_t g_ld, void* const* dsrc, int64_t dsrc_ld, void* dq,
+                                   float* dq_f32, void* dw_o, float* dw_o_f32, void* workspace,
+                                   size_t workspace_bytes, void* stream) {
+    return bwd_impl(p, q, w_o, dy, alpha, rstd, logit, o_rstd, o_pre, g_partial, g_ld, dsrc, dsrc_ld, dq,
+                    dq_f32, dw_o, dw_o_f32, workspace, workspace_bytes, stream);
 }
 
 // ---------------------------------------------------------------------------
@@ -576,18 +631,20 @@ attnres_status attnres_multi_plan_info(const attnres_multi_params* p, int64_t ou
     return ATTNRES_OK;
 }
 
-attnres_status attnres_multi_fwd(const attnres_multi_params* p, const void* q, void* y, float* alpha,
-                                 float* rstd, float* logit, void* stream) {
+static attnres_status multi_fwd_impl(const attnres_multi_params* p, const void* q, int E, const int64_t* ids,
+                                     void* y, float* alpha, float* rstd, float* logit, void* stream) {
     attnres_status st = check_multi(p);
     if (st != ATTNRES_OK) return st;
     const attnres_params& b = p->base;
+    if (ids && E < 1) return ATTNRES_ERR_INVALID_ARG;
     if (b.N == 0) return ATTNRES_OK;
     if (!q || !y || !alpha || !rstd || !logit) return ATTNRES_ERR_INVALID_ARG;
+    if (ids && (reinterpret_cast<uintptr_t>(ids) & 7u)) return ATTNRES_ERR_ALIGNMENT;
     if (!aligned16(y) || !aligned4(alpha) || !aligned4(rstd) || !aligned4(logit) ||
         (reinterpret_cast<uintptr_t>(q) & 1u))
         return ATTNRES_ERR_ALIGNMENT;
     MultiPlan pl;
-    st = make_multi_plan(p, &pl);
+    st = make_multi_plan(p, &pl, ids ? E : 0);
     if (st != ATTNRES_OK) return st;
     MultiFwdArgs a;
     std::memset(&a, 0, sizeof a);
@@ -613,6 +670,8 @@ attnres_status attnres_multi_fwd(const attnres_multi_params* p, const void* q, v
     a.kv0 = pl.kv0;
     a.nkv = pl.nkv;
     a.q = static_cast<const uint16_t*>(q);
+    a.ids = reinterpret_cast<const long long*>(ids);
+    a.E = ids ? E : 0;
     a.y = static_cast<uint16_t*>(y);
     a.alpha = alpha;
     a.rstd = rstd;
@@ -621,22 +680,41 @@ attnres_status attnres_multi_fwd(const attnres_multi_params* p, const void* q, v
                                                                                     : ATTNRES_ERR_CUDA;
 }
 
-size_t attnres_multi_bwd_workspace_bytes(const attnres_multi_params* p) {
+attnres_status attnres_multi_fwd(const attnres_multi_params* p, const void* q, void* y, float* alpha,
+                                 float* rstd, float* logit, void* stream) {
+    return multi_fwd_impl(p, q, 0, nullptr, y, alpha, rstd, logit, stream);
+}
+
+attnres_status attnres_selected_fwd(const attnres_multi_params* p, const void* bank, int32_t E,
+                                    const int64_t* ids, void* y, float* alpha, float* rstd, float* logit,
+                                    void* stream) {
+    if (E < 1 || (p && p->base.N > 0 && !ids)) return ATTNRES_ERR_INVALID_ARG;
+    return multi_fwd_impl(p, bank, E, ids, y, alpha, rstd, logit, stream);
+}
+
+static size_t multi_ws_impl(const attnres_multi_params* p, int E) {
     if (check_multi(p) != ATTNRES_OK) return 0;
     MultiPlan pl;
-    if (make_multi_plan(p, &pl) != ATTNRES_OK) return 0;
+    if (make_multi_plan(p, &pl, E) != ATTNRES_OK) return 0;
     return pl.ws_bytes;
 }
 
-attnres_status attnres_multi_bwd(const attnres_multi_params* p, const void* q, const void* dy,
-                                 const float* alpha, const float* rstd, const float* logit,
-                                 void* const* dsrc, int64_t dsrc_ld, void* dq, float* dq_f32,
-                                 void* workspace, size_t workspace_bytes, void* stream) {
+size_t attnres_multi_bwd_workspace_bytes(const attnres_multi_params* p) { return multi_ws_impl(p, 0); }
+
+size_t attnres_selected_bwd_workspace_bytes(const attnres_multi_params* p, int32_t E) {
+    return E < 1 ? 0 : multi_ws_impl(p, E);
+}
+
+static attnres_status multi_bwd_impl(const attnres_multi_params* p, const void* q, int E, const int64_t* ids,
+                                     const void* dy, const float* alpha, const float* rstd, const float* logit,
+                                     void* const* dsrc, int64_t dsrc_ld, void* dq, float* dq_f32,
+                                     void* workspace, size_t workspace_bytes, void* stream) {
     attnres_status st = check_multi(p);
     if (st != ATTNRES_OK) return st;
     const attnres_params& b = p->base;
     cudaStream_t s0 = static_cast<cudaStream_t>(stream);
-    const size_t nq = static_cast<size_t>(p->M) * static_cast<size_t>(b.R);
+    const size_t nq = static_cast<size_t>(ids ? E : p->M) * static_cast<size_t>(b.R);
+    if (ids && (reinterpret_cast<uintptr_t>(ids) & 7u)) return ATTNRES_ERR_ALIGNMENT;
     if (!dq) return ATTNRES_ERR_INVALID_ARG;
     if ((reinterpret_cast<uintptr_t>(dq) & 1u) || (dq_f32 && !aligned4(dq_f32))) return ATTNRES_ERR_ALIGNMENT;
     if (b.N == 0) {
@@ -652,7 +730,7 @@ attnres_status attnres_multi_bwd(const attnres_multi_params* p, const void* q, c
     st = check_dsrc(&b, dsrc, dsrc_ld);
     if (st != ATTNRES_OK) return st;
     MultiPlan pl;
-    st = make_multi_plan(p, &pl);
+    st = make_multi_plan(p, &pl, ids ? E : 0);
     if (st != ATTNRES_OK) return st;
     if (!pl.bwd_ok) return ATTNRES_ERR_UNSUPPORTED;
     if (!workspace || workspace_bytes < pl.ws_bytes) return ATTNRES_ERR_WORKSPACE;
@@ -692,7 +770,38 @@ attnres_status attnres_multi_bwd(const attnres_multi_params* p, const void* q, c
     a.part = static_cast<float*>(workspace);
     a.dq = static_cast<uint16_t*>(dq);
     a.dq_f32 = dq_f32;
+    a.ids = reinterpret_cast<const long long*>(ids);
+    a.E = ids ? E : 0;
     return launch_multi_bwd(pl, a, s0) == cudaSuccess ? ATTNRES_OK : ATTNRES_ERR_CUDA;
+}
+
+attnres_status attnres_multi_bwd(const attnres_multi_params* p, const void* q, const void* dy,
+                                 const float* alpha, const float* rstd, const float* logit,
+                                 void* const* dsrc, int64_t dsrc_ld, void* dq, float* dq_f32,
+                                 void* workspace, size_t workspace_bytes, void* stream) {
+    return multi_bwd_impl(p, q, 0, nullptr, dy, alpha, rstd, logit, dsrc, dsrc_ld, dq, dq_f32, workspace,
+                          workspace_bytes, stream);
+}
+
+attnres_status attnres_selected_bwd(const attnres_multi_params* p, const void* bank, int32_t E,
+                                    const int64_t* ids, const void* dy, const float* alpha,
+                                    const float* rstd, const float* logit, void* const* dsrc,
+                                    int64_t dsrc_ld, void* dbank, float* dbank_f32, void* workspace,
+                                    size_t workspace_bytes, void* stream) {
+    if (E < 1 || (p && p->base.N > 0 && !ids)) return ATTNRES_ERR_INVALID_ARG;
+    if (!ids) {  // no tokens: the bank gradient is zero
+        attnres_status st = check_multi(p);
+        if (st != ATTNRES_OK) return st;
+        if (!dbank) return ATTNRES_ERR_INVALID_ARG;
+        const size_t nb = static_cast<size_t>(E) * static_cast<size_t>(p->base.R);
+        cudaStream_t s0 = static_cast<cudaStream_t>(stream);
+        if (cudaMemsetAsync(dbank, 0, nb * 2, s0) != cudaSuccess ||
+            (dbank_f32 && cudaMemsetAsync(dbank_f32, 0, nb * 4, s0) != cudaSuccess))
+            return ATTNRES_ERR_CUDA;
+        return ATTNRES_OK;
+    }
+    return multi_bwd_impl(p, bank, E, ids, dy, alpha, rstd, logit, dsrc, dsrc_ld, dbank, dbank_f32, workspace,
+                          workspace_bytes, stream);
 }
 
 }  // extern "C"

@@ -532,6 +532,15 @@ __global__ void __launch_bounds__(kMaxThreads, 1) attnres_bwd_kernel(const __gri
                                     dq_acc[i][kk] = ffma2(k12, x, dq_acc[i][kk]);
                                 }
                             }
+                            if (a.dlast_add && s == S - 1) {
+                                // gradient reaching the last source from elsewhere (a fused
+                                // block-partial sum's later uses), added before rounding
+                                const uint4 gv = ld_global_nc_v4(reinterpret_cast<const char*>(a.dlast_add) +
+                                                                 (n * a.dlast_add_ld * 2 + d_off) + i * vstep);
+#pragma unroll
+                                for (int kk = 0; kk < 4; ++kk)
+                                    dv[kk] = ffma2(make_float2(1.0f, 1.0f), bf2_to_f2(u4_get(gv, kk)), dv[kk]);
+                            }
                             st_global_cs_v4(drow + static_cast<long long>(i) * vstep,
                                             make_uint4(pack_f2(dv[0]), pack_f2(dv[1]), pack_f2(dv[2]), pack_f2(dv[3])));
                         }

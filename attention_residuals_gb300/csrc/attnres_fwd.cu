@@ -24,6 +24,13 @@
 // second barrier is needed), and pass 2 adds the weighted rows into FP32
 // registers, thread t owning fixed columns, and releases the chunks.  The output norm needs one more CTA reduction per
 // token.  The pre-norm mixture o is written (FP32) only when asked for.
+// Fused block-partial sum ("Fast Attention Residuals", section "Full and
+// Block schedules": the caller sums the partial block before the read): with
+// `delta` set, the producer also streams the token's delta row into a small
+// slot ring, and the warp whose pass-1 row is the last source first replaces
+// that row in shared memory by the bf16 sum src[S-1] + delta and stores it
+// as the new partial sum; the group barrier then orders those writes before
+// pass 2, so the sum is never re-read from HBM.
 // This is a bandwidth-bound per-token reduction: no tensor cores.
 #include <cfloat>
 
@@ -46,9 +53,12 @@ __global__ void __launch_bounds__(kMaxThreads, fwd_ctas_per_sm(VPT)) attnres_fwd
     const int K = a.chunks;  // ring depth in chunks
     const int G = a.rows;    // rows per chunk
     const int GG = a.group;  // softmax group rows (whole chunks)
-    const SmemLayout L = make_layout(K, G, a.slot_bytes, 0, a.s_pad, false);
+    const int DSL = a.delta ? kDeltaSlots : 0;  // slots for the added rows (fused partial sum)
+    const SmemLayout L = make_layout(K, G, a.slot_bytes, DSL, a.s_pad, false);
     uint64_t* full = reinterpret_cast<uint64_t*>(smem + L.full);
     uint64_t* empty = reinterpret_cast<uint64_t*>(smem + L.empty);
+    uint64_t* dfull = reinterpret_cast<uint64_t*>(smem + L.dyfull);
+    uint64_t* dempty = reinterpret_cast<uint64_t*>(smem + L.dyempty);
     float* red = reinterpret_cast<float*>(smem + L.red);     // [2][red_rows][kRedPitch]
     float* zall = reinterpret_cast<float*>(smem + L.coef);  // [s_pad]
     float* rall = zall + a.s_pad;                           // [s_pad]
@@ -66,6 +76,10 @@ __global__ void __launch_bounds__(kMaxThreads, fwd_ctas_per_sm(VPT)) attnres_fwd
             mbar_init(full + k, 1);
             mbar_init(empty + k, ncw);
         }
+        for (int k = 0; k < DSL; ++k) {
+            mbar_init(dfull + k, 1);
+            mbar_init(dempty + k, 1);  // released by the one warp that forms the sum
+        }
         *abort_flag = 0;
         mbar_fence_init();
     }
@@ -80,7 +94,21 @@ __global__ void __launch_bounds__(kMaxThreads, fwd_ctas_per_sm(VPT)) attnres_fwd
             int k = 0;
             uint32_t phase = 0;
             long long issued = 0;  // chunk fills started
+            int dk = 0;
+            uint32_t dphase = 0;
+            long long d_issued = 0;
             for (long long n = blockIdx.x; n < N && !*abort_flag; n += gridDim.x) {
+                if (DSL) {
+                    // the row added to the last source, into its own slot
+                    if (!mbar_wait(dempty + dk, dphase ^ 1u, abort_flag, &g_fwd_error, kSiteFwdProducer)) break;
+                    mbar_arrive_expect_tx(dfull + dk, bytes);
+                    tma_load_1d(smem + L.dyring + dk * sb, a.delta + n * a.delta_ld, bytes, dfull + dk, pol);
+                    ++d_issued;
+                    if (++dk == DSL) {
+                        dk = 0;
+                        dphase ^= 1u;
+                    }
+                }
                 for (int g0 = 0; g0 < S; g0 += G) {
                     const int gs = min(G, S - g0);
                     if (!mbar_wait(empty + k, phase ^ 1u, abort_flag, &g_fwd_error, kSiteFwdProducer)) break;
@@ -103,6 +131,11 @@ __global__ void __launch_bounds__(kMaxThreads, fwd_ctas_per_sm(VPT)) attnres_fwd
                     const long long fills = (issued - 1 - c) / K + 1;
                     volatile int no_abort = 0;
                     mbar_wait(full + c, static_cast<uint32_t>((fills - 1) & 1), &no_abort, &g_fwd_error, kSiteDrain);
+                }
+                for (int c = 0; c < DSL && c < d_issued; ++c) {
+                    const long long fills = (d_issued - 1 - c) / DSL + 1;
+                    volatile int no_abort = 0;
+                    mbar_wait(dfull + c, static_cast<uint32_t>((fills - 1) & 1), &no_abort, &g_fwd_error, kSiteDrain);
                 }
             }
         }
@@ -175,6 +208,10 @@ __global__ void __launch_bounds__(kMaxThreads, fwd_ctas_per_sm(VPT)) attnres_fwd
     uint32_t cphase = 0;   // its fill parity
     uint32_t cbase = ring_lo;
     int rbuf = 0;
+    int dslot = 0;               // slot of this token's added row (fused partial sum)
+    uint32_t dslot_phase = 0;
+    const uint32_t dfull_s = sbase + L.dyfull;
+    const uint32_t dempty_s = sbase + L.dyempty;
 
     for (long long n = blockIdx.x; n < N; n += gridDim.x) {
         float2 acc[VPT][4];
@@ -211,6 +248,23 @@ __global__ void __launch_bounds__(kMaxThreads, fwd_ctas_per_sm(VPT)) attnres_fwd
                     if (++kc == K) kc = 0;
                 }
                 const uint32_t row_raw = ring_raw + static_cast<uint32_t>(kc) * cb + static_cast<uint32_t>(rr) * sb;
+                if (DSL && g0 + r == S - 1) {
+                    // fused block-partial sum: the last source becomes
+                    // src[S-1] + delta (bf16 add) in place, and is stored
+                    mbar_wait_s(dfull_s + 8u * dslot, dslot_phase, abort_flag, &g_fwd_error, kSiteFwdConsumer);
+                    const uint32_t drow = sbase + L.dyring + static_cast<uint32_t>(dslot) * sb;
+                    uint16_t* prow = a.partial_out + n * a.partial_ld;
+                    uint32_t ddep = 0;
+                    for (int w = lane; w < ncv; w += 32) {
+                        const uint4 dv = lds128(drow + 16u * w);
+                        ddep ^= dv.x;
+                        const uint4 pv = add_bf16x8(lds128(row_raw + 16u * w), dv);
+                        sts128(row_raw + 16u * w, pv);
+                        st_global_cs_v4(prow + 8 * w, pv);
+                    }
+                    __syncwarp();  // the sums are visible to every lane of this warp
+                    if (lane == 0) mbar_arrive_after(dempty_s + 8u * dslot, ddep);
+                }
                 float s0 = 0.0f, s1 = 0.0f, t0 = 0.0f, t1 = 0.0f;
                 float s2 = 0.0f, s3 = 0.0f, t2 = 0.0f, t3 = 0.0f;
                 int v = kv0 + lane;
@@ -362,6 +416,10 @@ __global__ void __launch_bounds__(kMaxThreads, fwd_ctas_per_sm(VPT)) attnres_fwd
                 a.rstd[n * S + s] = rall[s];
                 a.logit[n * S + s] = z;
             }
+        }
+        if (DSL && ++dslot == DSL) {
+            dslot = 0;
+            dslot_phase ^= 1u;
         }
     }
 }

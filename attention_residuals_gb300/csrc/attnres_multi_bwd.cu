@@ -57,8 +57,13 @@ __global__ void __launch_bounds__(kMultiBwdThreads, 1) attnres_multi_bwd_kernel(
     const int DS = a.dy_slots;
     const int s_pad = a.s_pad, m_pad = a.m_pad;
     const int nmb = (M + MB - 1) / MB;
+    const bool selected = a.ids != nullptr;  // per-token queries from a bank
+    // one register block of fixed queries: q and dq live in registers;
+    // otherwise q comes from shared memory and dq sums go to shared memory
+    const bool regblock = nmb == 1 && !selected;
+    const int QR = selected ? a.E : M;       // rows of dq (queries or bank rows)
     const MultiLayout L =
-        make_multi_layout(K, G, a.slot_bytes, M, DS, s_pad, m_pad, a.nkv, nmb > 1 ? a.nkv : 0, true);
+        make_multi_layout(K, G, a.slot_bytes, M, DS, s_pad, m_pad, a.nkv, regblock ? 0 : a.nkv, true, QR);
     uint64_t* full = reinterpret_cast<uint64_t*>(smem + L.full);
     uint64_t* empty = reinterpret_cast<uint64_t*>(smem + L.empty);
     uint64_t* dyfull = reinterpret_cast<uint64_t*>(smem + L.dyfull);
@@ -101,8 +106,8 @@ __global__ void __launch_bounds__(kMultiBwdThreads, 1) attnres_multi_bwd_kernel(
     }
     // coefficients of padded queries stay zero; dq sums start at zero
     for (int i = threadIdx.x; i < 2 * s_pad * m_pad; i += blockDim.x) al_t[i] = 0.0f;
-    if (nmb > 1)
-        for (int i = threadIdx.x; i < M * a.nkv * 8; i += blockDim.x) dqsm[i] = 0.0f;
+    if (!regblock)
+        for (int i = threadIdx.x; i < QR * a.nkv * 8; i += blockDim.x) dqsm[i] = 0.0f;
     __syncthreads();
 
     if (warp == ncw) {
@@ -216,15 +221,31 @@ __global__ void __launch_bounds__(kMultiBwdThreads, 1) attnres_multi_bwd_kernel(
     const uint32_t tfull_s = sbase + L.tfull;
     const uint32_t tempty_s = sbase + L.tempty;
     const uint32_t qsm_s = sbase + L.qsm;
-    {
+    // Bank row of slot m of token n (selected queries); -1 for an id outside
+    // [0, E), which is recorded as an error and contributes nothing.
+    auto bank_row = [&](long long n, int m) -> int {
+        const long long id = a.ids[n * M + m];
+        if (id < 0 || id >= a.E) {
+            atomicCAS(&g_multi_bwd_error, 0u, static_cast<unsigned>(kSiteBadId));
+            return -1;
+        }
+        return static_cast<int>(id);
+    };
+    // queries by key channel into shared memory (token n's bank rows when selected)
+    auto load_q = [&](long long n) {
         uint16_t* qsm = reinterpret_cast<uint16_t*>(smem + L.qsm);
         for (int i = threadIdx.x; i < m_pad * kw; i += nct) {
             const int m = i / kw;
             const int c = 8 * kv0 + (i - m * kw);
-            qsm[i] = (m < M && c >= ko && c < kend) ? a.q[static_cast<long long>(m) * a.R + (c - ko)]
-                                                    : static_cast<uint16_t>(0);
+            uint16_t v = 0;
+            if (m < M && c >= ko && c < kend) {
+                const int row = selected ? bank_row(n, m) : m;
+                if (row >= 0) v = a.q[static_cast<long long>(row) * a.R + (c - ko)];
+            }
+            qsm[i] = v;
         }
-    }
+    };
+    if (!selected) load_q(0);
     // One register block: the query values at the owned key vectors and the
     // dq sums live in registers for the whole launch.
     float2 qf[MB][VPT][4];
@@ -239,7 +260,7 @@ __global__ void __launch_bounds__(kMultiBwdThreads, 1) attnres_multi_bwd_kernel(
 #pragma unroll
                 for (int h = 0; h < 2; ++h) {
                     const int e = 2 * kk + h;
-                    const bool in = nmb == 1 && j < M && ((kmask[i] >> e) & 1u);
+                    const bool in = regblock && j < M && ((kmask[i] >> e) & 1u);
                     qv[h] = in ? bf16_bits_to_float(a.q[static_cast<long long>(j) * a.R + (8 * col[i] + e - ko)])
                                : 0.0f;
                 }
@@ -297,6 +318,9 @@ __global__ void __launch_bounds__(kMultiBwdThreads, 1) attnres_multi_bwd_kernel(
             }
         }
         named_bar_sync(1, nct);
+        // every warp is past the previous token's write and dq passes: the
+        // token's bank rows can replace the queries in shared memory
+        if (selected) load_q(n);
         // coefficients: one warp per query, lanes over sources
         {
             const float* tk = tok + ts * tstride;
@@ -332,7 +356,7 @@ __global__ void __launch_bounds__(kMultiBwdThreads, 1) attnres_multi_bwd_kernel(
         if (lane == 0) mbar_arrive_s(tempty_s + 8u * ts);
 
         // write pass: dv_s for every source row, one store per row
-        if (nmb == 1) {
+        if (regblock) {
             float2 dyf[MB][VPT][4];
             uint32_t ddep = 0;
 #pragma unroll
@@ -504,10 +528,12 @@ __global__ void __launch_bounds__(kMultiBwdThreads, 1) attnres_multi_bwd_kernel(
 #pragma unroll
                 for (int j = 0; j < MB; ++j) {
                     if (mb + j >= M) continue;
+                    const int row = selected ? bank_row(n, mb + j) : mb + j;
+                    if (row < 0) continue;
 #pragma unroll
                     for (int i = 0; i < VPT; ++i) {
                         if (kvi[i] < 0) continue;
-                        float2* d2 = reinterpret_cast<float2*>(dqsm + (mb + j) * kw + 8 * kvi[i]);
+                        float2* d2 = reinterpret_cast<float2*>(dqsm + row * kw + 8 * kvi[i]);
 #pragma unroll
                         for (int kk = 0; kk < 4; ++kk) {
                             const float2 o = d2[kk];
@@ -540,14 +566,14 @@ __global__ void __launch_bounds__(kMultiBwdThreads, 1) attnres_multi_bwd_kernel(
         }
     }
 
-    // this CTA's FP32 partial row: part[cta][m * R + (c - ko)]
-    float* prow = a.part + static_cast<long long>(blockIdx.x) * M * a.R;
+    // this CTA's FP32 partial row: part[cta][m * R + (c - ko)], m < QR
+    float* prow = a.part + static_cast<long long>(blockIdx.x) * QR * a.R;
 #pragma unroll
     for (int i = 0; i < VPT; ++i) {
         if (kvi[i] < 0) continue;
-        for (int m = 0; m < M; ++m) {
+        for (int m = 0; m < QR; ++m) {
             float v8[8];
-            if (nmb == 1) {
+            if (regblock) {
 #pragma unroll
                 for (int j = 0; j < MB; ++j) {
                     if (j == m) {
@@ -578,7 +604,7 @@ cudaError_t launch_t(const MultiPlan& plan, const MultiBwdArgs& a, cudaStream_t 
     kern<<<plan.grid, (plan.b_ncw + 1) * 32, plan.smem_bwd, stream>>>(a);
     err = cudaGetLastError();
     if (err != cudaSuccess) return err;
-    const int W = a.M * a.R;
+    const int W = (a.ids ? a.E : a.M) * a.R;
     return launch_finalize(a.part, plan.grid, W, W, const_cast<uint16_t*>(a.dq), a.dq_f32, nullptr, nullptr,
                            stream);
 }

@@ -138,7 +138,8 @@ __global__ void __launch_bounds__(kMaxThreads, multi_fwd_ctas_per_sm(VPT))
     const int kv0 = a.kv0, nkv = a.nkv;
     const int kw = nkv * 8;
     const uint32_t kwb = static_cast<uint32_t>(nkv) * 16u;  // bytes per query row in shared memory
-    const bool q_once = a.qrows >= M;                      // every query stays in shared memory
+    const bool selected = a.ids != nullptr;                // per-token queries from a bank
+    const bool q_once = !selected && a.qrows >= M;         // every query stays in shared memory
     int col[VPT];
 #pragma unroll
     for (int i = 0; i < VPT; ++i) {
@@ -162,14 +163,27 @@ __global__ void __launch_bounds__(kMaxThreads, multi_fwd_ctas_per_sm(VPT))
     // With an aligned key and a 16-byte aligned query array a query row is
     // copied as whole 16-byte vectors (the key window is then exactly R).
     const bool q_vec = key_aligned && (reinterpret_cast<uintptr_t>(a.q) & 15u) == 0;
-    auto load_q = [&](int m0, int rows) {
+    // Source row of query m of token n: the query array, or the bank row the
+    // token selects (an id outside [0, E) is recorded as an error and reads
+    // as a zero query).
+    auto qsrc = [&](long long n, int m) -> const uint16_t* {
+        if (!selected) return a.q + static_cast<long long>(m) * a.R;
+        const long long id = a.ids[n * M + m];
+        if (id < 0 || id >= a.E) {
+            atomicCAS(&g_multi_error, 0u, static_cast<unsigned>(kSiteBadId));
+            return nullptr;
+        }
+        return a.q + id * a.R;
+    };
+    auto load_q = [&](long long n, int m0, int rows) {
         if (q_vec) {
 #pragma unroll 4
             for (int i = threadIdx.x; i < rows * nkv; i += nct) {
                 const int j = i / nkv;
                 const int m = m0 + j;
                 uint4 w = make_uint4(0u, 0u, 0u, 0u);
-                if (m < M) w = ld_global_nc_v4(a.q + static_cast<long long>(m) * a.R + 8 * (i - j * nkv));
+                const uint16_t* src = m < M ? qsrc(n, m) : nullptr;
+                if (src) w = ld_global_nc_v4(src + 8 * (i - j * nkv));
                 *reinterpret_cast<uint4*>(qsm + 8 * i) = w;
             }
         } else {
@@ -178,12 +192,12 @@ __global__ void __launch_bounds__(kMaxThreads, multi_fwd_ctas_per_sm(VPT))
                 const int j = i / kw;
                 const int c = 8 * kv0 + (i - j * kw);
                 const int m = m0 + j;
-                qsm[i] = (m < M && c >= ko && c < kend) ? a.q[static_cast<long long>(m) * a.R + (c - ko)]
-                                                        : static_cast<uint16_t>(0);
+                const uint16_t* src = (m < M && c >= ko && c < kend) ? qsrc(n, m) : nullptr;
+                qsm[i] = src ? src[c - ko] : static_cast<uint16_t>(0);
             }
         }
     };
-    if (q_once) load_q(0, a.qrows);
+    if (q_once) load_q(0, 0, a.qrows);
     named_bar_sync(1, nct);
 
     int ck = 0;            // current chunk
@@ -197,7 +211,7 @@ __global__ void __launch_bounds__(kMaxThreads, multi_fwd_ctas_per_sm(VPT))
             const bool first = b == 0;
             if (!q_once) {
                 // every warp finished the previous block's pass 1 before its last barrier
-                load_q(m0, MB);
+                load_q(n, m0, MB);
                 named_bar_sync(1, nct);
             }
             const uint32_t qbase = qsm_s + static_cast<uint32_t>(q_once ? m0 : 0) * kwb;

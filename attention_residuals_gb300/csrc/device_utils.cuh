@@ -377,6 +377,21 @@ __device__ __forceinline__ uint4 mask_bf16x8(const uint4& x, int j0, int lo, int
     return make_uint4(w[0], w[1], w[2], w[3]);
 }
 
+__device__ __forceinline__ void sts128(uint32_t addr, const uint4& v) {
+    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
+                 : "memory");
+}
+
+// a + b for two bf16x8 vectors: each pair widened exactly to FP32, added
+// once, rounded to bf16 (nearest, ties to even) -- a bf16 tensor add.
+__device__ __forceinline__ uint4 add_bf16x8(const uint4& a, const uint4& b) {
+    const float2 one = make_float2(1.0f, 1.0f);
+    uint32_t w[4];
+#pragma unroll
+    for (int kk = 0; kk < 4; ++kk) w[kk] = pack_f2(ffma2(one, bf2_to_f2(u4_get(a, kk)), bf2_to_f2(u4_get(b, kk))));
+    return make_uint4(w[0], w[1], w[2], w[3]);
+}
+
 // Position in the shared-memory row ring: row address, slot index, phase.
 struct RingCursor {
     uint32_t row;

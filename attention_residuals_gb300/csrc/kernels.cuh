@@ -30,6 +30,7 @@ enum WaitSite : unsigned {
     kSiteBwdConsumer = 4,
     kSiteBwdTokStat = 5,
     kSiteDrain = 6,
+    kSiteBadId = 7,  // a selected-query id outside [0, E)
 };
 
 // Launch plan: one persistent CTA per SM.  `ncw` consumer warps each own
@@ -72,8 +73,9 @@ constexpr int kRedPitch = 20;
 __host__ __device__ inline uint32_t align_up(uint32_t x, uint32_t a) { return (x + a - 1) / a * a; }
 
 // Forward: chunk ring, z[s_pad] and rstd[s_pad] of the current token, and
-// the query as bf16 indexed by channel (slot_bytes, zero outside the key).
-// Backward: chunk ring, dy ring, token-statistics ring.
+// the query as bf16 indexed by channel (slot_bytes, zero outside the key);
+// with the fused block-partial sum, `dy_slots` single-row slots for the
+// added rows.  Backward: chunk ring, dy ring, token-statistics ring.
 __host__ __device__ inline SmemLayout make_layout(int chunks, int rows, int slot_bytes, int dy_slots,
                                                   int s_pad, bool backward) {
     SmemLayout L;
@@ -81,16 +83,16 @@ __host__ __device__ inline SmemLayout make_layout(int chunks, int rows, int slot
     L.ring = off;
     off += static_cast<uint32_t>(chunks) * static_cast<uint32_t>(rows) * static_cast<uint32_t>(slot_bytes);
     L.dyring = off;
-    off += backward ? static_cast<uint32_t>(dy_slots) * static_cast<uint32_t>(slot_bytes) : 0u;
+    off += static_cast<uint32_t>(dy_slots) * static_cast<uint32_t>(slot_bytes);
     off = align_up(off, 16);
     L.full = off;
     off += 8u * chunks;
     L.empty = off;
     off += 8u * chunks;
     L.dyfull = off;
-    off += backward ? 8u * dy_slots : 0u;
+    off += 8u * dy_slots;
     L.dyempty = off;
-    off += backward ? 8u * dy_slots : 0u;
+    off += 8u * dy_slots;
     L.tfull = off;
     off += backward ? 8u * kTokSlots : 0u;
     L.tempty = off;
@@ -128,7 +130,14 @@ struct FwdArgs {
     float* logit;
     float* o_rstd;
     float* o_pre;       // optional FP32 [N, D] pre-norm mixture
+    // Fused block-partial sum: source S-1 is formed as src[S-1] + delta
+    // (rounded to bf16) and written to partial_out; NULL = plain read.
+    const uint16_t* delta;
+    long long delta_ld;
+    uint16_t* partial_out;
+    long long partial_ld;
 };
+constexpr int kDeltaSlots = 2;
 
 struct BwdArgs {
     const void* src[ATTNRES_MAX_S];
@@ -154,6 +163,10 @@ struct BwdArgs {
     float* dq_f32;
     uint16_t* dw_o;
     float* dw_o_f32;
+    // optional gradient added to the last source's gradient before rounding
+    // (the fused block-partial sum's later uses); NULL = none
+    const uint16_t* dlast_add;
+    long long dlast_add_ld;
 };
 
 // ---------------------------------------------------------------------------
@@ -177,11 +190,12 @@ struct MultiLayout {
 // Backward layout.  Tables (floats): da[m_pad][s_pad], alpha[s_pad][m_pad],
 // b[s_pad][m_pad], zr[m_pad][s_pad].  qsm: m_pad query rows of nkv 16-byte
 // vectors (bf16).
-// dqsm (backward, only when the queries take several register blocks): M
-// rows of dq_nkv * 8 FP32 dq partial sums.
+// dqsm (only when the queries take several register blocks, or per-token
+// queries come from a bank): dq_rows rows (queries, or bank rows) of
+// dq_nkv * 8 FP32 partial sums.
 __host__ __device__ inline MultiLayout make_multi_layout(int chunks, int rows, int slot_bytes, int M,
                                                         int dy_slots, int s_pad, int m_pad, int nkv,
-                                                        int dq_nkv, bool backward) {
+                                                        int dq_nkv, bool backward, int dq_rows = -1) {
     MultiLayout L;
     uint32_t off = 0;
     L.ring = off;
@@ -211,7 +225,7 @@ __host__ __device__ inline MultiLayout make_multi_layout(int chunks, int rows, i
     L.qsm = off;
     off += static_cast<uint32_t>(m_pad) * static_cast<uint32_t>(nkv) * 16u;
     L.dqsm = off;
-    off += backward ? static_cast<uint32_t>(M) * static_cast<uint32_t>(dq_nkv) * 32u : 0u;
+    off += backward ? static_cast<uint32_t>(dq_rows < 0 ? M : dq_rows) * static_cast<uint32_t>(dq_nkv) * 32u : 0u;
     L.misc = off;  // abort flag
     off += 16u;
     L.total = align_up(off, 128);
@@ -267,6 +281,7 @@ struct MultiPlan {
     int f_group;           // forward softmax group rows (whole chunks, <= kMaxGroup)
     int qrows;             // query rows held in shared memory by the forward
     int bwd_ok;            // the backward's resident layout fits
+    int E;                 // query bank rows (selected-query read), 0 otherwise
     int ncw, vpt;          // forward: consumer warps, 16-byte vectors per thread
     int b_ncw, b_vpt;      // backward
     int mb_f, mb_b;        // queries per register block (forward / backward)
@@ -287,7 +302,9 @@ struct MultiFwdArgs {
     int chunks, rows, slot_bytes, ncw, s_pad, kv0, nkv;
     int group;             // softmax group rows (whole chunks)
     int qrows;             // query rows in shared memory (M, or MB: reloaded per block)
-    const uint16_t* q;     // [M][R]
+    const uint16_t* q;     // [M][R], or the query bank [E][R] when ids is set
+    const long long* ids;  // [N][M] bank row of every (token, slot), or NULL
+    int E;                 // bank rows
     uint16_t* y;
     float* alpha;          // [N][M][S]
     float* rstd;           // [N][S]
@@ -307,9 +324,11 @@ struct MultiBwdArgs {
     const float* alpha;
     const float* rstd;
     const float* logit;
-    float* part;           // [grid][M * R]
-    uint16_t* dq;          // [M][R]
-    float* dq_f32;         // [M][R] or NULL
+    float* part;           // [grid][Q * R], Q = M (or E with ids)
+    uint16_t* dq;          // [Q][R]
+    float* dq_f32;         // [Q][R] or NULL
+    const long long* ids;  // [N][M] bank row of every (token, slot), or NULL
+    int E;                 // bank rows
 };
 
 unsigned take_multi_fwd_error();

@@ -209,3 +209,72 @@ def attnres_multi_op(values, queries: Tensor, *, eps: float = _ops.EPS_DEFAULT, 
     ko = D - queries.shape[-1] if key_offset is None else int(key_offset)
     return read_multi_fwd(vals, queries, float(eps), float(scale), ko,
                           output_layout == "token_major")[0]
+
+
+# --------------------------------------------------------------------------
+# Selected-query read ("Fast Attention Residuals", section "Multi-query
+# AttnRes": attnres_selected)
+# --------------------------------------------------------------------------
+@torch.library.custom_op(f"{_NS}::read_selected_fwd", mutates_args=(), device_types="cuda")
+def read_selected_fwd(values: List[Tensor], bank: Tensor, ids: Tensor, eps: float, scale: float,
+                      key_offset: int) -> Tuple[Tensor, Tensor, Tensor, Tensor]:
+    S, D, packed, lead = _shape_info(values, bank.shape[-1])
+    r = _ops.attnres_selected_fwd(_as_values(values, packed), bank, ids, eps=eps, scale=scale,
+                                  key_offset=key_offset)
+    return r["y"], r["alpha"], r["rstd"], r["logit"]
+
+
+@read_selected_fwd.register_fake
+def _(values, bank, ids, eps, scale, key_offset):
+    S, D, packed, lead = _shape_info(values, bank.shape[-1])
+    K = ids.shape[-1]
+    N = 1
+    for d in lead:
+        N *= d
+    f32 = dict(dtype=torch.float32, device=bank.device)
+    y = torch.empty((*lead, K, D), dtype=torch.bfloat16, device=bank.device)
+    return y, torch.empty((N, K, S), **f32), torch.empty((N, S), **f32), torch.empty((N, K, S), **f32)
+
+
+@torch.library.custom_op(f"{_NS}::read_selected_bwd", mutates_args=(), device_types="cuda")
+def read_selected_bwd(values: List[Tensor], bank: Tensor, ids: Tensor, dy: Tensor, alpha: Tensor,
+                      rstd: Tensor, logit: Tensor, eps: float, scale: float,
+                      key_offset: int) -> Tuple[List[Tensor], Tensor]:
+    S, D, packed, lead = _shape_info(values, bank.shape[-1])
+    saved = {"alpha": alpha, "rstd": rstd, "logit": logit}
+    g = _ops.attnres_selected_bwd(_as_values(values, packed), bank, ids, dy.contiguous(), saved, eps=eps,
+                                  scale=scale, key_offset=key_offset)
+    dv = [g["dvalues"]] if packed else list(g["dvalues"])
+    return dv, g["dbank"]
+
+
+@read_selected_bwd.register_fake
+def _(values, bank, ids, dy, alpha, rstd, logit, eps, scale, key_offset):
+    return [torch.empty_like(v) for v in values], torch.empty_like(bank)
+
+
+def _sel_setup_context(ctx, inputs, output):
+    values, bank, ids, eps, scale, key_offset = inputs
+    y, alpha, rstd, logit = output
+    ctx.cfg = (eps, scale, key_offset)
+    ctx.save_for_backward(bank, ids, alpha, rstd, logit, *values)
+
+
+def _sel_backward(ctx, dy, d_alpha, d_rstd, d_logit):
+    bank, ids, alpha, rstd, logit, *values = ctx.saved_tensors
+    eps, scale, key_offset = ctx.cfg
+    dv, db = read_selected_bwd(list(values), bank, ids, dy.to(torch.bfloat16), alpha, rstd, logit, eps,
+                               scale, key_offset)
+    return list(dv), db, None, None, None, None
+
+
+read_selected_fwd.register_autograd(_sel_backward, setup_context=_sel_setup_context)
+
+
+def attnres_selected_op(values, query_bank: Tensor, ids: Tensor, *, eps: float = _ops.EPS_DEFAULT,
+                        scale: float = 1.0, key_offset: Optional[int] = None) -> Tensor:
+    """The selected-query read through the registered operator."""
+    vals = [values] if isinstance(values, Tensor) else list(values)
+    D = vals[0].shape[-1]
+    ko = D - query_bank.shape[-1] if key_offset is None else int(key_offset)
+    return read_selected_fwd(vals, query_bank, ids, float(eps), float(scale), ko)[0]

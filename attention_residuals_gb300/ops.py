@@ -398,6 +398,87 @@ def attnres_multi_bwd(values: Sources, queries: torch.Tensor, dy: torch.Tensor, 
 
 
 # --------------------------------------------------------------------------
+# Selected-query read ("Fast Attention Residuals", section "Multi-query
+# AttnRes": attnres_selected(sources, query_bank, ids) -> [..., K, D])
+# --------------------------------------------------------------------------
+def _check_bank_ids(bank: torch.Tensor, ids: torch.Tensor, view: _SourceView):
+    if bank.dim() != 2 or not (1 <= bank.shape[1] <= view.D):
+        raise ValueError("query_bank must be [E, R] with 1 <= R <= D")
+    if bank.dtype != torch.bfloat16 or not bank.is_cuda:
+        raise TypeError("query_bank must be a CUDA bf16 tensor")
+    if ids.dtype not in (torch.int64, torch.int32, torch.int16, torch.uint8, torch.int8) or not ids.is_cuda:
+        raise TypeError("ids must be a CUDA integer tensor")
+    if tuple(ids.shape[:-1]) != tuple(view.lead_shape) or ids.dim() < 1:
+        raise ValueError("ids must be [..., K] with the sources' leading shape")
+    K = ids.shape[-1]
+    if not (1 <= K <= _lib.MAX_M):
+        raise ValueError(f"at most {_lib.MAX_M} selected queries per token")
+    return bank.contiguous(), ids.reshape(view.N, K).to(torch.int64).contiguous(), K
+
+
+def attnres_selected_fwd(values: Sources, bank: torch.Tensor, ids: torch.Tensor, *,
+                         eps: float = EPS_DEFAULT, scale: float = 1.0, key_offset: Optional[int] = None,
+                         stream=None) -> dict:
+    """Selected-query forward: y [..., K, D] and the saved statistics
+    alpha/logit [N, K, S], rstd [N, S] (f32).  An id outside [0, E) is
+    reported by attnres_check_device_error()."""
+    view = _source_view(values)
+    bank, ids2, K = _check_bank_ids(bank, ids, view)
+    E, R = bank.shape
+    mp = make_multi_params(view, K, R, key_offset=key_offset, eps=eps, scale=scale, token_major=True)
+    dev = view.rows[0].device
+    S, N, D = len(view.rows), view.N, view.D
+    y = torch.empty((N, K, D), dtype=torch.bfloat16, device=dev)
+    f32 = dict(dtype=torch.float32, device=dev)
+    alpha = torch.empty((N, K, S), **f32)
+    rstd = torch.empty((N, S), **f32)
+    logit = torch.empty((N, K, S), **f32)
+    rc = _lib.load().attnres_selected_fwd(ctypes.byref(mp), _ptr(bank), ctypes.c_int32(E), _ptr(ids2), _ptr(y),
+                                          _ptr(alpha), _ptr(rstd), _ptr(logit), _stream(stream))
+    _lib.check(rc, "attnres_selected_fwd")
+    return {"y": y.view(*view.lead_shape, K, D), "alpha": alpha, "rstd": rstd, "logit": logit,
+            "view": view, "ids": ids2}
+
+
+def attnres_selected_bwd(values: Sources, bank: torch.Tensor, ids: torch.Tensor, dy: torch.Tensor,
+                         saved: dict, *, eps: float = EPS_DEFAULT, scale: float = 1.0,
+                         key_offset: Optional[int] = None, stream=None,
+                         workspace: Optional[torch.Tensor] = None) -> dict:
+    """Selected-query backward.  dy has the output's shape [..., K, D].
+    Returns dvalues (packed or a list, like the sources) and dbank [E, R]
+    in bf16 and fp32."""
+    view = saved.get("view") or _source_view(values)
+    bank, ids2, K = _check_bank_ids(bank, ids, view)
+    E, R = bank.shape
+    mp = make_multi_params(view, K, R, key_offset=key_offset, eps=eps, scale=scale, token_major=True)
+    S, N, D = len(view.rows), view.N, view.D
+    dev = view.rows[0].device
+    if dy.dtype != torch.bfloat16 or not dy.is_cuda or dy.numel() != K * N * D:
+        raise TypeError("dy must be a CUDA bf16 tensor shaped like the output")
+    dy3 = dy.reshape(N, K, D).contiguous()
+    if view.packed:
+        dpacked = torch.empty((S, N, D), dtype=torch.bfloat16, device=dev)
+        drows = [dpacked[s] for s in range(S)]
+    else:
+        dpacked = None
+        drows = [torch.empty((N, D), dtype=torch.bfloat16, device=dev) for _ in range(S)]
+    dptrs = (ctypes.c_void_p * S)(*[r.data_ptr() for r in drows])
+    db = torch.empty((E, R), dtype=torch.bfloat16, device=dev)
+    db32 = torch.empty((E, R), dtype=torch.float32, device=dev)
+    need = int(_lib.load().attnres_selected_bwd_workspace_bytes(ctypes.byref(mp), ctypes.c_int32(E)))
+    if workspace is None or workspace.numel() < need:
+        workspace = torch.empty((max(need, 16),), dtype=torch.uint8, device=dev)
+    rc = _lib.load().attnres_selected_bwd(
+        ctypes.byref(mp), _ptr(bank), ctypes.c_int32(E), _ptr(ids2), _ptr(dy3), _ptr(saved["alpha"]),
+        _ptr(saved["rstd"]), _ptr(saved["logit"]), dptrs, ctypes.c_int64(D), _ptr(db), _ptr(db32),
+        _ptr(workspace), ctypes.c_size_t(workspace.numel()), _stream(stream))
+    _lib.check(rc, "attnres_selected_bwd")
+    shape = (*view.lead_shape, D)
+    dv = dpacked.view(S, *shape) if dpacked is not None else [r.view(*shape) for r in drows]
+    return {"dvalues": dv, "dbank": db, "dbank_f32": db32}
+
+
+# --------------------------------------------------------------------------
 # Autograd operator
 # --------------------------------------------------------------------------
 def attnres(values: Sources, query: torch.Tensor, *, eps: float = EPS_DEFAULT, scale: float = 1.0,
@@ -429,3 +510,14 @@ def attnres_multi(values: Sources, queries: torch.Tensor, *, eps: float = EPS_DE
     from .custom_ops import attnres_multi_op
     return attnres_multi_op(values, queries, eps=eps, scale=scale, key_offset=key_offset,
                             output_layout=output_layout)
+
+
+def attnres_selected(values: Sources, query_bank: torch.Tensor, ids: torch.Tensor, *,
+                     eps: float = EPS_DEFAULT, scale: float = 1.0,
+                     key_offset: Optional[int] = None) -> torch.Tensor:
+    """Selected-query read: output [..., K, D], where slot k of token n reads
+    the sources with query_bank[ids[n, k]] ([E, R] bank, integer [..., K]
+    ids).  Differentiable in values and query_bank; registered torch
+    operators, so torch.compile(fullgraph=True) and CUDA graphs work."""
+    from .custom_ops import attnres_selected_op
+    return attnres_selected_op(values, query_bank, ids, eps=eps, scale=scale, key_offset=key_offset)

@@ -200,3 +200,51 @@ def make_multi_workload(key: str, *, N: Optional[int] = None, seed: Optional[int
     return make_multi(c["S"], n, c["D"], c["R"], c["M"], seed=100 + len(key) if seed is None else seed,
                       src_scale=c["src_scale"], device=device,
                       name=f"multi-query {key} S{c['S']} N{n} D{c['D']} R{c['R']} M{c['M']}")
+
+
+# ---------------------------------------------------------------------------
+# Selected-query reads ("Fast Attention Residuals", section "Multi-query
+# AttnRes": an [E, R] query bank and integer [..., K] ids per token)
+# ---------------------------------------------------------------------------
+@dataclass
+class SelectedWorkload:
+    name: str
+    S: int
+    N: int
+    D: int
+    R: int
+    E: int
+    K: int
+    key_offset: int
+    eps: float
+    scale: float
+    values: torch.Tensor            # packed [S, N, D] bf16
+    bank: torch.Tensor              # [E, R] bf16
+    ids: torch.Tensor               # [N, K] int64 in [0, E)
+    dy: torch.Tensor                # [N, K, D] bf16
+
+
+def make_selected(S: int, N: int, D: int, R: int, E: int, K: int, *, key_offset: Optional[int] = None,
+                  seed: int = 0, src_scale=None, device: str = "cpu", scale: float = 1.0,
+                  eps: float = EPS_DEFAULT, unused_rows: int = 0) -> SelectedWorkload:
+    """Sources N(0,1) (times one U[lo, hi] scalar per source when src_scale is
+    given), bank rows N(0,1) * R^-1/2, ids uniform over the first
+    E - unused_rows bank rows (the rest are never selected), dy N(0,1)."""
+    gen = torch.Generator(device=device)
+    gen.manual_seed(int(seed))
+    values = torch.empty((S, N, D), dtype=torch.bfloat16, device=device)
+    scales = None
+    if src_scale is not None:
+        lo, hi = src_scale
+        scales = lo + (hi - lo) * torch.rand((S,), generator=gen, device=device)
+    for s in range(S):
+        x = _randn((N, D), gen, device)
+        if scales is not None:
+            x *= scales[s]
+        values[s] = x.to(torch.bfloat16)
+    bank = (_randn((E, R), gen, device) * R ** -0.5).to(torch.bfloat16)
+    ids = torch.randint(0, max(1, E - unused_rows), (N, K), generator=gen, device=device, dtype=torch.int64)
+    dy = _randn((N, K, D), gen, device).to(torch.bfloat16)
+    ko = D - R if key_offset is None else int(key_offset)
+    return SelectedWorkload(name=f"selected S{S} N{N} D{D} R{R} E{E} K{K}", S=S, N=N, D=D, R=R, E=E, K=K,
+                            key_offset=ko, eps=eps, scale=scale, values=values, bank=bank, ids=ids, dy=dy)

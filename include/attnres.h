@@ -62,7 +62,7 @@ typedef enum {
     ATTNRES_ERR_UNSUPPORTED = 3,  /* legal shape this build does not handle       */
     ATTNRES_ERR_WORKSPACE = 4,    /* workspace NULL or smaller than required      */
     ATTNRES_ERR_CUDA = 5,         /* a CUDA runtime call or launch failed         */
-    ATTNRES_ERR_DEVICE = 6        /* a kernel reported a failed wait (see below)  */
+    ATTNRES_ERR_DEVICE = 6        /* a kernel reported a failed wait or a bad id  */
 } attnres_status;
 
 /*
@@ -151,6 +151,49 @@ attnres_status attnres_bwd(const attnres_params* p, const void* q, const void* w
                            size_t workspace_bytes, void* stream);
 
 /*
+ * Fused block-partial read ("Fast Attention Residuals", section "Full and
+ * Block schedules": Block supplies the embedding, the completed block sums
+ * and the current partial sum, which the caller sums before the read).
+ * Instead of materialising partial_new = partial + delta in a separate pass
+ * and reading it back, the forward takes the previous partial sum as the
+ * last source (src[S-1]) and the newest writer output `delta`, forms
+ *
+ *   partial_new[n] = partial[n] + delta[n]     (FP32 add, one bf16 rounding:
+ *                                               exactly a bf16 tensor add)
+ *
+ * in shared memory, writes it to `partial_out` and reads the sources
+ * (src[0..S-2], partial_new) exactly as attnres_fwd does.  One [N, D] read
+ * and one launch less per layer than summing first.
+ *   delta         bf16 rows at delta + n * delta_ld (16-byte aligned)
+ *   partial_out   bf16 rows at partial_out + n * partial_ld; may be the same
+ *                 memory as src[S-1] (an in-place update: each row is read
+ *                 before it is written), must not overlap anything else
+ * Other arguments, outputs and errors as attnres_fwd.
+ */
+attnres_status attnres_fwd_partial(const attnres_params* p, const void* q, const void* w_o,
+                                   const void* delta, int64_t delta_ld, void* partial_out,
+                                   int64_t partial_ld, void* y, float* alpha, float* rstd,
+                                   float* logit, float* o_rstd, float* o_pre, void* stream);
+
+/*
+ * Backward of the fused block-partial read.  The caller passes the sources
+ * with src[S-1] = partial_new (the forward's partial_out).  `g_partial`
+ * (bf16 rows at g_partial + n * g_ld, or NULL) is the gradient reaching
+ * partial_new from its later uses; it is added, before rounding, to the
+ * gradient of the last source, so dsrc[S-1] receives the full gradient of
+ * partial_new -- which is the gradient of both `partial` and `delta` (they
+ * feed partial_new with unit weight).  Other arguments, outputs and errors
+ * as attnres_bwd.
+ */
+attnres_status attnres_bwd_partial(const attnres_params* p, const void* q, const void* w_o,
+                                   const void* dy, const float* alpha, const float* rstd,
+                                   const float* logit, const float* o_rstd, const float* o_pre,
+                                   const void* g_partial, int64_t g_ld, void* const* dsrc,
+                                   int64_t dsrc_ld, void* dq, float* dq_f32, void* dw_o,
+                                   float* dw_o_f32, void* workspace, size_t workspace_bytes,
+                                   void* stream);
+
+/*
  * Backward without a caller-supplied workspace (no counterpart in the
  * papers; it exists for callers that cannot allocate device memory, such as
  * code running inside a region being captured into a CUDA graph, plugins
@@ -181,9 +224,11 @@ attnres_status attnres_bwd_noalloc(const attnres_params* p, const void* q, const
 /*
  * Kernels bound every wait on a shared-memory barrier.  A wait that runs out
  * of time makes the kernel record a nonzero code here and finish without
- * further waiting (its outputs are then garbage).  This call synchronises
- * the device, returns ATTNRES_ERR_DEVICE and clears the record if one was
- * set, ATTNRES_OK otherwise.
+ * further waiting (its outputs are then garbage); so does a selected-query
+ * id outside [0, E) (that query then reads as zero and adds nothing to the
+ * bank gradient).  This call synchronises the device, returns
+ * ATTNRES_ERR_DEVICE and clears the record if one was set, ATTNRES_OK
+ * otherwise.
  */
 attnres_status attnres_check_device_error(void);
 
@@ -283,6 +328,41 @@ attnres_status attnres_multi_bwd(const attnres_multi_params* p, const void* q, c
  * does not fit.
  */
 attnres_status attnres_multi_plan_info(const attnres_multi_params* p, int64_t out[8]);
+
+/* ------------------------------------------------------------------------
+ * Selected-query read ("Fast Attention Residuals", section "Multi-query
+ * AttnRes": attnres_selected(sources, query_bank, ids) takes an [E, R] bank
+ * and integer [..., K] ids and returns [..., K, D]).  Output (n, k) is the
+ * single-query read of token n's sources with query bank[ids[n][k]]:
+ *
+ *   z_nks = scale * r_ns * <t_ns, bank[ids[n][k]]>,  a_nk = softmax_s(z_nk),
+ *   y[n][k] = sum_s a_nks v_s[n]
+ *
+ * Gradients: dsrc sums over the K reads of each token; dbank[e] sums the
+ * query gradients of every (n, k) with ids[n][k] == e (zero for rows no
+ * token selects).  Same kernels, layouts and supported range as the
+ * multi-query read with M = K slots per token, plus the bank's dq rows
+ * (E * R * 4 bytes of shared memory) in the backward.
+ *   p        as for the multi-query read, M = K (1 <= K <= ATTNRES_MAX_M)
+ *   bank     bf16 [E][R] contiguous, E >= 1
+ *   ids      int64 [N][K] contiguous, 8-byte aligned; an id outside
+ *            [0, E) is recorded for attnres_check_device_error and the
+ *            slot reads as a zero query
+ *   y, alpha, rstd, logit   as for attnres_multi_fwd (slot k in place of m)
+ *   dbank    bf16 [E][R], dbank_f32 f32 [E][R] (may be NULL): written
+ * ------------------------------------------------------------------------ */
+attnres_status attnres_selected_fwd(const attnres_multi_params* p, const void* bank, int32_t E,
+                                    const int64_t* ids, void* y, float* alpha, float* rstd,
+                                    float* logit, void* stream);
+
+/* Bytes of workspace attnres_selected_bwd needs (grid * E * R * 4; 0 when N == 0). */
+size_t attnres_selected_bwd_workspace_bytes(const attnres_multi_params* p, int32_t E);
+
+attnres_status attnres_selected_bwd(const attnres_multi_params* p, const void* bank, int32_t E,
+                                    const int64_t* ids, const void* dy, const float* alpha,
+                                    const float* rstd, const float* logit, void* const* dsrc,
+                                    int64_t dsrc_ld, void* dbank, float* dbank_f32, void* workspace,
+                                    size_t workspace_bytes, void* stream);
 
 #ifdef __cplusplus
 }

@@ -182,3 +182,27 @@ def test_multi_missing_or_misaligned_pointers_rejected(lib):
     d = (ctypes.c_void_p * 4)(*[0x300000 + i * 0x10000 for i in range(4)])
     assert lib.attnres_multi_bwd(ctypes.byref(mp), fake, fake, fake, fake, fake, d, ctypes.c_int64(64),
                                  None, None, fake, ctypes.c_size_t(1 << 20), None) == 1
+
+
+# ------------------------------------------------------------ selected-query
+@pytest.mark.parametrize("kw,code", MULTI_BAD)
+def test_selected_rejects_bad_shapes_before_launch(lib, kw, code):
+    mp = _mparams(**kw)
+    fake = ctypes.c_void_p(0x200000)
+    assert lib.attnres_selected_fwd(ctypes.byref(mp), fake, 4, fake, fake, fake, fake, fake, None) == code
+    d = (ctypes.c_void_p * 4)(*[0x300000 + i * 0x10000 for i in range(4)])
+    rc = lib.attnres_selected_bwd(ctypes.byref(mp), fake, 4, fake, fake, fake, fake, fake, d,
+                                  ctypes.c_int64(64), fake, None, fake, ctypes.c_size_t(1 << 20), None)
+    assert rc == code
+    assert lib.attnres_selected_bwd_workspace_bytes(ctypes.byref(mp), 4) == 0
+
+
+def test_selected_bank_and_ids_checked(lib):
+    mp = _mparams()
+    fake = ctypes.c_void_p(0x200000)
+    # no bank rows, missing ids, misaligned ids
+    assert lib.attnres_selected_fwd(ctypes.byref(mp), fake, 0, fake, fake, fake, fake, fake, None) == 1
+    assert lib.attnres_selected_fwd(ctypes.byref(mp), fake, 4, None, fake, fake, fake, fake, None) == 1
+    assert lib.attnres_selected_fwd(ctypes.byref(mp), fake, 4, ctypes.c_void_p(0x200004), fake, fake, fake,
+                                    fake, None) == 2
+    assert lib.attnres_selected_bwd_workspace_bytes(ctypes.byref(mp), 0) == 0
