@@ -42,6 +42,8 @@ EXPORTED = [
     "attnres_selected_bwd_workspace_bytes",
     "attnres_fwd_partial",
     "attnres_bwd_partial",
+    "attnres_step_host",
+    "attnres_step_host_workspace_bytes",
 ]
 
 
@@ -68,6 +70,29 @@ class AttnresMultiParams(ctypes.Structure):
         ("out_ld_m", ctypes.c_int64),
         ("out_ld_n", ctypes.c_int64),
     ]
+
+
+class _Partial:
+    """A library handle that lacks some entry points (an explicitly loaded
+    older build): declaring a missing function is a no-op, calling it fails."""
+
+    def __init__(self, lib, missing):
+        self._lib = lib
+        self._missing = set(missing)
+
+    def __getattr__(self, name):
+        if name in self._missing:
+            return _Missing(name)
+        return getattr(self._lib, name)
+
+
+class _Missing:
+    def __init__(self, name):
+        self.name = name
+        self.argtypes = self.restype = None
+
+    def __call__(self, *args):
+        raise RuntimeError(f"this build of the library has no {self.name}")
 
 
 class AttnresError(RuntimeError):
@@ -99,6 +124,11 @@ def load(path: str | None = None):
                 f"AttnRes CUDA library not found at {p}; build it with "
                 "`python -m attention_residuals_gb300.build` (needs nvcc for sm_103a)")
         lib = ctypes.CDLL(p)
+        missing = [n for n in EXPORTED if not hasattr(lib, n)]
+        if missing and path is None:
+            raise RuntimeError(f"AttnRes CUDA library at {p} lacks {missing}; rebuild it")
+        if missing:  # an explicitly given older build: declare what it has
+            lib = _Partial(lib, missing)
         P = ctypes.POINTER(AttnresParams)
         vp, fp, i64, sz = ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int64, ctypes.c_size_t
         lib.attnres_fwd.restype = ctypes.c_int
@@ -132,6 +162,11 @@ def load(path: str | None = None):
         lib.attnres_bwd_partial.restype = ctypes.c_int
         lib.attnres_bwd_partial.argtypes = [P, vp, vp, vp, fp, fp, fp, fp, vp, vp, i64,
                                             ctypes.POINTER(ctypes.c_void_p), i64, vp, fp, vp, fp, vp, sz, vp]
+        lib.attnres_step_host_workspace_bytes.restype = sz
+        lib.attnres_step_host_workspace_bytes.argtypes = [P, i64]
+        lib.attnres_step_host.restype = ctypes.c_int
+        lib.attnres_step_host.argtypes = [P, vp, vp, vp, i64, vp, i64, ctypes.POINTER(ctypes.c_void_p), i64, vp,
+                                          fp, vp, fp, i64, vp, sz, ctypes.POINTER(ctypes.c_void_p)]
         i32 = ctypes.c_int32
         lib.attnres_selected_fwd.restype = ctypes.c_int
         lib.attnres_selected_fwd.argtypes = [MP, vp, i32, vp, vp, fp, fp, fp, vp]

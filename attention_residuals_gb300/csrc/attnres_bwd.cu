@@ -49,7 +49,9 @@ __device__ __forceinline__ float ldcg_f32(const float* p) { return __ldcg(p); }
 
 // KEYALL: every channel is a key channel (R == D), so no per-vector masks.
 // FULL: every consumer thread owns VPT whole vectors (D == 8 * VPT * 32 * ncw).
-template <int VPT, bool KEYALL, bool FULL>
+// ADDLAST: a gradient is added to the last source's (a.dlast_add set); a
+// compile-time flag so the plain backward carries none of its code.
+template <int VPT, bool KEYALL, bool FULL, bool ADDLAST>
 __global__ void __launch_bounds__(kMaxThreads, 1) attnres_bwd_kernel(const __grid_constant__ BwdArgs a) {
     extern __shared__ __align__(128) unsigned char smem[];
     const int ncw = a.ncw;
@@ -78,7 +80,6 @@ __global__ void __launch_bounds__(kMaxThreads, 1) attnres_bwd_kernel(const __gri
     const int D = a.D;
     const uint32_t sb = static_cast<uint32_t>(a.slot_bytes);
     const uint32_t cb = static_cast<uint32_t>(G) * sb;
-    const int nchunk = (S + G - 1) / G;  // chunks per pass of one token
 
     if (threadIdx.x == 0) {
         for (int k = 0; k < K; ++k) {
@@ -532,7 +533,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1) attnres_bwd_kernel(const __gri
                                     dq_acc[i][kk] = ffma2(k12, x, dq_acc[i][kk]);
                                 }
                             }
-                            if (a.dlast_add && s == S - 1) {
+                            if (ADDLAST && s == S - 1) {
                                 // gradient reaching the last source from elsewhere (a fused
                                 // block-partial sum's later uses), added before rounding
                                 const uint4 gv = ld_global_nc_v4(reinterpret_cast<const char*>(a.dlast_add) +
@@ -647,9 +648,9 @@ __global__ void __launch_bounds__(256) attnres_finalize_kernel(const float* __re
     }
 }
 
-template <int VPT, bool KEYALL, bool FULL>
+template <int VPT, bool KEYALL, bool FULL, bool ADDLAST>
 cudaError_t launch_bwd_t(const Plan& plan, const BwdArgs& a, cudaStream_t stream) {
-    auto kern = attnres_bwd_kernel<VPT, KEYALL, FULL>;
+    auto kern = attnres_bwd_kernel<VPT, KEYALL, FULL, ADDLAST>;
     cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                            static_cast<int>(plan.smem_bwd));
     if (err != cudaSuccess) return err;
@@ -664,10 +665,15 @@ cudaError_t launch_bwd_t(const Plan& plan, const BwdArgs& a, cudaStream_t stream
 
 template <int VPT>
 cudaError_t dispatch_key(const Plan& plan, const BwdArgs& a, cudaStream_t stream) {
+    if (a.dlast_add)  // the general column form
+        return a.R == a.D ? launch_bwd_t<VPT, true, false, true>(plan, a, stream)
+                          : launch_bwd_t<VPT, false, false, true>(plan, a, stream);
     const bool full = (a.D / 8) == VPT * 32 * plan.b_ncw;
     if (a.R == a.D)
-        return full ? launch_bwd_t<VPT, true, true>(plan, a, stream) : launch_bwd_t<VPT, true, false>(plan, a, stream);
-    return full ? launch_bwd_t<VPT, false, true>(plan, a, stream) : launch_bwd_t<VPT, false, false>(plan, a, stream);
+        return full ? launch_bwd_t<VPT, true, true, false>(plan, a, stream)
+                    : launch_bwd_t<VPT, true, false, false>(plan, a, stream);
+    return full ? launch_bwd_t<VPT, false, true, false>(plan, a, stream)
+                : launch_bwd_t<VPT, false, false, false>(plan, a, stream);
 }
 
 }  // namespace

@@ -45,7 +45,9 @@ namespace {
 __device__ unsigned int g_fwd_error = 0;
 
 // FULL: every consumer thread owns VPT whole vectors (D == 8 * VPT * 32 * ncw).
-template <int VPT, bool FULL>
+// FUSED: the block-partial sum is formed in the read (a.delta set); a
+// compile-time flag so the plain read carries none of its code.
+template <int VPT, bool FULL, bool FUSED>
 __global__ void __launch_bounds__(kMaxThreads, fwd_ctas_per_sm(VPT)) attnres_fwd_kernel(const __grid_constant__ FwdArgs a) {
     extern __shared__ __align__(128) unsigned char smem[];
     const int ncw = a.ncw;
@@ -53,7 +55,7 @@ __global__ void __launch_bounds__(kMaxThreads, fwd_ctas_per_sm(VPT)) attnres_fwd
     const int K = a.chunks;  // ring depth in chunks
     const int G = a.rows;    // rows per chunk
     const int GG = a.group;  // softmax group rows (whole chunks)
-    const int DSL = a.delta ? kDeltaSlots : 0;  // slots for the added rows (fused partial sum)
+    constexpr int DSL = FUSED ? kDeltaSlots : 0;  // slots for the added rows (fused partial sum)
     const SmemLayout L = make_layout(K, G, a.slot_bytes, DSL, a.s_pad, false);
     uint64_t* full = reinterpret_cast<uint64_t*>(smem + L.full);
     uint64_t* empty = reinterpret_cast<uint64_t*>(smem + L.empty);
@@ -424,9 +426,9 @@ __global__ void __launch_bounds__(kMaxThreads, fwd_ctas_per_sm(VPT)) attnres_fwd
     }
 }
 
-template <int VPT, bool FULL>
+template <int VPT, bool FULL, bool FUSED>
 cudaError_t launch_fwd_t(const Plan& plan, const FwdArgs& a, cudaStream_t stream) {
-    auto kern = attnres_fwd_kernel<VPT, FULL>;
+    auto kern = attnres_fwd_kernel<VPT, FULL, FUSED>;
     cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                            static_cast<int>(plan.smem_fwd));
     if (err != cudaSuccess) return err;
@@ -436,8 +438,9 @@ cudaError_t launch_fwd_t(const Plan& plan, const FwdArgs& a, cudaStream_t stream
 
 template <int VPT>
 cudaError_t dispatch_key(const Plan& plan, const FwdArgs& a, cudaStream_t stream) {
+    if (a.delta) return launch_fwd_t<VPT, false, true>(plan, a, stream);  // the general column form
     const bool full = (a.D / 8) == VPT * 32 * plan.ncw;
-    return full ? launch_fwd_t<VPT, true>(plan, a, stream) : launch_fwd_t<VPT, false>(plan, a, stream);
+    return full ? launch_fwd_t<VPT, true, false>(plan, a, stream) : launch_fwd_t<VPT, false, false>(plan, a, stream);
 }
 
 }  // namespace

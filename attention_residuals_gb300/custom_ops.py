@@ -278,3 +278,98 @@ def attnres_selected_op(values, query_bank: Tensor, ids: Tensor, *, eps: float =
     D = vals[0].shape[-1]
     ko = D - query_bank.shape[-1] if key_offset is None else int(key_offset)
     return read_selected_fwd(vals, query_bank, ids, float(eps), float(scale), ko)[0]
+
+
+# --------------------------------------------------------------------------
+# Fused block-partial read ("Fast Attention Residuals", section "Full and
+# Block schedules")
+# --------------------------------------------------------------------------
+@torch.library.custom_op(f"{_NS}::read_block_fwd", mutates_args=(), device_types="cuda")
+def read_block_fwd(values: List[Tensor], delta: Tensor, q: Tensor, w_o: Optional[Tensor], eps: float,
+                   scale: float, key_offset: int) -> Tuple[Tensor, Tensor, Tensor, Tensor, Tensor, Tensor,
+                                                           Tensor]:
+    r = _ops.attnres_partial_fwd(list(values[:-1]), values[-1], delta, q, w_o=w_o, eps=eps, scale=scale,
+                                 key_offset=key_offset)
+    empty = torch.empty((0,), dtype=torch.float32, device=q.device)
+    o_rstd = r["o_rstd"] if r["o_rstd"] is not None else empty
+    o_pre = r["o_pre"] if r["o_pre"] is not None else empty.clone()
+    return r["y"], r["partial_new"], r["alpha"], r["rstd"], r["logit"], o_rstd, o_pre
+
+
+@read_block_fwd.register_fake
+def _(values, delta, q, w_o, eps, scale, key_offset):
+    S, D = len(values), values[0].shape[-1]
+    lead = tuple(values[0].shape[:-1])
+    N = 1
+    for d in lead:
+        N *= d
+    f32 = dict(dtype=torch.float32, device=q.device)
+    y = torch.empty((*lead, D), dtype=torch.bfloat16, device=q.device)
+    pn = torch.empty((*lead, D), dtype=torch.bfloat16, device=q.device)
+    stats = [torch.empty((N, S), **f32) for _ in range(3)]
+    if w_o is not None:
+        o_rstd = torch.empty((N,), **f32)
+        save = not _bwd_resident(S, D, q.numel(), key_offset, True)
+        o_pre = torch.empty((N, D) if save else (0,), **f32)
+    else:
+        o_rstd = torch.empty((0,), **f32)
+        o_pre = torch.empty((0,), **f32)
+    return y, pn, stats[0], stats[1], stats[2], o_rstd, o_pre
+
+
+@torch.library.custom_op(f"{_NS}::read_block_bwd", mutates_args=(), device_types="cuda")
+def read_block_bwd(completed: List[Tensor], partial_new: Tensor, q: Tensor, w_o: Optional[Tensor], dy: Tensor,
+                   g_partial: Optional[Tensor], alpha: Tensor, rstd: Tensor, logit: Tensor, o_rstd: Tensor,
+                   o_pre: Tensor, eps: float, scale: float,
+                   key_offset: int) -> Tuple[List[Tensor], Tensor, Tensor, Tensor]:
+    saved = {"alpha": alpha, "rstd": rstd, "logit": logit,
+             "o_rstd": o_rstd if o_rstd.numel() else None, "o_pre": o_pre if o_pre.numel() else None}
+    g = _ops.attnres_partial_bwd(list(completed), partial_new, q, dy, saved, g_partial=g_partial, w_o=w_o,
+                                 eps=eps, scale=scale, key_offset=key_offset)
+    dw = g["dw_o"] if g["dw_o"] is not None else torch.empty((0,), dtype=torch.bfloat16, device=q.device)
+    return g["d_completed"], g["d_partial"], g["dq"].view_as(q), dw
+
+
+@read_block_bwd.register_fake
+def _(completed, partial_new, q, w_o, dy, g_partial, alpha, rstd, logit, o_rstd, o_pre, eps, scale, key_offset):
+    dw = torch.empty_like(w_o) if w_o is not None else torch.empty((0,), dtype=torch.bfloat16, device=q.device)
+    return [torch.empty_like(c) for c in completed], torch.empty_like(partial_new), torch.empty_like(q), dw
+
+
+def _block_setup_context(ctx, inputs, output):
+    values, delta, q, w_o, eps, scale, key_offset = inputs
+    y, partial_new, alpha, rstd, logit, o_rstd, o_pre = output
+    ctx.cfg = (eps, scale, key_offset)
+    ctx.has_w = w_o is not None
+    ctx.ncomp = len(values) - 1
+    ctx.save_for_backward(q, w_o if w_o is not None else q.new_empty((0,)), partial_new, alpha, rstd, logit,
+                          o_rstd, o_pre, *values[:-1])
+
+
+def _block_backward(ctx, dy, d_partial_new, d_alpha, d_rstd, d_logit, d_orstd, d_opre):
+    q, w_o, partial_new, alpha, rstd, logit, o_rstd, o_pre, *completed = ctx.saved_tensors
+    eps, scale, key_offset = ctx.cfg
+    if dy is None:
+        dy = torch.zeros_like(partial_new)
+    g = None if d_partial_new is None else d_partial_new.to(torch.bfloat16)
+    dcomp, dpart, dq, dw = read_block_bwd(list(completed), partial_new, q, w_o if ctx.has_w else None,
+                                          dy.to(torch.bfloat16), g, alpha, rstd, logit, o_rstd, o_pre, eps,
+                                          scale, key_offset)
+    return list(dcomp) + [dpart], dpart, dq, (dw if ctx.has_w else None), None, None, None
+
+
+read_block_fwd.register_autograd(_block_backward, setup_context=_block_setup_context)
+
+
+def attnres_block_read_op(completed, partial: Tensor, delta: Tensor, query: Tensor, *,
+                          eps: float = _ops.EPS_DEFAULT, scale: float = 1.0,
+                          out_norm_weight: Optional[Tensor] = None, key_offset: Optional[int] = None):
+    """The fused block-partial read through the registered operator."""
+    if isinstance(completed, Tensor):
+        comp = list(completed.unbind(0)) if completed.dim() == partial.dim() + 1 else [completed]
+    else:
+        comp = list(completed)
+    D = partial.shape[-1]
+    ko = D - query.numel() if key_offset is None else int(key_offset)
+    out = read_block_fwd(comp + [partial], delta, query, out_norm_weight, float(eps), float(scale), ko)
+    return out[0], out[1]

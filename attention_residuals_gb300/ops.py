@@ -286,6 +286,173 @@ def attnres_bwd_noalloc(values: Sources, q: torch.Tensor, dy: torch.Tensor, save
 
 
 # --------------------------------------------------------------------------
+# Training step from host memory (pipelined transfers; see attnres_step_host
+# in include/attnres.h)
+# --------------------------------------------------------------------------
+_copy_streams = {}
+
+
+def _host_rows(values) -> tuple:
+    vals = list(values.unbind(0)) if isinstance(values, torch.Tensor) else list(values)
+    D = vals[0].shape[-1]
+    rows = []
+    for v in vals:
+        if v.is_cuda or v.dtype != torch.bfloat16:
+            raise TypeError("host sources must be CPU bf16 tensors (pinned for full speed)")
+        if not v.is_contiguous():
+            raise ValueError("host sources must be contiguous")
+        rows.append(v.view(-1, D))
+    return vals, rows, D
+
+
+def attnres_step_host_workspace_bytes(params: _lib.AttnresParams, chunk_tokens: int) -> int:
+    return int(_lib.load().attnres_step_host_workspace_bytes(ctypes.byref(params), ctypes.c_int64(chunk_tokens)))
+
+
+def attnres_step_host(values, q: torch.Tensor, dy: torch.Tensor, *, w_o: Optional[torch.Tensor] = None,
+                      eps: float = EPS_DEFAULT, scale: float = 1.0, key_offset: Optional[int] = None,
+                      chunk_tokens: int = 4096, out: Optional[dict] = None,
+                      workspace: Optional[torch.Tensor] = None, device=None) -> dict:
+    """Forward + backward of the read with every input and output in host
+    memory (page-locked CPU tensors), transfers overlapped with the kernels
+    chunk by chunk.  Asynchronous on the current CUDA stream (synchronise it
+    before reading the outputs).  Returns host tensors y, dvalues (a list),
+    dq, dq_f32, dw_o, dw_o_f32."""
+    vals, rows, D = _host_rows(values)
+    S = len(rows)
+    N = rows[0].shape[0]
+    R = q.numel()
+    dev = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
+    p = _lib.AttnresParams()
+    p.S, p.D, p.R = S, D, R
+    p.key_offset = D - R if key_offset is None else int(key_offset)
+    p.N, p.eps, p.scale = N, float(eps), float(scale)
+    p.out_norm = 1 if w_o is not None else 0
+    p.split_n_threshold, p.src_ld = 0, D
+    for i, r in enumerate(rows):
+        p.src[i] = r.data_ptr()
+    o = dict(out or {})
+    pin = dict(dtype=torch.bfloat16, pin_memory=True)
+    y = o.get("y") if o.get("y") is not None else torch.empty((N, D), **pin)
+    dv = o.get("dvalues") if o.get("dvalues") is not None else [torch.empty((N, D), **pin) for _ in range(S)]
+    dq = o.get("dq") if o.get("dq") is not None else torch.empty((R,), **pin)
+    dq32 = o.get("dq_f32") if o.get("dq_f32") is not None else torch.empty((R,), dtype=torch.float32,
+                                                                           pin_memory=True)
+    dw = dw32 = None
+    if w_o is not None:
+        dw = o.get("dw_o") if o.get("dw_o") is not None else torch.empty((D,), **pin)
+        dw32 = o.get("dw_o_f32") if o.get("dw_o_f32") is not None else torch.empty((D,), dtype=torch.float32,
+                                                                                   pin_memory=True)
+    need = attnres_step_host_workspace_bytes(p, chunk_tokens)
+    if workspace is None or workspace.numel() < need:
+        workspace = torch.empty((max(need, 256),), dtype=torch.uint8, device=dev)
+    if dev.index not in _copy_streams:
+        _copy_streams[dev.index] = (torch.cuda.Stream(dev), torch.cuda.Stream(dev))
+    s_in, s_out = _copy_streams[dev.index]
+    streams = (ctypes.c_void_p * 3)(torch.cuda.current_stream(dev).cuda_stream, s_in.cuda_stream,
+                                    s_out.cuda_stream)
+    dptrs = (ctypes.c_void_p * S)(*[d.data_ptr() for d in dv])
+    # keep every host buffer the enqueued copies read alive with the result
+    keep = (q.contiguous(), None if w_o is None else w_o.contiguous(), dy.reshape(N, D).contiguous())
+    rc = _lib.load().attnres_step_host(
+        ctypes.byref(p), _ptr(keep[0]), _ptr(keep[1]),
+        _ptr(keep[2]), ctypes.c_int64(D), _ptr(y), ctypes.c_int64(D), dptrs, ctypes.c_int64(D),
+        _ptr(dq), _ptr(dq32), _ptr(dw), _ptr(dw32), ctypes.c_int64(chunk_tokens), _ptr(workspace),
+        ctypes.c_size_t(workspace.numel()), streams)
+    _lib.check(rc, "attnres_step_host")
+    return {"y": y, "dvalues": dv, "dq": dq, "dq_f32": dq32, "dw_o": dw, "dw_o_f32": dw32,
+            "workspace": workspace, "inputs": (vals, keep)}
+
+
+# --------------------------------------------------------------------------
+# Fused block-partial read ("Fast Attention Residuals", section "Full and
+# Block schedules": the caller's partial-block sum formed inside the read)
+# --------------------------------------------------------------------------
+def _row2d(t: torch.Tensor, N: int, D: int, name: str) -> torch.Tensor:
+    if t.dtype != torch.bfloat16 or not t.is_cuda or t.numel() != N * D:
+        raise TypeError(f"{name} must be a CUDA bf16 tensor shaped like one source")
+    r = t.reshape(N, D)
+    return r if (r.is_contiguous() and r.data_ptr() % 16 == 0) else r.contiguous()
+
+
+def attnres_partial_fwd(completed: Sources, partial: torch.Tensor, delta: torch.Tensor, q: torch.Tensor, *,
+                        w_o: Optional[torch.Tensor] = None, eps: float = EPS_DEFAULT, scale: float = 1.0,
+                        key_offset: Optional[int] = None, partial_out: Optional[torch.Tensor] = None,
+                        stream=None) -> dict:
+    """Fused block-partial forward: partial_new = partial + delta (bf16 add)
+    is formed inside the read of (completed..., partial_new).  Returns y,
+    partial_new and the saved statistics (as attnres_fwd).  partial_out may
+    be given (even `partial` itself, for an in-place update)."""
+    comp = [completed] if isinstance(completed, torch.Tensor) and completed.dim() == partial.dim() else completed
+    comp = list(comp.unbind(0)) if isinstance(comp, torch.Tensor) else list(comp)
+    view = _source_view(comp + [partial])
+    N, D = view.N, view.D
+    R = q.numel()
+    q = _check_vec(q, R, "q")
+    w_o = _check_vec(w_o, D, "w_o")
+    d2 = _row2d(delta, N, D, "delta")
+    pout = torch.empty((N, D), dtype=torch.bfloat16, device=view.rows[0].device) if partial_out is None \
+        else _row2d(partial_out, N, D, "partial_out")
+    p = make_params(view, R, key_offset=key_offset, eps=eps, scale=scale, out_norm=w_o is not None)
+    S, dev = len(view.rows), view.rows[0].device
+    f32 = dict(dtype=torch.float32, device=dev)
+    y = torch.empty((N, D), dtype=torch.bfloat16, device=dev)
+    alpha, rstd, logit = (torch.empty((N, S), **f32) for _ in range(3))
+    o_rstd = o_pre = None
+    if w_o is not None:
+        o_rstd = torch.empty((N,), **f32)
+        if N > 0 and not _plan(p)["bwd_resident"]:
+            o_pre = torch.empty((N, D), **f32)
+    rc = _lib.load().attnres_fwd_partial(ctypes.byref(p), _ptr(q), _ptr(w_o), _ptr(d2), ctypes.c_int64(D),
+                                         _ptr(pout), ctypes.c_int64(D), _ptr(y), _ptr(alpha), _ptr(rstd),
+                                         _ptr(logit), _ptr(o_rstd), _ptr(o_pre), _stream(stream))
+    _lib.check(rc, "attnres_fwd_partial")
+    shape = (*view.lead_shape, D)
+    return {"y": y.view(shape), "partial_new": pout.view(shape), "alpha": alpha, "rstd": rstd,
+            "logit": logit, "o_rstd": o_rstd, "o_pre": o_pre}
+
+
+def attnres_partial_bwd(completed: Sources, partial_new: torch.Tensor, q: torch.Tensor, dy: torch.Tensor,
+                        saved: dict, *, g_partial: Optional[torch.Tensor] = None,
+                        w_o: Optional[torch.Tensor] = None, eps: float = EPS_DEFAULT, scale: float = 1.0,
+                        key_offset: Optional[int] = None, stream=None) -> dict:
+    """Backward of the fused block-partial read.  Returns d_completed (a
+    list), d_partial (the gradient of both `partial` and `delta`, including
+    g_partial, the gradient reaching partial_new from its later uses), dq
+    and dw_o (bf16 and fp32)."""
+    comp = list(completed.unbind(0)) if (isinstance(completed, torch.Tensor) and
+                                         completed.dim() == partial_new.dim() + 1) else list(completed)
+    view = _source_view(comp + [partial_new])
+    N, D = view.N, view.D
+    R = q.numel()
+    q = _check_vec(q, R, "q")
+    w_o = _check_vec(w_o, D, "w_o")
+    p = make_params(view, R, key_offset=key_offset, eps=eps, scale=scale, out_norm=w_o is not None)
+    S, dev = len(view.rows), view.rows[0].device
+    dy2 = _row2d(dy, N, D, "dy")
+    g2 = None if g_partial is None else _row2d(g_partial, N, D, "g_partial")
+    drows = [torch.empty((N, D), dtype=torch.bfloat16, device=dev) for _ in range(S)]
+    dptrs = (ctypes.c_void_p * S)(*[r.data_ptr() for r in drows])
+    dq = torch.empty((R,), dtype=torch.bfloat16, device=dev)
+    dq32 = torch.empty((R,), dtype=torch.float32, device=dev)
+    dw = dw32 = None
+    if w_o is not None:
+        dw = torch.empty((D,), dtype=torch.bfloat16, device=dev)
+        dw32 = torch.empty((D,), dtype=torch.float32, device=dev)
+    need = attnres_bwd_workspace_bytes(p)
+    ws = torch.empty((max(need, 16),), dtype=torch.uint8, device=dev)
+    rc = _lib.load().attnres_bwd_partial(
+        ctypes.byref(p), _ptr(q), _ptr(w_o), _ptr(dy2), _ptr(saved["alpha"]), _ptr(saved["rstd"]),
+        _ptr(saved["logit"]), _ptr(saved.get("o_rstd")), _ptr(saved.get("o_pre")), _ptr(g2),
+        ctypes.c_int64(D), dptrs, ctypes.c_int64(D), _ptr(dq), _ptr(dq32), _ptr(dw), _ptr(dw32), _ptr(ws),
+        ctypes.c_size_t(ws.numel()), _stream(stream))
+    _lib.check(rc, "attnres_bwd_partial")
+    shape = (*view.lead_shape, D)
+    return {"d_completed": [r.view(shape) for r in drows[:-1]], "d_partial": drows[-1].view(shape),
+            "dq": dq, "dq_f32": dq32, "dw_o": dw, "dw_o_f32": dw32}
+
+
+# --------------------------------------------------------------------------
 # Multi-query read ("Fast Attention Residuals", section "Multi-query AttnRes")
 # --------------------------------------------------------------------------
 _MULTI_PLAN_KEYS = ["grid", "consumer_warps", "vectors_per_thread", "query_blocks", "fwd_ring",
@@ -521,3 +688,17 @@ def attnres_selected(values: Sources, query_bank: torch.Tensor, ids: torch.Tenso
     operators, so torch.compile(fullgraph=True) and CUDA graphs work."""
     from .custom_ops import attnres_selected_op
     return attnres_selected_op(values, query_bank, ids, eps=eps, scale=scale, key_offset=key_offset)
+
+
+def attnres_block_read(completed: Sources, partial: torch.Tensor, delta: torch.Tensor, query: torch.Tensor,
+                       *, eps: float = EPS_DEFAULT, scale: float = 1.0,
+                       out_norm_weight: Optional[torch.Tensor] = None, key_offset: Optional[int] = None):
+    """Block-schedule read with the partial-block sum fused in: returns
+    (attnres((*completed, partial + delta), query), partial + delta), the
+    sum formed inside the read (one [..., D] pass less than summing first).
+    completed: packed [S-1, ..., D] or a list of [..., D] completed block
+    sums (the embedding first); partial: the current partial sum; delta:
+    the newest writer output.  Differentiable in every tensor argument."""
+    from .custom_ops import attnres_block_read_op
+    return attnres_block_read_op(completed, partial, delta, query, eps=eps, scale=scale,
+                                 out_norm_weight=out_norm_weight, key_offset=key_offset)

@@ -252,37 +252,38 @@ class LongRead:
                            wl.dy if dy is None else dy, self.f, w_o=wl.w_o if w is None else w,
                            key_offset=wl.key_offset, workspace=self.ws, dvalues=self.dv, stream=stream)
 
-    def e2e(self, stream):
-        """A step through the same API from pinned host buffers: inputs copied
-        in, fwd + bwd, every output copied back."""
+    def e2e(self, stream, chunk_tokens=8192):
+        """A step through the C ABI's host-buffer call (attnres_step_host):
+        sources, query, weight and dy in page-locked host memory, y,
+        dvalues, dq and dw_o copied back to it, transfers overlapped with
+        the kernels chunk by chunk."""
         import torch
+        from attention_residuals_gb300 import attnres_step_host
         wl = self.wl
         v, q, w, dy = wl.values, wl.q, wl.w_o, wl.dy
-        N, D, R = wl.N, wl.D, wl.R
-        h = {"v": torch.empty(v.shape, dtype=v.dtype, pin_memory=True), "q": q.cpu().pin_memory(),
-             "w": w.cpu().pin_memory(), "dy": torch.empty(dy.shape, dtype=dy.dtype, pin_memory=True),
-             "y": torch.empty((N, D), dtype=torch.bfloat16, pin_memory=True),
-             "dv": torch.empty(v.shape, dtype=v.dtype, pin_memory=True),
-             "dq": torch.empty((R,), dtype=torch.bfloat16, pin_memory=True),
-             "dw": torch.empty((D,), dtype=torch.bfloat16, pin_memory=True)}
+        S, N, D, R = wl.S, wl.N, wl.D, wl.R
+        pin = dict(pin_memory=True)
+        h = {"v": torch.empty(v.shape, dtype=v.dtype, **pin), "q": q.cpu().pin_memory(),
+             "w": w.cpu().pin_memory(), "dy": torch.empty(dy.shape, dtype=dy.dtype, **pin)}
         h["v"].copy_(v)
         h["dy"].copy_(dy)
-        d = {"v": torch.empty_like(v), "q": torch.empty_like(q), "w": torch.empty_like(w),
-             "dy": torch.empty_like(dy)}
+        out = {"y": torch.empty((N, D), dtype=torch.bfloat16, **pin),
+               "dvalues": [torch.empty((N, D), dtype=torch.bfloat16, **pin) for _ in range(S)],
+               "dq": torch.empty((R,), dtype=torch.bfloat16, **pin),
+               "dq_f32": torch.empty((R,), dtype=torch.float32, **pin),
+               "dw_o": torch.empty((D,), dtype=torch.bfloat16, **pin),
+               "dw_o_f32": torch.empty((D,), dtype=torch.float32, **pin)}
+        ws = {}
 
         def step():
-            for k in ("v", "q", "w", "dy"):
-                d[k].copy_(h[k], non_blocking=True)
-            self.fwd(stream, d["v"], d["q"], d["w"])
-            b = self.bwd(stream, d["v"], d["q"], d["w"], d["dy"])
-            h["y"].copy_(self.out["y"], non_blocking=True)
-            h["dv"].copy_(self.dv, non_blocking=True)
-            h["dq"].copy_(b["dq"], non_blocking=True)
-            h["dw"].copy_(b["dw_o"], non_blocking=True)
+            r = attnres_step_host(h["v"], h["q"], h["dy"], w_o=h["w"], key_offset=wl.key_offset,
+                                  chunk_tokens=chunk_tokens, out=out, workspace=ws.get("t"))
+            ws["t"] = r["workspace"]
 
         h2d = sum(h[k].numel() for k in ("v", "q", "w", "dy")) * 2
-        d2h = sum(h[k].numel() for k in ("y", "dv", "dq", "dw")) * 2
-        return step, h2d, d2h, h
+        d2h = (out["y"].numel() + S * N * D + R + D) * 2 + (R + D) * 4
+        self.e2e_detail = {"api": "attnres_step_host (C ABI, host buffers)", "chunk_tokens": chunk_tokens}
+        return step, h2d, d2h, (h, out, ws)
 
     def traffic(self):
         return profiled_traffic("cfg3")
@@ -511,7 +512,8 @@ def run_ours(args):
     # ---------------------------------------------------------- end to end
     e2e = None
     if not args.no_e2e:
-        e2e_step, h2d, d2h, host = work.e2e(stream)
+        e2e_step, h2d, d2h, host = (work.e2e(stream, args.e2e_chunk) if work.key == "long"
+                                    else work.e2e(stream))
         e2e_step()
         torch.cuda.synchronize()
         KE = max(1, min(args.e2e_steps, K))
@@ -529,7 +531,9 @@ def run_ours(args):
         if pg is not None:
             e2e_ms = max_over_ranks([e2e_ms], device=dev)[0]
         e2e = {"value": weak_scaling_throughput(nbytes["total"], world, e2e_ms), "unit": "GB/s",
-               "ms_per_step": e2e_ms, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+               "ms_per_step": e2e_ms, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+               "host_link_gbs": (h2d + d2h) / (e2e_ms * 1e-3) / 1e9}
+        e2e.update(getattr(work, "e2e_detail", {}))
         del host
 
     # ---------------------------------------------------------- CPU baseline
@@ -594,6 +598,8 @@ def main(argv=None):
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", choices=sorted(WORKLOADS), default="long")
     ap.add_argument("--e2e-steps", type=int, default=5)
+    ap.add_argument("--e2e-chunk", type=int, default=8192,
+                    help="tokens per chunk of the host-buffer step (long workload)")
     ap.add_argument("--cpu-tokens", type=int, default=8192)
     ap.add_argument("--ref-tokens", type=int, default=1024)
     ap.add_argument("--no-e2e", action="store_true")

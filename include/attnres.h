@@ -222,6 +222,40 @@ attnres_status attnres_bwd_noalloc(const attnres_params* p, const void* q, const
                                    void* dw_o, float* dw_o_f32, void* stream);
 
 /*
+ * Training step from host memory: attnres_fwd + attnres_bwd over all N
+ * tokens with the sources and dy in HOST memory and every result written
+ * back to HOST memory.  Tokens are independent ("Fast Attention Residuals",
+ * section "Equation"), so the step runs over chunks of chunk_tokens tokens
+ * with double-buffered device staging on three streams: streams[1] copies
+ * chunk c+1 in, streams[0] runs chunk c's kernels, streams[2] copies chunk
+ * c-1's y and dvalues out, so both copy directions and the kernels overlap.
+ * dq and dw_o sum every chunk's FP32 sums in chunk order (reproducible).
+ *   p          as for attnres_fwd, except src[s] are HOST pointers (pinned
+ *              memory gives asynchronous full-speed copies; pageable memory
+ *              works but each copy then blocks the host)
+ *   q, w_o     HOST bf16 [R] and [D] (w_o iff out_norm)
+ *   dy         HOST bf16 rows at dy + n * dy_ld
+ *   y          HOST bf16 rows at y + n * y_ld (written)
+ *   dsrc[s]    HOST bf16 rows at dsrc[s] + n * dsrc_ld (written)
+ *   dq, dq_f32, dw_o, dw_o_f32   HOST, written (the FP32 copies may be NULL;
+ *              dw_o required iff out_norm)
+ *   workspace  DEVICE, at least attnres_step_host_workspace_bytes(p,
+ *              chunk_tokens) bytes, 256-byte aligned
+ *   streams    three cudaStream_t (entries may repeat; NULL = legacy default)
+ * Asynchronous: returns once everything is enqueued; streams[0] waits for the
+ * other two at its end, so synchronising streams[0] (or an event recorded on
+ * it after the call) completes the step.  Host buffers must stay valid and
+ * untouched until then.  The per-token statistics stay on the device.
+ * Errors: as attnres_fwd and attnres_bwd, plus WORKSPACE.
+ */
+size_t attnres_step_host_workspace_bytes(const attnres_params* p, int64_t chunk_tokens);
+attnres_status attnres_step_host(const attnres_params* p, const void* q, const void* w_o,
+                                 const void* dy, int64_t dy_ld, void* y, int64_t y_ld,
+                                 void* const* dsrc, int64_t dsrc_ld, void* dq, float* dq_f32,
+                                 void* dw_o, float* dw_o_f32, int64_t chunk_tokens, void* workspace,
+                                 size_t workspace_bytes, void* const* streams);
+
+/*
  * Kernels bound every wait on a shared-memory barrier.  A wait that runs out
  * of time makes the kernel record a nonzero code here and finish without
  * further waiting (its outputs are then garbage); so does a selected-query

@@ -1,0 +1,123 @@
+"""GPU parity of the fused block-partial read ("Fast Attention Residuals",
+section "Full and Block schedules": the caller's partial-block sum formed
+inside the read) through the C ABI, against the FP64 oracle.
+
+partial_new = partial + delta is integer-exact work (one bf16 rounding of an
+FP32 sum) and is compared bit for bit; the read and its gradients use the
+single-query tolerances (parity_utils).  Shapes cover the block workload
+(eight completed block sums plus the partial, sliced key), the output norm,
+both key placements, one source only (no completed block), the streaming
+backward (rows too large to stay resident), in-place updates of the partial
+sum, and autograd through torch.compile with the new partial sum used
+downstream.
+"""
+import numpy as np
+import pytest
+import torch
+
+from attention_residuals_gb300 import (attnres_block_read, attnres_check_device_error,
+                                       attnres_partial_bwd, attnres_partial_fwd, attnres_plan_info)
+from attention_residuals_gb300.workloads import make_random
+from oracle.partial import attnres_partial_oracle, partial_sum_bits
+from parity_utils import (ALPHA_ABS, GRAD_REL_L2, STAT_REL, Y_REL, bf16_rne, rel_l2, to_np, y_rel_err)
+
+pytestmark = pytest.mark.gpu
+
+
+def _bits(t):
+    return t.detach().cpu().contiguous().view(torch.int16).numpy().view(np.uint16)
+
+
+def _case(S, N, D, R, ko, out_norm, seed):
+    wl = make_random(S + 1, N, D, R, key_offset=ko, out_norm=out_norm, seed=seed)
+    completed, partial, delta = wl.values[:S - 1], wl.values[S - 1], wl.values[S]
+    g = torch.Generator().manual_seed(seed + 1)
+    gp = torch.randn(N, D, generator=g).to(torch.bfloat16)
+    return wl, completed, partial, delta, gp
+
+
+SHAPES = [
+    # S (sources incl. the partial), N, D, R, ko, out_norm
+    (9, 263, 4096, 1024, 0, False),     # block workload shape, first R channels
+    (9, 263, 4096, 1024, 3072, False),  # final R channels (the page's placement)
+    (10, 157, 4096, 4096, 0, True),     # output norm
+    (1, 77, 1024, 1024, 0, False),      # the partial sum alone
+    (5, 301, 2048, 512, 1536, True),
+    (40, 9, 8192, 8192, 0, True),       # streaming backward
+]
+
+
+@pytest.mark.parametrize("S,N,D,R,ko,out_norm", SHAPES)
+def test_partial_matches_oracle(S, N, D, R, ko, out_norm):
+    wl, completed, partial, delta, gp = _case(S, N, D, R, ko, out_norm, seed=S * 13 + R)
+    q = wl.q.cuda()
+    w = wl.w_o.cuda() if out_norm else None
+    comp_d = [c.cuda() for c in completed]
+    fwd = attnres_partial_fwd(comp_d, partial.cuda(), delta.cuda(), q, w_o=w, key_offset=ko)
+    bwd = attnres_partial_bwd(comp_d, fwd["partial_new"], q, wl.dy.cuda(), fwd, g_partial=gp.cuda(), w_o=w,
+                              key_offset=ko)
+    torch.cuda.synchronize()
+    attnres_check_device_error()
+    ref = attnres_partial_oracle(completed, partial, delta, wl.q, w_o=wl.w_o, dy=wl.dy, g_partial=gp,
+                                 key_offset=ko)
+    np.testing.assert_array_equal(_bits(fwd["partial_new"]), partial_sum_bits(partial, delta))
+    errs = {"y": y_rel_err(to_np(fwd["y"]), ref["y"]),
+            "alpha": float(np.max(np.abs(to_np(fwd["alpha"]) - ref["alpha"]))),
+            "rstd": float(np.max(np.abs(to_np(fwd["rstd"]) / ref["rstd"] - 1)))}
+    assert errs["y"] <= Y_REL and errs["alpha"] <= ALPHA_ABS and errs["rstd"] <= STAT_REL, errs
+    if S > 1:
+        errs["d_completed"] = rel_l2(to_np(torch.stack(bwd["d_completed"])), ref["d_completed"])
+        assert errs["d_completed"] <= GRAD_REL_L2, errs
+    errs["d_partial"] = rel_l2(to_np(bwd["d_partial"]), ref["d_partial"])
+    errs["dq_f32"] = rel_l2(to_np(bwd["dq_f32"]), ref["dq"])
+    assert errs["d_partial"] <= GRAD_REL_L2 and errs["dq_f32"] <= GRAD_REL_L2, errs
+    np.testing.assert_array_equal(to_np(bwd["dq"]), bf16_rne(to_np(bwd["dq_f32"])))
+    if out_norm:
+        errs["dw_o_f32"] = rel_l2(to_np(bwd["dw_o_f32"]), ref["dw_o"])
+        assert errs["dw_o_f32"] <= GRAD_REL_L2, errs
+    print(attnres_plan_info(comp_d + [fwd["partial_new"]], R, key_offset=ko, out_norm=out_norm), errs)
+
+
+def test_partial_in_place_update_and_no_extra_gradient():
+    wl, completed, partial, delta, gp = _case(6, 500, 2048, 2048, 0, False, seed=5)
+    q = wl.q.cuda()
+    comp_d = [c.cuda() for c in completed]
+    out_of_place = attnres_partial_fwd(comp_d, partial.cuda(), delta.cuda(), q, key_offset=0)
+    acc = partial.cuda().clone()
+    in_place = attnres_partial_fwd(comp_d, acc, delta.cuda(), q, key_offset=0, partial_out=acc)
+    torch.cuda.synchronize()
+    assert torch.equal(acc, out_of_place["partial_new"])
+    assert torch.equal(in_place["y"], out_of_place["y"])
+    # without g_partial the last gradient is the read's alone
+    b = attnres_partial_bwd(comp_d, acc, q, wl.dy.cuda(), in_place, key_offset=0)
+    ref = attnres_partial_oracle(completed, partial, delta, wl.q, dy=wl.dy, key_offset=0)
+    assert rel_l2(to_np(b["d_partial"]), ref["d_partial"]) <= GRAD_REL_L2
+
+
+@pytest.mark.parametrize("out_norm", [False, True])
+def test_block_read_autograd_compile(out_norm):
+    torch._dynamo.reset()
+    wl, completed, partial, delta, gp = _case(5, 96, 1024, 256, 768, out_norm, seed=31 + out_norm)
+    comp = completed.cuda().requires_grad_(True)
+    part = partial.cuda().requires_grad_(True)
+    dl = delta.cuda().requires_grad_(True)
+    q = wl.q.cuda().requires_grad_(True)
+    w = wl.w_o.cuda().requires_grad_(True) if out_norm else None
+
+    def step(c, p, d, qq, ww):
+        y, pn = attnres_block_read(c, p, d, qq, out_norm_weight=ww)
+        return y, pn
+
+    f = torch.compile(step, fullgraph=True, dynamic=False)
+    y, pn = f(comp, part, dl, q, w)
+    torch.autograd.backward([y, pn], [wl.dy.cuda(), gp.cuda()])
+    torch.cuda.synchronize()
+    ref = attnres_partial_oracle(completed, partial, delta, wl.q, w_o=wl.w_o, dy=wl.dy, g_partial=gp,
+                                 key_offset=768)
+    np.testing.assert_array_equal(_bits(pn), partial_sum_bits(partial, delta))
+    assert y_rel_err(to_np(y), ref["y"]) <= Y_REL
+    assert rel_l2(to_np(comp.grad), ref["d_completed"]) <= GRAD_REL_L2
+    assert rel_l2(to_np(part.grad), ref["d_partial"]) <= GRAD_REL_L2
+    assert torch.equal(part.grad, dl.grad)
+    # autograd hands back the bf16 dq; its rounding alone is up to 2^-8 per element
+    assert rel_l2(to_np(q.grad), ref["dq"]) <= 4e-3
