@@ -64,7 +64,8 @@ attnres_status check_shape(const attnres_params* p) {
 }
 
 // fused: the forward also streams one added row per token (block-partial sum).
-attnres_status make_plan(const attnres_params* p, Plan* plan, bool fused = false) {
+// addlast: the backward also streams one added gradient row per token.
+attnres_status make_plan(const attnres_params* p, Plan* plan, bool fused = false, bool addlast = false) {
     DeviceInfo dev;
     if (!device_info(&dev)) return ATTNRES_ERR_CUDA;
     Plan pl{};
@@ -120,7 +121,8 @@ attnres_status make_plan(const attnres_params* p, Plan* plan, bool fused = false
     // chunks, at most ~60% of the ring so the next token can load meanwhile)
     // or streamed chunks (at least four in the ring).
     {
-        pl.dy_slots = sb > 8192 ? 2 : 4;
+        // dy slots: two tokens in flight (an added gradient row takes a slot too)
+        pl.dy_slots = (sb > 8192 && !addlast) ? 2 : 4;
         const long long fixed = make_layout(0, 1, pl.slot_bytes, pl.dy_slots, pl.s_pad, true).total + 64;
         const long long avail = optin - fixed;
         pl.resident = (static_cast<long long>(S) * sb * 10 <= avail * 6) ? 1 : 0;
@@ -290,8 +292,8 @@ attnres_status make_multi_plan(const attnres_multi_params* p, MultiPlan* plan, i
     pl.b_ncw = (ncv + 32 * pl.b_vpt - 1) / (32 * pl.b_vpt);
     pl.mb_b = p2 < 2 / pl.b_vpt ? p2 : 2 / pl.b_vpt;
     const int nmb = (M + pl.mb_b - 1) / pl.mb_b;
-    const bool regblock = nmb == 1 && E == 0;
-    const int dq_nkv = regblock ? 0 : pl.nkv;
+    const bool dq_in_smem = nmb > 1 || E > 0;
+    const int dq_nkv = dq_in_smem ? pl.nkv : 0;
     const int dq_rows = E > 0 ? E : M;
     pl.E = E;
     pl.bwd_ok = 0;
@@ -474,7 +476,7 @@ static attnres_status bwd_impl(const attnres_params* p, const void* q, const voi
     st = check_dsrc(p, dsrc, dsrc_ld);
     if (st != ATTNRES_OK) return st;
     Plan pl;
-    st = make_plan(p, &pl);
+    st = make_plan(p, &pl, false, g_last != nullptr);
     if (st != ATTNRES_OK) return st;
     if (!workspace || workspace_bytes < pl.ws_bytes) return ATTNRES_ERR_WORKSPACE;
     if (!aligned16(workspace)) return ATTNRES_ERR_ALIGNMENT;

@@ -146,6 +146,19 @@ __global__ void __launch_bounds__(kMaxThreads, 1) attnres_bwd_kernel(const __gri
                         dk = 0;
                         dphase ^= 1u;
                     }
+                    if constexpr (ADDLAST) {
+                        // the gradient added to the last source rides in the next dy slot
+                        if (mbar_wait(dyempty + dk, dphase ^ 1u, abort_flag, &g_bwd_error, kSiteBwdProducer)) {
+                            mbar_arrive_expect_tx(dyfull + dk, row_bytes);
+                            tma_load_1d(dyring + dk * sb, a.dlast_add + n * a.dlast_add_ld, row_bytes, dyfull + dk,
+                                        pol);
+                            ++dy_issued;
+                            if (++dk == DS) {
+                                dk = 0;
+                                dphase ^= 1u;
+                            }
+                        }
+                    }
                 }
                 for (int pass = 0; pass < npass && !*abort_flag; ++pass) {
                     const bool keys = !a.resident && pass == npass - 1;
@@ -291,6 +304,16 @@ __global__ void __launch_bounds__(kMaxThreads, 1) attnres_bwd_kernel(const __gri
             }
             __syncwarp();
             if (lane == 0) mbar_arrive_after(dyempty_s + 8u * dk, dep);
+            if (++dk == DS) {
+                dk = 0;
+                dphase ^= 1u;
+            }
+        }
+        // the added gradient's slot (held until the write pass has used it)
+        int gk = 0;
+        if constexpr (ADDLAST) {
+            gk = dk;
+            mbar_wait_s(dyfull_s + 8u * dk, dphase, abort_flag, &g_bwd_error, kSiteBwdConsumer);
             if (++dk == DS) {
                 dk = 0;
                 dphase ^= 1u;
@@ -484,6 +507,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1) attnres_bwd_kernel(const __gri
         }
 
         // ---- write pass: dv_s rows and dq contributions
+        uint32_t gdep = 0;  // data dependency of the added gradient's loads
         {
             int k = a.resident ? tk_ck : ck;
             uint32_t ph = a.resident ? tk_phase : cphase;
@@ -536,8 +560,8 @@ __global__ void __launch_bounds__(kMaxThreads, 1) attnres_bwd_kernel(const __gri
                             if (ADDLAST && s == S - 1) {
                                 // gradient reaching the last source from elsewhere (a fused
                                 // block-partial sum's later uses), added before rounding
-                                const uint4 gv = ld_global_nc_v4(reinterpret_cast<const char*>(a.dlast_add) +
-                                                                 (n * a.dlast_add_ld * 2 + d_off) + i * vstep);
+                                const uint4 gv = lds128(dy_lo + gk * sb + i * vstep);
+                                gdep ^= gv.x;
 #pragma unroll
                                 for (int kk = 0; kk < 4; ++kk)
                                     dv[kk] = ffma2(make_float2(1.0f, 1.0f), bf2_to_f2(u4_get(gv, kk)), dv[kk]);
@@ -555,6 +579,10 @@ __global__ void __launch_bounds__(kMaxThreads, 1) attnres_bwd_kernel(const __gri
             ck = k;
             cphase = ph;
             cbase = base;
+        }
+        if constexpr (ADDLAST) {
+            __syncwarp();
+            if (lane == 0) mbar_arrive_after(dyempty_s + 8u * gk, gdep);
         }
     }
 

@@ -58,12 +58,15 @@ __global__ void __launch_bounds__(kMultiBwdThreads, 1) attnres_multi_bwd_kernel(
     const int s_pad = a.s_pad, m_pad = a.m_pad;
     const int nmb = (M + MB - 1) / MB;
     const bool selected = a.ids != nullptr;  // per-token queries from a bank
-    // one register block of fixed queries: q and dq live in registers;
-    // otherwise q comes from shared memory and dq sums go to shared memory
-    const bool regblock = nmb == 1 && !selected;
+    // one register block: q and the token's dq live in registers (fixed
+    // queries: dq for the whole launch; selected queries: q reloaded and dq
+    // added to the bank row's shared-memory sums per token); several blocks:
+    // q comes from shared memory per row and dq sums go to shared memory
+    const bool regblock = nmb == 1;
+    const bool dq_in_smem = !regblock || selected;
     const int QR = selected ? a.E : M;       // rows of dq (queries or bank rows)
     const MultiLayout L =
-        make_multi_layout(K, G, a.slot_bytes, M, DS, s_pad, m_pad, a.nkv, regblock ? 0 : a.nkv, true, QR);
+        make_multi_layout(K, G, a.slot_bytes, M, DS, s_pad, m_pad, a.nkv, dq_in_smem ? a.nkv : 0, true, QR);
     uint64_t* full = reinterpret_cast<uint64_t*>(smem + L.full);
     uint64_t* empty = reinterpret_cast<uint64_t*>(smem + L.empty);
     uint64_t* dyfull = reinterpret_cast<uint64_t*>(smem + L.dyfull);
@@ -106,7 +109,7 @@ __global__ void __launch_bounds__(kMultiBwdThreads, 1) attnres_multi_bwd_kernel(
     }
     // coefficients of padded queries stay zero; dq sums start at zero
     for (int i = threadIdx.x; i < 2 * s_pad * m_pad; i += blockDim.x) al_t[i] = 0.0f;
-    if (!regblock)
+    if (dq_in_smem)
         for (int i = threadIdx.x; i < QR * a.nkv * 8; i += blockDim.x) dqsm[i] = 0.0f;
     __syncthreads();
 
@@ -232,8 +235,23 @@ __global__ void __launch_bounds__(kMultiBwdThreads, 1) attnres_multi_bwd_kernel(
         return static_cast<int>(id);
     };
     // queries by key channel into shared memory (token n's bank rows when selected)
+    const bool q_vec = ((ko | kend) & 7) == 0 && (reinterpret_cast<uintptr_t>(a.q) & 15u) == 0;
     auto load_q = [&](long long n) {
         uint16_t* qsm = reinterpret_cast<uint16_t*>(smem + L.qsm);
+        if (q_vec) {
+            // aligned key: whole 16-byte vectors of each query (bank) row
+#pragma unroll 4
+            for (int i = threadIdx.x; i < m_pad * nkv; i += nct) {
+                const int m = i / nkv;
+                uint4 w = make_uint4(0u, 0u, 0u, 0u);
+                if (m < M) {
+                    const int row = selected ? bank_row(n, m) : m;
+                    if (row >= 0) w = ld_global_nc_v4(a.q + static_cast<long long>(row) * a.R + 8 * (i - m * nkv));
+                }
+                *reinterpret_cast<uint4*>(qsm + 8 * i) = w;
+            }
+            return;
+        }
         for (int i = threadIdx.x; i < m_pad * kw; i += nct) {
             const int m = i / kw;
             const int c = 8 * kv0 + (i - m * kw);
@@ -260,7 +278,7 @@ __global__ void __launch_bounds__(kMultiBwdThreads, 1) attnres_multi_bwd_kernel(
 #pragma unroll
                 for (int h = 0; h < 2; ++h) {
                     const int e = 2 * kk + h;
-                    const bool in = regblock && j < M && ((kmask[i] >> e) & 1u);
+                    const bool in = regblock && !selected && j < M && ((kmask[i] >> e) & 1u);
                     qv[h] = in ? bf16_bits_to_float(a.q[static_cast<long long>(j) * a.R + (8 * col[i] + e - ko)])
                                : 0.0f;
                 }
@@ -321,8 +339,46 @@ __global__ void __launch_bounds__(kMultiBwdThreads, 1) attnres_multi_bwd_kernel(
         // every warp is past the previous token's write and dq passes: the
         // token's bank rows can replace the queries in shared memory
         if (selected) load_q(n);
-        // coefficients: one warp per query, lanes over sources
-        {
+        // coefficients.  M <= 4: warp 0 forms every query's and also
+        // c_s = sum_m zr_ms (into zr_t[s]); otherwise one warp per query and
+        // the write pass adds the zr rows itself.
+        const bool one_warp_coef = M <= 4;
+        if (one_warp_coef) {
+            if (warp == 0) {
+                const float* tk = tok + ts * tstride;
+                float cs[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+                for (int m = 0; m < M; ++m) {
+                    float al[4], da[4], z[4], rs[4];
+                    float p = 0.0f;
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        const int s = lane + 32 * i;
+                        al[i] = da[i] = z[i] = rs[i] = 0.0f;
+                        if (s < S) {
+                            al[i] = tk[m * S + s];
+                            z[i] = tk[MS + m * S + s];
+                            rs[i] = tk[2 * MS + s];
+                            da[i] = da_t[m * s_pad + s];
+                            p = fmaf(al[i], da[i], p);
+                        }
+                    }
+                    const float delta = warp_sum(p);
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        const int s = lane + 32 * i;
+                        if (s < S) {
+                            const float dz = al[i] * (da[i] - delta);
+                            al_t[s * m_pad + m] = al[i];
+                            b_t[s * m_pad + m] = scale * rs[i] * dz;
+                            cs[i] += -(dz * z[i]) * (rs[i] * rs[i]) * inv_r;
+                        }
+                    }
+                }
+#pragma unroll
+                for (int i = 0; i < 4; ++i)
+                    if (lane + 32 * i < S) zr_t[lane + 32 * i] = cs[i];
+            }
+        } else {
             const float* tk = tok + ts * tstride;
             for (int m = warp; m < M; m += ncw) {
                 float al[4], da[4], z[4], rs[4];
@@ -357,6 +413,22 @@ __global__ void __launch_bounds__(kMultiBwdThreads, 1) attnres_multi_bwd_kernel(
 
         // write pass: dv_s for every source row, one store per row
         if (regblock) {
+            if (selected) {
+                // this token's bank rows: query values at the owned key vectors
+                // from shared memory, and a fresh dq sum
+#pragma unroll
+                for (int j = 0; j < MB; ++j)
+#pragma unroll
+                    for (int i = 0; i < VPT; ++i) {
+                        uint4 qv = make_uint4(0u, 0u, 0u, 0u);
+                        if (kvi[i] >= 0) qv = lds128(qsm_s + static_cast<uint32_t>(j) * kwb + 16u * kvi[i]);
+#pragma unroll
+                        for (int kk = 0; kk < 4; ++kk) {
+                            qf[j][i][kk] = key_part(bf2_to_f2(u4_get(qv, kk)), kmask[i], kk);
+                            dqa[j][i][kk] = make_float2(0.0f, 0.0f);
+                        }
+                    }
+            }
             float2 dyf[MB][VPT][4];
             uint32_t ddep = 0;
 #pragma unroll
@@ -381,14 +453,21 @@ __global__ void __launch_bounds__(kMultiBwdThreads, 1) attnres_multi_bwd_kernel(
                 for (int r = 0; r < rn; ++r) {
                     const int s = r0 + r;
                     float2 al2[MB], bl2[MB];
+                    {
+                        // the row's first four weights / b coefficients in one 16-byte load each
+                        const float4 a4 = *reinterpret_cast<const float4*>(al_t + s * m_pad);
+                        const float4 b4 = *reinterpret_cast<const float4*>(b_t + s * m_pad);
+                        const float av[4] = {a4.x, a4.y, a4.z, a4.w};
+                        const float bv[4] = {b4.x, b4.y, b4.z, b4.w};
 #pragma unroll
-                    for (int j = 0; j < MB; ++j) {
-                        const float av = al_t[s * m_pad + j], bv = b_t[s * m_pad + j];
-                        al2[j] = make_float2(av, av);
-                        bl2[j] = make_float2(bv, bv);
+                        for (int j = 0; j < MB; ++j) {
+                            al2[j] = make_float2(av[j], av[j]);
+                            bl2[j] = make_float2(bv[j], bv[j]);
+                        }
                     }
-                    float cs = 0.0f;
-                    for (int m = 0; m < M; ++m) cs += zr_t[m * s_pad + s];
+                    float cs = zr_t[s];
+                    if (!one_warp_coef)
+                        for (int m = 1; m < M; ++m) cs += zr_t[m * s_pad + s];
                     const float2 cs2 = make_float2(cs, cs);
                     uint16_t* drow = static_cast<uint16_t*>(a.dsrc[s]) + n * a.dsrc_ld;
 #pragma unroll
@@ -404,9 +483,11 @@ __global__ void __launch_bounds__(kMultiBwdThreads, 1) attnres_multi_bwd_kernel(
                                 for (int j = 1; j < MB; ++j) o[kk] = ffma2(al2[j], dyf[j][i][kk], o[kk]);
                             }
                             if (kvi[i] >= 0) {
+                                const bool whole = kmask[i] == 0xffu;  // every channel a key channel
 #pragma unroll
                                 for (int kk = 0; kk < 4; ++kk) {
-                                    const float2 xk = key_part(bf2_to_f2(u4_get(xv, kk)), kmask[i], kk);
+                                    const float2 x2 = bf2_to_f2(u4_get(xv, kk));
+                                    const float2 xk = whole ? x2 : key_part(x2, kmask[i], kk);
                                     o[kk] = ffma2(cs2, xk, o[kk]);
 #pragma unroll
                                     for (int j = 0; j < MB; ++j) {
@@ -425,6 +506,25 @@ __global__ void __launch_bounds__(kMultiBwdThreads, 1) attnres_multi_bwd_kernel(
                 if (lane == 0) mbar_arrive_after(empty_s + 8u * kc, dep);
                 if (++kc == K) kc = 0;
             }
+            if (selected) {
+                // the token's dq into its bank rows' sums (own columns only)
+#pragma unroll
+                for (int j = 0; j < MB; ++j) {
+                    if (j >= M) continue;
+                    const int row = bank_row(n, j);
+                    if (row < 0) continue;
+#pragma unroll
+                    for (int i = 0; i < VPT; ++i) {
+                        if (kvi[i] < 0) continue;
+                        float2* d2 = reinterpret_cast<float2*>(dqsm + row * kw + 8 * kvi[i]);
+#pragma unroll
+                        for (int kk = 0; kk < 4; ++kk) {
+                            const float2 o = d2[kk];
+                            d2[kk] = make_float2(o.x + dqa[j][i][kk].x, o.y + dqa[j][i][kk].y);
+                        }
+                    }
+                }
+            }
         } else {
             // several register blocks: dy and query vectors come from shared
             // memory for every row, dq sums go to shared memory afterwards
@@ -436,8 +536,9 @@ __global__ void __launch_bounds__(kMultiBwdThreads, 1) attnres_multi_bwd_kernel(
                     uint32_t rowa = ring_lo + static_cast<uint32_t>(kc) * cb;
                     for (int r = 0; r < rn; ++r) {
                         const int s = r0 + r;
-                        float cs = 0.0f;
-                        for (int m = 0; m < M; ++m) cs += zr_t[m * s_pad + s];
+                        float cs = zr_t[s];
+                        if (!one_warp_coef)
+                            for (int m = 1; m < M; ++m) cs += zr_t[m * s_pad + s];
                         const float2 cs2 = make_float2(cs, cs);
                         uint16_t* drow = static_cast<uint16_t*>(a.dsrc[s]) + n * a.dsrc_ld;
 #pragma unroll
@@ -573,7 +674,7 @@ __global__ void __launch_bounds__(kMultiBwdThreads, 1) attnres_multi_bwd_kernel(
         if (kvi[i] < 0) continue;
         for (int m = 0; m < QR; ++m) {
             float v8[8];
-            if (regblock) {
+            if (regblock && !selected) {
 #pragma unroll
                 for (int j = 0; j < MB; ++j) {
                     if (j == m) {

@@ -382,8 +382,209 @@ class MultiRead:
         return time.perf_counter() - t
 
 
-WORKLOADS = {"long": LongRead, "multi": MultiRead}
-FULL_TOKENS = {"long": 32768, "multi": 32768}
+def selected_algorithmic_bytes(S, N, D, R, K, E, P):
+    """Selected-query read: as the multi-query read with K slots per token,
+    plus the ids [N, K] (int64) read by both kernels and the [P, E*R] FP32
+    bank-gradient partial rows."""
+    b = multi_algorithmic_bytes(S, N, D, R, K, 0)
+    ids = N * K * 8
+    return {"fwd": b["fwd"] + ids, "bwd": b["bwd"] + ids + 2 * P * E * R * 4,
+            "total": b["fwd"] + b["bwd"] + 2 * ids + 2 * P * E * R * 4}
+
+
+def block_algorithmic_bytes(S, N, D, R, P):
+    """Fused block-partial read, S sources counting the partial sum: the
+    forward reads S-1 completed sources, the previous partial and delta, and
+    writes the new partial, y and the statistics; the backward reads the S
+    sources (the new partial among them), dy and the new partial's extra
+    gradient, and writes dvalues."""
+    row = N * D * 2
+    stats = 3 * N * S * 4
+    fwd = (S + 1) * row + 2 * row + stats
+    bwd = 2 * S * row + 2 * row + stats + 2 * P * R * 4
+    return {"fwd": fwd, "bwd": bwd, "total": fwd + bwd}
+
+
+class SelectedRead(MultiRead):
+    """Selected-query read: an 8-row query bank, two slots per token, over
+    the long-sequence sources."""
+    key = "selected"
+    roofline_kernel = "attnres_multi_bwd_kernel with a query bank (+ finalize)"
+
+    def __init__(self, tokens=None, seed=0, device="cpu"):
+        from attention_residuals_gb300.workloads import make_selected
+        self.wl = make_selected(10, 32768 if tokens is None else tokens, 4096, 1024, 8, 2,
+                                seed=300 + 1000 * seed, src_scale=(0.5, 2.0), device=device)
+
+    def bytes_for(self, P):
+        wl = self.wl
+        return selected_algorithmic_bytes(wl.S, wl.N, wl.D, wl.R, wl.K, wl.E, P)
+
+    def describe(self):
+        wl = self.wl
+        return (f"selected-query K={wl.K} E={wl.E} S={wl.S} N={wl.N} D={wl.D} R={wl.R} "
+                f"key_offset={wl.key_offset} bf16 (bank of 8 queries over the long-sequence sources)")
+
+    def prepare(self, dev):
+        import torch
+        from attention_residuals_gb300 import attnres_multi_plan_info
+        wl = self.wl
+        self.info = attnres_multi_plan_info(wl.values, wl.K, wl.R, key_offset=wl.key_offset)
+        self.bytes = self.bytes_for(self.info["grid"] % 1000)
+        self.ws = torch.empty((64 << 20,), dtype=torch.uint8, device=dev)
+        self.launches = 3
+        self.f = None
+
+    def fwd(self, stream, values=None, bank=None, ids=None):
+        from attention_residuals_gb300 import attnres_selected_fwd
+        wl = self.wl
+        self.f = attnres_selected_fwd(wl.values if values is None else values, wl.bank if bank is None else bank,
+                                      wl.ids if ids is None else ids, key_offset=wl.key_offset, stream=stream)
+        return self.f
+
+    def bwd(self, stream, values=None, bank=None, ids=None, dy=None):
+        from attention_residuals_gb300 import attnres_selected_bwd
+        wl = self.wl
+        return attnres_selected_bwd(wl.values if values is None else values, wl.bank if bank is None else bank,
+                                    wl.ids if ids is None else ids, wl.dy if dy is None else dy, self.f,
+                                    key_offset=wl.key_offset, stream=stream, workspace=self.ws)
+
+    def e2e(self, stream):
+        import torch
+        wl = self.wl
+        h = {"v": torch.empty(wl.values.shape, dtype=torch.bfloat16, pin_memory=True),
+             "bank": wl.bank.cpu().pin_memory(), "ids": wl.ids.cpu().pin_memory(),
+             "dy": torch.empty(wl.dy.shape, dtype=torch.bfloat16, pin_memory=True),
+             "y": torch.empty(wl.dy.shape, dtype=torch.bfloat16, pin_memory=True),
+             "dv": torch.empty(wl.values.shape, dtype=torch.bfloat16, pin_memory=True),
+             "db": torch.empty(wl.bank.shape, dtype=torch.bfloat16, pin_memory=True)}
+        h["v"].copy_(wl.values)
+        h["dy"].copy_(wl.dy)
+        d = {k: torch.empty_like(getattr(wl, n)) for k, n in (("v", "values"), ("bank", "bank"), ("ids", "ids"),
+                                                                ("dy", "dy"))}
+
+        def step():
+            for k in ("v", "bank", "ids", "dy"):
+                d[k].copy_(h[k], non_blocking=True)
+            f = self.fwd(stream, d["v"], d["bank"], d["ids"])
+            b = self.bwd(stream, d["v"], d["bank"], d["ids"], d["dy"])
+            h["y"].copy_(f["y"], non_blocking=True)
+            h["dv"].copy_(b["dvalues"], non_blocking=True)
+            h["db"].copy_(b["dbank"], non_blocking=True)
+
+        h2d = (h["v"].numel() + h["bank"].numel() + h["dy"].numel()) * 2 + h["ids"].numel() * 8
+        d2h = (h["y"].numel() + h["dv"].numel() + h["db"].numel()) * 2
+        return step, h2d, d2h, (h, d)
+
+    def traffic(self):
+        return None
+
+    def oracle_seconds(self, cores):
+        from oracle.multi import attnres_selected_oracle
+        wl = self.wl
+        t = time.perf_counter()
+        attnres_selected_oracle(wl.values, wl.bank, wl.ids.numpy(), dy=wl.dy, key_offset=wl.key_offset,
+                                nthreads=cores, want_dvalues=True)
+        return time.perf_counter() - t
+
+
+class BlockRead:
+    """Block-schedule read with the partial-block sum fused in: eight
+    completed block sums and the running partial sum (S=9 sources), the
+    newest writer output added inside the read, sliced key R=1024."""
+    key = "block"
+    roofline_kernel = "attnres_bwd_kernel with the added gradient (+ finalize)"
+
+    def __init__(self, tokens=None, seed=0, device="cpu"):
+        import torch
+        from attention_residuals_gb300.workloads import make_workload
+        wl = make_workload(4, N=tokens, seed=400 + 1000 * seed, device=device)
+        self.wl = wl
+        self.completed = wl.values[:-1]
+        self.partial = wl.values[-1]
+        g = torch.Generator(device=device)
+        g.manual_seed(401 + 1000 * seed)
+        self.delta = torch.randn(self.partial.shape, generator=g, device=device).to(torch.bfloat16)
+        self.gp = torch.randn(self.partial.shape, generator=g, device=device).to(torch.bfloat16)
+
+    def bytes_for(self, P):
+        wl = self.wl
+        return block_algorithmic_bytes(wl.S, wl.N, wl.D, wl.R, P)
+
+    def describe(self):
+        wl = self.wl
+        return (f"block schedule S={wl.S} (8 completed block sums + the partial sum, delta added in the "
+                f"read) N={wl.N} D={wl.D} R={wl.R} key_offset={wl.key_offset} bf16")
+
+    def prepare(self, dev):
+        import torch
+        from attention_residuals_gb300 import attnres_plan_info
+        wl = self.wl
+        self.comp = list(self.completed.unbind(0))
+        self.info = attnres_plan_info(wl.values, wl.R, key_offset=wl.key_offset, out_norm=False)
+        self.bytes = self.bytes_for(self.info["grid"])
+        self.pout = torch.empty_like(self.partial)
+        self.launches = 2 + (1 if self.info["bwd_split"] else 0)
+        self.f = None
+
+    def fwd(self, stream):
+        from attention_residuals_gb300 import attnres_partial_fwd
+        self.f = attnres_partial_fwd(self.comp, self.partial, self.delta, self.wl.q, key_offset=self.wl.key_offset,
+                                     partial_out=self.pout, stream=stream)
+        return self.f
+
+    def bwd(self, stream):
+        from attention_residuals_gb300 import attnres_partial_bwd
+        return attnres_partial_bwd(self.comp, self.pout, self.wl.q, self.wl.dy, self.f, g_partial=self.gp,
+                                   key_offset=self.wl.key_offset, stream=stream)
+
+    def e2e(self, stream):
+        import torch
+        wl = self.wl
+        pin = dict(dtype=torch.bfloat16, pin_memory=True)
+        h = {"c": torch.empty(self.completed.shape, **pin), "p": torch.empty(self.partial.shape, **pin),
+             "d": torch.empty(self.partial.shape, **pin), "dy": torch.empty(wl.dy.shape, **pin),
+             "g": torch.empty(self.partial.shape, **pin), "y": torch.empty(wl.dy.shape, **pin),
+             "pn": torch.empty(self.partial.shape, **pin), "dc": torch.empty(self.completed.shape, **pin),
+             "dp": torch.empty(self.partial.shape, **pin)}
+        h["c"].copy_(self.completed)
+        h["p"].copy_(self.partial)
+        h["d"].copy_(self.delta)
+        h["dy"].copy_(wl.dy)
+        h["g"].copy_(self.gp)
+        d = {k: torch.empty_like(h[k], device=stream.device) for k in ("c", "p", "d", "dy", "g")}
+        from attention_residuals_gb300 import attnres_partial_bwd, attnres_partial_fwd
+
+        def step():
+            for k in ("c", "p", "d", "dy", "g"):
+                d[k].copy_(h[k], non_blocking=True)
+            comp = list(d["c"].unbind(0))
+            f = attnres_partial_fwd(comp, d["p"], d["d"], wl.q, key_offset=wl.key_offset, stream=stream)
+            b = attnres_partial_bwd(comp, f["partial_new"], wl.q, d["dy"], f, g_partial=d["g"],
+                                    key_offset=wl.key_offset, stream=stream)
+            h["y"].copy_(f["y"], non_blocking=True)
+            h["pn"].copy_(f["partial_new"], non_blocking=True)
+            h["dc"].copy_(torch.stack(b["d_completed"]), non_blocking=True)
+            h["dp"].copy_(b["d_partial"], non_blocking=True)
+
+        h2d = sum(h[k].numel() for k in ("c", "p", "d", "dy", "g")) * 2
+        d2h = sum(h[k].numel() for k in ("y", "pn", "dc", "dp")) * 2
+        return step, h2d, d2h, (h, d)
+
+    def traffic(self):
+        return None
+
+    def oracle_seconds(self, cores):
+        from oracle.partial import attnres_partial_oracle
+        wl = self.wl
+        t = time.perf_counter()
+        attnres_partial_oracle(self.completed, self.partial, self.delta, wl.q, dy=wl.dy, g_partial=self.gp,
+                               key_offset=wl.key_offset, nthreads=cores)
+        return time.perf_counter() - t
+
+
+WORKLOADS = {"long": LongRead, "multi": MultiRead, "selected": SelectedRead, "block": BlockRead}
+FULL_TOKENS = {"long": 32768, "multi": 32768, "selected": 32768, "block": 16384}
 
 
 # --------------------------------------------------------------------------

@@ -32,7 +32,7 @@ def test_multi_byte_model():
     assert b["bwd"] == 2 * v + out + stats + 2 * 152 * 2 * 1024 * 4
 
 
-@pytest.mark.parametrize("workload", ["long", "multi"])
+@pytest.mark.parametrize("workload", ["long", "multi", "selected", "block"])
 def test_reference_arm_prints_one_json_line(workload):
     r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference",
                         "--workload", workload, "--steps", "1", "--warmup", "3", "--ref-tokens", "16"],
@@ -47,3 +47,15 @@ def test_reference_arm_prints_one_json_line(workload):
     assert d["impl"] == "reference" and d["value"] > 0
     assert d["e2e"]["h2d_bytes_per_step"] == 0
     assert d["cpu_baseline"]["kind"] == "oracle"
+
+
+def test_extension_byte_models():
+    s = bench.selected_algorithmic_bytes(S=10, N=100, D=64, R=16, K=2, E=8, P=4)
+    m = bench.multi_algorithmic_bytes(S=10, N=100, D=64, R=16, M=2, P=0)
+    assert s["fwd"] == m["fwd"] + 100 * 2 * 8
+    assert s["bwd"] == m["bwd"] + 100 * 2 * 8 + 2 * 4 * 8 * 16 * 4
+    b = bench.block_algorithmic_bytes(S=9, N=10, D=64, R=16, P=3)
+    row = 10 * 64 * 2
+    # reads: S-1 completed + the previous partial + delta; writes: the new partial + y
+    assert b["fwd"] == (8 + 2) * row + 2 * row + 3 * 10 * 9 * 4
+    assert b["bwd"] == 2 * 9 * row + 2 * row + 3 * 10 * 9 * 4 + 2 * 3 * 16 * 4
