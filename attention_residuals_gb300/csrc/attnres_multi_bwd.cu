@@ -314,20 +314,38 @@ __global__ void __launch_bounds__(kMultiBwdThreads, 1) attnres_multi_bwd_kernel(
             if (kc >= K) kc -= K;
             const uint32_t row = ring_raw + static_cast<uint32_t>(kc) * cb + static_cast<uint32_t>(r % G) * sb;
             for (int m4 = 0; m4 < M; m4 += 4) {
-                float t[4][2];
+                // two vectors per step into separate sums: half the FMA chain
+                float t[4][2], u[4][2];
 #pragma unroll
-                for (int j = 0; j < 4; ++j) t[j][0] = t[j][1] = 0.0f;
-                for (int v = lane; v < ncv; v += 32) {
-                    const uint4 x = lds128(row + 16u * v);
+                for (int j = 0; j < 4; ++j) t[j][0] = t[j][1] = u[j][0] = u[j][1] = 0.0f;
+                int v = lane;
+                for (; v + 32 < ncv; v += 64) {
+                    const uint4 x0 = lds128(row + 16u * v);
+                    const uint4 x1 = lds128(row + 16u * (v + 32));
 #pragma unroll
                     for (int j = 0; j < 4; ++j) {
                         if (m4 + j < M) {
-                            const uint4 y = lds128(dyb + static_cast<uint32_t>(m4 + j) * sb + 16u * v);
-                            bf16_dot8(x, y, t[j][0], t[j][1]);
+                            const uint32_t yrow = dyb + static_cast<uint32_t>(m4 + j) * sb;
+                            const uint4 y0 = lds128(yrow + 16u * v);
+                            const uint4 y1 = lds128(yrow + 16u * (v + 32));
+                            bf16_dot8(x0, y0, t[j][0], t[j][1]);
+                            bf16_dot8(x1, y1, u[j][0], u[j][1]);
                         }
                     }
                 }
-                float part[4] = {t[0][0] + t[0][1], t[1][0] + t[1][1], t[2][0] + t[2][1], t[3][0] + t[3][1]};
+                if (v < ncv) {
+                    const uint4 x0 = lds128(row + 16u * v);
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        if (m4 + j < M) {
+                            const uint4 y0 = lds128(dyb + static_cast<uint32_t>(m4 + j) * sb + 16u * v);
+                            bf16_dot8(x0, y0, t[j][0], t[j][1]);
+                        }
+                    }
+                }
+                float part[4];
+#pragma unroll
+                for (int j = 0; j < 4; ++j) part[j] = (t[j][0] + t[j][1]) + (u[j][0] + u[j][1]);
                 warp_reduce_scatter<4>(part, lane);
                 if ((lane & 7) == 0) {
                     const int e = lane >> 3;
@@ -450,6 +468,7 @@ __global__ void __launch_bounds__(kMultiBwdThreads, 1) attnres_multi_bwd_kernel(
                 const int rn = min(G, S - r0);
                 uint32_t dep = 0;
                 uint32_t rowa = ring_lo + static_cast<uint32_t>(kc) * cb;
+#pragma unroll 2
                 for (int r = 0; r < rn; ++r) {
                     const int s = r0 + r;
                     float2 al2[MB], bl2[MB];

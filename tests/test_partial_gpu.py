@@ -121,3 +121,33 @@ def test_block_read_autograd_compile(out_norm):
     assert torch.equal(part.grad, dl.grad)
     # autograd hands back the bf16 dq; its rounding alone is up to 2^-8 per element
     assert rel_l2(to_np(q.grad), ref["dq"]) <= 4e-3
+
+
+def test_block_full_size_sampled():
+    # the benchmark's block workload at full size (eight completed block sums,
+    # the partial sum, N=16384, D=4096, R=1024): sampled tokens element by
+    # element, the new partial sum bit for bit everywhere, dq over every token
+    from attention_residuals_gb300.workloads import make_workload
+    wl = make_workload(4, seed=404, device="cuda")
+    comp = list(wl.values[:-1].unbind(0))
+    partial = wl.values[-1]
+    g = torch.Generator(device="cuda").manual_seed(405)
+    delta = torch.randn(partial.shape, generator=g, device="cuda").to(torch.bfloat16)
+    gp = torch.randn(partial.shape, generator=g, device="cuda").to(torch.bfloat16)
+    f = attnres_partial_fwd(comp, partial, delta, wl.q, key_offset=wl.key_offset)
+    b = attnres_partial_bwd(comp, f["partial_new"], wl.q, wl.dy, f, g_partial=gp, key_offset=wl.key_offset)
+    torch.cuda.synchronize()
+    attnres_check_device_error()
+    np.testing.assert_array_equal(_bits(f["partial_new"]), partial_sum_bits(partial.cpu(), delta.cpu()))
+    rng = np.random.default_rng(3)
+    idx = np.array(sorted(set(rng.choice(wl.N, 40, replace=False).tolist()) | {0, wl.N - 1}))
+    it = torch.as_tensor(idx, device="cuda")
+    sel = lambda t: t.index_select(-2, it).cpu()
+    ref = attnres_partial_oracle(torch.stack([sel(c) for c in comp]), sel(partial), sel(delta), wl.q.cpu(),
+                                 dy=sel(wl.dy), g_partial=sel(gp), key_offset=wl.key_offset)
+    assert y_rel_err(to_np(f["y"].index_select(0, it)), ref["y"]) <= Y_REL
+    assert rel_l2(to_np(torch.stack([c.index_select(0, it) for c in b["d_completed"]])), ref["d_completed"]) <= GRAD_REL_L2
+    assert rel_l2(to_np(b["d_partial"].index_select(0, it)), ref["d_partial"]) <= GRAD_REL_L2
+    full = attnres_partial_oracle(torch.stack([c.cpu() for c in comp]), partial.cpu(), delta.cpu(), wl.q.cpu(),
+                                  dy=wl.dy.cpu(), g_partial=gp.cpu(), key_offset=wl.key_offset)
+    assert rel_l2(to_np(b["dq_f32"]), full["dq"]) <= GRAD_REL_L2

@@ -133,3 +133,29 @@ def test_selected_autograd_compile():
     assert rel_l2(to_np(v.grad), ref["dvalues"]) <= GRAD_REL_L2
     # autograd returns the bf16 bank gradient; its rounding alone is up to 2^-8 per element
     assert rel_l2(to_np(bank.grad), ref["dbank"]) <= 4e-3
+
+
+def test_selected_full_size_sampled():
+    # the benchmark's selected-query workload at full size: sampled tokens
+    # element by element, the bank gradient over every token
+    wl = make_selected(10, 32768, 4096, 1024, 8, 2, seed=300, src_scale=(0.5, 2.0), device="cuda")
+    v, bank, ids, dy = wl.values, wl.bank, wl.ids, wl.dy
+    f = attnres_selected_fwd(v, bank, ids)
+    b = attnres_selected_bwd(v, bank, ids, dy, f)
+    b2 = attnres_selected_bwd(v, bank, ids, dy, f)
+    torch.cuda.synchronize()
+    attnres_check_device_error()
+    assert torch.equal(b["dbank_f32"], b2["dbank_f32"]) and torch.equal(b["dvalues"], b2["dvalues"])
+    del b2
+    g = np.random.default_rng(2)
+    idx = np.array(sorted(set(g.choice(wl.N, 40, replace=False).tolist()) | {0, wl.N - 1}))
+    it = torch.as_tensor(idx, device="cuda")
+    ref = attnres_selected_oracle(v.index_select(1, it).cpu(), bank.cpu(), ids.index_select(0, it).cpu().numpy(),
+                                  dy=dy.index_select(0, it).cpu(), key_offset=wl.key_offset)
+    y = to_np(f["y"].index_select(0, it))
+    assert max(y_rel_err(y[:, k], ref["y"][:, k]) for k in range(2)) <= Y_REL
+    assert rel_l2(to_np(b["dvalues"].index_select(1, it)), ref["dvalues"]) <= GRAD_REL_L2
+    full = attnres_selected_oracle(v.cpu(), bank.cpu(), ids.cpu().numpy(), dy=dy.cpu(), key_offset=wl.key_offset,
+                                   want_dvalues=False)
+    assert rel_l2(to_np(b["dbank_f32"]), full["dbank"]) <= GRAD_REL_L2
+    np.testing.assert_array_equal(to_np(b["dbank"]), bf16_rne(to_np(b["dbank_f32"])))
