@@ -48,6 +48,8 @@ WORKLOAD_CFG = 3
 FALLBACK_HBM_GBS = 6800.0
 PROFILE_TRAFFIC = os.path.join(ROOT, "profiles", "attnres_bwd_traffic.json")
 PROFILE_TRAFFIC_MULTI = os.path.join(ROOT, "profiles", "attnres_multi_bwd_traffic.json")
+PROFILE_TRAFFIC_SELECTED = os.path.join(ROOT, "profiles", "attnres_selected_bwd_traffic.json")
+PROFILE_TRAFFIC_BLOCK = os.path.join(ROOT, "profiles", "attnres_block_bwd_traffic.json")
 
 
 # --------------------------------------------------------------------------
@@ -477,7 +479,7 @@ class SelectedRead(MultiRead):
         return step, h2d, d2h, (h, d)
 
     def traffic(self):
-        return None
+        return profiled_traffic("selected-long", PROFILE_TRAFFIC_SELECTED, MULTI_SOURCES)
 
     def oracle_seconds(self, cores):
         from oracle.multi import attnres_selected_oracle
@@ -572,7 +574,7 @@ class BlockRead:
         return step, h2d, d2h, (h, d)
 
     def traffic(self):
-        return None
+        return profiled_traffic("block", PROFILE_TRAFFIC_BLOCK)
 
     def oracle_seconds(self, cores):
         from oracle.partial import attnres_partial_oracle
