@@ -232,6 +232,7 @@ attnres_status make_multi_plan(const attnres_multi_params* p, MultiPlan* plan, i
     if (!device_info(&dev)) return ATTNRES_ERR_CUDA;
     const attnres_params& b = p->base;
     MultiPlan pl{};
+    pl.E = E;  // the occupancy queries below pick the kernels by it
     const int ncv = b.D / 8;
     const int M = p->M;
     const int p2 = pow2_ceil(M);
@@ -257,7 +258,12 @@ attnres_status make_multi_plan(const attnres_multi_params* p, MultiPlan* plan, i
         if (cps * (pl.ncw + 1) * 32 > 2048) continue;
         const uint32_t budget = cps > 1 ? optin / cps - 1024 : optin;
         const uint32_t qall = static_cast<uint32_t>(nblk * pl.mb_f) * static_cast<uint32_t>(pl.nkv) * 16u;
-        const int qrows = qall <= budget / 2 ? nblk * pl.mb_f : pl.mb_f;
+        int qrows = qall <= budget / 2 ? nblk * pl.mb_f : pl.mb_f;
+        // selected queries: the whole bank (and a zero row for bad ids) when it
+        // takes at most half the budget, else each block's rows per token
+        const uint32_t ball = static_cast<uint32_t>(E + 1) * static_cast<uint32_t>(pl.nkv) * 16u;
+        const int bank = (E > 0 && ball <= budget / 2) ? E + 1 : 0;
+        if (E > 0) qrows = bank ? bank : pl.mb_f;
         auto ffits = [&](int chunks, int rows) {
             return make_multi_fwd_layout(chunks, rows, pl.slot_bytes, pl.s_pad, qrows, pl.nkv).total <= budget;
         };
@@ -277,6 +283,7 @@ attnres_status make_multi_plan(const attnres_multi_params* p, MultiPlan* plan, i
         pl.f_chunks = chunks;
         pl.f_group = gc * rows;
         pl.qrows = qrows;
+        pl.bank_f = bank;
         pl.smem_fwd = make_multi_fwd_layout(chunks, rows, pl.slot_bytes, pl.s_pad, qrows, pl.nkv).total;
         // more than one CTA per SM only when the kernel's registers allow it
         if (cps > 1 && multi_fwd_occupancy(pl) < cps) continue;
@@ -295,26 +302,34 @@ attnres_status make_multi_plan(const attnres_multi_params* p, MultiPlan* plan, i
     const bool dq_in_smem = nmb > 1 || E > 0;
     const int dq_nkv = dq_in_smem ? pl.nkv : 0;
     const int dq_rows = E > 0 ? E : M;
-    pl.E = E;
     pl.bwd_ok = 0;
     int bcps = 1;
-    for (int cps = kMultiMaxCtasPerSm; cps >= 1 && !pl.bwd_ok; --cps) {
-        if (cps * (pl.b_ncw + 1) * 32 > 2048 || pl.b_ncw > kMultiBwdWarps) continue;
-        const uint32_t budget = cps > 1 ? optin / cps - 1024 : optin;
-        for (int ds = 2; ds >= 1 && !pl.bwd_ok; --ds) {
-            auto bfits = [&](int K, int G) {
-                return make_multi_layout(K, G, pl.slot_bytes, M, ds, pl.s_pad, pl.m_pad, pl.nkv, dq_nkv, true,
-                                         dq_rows).total <= budget;
-            };
-            if (!pick_ring(b.S, bfits, &pl.b_rows, &pl.b_chunks)) continue;
-            pl.dy_slots = ds;
-            pl.smem_bwd = make_multi_layout(pl.b_chunks, pl.b_rows, pl.slot_bytes, M, ds, pl.s_pad, pl.m_pad,
-                                            pl.nkv, dq_nkv, true, dq_rows).total;
-            if (cps > 1 && multi_bwd_occupancy(pl) < cps) continue;
-            pl.bwd_ok = 1;
-            bcps = cps;
+    // selected queries: first with the bank resident in shared memory, then
+    // with each token's bank rows loaded per token
+    for (int bank = (E > 0 && nmb == 1) ? E + 1 : 0; bank >= 0 && !pl.bwd_ok; bank = bank > 0 ? 0 : -1) {
+        const int q_rows = bank > pl.m_pad ? bank : pl.m_pad;
+        pl.bank_b = bank;
+        for (int cps = kMultiMaxCtasPerSm; cps >= 1 && !pl.bwd_ok; --cps) {
+            if (cps * (pl.b_ncw + 1) * 32 > 2048 || pl.b_ncw > kMultiBwdWarps) continue;
+            const uint32_t budget = cps > 1 ? optin / cps - 1024 : optin;
+            for (int ds = 2; ds >= 1 && !pl.bwd_ok; --ds) {
+                auto bfits = [&](int K, int G) {
+                    return make_multi_layout(K, G, pl.slot_bytes, M, ds, pl.s_pad, pl.m_pad, pl.nkv, dq_nkv, true,
+                                             dq_rows, q_rows).total <= budget;
+                };
+                if (!pick_ring(b.S, bfits, &pl.b_rows, &pl.b_chunks)) continue;
+                // the bank stays only where the ring still loads the next token meanwhile
+                if (bank > 0 && pl.b_chunks < (b.S + pl.b_rows - 1) / pl.b_rows + 1) continue;
+                pl.dy_slots = ds;
+                pl.smem_bwd = make_multi_layout(pl.b_chunks, pl.b_rows, pl.slot_bytes, M, ds, pl.s_pad, pl.m_pad,
+                                                pl.nkv, dq_nkv, true, dq_rows, q_rows).total;
+                if (cps > 1 && multi_bwd_occupancy(pl) < cps) continue;
+                pl.bwd_ok = 1;
+                bcps = cps;
+            }
         }
     }
+    if (!pl.bwd_ok) pl.bank_b = 0;
     long long grid = static_cast<long long>(bcps) * dev.sm_count;
     if (b.N < grid) grid = b.N;
     pl.grid = static_cast<int>(grid < 1 ? 1 : grid);
@@ -674,6 +689,7 @@ static attnres_status multi_fwd_impl(const attnres_multi_params* p, const void* 
     a.q = static_cast<const uint16_t*>(q);
     a.ids = reinterpret_cast<const long long*>(ids);
     a.E = ids ? E : 0;
+    a.bank_rows = ids ? pl.bank_f : 0;
     a.y = static_cast<uint16_t*>(y);
     a.alpha = alpha;
     a.rstd = rstd;
@@ -774,6 +790,7 @@ static attnres_status multi_bwd_impl(const attnres_multi_params* p, const void* 
     a.dq_f32 = dq_f32;
     a.ids = reinterpret_cast<const long long*>(ids);
     a.E = ids ? E : 0;
+    a.bank_rows = ids ? pl.bank_b : 0;
     return launch_multi_bwd(pl, a, s0) == cudaSuccess ? ATTNRES_OK : ATTNRES_ERR_CUDA;
 }
 

@@ -45,7 +45,7 @@ __device__ __forceinline__ float2 key_part(const float2 x, unsigned mask, int kk
     return make_float2((mask >> (2 * kk)) & 1u ? x.x : 0.0f, (mask >> (2 * kk + 1)) & 1u ? x.y : 0.0f);
 }
 
-template <int VPT, int MB>
+template <int VPT, int MB, bool SEL>
 __global__ void __launch_bounds__(kMultiBwdThreads, 1) attnres_multi_bwd_kernel(const __grid_constant__ MultiBwdArgs a) {
     extern __shared__ __align__(128) unsigned char smem[];
     const int ncw = a.ncw;
@@ -57,7 +57,7 @@ __global__ void __launch_bounds__(kMultiBwdThreads, 1) attnres_multi_bwd_kernel(
     const int DS = a.dy_slots;
     const int s_pad = a.s_pad, m_pad = a.m_pad;
     const int nmb = (M + MB - 1) / MB;
-    const bool selected = a.ids != nullptr;  // per-token queries from a bank
+    const bool selected = SEL;         // per-token queries from a bank (a.ids set)
     // one register block: q and the token's dq live in registers (fixed
     // queries: dq for the whole launch; selected queries: q reloaded and dq
     // added to the bank row's shared-memory sums per token); several blocks:
@@ -65,8 +65,11 @@ __global__ void __launch_bounds__(kMultiBwdThreads, 1) attnres_multi_bwd_kernel(
     const bool regblock = nmb == 1;
     const bool dq_in_smem = !regblock || selected;
     const int QR = selected ? a.E : M;       // rows of dq (queries or bank rows)
-    const MultiLayout L =
-        make_multi_layout(K, G, a.slot_bytes, M, DS, s_pad, m_pad, a.nkv, dq_in_smem ? a.nkv : 0, true, QR);
+    // selected queries with one register block: the whole bank (and a zero
+    // row, index E) stays in shared memory, addressed by the token's ids
+    const bool bank_res = selected && regblock && a.bank_rows > 0;
+    const MultiLayout L = make_multi_layout(K, G, a.slot_bytes, M, DS, s_pad, m_pad, a.nkv, dq_in_smem ? a.nkv : 0,
+                                            true, QR, a.bank_rows > 0 ? max(a.bank_rows, m_pad) : -1);
     uint64_t* full = reinterpret_cast<uint64_t*>(smem + L.full);
     uint64_t* empty = reinterpret_cast<uint64_t*>(smem + L.empty);
     uint64_t* dyfull = reinterpret_cast<uint64_t*>(smem + L.dyfull);
@@ -78,7 +81,11 @@ __global__ void __launch_bounds__(kMultiBwdThreads, 1) attnres_multi_bwd_kernel(
     float* al_t = da_t + m_pad * s_pad;                    // [s_pad][m_pad]
     float* b_t = al_t + s_pad * m_pad;                     // [s_pad][m_pad]
     float* zr_t = b_t + s_pad * m_pad;                     // [m_pad][s_pad]
-    float* dqsm = reinterpret_cast<float*>(smem + L.dqsm);  // [M][nkv * 8] (several blocks)
+    // dq sums (several blocks, or bank rows): row m, key vector v, channel e at
+    // dqsm[m * nkv * 8 + (e / 4) * nkv * 4 + v * 4 + e % 4] -- two planes of
+    // four channels, so a warp's 16-byte accesses to consecutive vectors are
+    // free of bank conflicts
+    float* dqsm = reinterpret_cast<float*>(smem + L.dqsm);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L.misc);
     const int tstride = static_cast<int>(L.tstride);
 
@@ -192,6 +199,16 @@ __global__ void __launch_bounds__(kMultiBwdThreads, 1) attnres_multi_bwd_kernel(
     const int ko = a.ko, kend = a.ko + a.R;
     const int kv0 = a.kv0, nkv = a.nkv;
     const int kw = nkv * 8;
+    // dq sums of one owned key vector (eight channels as four pairs) into row m
+    auto dq_add = [&](int m, int v, const float2 (&d)[4]) {
+        float4* p0 = reinterpret_cast<float4*>(dqsm + m * kw + 4 * v);
+        float4* p1 = reinterpret_cast<float4*>(dqsm + m * kw + (kw >> 1) + 4 * v);
+        float4 x = *p0, y = *p1;
+        x.x += d[0].x; x.y += d[0].y; x.z += d[1].x; x.w += d[1].y;
+        y.x += d[2].x; y.y += d[2].y; y.z += d[3].x; y.w += d[3].y;
+        *p0 = x;
+        *p1 = y;
+    };
     const uint32_t kwb = static_cast<uint32_t>(nkv) * 16u;
     int col[VPT];
     int kvi[VPT];        // key vector index within the key window, -1 outside
@@ -264,6 +281,35 @@ __global__ void __launch_bounds__(kMultiBwdThreads, 1) attnres_multi_bwd_kernel(
         }
     };
     if (!selected) load_q(0);
+    if (bank_res) {
+        uint16_t* qsm = reinterpret_cast<uint16_t*>(smem + L.qsm);
+        if (q_vec) {
+            for (int i = threadIdx.x; i < a.bank_rows * nkv; i += nct) {
+                const int row = i / nkv;
+                uint4 w = make_uint4(0u, 0u, 0u, 0u);
+                if (row < a.E) w = ld_global_nc_v4(a.q + static_cast<long long>(row) * a.R + 8 * (i - row * nkv));
+                *reinterpret_cast<uint4*>(qsm + 8 * i) = w;
+            }
+        } else {
+            for (int i = threadIdx.x; i < a.bank_rows * kw; i += nct) {
+                const int row = i / kw;
+                const int c = 8 * kv0 + (i - row * kw);
+                qsm[i] = (row < a.E && c >= ko && c < kend) ? a.q[static_cast<long long>(row) * a.R + (c - ko)]
+                                                            : static_cast<uint16_t>(0);
+            }
+        }
+    }
+    // Resident bank: lane m < M of every warp holds the bank row of slot m,
+    // loaded one token ahead; an id outside [0, E) is recorded and reads the
+    // zero row (and adds to no dq row).
+    auto row_of = [&](long long id) -> int {
+        if (id < 0 || id >= a.E) {
+            atomicCAS(&g_multi_bwd_error, 0u, static_cast<unsigned>(kSiteBadId));
+            return a.E;
+        }
+        return static_cast<int>(id);
+    };
+    long long id_next = (bank_res && lane < M) ? a.ids[static_cast<long long>(blockIdx.x) * M + lane] : 0;
     // One register block: the query values at the owned key vectors and the
     // dq sums live in registers for the whole launch.
     float2 qf[MB][VPT][4];
@@ -294,6 +340,12 @@ __global__ void __launch_bounds__(kMultiBwdThreads, 1) attnres_multi_bwd_kernel(
     int ts = 0;
     uint32_t tphase = 0;
     for (long long n = blockIdx.x; n < N; n += gridDim.x) {
+        int my_row = 0;
+        if (bank_res) {
+            my_row = lane < M ? row_of(id_next) : a.E;
+            const long long nn = n + gridDim.x;
+            id_next = (lane < M && nn < N) ? a.ids[nn * M + lane] : 0;
+        }
         {
             int k = ck;
             uint32_t ph = cphase;
@@ -356,7 +408,7 @@ __global__ void __launch_bounds__(kMultiBwdThreads, 1) attnres_multi_bwd_kernel(
         named_bar_sync(1, nct);
         // every warp is past the previous token's write and dq passes: the
         // token's bank rows can replace the queries in shared memory
-        if (selected) load_q(n);
+        if (selected && !bank_res) load_q(n);
         // coefficients.  M <= 4: warp 0 forms every query's and also
         // c_s = sum_m zr_ms (into zr_t[s]); otherwise one warp per query and
         // the write pass adds the zr rows itself.
@@ -435,17 +487,23 @@ __global__ void __launch_bounds__(kMultiBwdThreads, 1) attnres_multi_bwd_kernel(
                 // this token's bank rows: query values at the owned key vectors
                 // from shared memory, and a fresh dq sum
 #pragma unroll
-                for (int j = 0; j < MB; ++j)
+                for (int j = 0; j < MB; ++j) {
+                    uint32_t qrow = qsm_s + static_cast<uint32_t>(j) * kwb;
+                    if (bank_res) {
+                        const int r = __shfl_sync(0xffffffffu, my_row, j);
+                        qrow = qsm_s + static_cast<uint32_t>(j < M ? r : a.E) * kwb;
+                    }
 #pragma unroll
                     for (int i = 0; i < VPT; ++i) {
                         uint4 qv = make_uint4(0u, 0u, 0u, 0u);
-                        if (kvi[i] >= 0) qv = lds128(qsm_s + static_cast<uint32_t>(j) * kwb + 16u * kvi[i]);
+                        if (kvi[i] >= 0) qv = lds128(qrow + 16u * kvi[i]);
 #pragma unroll
                         for (int kk = 0; kk < 4; ++kk) {
                             qf[j][i][kk] = key_part(bf2_to_f2(u4_get(qv, kk)), kmask[i], kk);
                             dqa[j][i][kk] = make_float2(0.0f, 0.0f);
                         }
                     }
+                }
             }
             float2 dyf[MB][VPT][4];
             uint32_t ddep = 0;
@@ -530,18 +588,17 @@ __global__ void __launch_bounds__(kMultiBwdThreads, 1) attnres_multi_bwd_kernel(
 #pragma unroll
                 for (int j = 0; j < MB; ++j) {
                     if (j >= M) continue;
-                    const int row = bank_row(n, j);
+                    int row;
+                    if (bank_res) {
+                        row = __shfl_sync(0xffffffffu, my_row, j);
+                        if (row >= a.E) row = -1;
+                    } else {
+                        row = bank_row(n, j);
+                    }
                     if (row < 0) continue;
 #pragma unroll
-                    for (int i = 0; i < VPT; ++i) {
-                        if (kvi[i] < 0) continue;
-                        float2* d2 = reinterpret_cast<float2*>(dqsm + row * kw + 8 * kvi[i]);
-#pragma unroll
-                        for (int kk = 0; kk < 4; ++kk) {
-                            const float2 o = d2[kk];
-                            d2[kk] = make_float2(o.x + dqa[j][i][kk].x, o.y + dqa[j][i][kk].y);
-                        }
-                    }
+                    for (int i = 0; i < VPT; ++i)
+                        if (kvi[i] >= 0) dq_add(row, kvi[i], dqa[j][i]);
                 }
             }
         } else {
@@ -651,15 +708,8 @@ __global__ void __launch_bounds__(kMultiBwdThreads, 1) attnres_multi_bwd_kernel(
                     const int row = selected ? bank_row(n, mb + j) : mb + j;
                     if (row < 0) continue;
 #pragma unroll
-                    for (int i = 0; i < VPT; ++i) {
-                        if (kvi[i] < 0) continue;
-                        float2* d2 = reinterpret_cast<float2*>(dqsm + row * kw + 8 * kvi[i]);
-#pragma unroll
-                        for (int kk = 0; kk < 4; ++kk) {
-                            const float2 o = d2[kk];
-                            d2[kk] = make_float2(o.x + dqt[j][i][kk].x, o.y + dqt[j][i][kk].y);
-                        }
-                    }
+                    for (int i = 0; i < VPT; ++i)
+                        if (kvi[i] >= 0) dq_add(row, kvi[i], dqt[j][i]);
                 }
             }
             // the chunks held every row until the dq pass
@@ -706,7 +756,7 @@ __global__ void __launch_bounds__(kMultiBwdThreads, 1) attnres_multi_bwd_kernel(
                 }
             } else {
 #pragma unroll
-                for (int e = 0; e < 8; ++e) v8[e] = dqsm[m * kw + 8 * kvi[i] + e];
+                for (int e = 0; e < 8; ++e) v8[e] = dqsm[m * kw + (e >> 2) * (kw >> 1) + 4 * kvi[i] + (e & 3)];
             }
 #pragma unroll
             for (int e = 0; e < 8; ++e)
@@ -715,9 +765,9 @@ __global__ void __launch_bounds__(kMultiBwdThreads, 1) attnres_multi_bwd_kernel(
     }
 }
 
-template <int VPT, int MB>
+template <int VPT, int MB, bool SEL>
 cudaError_t launch_t(const MultiPlan& plan, const MultiBwdArgs& a, cudaStream_t stream) {
-    auto kern = attnres_multi_bwd_kernel<VPT, MB>;
+    auto kern = attnres_multi_bwd_kernel<VPT, MB, SEL>;
     cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                            static_cast<int>(plan.smem_bwd));
     if (err != cudaSuccess) return err;
@@ -729,9 +779,9 @@ cudaError_t launch_t(const MultiPlan& plan, const MultiBwdArgs& a, cudaStream_t 
                            stream);
 }
 
-template <int VPT, int MB>
+template <int VPT, int MB, bool SEL>
 int occupancy_t(const MultiPlan& plan) {
-    auto kern = attnres_multi_bwd_kernel<VPT, MB>;
+    auto kern = attnres_multi_bwd_kernel<VPT, MB, SEL>;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(plan.smem_bwd)) !=
         cudaSuccess)
         return 0;
@@ -750,23 +800,35 @@ unsigned take_multi_bwd_error() {
     return v;
 }
 
-int multi_bwd_occupancy(const MultiPlan& plan) {
+namespace {
+template <bool SEL>
+int bwd_occupancy_sel(const MultiPlan& plan) {
     switch (plan.b_vpt * 10 + plan.mb_b) {
-        case 11: return occupancy_t<1, 1>(plan);
-        case 12: return occupancy_t<1, 2>(plan);
-        case 21: return occupancy_t<2, 1>(plan);
+        case 11: return occupancy_t<1, 1, SEL>(plan);
+        case 12: return occupancy_t<1, 2, SEL>(plan);
+        case 21: return occupancy_t<2, 1, SEL>(plan);
         default: return 0;
     }
 }
 
-cudaError_t launch_multi_bwd(const MultiPlan& plan, const MultiBwdArgs& a, cudaStream_t stream) {
-    const int key = plan.b_vpt * 10 + plan.mb_b;
-    switch (key) {
-        case 11: return launch_t<1, 1>(plan, a, stream);
-        case 12: return launch_t<1, 2>(plan, a, stream);
-        case 21: return launch_t<2, 1>(plan, a, stream);
+template <bool SEL>
+cudaError_t launch_bwd_sel(const MultiPlan& plan, const MultiBwdArgs& a, cudaStream_t stream) {
+    switch (plan.b_vpt * 10 + plan.mb_b) {
+        case 11: return launch_t<1, 1, SEL>(plan, a, stream);
+        case 12: return launch_t<1, 2, SEL>(plan, a, stream);
+        case 21: return launch_t<2, 1, SEL>(plan, a, stream);
         default: return cudaErrorInvalidConfiguration;
     }
+}
+}  // namespace
+
+// plan.E > 0: the selected-query kernels (a query bank and per-token ids)
+int multi_bwd_occupancy(const MultiPlan& plan) {
+    return plan.E > 0 ? bwd_occupancy_sel<true>(plan) : bwd_occupancy_sel<false>(plan);
+}
+
+cudaError_t launch_multi_bwd(const MultiPlan& plan, const MultiBwdArgs& a, cudaStream_t stream) {
+    return a.ids ? launch_bwd_sel<true>(plan, a, stream) : launch_bwd_sel<false>(plan, a, stream);
 }
 
 }  // namespace attnres

@@ -47,7 +47,7 @@ __device__ __forceinline__ uint64_t policy_evict_last() {
     return p;
 }
 
-template <int VPT, int MB>
+template <int VPT, int MB, bool SEL>
 __global__ void __launch_bounds__(kMaxThreads, multi_fwd_ctas_per_sm(VPT))
     attnres_multi_fwd_kernel(const __grid_constant__ MultiFwdArgs a) {
     constexpr int KV = 1 + MB;                     // values reduced per row
@@ -138,8 +138,9 @@ __global__ void __launch_bounds__(kMaxThreads, multi_fwd_ctas_per_sm(VPT))
     const int kv0 = a.kv0, nkv = a.nkv;
     const int kw = nkv * 8;
     const uint32_t kwb = static_cast<uint32_t>(nkv) * 16u;  // bytes per query row in shared memory
-    const bool selected = a.ids != nullptr;                // per-token queries from a bank
+    const bool selected = SEL;                       // per-token queries from a bank (a.ids set)
     const bool q_once = !selected && a.qrows >= M;         // every query stays in shared memory
+    const bool bank_res = selected && a.bank_rows > 0;     // the whole bank stays in shared memory
     int col[VPT];
 #pragma unroll
     for (int i = 0; i < VPT; ++i) {
@@ -198,7 +199,36 @@ __global__ void __launch_bounds__(kMaxThreads, multi_fwd_ctas_per_sm(VPT))
         }
     };
     if (q_once) load_q(0, 0, a.qrows);
+    if (bank_res) {
+        // the bank by key channel, and a zero row (index E) read for ids outside [0, E)
+        if (q_vec) {
+            for (int i = threadIdx.x; i < a.bank_rows * nkv; i += nct) {
+                const int row = i / nkv;
+                uint4 w = make_uint4(0u, 0u, 0u, 0u);
+                if (row < a.E) w = ld_global_nc_v4(a.q + static_cast<long long>(row) * a.R + 8 * (i - row * nkv));
+                *reinterpret_cast<uint4*>(qsm + 8 * i) = w;
+            }
+        } else {
+            for (int i = threadIdx.x; i < a.bank_rows * kw; i += nct) {
+                const int row = i / kw;
+                const int c = 8 * kv0 + (i - row * kw);
+                qsm[i] = (row < a.E && c >= ko && c < kend) ? a.q[static_cast<long long>(row) * a.R + (c - ko)]
+                                                            : static_cast<uint16_t>(0);
+            }
+        }
+    }
     named_bar_sync(1, nct);
+    // Resident bank: lane m < M of every warp holds the bank row of slot m,
+    // loaded one token ahead; an id outside [0, E) is recorded and reads the
+    // zero row.
+    auto row_of = [&](long long id) -> int {
+        if (id < 0 || id >= a.E) {
+            atomicCAS(&g_multi_error, 0u, static_cast<unsigned>(kSiteBadId));
+            return a.E;
+        }
+        return static_cast<int>(id);
+    };
+    long long id_next = (bank_res && lane < M) ? a.ids[static_cast<long long>(blockIdx.x) * M + lane] : 0;
 
     int ck = 0;            // current chunk
     uint32_t cphase = 0;   // its fill parity
@@ -206,15 +236,28 @@ __global__ void __launch_bounds__(kMaxThreads, multi_fwd_ctas_per_sm(VPT))
     int rbuf = 0;
 
     for (long long n = blockIdx.x; n < N; n += gridDim.x) {
+        int my_row = 0;
+        if (bank_res) {
+            my_row = lane < M ? row_of(id_next) : a.E;
+            const long long nn = n + gridDim.x;
+            id_next = (lane < M && nn < N) ? a.ids[nn * M + lane] : 0;
+        }
         for (int b = 0; b < nblk; ++b) {
             const int m0 = b * MB;
             const bool first = b == 0;
-            if (!q_once) {
+            if (!q_once && !bank_res) {
                 // every warp finished the previous block's pass 1 before its last barrier
                 load_q(n, m0, MB);
                 named_bar_sync(1, nct);
             }
             const uint32_t qbase = qsm_s + static_cast<uint32_t>(q_once ? m0 : 0) * kwb;
+            uint32_t qaddr[MB];  // shared-memory row of each query of the block
+#pragma unroll
+            for (int j = 0; j < MB; ++j) {
+                const int r = __shfl_sync(0xffffffffu, my_row, (m0 + j) & 31);
+                qaddr[j] = bank_res ? qsm_s + static_cast<uint32_t>(m0 + j < M ? r : a.E) * kwb
+                                    : qbase + static_cast<uint32_t>(j) * kwb;
+            }
             float2 acc[MB][VPT][4];
 #pragma unroll
             for (int j = 0; j < MB; ++j)
@@ -264,7 +307,7 @@ __global__ void __launch_bounds__(kMaxThreads, multi_fwd_ctas_per_sm(VPT))
                         if (first) bf16_sq8(x, s0, s1);
 #pragma unroll
                         for (int j = 0; j < MB; ++j) {
-                            const uint4 qv = lds128(qbase + static_cast<uint32_t>(j) * kwb + 16u * v);
+                            const uint4 qv = lds128(qaddr[j] + 16u * v);
                             bf16_dot8(x, qv, t[j][0], t[j][1]);
                         }
                     }
@@ -396,9 +439,9 @@ __global__ void __launch_bounds__(kMaxThreads, multi_fwd_ctas_per_sm(VPT))
     }
 }
 
-template <int VPT, int MB>
+template <int VPT, int MB, bool SEL>
 cudaError_t launch_t(const MultiPlan& plan, const MultiFwdArgs& a, cudaStream_t stream) {
-    auto kern = attnres_multi_fwd_kernel<VPT, MB>;
+    auto kern = attnres_multi_fwd_kernel<VPT, MB, SEL>;
     cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                            static_cast<int>(plan.smem_fwd));
     if (err != cudaSuccess) return err;
@@ -406,9 +449,9 @@ cudaError_t launch_t(const MultiPlan& plan, const MultiFwdArgs& a, cudaStream_t 
     return cudaGetLastError();
 }
 
-template <int VPT, int MB>
+template <int VPT, int MB, bool SEL>
 int occupancy_t(const MultiPlan& plan) {
-    auto kern = attnres_multi_fwd_kernel<VPT, MB>;
+    auto kern = attnres_multi_fwd_kernel<VPT, MB, SEL>;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(plan.smem_fwd)) !=
         cudaSuccess)
         return 0;
@@ -427,29 +470,41 @@ unsigned take_multi_fwd_error() {
     return v;
 }
 
-int multi_fwd_occupancy(const MultiPlan& plan) {
+namespace {
+template <bool SEL>
+int fwd_occupancy_sel(const MultiPlan& plan) {
     switch (plan.vpt * 10 + plan.mb_f) {
-        case 11: return occupancy_t<1, 1>(plan);
-        case 12: return occupancy_t<1, 2>(plan);
-        case 14: return occupancy_t<1, 4>(plan);
-        case 21: return occupancy_t<2, 1>(plan);
-        case 22: return occupancy_t<2, 2>(plan);
-        case 41: return occupancy_t<4, 1>(plan);
+        case 11: return occupancy_t<1, 1, SEL>(plan);
+        case 12: return occupancy_t<1, 2, SEL>(plan);
+        case 14: return occupancy_t<1, 4, SEL>(plan);
+        case 21: return occupancy_t<2, 1, SEL>(plan);
+        case 22: return occupancy_t<2, 2, SEL>(plan);
+        case 41: return occupancy_t<4, 1, SEL>(plan);
         default: return 0;
     }
 }
 
-cudaError_t launch_multi_fwd(const MultiPlan& plan, const MultiFwdArgs& a, cudaStream_t stream) {
-    const int key = plan.vpt * 10 + plan.mb_f;
-    switch (key) {
-        case 11: return launch_t<1, 1>(plan, a, stream);
-        case 12: return launch_t<1, 2>(plan, a, stream);
-        case 14: return launch_t<1, 4>(plan, a, stream);
-        case 21: return launch_t<2, 1>(plan, a, stream);
-        case 22: return launch_t<2, 2>(plan, a, stream);
-        case 41: return launch_t<4, 1>(plan, a, stream);
+template <bool SEL>
+cudaError_t launch_fwd_sel(const MultiPlan& plan, const MultiFwdArgs& a, cudaStream_t stream) {
+    switch (plan.vpt * 10 + plan.mb_f) {
+        case 11: return launch_t<1, 1, SEL>(plan, a, stream);
+        case 12: return launch_t<1, 2, SEL>(plan, a, stream);
+        case 14: return launch_t<1, 4, SEL>(plan, a, stream);
+        case 21: return launch_t<2, 1, SEL>(plan, a, stream);
+        case 22: return launch_t<2, 2, SEL>(plan, a, stream);
+        case 41: return launch_t<4, 1, SEL>(plan, a, stream);
         default: return cudaErrorInvalidConfiguration;
     }
+}
+}  // namespace
+
+// plan.E > 0: the selected-query kernels (a query bank and per-token ids)
+int multi_fwd_occupancy(const MultiPlan& plan) {
+    return plan.E > 0 ? fwd_occupancy_sel<true>(plan) : fwd_occupancy_sel<false>(plan);
+}
+
+cudaError_t launch_multi_fwd(const MultiPlan& plan, const MultiFwdArgs& a, cudaStream_t stream) {
+    return a.ids ? launch_fwd_sel<true>(plan, a, stream) : launch_fwd_sel<false>(plan, a, stream);
 }
 
 }  // namespace attnres

@@ -188,14 +188,15 @@ struct MultiLayout {
 };
 
 // Backward layout.  Tables (floats): da[m_pad][s_pad], alpha[s_pad][m_pad],
-// b[s_pad][m_pad], zr[m_pad][s_pad].  qsm: m_pad query rows of nkv 16-byte
-// vectors (bf16).
+// b[s_pad][m_pad], zr[m_pad][s_pad].  qsm: q_rows (default m_pad) query rows
+// of nkv 16-byte vectors (bf16); a resident query bank takes E + 1 rows.
 // dqsm (only when the queries take several register blocks, or per-token
 // queries come from a bank): dq_rows rows (queries, or bank rows) of
 // dq_nkv * 8 FP32 partial sums.
 __host__ __device__ inline MultiLayout make_multi_layout(int chunks, int rows, int slot_bytes, int M,
                                                         int dy_slots, int s_pad, int m_pad, int nkv,
-                                                        int dq_nkv, bool backward, int dq_rows = -1) {
+                                                        int dq_nkv, bool backward, int dq_rows = -1,
+                                                        int q_rows = -1) {
     MultiLayout L;
     uint32_t off = 0;
     L.ring = off;
@@ -223,7 +224,7 @@ __host__ __device__ inline MultiLayout make_multi_layout(int chunks, int rows, i
     off += 4u * m_pad * s_pad * 4u;
     off = align_up(off, 16);
     L.qsm = off;
-    off += static_cast<uint32_t>(m_pad) * static_cast<uint32_t>(nkv) * 16u;
+    off += static_cast<uint32_t>(q_rows < 0 ? m_pad : q_rows) * static_cast<uint32_t>(nkv) * 16u;
     L.dqsm = off;
     off += backward ? static_cast<uint32_t>(dq_rows < 0 ? M : dq_rows) * static_cast<uint32_t>(dq_nkv) * 32u : 0u;
     L.misc = off;  // abort flag
@@ -282,6 +283,8 @@ struct MultiPlan {
     int qrows;             // query rows held in shared memory by the forward
     int bwd_ok;            // the backward's resident layout fits
     int E;                 // query bank rows (selected-query read), 0 otherwise
+    int bank_f, bank_b;    // E + 1 when the bank (plus a zero row) stays in the forward's /
+                           // backward's shared memory for the whole launch, else 0
     int ncw, vpt;          // forward: consumer warps, 16-byte vectors per thread
     int b_ncw, b_vpt;      // backward
     int mb_f, mb_b;        // queries per register block (forward / backward)
@@ -305,6 +308,7 @@ struct MultiFwdArgs {
     const uint16_t* q;     // [M][R], or the query bank [E][R] when ids is set
     const long long* ids;  // [N][M] bank row of every (token, slot), or NULL
     int E;                 // bank rows
+    int bank_rows;         // E + 1: the bank and a zero row stay in qsm (rows as ids), else 0
     uint16_t* y;
     float* alpha;          // [N][M][S]
     float* rstd;           // [N][S]
@@ -329,6 +333,7 @@ struct MultiBwdArgs {
     float* dq_f32;         // [Q][R] or NULL
     const long long* ids;  // [N][M] bank row of every (token, slot), or NULL
     int E;                 // bank rows
+    int bank_rows;         // E + 1: the bank and a zero row stay in qsm (rows as ids), else 0
 };
 
 unsigned take_multi_fwd_error();

@@ -65,6 +65,7 @@ SHAPES = [
     (6, 129, 2048, 512, 9, 3),       # several query blocks in the backward
     (5, 61, 256, 100, 5, 4),         # unaligned key slice (scalar query gather)
     (12, 40, 512, 512, 16, 1),
+    (4, 33, 4096, 4096, 7, 2),       # a bank too large to stay in shared memory
 ]
 
 
@@ -108,12 +109,19 @@ def test_selected_out_of_range_id_is_reported():
     ids = wl.ids.clone()
     ids[5, 1] = 7                          # outside [0, 3)
     v, bank = wl.values.cuda(), wl.bank.cuda()
-    attnres_selected_fwd(v, bank, ids.cuda())
+    f = attnres_selected_fwd(v, bank, ids.cuda())
     torch.cuda.synchronize()
     with pytest.raises(AttnresError) as e:
         attnres_check_device_error()
     assert e.value.name == "ATTNRES_ERR_DEVICE"
     attnres_check_device_error()           # the record was cleared
+    # the backward reports it too; the bad slot adds to no bank row
+    g = attnres_selected_bwd(v, bank, ids.cuda(), wl.dy.cuda(), f)
+    torch.cuda.synchronize()
+    with pytest.raises(AttnresError) as e:
+        attnres_check_device_error()
+    assert e.value.name == "ATTNRES_ERR_DEVICE"
+    assert torch.isfinite(g["dbank_f32"]).all() and torch.isfinite(g["dvalues"].float()).all()
 
 
 def test_selected_autograd_compile():
