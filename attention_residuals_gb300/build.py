@@ -21,8 +21,8 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 LIB_NAME = "libattnres_gb300.so"
 LIB_PATH = os.path.join(PKG, LIB_NAME)
-SOURCES = ["attnres_fwd.cu", "attnres_bwd.cu", "attnres_multi_fwd.cu", "attnres_multi_bwd.cu",
-           "attnres_api.cu", "attnres_host.cu"]
+SOURCES = ["attnres_fwd.cu", "attnres_bwd.cu", "attnres_bwd_norm.cu", "attnres_bwd_opre.cu",
+           "attnres_multi_fwd.cu", "attnres_multi_bwd.cu", "attnres_api.cu", "attnres_host.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

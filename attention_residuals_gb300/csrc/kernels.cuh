@@ -352,6 +352,12 @@ cudaError_t launch_finalize(const float* part, int P, int R, int W, uint16_t* dq
 // of failed waits (read and cleared; 0 = none).
 unsigned take_fwd_error();
 unsigned take_bwd_error();
+// backward kernels with the output norm, by where o comes from (the dispatch
+// in launch_bwd picks them); each unit's wait-failure record
+cudaError_t launch_bwd_norm_rebuild(const Plan& plan, const BwdArgs& a, cudaStream_t stream);
+cudaError_t launch_bwd_norm_saved(const Plan& plan, const BwdArgs& a, cudaStream_t stream);
+unsigned take_bwd_error_rebuild();
+unsigned take_bwd_error_saved();
 cudaError_t launch_fwd(const Plan& plan, const FwdArgs& a, cudaStream_t stream);
 cudaError_t launch_bwd(const Plan& plan, const BwdArgs& a, cudaStream_t stream);
 
