@@ -1,7 +1,8 @@
 // attnres_bwd.cu -- backward launches of the Attention Residuals read
-// operator: the kernels without the output norm (the other modes are
-// instantiated in attnres_bwd_norm.cu and attnres_bwd_opre.cu), the
-// finalize launch, the mode dispatch and the error record.
+// operator: the kernels without the output norm (the run-time mode form;
+// the norm modes are instantiated in attnres_bwd_norm.cu and
+// attnres_bwd_opre.cu), the finalize launch, the mode dispatch and the error
+// record.
 #include "attnres_bwd_kernel.cuh"
 
 namespace attnres {
@@ -21,7 +22,7 @@ unsigned take_bwd_error() {
 }
 
 cudaError_t launch_bwd(const Plan& plan, const BwdArgs& a, cudaStream_t stream) {
-    if (!a.out_norm) return launch_bwd_mode<0>(plan, a, stream);
+    if (!a.out_norm) return launch_bwd_mode<-1>(plan, a, stream);
     return a.o_pre ? launch_bwd_norm_saved(plan, a, stream) : launch_bwd_norm_rebuild(plan, a, stream);
 }
 

@@ -1,8 +1,8 @@
 // attnres_bwd_kernel.cuh -- backward kernel and dq/dw_o finalize of the
 // Attention Residuals read operator, as a template that each including
-// translation unit instantiates for one output-norm mode (NORM: 0 none, 1 o
-// rebuilt from the sources, 2 the caller's FP32 o), so the units compile in
-// parallel and each mode's code carries no branches of the others.
+// translation unit instantiates for one output-norm mode (NORM: 1 o rebuilt
+// from the sources, 2 the caller's FP32 o; -1 the mode read from the
+// arguments at run time), so the units compile in parallel.
 //
 // Per token, with the forward's saved alpha, rstd, logit (and o_rstd when the
 // output RMSNorm is on; "[Perf] Parallelize AttnRes long-sequence
@@ -56,11 +56,16 @@ __device__ __forceinline__ float ldcg_f32(const float* p) { return __ldcg(p); }
 // FULL: every consumer thread owns VPT whole vectors (D == 8 * VPT * 32 * ncw).
 // ADDLAST: a gradient is added to the last source's (a.dlast_add set); a
 // compile-time flag so the plain backward carries none of its code.
-// NORM: output RMSNorm mode (0 none, 1 o rebuilt from the sources, 2 the
-// caller's FP32 o in a.o_pre), fixed by the including unit.
+// NORM: output RMSNorm mode fixed by the including unit: 1 o rebuilt from
+// the sources, 2 the caller's FP32 o in a.o_pre, -1 read from a.out_norm and
+// a.o_pre at run time (the form the launches without the norm use: with
+// the norm code compiled in but skipped, they measured faster than a fixed
+// no-norm mode).
 template <int VPT, bool KEYALL, bool FULL, bool ADDLAST, int NORM>
 __global__ void __launch_bounds__(kMaxThreads, 1) attnres_bwd_kernel(const __grid_constant__ BwdArgs a) {
     extern __shared__ __align__(128) unsigned char smem[];
+    const bool norm_on = NORM < 0 ? a.out_norm != 0 : NORM != 0;  // output RMSNorm
+    const bool o_saved = NORM < 0 ? a.o_pre != nullptr : NORM == 2;  // o from the caller
     const int ncw = a.ncw;
     const int nct = ncw * 32;
     const int K = a.chunks;   // ring depth in chunks
@@ -118,7 +123,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1) attnres_bwd_kernel(const __gri
         const uint32_t key_bytes = key_only ? static_cast<uint32_t>(a.R) * 2u : row_bytes;
         // Passes over the source rows per token: resident -> one; streaming
         // -> (o rebuild when needed), dot pass, write pass (key slices).
-        const int npass = a.resident ? 1 : (NORM == 1 ? 3 : 2);
+        const int npass = a.resident ? 1 : ((norm_on && !o_saved) ? 3 : 2);
         unsigned char* ring = smem + L.ring;
         unsigned char* dyring = smem + L.dyring;
         int k = 0;
@@ -138,7 +143,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1) attnres_bwd_kernel(const __gri
                 cp_async_4(dst + s_pad + e, a.rstd + n * S + e);
                 cp_async_4(dst + 2 * s_pad + e, a.logit + n * S + e);
             }
-            if (NORM != 0 && lane == 0) cp_async_4(dst + 3 * s_pad, a.o_rstd + n);
+            if (norm_on && lane == 0) cp_async_4(dst + 3 * s_pad, a.o_rstd + n);
             cp_async_arrive_noinc(tfull + ts);
             if (++ts == kTokSlots) {
                 ts = 0;
@@ -231,7 +236,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1) attnres_bwd_kernel(const __gri
                 const bool in_key = col[i] >= 0 && j >= ko && j < kend;
                 m |= in_key ? (1u << (2 * kk + h)) : 0u;
                 qv[h] = in_key ? a.scale * bf16_bits_to_float(a.q[j - ko]) : 0.0f;
-                const uint32_t wh = (NORM != 0 && col[i] >= 0) ? a.w_o[j] : 0x3f80u;
+                const uint32_t wh = (norm_on && col[i] >= 0) ? a.w_o[j] : 0x3f80u;
                 wv |= wh << (16 * h);
             }
             qs[i][kk] = make_float2(qv[0], qv[1]);
@@ -332,12 +337,12 @@ __global__ void __launch_bounds__(kMaxThreads, 1) attnres_bwd_kernel(const __gri
 
         // ---- gradient wrt the mixture o (kept in registers)
         float2 dout[VPT][4];
-        if constexpr (NORM != 0) {
+        if (norm_on) {
             // o = sum_s alpha_s v_s in FP32: the caller's saved copy, or
             // rebuilt from the source rows (resident: the rows the other
             // passes use; streaming: a dedicated pass of chunks).
             float2 o[VPT][4];
-            if constexpr (NORM == 2) {
+            if (o_saved) {
                 const float* prow = a.o_pre + n * static_cast<long long>(D);
 #pragma unroll
                 for (int i = 0; i < VPT; ++i) {
@@ -595,7 +600,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1) attnres_bwd_kernel(const __gri
 
     // ---------------------------------------------- per-CTA partial sums
     const int R = a.R;
-    const int Dw = NORM != 0 ? D : 0;
+    const int Dw = norm_on ? D : 0;
     const int W = R + Dw;
     float* my_part = a.part + static_cast<size_t>(blockIdx.x) * W;
 #pragma unroll
@@ -608,7 +613,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1) attnres_bwd_kernel(const __gri
                 const float dwv = (e & 1) ? dw_acc[i][e >> 1].y : dw_acc[i][e >> 1].x;
                 // dq = scale * sum_s dz_s k_s = scale * sum_s c1_s t_s
                 if ((kmask[i] >> e) & 1u) my_part[j - ko] = a.scale * dqv;
-                if (NORM != 0) my_part[R + j] = dwv;
+                if (norm_on) my_part[R + j] = dwv;
             }
         }
     }
@@ -692,7 +697,7 @@ cudaError_t launch_bwd_t(const Plan& plan, const BwdArgs& a, cudaStream_t stream
     kern<<<plan.grid, (plan.b_ncw + 1) * 32, plan.smem_bwd, stream>>>(a);
     err = cudaGetLastError();
     if (err != cudaSuccess || !plan.split) return err;
-    const int W = a.R + (NORM != 0 ? a.D : 0);
+    const int W = a.R + (a.out_norm ? a.D : 0);
     attnres_finalize_kernel<<<(W + 255) / 256, 256, 0, stream>>>(a.part, plan.grid, a.R, W, a.dq,
                                                                  a.dq_f32, a.dw_o, a.dw_o_f32);
     return cudaGetLastError();

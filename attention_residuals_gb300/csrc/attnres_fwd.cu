@@ -47,7 +47,9 @@ __device__ unsigned int g_fwd_error = 0;
 // FULL: every consumer thread owns VPT whole vectors (D == 8 * VPT * 32 * ncw).
 // FUSED: the block-partial sum is formed in the read (a.delta set); a
 // compile-time flag so the plain read carries none of its code.
-template <int VPT, bool FULL, bool FUSED>
+// NORM: output RMSNorm mode (0 none, 1 on, 2 on and the FP32 o also stored
+// to a.o_pre), likewise fixed at compile time.
+template <int VPT, bool FULL, bool FUSED, int NORM>
 __global__ void __launch_bounds__(kMaxThreads, fwd_ctas_per_sm(VPT)) attnres_fwd_kernel(const __grid_constant__ FwdArgs a) {
     extern __shared__ __align__(128) unsigned char smem[];
     const int ncw = a.ncw;
@@ -135,7 +137,7 @@ __global__ void __launch_bounds__(kMaxThreads, fwd_ctas_per_sm(VPT)) attnres_fwd
                     mbar_wait(full + c, static_cast<uint32_t>((fills - 1) & 1), &no_abort, &g_fwd_error, kSiteDrain);
                 }
                 for (int c = 0; c < DSL && c < d_issued; ++c) {
-                    const long long fills = (d_issued - 1 - c) / DSL + 1;
+                    const long long fills = (d_issued - 1 - c) / (DSL > 0 ? DSL : 1) + 1;
                     volatile int no_abort = 0;
                     mbar_wait(dfull + c, static_cast<uint32_t>((fills - 1) & 1), &no_abort, &g_fwd_error, kSiteDrain);
                 }
@@ -160,7 +162,7 @@ __global__ void __launch_bounds__(kMaxThreads, fwd_ctas_per_sm(VPT)) attnres_fwd
 #pragma unroll
             for (int h = 0; h < 2; ++h) {
                 const int j = 8 * c + 2 * kk + h;
-                const uint32_t wh = (a.out_norm && col[i] >= 0) ? a.w_o[j] : 0x3f80u;
+                const uint32_t wh = (NORM != 0 && col[i] >= 0) ? a.w_o[j] : 0x3f80u;
                 wv |= wh << (16 * h);
             }
             ww[kk] = wv;
@@ -374,7 +376,7 @@ __global__ void __launch_bounds__(kMaxThreads, fwd_ctas_per_sm(VPT)) attnres_fwd
         for (int i = 0; i < VPT; ++i)
 #pragma unroll
             for (int kk = 0; kk < 4; ++kk) acc[i][kk] = fmul2(acc[i][kk], inv_l2);
-        if (a.out_norm) {
+        if constexpr (NORM != 0) {
             float2 ss2 = make_float2(0.0f, 0.0f);
 #pragma unroll
             for (int i = 0; i < VPT; ++i)
@@ -390,7 +392,7 @@ __global__ void __launch_bounds__(kMaxThreads, fwd_ctas_per_sm(VPT)) attnres_fwd
             if (threadIdx.x == 0) a.o_rstd[n] = rho;
         }
         uint16_t* yrow = a.y + n * static_cast<long long>(a.D);
-        float* prow = a.o_pre ? a.o_pre + n * static_cast<long long>(a.D) : nullptr;
+        float* prow = NORM == 2 ? a.o_pre + n * static_cast<long long>(a.D) : nullptr;
         const float2 rho2 = make_float2(rho, rho);
 #pragma unroll
         for (int i = 0; i < VPT; ++i) {
@@ -426,9 +428,9 @@ __global__ void __launch_bounds__(kMaxThreads, fwd_ctas_per_sm(VPT)) attnres_fwd
     }
 }
 
-template <int VPT, bool FULL, bool FUSED>
+template <int VPT, bool FULL, bool FUSED, int NORM>
 cudaError_t launch_fwd_t(const Plan& plan, const FwdArgs& a, cudaStream_t stream) {
-    auto kern = attnres_fwd_kernel<VPT, FULL, FUSED>;
+    auto kern = attnres_fwd_kernel<VPT, FULL, FUSED, NORM>;
     cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                            static_cast<int>(plan.smem_fwd));
     if (err != cudaSuccess) return err;
@@ -436,11 +438,18 @@ cudaError_t launch_fwd_t(const Plan& plan, const FwdArgs& a, cudaStream_t stream
     return cudaGetLastError();
 }
 
-template <int VPT>
+template <int VPT, int NORM>
 cudaError_t dispatch_key(const Plan& plan, const FwdArgs& a, cudaStream_t stream) {
-    if (a.delta) return launch_fwd_t<VPT, false, true>(plan, a, stream);  // the general column form
+    if (a.delta) return launch_fwd_t<VPT, false, true, NORM>(plan, a, stream);  // the general column form
     const bool full = (a.D / 8) == VPT * 32 * plan.ncw;
-    return full ? launch_fwd_t<VPT, true, false>(plan, a, stream) : launch_fwd_t<VPT, false, false>(plan, a, stream);
+    return full ? launch_fwd_t<VPT, true, false, NORM>(plan, a, stream)
+                : launch_fwd_t<VPT, false, false, NORM>(plan, a, stream);
+}
+
+template <int VPT>
+cudaError_t dispatch_norm(const Plan& plan, const FwdArgs& a, cudaStream_t stream) {
+    if (!a.out_norm) return dispatch_key<VPT, 0>(plan, a, stream);
+    return a.o_pre ? dispatch_key<VPT, 2>(plan, a, stream) : dispatch_key<VPT, 1>(plan, a, stream);
 }
 
 }  // namespace
@@ -454,9 +463,9 @@ unsigned take_fwd_error() {
 
 cudaError_t launch_fwd(const Plan& plan, const FwdArgs& a, cudaStream_t stream) {
     switch (plan.vpt) {
-        case 1: return dispatch_key<1>(plan, a, stream);
-        case 2: return dispatch_key<2>(plan, a, stream);
-        case 4: return dispatch_key<4>(plan, a, stream);
+        case 1: return dispatch_norm<1>(plan, a, stream);
+        case 2: return dispatch_norm<2>(plan, a, stream);
+        case 4: return dispatch_norm<4>(plan, a, stream);
         default: return cudaErrorInvalidConfiguration;
     }
 }
