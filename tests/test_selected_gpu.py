@@ -124,6 +124,31 @@ def test_selected_out_of_range_id_is_reported():
     assert torch.isfinite(g["dbank_f32"]).all() and torch.isfinite(g["dvalues"].float()).all()
 
 
+def test_selected_bad_id_reads_a_zero_query():
+    # an id outside [0, E) is reported and otherwise acts as a zero query: the
+    # results equal the oracle's with that slot pointing at an extra zero bank
+    # row, and no bank row receives its gradient
+    wl = make_selected(6, 50, 1024, 256, 4, 2, seed=17)
+    ids = wl.ids.clone()
+    ids[7, 0] = -3
+    ids[20, 1] = 9
+    v, bank, dy = wl.values.cuda(), wl.bank.cuda(), wl.dy.cuda()
+    f = attnres_selected_fwd(v, bank, ids.cuda())
+    g = attnres_selected_bwd(v, bank, ids.cuda(), dy, f)
+    torch.cuda.synchronize()
+    with pytest.raises(AttnresError):
+        attnres_check_device_error()
+    zbank = torch.cat([wl.bank, torch.zeros(1, wl.bank.shape[1], dtype=wl.bank.dtype)])
+    zids = ids.clone().numpy()
+    zids[(zids < 0) | (zids >= wl.E)] = wl.E
+    ref = attnres_selected_oracle(wl.values, zbank, zids, dy=wl.dy, key_offset=wl.key_offset)
+    y = to_np(f["y"]).reshape(wl.N, wl.K, wl.D)
+    assert max(y_rel_err(y[:, k], ref["y"][:, k]) for k in range(wl.K)) <= Y_REL
+    assert float(np.max(np.abs(to_np(f["alpha"]) - ref["alpha"]))) <= ALPHA_ABS
+    assert rel_l2(to_np(g["dvalues"]), ref["dvalues"]) <= GRAD_REL_L2
+    assert rel_l2(to_np(g["dbank_f32"]), ref["dbank"][:wl.E]) <= GRAD_REL_L2
+
+
 def test_selected_autograd_compile():
     torch._dynamo.reset()
     wl = make_selected(5, 64, 1024, 128, 4, 2, seed=21)
