@@ -200,12 +200,6 @@ attnres_status check_multi(const attnres_multi_params* p) {
     return ATTNRES_OK;
 }
 
-int pow2_ceil(int x) {
-    int p = 1;
-    while (p < x) p <<= 1;
-    return p;
-}
-
 // Chunk ring for a resident token: the fewest chunks per token that leave
 // room for one more chunk (so the next token starts loading), then as many
 // chunks as fit; as a last resort the token alone.
@@ -235,7 +229,6 @@ attnres_status make_multi_plan(const attnres_multi_params* p, MultiPlan* plan, i
     pl.E = E;  // the occupancy queries below pick the kernels by it
     const int ncv = b.D / 8;
     const int M = p->M;
-    const int p2 = pow2_ceil(M);
     pl.slot_bytes = static_cast<int>(align_up(static_cast<uint32_t>(b.D) * 2u, 128u));
     pl.s_pad = static_cast<int>(align_up(static_cast<uint32_t>(b.S), 4u));
     pl.m_pad = static_cast<int>(align_up(static_cast<uint32_t>(M), 4u));
@@ -251,7 +244,8 @@ attnres_status make_multi_plan(const attnres_multi_params* p, MultiPlan* plan, i
     pl.vpt = ncv <= 256 ? 1 : (ncv <= 512 ? 2 : 4);
     pl.ncw = (ncv + 32 * pl.vpt - 1) / (32 * pl.vpt);
     if (pl.ncw < 1 || pl.ncw > kMaxConsumerWarps) return ATTNRES_ERR_UNSUPPORTED;
-    pl.mb_f = p2 < kMultiMaxMB / pl.vpt ? p2 : kMultiMaxMB / pl.vpt;
+    pl.mq = multi_fixed_m(M);
+    pl.mb_f = multi_fwd_mb(M, pl.vpt);
     const int nblk = (M + pl.mb_f - 1) / pl.mb_f;
     bool fok = false;
     for (int cps = kMultiMaxCtasPerSm; cps >= 1 && !fok; --cps) {
@@ -297,7 +291,7 @@ attnres_status make_multi_plan(const attnres_multi_params* p, MultiPlan* plan, i
     // Backward: a token's rows, its dy rows and the queries stay resident.
     pl.b_vpt = ncv <= 32 * kMultiBwdWarps ? 1 : 2;
     pl.b_ncw = (ncv + 32 * pl.b_vpt - 1) / (32 * pl.b_vpt);
-    pl.mb_b = p2 < 2 / pl.b_vpt ? p2 : 2 / pl.b_vpt;
+    pl.mb_b = multi_bwd_mb(M, pl.b_vpt);
     const int nmb = (M + pl.mb_b - 1) / pl.mb_b;
     const bool dq_in_smem = nmb > 1 || E > 0;
     const int dq_nkv = dq_in_smem ? pl.nkv : 0;

@@ -45,7 +45,7 @@ __device__ __forceinline__ float2 key_part(const float2 x, unsigned mask, int kk
     return make_float2((mask >> (2 * kk)) & 1u ? x.x : 0.0f, (mask >> (2 * kk + 1)) & 1u ? x.y : 0.0f);
 }
 
-template <int VPT, int MB, bool SEL>
+template <int VPT, int MB, bool SEL, int MQ>
 __global__ void __launch_bounds__(kMultiBwdThreads, 1) attnres_multi_bwd_kernel(const __grid_constant__ MultiBwdArgs a) {
     extern __shared__ __align__(128) unsigned char smem[];
     const int ncw = a.ncw;
@@ -53,7 +53,7 @@ __global__ void __launch_bounds__(kMultiBwdThreads, 1) attnres_multi_bwd_kernel(
     const int K = a.chunks;
     const int G = a.rows;
     const int S = a.S;
-    const int M = a.M;
+    const int M = MQ > 0 ? MQ : a.M;  // MQ > 0: the query count is fixed at compile time
     const int DS = a.dy_slots;
     const int s_pad = a.s_pad, m_pad = a.m_pad;
     const int nmb = (M + MB - 1) / MB;
@@ -765,9 +765,9 @@ __global__ void __launch_bounds__(kMultiBwdThreads, 1) attnres_multi_bwd_kernel(
     }
 }
 
-template <int VPT, int MB, bool SEL>
+template <int VPT, int MB, bool SEL, int MQ>
 cudaError_t launch_t(const MultiPlan& plan, const MultiBwdArgs& a, cudaStream_t stream) {
-    auto kern = attnres_multi_bwd_kernel<VPT, MB, SEL>;
+    auto kern = attnres_multi_bwd_kernel<VPT, MB, SEL, MQ>;
     cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                            static_cast<int>(plan.smem_bwd));
     if (err != cudaSuccess) return err;
@@ -779,9 +779,9 @@ cudaError_t launch_t(const MultiPlan& plan, const MultiBwdArgs& a, cudaStream_t 
                            stream);
 }
 
-template <int VPT, int MB, bool SEL>
+template <int VPT, int MB, bool SEL, int MQ>
 int occupancy_t(const MultiPlan& plan) {
-    auto kern = attnres_multi_bwd_kernel<VPT, MB, SEL>;
+    auto kern = attnres_multi_bwd_kernel<VPT, MB, SEL, MQ>;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(plan.smem_bwd)) !=
         cudaSuccess)
         return 0;
@@ -801,23 +801,60 @@ unsigned take_multi_bwd_error() {
 }
 
 namespace {
+// With a fixed query count only the block size the planner derives from it
+// (multi_bwd_mb) is instantiated.
+template <int VPT, int MB, bool SEL, int MQ>
+constexpr bool bwd_reachable() {
+    return MQ == 0 || MB == multi_bwd_mb(MQ, VPT);
+}
+
+template <bool SEL, int MQ>
+int bwd_occupancy_mq(const MultiPlan& plan) {
+#define ATTNRES_OCC(V, B)                                                        \
+    case V * 10 + B:                                                             \
+        if constexpr (bwd_reachable<V, B, SEL, MQ>()) return occupancy_t<V, B, SEL, MQ>(plan); \
+        return 0;
+    switch (plan.b_vpt * 10 + plan.mb_b) {
+        ATTNRES_OCC(1, 1)
+        ATTNRES_OCC(1, 2)
+        ATTNRES_OCC(2, 1)
+        default: return 0;
+    }
+#undef ATTNRES_OCC
+}
+
+template <bool SEL, int MQ>
+cudaError_t launch_bwd_mq(const MultiPlan& plan, const MultiBwdArgs& a, cudaStream_t stream) {
+#define ATTNRES_LAUNCH(V, B)                                                                  \
+    case V * 10 + B:                                                                          \
+        if constexpr (bwd_reachable<V, B, SEL, MQ>()) return launch_t<V, B, SEL, MQ>(plan, a, stream); \
+        return cudaErrorInvalidConfiguration;
+    switch (plan.b_vpt * 10 + plan.mb_b) {
+        ATTNRES_LAUNCH(1, 1)
+        ATTNRES_LAUNCH(1, 2)
+        ATTNRES_LAUNCH(2, 1)
+        default: return cudaErrorInvalidConfiguration;
+    }
+#undef ATTNRES_LAUNCH
+}
+
 template <bool SEL>
 int bwd_occupancy_sel(const MultiPlan& plan) {
-    switch (plan.b_vpt * 10 + plan.mb_b) {
-        case 11: return occupancy_t<1, 1, SEL>(plan);
-        case 12: return occupancy_t<1, 2, SEL>(plan);
-        case 21: return occupancy_t<2, 1, SEL>(plan);
-        default: return 0;
+    switch (plan.mq) {
+        case 1: return bwd_occupancy_mq<SEL, 1>(plan);
+        case 2: return bwd_occupancy_mq<SEL, 2>(plan);
+        case 4: return bwd_occupancy_mq<SEL, 4>(plan);
+        default: return bwd_occupancy_mq<SEL, 0>(plan);
     }
 }
 
 template <bool SEL>
 cudaError_t launch_bwd_sel(const MultiPlan& plan, const MultiBwdArgs& a, cudaStream_t stream) {
-    switch (plan.b_vpt * 10 + plan.mb_b) {
-        case 11: return launch_t<1, 1, SEL>(plan, a, stream);
-        case 12: return launch_t<1, 2, SEL>(plan, a, stream);
-        case 21: return launch_t<2, 1, SEL>(plan, a, stream);
-        default: return cudaErrorInvalidConfiguration;
+    switch (plan.mq) {
+        case 1: return launch_bwd_mq<SEL, 1>(plan, a, stream);
+        case 2: return launch_bwd_mq<SEL, 2>(plan, a, stream);
+        case 4: return launch_bwd_mq<SEL, 4>(plan, a, stream);
+        default: return launch_bwd_mq<SEL, 0>(plan, a, stream);
     }
 }
 }  // namespace

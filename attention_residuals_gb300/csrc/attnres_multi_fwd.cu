@@ -47,7 +47,7 @@ __device__ __forceinline__ uint64_t policy_evict_last() {
     return p;
 }
 
-template <int VPT, int MB, bool SEL>
+template <int VPT, int MB, bool SEL, int MQ>
 __global__ void __launch_bounds__(kMaxThreads, multi_fwd_ctas_per_sm(VPT))
     attnres_multi_fwd_kernel(const __grid_constant__ MultiFwdArgs a) {
     constexpr int KV = 1 + MB;                     // values reduced per row
@@ -59,7 +59,7 @@ __global__ void __launch_bounds__(kMaxThreads, multi_fwd_ctas_per_sm(VPT))
     const int G = a.rows;
     const int GG = a.group;
     const int S = a.S;
-    const int M = a.M;
+    const int M = MQ > 0 ? MQ : a.M;               // MQ > 0: the query count is fixed at compile time
     const int s_pad = a.s_pad;
     const int nblk = (M + MB - 1) / MB;            // register blocks of queries
     // A token that fits in one softmax group is loaded once and every block
@@ -439,9 +439,9 @@ __global__ void __launch_bounds__(kMaxThreads, multi_fwd_ctas_per_sm(VPT))
     }
 }
 
-template <int VPT, int MB, bool SEL>
+template <int VPT, int MB, bool SEL, int MQ>
 cudaError_t launch_t(const MultiPlan& plan, const MultiFwdArgs& a, cudaStream_t stream) {
-    auto kern = attnres_multi_fwd_kernel<VPT, MB, SEL>;
+    auto kern = attnres_multi_fwd_kernel<VPT, MB, SEL, MQ>;
     cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                            static_cast<int>(plan.smem_fwd));
     if (err != cudaSuccess) return err;
@@ -449,9 +449,9 @@ cudaError_t launch_t(const MultiPlan& plan, const MultiFwdArgs& a, cudaStream_t 
     return cudaGetLastError();
 }
 
-template <int VPT, int MB, bool SEL>
+template <int VPT, int MB, bool SEL, int MQ>
 int occupancy_t(const MultiPlan& plan) {
-    auto kern = attnres_multi_fwd_kernel<VPT, MB, SEL>;
+    auto kern = attnres_multi_fwd_kernel<VPT, MB, SEL, MQ>;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(plan.smem_fwd)) !=
         cudaSuccess)
         return 0;
@@ -471,29 +471,66 @@ unsigned take_multi_fwd_error() {
 }
 
 namespace {
+// One (VPT, MB) pair per plan; with a fixed query count only the block size
+// the planner derives from it (multi_fwd_mb) is instantiated.
+template <int VPT, int MB, bool SEL, int MQ>
+constexpr bool fwd_reachable() {
+    return MQ == 0 || MB == multi_fwd_mb(MQ, VPT);
+}
+
+template <bool SEL, int MQ>
+int fwd_occupancy_mq(const MultiPlan& plan) {
+#define ATTNRES_OCC(V, B)                                                        \
+    case V * 10 + B:                                                             \
+        if constexpr (fwd_reachable<V, B, SEL, MQ>()) return occupancy_t<V, B, SEL, MQ>(plan); \
+        return 0;
+    switch (plan.vpt * 10 + plan.mb_f) {
+        ATTNRES_OCC(1, 1)
+        ATTNRES_OCC(1, 2)
+        ATTNRES_OCC(1, 4)
+        ATTNRES_OCC(2, 1)
+        ATTNRES_OCC(2, 2)
+        ATTNRES_OCC(4, 1)
+        default: return 0;
+    }
+#undef ATTNRES_OCC
+}
+
+template <bool SEL, int MQ>
+cudaError_t launch_fwd_mq(const MultiPlan& plan, const MultiFwdArgs& a, cudaStream_t stream) {
+#define ATTNRES_LAUNCH(V, B)                                                                  \
+    case V * 10 + B:                                                                          \
+        if constexpr (fwd_reachable<V, B, SEL, MQ>()) return launch_t<V, B, SEL, MQ>(plan, a, stream); \
+        return cudaErrorInvalidConfiguration;
+    switch (plan.vpt * 10 + plan.mb_f) {
+        ATTNRES_LAUNCH(1, 1)
+        ATTNRES_LAUNCH(1, 2)
+        ATTNRES_LAUNCH(1, 4)
+        ATTNRES_LAUNCH(2, 1)
+        ATTNRES_LAUNCH(2, 2)
+        ATTNRES_LAUNCH(4, 1)
+        default: return cudaErrorInvalidConfiguration;
+    }
+#undef ATTNRES_LAUNCH
+}
+
 template <bool SEL>
 int fwd_occupancy_sel(const MultiPlan& plan) {
-    switch (plan.vpt * 10 + plan.mb_f) {
-        case 11: return occupancy_t<1, 1, SEL>(plan);
-        case 12: return occupancy_t<1, 2, SEL>(plan);
-        case 14: return occupancy_t<1, 4, SEL>(plan);
-        case 21: return occupancy_t<2, 1, SEL>(plan);
-        case 22: return occupancy_t<2, 2, SEL>(plan);
-        case 41: return occupancy_t<4, 1, SEL>(plan);
-        default: return 0;
+    switch (plan.mq) {
+        case 1: return fwd_occupancy_mq<SEL, 1>(plan);
+        case 2: return fwd_occupancy_mq<SEL, 2>(plan);
+        case 4: return fwd_occupancy_mq<SEL, 4>(plan);
+        default: return fwd_occupancy_mq<SEL, 0>(plan);
     }
 }
 
 template <bool SEL>
 cudaError_t launch_fwd_sel(const MultiPlan& plan, const MultiFwdArgs& a, cudaStream_t stream) {
-    switch (plan.vpt * 10 + plan.mb_f) {
-        case 11: return launch_t<1, 1, SEL>(plan, a, stream);
-        case 12: return launch_t<1, 2, SEL>(plan, a, stream);
-        case 14: return launch_t<1, 4, SEL>(plan, a, stream);
-        case 21: return launch_t<2, 1, SEL>(plan, a, stream);
-        case 22: return launch_t<2, 2, SEL>(plan, a, stream);
-        case 41: return launch_t<4, 1, SEL>(plan, a, stream);
-        default: return cudaErrorInvalidConfiguration;
+    switch (plan.mq) {
+        case 1: return launch_fwd_mq<SEL, 1>(plan, a, stream);
+        case 2: return launch_fwd_mq<SEL, 2>(plan, a, stream);
+        case 4: return launch_fwd_mq<SEL, 4>(plan, a, stream);
+        default: return launch_fwd_mq<SEL, 0>(plan, a, stream);
     }
 }
 }  // namespace

@@ -244,6 +244,19 @@ constexpr int kMultiMaxMB = 4;
 // narrower rows (fewer warps) on an SM when they fit.
 __host__ __device__ constexpr int multi_fwd_ctas_per_sm(int vpt) { return vpt <= 2 ? 2 : 1; }
 constexpr int kMultiMaxCtasPerSm = 4;
+// Query counts with their own kernel instantiations (M a compile-time
+// constant: no per-query predicates in the unrolled loops); other counts run
+// the run-time-M kernels.
+__host__ __device__ constexpr int multi_fixed_m(int M) { return (M == 1 || M == 2 || M == 4) ? M : 0; }
+__host__ __device__ constexpr int multi_pow2_ceil(int x) { return x <= 1 ? 1 : 2 * multi_pow2_ceil((x + 1) / 2); }
+// Queries per register block: forward 4 / VPT, backward 2 / VPT, at most the
+// next power of two of M.
+__host__ __device__ constexpr int multi_fwd_mb(int M, int vpt) {
+    return multi_pow2_ceil(M) < kMultiMaxMB / vpt ? multi_pow2_ceil(M) : kMultiMaxMB / vpt;
+}
+__host__ __device__ constexpr int multi_bwd_mb(int M, int vpt) {
+    return multi_pow2_ceil(M) < 2 / vpt ? multi_pow2_ceil(M) : 2 / vpt;
+}
 
 struct MultiFwdLayout {
     uint32_t ring, full, empty, red, zall, rall, qsm, misc, total;
@@ -288,6 +301,7 @@ struct MultiPlan {
     int ncw, vpt;          // forward: consumer warps, 16-byte vectors per thread
     int b_ncw, b_vpt;      // backward
     int mb_f, mb_b;        // queries per register block (forward / backward)
+    int mq;                // M when the kernels are instantiated for it (1, 2 or 4), else 0
     int slot_bytes, s_pad, m_pad;
     int kv0, nkv;          // key window in 16-byte vectors
     int f_rows, f_chunks;  // forward chunk ring
