@@ -61,7 +61,9 @@ __device__ __forceinline__ float ldcg_f32(const float* p) { return __ldcg(p); }
 // a.o_pre at run time (the form the launches without the norm use: with
 // the norm code compiled in but skipped, they measured faster than a fixed
 // no-norm mode).
-template <int VPT, bool KEYALL, bool FULL, bool ADDLAST, int NORM>
+// NJ: groups of 32 sources whose coefficients each lane holds (1: S <= 32,
+// 4: up to 128 sources).
+template <int VPT, bool KEYALL, bool FULL, bool ADDLAST, int NORM, int NJ>
 __global__ void __launch_bounds__(kMaxThreads, 1) attnres_bwd_kernel(const __grid_constant__ BwdArgs a) {
     extern __shared__ __align__(128) unsigned char smem[];
     const bool norm_on = NORM < 0 ? a.out_norm != 0 : NORM != 0;  // output RMSNorm
@@ -479,13 +481,13 @@ __global__ void __launch_bounds__(kMaxThreads, 1) attnres_bwd_kernel(const __gri
         named_bar_sync(1, nct);
 
         // ---- per-source coefficients, computed by every warp (identically)
-        // and kept in registers: lane l holds sources l, l+32, l+64, l+96.
-        float cal[4], ck1[4], ck2[4];
+        // and kept in registers: lane l holds sources l, l+32, ... (NJ of them).
+        float cal[NJ], ck1[NJ], ck2[NJ];
         {
-            float dav[4];
+            float dav[NJ];
             float part_delta = 0.0f;
 #pragma unroll
-            for (int j = 0; j < 4; ++j) {
+            for (int j = 0; j < NJ; ++j) {
                 const int s = lane + 32 * j;
                 float d = 0.0f;
                 if (s < S) {
@@ -496,7 +498,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1) attnres_bwd_kernel(const __gri
             }
             const float delta = warp_sum(part_delta);
 #pragma unroll
-            for (int j = 0; j < 4; ++j) {
+            for (int j = 0; j < NJ; ++j) {
                 const int s = lane + 32 * j;
                 cal[j] = ck1[j] = ck2[j] = 0.0f;
                 if (s < S) {
@@ -536,15 +538,22 @@ __global__ void __launch_bounds__(kMaxThreads, 1) attnres_bwd_kernel(const __gri
                 for (int r = 0; r < gs; ++r) {
                     const int s = g0 + r;
                     float al, k1, k2;
-                    if (S <= 32) {
+                    if constexpr (NJ == 1) {
                         al = __shfl_sync(0xffffffffu, cal[0], s);
                         k1 = __shfl_sync(0xffffffffu, ck1[0], s);
                         k2 = __shfl_sync(0xffffffffu, ck2[0], s);
                     } else {
-                        const int j = s >> 5;
-                        al = __shfl_sync(0xffffffffu, j == 0 ? cal[0] : j == 1 ? cal[1] : j == 2 ? cal[2] : cal[3], s & 31);
-                        k1 = __shfl_sync(0xffffffffu, j == 0 ? ck1[0] : j == 1 ? ck1[1] : j == 2 ? ck1[2] : ck1[3], s & 31);
-                        k2 = __shfl_sync(0xffffffffu, j == 0 ? ck2[0] : j == 1 ? ck2[1] : j == 2 ? ck2[2] : ck2[3], s & 31);
+                        static_assert(NJ == 4, "one or four groups of 32 sources");
+                        if (S <= 32) {
+                            al = __shfl_sync(0xffffffffu, cal[0], s);
+                            k1 = __shfl_sync(0xffffffffu, ck1[0], s);
+                            k2 = __shfl_sync(0xffffffffu, ck2[0], s);
+                        } else {
+                            const int j = s >> 5;
+                            al = __shfl_sync(0xffffffffu, j == 0 ? cal[0] : j == 1 ? cal[1] : j == 2 ? cal[2] : cal[3], s & 31);
+                            k1 = __shfl_sync(0xffffffffu, j == 0 ? ck1[0] : j == 1 ? ck1[1] : j == 2 ? ck1[2] : ck1[3], s & 31);
+                            k2 = __shfl_sync(0xffffffffu, j == 0 ? ck2[0] : j == 1 ? ck2[1] : j == 2 ? ck2[2] : ck2[3], s & 31);
+                        }
                     }
                     const float2 al2 = make_float2(al, al), k12 = make_float2(k1, k1), k22 = make_float2(k2, k2);
                     char* drow = dstride ? dnext : static_cast<char*>(a.dsrc[s]) + row_off;
@@ -688,9 +697,9 @@ __global__ void __launch_bounds__(256) attnres_finalize_kernel(const float* __re
     }
 }
 
-template <int VPT, bool KEYALL, bool FULL, bool ADDLAST, int NORM>
+template <int VPT, bool KEYALL, bool FULL, bool ADDLAST, int NORM, int NJ = 1>
 cudaError_t launch_bwd_t(const Plan& plan, const BwdArgs& a, cudaStream_t stream) {
-    auto kern = attnres_bwd_kernel<VPT, KEYALL, FULL, ADDLAST, NORM>;
+    auto kern = attnres_bwd_kernel<VPT, KEYALL, FULL, ADDLAST, NORM, NJ>;
     cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                            static_cast<int>(plan.smem_bwd));
     if (err != cudaSuccess) return err;
@@ -703,17 +712,31 @@ cudaError_t launch_bwd_t(const Plan& plan, const BwdArgs& a, cudaStream_t stream
     return cudaGetLastError();
 }
 
-template <int VPT, int NORM>
-cudaError_t dispatch_key(const Plan& plan, const BwdArgs& a, cudaStream_t stream) {
+template <int VPT, int NORM, int NJ>
+cudaError_t dispatch_cols(const Plan& plan, const BwdArgs& a, cudaStream_t stream) {
     if (a.dlast_add)  // the general column form
-        return a.R == a.D ? launch_bwd_t<VPT, true, false, true, NORM>(plan, a, stream)
-                          : launch_bwd_t<VPT, false, false, true, NORM>(plan, a, stream);
+        return a.R == a.D ? launch_bwd_t<VPT, true, false, true, NORM, NJ>(plan, a, stream)
+                          : launch_bwd_t<VPT, false, false, true, NORM, NJ>(plan, a, stream);
     const bool full = (a.D / 8) == VPT * 32 * plan.b_ncw;
     if (a.R == a.D)
-        return full ? launch_bwd_t<VPT, true, true, false, NORM>(plan, a, stream)
-                    : launch_bwd_t<VPT, true, false, false, NORM>(plan, a, stream);
-    return full ? launch_bwd_t<VPT, false, true, false, NORM>(plan, a, stream)
-                : launch_bwd_t<VPT, false, false, false, NORM>(plan, a, stream);
+        return full ? launch_bwd_t<VPT, true, true, false, NORM, NJ>(plan, a, stream)
+                    : launch_bwd_t<VPT, true, false, false, NORM, NJ>(plan, a, stream);
+    if constexpr (NORM < 0 && NJ == 1) {
+        return cudaErrorInvalidConfiguration;  // not dispatched (dispatch_key)
+    } else {
+        return full ? launch_bwd_t<VPT, false, true, false, NORM, NJ>(plan, a, stream)
+                    : launch_bwd_t<VPT, false, false, false, NORM, NJ>(plan, a, stream);
+    }
+}
+
+// One group of 32 sources per lane when S <= 32, four otherwise -- except the
+// sliced-key launches without the norm and without an added gradient, whose
+// four-group form measured faster (sliced block shape: 0.394 against 0.415
+// ms; the full-key short shape ran 0.131 against 0.147 ms with one group).
+template <int VPT, int NORM>
+cudaError_t dispatch_key(const Plan& plan, const BwdArgs& a, cudaStream_t stream) {
+    const bool one_group = a.S <= 32 && (NORM >= 0 || a.dlast_add || a.R == a.D);
+    return one_group ? dispatch_cols<VPT, NORM, 1>(plan, a, stream) : dispatch_cols<VPT, NORM, 4>(plan, a, stream);
 }
 
 // Every kernel of this unit's output-norm mode.
