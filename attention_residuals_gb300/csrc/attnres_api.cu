@@ -293,7 +293,7 @@ attnres_status make_multi_plan(const attnres_multi_params* p, MultiPlan* plan, i
     pl.b_ncw = (ncv + 32 * pl.b_vpt - 1) / (32 * pl.b_vpt);
     pl.mb_b = multi_bwd_mb(M, pl.b_vpt);
     const int nmb = (M + pl.mb_b - 1) / pl.mb_b;
-    const bool dq_in_smem = nmb > 1 || E > 0;
+    const bool dq_in_smem = nmb > 1;  // one block: dq in registers (selected: reduced into the workspace)
     const int dq_nkv = dq_in_smem ? pl.nkv : 0;
     const int dq_rows = E > 0 ? E : M;
     pl.bwd_ok = 0;

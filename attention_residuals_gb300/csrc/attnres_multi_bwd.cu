@@ -63,7 +63,9 @@ __global__ void __launch_bounds__(kMultiBwdThreads, 1) attnres_multi_bwd_kernel(
     // added to the bank row's shared-memory sums per token); several blocks:
     // q comes from shared memory per row and dq sums go to shared memory
     const bool regblock = nmb == 1;
-    const bool dq_in_smem = !regblock || selected;
+    // selected queries with one register block add each token's dq straight
+    // into this CTA's workspace row (vector reductions to L2, no return value)
+    const bool dq_in_smem = !regblock;
     const int QR = selected ? a.E : M;       // rows of dq (queries or bank rows)
     // selected queries with one register block: the whole bank (and a zero
     // row, index E) stays in shared memory, addressed by the token's ids
@@ -199,6 +201,22 @@ __global__ void __launch_bounds__(kMultiBwdThreads, 1) attnres_multi_bwd_kernel(
     const int ko = a.ko, kend = a.ko + a.R;
     const int kv0 = a.kv0, nkv = a.nkv;
     const int kw = nkv * 8;
+    // this CTA's FP32 partial rows: part[cta][m * R + (c - ko)], m < QR
+    float* prow = a.part + static_cast<long long>(blockIdx.x) * QR * a.R;
+    // 16-byte reductions need the vector's first key channel 4-aligned in the row
+    const bool red_vec = ((ko & 3) == 0) && ((a.R & 3) == 0);
+    // dq of one owned key vector into bank row m of this CTA's partial rows
+    auto dq_red = [&](int m, int c, unsigned msk, const float2 (&d)[4]) {
+        float* p = prow + static_cast<long long>(m) * a.R + (8 * c - ko);
+        if (red_vec && msk == 0xffu) {
+            red_add_v4(p, d[0].x, d[0].y, d[1].x, d[1].y);
+            red_add_v4(p + 4, d[2].x, d[2].y, d[3].x, d[3].y);
+        } else {
+#pragma unroll
+            for (int e = 0; e < 8; ++e)
+                if ((msk >> e) & 1u) red_add_f32(p + e, (e & 1) ? d[e >> 1].y : d[e >> 1].x);
+        }
+    };
     // dq sums of one owned key vector (eight channels as four pairs) into row m
     auto dq_add = [&](int m, int v, const float2 (&d)[4]) {
         float4* p0 = reinterpret_cast<float4*>(dqsm + m * kw + 4 * v);
@@ -224,6 +242,18 @@ __global__ void __launch_bounds__(kMultiBwdThreads, 1) attnres_multi_bwd_kernel(
             if (kvi[i] >= 0 && j >= ko && j < kend) m |= 1u << e;
         }
         kmask[i] = m;
+    }
+    if (regblock && selected) {
+        // this thread's key channels of the CTA's partial rows start at zero
+        // (the same thread adds to them later, so program order suffices)
+#pragma unroll
+        for (int i = 0; i < VPT; ++i) {
+            if (kvi[i] < 0) continue;
+            for (int m = 0; m < QR; ++m)
+#pragma unroll
+                for (int e = 0; e < 8; ++e)
+                    if ((kmask[i] >> e) & 1u) prow[static_cast<long long>(m) * a.R + (8 * col[i] + e - ko)] = 0.0f;
+        }
     }
     const float inv_r = 1.0f / static_cast<float>(a.R);
     const float scale = a.scale;
@@ -598,7 +628,7 @@ __global__ void __launch_bounds__(kMultiBwdThreads, 1) attnres_multi_bwd_kernel(
                     if (row < 0) continue;
 #pragma unroll
                     for (int i = 0; i < VPT; ++i)
-                        if (kvi[i] >= 0) dq_add(row, kvi[i], dqa[j][i]);
+                        if (kvi[i] >= 0) dq_red(row, col[i], kmask[i], dqa[j][i]);
                 }
             }
         } else {
@@ -736,31 +766,32 @@ __global__ void __launch_bounds__(kMultiBwdThreads, 1) attnres_multi_bwd_kernel(
         }
     }
 
-    // this CTA's FP32 partial row: part[cta][m * R + (c - ko)], m < QR
-    float* prow = a.part + static_cast<long long>(blockIdx.x) * QR * a.R;
+    // the partial rows already hold the reductions of selected queries with one block
+    if (!(regblock && selected)) {
 #pragma unroll
-    for (int i = 0; i < VPT; ++i) {
-        if (kvi[i] < 0) continue;
-        for (int m = 0; m < QR; ++m) {
-            float v8[8];
-            if (regblock && !selected) {
+        for (int i = 0; i < VPT; ++i) {
+            if (kvi[i] < 0) continue;
+            for (int m = 0; m < QR; ++m) {
+                float v8[8];
+                if (regblock && !selected) {
 #pragma unroll
-                for (int j = 0; j < MB; ++j) {
-                    if (j == m) {
+                    for (int j = 0; j < MB; ++j) {
+                        if (j == m) {
 #pragma unroll
-                        for (int kk = 0; kk < 4; ++kk) {
-                            v8[2 * kk] = dqa[j][i][kk].x;
-                            v8[2 * kk + 1] = dqa[j][i][kk].y;
+                            for (int kk = 0; kk < 4; ++kk) {
+                                v8[2 * kk] = dqa[j][i][kk].x;
+                                v8[2 * kk + 1] = dqa[j][i][kk].y;
+                            }
                         }
                     }
+                } else {
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) v8[e] = dqsm[m * kw + (e >> 2) * (kw >> 1) + 4 * kvi[i] + (e & 3)];
                 }
-            } else {
 #pragma unroll
-                for (int e = 0; e < 8; ++e) v8[e] = dqsm[m * kw + (e >> 2) * (kw >> 1) + 4 * kvi[i] + (e & 3)];
+                for (int e = 0; e < 8; ++e)
+                    if ((kmask[i] >> e) & 1u) prow[m * a.R + (8 * col[i] + e - ko)] = v8[e];
             }
-#pragma unroll
-            for (int e = 0; e < 8; ++e)
-                if ((kmask[i] >> e) & 1u) prow[m * a.R + (8 * col[i] + e - ko)] = v8[e];
         }
     }
 }
