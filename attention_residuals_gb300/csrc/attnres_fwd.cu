@@ -273,6 +273,9 @@ __global__ void __launch_bounds__(kMaxThreads, fwd_ctas_per_sm(VPT)) attnres_fwd
                 float s2 = 0.0f, s3 = 0.0f, t2 = 0.0f, t3 = 0.0f;
                 int v = kv0 + lane;
                 if (key_aligned) {
+                    // four iterations unrolled: more of a row's loads in flight
+                    // (measured 0.508 -> 0.489 ms on the long workload)
+#pragma unroll 4
                     for (; v + 32 < kv1; v += 64) {
                         const uint4 x0 = lds128(row_raw + 16u * v);
                         const uint4 q0 = lds128(qsm_s + 16u * v);

@@ -79,6 +79,8 @@ SHAPES = [
     (1, 30, 1024, 512, 512, 4),      # one source
     (12, 161, 2048, 512, 1536, 8),   # M = 8
     (16, 23, 4096, 1024, 3072, 3),   # forward: several softmax groups and two passes per token
+    (9, 77, 2048, 512, 1536, 1),     # one query (the fixed-count kernels for M = 1)
+    (5, 90, 1024, 256, 768, 4),      # M = 4 at one vector per thread: four per forward block
 ]
 
 

@@ -66,6 +66,7 @@ SHAPES = [
     (5, 61, 256, 100, 5, 4),         # unaligned key slice (scalar query gather)
     (12, 40, 512, 512, 16, 1),
     (4, 33, 4096, 4096, 7, 2),       # a bank too large to stay in shared memory
+    (6, 70, 512, 100, 6, 2),         # one register block, unaligned key: per-channel dq reductions
 ]
 
 
