@@ -372,7 +372,9 @@ __global__ void __launch_bounds__(kMaxThreads, 1) attnres_bwd_kernel(const __gri
                     mbar_wait_s(full_s + 8u * k, ph, abort_flag, &g_bwd_error, kSiteBwdConsumer);
                     uint32_t dep = 0;
                     uint32_t rowa = base;
-#pragma unroll 2
+                    // four rows at a time where the norm is fixed on (0.889 -> 0.877 ms
+                    // on the long workload), two in the run-time form
+#pragma unroll(NORM > 0 ? 4 : 2)
                     for (int r = 0; r < gs; ++r) {
                         const float al = tk[g0 + r];
                         const float2 al2 = make_float2(al, al);
