@@ -30,6 +30,13 @@
 // all of the CTA's tokens; with several they accumulate in shared memory.
 // Each CTA writes one FP32 partial row [M * R]; a finalize kernel adds the
 // rows in CTA order (bitwise reproducible).
+// Selected queries (SEL: per-token rows of an [E, R] bank chosen by ids): the
+// bank stays in shared memory when it fits (rows addressed by id, ids loaded
+// one token ahead); with one register block each token's dq is added into
+// the CTA's FP32 partial rows [E * R] in the workspace by vector reductions
+// (every address has one writer thread, so the sums are reproducible), with
+// several blocks it goes through the shared-memory table as for fixed queries.
+// MQ > 0 fixes the query count at compile time (M = 1, 2, 4).
 #include <cfloat>
 
 #include "device_utils.cuh"

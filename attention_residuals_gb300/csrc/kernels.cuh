@@ -190,9 +190,8 @@ struct MultiLayout {
 // Backward layout.  Tables (floats): da[m_pad][s_pad], alpha[s_pad][m_pad],
 // b[s_pad][m_pad], zr[m_pad][s_pad].  qsm: q_rows (default m_pad) query rows
 // of nkv 16-byte vectors (bf16); a resident query bank takes E + 1 rows.
-// dqsm (only when the queries take several register blocks, or per-token
-// queries come from a bank): dq_rows rows (queries, or bank rows) of
-// dq_nkv * 8 FP32 partial sums.
+// dqsm (only when the queries take several register blocks): dq_rows rows
+// (queries, or bank rows) of dq_nkv * 8 FP32 partial sums.
 __host__ __device__ inline MultiLayout make_multi_layout(int chunks, int rows, int slot_bytes, int M,
                                                         int dy_slots, int s_pad, int m_pad, int nkv,
                                                         int dq_nkv, bool backward, int dq_rows = -1,
