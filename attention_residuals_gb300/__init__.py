@@ -12,6 +12,7 @@ from .ops import (  # noqa: F401
     attnres_bwd_workspace_bytes,
     attnres_check_device_error,
     attnres_fwd,
+    attnres_jit_kernel_count,
     attnres_multi,
     attnres_multi_bwd,
     attnres_multi_fwd,

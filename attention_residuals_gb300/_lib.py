@@ -31,6 +31,7 @@ EXPORTED = [
     "attnres_bwd_noalloc",
     "attnres_bwd_workspace_bytes",
     "attnres_check_device_error",
+    "attnres_jit_kernel_count",
     "attnres_status_string",
     "attnres_plan_info",
     "attnres_multi_fwd",
@@ -143,6 +144,8 @@ def load(path: str | None = None):
                                             ctypes.POINTER(ctypes.c_void_p), i64, vp, fp, vp, fp, vp]
         lib.attnres_check_device_error.restype = ctypes.c_int
         lib.attnres_check_device_error.argtypes = []
+        lib.attnres_jit_kernel_count.restype = ctypes.c_int
+        lib.attnres_jit_kernel_count.argtypes = []
         lib.attnres_status_string.restype = ctypes.c_char_p
         lib.attnres_status_string.argtypes = [ctypes.c_int]
         lib.attnres_plan_info.restype = ctypes.c_int

@@ -22,7 +22,11 @@ INCLUDE = os.path.join(ROOT, "include")
 LIB_NAME = "libattnres_gb300.so"
 LIB_PATH = os.path.join(PKG, LIB_NAME)
 SOURCES = ["attnres_fwd.cu", "attnres_bwd.cu", "attnres_bwd_norm.cu", "attnres_bwd_opre.cu",
-           "attnres_multi_fwd.cu", "attnres_multi_bwd.cu", "attnres_api.cu", "attnres_host.cu"]
+           "attnres_multi_fwd.cu", "attnres_multi_bwd.cu", "attnres_api.cu", "attnres_host.cu", "attnres_jit.cu"]
+# Sources the library compiles again at run time for exact plan shapes
+# (attnres_jit.cu): embedded as string literals under their include names.
+JIT_FILES = [("attnres_fwd_kernel.cuh", CSRC), ("device_utils.cuh", CSRC), ("kernels.cuh", CSRC),
+             ("attnres.h", INCLUDE)]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 
@@ -49,16 +53,33 @@ def _stale() -> bool:
     return any(os.path.getmtime(d) > t for d in deps if os.path.isfile(d))
 
 
+def _write_jit_sources(path: str) -> None:
+    delim = "ATTNRES_SRC"
+    parts = ["struct JitFile { const char* name; const char* text; };",
+             "static const JitFile kJitFiles[] = {"]
+    for name, folder in JIT_FILES:
+        with open(os.path.join(folder, name)) as f:
+            text = f.read()
+        if f"){delim}\"" in text:
+            raise RuntimeError(f"{name} contains the raw-string delimiter")
+        parts.append(f'    {{"{name}", R"{delim}({text}){delim}"}},')
+    parts.append("};")
+    with open(path, "w") as f:
+        f.write("\n".join(parts) + "\n")
+
+
 def build(force: bool = False, verbose: bool = False, extra_flags=None) -> str:
     if not force and not _stale():
         return LIB_PATH
     nvcc = _nvcc()
+    tmp = tempfile.mkdtemp(prefix="attnres_build_")
+    libdir = _cuda_lib_dir()
     flags = ["-std=c++17", "-O3", *ARCH, "-lineinfo", "-Xcompiler", "-fPIC", "-I", INCLUDE,
-             "-I", CSRC] + list(extra_flags or [])
+             "-I", CSRC, "-I", tmp, f'-DATTNRES_CUDA_LIBDIR="{libdir}"'] + list(extra_flags or [])
     if verbose:
         flags += ["-Xptxas", "-v"]
-    tmp = tempfile.mkdtemp(prefix="attnres_build_")
     try:
+        _write_jit_sources(os.path.join(tmp, "attnres_jit_sources.inc"))
         def compile_one(src):
             obj = os.path.join(tmp, src.replace(".cu", ".o"))
             cmd = [nvcc, *flags, "-c", os.path.join(CSRC, src), "-o", obj]
@@ -72,9 +93,8 @@ def build(force: bool = False, verbose: bool = False, extra_flags=None) -> str:
         with ThreadPoolExecutor(max_workers=len(SOURCES)) as ex:
             objs = list(ex.map(compile_one, SOURCES))
         out_tmp = os.path.join(tmp, LIB_NAME)
-        libdir = _cuda_lib_dir()
         cmd = [nvcc, *ARCH, "-shared", "-cudart", "shared", *objs, "-o", out_tmp,
-               "-Xlinker", f"-rpath={libdir}"]
+               "-Xlinker", f"-rpath={libdir}", "-ldl"]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
             raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")

@@ -623,6 +623,8 @@ attnres_status attnres_check_device_error(void) {
 // ---------------------------------------------------------------------------
 // Multi-query read.
 // ---------------------------------------------------------------------------
+int attnres_jit_kernel_count(void) { return jit_fwd_kernels(); }
+
 attnres_status attnres_multi_plan_info(const attnres_multi_params* p, int64_t out[8]) {
     attnres_status st = check_multi(p);
     if (st != ATTNRES_OK) return st;

@@ -372,6 +372,15 @@ cudaError_t launch_bwd_norm_saved(const Plan& plan, const BwdArgs& a, cudaStream
 unsigned take_bwd_error_rebuild();
 unsigned take_bwd_error_saved();
 cudaError_t launch_fwd(const Plan& plan, const FwdArgs& a, cudaStream_t stream);
+// The forward compiled at run time for the plan's exact shape (S, rows per
+// chunk, group rows, ring depth as constants); cudaErrorNotSupported when
+// that path is off or unavailable (the caller then launches a precompiled
+// instance).  Its modules' wait-failure records, and how many kernels it holds.
+cudaError_t jit_launch_fwd(const Plan& plan, const FwdArgs& a, cudaStream_t stream);
+unsigned take_jit_fwd_error();
+int jit_fwd_kernels();
+// Tokens from which a forward launch uses the run-time-compiled kernel.
+constexpr long long kJitMinTokens = 1024;
 cudaError_t launch_bwd(const Plan& plan, const BwdArgs& a, cudaStream_t stream);
 
 }  // namespace attnres

@@ -149,6 +149,11 @@ def attnres_check_device_error() -> None:
     _lib.check(_lib.load().attnres_check_device_error(), "attnres_check_device_error")
 
 
+def attnres_jit_kernel_count() -> int:
+    """Forward kernels compiled at run time for exact plan shapes in this process."""
+    return int(_lib.load().attnres_jit_kernel_count())
+
+
 def attnres_fwd(values: Sources, q: torch.Tensor, *, w_o: Optional[torch.Tensor] = None,
                 eps: float = EPS_DEFAULT, scale: float = 1.0, key_offset: Optional[int] = None,
                 save_o_pre: Optional[bool] = None, stream=None, out: Optional[dict] = None) -> dict:
