@@ -25,8 +25,8 @@ SOURCES = ["attnres_fwd.cu", "attnres_bwd.cu", "attnres_bwd_norm.cu", "attnres_b
            "attnres_multi_fwd.cu", "attnres_multi_bwd.cu", "attnres_api.cu", "attnres_host.cu", "attnres_jit.cu"]
 # Sources the library compiles again at run time for exact plan shapes
 # (attnres_jit.cu): embedded as string literals under their include names.
-JIT_FILES = [("attnres_fwd_kernel.cuh", CSRC), ("device_utils.cuh", CSRC), ("kernels.cuh", CSRC),
-             ("attnres.h", INCLUDE)]
+JIT_FILES = [("attnres_fwd_kernel.cuh", CSRC), ("attnres_multi_fwd_kernel.cuh", CSRC), ("device_utils.cuh", CSRC),
+             ("kernels.cuh", CSRC), ("attnres.h", INCLUDE)]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

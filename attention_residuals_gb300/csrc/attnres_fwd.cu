@@ -38,7 +38,7 @@ unsigned take_fwd_error() {
     unsigned v = 0, zero = 0;
     if (cudaMemcpyFromSymbol(&v, g_fwd_error, sizeof v) != cudaSuccess) return 0xffffffffu;
     if (v) cudaMemcpyToSymbol(g_fwd_error, &zero, sizeof zero);
-    const unsigned j = take_jit_fwd_error();  // read (and cleared) either way
+    const unsigned j = take_jit_error(0);  // read (and cleared) either way
     return v ? v : j;
 }
 

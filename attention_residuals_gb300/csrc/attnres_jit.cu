@@ -1,7 +1,8 @@
-// attnres_jit.cu -- run-time compiled forward kernels for one plan's exact
-// shape.
+// attnres_jit.cu -- run-time compiled forward kernels (single- and
+// multi-query) for one plan's exact shape.
 //
-// The forward template (attnres_fwd_kernel.cuh) takes the source count, the
+// The forward templates (attnres_fwd_kernel.cuh, attnres_multi_fwd_kernel.cuh)
+// take the source count, the
 // rows per chunk, the softmax group rows and the ring depth either from its
 // arguments (the precompiled instances) or as template constants.  With the
 // constants the compiler unrolls a token's whole schedule (its groups, their
@@ -69,6 +70,7 @@ struct Api {
                              CUstream, void**, void**) = nullptr;
     CUresult (*memcpyDtoH)(void*, CUdeviceptr, size_t) = nullptr;
     CUresult (*memcpyHtoD)(CUdeviceptr, const void*, size_t) = nullptr;
+    CUresult (*occupancy)(int*, CUfunction, int, size_t) = nullptr;
 };
 
 template <typename F>
@@ -94,13 +96,16 @@ const Api& api() {
                sym(cu, "cuModuleGetFunction", &a.moduleGetFunction) &&
                sym(cu, "cuModuleGetGlobal_v2", &a.moduleGetGlobal) &&
                sym(cu, "cuFuncSetAttribute", &a.funcSetAttribute) && sym(cu, "cuLaunchKernel", &a.launchKernel) &&
-               sym(cu, "cuMemcpyDtoH_v2", &a.memcpyDtoH) && sym(cu, "cuMemcpyHtoD_v2", &a.memcpyHtoD);
+               sym(cu, "cuMemcpyDtoH_v2", &a.memcpyDtoH) && sym(cu, "cuMemcpyHtoD_v2", &a.memcpyHtoD) &&
+               sym(cu, "cuOccupancyMaxActiveBlocksPerMultiprocessor", &a.occupancy);
     });
     return a;
 }
 
-// One compiled kernel: a plan shape on one device.
-using Key = std::tuple<int, int, int, int, int, int, int, int, int>;  // device, VPT, FULL, FUSED, NORM, S, G, GG, K
+// One compiled kernel: a plan shape on one device.  kind 0: the single-query
+// forward <VPT, FULL, FUSED, NORM, S, G, GG, K>; kind 1: the multi-query
+// forward <VPT, MB, SEL, MQ, S, G, GG, K>.
+using Key = std::tuple<int, int, int, int, int, int, int, int, int, int>;  // device, kind, eight template values
 struct Entry {
     bool ok = false;
     CUmodule mod = nullptr;
@@ -121,8 +126,9 @@ Entry compile(const Key& k) {
     Entry e;
     const Api& A = api();
     if (!A.ok) return e;
-    const int vpt = std::get<1>(k), full = std::get<2>(k), fused = std::get<3>(k), norm = std::get<4>(k);
-    const int S = std::get<5>(k), G = std::get<6>(k), GG = std::get<7>(k), K = std::get<8>(k);
+    const int kind = std::get<1>(k);
+    const int t0 = std::get<2>(k), t1 = std::get<3>(k), t2 = std::get<4>(k), t3 = std::get<5>(k);
+    const int S = std::get<6>(k), G = std::get<7>(k), GG = std::get<8>(k), K = std::get<9>(k);
     std::vector<const char*> bodies, names;
     for (const auto& f : kJitFiles) {
         names.push_back(f.name);
@@ -134,11 +140,16 @@ Entry compile(const Key& k) {
         names.push_back(sys_names[i]);
         bodies.push_back(sys_bodies[i]);
     }
-    const char* src = "#define ATTNRES_FWD_NS jit\n#include \"attnres_fwd_kernel.cuh\"\n";
-    char expr[160];
-    std::snprintf(expr, sizeof expr, "attnres::jit::attnres_fwd_kernel<%d, %s, %s, %d, %d, %d, %d, %d>", vpt,
-                  full ? "true" : "false", fused ? "true" : "false", norm, S, G, GG, K);
-    const char* err_expr = "&attnres::jit::g_fwd_error";
+    const char* src = kind == 0 ? "#define ATTNRES_FWD_NS jit\n#include \"attnres_fwd_kernel.cuh\"\n"
+                                : "#define ATTNRES_FWD_NS jit\n#include \"attnres_multi_fwd_kernel.cuh\"\n";
+    char expr[192];
+    if (kind == 0)
+        std::snprintf(expr, sizeof expr, "attnres::jit::attnres_fwd_kernel<%d, %s, %s, %d, %d, %d, %d, %d>", t0,
+                      t1 ? "true" : "false", t2 ? "true" : "false", t3, S, G, GG, K);
+    else
+        std::snprintf(expr, sizeof expr, "attnres::jit::attnres_multi_fwd_kernel<%d, %d, %s, %d, %d, %d, %d, %d>",
+                      t0, t1, t2 ? "true" : "false", t3, S, G, GG, K);
+    const char* err_expr = kind == 0 ? "&attnres::jit::g_fwd_error" : "&attnres::jit::g_multi_error";
     nvrtcProgram prog;
     if (A.createProgram(&prog, src, "attnres_fwd_jit.cu", static_cast<int>(bodies.size()), bodies.data(),
                         names.data()) != NVRTC_SUCCESS)
@@ -174,16 +185,12 @@ Entry compile(const Key& k) {
     return e;
 }
 
-}  // namespace
 
-cudaError_t jit_launch_fwd(const Plan& plan, const FwdArgs& a, cudaStream_t stream) {
-    if (!jit_enabled()) return cudaErrorNotSupported;
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess) return cudaErrorNotSupported;
-    const int fused = a.delta ? 1 : 0;
-    const int full = (!fused && (a.D / 8) == plan.vpt * 32 * plan.ncw) ? 1 : 0;
-    const int norm = !a.out_norm ? 0 : (a.o_pre ? 2 : 1);
-    const Key k{dev, plan.vpt, full, fused, norm, a.S, a.rows, a.group, a.chunks};
+// Compile (once) and launch the kernel for key k with one struct argument.
+// `ctas_per_sm` is what the plan counted on: a compiled kernel that fits
+// fewer is not used.
+cudaError_t launch_key(const Key& k, unsigned grid, unsigned block, int smem, int ctas_per_sm, const void* args,
+                       cudaStream_t stream) {
     Entry* e = nullptr;
     {
         std::lock_guard<std::mutex> lock(g_mu);
@@ -191,30 +198,63 @@ cudaError_t jit_launch_fwd(const Plan& plan, const FwdArgs& a, cudaStream_t stre
         if (it == g_cache.end()) it = g_cache.emplace(k, compile(k)).first;
         e = &it->second;
         if (!e->ok) return cudaErrorNotSupported;
-        if (e->smem < static_cast<int>(plan.smem_fwd)) {
-            if (api().funcSetAttribute(e->fn, CU_FUNC_ATTRIBUTE_MAX_DYNAMIC_SHARED_SIZE_BYTES,
-                                       static_cast<int>(plan.smem_fwd)) != CUDA_SUCCESS)
+        if (e->smem < smem) {
+            int fit = 0;
+            if (api().funcSetAttribute(e->fn, CU_FUNC_ATTRIBUTE_MAX_DYNAMIC_SHARED_SIZE_BYTES, smem) != CUDA_SUCCESS ||
+                api().occupancy(&fit, e->fn, static_cast<int>(block), static_cast<size_t>(smem)) != CUDA_SUCCESS ||
+                fit < ctas_per_sm) {
+                e->ok = false;  // keep the precompiled kernels for this shape
                 return cudaErrorNotSupported;
-            e->smem = static_cast<int>(plan.smem_fwd);
+            }
+            e->smem = smem;
         }
     }
-    FwdArgs args = a;
-    void* params[] = {&args};
-    const CUresult r = api().launchKernel(e->fn, static_cast<unsigned>(plan.fgrid), 1, 1,
-                                          static_cast<unsigned>((plan.ncw + 1) * 32), 1, 1,
-                                          static_cast<unsigned>(plan.smem_fwd), reinterpret_cast<CUstream>(stream),
-                                          params, nullptr);
+    void* params[] = {const_cast<void*>(args)};
+    const CUresult r = api().launchKernel(e->fn, grid, 1, 1, block, 1, 1, static_cast<unsigned>(smem),
+                                          reinterpret_cast<CUstream>(stream), params, nullptr);
     return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorLaunchFailure;
 }
 
-unsigned take_jit_fwd_error() {
+int sm_count() {
+    int dev = 0, n = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+        return 0;
+    return n;
+}
+
+}  // namespace
+
+cudaError_t jit_launch_fwd(const Plan& plan, const FwdArgs& a, cudaStream_t stream) {
+    if (!jit_enabled()) return cudaErrorNotSupported;
+    int dev = 0;
+    const int sms = sm_count();
+    if (cudaGetDevice(&dev) != cudaSuccess || sms == 0) return cudaErrorNotSupported;
+    const int fused = a.delta ? 1 : 0;
+    const int full = (!fused && (a.D / 8) == plan.vpt * 32 * plan.ncw) ? 1 : 0;
+    const int norm = !a.out_norm ? 0 : (a.o_pre ? 2 : 1);
+    const Key k{dev, 0, plan.vpt, full, fused, norm, a.S, a.rows, a.group, a.chunks};
+    return launch_key(k, static_cast<unsigned>(plan.fgrid), static_cast<unsigned>((plan.ncw + 1) * 32),
+                      static_cast<int>(plan.smem_fwd), (plan.fgrid + sms - 1) / sms, &a, stream);
+}
+
+cudaError_t jit_launch_multi_fwd(const MultiPlan& plan, const MultiFwdArgs& a, cudaStream_t stream) {
+    if (!jit_enabled()) return cudaErrorNotSupported;
+    int dev = 0;
+    const int sms = sm_count();
+    if (cudaGetDevice(&dev) != cudaSuccess || sms == 0) return cudaErrorNotSupported;
+    const Key k{dev, 1, plan.vpt, plan.mb_f, a.ids ? 1 : 0, plan.mq, a.S, a.rows, a.group, a.chunks};
+    return launch_key(k, static_cast<unsigned>(plan.fgrid), static_cast<unsigned>((plan.ncw + 1) * 32),
+                      static_cast<int>(plan.smem_fwd), (plan.fgrid + sms - 1) / sms, &a, stream);
+}
+
+unsigned take_jit_error(int kind) {
     std::lock_guard<std::mutex> lock(g_mu);
     unsigned first = 0;
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return 0;
     for (auto& kv : g_cache) {
         Entry& e = kv.second;
-        if (!e.ok || std::get<0>(kv.first) != dev) continue;
+        if (!e.mod || !e.err || std::get<0>(kv.first) != dev || std::get<1>(kv.first) != kind) continue;
         unsigned v = 0;
         if (api().memcpyDtoH(&v, e.err, sizeof v) != CUDA_SUCCESS) return 0xffffffffu;
         if (v) {

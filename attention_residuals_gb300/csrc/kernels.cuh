@@ -372,12 +372,13 @@ cudaError_t launch_bwd_norm_saved(const Plan& plan, const BwdArgs& a, cudaStream
 unsigned take_bwd_error_rebuild();
 unsigned take_bwd_error_saved();
 cudaError_t launch_fwd(const Plan& plan, const FwdArgs& a, cudaStream_t stream);
-// The forward compiled at run time for the plan's exact shape (S, rows per
+// The forwards compiled at run time for the plan's exact shape (S, rows per
 // chunk, group rows, ring depth as constants); cudaErrorNotSupported when
 // that path is off or unavailable (the caller then launches a precompiled
 // instance).  Its modules' wait-failure records, and how many kernels it holds.
 cudaError_t jit_launch_fwd(const Plan& plan, const FwdArgs& a, cudaStream_t stream);
-unsigned take_jit_fwd_error();
+cudaError_t jit_launch_multi_fwd(const MultiPlan& plan, const MultiFwdArgs& a, cudaStream_t stream);
+unsigned take_jit_error(int kind);  // 0: single-query forward, 1: multi-query forward
 int jit_fwd_kernels();
 // Tokens from which a forward launch uses the run-time-compiled kernel.
 constexpr long long kJitMinTokens = 1024;

@@ -283,10 +283,10 @@ const char* attnres_status_string(attnres_status s);
 attnres_status attnres_plan_info(const attnres_params* p, int64_t out[8]);
 
 /*
- * Forward launches of at least 1024 tokens run a kernel compiled at run time
- * (NVRTC) for the plan's exact shape -- the source count, rows per chunk,
- * softmax group rows and ring depth as constants -- once per shape and
- * device in a process; when NVRTC or the driver library cannot be opened, or
+ * Forward launches (single- and multi-query) of at least 1024 tokens run a
+ * kernel compiled at run time (NVRTC) for the plan's exact shape -- the
+ * source count, rows per chunk, softmax group rows and ring depth as
+ * constants -- once per shape and device in a process; when NVRTC or the driver library cannot be opened, or
  * a compile fails, the precompiled kernels run instead.  ATTNRES_JIT=0 in
  * the environment turns the run-time path off.  This call returns how many
  * such kernels this process holds (a diagnostic; never fails).

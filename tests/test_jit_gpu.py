@@ -62,3 +62,26 @@ def test_runtime_compiled_fused_partial_forward(monkeypatch):
     attnres_check_device_error()
     for k in ("y", "alpha", "partial_new"):
         assert torch.equal(outs[0][k], outs[1][k]), k
+
+
+@pytest.mark.parametrize("selected", [False, True])
+def test_runtime_compiled_multi_forward_matches_precompiled(monkeypatch, selected):
+    from attention_residuals_gb300 import attnres_multi_fwd, attnres_selected_fwd
+    from attention_residuals_gb300.workloads import make_multi, make_selected
+    outs = []
+    if selected:
+        wl = make_selected(10, 2048, 4096, 1024, 8, 2, seed=12, src_scale=(0.5, 2.0), device="cuda")
+        run = lambda: attnres_selected_fwd(wl.values, wl.bank, wl.ids)
+    else:
+        wl = make_multi(10, 2048, 4096, 1024, 2, seed=13, src_scale=(0.5, 2.0), device="cuda")
+        run = lambda: attnres_multi_fwd(wl.values, wl.queries)
+    for jit in (False, True):
+        monkeypatch.setenv("ATTNRES_JIT", "1" if jit else "0")
+        before = attnres_jit_kernel_count()
+        outs.append(run())
+        torch.cuda.synchronize()
+        if jit:
+            assert attnres_jit_kernel_count() >= max(before, 1)
+    attnres_check_device_error()
+    for k in ("y", "alpha", "rstd", "logit"):
+        assert torch.equal(outs[0][k], outs[1][k]), k
