@@ -784,7 +784,8 @@ def run_ours(args):
         "roofline": {"bound": "hbm", "kernel": work.roofline_kernel,
                      "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "peak_kind": f"{peak_kind} HBM copy bandwidth",
-                     "traffic": work.traffic()},
+                     # the committed counters describe the full-size launch only
+                     "traffic": work.traffic() if args.tokens in (None, FULL_TOKENS[args.workload]) else None},
         "clocks": clocks,
         "gpu_launches": work.launches * K,
         "e2e": e2e,
