@@ -195,7 +195,15 @@ cudaError_t launch_key(const Key& k, unsigned grid, unsigned block, int smem, in
     {
         std::lock_guard<std::mutex> lock(g_mu);
         auto it = g_cache.find(k);
-        if (it == g_cache.end()) it = g_cache.emplace(k, compile(k)).first;
+        if (it == g_cache.end()) {
+            // Compiling and loading a module are not stream work: during a
+            // CUDA-graph capture they could invalidate it, so a shape first
+            // seen there runs the precompiled kernel (and compiles later).
+            cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+            if (cudaStreamIsCapturing(stream, &cap) != cudaSuccess || cap != cudaStreamCaptureStatusNone)
+                return cudaErrorNotSupported;
+            it = g_cache.emplace(k, compile(k)).first;
+        }
         e = &it->second;
         if (!e->ok) return cudaErrorNotSupported;
         if (e->smem < smem) {
