@@ -8,9 +8,14 @@ kernels ("Fast Attention Residuals", Quickstart: the read is compiled with
 fullgraph=True and replayed in CUDA graphs).  The operators compute nothing
 themselves: every step runs in the CUDA library.
 
-Values travel as a list: either one packed [S, ..., D] tensor or S separate
-[..., D] tensors; the gradient comes back in the same form (a packed input
-gets one packed gradient, with no stacking copy).
+Values travel as a list plus a `packed` flag: either one packed
+[S, ..., D] tensor (packed=True) or S separate [..., D] tensors; the
+gradient comes back in the same form (a packed input gets one packed
+gradient, with no stacking copy).  The flag is explicit because a list of
+one [T, D] source and one packed [S, D] tensor (one token) have the same
+shape.  The backward operators also return the FP32 sums of the reduced
+gradients (dq, dw_o, the bank gradient) next to their bf16 roundings;
+autograd uses the bf16 copies.
 """
 from __future__ import annotations
 
@@ -26,11 +31,20 @@ from . import ops as _ops
 _NS = "attnres_gb300"
 
 
-def _shape_info(values: List[Tensor], R: int) -> Tuple[int, int, int, tuple]:
-    if len(values) == 1 and values[0].dim() >= 2:
+def _shape_info(values: List[Tensor], packed: bool) -> Tuple[int, int, int, tuple]:
+    if packed:
+        if len(values) != 1 or values[0].dim() < 2:
+            raise ValueError("packed values are one [S, ..., D] tensor")
         v = values[0]
         return v.shape[0], v.shape[-1], 1, tuple(v.shape[1:-1])
     return len(values), values[0].shape[-1], 0, tuple(values[0].shape[:-1])
+
+
+def _pack_args(values):
+    """(list of tensors, packed flag) for a user's values argument."""
+    if isinstance(values, Tensor):
+        return [values], True
+    return list(values), False
 
 
 def _bwd_resident(S: int, D: int, R: int, key_offset: int, out_norm: bool) -> bool:
@@ -50,8 +64,8 @@ def _as_values(values: List[Tensor], packed: int):
 
 @torch.library.custom_op(f"{_NS}::read_fwd", mutates_args=(), device_types="cuda")
 def read_fwd(values: List[Tensor], q: Tensor, w_o: Optional[Tensor], eps: float, scale: float,
-             key_offset: int) -> Tuple[Tensor, Tensor, Tensor, Tensor, Tensor, Tensor]:
-    S, D, packed, lead = _shape_info(values, q.numel())
+             key_offset: int, packed: bool) -> Tuple[Tensor, Tensor, Tensor, Tensor, Tensor, Tensor]:
+    S, D, packed, lead = _shape_info(values, packed)
     save = w_o is not None and not _bwd_resident(S, D, q.numel(), key_offset, True)
     r = _ops.attnres_fwd(_as_values(values, packed), q, w_o=w_o, eps=eps, scale=scale,
                          key_offset=key_offset, save_o_pre=save)
@@ -63,8 +77,8 @@ def read_fwd(values: List[Tensor], q: Tensor, w_o: Optional[Tensor], eps: float,
 
 
 @read_fwd.register_fake
-def _(values, q, w_o, eps, scale, key_offset):
-    S, D, packed, lead = _shape_info(values, q.numel())
+def _(values, q, w_o, eps, scale, key_offset, packed):
+    S, D, packed, lead = _shape_info(values, packed)
     N = 1
     for d in lead:
         N *= d
@@ -84,8 +98,8 @@ def _(values, q, w_o, eps, scale, key_offset):
 @torch.library.custom_op(f"{_NS}::read_bwd", mutates_args=(), device_types="cuda")
 def read_bwd(values: List[Tensor], q: Tensor, w_o: Optional[Tensor], dy: Tensor, alpha: Tensor,
              rstd: Tensor, logit: Tensor, o_rstd: Tensor, o_pre: Tensor, eps: float, scale: float,
-             key_offset: int) -> Tuple[List[Tensor], Tensor, Tensor]:
-    S, D, packed, lead = _shape_info(values, q.numel())
+             key_offset: int, packed: bool) -> Tuple[List[Tensor], Tensor, Tensor, Tensor, Tensor]:
+    S, D, packed, lead = _shape_info(values, packed)
     saved = {"alpha": alpha, "rstd": rstd, "logit": logit,
              "o_rstd": o_rstd if o_rstd.numel() else None,
              "o_pre": o_pre if o_pre.numel() else None}
@@ -93,21 +107,25 @@ def read_bwd(values: List[Tensor], q: Tensor, w_o: Optional[Tensor], dy: Tensor,
                          scale=scale, key_offset=key_offset)
     dv = [g["dvalues"]] if packed else list(g["dvalues"])
     dw = g["dw_o"] if g["dw_o"] is not None else torch.empty((0,), dtype=torch.bfloat16, device=q.device)
-    return dv, g["dq"].view_as(q), dw
+    dw32 = g["dw_o_f32"] if g["dw_o_f32"] is not None else torch.empty((0,), dtype=torch.float32,
+                                                                        device=q.device)
+    return dv, g["dq"].view_as(q), dw, g["dq_f32"].view(q.shape), dw32
 
 
 @read_bwd.register_fake
-def _(values, q, w_o, dy, alpha, rstd, logit, o_rstd, o_pre, eps, scale, key_offset):
+def _(values, q, w_o, dy, alpha, rstd, logit, o_rstd, o_pre, eps, scale, key_offset, packed):
     dv = [torch.empty_like(v) for v in values]
     dw = torch.empty_like(w_o) if w_o is not None else torch.empty((0,), dtype=torch.bfloat16,
                                                                    device=q.device)
-    return dv, torch.empty_like(q), dw
+    f32 = dict(dtype=torch.float32, device=q.device)
+    dw32 = torch.empty(w_o.shape if w_o is not None else (0,), **f32)
+    return dv, torch.empty_like(q), dw, torch.empty(q.shape, **f32), dw32
 
 
 def _setup_context(ctx, inputs, output):
-    values, q, w_o, eps, scale, key_offset = inputs
+    values, q, w_o, eps, scale, key_offset, packed = inputs
     y, alpha, rstd, logit, o_rstd, o_pre = output
-    ctx.cfg = (eps, scale, key_offset)
+    ctx.cfg = (eps, scale, key_offset, packed)
     ctx.has_w = w_o is not None
     ctx.nvalues = len(values)
     ctx.save_for_backward(q, w_o if w_o is not None else q.new_empty((0,)), alpha, rstd, logit,
@@ -116,10 +134,10 @@ def _setup_context(ctx, inputs, output):
 
 def _backward(ctx, dy, d_alpha, d_rstd, d_logit, d_orstd, d_opre):
     q, w_o, alpha, rstd, logit, o_rstd, o_pre, *values = ctx.saved_tensors
-    eps, scale, key_offset = ctx.cfg
-    dv, dq, dw = read_bwd(list(values), q, w_o if ctx.has_w else None, dy.to(torch.bfloat16),
-                          alpha, rstd, logit, o_rstd, o_pre, eps, scale, key_offset)
-    return list(dv), dq, (dw if ctx.has_w else None), None, None, None
+    eps, scale, key_offset, packed = ctx.cfg
+    dv, dq, dw, _, _ = read_bwd(list(values), q, w_o if ctx.has_w else None, dy.to(torch.bfloat16),
+                                alpha, rstd, logit, o_rstd, o_pre, eps, scale, key_offset, packed)
+    return list(dv), dq, (dw if ctx.has_w else None), None, None, None, None
 
 
 read_fwd.register_autograd(_backward, setup_context=_setup_context)
@@ -128,10 +146,10 @@ read_fwd.register_autograd(_backward, setup_context=_setup_context)
 def attnres_op(values, query: Tensor, *, eps: float = _ops.EPS_DEFAULT, scale: float = 1.0,
                out_norm_weight: Optional[Tensor] = None, key_offset: Optional[int] = None) -> Tensor:
     """The read through the registered operator (compile- and graph-safe)."""
-    vals = [values] if isinstance(values, Tensor) else list(values)
+    vals, packed = _pack_args(values)
     D = vals[0].shape[-1]
     ko = D - query.numel() if key_offset is None else int(key_offset)
-    y = read_fwd(vals, query, out_norm_weight, float(eps), float(scale), ko)[0]
+    y = read_fwd(vals, query, out_norm_weight, float(eps), float(scale), ko, packed)[0]
     return y
 
 
@@ -144,16 +162,16 @@ def _multi_out_shape(lead, M: int, D: int, token_major: bool):
 
 @torch.library.custom_op(f"{_NS}::read_multi_fwd", mutates_args=(), device_types="cuda")
 def read_multi_fwd(values: List[Tensor], queries: Tensor, eps: float, scale: float, key_offset: int,
-                   token_major: bool) -> Tuple[Tensor, Tensor, Tensor, Tensor]:
-    S, D, packed, lead = _shape_info(values, queries.shape[-1])
+                   token_major: bool, packed: bool) -> Tuple[Tensor, Tensor, Tensor, Tensor]:
+    S, D, packed, lead = _shape_info(values, packed)
     r = _ops.attnres_multi_fwd(_as_values(values, packed), queries, eps=eps, scale=scale,
                                key_offset=key_offset, token_major=token_major)
     return r["y"], r["alpha"], r["rstd"], r["logit"]
 
 
 @read_multi_fwd.register_fake
-def _(values, queries, eps, scale, key_offset, token_major):
-    S, D, packed, lead = _shape_info(values, queries.shape[-1])
+def _(values, queries, eps, scale, key_offset, token_major, packed):
+    S, D, packed, lead = _shape_info(values, packed)
     M = queries.shape[0]
     N = 1
     for d in lead:
@@ -167,33 +185,34 @@ def _(values, queries, eps, scale, key_offset, token_major):
 @torch.library.custom_op(f"{_NS}::read_multi_bwd", mutates_args=(), device_types="cuda")
 def read_multi_bwd(values: List[Tensor], queries: Tensor, dy: Tensor, alpha: Tensor, rstd: Tensor,
                    logit: Tensor, eps: float, scale: float, key_offset: int,
-                   token_major: bool) -> Tuple[List[Tensor], Tensor]:
-    S, D, packed, lead = _shape_info(values, queries.shape[-1])
+                   token_major: bool, packed: bool) -> Tuple[List[Tensor], Tensor, Tensor]:
+    S, D, packed, lead = _shape_info(values, packed)
     saved = {"alpha": alpha, "rstd": rstd, "logit": logit, "token_major": token_major}
     g = _ops.attnres_multi_bwd(_as_values(values, packed), queries, dy.contiguous(), saved, eps=eps,
                                scale=scale, key_offset=key_offset, token_major=token_major)
     dv = [g["dvalues"]] if packed else list(g["dvalues"])
-    return dv, g["dq"]
+    return dv, g["dq"], g["dq_f32"]
 
 
 @read_multi_bwd.register_fake
-def _(values, queries, dy, alpha, rstd, logit, eps, scale, key_offset, token_major):
-    return [torch.empty_like(v) for v in values], torch.empty_like(queries)
+def _(values, queries, dy, alpha, rstd, logit, eps, scale, key_offset, token_major, packed):
+    return ([torch.empty_like(v) for v in values], torch.empty_like(queries),
+            torch.empty(queries.shape, dtype=torch.float32, device=queries.device))
 
 
 def _multi_setup_context(ctx, inputs, output):
-    values, queries, eps, scale, key_offset, token_major = inputs
+    values, queries, eps, scale, key_offset, token_major, packed = inputs
     y, alpha, rstd, logit = output
-    ctx.cfg = (eps, scale, key_offset, token_major)
+    ctx.cfg = (eps, scale, key_offset, token_major, packed)
     ctx.save_for_backward(queries, alpha, rstd, logit, *values)
 
 
 def _multi_backward(ctx, dy, d_alpha, d_rstd, d_logit):
     queries, alpha, rstd, logit, *values = ctx.saved_tensors
-    eps, scale, key_offset, token_major = ctx.cfg
-    dv, dq = read_multi_bwd(list(values), queries, dy.to(torch.bfloat16), alpha, rstd, logit, eps,
-                            scale, key_offset, token_major)
-    return list(dv), dq, None, None, None, None
+    eps, scale, key_offset, token_major, packed = ctx.cfg
+    dv, dq, _ = read_multi_bwd(list(values), queries, dy.to(torch.bfloat16), alpha, rstd, logit, eps,
+                               scale, key_offset, token_major, packed)
+    return list(dv), dq, None, None, None, None, None
 
 
 read_multi_fwd.register_autograd(_multi_backward, setup_context=_multi_setup_context)
@@ -204,11 +223,11 @@ def attnres_multi_op(values, queries: Tensor, *, eps: float = _ops.EPS_DEFAULT, 
     """The multi-query read through the registered operator."""
     if output_layout not in ("query_major", "token_major"):
         raise ValueError("output_layout must be 'query_major' or 'token_major'")
-    vals = [values] if isinstance(values, Tensor) else list(values)
+    vals, packed = _pack_args(values)
     D = vals[0].shape[-1]
     ko = D - queries.shape[-1] if key_offset is None else int(key_offset)
     return read_multi_fwd(vals, queries, float(eps), float(scale), ko,
-                          output_layout == "token_major")[0]
+                          output_layout == "token_major", packed)[0]
 
 
 # --------------------------------------------------------------------------
@@ -217,16 +236,16 @@ def attnres_multi_op(values, queries: Tensor, *, eps: float = _ops.EPS_DEFAULT, 
 # --------------------------------------------------------------------------
 @torch.library.custom_op(f"{_NS}::read_selected_fwd", mutates_args=(), device_types="cuda")
 def read_selected_fwd(values: List[Tensor], bank: Tensor, ids: Tensor, eps: float, scale: float,
-                      key_offset: int) -> Tuple[Tensor, Tensor, Tensor, Tensor]:
-    S, D, packed, lead = _shape_info(values, bank.shape[-1])
+                      key_offset: int, packed: bool) -> Tuple[Tensor, Tensor, Tensor, Tensor]:
+    S, D, packed, lead = _shape_info(values, packed)
     r = _ops.attnres_selected_fwd(_as_values(values, packed), bank, ids, eps=eps, scale=scale,
                                   key_offset=key_offset)
     return r["y"], r["alpha"], r["rstd"], r["logit"]
 
 
 @read_selected_fwd.register_fake
-def _(values, bank, ids, eps, scale, key_offset):
-    S, D, packed, lead = _shape_info(values, bank.shape[-1])
+def _(values, bank, ids, eps, scale, key_offset, packed):
+    S, D, packed, lead = _shape_info(values, packed)
     K = ids.shape[-1]
     N = 1
     for d in lead:
@@ -239,33 +258,34 @@ def _(values, bank, ids, eps, scale, key_offset):
 @torch.library.custom_op(f"{_NS}::read_selected_bwd", mutates_args=(), device_types="cuda")
 def read_selected_bwd(values: List[Tensor], bank: Tensor, ids: Tensor, dy: Tensor, alpha: Tensor,
                       rstd: Tensor, logit: Tensor, eps: float, scale: float,
-                      key_offset: int) -> Tuple[List[Tensor], Tensor]:
-    S, D, packed, lead = _shape_info(values, bank.shape[-1])
+                      key_offset: int, packed: bool) -> Tuple[List[Tensor], Tensor, Tensor]:
+    S, D, packed, lead = _shape_info(values, packed)
     saved = {"alpha": alpha, "rstd": rstd, "logit": logit}
     g = _ops.attnres_selected_bwd(_as_values(values, packed), bank, ids, dy.contiguous(), saved, eps=eps,
                                   scale=scale, key_offset=key_offset)
     dv = [g["dvalues"]] if packed else list(g["dvalues"])
-    return dv, g["dbank"]
+    return dv, g["dbank"], g["dbank_f32"]
 
 
 @read_selected_bwd.register_fake
-def _(values, bank, ids, dy, alpha, rstd, logit, eps, scale, key_offset):
-    return [torch.empty_like(v) for v in values], torch.empty_like(bank)
+def _(values, bank, ids, dy, alpha, rstd, logit, eps, scale, key_offset, packed):
+    return ([torch.empty_like(v) for v in values], torch.empty_like(bank),
+            torch.empty(bank.shape, dtype=torch.float32, device=bank.device))
 
 
 def _sel_setup_context(ctx, inputs, output):
-    values, bank, ids, eps, scale, key_offset = inputs
+    values, bank, ids, eps, scale, key_offset, packed = inputs
     y, alpha, rstd, logit = output
-    ctx.cfg = (eps, scale, key_offset)
+    ctx.cfg = (eps, scale, key_offset, packed)
     ctx.save_for_backward(bank, ids, alpha, rstd, logit, *values)
 
 
 def _sel_backward(ctx, dy, d_alpha, d_rstd, d_logit):
     bank, ids, alpha, rstd, logit, *values = ctx.saved_tensors
-    eps, scale, key_offset = ctx.cfg
-    dv, db = read_selected_bwd(list(values), bank, ids, dy.to(torch.bfloat16), alpha, rstd, logit, eps,
-                               scale, key_offset)
-    return list(dv), db, None, None, None, None
+    eps, scale, key_offset, packed = ctx.cfg
+    dv, db, _ = read_selected_bwd(list(values), bank, ids, dy.to(torch.bfloat16), alpha, rstd, logit, eps,
+                                  scale, key_offset, packed)
+    return list(dv), db, None, None, None, None, None
 
 
 read_selected_fwd.register_autograd(_sel_backward, setup_context=_sel_setup_context)
@@ -274,10 +294,10 @@ read_selected_fwd.register_autograd(_sel_backward, setup_context=_sel_setup_cont
 def attnres_selected_op(values, query_bank: Tensor, ids: Tensor, *, eps: float = _ops.EPS_DEFAULT,
                         scale: float = 1.0, key_offset: Optional[int] = None) -> Tensor:
     """The selected-query read through the registered operator."""
-    vals = [values] if isinstance(values, Tensor) else list(values)
+    vals, packed = _pack_args(values)
     D = vals[0].shape[-1]
     ko = D - query_bank.shape[-1] if key_offset is None else int(key_offset)
-    return read_selected_fwd(vals, query_bank, ids, float(eps), float(scale), ko)[0]
+    return read_selected_fwd(vals, query_bank, ids, float(eps), float(scale), ko, packed)[0]
 
 
 # --------------------------------------------------------------------------
@@ -321,19 +341,24 @@ def _(values, delta, q, w_o, eps, scale, key_offset):
 def read_block_bwd(completed: List[Tensor], partial_new: Tensor, q: Tensor, w_o: Optional[Tensor], dy: Tensor,
                    g_partial: Optional[Tensor], alpha: Tensor, rstd: Tensor, logit: Tensor, o_rstd: Tensor,
                    o_pre: Tensor, eps: float, scale: float,
-                   key_offset: int) -> Tuple[List[Tensor], Tensor, Tensor, Tensor]:
+                   key_offset: int) -> Tuple[List[Tensor], Tensor, Tensor, Tensor, Tensor, Tensor]:
     saved = {"alpha": alpha, "rstd": rstd, "logit": logit,
              "o_rstd": o_rstd if o_rstd.numel() else None, "o_pre": o_pre if o_pre.numel() else None}
     g = _ops.attnres_partial_bwd(list(completed), partial_new, q, dy, saved, g_partial=g_partial, w_o=w_o,
                                  eps=eps, scale=scale, key_offset=key_offset)
     dw = g["dw_o"] if g["dw_o"] is not None else torch.empty((0,), dtype=torch.bfloat16, device=q.device)
-    return g["d_completed"], g["d_partial"], g["dq"].view_as(q), dw
+    dw32 = g["dw_o_f32"] if g["dw_o_f32"] is not None else torch.empty((0,), dtype=torch.float32,
+                                                                        device=q.device)
+    return g["d_completed"], g["d_partial"], g["dq"].view_as(q), dw, g["dq_f32"].view(q.shape), dw32
 
 
 @read_block_bwd.register_fake
 def _(completed, partial_new, q, w_o, dy, g_partial, alpha, rstd, logit, o_rstd, o_pre, eps, scale, key_offset):
     dw = torch.empty_like(w_o) if w_o is not None else torch.empty((0,), dtype=torch.bfloat16, device=q.device)
-    return [torch.empty_like(c) for c in completed], torch.empty_like(partial_new), torch.empty_like(q), dw
+    f32 = dict(dtype=torch.float32, device=q.device)
+    dw32 = torch.empty(w_o.shape if w_o is not None else (0,), **f32)
+    return ([torch.empty_like(c) for c in completed], torch.empty_like(partial_new), torch.empty_like(q), dw,
+            torch.empty(q.shape, **f32), dw32)
 
 
 def _block_setup_context(ctx, inputs, output):
@@ -352,9 +377,9 @@ def _block_backward(ctx, dy, d_partial_new, d_alpha, d_rstd, d_logit, d_orstd, d
     if dy is None:
         dy = torch.zeros_like(partial_new)
     g = None if d_partial_new is None else d_partial_new.to(torch.bfloat16)
-    dcomp, dpart, dq, dw = read_block_bwd(list(completed), partial_new, q, w_o if ctx.has_w else None,
-                                          dy.to(torch.bfloat16), g, alpha, rstd, logit, o_rstd, o_pre, eps,
-                                          scale, key_offset)
+    dcomp, dpart, dq, dw, _, _ = read_block_bwd(list(completed), partial_new, q, w_o if ctx.has_w else None,
+                                                dy.to(torch.bfloat16), g, alpha, rstd, logit, o_rstd, o_pre,
+                                                eps, scale, key_offset)
     return list(dcomp) + [dpart], dpart, dq, (dw if ctx.has_w else None), None, None, None
 
 

@@ -120,6 +120,29 @@ def _check_vec(t: Optional[torch.Tensor], n: int, name: str):
     return t.contiguous()
 
 
+def _check_out(t: Optional[torch.Tensor], n: int, dtype: torch.dtype, name: str, device) -> None:
+    """A caller-supplied output: contiguous, on the sources' device, n elements of dtype."""
+    if t is None:
+        return
+    if t.dtype != dtype or t.device != device or t.numel() != n or not t.is_contiguous():
+        raise TypeError(f"{name} must be a contiguous {dtype} tensor with {n} elements on {device}")
+
+
+def _out_rows(t: torch.Tensor, N: int, D: int, name: str) -> torch.Tensor:
+    """[N, D] rows of a caller-supplied gradient buffer, without a copy: the
+    kernel writes through this view, so a copy would leave the caller's
+    buffer untouched."""
+    if t.dtype != torch.bfloat16 or not t.is_cuda or t.numel() != N * D:
+        raise TypeError(f"{name} must be a CUDA bf16 tensor of {N} rows of {D}")
+    try:
+        r = t.view(N, D)
+    except RuntimeError as e:
+        raise ValueError(f"{name}: rows must be addressable as [N, D] with unit column stride") from e
+    if N > 1 and r.stride(1) != 1:
+        raise ValueError(f"{name}: rows must have unit column stride")
+    return r
+
+
 # --------------------------------------------------------------------------
 # C-ABI mirrors
 # --------------------------------------------------------------------------
@@ -221,11 +244,13 @@ def attnres_bwd(values: Sources, q: torch.Tensor, dy: torch.Tensor, saved: dict,
     else:
         if isinstance(dvalues, torch.Tensor):
             dpacked = dvalues
-            drows = [dvalues[s].reshape(N, D) for s in range(S)]
+            drows = [_out_rows(dvalues[s], N, D, "dvalues") for s in range(S)]
         else:
             dpacked = None
-            drows = [d.reshape(N, D) for d in dvalues]
+            drows = [_out_rows(d, N, D, "dvalues") for d in dvalues]
     dld = int(drows[0].stride(0)) if N > 1 else D
+    if N > 1 and any(int(r.stride(0)) != dld for r in drows):
+        raise ValueError("dvalues: every source's gradient rows need the same row stride")
     dptrs = (ctypes.c_void_p * S)(*[r.data_ptr() for r in drows])
     dq = torch.empty((R,), dtype=torch.bfloat16, device=dev)
     dq32 = torch.empty((R,), dtype=torch.float32, device=dev)
@@ -271,16 +296,22 @@ def attnres_bwd_noalloc(values: Sources, q: torch.Tensor, dy: torch.Tensor, save
     dev = view.rows[0].device
     if dy.dtype != torch.bfloat16 or not dy.is_cuda or dy.numel() != N * D:
         raise TypeError("dy must be a CUDA bf16 tensor shaped like the output")
-    dy2 = dy.reshape(N, D)
-    if not dy2.is_contiguous():
+    if not dy.is_contiguous():
         raise ValueError("dy must be contiguous (the no-allocation path makes no copies)")
+    dy2 = dy.view(N, D)
     if dvalues is None or dq is None or (w_o is not None and dw_o is None):
         raise ValueError("the no-allocation path needs preallocated dvalues, dq (and dw_o)")
+    _check_out(dq, R, torch.bfloat16, "dq", dev)
+    _check_out(dq_f32, R, torch.float32, "dq_f32", dev)
+    _check_out(dw_o, D, torch.bfloat16, "dw_o", dev)
+    _check_out(dw_o_f32, D, torch.float32, "dw_o_f32", dev)
     if isinstance(dvalues, torch.Tensor):
-        drows = [dvalues[s].reshape(N, D) for s in range(S)]
+        drows = [_out_rows(dvalues[s], N, D, "dvalues") for s in range(S)]
     else:
-        drows = [d.reshape(N, D) for d in dvalues]
+        drows = [_out_rows(d, N, D, "dvalues") for d in dvalues]
     dld = int(drows[0].stride(0)) if N > 1 else D
+    if N > 1 and any(int(r.stride(0)) != dld for r in drows):
+        raise ValueError("dvalues: every source's gradient rows need the same row stride")
     dptrs = (ctypes.c_void_p * S)(*[r.data_ptr() for r in drows])
     rc = _lib.load().attnres_bwd_noalloc(
         ctypes.byref(p), _ptr(q), _ptr(w_o), _ptr(dy2), _ptr(saved["alpha"]), _ptr(saved["rstd"]),
@@ -396,8 +427,13 @@ def attnres_partial_fwd(completed: Sources, partial: torch.Tensor, delta: torch.
     q = _check_vec(q, R, "q")
     w_o = _check_vec(w_o, D, "w_o")
     d2 = _row2d(delta, N, D, "delta")
-    pout = torch.empty((N, D), dtype=torch.bfloat16, device=view.rows[0].device) if partial_out is None \
-        else _row2d(partial_out, N, D, "partial_out")
+    if partial_out is None:
+        pout = torch.empty((N, D), dtype=torch.bfloat16, device=view.rows[0].device)
+    else:
+        # written in place: a view of the caller's buffer, never a copy
+        pout = _out_rows(partial_out, N, D, "partial_out")
+        if (N > 1 and pout.stride(0) != D) or pout.data_ptr() % 16:
+            raise ValueError("partial_out must be contiguous [.., D] rows starting on 16 bytes")
     p = make_params(view, R, key_offset=key_offset, eps=eps, scale=scale, out_norm=w_o is not None)
     S, dev = len(view.rows), view.rows[0].device
     f32 = dict(dtype=torch.float32, device=dev)

@@ -17,7 +17,9 @@ from attention_residuals_gb300 import (attnres_check_device_error, attnres_multi
 from attention_residuals_gb300._lib import AttnresError
 from attention_residuals_gb300.workloads import make_multi, make_multi_workload
 from oracle.multi import attnres_multi_oracle
-from parity_utils import (ALPHA_ABS, GRAD_REL_L2, STAT_REL, Y_REL, bf16_rne, rel_l2, to_np,
+from op_grads import multi_grads
+from parity_utils import (ALPHA_ABS, GRAD_REL_L2, STAT_REL, Y_REL, bf16_rne, check_dvalues, check_vec_grad,
+                          rel_l2, to_np,
                           y_rel_err)
 
 pytestmark = pytest.mark.gpu
@@ -39,11 +41,8 @@ def _check(wl, fwd, bwd, ref, token_major, tag):
         assert errs["logit"] <= STAT_REL, (tag, errs)
     assert errs["y"] <= Y_REL, (tag, errs)
     if bwd is not None:
-        errs["dvalues"] = rel_l2(to_np(bwd["dvalues"]).reshape(S, N, D), ref["dvalues"])
-        errs["dq_f32"] = rel_l2(to_np(bwd["dq_f32"]), ref["dq"])
-        assert errs["dvalues"] <= GRAD_REL_L2, (tag, errs)
-        assert errs["dq_f32"] <= GRAD_REL_L2, (tag, errs)
-        np.testing.assert_array_equal(to_np(bwd["dq"]), bf16_rne(to_np(bwd["dq_f32"])))
+        check_dvalues(to_np(bwd["dvalues"]).reshape(S, N, D), ref["dvalues"], errs, tag)
+        check_vec_grad(bwd["dq"], bwd["dq_f32"], ref["dq"], errs, tag, "dq")
     return errs
 
 
@@ -167,10 +166,13 @@ def test_multi_autograd_compile_and_shared_sources():
     vref = torch.stack([wl.values[i] for i in (0, 1, 0, 2)])
     ref = attnres_multi_oracle(vref, wl.queries, dy=wl.dy, key_offset=1024 - 256)
     assert max(y_rel_err(to_np(y[m]), ref["y"][m]) for m in range(2)) <= Y_REL
-    assert rel_l2(to_np(x[0].grad), ref["dvalues"][0] + ref["dvalues"][2]) <= GRAD_REL_L2
-    assert rel_l2(to_np(x[2].grad), ref["dvalues"][3]) <= GRAD_REL_L2
-    # autograd returns the bf16 dq; its rounding alone is up to 2^-8 per element
-    assert rel_l2(to_np(Q.grad), ref["dq"]) <= 4e-3
+    check_dvalues(to_np(x[0].grad), ref["dvalues"][0] + ref["dvalues"][2], {}, "shared x0")
+    check_dvalues(to_np(x[2].grad), ref["dvalues"][3], {}, "x2")
+    # autograd's bf16 dq is the operator's, bit for bit; its FP32 sum is held to
+    # the tolerance and the bf16 copy must be that sum's RNE rounding
+    g = multi_grads([x[0], x[1], x[0], x[2]], Q, wl.dy.cuda())
+    assert torch.equal(Q.grad, g["dq"])
+    check_vec_grad(g["dq"], g["dq_f32"], ref["dq"], {}, "autograd", "dq")
     yt = attnres_multi(torch.stack([t.detach() for t in x]), Q.detach(), output_layout="token_major")
     assert yt.shape == (90, 2, 1024)
 
@@ -193,8 +195,7 @@ def test_multi_long_full_size_sampled():
     y = to_np(fwd["y"].index_select(1, it))
     assert max(y_rel_err(y[m], ref["y"][m]) for m in range(wl.M)) <= Y_REL
     assert float(np.max(np.abs(to_np(fwd["alpha"].index_select(0, it)) - ref["alpha"]))) <= ALPHA_ABS
-    assert rel_l2(to_np(bwd["dvalues"].index_select(1, it)), ref["dvalues"]) <= GRAD_REL_L2
+    check_dvalues(to_np(bwd["dvalues"].index_select(1, it)), ref["dvalues"], {}, "full")
     full = attnres_multi_oracle(v.cpu(), Q.cpu(), dy=dy.cpu(), key_offset=wl.key_offset,
                                 want_dvalues=False)
-    assert rel_l2(to_np(bwd["dq_f32"]), full["dq"]) <= GRAD_REL_L2
-    np.testing.assert_array_equal(to_np(bwd["dq"]), bf16_rne(to_np(bwd["dq_f32"])))
+    check_vec_grad(bwd["dq"], bwd["dq_f32"], full["dq"], {}, "full", "dq")

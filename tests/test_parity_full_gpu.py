@@ -15,7 +15,7 @@ import torch
 from attention_residuals_gb300 import attnres_bwd, attnres_fwd, attnres_plan_info
 from attention_residuals_gb300.workloads import make_workload
 from oracle import attnres_oracle
-from parity_utils import GRAD_REL_L2, bf16_rne, check_forward, rel_l2, to_np
+from parity_utils import check_dvalues, check_forward, check_vec_grad, to_np
 
 pytestmark = pytest.mark.gpu
 
@@ -56,18 +56,12 @@ def test_full_size(cfg, ko):
            "rstd": fwd["rstd"].index_select(0, it), "logit": fwd["logit"].index_select(0, it),
            "o_rstd": None if fwd["o_rstd"] is None else fwd["o_rstd"].index_select(0, it)}
     errs = check_forward(sub, ref, out_norm=wl.out_norm, tag=f"cfg{cfg} ko={ko}")
-    dv = to_np(bwd["dvalues"].index_select(1, it))
-    errs["dvalues"] = rel_l2(dv, ref["dvalues"])
-    assert errs["dvalues"] <= GRAD_REL_L2, errs
+    check_dvalues(to_np(bwd["dvalues"].index_select(1, it)), ref["dvalues"], errs, f"cfg{cfg}")
 
     # dq / dw_o over all tokens
     full = attnres_oracle(v.cpu(), q.cpu(), w_o=None if w is None else w.cpu(), dy=dy.cpu(),
                           key_offset=ko, want_dvalues=False)
-    errs["dq_f32"] = rel_l2(to_np(bwd["dq_f32"]), full["dq"])
-    assert errs["dq_f32"] <= GRAD_REL_L2, errs
-    np.testing.assert_array_equal(to_np(bwd["dq"]), bf16_rne(to_np(bwd["dq_f32"])))
+    check_vec_grad(bwd["dq"], bwd["dq_f32"], full["dq"], errs, f"cfg{cfg}", "dq")
     if wl.out_norm:
-        errs["dw_o_f32"] = rel_l2(to_np(bwd["dw_o_f32"]), full["dw_o"])
-        assert errs["dw_o_f32"] <= GRAD_REL_L2, errs
-        np.testing.assert_array_equal(to_np(bwd["dw_o"]), bf16_rne(to_np(bwd["dw_o_f32"])))
+        check_vec_grad(bwd["dw_o"], bwd["dw_o_f32"], full["dw_o"], errs, f"cfg{cfg}", "dw_o")
     print(f"cfg{cfg} ko={ko} plan={info} errs={errs}")
