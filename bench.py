@@ -9,10 +9,25 @@ N=32768 tokens, D=4096, bf16, output RMSNorm on (the shape of the first row
 of the benchmark table in "[Perf] Parallelize AttnRes long-sequence
 reduction", Test plan).
 
-`--workload multi`: one step = attnres_multi_fwd + attnres_multi_bwd with
-M=2 queries of rank R=1024 over the same S=10, N=32768, D=4096 sources
-("Fast Attention Residuals", section "Multi-query AttnRes": two queries
-route two roles from one read).
+The other rows of that table and the pages' other workloads have their own
+lines, each the same contract with its own byte model:
+  `--workload short`   S=8, N=8192, D=2048 (the table's last row; dq and
+                       dw_o reduced inside the backward launch, N < 16384)
+  `--workload sliced`  the Block schedule's sliced read: 8 block sums + the
+                       partial sum (S=9), N=16384, D=4096, R=1024, 2% zero
+                       rows; one step reads with the key in the first R
+                       channels and again with it in the final R channels
+                       ("Fast Attention Residuals", sections "Full and Block
+                       schedules" and "Sliced LR-AttnRes")
+  `--workload deep`    S=64, N=8192, D=8192, output RMSNorm on (the table's
+                       third row; 8.6 GB of sources)
+  `--workload multi`   attnres_multi_fwd + attnres_multi_bwd with M=2
+                       queries of rank R=1024 over the long workload's
+                       sources ("Fast Attention Residuals", section
+                       "Multi-query AttnRes": two queries route two roles
+                       from one read)
+  `--workload selected`  per-token queries from an 8-row bank, K=2 slots
+  `--workload block`   the fused block-partial read
 
 The metric is effective HBM bandwidth: the algorithmic bytes one step must
 move (sources read in the forward and again in the backward, dvalues
@@ -20,16 +35,19 @@ written, outputs written, upstream gradients read, saved statistics and the
 FP32 partial sums) divided by the measured step time.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                    [--workload long|multi]
+                    [--workload long|short|sliced|deep|multi|selected|block]
 
 Prints ONE JSON line on rank 0.  With --gpus N > 1 run it under
 torch.distributed.run: every rank processes its own full batch (weak
-scaling, no collective inside the timed region).  --impl reference times
-the FP64 CPU oracle on the host cores instead (rank 0 only).
+scaling, data parallel) and each step ends with the one exchange the method
+has, the sum of the FP32 dq (and dw_o) over ranks (an all-reduce of R + D
+floats).  --impl reference times the FP64 CPU oracle on the host cores
+instead (rank 0 only).
 """
 from __future__ import annotations
 
 import argparse
+import dataclasses
 import hashlib
 import json
 import os
@@ -46,6 +64,7 @@ if ROOT not in sys.path:
 METRIC = "AttnRes fwd+bwd ms and effective HBM GB/s (% of roofline), bf16, 1×GB300"
 WORKLOAD_CFG = 3
 FALLBACK_HBM_GBS = 6800.0
+NOMINAL_HBM_GBS = 7900.0   # GB300 HBM3e data-sheet bandwidth (context for the measured-peak fraction)
 PROFILE_TRAFFIC = os.path.join(ROOT, "profiles", "attnres_bwd_traffic.json")
 PROFILE_TRAFFIC_MULTI = os.path.join(ROOT, "profiles", "attnres_multi_bwd_traffic.json")
 PROFILE_TRAFFIC_SELECTED = os.path.join(ROOT, "profiles", "attnres_selected_bwd_traffic.json")
@@ -55,17 +74,21 @@ PROFILE_TRAFFIC_BLOCK = os.path.join(ROOT, "profiles", "attnres_block_bwd_traffi
 # --------------------------------------------------------------------------
 # Byte model
 # --------------------------------------------------------------------------
-def algorithmic_bytes(S, N, D, R, out_norm, P):
+def algorithmic_bytes(S, N, D, R, out_norm, P, o_pre=False):
     """Bytes each kernel must move (bf16 = 2 B, fp32 = 4 B): the forward reads
     the sources and writes y plus the per-token statistics; the backward reads
     the sources again, reads dy and the statistics, writes dvalues and moves
-    the FP32 partial sums of dq/dw_o (P rows written, then read)."""
+    the FP32 partial sums of dq/dw_o (P rows written, then read).  With
+    o_pre, the forward also writes the FP32 pre-norm mixture and the
+    backward reads it (what the plan does when a token's rows cannot stay
+    on chip through the backward)."""
     v = S * N * D * 2
     row = N * D * 2
     stats = 3 * N * S * 4 + (N * 4 if out_norm else 0)
-    fwd = v + row + stats
+    opre = N * D * 4 if (out_norm and o_pre) else 0
+    fwd = v + row + stats + opre
     W = R + (D if out_norm else 0)
-    bwd = 2 * v + row + stats + 2 * P * W * 4
+    bwd = 2 * v + row + stats + 2 * P * W * 4 + opre
     return {"fwd": fwd, "bwd": bwd, "total": fwd + bwd}
 
 
@@ -207,23 +230,42 @@ def dist_env():
 # Workloads: what one step runs, its bytes, its end-to-end variant and its
 # oracle (the CPU baseline and the reference arm)
 # --------------------------------------------------------------------------
-class LongRead:
-    """Single-query read on the long-sequence workload (output RMSNorm on)."""
+class SingleRead:
+    """Single-query read of one of the pages' workloads (seeded synthetic
+    inputs, attention_residuals_gb300.workloads).  One step = the forward and
+    backward for every key offset in `key_offsets` (two reads of the same
+    sources for the sliced workload)."""
     key = "long"
+    cfg = 3
+    key_offsets = (0,)
+    label = "long-sequence"
     roofline_kernel = "attnres_bwd_kernel (+ finalize)"
+    traffic_path = PROFILE_TRAFFIC
+    traffic_key = "cfg3"
+    e2e_chunk = 8192      # tokens per chunk of the host-buffer step
+    cpu_tokens = 8192     # oracle sample for the CPU baseline
+    ref_tokens = 1024     # oracle sample per reference-arm step
 
     def __init__(self, tokens=None, seed=0, device="cpu"):
         from attention_residuals_gb300.workloads import make_workload
-        self.wl = make_workload(WORKLOAD_CFG, N=tokens, seed=WORKLOAD_CFG + 1000 * seed, device=device)
+        wl = make_workload(self.cfg, N=tokens, seed=self.cfg + 1000 * seed, device=device)
+        self.wls = [dataclasses.replace(wl, key_offset=ko) for ko in self.key_offsets]
+        self.wl = self.wls[0]
+        self.o_pre = False
 
     def bytes_for(self, P):
-        wl = self.wl
-        return algorithmic_bytes(wl.S, wl.N, wl.D, wl.R, wl.out_norm, P)
+        tot = {"fwd": 0, "bwd": 0, "total": 0}
+        for wl in self.wls:
+            b = algorithmic_bytes(wl.S, wl.N, wl.D, wl.R, wl.out_norm, P, self.o_pre)
+            for k in tot:
+                tot[k] += b[k]
+        return tot
 
     def describe(self):
         wl = self.wl
-        return (f"S={wl.S} N={wl.N} D={wl.D} R={wl.R} key_offset={wl.key_offset} out-norm bf16 "
-                f"(long-sequence)")
+        ko = "/".join(str(w.key_offset) for w in self.wls)
+        return (f"S={wl.S} N={wl.N} D={wl.D} R={wl.R} key_offset={ko}{' out-norm' if wl.out_norm else ''} "
+                f"bf16 ({self.label})")
 
     # ---------------------------------------------------------------- GPU
     def prepare(self, dev):
@@ -231,76 +273,137 @@ class LongRead:
         from attention_residuals_gb300 import attnres_plan_info
         wl = self.wl
         S, N, D, R = wl.S, wl.N, wl.D, wl.R
-        self.info = attnres_plan_info(wl.values, R, key_offset=wl.key_offset, out_norm=wl.out_norm)
+        self.infos = [attnres_plan_info(w.values, R, key_offset=w.key_offset, out_norm=w.out_norm)
+                      for w in self.wls]
+        self.info = self.infos[0]
+        self.o_pre = bool(wl.out_norm and not self.info["bwd_resident"])
         self.bytes = self.bytes_for(self.info["grid"])
         f32 = dict(dtype=torch.float32, device=dev)
-        self.out = {"y": torch.empty((N, D), dtype=torch.bfloat16, device=dev),
-                    "alpha": torch.empty((N, S), **f32), "rstd": torch.empty((N, S), **f32),
-                    "logit": torch.empty((N, S), **f32), "o_rstd": torch.empty((N,), **f32)}
+        self.outs = []
+        for _ in self.wls:
+            o = {"y": torch.empty((N, D), dtype=torch.bfloat16, device=dev),
+                 "alpha": torch.empty((N, S), **f32), "rstd": torch.empty((N, S), **f32),
+                 "logit": torch.empty((N, S), **f32)}
+            if wl.out_norm:
+                o["o_rstd"] = torch.empty((N,), **f32)
+                if self.o_pre:
+                    o["o_pre"] = torch.empty((N, D), **f32)
+            self.outs.append(o)
         self.dv = torch.empty_like(wl.values)
         self.ws = torch.empty((64 << 20,), dtype=torch.uint8, device=dev)
-        self.launches = 2 + (1 if self.info["bwd_split"] else 0)
-        self.f = None
+        self.launches = sum(2 + (1 if i["bwd_split"] else 0) for i in self.infos)
+        self.f = [None] * len(self.wls)
 
     def fwd(self, stream, values=None, q=None, w=None):
         from attention_residuals_gb300 import attnres_fwd
-        wl = self.wl
-        self.f = attnres_fwd(wl.values if values is None else values, wl.q if q is None else q,
-                             w_o=wl.w_o if w is None else w, key_offset=wl.key_offset, out=self.out,
-                             stream=stream)
+        for i, wl in enumerate(self.wls):
+            self.f[i] = attnres_fwd(wl.values if values is None else values, wl.q if q is None else q,
+                                    w_o=wl.w_o if w is None else w, key_offset=wl.key_offset, out=self.outs[i],
+                                    save_o_pre=self.o_pre, stream=stream)
         return self.f
 
     def bwd(self, stream, values=None, q=None, w=None, dy=None):
         from attention_residuals_gb300 import attnres_bwd
-        wl = self.wl
-        return attnres_bwd(wl.values if values is None else values, wl.q if q is None else q,
-                           wl.dy if dy is None else dy, self.f, w_o=wl.w_o if w is None else w,
-                           key_offset=wl.key_offset, workspace=self.ws, dvalues=self.dv, stream=stream)
+        res = None
+        for i, wl in enumerate(self.wls):
+            res = attnres_bwd(wl.values if values is None else values, wl.q if q is None else q,
+                              wl.dy if dy is None else dy, self.f[i], w_o=wl.w_o if w is None else w,
+                              key_offset=wl.key_offset, workspace=self.ws, dvalues=self.dv, stream=stream)
+        return res
 
-    def e2e(self, stream, chunk_tokens=8192):
+    def grads(self, res):
+        """The step's FP32 reduced gradients (what data parallelism sums over ranks)."""
+        return [res["dq_f32"], res.get("dw_o_f32")]
+
+    def e2e(self, stream, chunk_tokens=None):
         """A step through the C ABI's host-buffer call (attnres_step_host):
         sources, query, weight and dy in page-locked host memory, y,
         dvalues, dq and dw_o copied back to it, transfers overlapped with
-        the kernels chunk by chunk."""
+        the kernels chunk by chunk (once per key offset)."""
         import torch
         from attention_residuals_gb300 import attnres_step_host
+        chunk_tokens = chunk_tokens or self.e2e_chunk
         wl = self.wl
         v, q, w, dy = wl.values, wl.q, wl.w_o, wl.dy
         S, N, D, R = wl.S, wl.N, wl.D, wl.R
         pin = dict(pin_memory=True)
         h = {"v": torch.empty(v.shape, dtype=v.dtype, **pin), "q": q.cpu().pin_memory(),
-             "w": w.cpu().pin_memory(), "dy": torch.empty(dy.shape, dtype=dy.dtype, **pin)}
+             "w": None if w is None else w.cpu().pin_memory(),
+             "dy": torch.empty(dy.shape, dtype=dy.dtype, **pin)}
         h["v"].copy_(v)
         h["dy"].copy_(dy)
         out = {"y": torch.empty((N, D), dtype=torch.bfloat16, **pin),
                "dvalues": [torch.empty((N, D), dtype=torch.bfloat16, **pin) for _ in range(S)],
                "dq": torch.empty((R,), dtype=torch.bfloat16, **pin),
-               "dq_f32": torch.empty((R,), dtype=torch.float32, **pin),
-               "dw_o": torch.empty((D,), dtype=torch.bfloat16, **pin),
-               "dw_o_f32": torch.empty((D,), dtype=torch.float32, **pin)}
+               "dq_f32": torch.empty((R,), dtype=torch.float32, **pin)}
+        if w is not None:
+            out["dw_o"] = torch.empty((D,), dtype=torch.bfloat16, **pin)
+            out["dw_o_f32"] = torch.empty((D,), dtype=torch.float32, **pin)
         ws = {}
 
         def step():
-            r = attnres_step_host(h["v"], h["q"], h["dy"], w_o=h["w"], key_offset=wl.key_offset,
-                                  chunk_tokens=chunk_tokens, out=out, workspace=ws.get("t"))
-            ws["t"] = r["workspace"]
+            for x in self.wls:
+                r = attnres_step_host(h["v"], h["q"], h["dy"], w_o=h["w"], key_offset=x.key_offset,
+                                      chunk_tokens=chunk_tokens, out=out, workspace=ws.get("t"))
+                ws["t"] = r["workspace"]
 
-        h2d = sum(h[k].numel() for k in ("v", "q", "w", "dy")) * 2
-        d2h = (out["y"].numel() + S * N * D + R + D) * 2 + (R + D) * 4
+        reads = len(self.wls)
+        wd = 0 if w is None else D
+        h2d = reads * (v.numel() + dy.numel() + R + wd) * 2
+        d2h = reads * ((N * D + S * N * D + R + wd) * 2 + (R + wd) * 4)
         self.e2e_detail = {"api": "attnres_step_host (C ABI, host buffers)", "chunk_tokens": chunk_tokens}
         return step, h2d, d2h, (h, out, ws)
 
     def traffic(self):
-        return profiled_traffic("cfg3")
+        return profiled_traffic(self.traffic_key, self.traffic_path)
 
     # ---------------------------------------------------------------- CPU
     def oracle_seconds(self, cores):
         from oracle import attnres_oracle
-        wl = self.wl
         t = time.perf_counter()
-        attnres_oracle(wl.values, wl.q, w_o=wl.w_o, dy=wl.dy, key_offset=wl.key_offset,
-                       nthreads=cores, want_dvalues=True)
+        for wl in self.wls:
+            attnres_oracle(wl.values, wl.q, w_o=wl.w_o, dy=wl.dy, key_offset=wl.key_offset,
+                           nthreads=cores, want_dvalues=True)
         return time.perf_counter() - t
+
+
+class LongRead(SingleRead):
+    """S=10, N=32768, D=4096, output RMSNorm on: the split-N reduction path."""
+
+
+class ShortRead(SingleRead):
+    """S=8, N=8192, D=2048: the in-kernel (single-launch) reduction path."""
+    key = "short"
+    cfg = 2
+    label = "short, in-kernel reduction"
+    roofline_kernel = "attnres_bwd_kernel (in-kernel reduction)"
+    traffic_path = os.path.join(ROOT, "profiles", "attnres_short_bwd_traffic.json")
+    traffic_key = "cfg2"
+
+
+class SlicedRead(SingleRead):
+    """The Block schedule's sliced low-rank read: R = D/4 = 1024 key channels,
+    read once with the key in the first R channels and once in the final R."""
+    key = "sliced"
+    cfg = 4
+    key_offsets = (0, 3072)
+    label = "sliced block schedule, 8 block sums + partial, 2% zero rows, both key placements"
+    roofline_kernel = "attnres_bwd_kernel x2 (+ finalize)"
+    traffic_path = os.path.join(ROOT, "profiles", "attnres_sliced_bwd_traffic.json")
+    traffic_key = "cfg4"
+
+
+class DeepRead(SingleRead):
+    """S=64, N=8192, D=8192, output RMSNorm on: a token's rows are 1 MB."""
+    key = "deep"
+    cfg = 5
+    label = "deep"
+    roofline_kernel = "attnres_bwd_kernel (+ finalize)"
+    traffic_path = os.path.join(ROOT, "profiles", "attnres_deep_bwd_traffic.json")
+    traffic_key = "cfg5"
+    e2e_chunk = 1024
+    cpu_tokens = 512
+    ref_tokens = 64
 
 
 class MultiRead:
@@ -373,6 +476,9 @@ class MultiRead:
         h2d = sum(h[k].numel() for k in ("v", "q", "dy")) * 2
         d2h = sum(h[k].numel() for k in ("y", "dv", "dq")) * 2
         return step, h2d, d2h, h
+
+    def grads(self, res):
+        return [res["dq_f32"]]
 
     def traffic(self):
         return profiled_traffic("multi-long", PROFILE_TRAFFIC_MULTI, MULTI_SOURCES)
@@ -481,6 +587,9 @@ class SelectedRead(MultiRead):
         d2h = (h["y"].numel() + h["dv"].numel() + h["db"].numel()) * 2
         return step, h2d, d2h, (h, d)
 
+    def grads(self, res):
+        return [res["dbank_f32"]]
+
     def traffic(self):
         return profiled_traffic("selected-long", PROFILE_TRAFFIC_SELECTED, MULTI_SOURCES)
 
@@ -576,6 +685,9 @@ class BlockRead:
         d2h = sum(h[k].numel() for k in ("y", "pn", "dc", "dp")) * 2
         return step, h2d, d2h, (h, d)
 
+    def grads(self, res):
+        return [res["dq_f32"], res.get("dw_o_f32")]
+
     def traffic(self):
         return profiled_traffic("block", PROFILE_TRAFFIC_BLOCK)
 
@@ -588,8 +700,30 @@ class BlockRead:
         return time.perf_counter() - t
 
 
-WORKLOADS = {"long": LongRead, "multi": MultiRead, "selected": SelectedRead, "block": BlockRead}
-FULL_TOKENS = {"long": 32768, "multi": 32768, "selected": 32768, "block": 16384}
+WORKLOADS = {"long": LongRead, "short": ShortRead, "sliced": SlicedRead, "deep": DeepRead, "multi": MultiRead,
+             "selected": SelectedRead, "block": BlockRead}
+FULL_TOKENS = {"long": 32768, "short": 8192, "sliced": 16384, "deep": 8192, "multi": 32768, "selected": 32768,
+               "block": 16384}
+
+
+def make_exchange(pg, work):
+    """The step's data-parallel exchange: the FP32 reduced gradients of one
+    step (dq, dw_o or the bank gradient) summed over ranks in place -- the
+    method's one exchange step, R + D floats.  `pg` is torch.distributed (or
+    None for one process); `work` names the gradients of a backward result."""
+    def exchange(res):
+        if pg is not None:
+            for g in work.grads(res):
+                if g is not None:
+                    pg.all_reduce(g)
+        return res
+    return exchange
+
+
+def run_step(work, stream, exchange):
+    """One step: forward, backward, exchange."""
+    work.fwd(stream)
+    return exchange(work.bwd(stream))
 
 
 # --------------------------------------------------------------------------
@@ -602,27 +736,28 @@ def run_reference(args):
     from oracle import build_oracle
     build_oracle()
     W = WORKLOADS[args.workload]
-    sample = args.ref_tokens
+    sample = args.ref_tokens or getattr(W, "ref_tokens", 1024)
     wl = W(tokens=sample)
     n_full = FULL_TOKENS[args.workload]
     b = wl.bytes_for(1)["total"]
     cores = os.cpu_count() or 1
-    small = W(tokens=16)
-    for _ in range(args.warmup):  # untimed warm-up steps on a small sample
-        small.oracle_seconds(cores)
+    for _ in range(args.warmup):  # untimed warm-up steps on the timed sample itself
+        wl.oracle_seconds(cores)
     times = [wl.oracle_seconds(cores) for _ in range(max(1, args.steps))]
     t = sum(times) / len(times)
     gbs = b / t / 1e9
     line = {
         "metric": METRIC, "value": gbs, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
-        "warmup": args.warmup, "ms_per_step": t * 1e3 * (n_full / sample),
+        "warmup": args.warmup, "ms_per_step": t * 1e3,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic", "impl": "reference",
         "config": {"workload": wl.describe().replace(f"N={sample}", f"N={n_full}"),
-                   "sample_tokens": sample},
+                   "sample_tokens": sample,
+                   # what a whole step of n_full tokens would take at the measured rate (not run)
+                   "ms_per_step_extrapolated": t * 1e3 * (n_full / sample)},
         "cpu_baseline": {"value": gbs, "unit": "GB/s", "cores": cores, "kind": "oracle",
-                         "sample": f"{sample} of {n_full} tokens per step, fwd+bwd in FP64; "
-                                   f"ms_per_step scaled to the full {n_full} tokens"},
+                         "sample": f"{sample} of {n_full} tokens per step, fwd+bwd in FP64; ms_per_step is "
+                                   f"the measured time of that sample"},
         "e2e": {"value": gbs, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
@@ -655,16 +790,18 @@ def run_ours(args):
     W = WORKLOADS[args.workload]
 
     # CPU baseline sample is generated before any GPU work (rank 0, N=1 only).
-    cpu_wl = W(tokens=args.cpu_tokens) if (rank == 0 and world == 1 and not args.no_cpu) else None
+    cpu_tokens = args.cpu_tokens or getattr(W, "cpu_tokens", 8192)
+    cpu_wl = W(tokens=cpu_tokens) if (rank == 0 and world == 1 and not args.no_cpu) else None
 
     work = W(tokens=args.tokens, seed=rank, device=str(dev))
     work.prepare(dev)
     nbytes = work.bytes
     stream = torch.cuda.current_stream(dev)
 
+    exchange = make_exchange(pg, work)
     for _ in range(max(3, args.warmup)):
         work.fwd(stream)
-        work.bwd(stream)
+        exchange(work.bwd(stream))
     torch.cuda.synchronize()
 
     K = args.steps
@@ -683,7 +820,7 @@ def run_ours(args):
         ev[k][0].record(stream)
         work.fwd(stream)
         ev[k][1].record(stream)
-        work.bwd(stream)
+        exchange(work.bwd(stream))
         ev[k][2].record(stream)
     e_end.record(stream)
     torch.cuda.synchronize()
@@ -718,7 +855,7 @@ def run_ours(args):
     # ---------------------------------------------------------- end to end
     e2e = None
     if not args.no_e2e:
-        e2e_step, h2d, d2h, host = (work.e2e(stream, args.e2e_chunk) if work.key == "long"
+        e2e_step, h2d, d2h, host = (work.e2e(stream, args.e2e_chunk) if isinstance(work, SingleRead)
                                     else work.e2e(stream))
         e2e_step()
         torch.cuda.synchronize()
@@ -749,7 +886,7 @@ def run_ours(args):
         secs = cpu_wl.oracle_seconds(cores)
         cb = cpu_wl.bytes_for(1)["total"]
         cpu = {"value": cb / secs / 1e9, "unit": "GB/s", "cores": cores, "kind": "oracle",
-               "sample": f"{args.cpu_tokens} of {work.wl.N} tokens of the same workload, fwd+bwd in "
+               "sample": f"{cpu_tokens} of {work.wl.N} tokens of the same workload, fwd+bwd in "
                          f"FP64 ({secs:.1f} s)"}
 
     if rank != 0:
@@ -778,12 +915,16 @@ def run_ours(args):
                    "fwd_ms": fwd_ms, "bwd_ms": bwd_ms,
                    "frac_of_peak_step": value / world / peak,
                    "device_copy_gbs": copy_gbs,
-                   "l2": "inputs larger than L2 (2.7 GB of sources per step); no flush",
-                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+                   "l2": f"inputs larger than L2 ({work.wl.values.numel() * 2 / 1e9:.2f} GB of sources per step); "
+                         f"no flush",
+                   "parallelism": (f"data parallel x{world} (own batch per rank, dq/dw_o all-reduced)"
+                                   if world > 1 else "single GPU"),
                    "plan": work.info},
         "roofline": {"bound": "hbm", "kernel": work.roofline_kernel,
                      "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "peak_kind": f"{peak_kind} HBM copy bandwidth",
+                     "frac_of_nominal": achieved / NOMINAL_HBM_GBS,
+                     "nominal_peak": NOMINAL_HBM_GBS,
                      # the committed counters describe the full-size launch only
                      "traffic": work.traffic() if args.tokens in (None, FULL_TOKENS[args.workload]) else None},
         "clocks": clocks,
@@ -805,10 +946,10 @@ def main(argv=None):
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", choices=sorted(WORKLOADS), default="long")
     ap.add_argument("--e2e-steps", type=int, default=5)
-    ap.add_argument("--e2e-chunk", type=int, default=8192,
-                    help="tokens per chunk of the host-buffer step (long workload)")
-    ap.add_argument("--cpu-tokens", type=int, default=8192)
-    ap.add_argument("--ref-tokens", type=int, default=1024)
+    ap.add_argument("--e2e-chunk", type=int, default=None,
+                    help="tokens per chunk of the host-buffer step (single-query workloads)")
+    ap.add_argument("--cpu-tokens", type=int, default=None, help="oracle sample (default: per workload)")
+    ap.add_argument("--ref-tokens", type=int, default=None, help="reference-arm sample (default: per workload)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--no-copy-probe", action="store_true")

@@ -1,9 +1,10 @@
 """CPU checks of the benchmark's byte models and its reference arm (the FP64
-oracle timed on the host cores), for both workloads."""
+oracle timed on the host cores), for every workload."""
 import json
 import subprocess
 import sys
 import os
+import time
 
 import pytest
 
@@ -21,6 +22,19 @@ def test_single_byte_model():
     assert b["fwd"] == v + row + stats
     assert b["bwd"] == 2 * v + row + stats + 2 * 152 * (4096 + 4096) * 4
     assert b["total"] == b["fwd"] + b["bwd"]
+    # a saved FP32 pre-norm mixture is written by the forward and read by the backward
+    c = bench.algorithmic_bytes(S=10, N=32768, D=4096, R=4096, out_norm=True, P=152, o_pre=True)
+    assert c["fwd"] - b["fwd"] == c["bwd"] - b["bwd"] == 32768 * 4096 * 4
+    assert bench.algorithmic_bytes(S=2, N=8, D=64, R=64, out_norm=False, P=1, o_pre=True) == \
+        bench.algorithmic_bytes(S=2, N=8, D=64, R=64, out_norm=False, P=1)
+
+
+def test_sliced_step_reads_twice():
+    w = bench.SlicedRead(tokens=8)
+    assert [x.key_offset for x in w.wls] == [0, 3072]
+    one = bench.algorithmic_bytes(9, 8, 4096, 1024, False, 1)
+    assert w.bytes_for(1)["total"] == 2 * one["total"]
+    assert w.wls[0].values is w.wls[1].values   # the same sources, read twice
 
 
 def test_multi_byte_model():
@@ -32,11 +46,13 @@ def test_multi_byte_model():
     assert b["bwd"] == 2 * v + out + stats + 2 * 152 * 2 * 1024 * 4
 
 
-@pytest.mark.parametrize("workload", ["long", "multi", "selected", "block"])
+@pytest.mark.parametrize("workload", ["long", "short", "sliced", "deep", "multi", "selected", "block"])
 def test_reference_arm_prints_one_json_line(workload):
+    t0 = time.time()
     r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference",
-                        "--workload", workload, "--steps", "1", "--warmup", "3", "--ref-tokens", "16"],
+                        "--workload", workload, "--steps", "2", "--warmup", "3", "--ref-tokens", "16"],
                        capture_output=True, text=True, timeout=600, cwd=ROOT)
+    wall = time.time() - t0
     assert r.returncode == 0, r.stderr
     lines = [ln for ln in r.stdout.splitlines() if ln.strip()]
     assert len(lines) == 1
@@ -47,6 +63,9 @@ def test_reference_arm_prints_one_json_line(workload):
     assert d["impl"] == "reference" and d["value"] > 0
     assert d["e2e"]["h2d_bytes_per_step"] == 0
     assert d["cpu_baseline"]["kind"] == "oracle"
+    # ms_per_step is what a timed step measured: the steps fit in the run's wall time
+    assert d["steps"] * d["ms_per_step"] * 1e-3 < wall
+    assert d["config"]["sample_tokens"] == 16
 
 
 def test_extension_byte_models():

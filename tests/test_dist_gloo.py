@@ -103,3 +103,51 @@ def test_data_parallel_grads_equal_single_process_gloo():
     np.testing.assert_allclose(dq, full["dq"], rtol=1e-5, atol=1e-6)   # sum of FP32 partials
     np.testing.assert_allclose(dw, full["dw_o"], rtol=1e-5, atol=1e-6)
     np.testing.assert_allclose(dq16, full["dq"], rtol=1e-2, atol=1e-2)
+
+
+class _OracleShard:
+    """The benchmark's workload interface (fwd, bwd, grads) with the FP64
+    oracle standing in for the kernels, on this rank's token shard."""
+
+    def __init__(self, rank, world):
+        from attention_residuals_gb300.workloads import make_random
+        self.wl = make_random(4, 29, 64, 32, key_offset=16, out_norm=True, seed=9)
+        self.a, self.b = shard_tokens(self.wl.N, rank, world)
+
+    def fwd(self, stream):
+        return None
+
+    def bwd(self, stream):
+        from oracle import attnres_oracle
+        wl, a, b = self.wl, self.a, self.b
+        r = attnres_oracle(wl.values[:, a:b], wl.q, w_o=wl.w_o, dy=wl.dy[a:b], key_offset=16, nthreads=1)
+        return {"dq_f32": torch.tensor(r["dq"], dtype=torch.float32),
+                "dw_o_f32": torch.tensor(r["dw_o"], dtype=torch.float32)}
+
+    def grads(self, res):
+        return [res["dq_f32"], res["dw_o_f32"]]
+
+
+def _bench_step_worker(rank, world, port, out):
+    _init(rank, world, port)
+    try:
+        import bench
+        work = _OracleShard(rank, world)
+        res = bench.run_step(work, None, bench.make_exchange(dist, work))
+        if rank == 0:
+            out.put((res["dq_f32"].numpy(), res["dw_o_f32"].numpy()))
+    finally:
+        dist.destroy_process_group()
+
+
+def test_bench_step_exchange_gloo():
+    # The benchmark's data-parallel step (forward, backward, the all-reduce of
+    # the FP32 reduced gradients) on two ranks with token shards equals the
+    # single-process gradients.
+    dq, dw = _run(_bench_step_worker)
+    from attention_residuals_gb300.workloads import make_random
+    from oracle import attnres_oracle
+    wl = make_random(4, 29, 64, 32, key_offset=16, out_norm=True, seed=9)
+    full = attnres_oracle(wl.values, wl.q, w_o=wl.w_o, dy=wl.dy, key_offset=16, nthreads=1)
+    np.testing.assert_allclose(dq, full["dq"], rtol=1e-5, atol=1e-6)
+    np.testing.assert_allclose(dw, full["dw_o"], rtol=1e-5, atol=1e-6)
