@@ -1,6 +1,7 @@
 // attnres_api.cu -- the C ABI: argument validation, launch planning and
 // workspace sizing for the AttnRes read operator (include/attnres.h).
 #include <cmath>
+#include <cstdlib>
 #include <cstring>
 #include <mutex>
 
@@ -13,6 +14,7 @@ namespace {
 struct DeviceInfo {
     int sm_count = 0;
     int smem_optin = 0;
+    int l2_bytes = 0;
 };
 
 // Per-device properties, queried once.
@@ -31,6 +33,7 @@ bool device_info(DeviceInfo* out) {
     if (cudaDeviceGetAttribute(&d.smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) !=
         cudaSuccess)
         return false;
+    if (cudaDeviceGetAttribute(&d.l2_bytes, cudaDevAttrL2CacheSize, dev) != cudaSuccess) return false;
     if (dev < 64) {
         cache[dev] = d;
         have[dev] = true;
@@ -40,6 +43,24 @@ bool device_info(DeviceInfo* out) {
 }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// The cluster backward's switch, ATTNRES_BWD_CLUSTER (read on every call, so
+// tests can run every form): unset = the planner's choice, "0" = never (the
+// one-CTA streaming backward), "<n>" = clusters of n CTAs with resident rows
+// (n = 2, 4 or 8), "s<n>" = clusters of n CTAs streaming the rows.
+struct ClusterChoice {
+    int mode;  // -1 planner, 0 off, 1 resident, 2 streaming
+    int cl;
+};
+ClusterChoice cluster_choice() {
+    const char* v = std::getenv("ATTNRES_BWD_CLUSTER");
+    if (!v || !v[0]) return {-1, 0};
+    if (v[0] == '0' && v[1] == '\0') return {0, 0};
+    const bool strm = v[0] == 's';
+    const int n = std::atoi(strm ? v + 1 : v);
+    if (n != 2 && n != 4 && n != 8) return {-1, 0};
+    return {strm ? 2 : 1, n};
+}
 bool aligned4(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
 
 attnres_status check_shape(const attnres_params* p) {
@@ -144,17 +165,98 @@ attnres_status make_plan(const attnres_params* p, Plan* plan, bool fused = false
     }
     pl.smem_fwd = make_layout(pl.f_chunks, pl.f_rows, pl.slot_bytes, fused ? kDeltaSlots : 0, pl.s_pad, false).total;
     pl.smem_bwd = make_layout(pl.b_chunks, pl.b_rows, pl.slot_bytes, pl.dy_slots, pl.s_pad, true).total;
+    pl.b_slot_bytes = pl.slot_bytes;
     const int thr = p->split_n_threshold > 0 ? p->split_n_threshold : ATTNRES_DEFAULT_SPLIT_N;
     pl.split = p->N >= thr ? 1 : 0;
     long long grid = dev.sm_count;
     if (p->N < grid) grid = p->N;
     if (grid < 1) grid = 1;
     pl.grid = static_cast<int>(grid);
+    pl.cl = 1;
+    pl.slice = p->D;
+    pl.nparts = pl.grid;
+    // Rows too many for one SM: the backward streams them once per pass, and
+    // a row's later reads hit L2 only while the rows read in between -- over
+    // the whole grid, (tokens in flight) x (one token's rows) -- fit in it.
+    // When one CTA per token overflows half the L2 that way, a cluster of cl
+    // CTAs shares each token, each owning a D/cl column slice of every row:
+    // cl times fewer tokens in flight.  The smallest cluster that brings the
+    // reuse distance within 3/4 of the L2 is taken (measured on the deep
+    // shape, S=64, D=8192: one CTA 4.15 ms, clusters of 2 / 4 / 8 3.90 / 5.15 /
+    // 11.3 ms -- smaller slices add per-token exchange and barrier time).
+    // Resident slices (forced by the switch): the smallest cluster whose
+    // slices stay in shared memory.
+    const ClusterChoice cc = cluster_choice();
+    const long long token_bytes = static_cast<long long>(S) * p->D * 2;
+    const bool reuse_overflows = (p->N < pl.grid ? p->N : pl.grid) * token_bytes > dev.l2_bytes / 2;
+    if (!pl.resident && !addlast && p->N > 0 && cc.mode != 0 && (cc.mode > 0 || reuse_overflows)) {
+        auto try_cluster = [&](int cl, bool resident, Plan* out) -> bool {
+            if (p->D % (8 * cl) != 0) return false;
+            Plan c = pl;
+            c.cl = cl;
+            c.slice = p->D / cl;
+            const int ncv = c.slice / 8;
+            if (ncv > 512) return false;
+            c.b_vpt = ncv <= 256 ? 1 : 2;
+            c.b_ncw = (ncv + 32 * c.b_vpt - 1) / (32 * c.b_vpt);
+            c.b_slot_bytes = static_cast<int>(align_up(static_cast<uint32_t>(c.slice) * 2u, 128u));
+            c.dy_slots = c.b_slot_bytes > 8192 ? 2 : 4;
+            const long long csb = c.b_slot_bytes;
+            const long long cfixed = make_cluster_layout(0, 1, c.b_slot_bytes, c.dy_slots, c.s_pad, cl).total + 64;
+            const long long cavail = optin - cfixed;
+            auto chunks_for = [&](int rows) {
+                int k = 0;
+                while (k < kMaxChunks &&
+                       make_cluster_layout(k + 1, rows, c.b_slot_bytes, c.dy_slots, c.s_pad, cl).total <=
+                           static_cast<uint32_t>(optin))
+                    ++k;
+                return k;
+            };
+            if (resident) {
+                // a whole token per chunk when two fit, else quarters of a token (finer
+                // releases let the next token's rows load during the write pass); the
+                // slices stay with room for the next token to start loading
+                c.b_rows = (2LL * S * csb <= cavail) ? S : (S + 3) / 4;
+                c.b_chunks = chunks_for(c.b_rows);
+                const int per_token = (S + c.b_rows - 1) / c.b_rows;
+                if (c.b_chunks < (per_token == 1 ? 2 : per_token + (per_token + 1) / 2)) return false;
+            } else {
+                // at least four chunks in flight, at most 16 rows each
+                long long g = cavail / (4 * csb);
+                if (g > 16) g = 16;
+                if (g < 1) g = 1;
+                c.b_rows = static_cast<int>(g);
+                c.b_chunks = chunks_for(c.b_rows);
+                if (c.b_chunks < 2) return false;
+            }
+            c.resident = resident ? 1 : 0;
+            c.smem_bwd = make_cluster_layout(c.b_chunks, c.b_rows, c.b_slot_bytes, c.dy_slots, c.s_pad, cl).total;
+            c.split = 1;  // the clusters' partial rows are always added by the finalize kernel
+            const int active = bwd_cluster_max_active(c, p->R == p->D, p->out_norm != 0, S);
+            if (active < 1) return false;
+            long long ncl = active;
+            if (p->N < ncl) ncl = p->N;
+            if (!resident && cc.mode != 2 && cl < kClusterMax && ncl * token_bytes > dev.l2_bytes / 4 * 3)
+                return false;  // a larger cluster shortens the reuse distance further
+            c.nparts = static_cast<int>(ncl);
+            c.grid = c.nparts * cl;
+            *out = c;
+            return true;
+        };
+        Plan c;
+        bool found = false;
+        if (cc.mode > 0) {
+            found = try_cluster(cc.cl, cc.mode == 1, &c);
+        } else {
+            for (int cl = 2; cl <= kClusterMax && !found; cl *= 2) found = try_cluster(cl, false, &c);
+        }
+        if (found) pl = c;
+    }
     pl.ngroups = (pl.grid + kGroupTicket - 1) / kGroupTicket;
     const size_t W = static_cast<size_t>(p->R) + (p->out_norm ? static_cast<size_t>(p->D) : 0u);
     size_t off = align_up(static_cast<uint32_t>((pl.ngroups + 1) * 4), 256u);
     pl.ws_part_off = off;
-    off += align_up(static_cast<uint32_t>(pl.grid * W * 4), 256u);
+    off += align_up(static_cast<uint32_t>(pl.nparts * W * 4), 256u);
     pl.ws_gpart_off = off;
     off += static_cast<size_t>(pl.ngroups) * W * 4;
     pl.ws_bytes = p->N == 0 ? 0 : off;
@@ -352,7 +454,7 @@ const char* attnres_status_string(attnres_status s) {
     }
 }
 
-attnres_status attnres_plan_info(const attnres_params* p, int64_t out[8]) {
+attnres_status attnres_plan_info(const attnres_params* p, int64_t out[10]) {
     attnres_status st = check_shape(p);
     if (st != ATTNRES_OK) return st;
     if (!out) return ATTNRES_ERR_INVALID_ARG;
@@ -367,6 +469,8 @@ attnres_status attnres_plan_info(const attnres_params* p, int64_t out[8]) {
     out[5] = pl.resident;
     out[6] = static_cast<int64_t>(pl.smem_bwd);
     out[7] = pl.split;
+    out[8] = pl.cl;
+    out[9] = pl.nparts;
     return ATTNRES_OK;
 }
 
@@ -520,12 +624,14 @@ static attnres_status bwd_impl(const attnres_params* p, const void* q, const voi
     a.chunks = pl.b_chunks;
     a.rows = pl.b_rows;
     a.dy_slots = pl.dy_slots;
-    a.slot_bytes = pl.slot_bytes;
+    a.slot_bytes = pl.b_slot_bytes;
     a.ncw = pl.b_ncw;
     a.s_pad = pl.s_pad;
     a.resident = pl.resident;
     a.split = pl.split;
     a.ngroups = pl.ngroups;
+    a.cl = pl.cl;
+    a.slice = pl.slice;
     a.q = static_cast<const uint16_t*>(q);
     a.w_o = static_cast<const uint16_t*>(w_o);
     a.dy = static_cast<const uint16_t*>(dy);

@@ -18,10 +18,12 @@ unsigned take_bwd_error() {
     const unsigned e0 = take_unit_error();
     const unsigned e1 = take_bwd_error_rebuild();
     const unsigned e2 = take_bwd_error_saved();
-    return e0 ? e0 : (e1 ? e1 : e2);
+    const unsigned e3 = take_bwd_error_cluster();
+    return e0 ? e0 : (e1 ? e1 : (e2 ? e2 : e3));
 }
 
 cudaError_t launch_bwd(const Plan& plan, const BwdArgs& a, cudaStream_t stream) {
+    if (plan.cl > 1) return launch_bwd_cluster(plan, a, stream);
     if (!a.out_norm) return launch_bwd_mode<-1>(plan, a, stream);
     return a.o_pre ? launch_bwd_norm_saved(plan, a, stream) : launch_bwd_norm_rebuild(plan, a, stream);
 }

@@ -72,7 +72,7 @@ bool host_step_layout(const attnres_params* p, int64_t T, HostStepLayout* L) {
         // the forward keeps FP32 o only when the backward cannot keep a
         // token's rows resident (the same rule as the Python binding)
         const attnres_params c = chunk_params(p, T);
-        int64_t info[8];
+        int64_t info[10];
         const bool resident = attnres_plan_info(&c, info) == ATTNRES_OK && info[5] != 0;
         L->has_o_pre = p->out_norm && !resident;
         if (L->has_o_pre) off = up256(off + t * D * 4);

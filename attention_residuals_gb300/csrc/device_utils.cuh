@@ -425,6 +425,98 @@ __device__ __forceinline__ uint4 add_bf16x8(const uint4& a, const uint4& b) {
     return make_uint4(w[0], w[1], w[2], w[3]);
 }
 
+// ------------------------------------------------------ thread-block clusters
+// This CTA's rank inside its cluster, the cluster's index and the number of
+// clusters in the grid (x dimension).
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+__device__ __forceinline__ uint32_t cluster_index_x() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%clusterid.x;" : "=r"(r));
+    return r;
+}
+__device__ __forceinline__ uint32_t cluster_count_x() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%nclusterid.x;" : "=r"(r));
+    return r;
+}
+
+// Shared::cluster address of the same shared-memory location in CTA `rank`
+// of this cluster (distributed shared memory).
+__device__ __forceinline__ uint32_t cluster_map(uint32_t smem_addr, uint32_t rank) {
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(smem_addr), "r"(rank));
+    return r;
+}
+
+// Store one float into another CTA's shared memory (address from cluster_map).
+__device__ __forceinline__ void st_cluster_f32(uint32_t addr, float v) {
+    asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(addr), "f"(v) : "memory");
+}
+
+// Arrive on an mbarrier of another CTA of the cluster; release at cluster
+// scope orders this thread's earlier stores (local or remote) before it.
+__device__ __forceinline__ void mbar_arrive_remote(uint32_t remote_bar) {
+    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(remote_bar) : "memory");
+}
+
+// Wait on a local mbarrier whose arrivals come from other CTAs of the
+// cluster: acquire at cluster scope, so their stores before arriving are
+// visible afterwards.  Bounded like mbar_wait_s (about two seconds).
+__device__ __forceinline__ bool mbar_test_cluster_s(uint32_t bar, uint32_t parity, uint32_t hint_ns) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity), "r"(hint_ns)
+        : "memory");
+    return ok != 0;
+}
+
+__device__ __forceinline__ bool mbar_poll_cluster_s(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+static __device__ __noinline__ bool mbar_wait_cluster_s(uint32_t bar, uint32_t parity, volatile int* abort,
+                                                        unsigned* err, unsigned where) {
+    if (mbar_poll_cluster_s(bar, parity)) return true;
+    if (*abort) return false;
+    const uint64_t t0 = global_timer_ns();
+    uint32_t spins = 0;
+    while (!mbar_test_cluster_s(bar, parity, 20000u)) {
+        if (((++spins) & 15u) == 0u) {
+            if (*abort) return false;
+            if (global_timer_ns() - t0 > 2000000000ull) {
+                atomicCAS(err, 0u, where);
+                *abort = 1;
+                return false;
+            }
+        }
+    }
+    return true;
+}
+
+// Every thread of every CTA of the cluster meets here (release / acquire at
+// cluster scope).  Only at kernel start (after barrier initialisation) and
+// end (so no CTA exits while a peer may still address its shared memory),
+// where every thread arrives after finitely many bounded waits.
+__device__ __forceinline__ void cluster_sync_all() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
 // Position in the shared-memory row ring: row address, slot index, phase.
 struct RingCursor {
     uint32_t row;

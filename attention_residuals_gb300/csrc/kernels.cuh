@@ -31,6 +31,7 @@ enum WaitSite : unsigned {
     kSiteBwdTokStat = 5,
     kSiteDrain = 6,
     kSiteBadId = 7,  // a selected-query id outside [0, E)
+    kSiteBwdExchange = 8,  // a cluster peer's partial sums did not arrive
 };
 
 // Launch plan: one persistent CTA per SM.  `ncw` consumer warps each own
@@ -44,7 +45,8 @@ struct Plan {
     int fgrid;               // forward CTAs (fwd_ctas_per_sm per SM)
     int ncw, vpt;            // forward: consumer warps, 16-byte vectors per thread
     int b_ncw, b_vpt;        // backward
-    int slot_bytes;
+    int slot_bytes;          // forward ring slot (one whole row)
+    int b_slot_bytes;        // backward ring slot (a row, or a cluster CTA's column slice)
     int s_pad;
     int f_rows, f_chunks;    // forward: rows per chunk, ring depth
     int f_group;             // forward softmax group rows (whole chunks)
@@ -52,6 +54,9 @@ struct Plan {
     int dy_slots;
     int resident;            // backward keeps a token's rows between its passes
     int split;               // backward reduction via the finalize kernel
+    int cl;                  // backward CTAs per token (a thread-block cluster; 1 = none)
+    int slice;               // columns of a token each backward CTA holds (D / cl)
+    int nparts;              // backward partial rows (CTAs, or clusters)
     size_t smem_fwd;
     size_t smem_bwd;
     size_t ws_bytes;         // backward workspace
@@ -148,6 +153,7 @@ struct BwdArgs {
     int S, D, R, ko, out_norm;
     float eps, scale;
     int chunks, rows, slot_bytes, dy_slots, ncw, s_pad, resident, split, ngroups;
+    int cl, slice;      // cluster size and columns per CTA (cl == 1: slice == D)
     const uint16_t* q;
     const uint16_t* w_o;
     const uint16_t* dy;
@@ -168,6 +174,38 @@ struct BwdArgs {
     const uint16_t* dlast_add;
     long long dlast_add_ld;
 };
+
+// Backward over a thread-block cluster: the backward layout of one CTA's
+// column slice plus the exchange area, [2 buffers][cl ranks][s_pad] floats
+// that peers write their per-token partial sums into, and two mbarriers
+// (one per buffer) that count the peers' arrivals.
+struct ClusterLayout {
+    SmemLayout base;
+    uint32_t xbar, xbuf, total;
+};
+
+constexpr int kClusterMax = 8;          // portable cluster size
+constexpr int kExchangeArrivals = 32;   // arrivals per exchange (every lane of one warp in each CTA)
+
+__host__ __device__ inline ClusterLayout make_cluster_layout(int chunks, int rows, int slot_bytes, int dy_slots,
+                                                             int s_pad, int cl) {
+    ClusterLayout L;
+    L.base = make_layout(chunks, rows, slot_bytes, dy_slots, s_pad, true);
+    uint32_t off = align_up(L.base.total, 16);
+    L.xbar = off;
+    off += 2u * 8u;
+    L.xbuf = off;
+    off += 2u * static_cast<uint32_t>(cl) * static_cast<uint32_t>(s_pad) * 4u;
+    L.total = align_up(off, 128);
+    return L;
+}
+
+// The cluster backward (attnres_bwd_cluster.cu): launch, the largest number
+// of its clusters that fit on the device at once (0 when the shape cannot
+// run as a cluster), and its wait-failure record.
+cudaError_t launch_bwd_cluster(const Plan& plan, const BwdArgs& a, cudaStream_t stream);
+int bwd_cluster_max_active(const Plan& plan, bool keyall, bool norm, int S);
+unsigned take_bwd_error_cluster();
 
 // ---------------------------------------------------------------------------
 // Multi-query read: M queries share one read of the sources.  A token's S

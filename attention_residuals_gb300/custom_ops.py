@@ -53,7 +53,7 @@ def _bwd_resident(S: int, D: int, R: int, key_offset: int, out_norm: bool) -> bo
     p = _lib.AttnresParams()
     p.S, p.D, p.R, p.key_offset, p.N = S, D, R, key_offset, 0
     p.eps, p.scale, p.out_norm, p.split_n_threshold, p.src_ld = 2.0 ** -23, 1.0, int(out_norm), 0, D
-    out = (ctypes.c_int64 * 8)()
+    out = (ctypes.c_int64 * 10)()
     rc = _lib.load().attnres_plan_info(ctypes.byref(p), out)
     return rc == 0 and bool(out[5])
 

@@ -147,11 +147,11 @@ def _out_rows(t: torch.Tensor, N: int, D: int, name: str) -> torch.Tensor:
 # C-ABI mirrors
 # --------------------------------------------------------------------------
 _PLAN_KEYS = ["grid", "consumer_warps", "vectors_per_thread", "bwd_ring", "fwd_ring",
-              "bwd_resident", "bwd_smem_bytes", "bwd_split"]
+              "bwd_resident", "bwd_smem_bytes", "bwd_split", "bwd_cluster", "bwd_partial_rows"]
 
 
 def _plan(p: _lib.AttnresParams) -> dict:
-    out = (ctypes.c_int64 * 8)()
+    out = (ctypes.c_int64 * 10)()
     _lib.check(_lib.load().attnres_plan_info(ctypes.byref(p), out), "attnres_plan_info")
     return dict(zip(_PLAN_KEYS, list(out)))
 

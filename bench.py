@@ -105,9 +105,9 @@ def multi_algorithmic_bytes(S, N, D, R, M, P):
     return {"fwd": fwd, "bwd": bwd, "total": fwd + bwd}
 
 
-SINGLE_SOURCES = ["attnres_api.cu", "attnres_bwd.cu", "attnres_bwd_kernel.cuh", "attnres_bwd_norm.cu",
-                  "attnres_bwd_opre.cu", "attnres_fwd.cu", "attnres_fwd_kernel.cuh", "attnres_jit.cu",
-                  "device_utils.cuh", "kernels.cuh"]
+SINGLE_SOURCES = ["attnres_api.cu", "attnres_bwd.cu", "attnres_bwd_cluster.cu", "attnres_bwd_kernel.cuh",
+                  "attnres_bwd_norm.cu", "attnres_bwd_opre.cu", "attnres_fwd.cu", "attnres_fwd_kernel.cuh",
+                  "attnres_jit.cu", "device_utils.cuh", "kernels.cuh"]
 MULTI_SOURCES = ["attnres_api.cu", "attnres_bwd.cu", "attnres_bwd_kernel.cuh", "attnres_jit.cu",
                  "attnres_multi_bwd.cu", "attnres_multi_fwd.cu", "attnres_multi_fwd_kernel.cuh", "device_utils.cuh",
                  "kernels.cuh"]

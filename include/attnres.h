@@ -27,12 +27,29 @@
  * CTA of each group, then the last group, add the partials).  Both orders are
  * fixed, so dq and dw_o are bitwise reproducible run to run.
  *
+ * A token whose S source rows do not fit in one SM's shared memory (e.g. 64
+ * rows of 8192 channels, 1 MB) is shared by a thread-block cluster of 2, 4
+ * or 8 CTAs in the backward, each holding D/size columns of every row, so
+ * that each row is still read from HBM once; the CTAs exchange their partial
+ * sums of the two full-width reductions through distributed shared memory.
+ * Its partial rows (one per cluster) always go through the finalize kernel.
+ * Shapes no cluster can hold stream the rows once per pass instead.
+ * ATTNRES_BWD_CLUSTER=0 in the environment (read on every call) keeps the
+ * streaming backward for every shape.
+ *
  * Conventions for every entry point:
  *  - All tensor pointers are DEVICE pointers of the current CUDA device,
  *    except the attnres_params struct and the dsrc pointer array, which live
  *    in host memory and are read during the call only.
  *  - The caller owns every buffer, including the backward workspace.  The
- *    library allocates no device memory.
+ *    library allocates no device memory for data.  One exception: the first
+ *    forward of 1024 or more tokens with a new shape on a device compiles a
+ *    kernel for that shape on the host (NVRTC, inside the call, typically a
+ *    few hundred milliseconds) and loads it as a module, for which the
+ *    driver allocates the module's code and a 4-byte error word; later calls
+ *    of that shape reuse it.  A shape first seen while the stream is being
+ *    captured into a CUDA graph runs a precompiled kernel instead (see
+ *    attnres_jit_kernel_count; ATTNRES_JIT=0 turns the run-time path off).
  *  - Calls are asynchronous on `stream` (a cudaStream_t, NULL = legacy
  *    default stream) and never synchronise the host.
  *  - Arguments are validated before anything is enqueued; on any error
@@ -108,8 +125,10 @@ typedef struct {
  *                        the pre-norm mixture o.  The backward rebuilds o from
  *                        the sources when it is NULL, which is free when the
  *                        backward keeps a token's rows in shared memory
- *                        (attnres_plan_info slot 5) and costs one more pass
- *                        over the sources otherwise.
+ *                        (attnres_plan_info slot 5, which counts a cluster's
+ *                        column slices) and costs one more pass over the
+ *                        sources otherwise.  The cluster backward always
+ *                        rebuilds o and does not read o_pre.
  *   q       bf16 [R]     query;  w_o bf16 [D], required iff out_norm
  * alpha, rstd, logit, o_rstd (and o_pre) are what attnres_bwd consumes.
  * Errors: INVALID_ARG (sizes, NULL pointers), ALIGNMENT (16-byte rows),
@@ -122,7 +141,8 @@ attnres_status attnres_fwd(const attnres_params* p, const void* q, const void* w
 /*
  * Bytes of device workspace attnres_bwd needs for these params on the
  * current device (0 when N == 0).  Depends on S, D, R, N, out_norm,
- * split_n_threshold and the device's SM count only.
+ * split_n_threshold, the device's SM count and shared memory, and
+ * ATTNRES_BWD_CLUSTER only.
  */
 size_t attnres_bwd_workspace_bytes(const attnres_params* p);
 
@@ -271,16 +291,18 @@ const char* attnres_status_string(attnres_status s);
 
 /*
  * Launch plan the library would use for these params on the current device
- * (for tests and benchmarks; no launch happens).  Fills out[0..7] with:
- * grid CTAs, consumer warps (forward * 1000 + backward), 16-byte vectors
+ * (for tests and benchmarks; no launch happens).  Fills out[0..9] with:
+ * backward CTAs, consumer warps (forward * 1000 + backward), 16-byte vectors
  * per thread (forward * 1000 + backward), the backward ring
  * (chunks * 1000 + rows per chunk), the forward ring (chunks * 1000 + rows
  * per chunk = softmax group), the backward resident flag (1 = a token's
  * source rows stay in shared memory for all backward passes), dynamic
- * shared memory bytes of the backward kernel, and the backward reduction
- * path (0 = in-kernel, 1 = finalize kernel).
+ * shared memory bytes of the backward kernel, the backward reduction path
+ * (0 = in-kernel, 1 = finalize kernel), the backward cluster size (CTAs
+ * that share one token, each holding D / size columns of its rows; 1 = one
+ * CTA per token) and the number of FP32 partial rows the finalize adds.
  */
-attnres_status attnres_plan_info(const attnres_params* p, int64_t out[8]);
+attnres_status attnres_plan_info(const attnres_params* p, int64_t out[10]);
 
 /*
  * Forward launches (single- and multi-query) of at least 1024 tokens run a

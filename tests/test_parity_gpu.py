@@ -79,13 +79,15 @@ def test_token_counts(N):
 
 
 @pytest.mark.parametrize("save_o_pre", [None, False, True])
-def test_streaming_backward_many_sources(save_o_pre):
-    # 64 rows of 8 KB do not fit the ring: the backward streams the rows once
-    # per pass (o rebuild unless o_pre was saved, dot pass, key slices).
+def test_streaming_backward_many_sources(save_o_pre, monkeypatch):
+    # 64 rows of 8 KB do not fit one SM: with the cluster backward switched off
+    # the backward streams the rows once per pass (o rebuild unless o_pre was
+    # saved, dot pass, key slices).
+    monkeypatch.setenv("ATTNRES_BWD_CLUSTER", "0")
     wl = make_random(64, 90, 4096, 1024, key_offset=1024, out_norm=True, seed=64)
     v, q, w, dy = cuda_copy(wl)
     info = attnres_plan_info(v, 1024, key_offset=1024, out_norm=True)
-    assert info["bwd_resident"] == 0
+    assert info["bwd_resident"] == 0 and info["bwd_cluster"] == 1
     fwd = attnres_fwd(v, q, w_o=w, key_offset=1024, save_o_pre=save_o_pre)
     assert (fwd["o_pre"] is not None) == (save_o_pre is not False)
     bwd = attnres_bwd(v, q, dy, fwd, w_o=w, key_offset=1024)
@@ -101,12 +103,16 @@ def test_streaming_backward_many_sources(save_o_pre):
         assert rel_l2(to_np(fwd["o_pre"]), o_ref) < 1e-5
 
 
+@pytest.mark.parametrize("cluster", ["0", "s2"])
 @pytest.mark.parametrize("S,D,outn", [(24, 8192, True), (40, 6144, False), (130 // 2, 2048, True)])
-def test_streaming_wide_rows_deterministic(S, D, outn):
-    # rows too many to stay resident; 4 vectors per thread for D > 4096
+def test_streaming_wide_rows_deterministic(S, D, outn, cluster, monkeypatch):
+    # rows too many to stay resident in one SM: streamed by one CTA (4 vectors
+    # per thread for D > 4096) or held as column slices by a cluster
+    monkeypatch.setenv("ATTNRES_BWD_CLUSTER", cluster)
     wl = make_random(S, 70, D, out_norm=outn, seed=S + D)
     v, q, w, dy = cuda_copy(wl)
     info = attnres_plan_info(v, D, key_offset=0, out_norm=outn)
+    assert (info["bwd_cluster"] > 1) == (cluster != "0"), info
     fwd = attnres_fwd(v, q, w_o=w, key_offset=0)
     outs = [attnres_bwd(v, q, dy, fwd, w_o=w, key_offset=0) for _ in range(3)]
     torch.cuda.synchronize()
