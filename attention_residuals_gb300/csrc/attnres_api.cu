@@ -264,6 +264,8 @@ attnres_status make_plan(const attnres_params* p, Plan* plan, bool fused = false
     return ATTNRES_OK;
 }
 
+size_t align_up_sz(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
 bool ranges_overlap(const void* a, size_t na, const void* b, size_t nb) {
     const uintptr_t x = reinterpret_cast<uintptr_t>(a), y = reinterpret_cast<uintptr_t>(b);
     return x < y + nb && y < x + na;
@@ -430,6 +432,71 @@ attnres_status make_multi_plan(const attnres_multi_params* p, MultiPlan* plan, i
     if (b.N < grid) grid = b.N;
     pl.grid = static_cast<int>(grid < 1 ? 1 : grid);
     pl.ws_bytes = b.N == 0 ? 0 : static_cast<size_t>(pl.grid) * dq_rows * b.R * 4;
+
+    // General backward (two kernels over column blocks, attnres_multi_general.cu):
+    // every shape whose token does not fit the resident layout, and more than
+    // kMultiResidentMaxM queries.
+    // ATTNRES_MULTI_BWD=general / resident (read on every call) forces one
+    // form where it fits, so both can be tested and timed on any shape.
+    const char* form = std::getenv("ATTNRES_MULTI_BWD");
+    const bool want_gen = form && std::strcmp(form, "general") == 0;
+    const bool want_res = form && std::strcmp(form, "resident") == 0;
+    pl.gen = 0;
+    if (!pl.bwd_ok || (M > kMultiResidentMaxM && !want_res) || want_gen) {
+        const int S = b.S;
+        const int s8 = (S + 7) / 8 * 8;
+        const int ntiles = s8 / 8;
+        pl.gen_s8 = s8;
+        pl.gen_kgroups = ntiles < 8 ? 8 / ntiles : 1;
+        pl.gen_cs = static_cast<int>(align_up(static_cast<uint32_t>(2 * M + 1), 4u));
+        // coefficient kernel: the widest column block (a multiple of 16) whose
+        // ring of two to four row blocks fits
+        bool ok_a = false;
+        for (int dc = 512; dc >= 16 && !ok_a; dc /= 2) {
+            const int pitch = dc * 2 + 16;
+            for (int bufs = 4; bufs >= 2 && !ok_a; --bufs) {
+                const size_t sm = multi_gen_smem_a(bufs, s8, pitch, M, S, pl.gen_kgroups, pl.gen_cs);
+                if (sm <= optin) {
+                    ok_a = true;
+                    pl.gen_dc = dc;
+                    pl.gen_pitch = pitch;
+                    pl.gen_bufs = bufs;
+                    pl.gen_smem_a = sm;
+                }
+            }
+        }
+        // gradient kernel: 512-column blocks, source chunks of up to 8 rows;
+        // a bank of at most 64 KB at these columns stays in shared memory
+        pl.gen_dcb = kMultiGenColumns;
+        pl.gen_rows_b = S < 8 ? S : 8;
+        pl.gen_bank_rows = (E > 0 && static_cast<long long>(E + 1) * pl.gen_dcb * 2 <= 65536) ? E + 1 : 0;
+        bool ok_b = false;
+        for (int chunks = 8; chunks >= 2 && !ok_b; --chunks) {
+            const size_t sm = multi_gen_smem_b(S, pl.gen_cs, M, pl.gen_dcb, pl.gen_rows_b, chunks, pl.gen_bank_rows);
+            if (sm <= optin) {
+                ok_b = true;
+                pl.gen_chunks_b = chunks;
+                pl.gen_smem_b = sm;
+            }
+        }
+        if (ok_a && ok_b) {
+            pl.gen = 1;
+            pl.bwd_ok = 1;
+            long long ga = dev.sm_count;
+            if (b.N < ga) ga = b.N;
+            pl.gen_grid_a = static_cast<int>(ga < 1 ? 1 : ga);
+            const int nbb = (b.D + pl.gen_dcb - 1) / pl.gen_dcb;
+            long long groups = dev.sm_count / nbb;
+            if (groups < 1) groups = 1;
+            if (b.N < groups) groups = b.N;
+            if (groups < 1) groups = 1;
+            pl.gen_groups = static_cast<int>(groups);
+            pl.gen_grid_b = pl.gen_groups * nbb;
+            const size_t coef_bytes = static_cast<size_t>(b.N) * S * pl.gen_cs * 4;
+            pl.gen_part_off = align_up_sz(coef_bytes, 256);
+            pl.ws_bytes = b.N == 0 ? 0 : pl.gen_part_off + static_cast<size_t>(pl.gen_groups) * dq_rows * b.R * 4;
+        }
+    }
     *plan = pl;
     return ATTNRES_OK;
 }
@@ -722,8 +789,10 @@ attnres_status attnres_check_device_error(void) {
     const unsigned b = take_bwd_error();
     const unsigned mf = take_multi_fwd_error();
     const unsigned mb = take_multi_bwd_error();
-    if (f == 0xffffffffu || b == 0xffffffffu || mf == 0xffffffffu || mb == 0xffffffffu) return ATTNRES_ERR_CUDA;
-    return (f || b || mf || mb) ? ATTNRES_ERR_DEVICE : ATTNRES_OK;
+    const unsigned mg = take_multi_gen_error();
+    if (f == 0xffffffffu || b == 0xffffffffu || mf == 0xffffffffu || mb == 0xffffffffu || mg == 0xffffffffu)
+        return ATTNRES_ERR_CUDA;
+    return (f || b || mf || mb || mg) ? ATTNRES_ERR_DEVICE : ATTNRES_OK;
 }
 
 // ---------------------------------------------------------------------------
@@ -731,7 +800,7 @@ attnres_status attnres_check_device_error(void) {
 // ---------------------------------------------------------------------------
 int attnres_jit_kernel_count(void) { return jit_fwd_kernels(); }
 
-attnres_status attnres_multi_plan_info(const attnres_multi_params* p, int64_t out[8]) {
+attnres_status attnres_multi_plan_info(const attnres_multi_params* p, int64_t out[10]) {
     attnres_status st = check_multi(p);
     if (st != ATTNRES_OK) return st;
     if (!out) return ATTNRES_ERR_INVALID_ARG;
@@ -746,7 +815,9 @@ attnres_status attnres_multi_plan_info(const attnres_multi_params* p, int64_t ou
     out[4] = pl.f_chunks * 1000 + pl.f_rows;
     out[5] = pl.b_chunks * 1000 + pl.b_rows;
     out[6] = pl.dy_slots;
-    out[7] = static_cast<int64_t>(pl.smem_bwd);
+    out[7] = static_cast<int64_t>(pl.gen ? pl.gen_smem_b : pl.smem_bwd);
+    out[8] = pl.gen;
+    out[9] = pl.gen ? pl.gen_groups : 0;
     return ATTNRES_OK;
 }
 
@@ -855,6 +926,50 @@ static attnres_status multi_bwd_impl(const attnres_multi_params* p, const void* 
     if (!pl.bwd_ok) return ATTNRES_ERR_UNSUPPORTED;
     if (!workspace || workspace_bytes < pl.ws_bytes) return ATTNRES_ERR_WORKSPACE;
     if (!aligned16(workspace)) return ATTNRES_ERR_ALIGNMENT;
+    if (pl.gen) {
+        if (reinterpret_cast<uintptr_t>(workspace) & 255u) return ATTNRES_ERR_ALIGNMENT;
+        MultiGenArgs g;
+        std::memset(&g, 0, sizeof g);
+        for (int s = 0; s < b.S; ++s) {
+            g.src[s] = b.src[s];
+            g.dsrc[s] = dsrc[s];
+        }
+        g.N = b.N;
+        g.src_ld = b.src_ld;
+        g.dsrc_ld = dsrc_ld;
+        g.dy_ms = p->out_ld_m;
+        g.dy_ns = p->out_ld_n;
+        g.S = b.S;
+        g.D = b.D;
+        g.R = b.R;
+        g.ko = b.key_offset;
+        g.M = p->M;
+        g.E = ids ? E : 0;
+        g.scale = b.scale;
+        g.s8 = pl.gen_s8;
+        g.kgroups = pl.gen_kgroups;
+        g.bufs = pl.gen_bufs;
+        g.dc = pl.gen_dc;
+        g.nblocks = (b.D + pl.gen_dc - 1) / pl.gen_dc;
+        g.pitch = pl.gen_pitch;
+        g.cs = pl.gen_cs;
+        g.dcb = pl.gen_dcb;
+        g.rows_b = pl.gen_rows_b;
+        g.chunks_b = pl.gen_chunks_b;
+        g.bank_rows = ids ? pl.gen_bank_rows : 0;
+        g.q = static_cast<const uint16_t*>(q);
+        g.ids = reinterpret_cast<const long long*>(ids);
+        g.dy = static_cast<const uint16_t*>(dy);
+        g.alpha = alpha;
+        g.rstd = rstd;
+        g.logit = logit;
+        unsigned char* ws = static_cast<unsigned char*>(workspace);
+        g.coef = reinterpret_cast<float*>(ws);
+        g.part = reinterpret_cast<float*>(ws + pl.gen_part_off);
+        g.dq = static_cast<uint16_t*>(dq);
+        g.dq_f32 = dq_f32;
+        return launch_multi_bwd_general(pl, g, s0) == cudaSuccess ? ATTNRES_OK : ATTNRES_ERR_CUDA;
+    }
     MultiBwdArgs a;
     std::memset(&a, 0, sizeof a);
     for (int s = 0; s < b.S; ++s) {

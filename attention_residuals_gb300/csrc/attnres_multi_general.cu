@@ -1,0 +1,717 @@
+// attnres_multi_general.cu -- backward of the multi-query and selected-query
+// reads for any shape (S <= 128 sources, D <= 8192 channels, M <= 16
+// queries), as two kernels over column blocks.
+//
+// Per token, with the forward's saved alpha_ms, logit z_ms and key rstd r_s
+// ("Fast Attention Residuals", sections "Multi-query AttnRes" and "Equation";
+// the chain rule of attnres_multi_bwd.cu):
+//   da_ms = <dy_m, v_s>,  delta_m = sum_s alpha_ms da_ms,  dz_ms = alpha_ms (da_ms - delta_m)
+//   b_ms  = scale r_s dz_ms,   c_s = -(r_s^2 / R) sum_m dz_ms z_ms
+//   dv_s  = sum_m alpha_ms dy_m  +  on key channels: sum_m b_ms q_m + c_s t_s
+//   dq_m += sum_s b_ms t_s                       (summed over tokens)
+//
+// Kernel A (coefficients) walks a token's rows in blocks of columns: a
+// producer warp copies the block of the M dy rows and the S source rows into
+// a shared-memory ring (1-D TMA, rows padded so ldmatrix is conflict-free),
+// and the consumer warps form DA = DY[M x D] . V[S x D]^T, a contraction over
+// the whole row, with bf16 tensor-core MMAs (mma.sync m16n8k16: the products
+// of bf16 operands are exact, the sums FP32).  After the last block the
+// partial tiles are added in a fixed order, every query's coefficients are
+// formed in FP32 and the token's table [S][alpha_s0..alpha_sM-1,
+// b_s0..b_sM-1, c_s] goes to the workspace.
+//
+// Kernel B (gradients) gives each CTA one block of 512 columns for a group of
+// tokens.  Thread t owns the column pair (2t, 2t+1) of the block: the token's
+// M dy values there, the M query values (fixed queries: for the whole
+// launch; selected queries: the token's bank rows) and the M dq sums live in
+// registers, so every source row costs one broadcast read of its
+// coefficient row, one read of the row's pair, 3M + 1 packed FMAs and one
+// 4-byte store (a warp stores 128 contiguous bytes).  dq: fixed queries keep
+// the sums in registers for all of the CTA's tokens and write one partial row
+// per token group; selected queries add each token's sums into the bank rows
+// of the group's partial row with L2 reductions (every address has one
+// writer thread, so the order and the result are fixed).  The finalize
+// kernel adds the groups' rows in order: bitwise reproducible.
+//
+// The sources and dy are read twice (once per kernel); the resident one-CTA
+// kernels of attnres_multi_bwd.cu read them once and run the shapes they
+// hold with few queries.
+#include "device_utils.cuh"
+#include "kernels.cuh"
+
+namespace attnres {
+namespace {
+
+// First failed wait of any launch of this unit (0 = none).
+__device__ unsigned int g_multi_gen_error = 0;
+// Sixteen zero bytes: copied behind a row block whose width is 8 modulo 16,
+// so the last MMA step reads zeros there.
+__device__ __align__(16) unsigned char g_zero16[16];
+
+constexpr int kGenWarps = 8;                     // consumer warps of both kernels
+constexpr int kGenThreads = (kGenWarps + 1) * 32;
+constexpr int kGenTokSlots = 2;
+
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+                 : "r"(addr));
+}
+
+__device__ __forceinline__ void ldsm_x2(uint32_t addr, uint32_t& r0, uint32_t& r1) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x2.shared.b16 {%0, %1}, [%2];" : "=r"(r0), "=r"(r1) : "r"(addr));
+}
+
+// d += A (16 x 16, row-major bf16) * B (16 x 8, column-major bf16), FP32 accumulators.
+__device__ __forceinline__ void mma_bf16_16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                               uint32_t b0, uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+        "{%0, %1, %2, %3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// ---------------------------------------------------------------- kernel A
+// Shared memory: ring of `bufs` row blocks ([16 dy rows][s8 source rows] x
+// pitch bytes; dy rows M..15 and source rows S..s8-1 stay zero), full/empty
+// barriers, statistics ring [kGenTokSlots][2*M*S + S], partial tiles
+// [kgroups][16][s8], DA [16][s8], zr [16][s8], coefficient table [S][cs].
+struct GenALayout {
+    uint32_t ring, full, empty, tfull, tempty, tok, red, da, zr, coef, misc, total;
+    uint32_t buf_bytes, tstride;
+};
+
+__host__ __device__ inline GenALayout gen_a_layout(int bufs, int s8, uint32_t pitch, int M, int S, int kgroups,
+                                                   int cs) {
+    GenALayout L;
+    L.buf_bytes = static_cast<uint32_t>(16 + s8) * pitch;
+    uint32_t off = 0;
+    L.ring = off;
+    off += static_cast<uint32_t>(bufs) * L.buf_bytes;
+    off = align_up(off, 16);
+    L.full = off;
+    off += 8u * bufs;
+    L.empty = off;
+    off += 8u * bufs;
+    L.tfull = off;
+    off += 8u * kGenTokSlots;
+    L.tempty = off;
+    off += 8u * kGenTokSlots;
+    off = align_up(off, 16);
+    L.tstride = align_up(static_cast<uint32_t>(2 * M * S + S), 4u);
+    L.tok = off;
+    off += kGenTokSlots * L.tstride * 4u;
+    L.red = off;
+    off += static_cast<uint32_t>(kgroups) * 16u * static_cast<uint32_t>(s8) * 4u;
+    L.da = off;
+    off += 16u * static_cast<uint32_t>(s8) * 4u;
+    L.zr = off;
+    off += 16u * static_cast<uint32_t>(s8) * 4u;
+    off = align_up(off, 16);
+    L.coef = off;
+    off += static_cast<uint32_t>(S) * static_cast<uint32_t>(cs) * 4u;
+    L.misc = off;
+    off += 16u;
+    L.total = align_up(off, 128);
+    return L;
+}
+
+__global__ void __launch_bounds__(kGenThreads, 1) attnres_multi_coef_kernel(const __grid_constant__ MultiGenArgs a) {
+    extern __shared__ __align__(128) unsigned char smem[];
+    const int S = a.S, M = a.M, s8 = a.s8;
+    const int MS = M * S;
+    const int ntiles = s8 / 8;
+    const int kg = a.kgroups;
+    const GenALayout L = gen_a_layout(a.bufs, s8, a.pitch, M, S, kg, a.cs);
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem + L.full);
+    uint64_t* empty = reinterpret_cast<uint64_t*>(smem + L.empty);
+    uint64_t* tfull = reinterpret_cast<uint64_t*>(smem + L.tfull);
+    uint64_t* tempty = reinterpret_cast<uint64_t*>(smem + L.tempty);
+    float* tok = reinterpret_cast<float*>(smem + L.tok);
+    float* red = reinterpret_cast<float*>(smem + L.red);
+    float* da = reinterpret_cast<float*>(smem + L.da);
+    float* zr = reinterpret_cast<float*>(smem + L.zr);
+    float* coef = reinterpret_cast<float*>(smem + L.coef);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L.misc);
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int B = a.bufs;
+    const int nb = a.nblocks;
+    const int dc = a.dc;
+    const long long N = a.N;
+    const int D = a.D;
+    const uint32_t pitch = a.pitch;
+    const int tstride = static_cast<int>(L.tstride);
+
+    if (threadIdx.x == 0) {
+        for (int b = 0; b < B; ++b) {
+            mbar_init(full + b, 1);
+            mbar_init(empty + b, kGenWarps);
+        }
+        for (int k = 0; k < kGenTokSlots; ++k) {
+            mbar_init(tfull + k, 32);
+            mbar_init(tempty + k, kGenWarps);
+        }
+        *abort_flag = 0;
+        mbar_fence_init();
+    }
+    // the padding rows of every buffer (dy rows M..15, source rows S..s8-1) stay zero
+    for (int b = 0; b < B; ++b) {
+        unsigned char* buf = smem + L.ring + b * L.buf_bytes;
+        const int pad_rows[2][2] = {{M, 16}, {16 + S, 16 + s8}};
+        for (int p = 0; p < 2; ++p)
+            for (int i = pad_rows[p][0] * static_cast<int>(pitch) / 16 + threadIdx.x;
+                 i < pad_rows[p][1] * static_cast<int>(pitch) / 16; i += blockDim.x)
+                *reinterpret_cast<uint4*>(buf + 16 * i) = make_uint4(0u, 0u, 0u, 0u);
+    }
+    __syncthreads();
+
+    if (warp == kGenWarps) {
+        // ------------------------------------------------------ producer
+        const uint64_t pol = policy_evict_first();
+        int b = 0;
+        uint32_t phase = 0;
+        int ts = 0;
+        uint32_t tphase = 0;
+        long long issued = 0;
+        for (long long n = blockIdx.x; n < N; n += gridDim.x) {
+            if (__shfl_sync(0xffffffffu, *abort_flag, 0)) break;
+            // saved statistics -> tok[ts] (all 32 lanes arrive on tfull)
+            mbar_wait(tempty + ts, tphase ^ 1u, abort_flag, &g_multi_gen_error, kSiteBwdProducer);
+            float* dst = tok + ts * tstride;
+            for (int e = lane; e < MS; e += 32) {
+                cp_async_4(dst + e, a.alpha + n * MS + e);
+                cp_async_4(dst + MS + e, a.logit + n * MS + e);
+            }
+            for (int e = lane; e < S; e += 32) cp_async_4(dst + 2 * MS + e, a.rstd + n * S + e);
+            cp_async_arrive_noinc(tfull + ts);
+            if (++ts == kGenTokSlots) {
+                ts = 0;
+                tphase ^= 1u;
+            }
+            if (lane == 0) {
+                for (int c = 0; c < nb; ++c) {
+                    const int c0 = c * dc;
+                    const int wc = min(dc, D - c0);
+                    const uint32_t bytes = static_cast<uint32_t>(wc) * 2u;
+                    const bool tail = (wc & 15) != 0;  // width 8 mod 16: zeros behind the block
+                    if (!mbar_wait(empty + b, phase ^ 1u, abort_flag, &g_multi_gen_error, kSiteBwdProducer)) break;
+                    mbar_arrive_expect_tx(full + b, (bytes + (tail ? 16u : 0u)) * static_cast<uint32_t>(M + S));
+                    unsigned char* buf = smem + L.ring + b * L.buf_bytes;
+                    for (int m = 0; m < M; ++m) {
+                        tma_load_1d(buf + m * pitch, a.dy + m * a.dy_ms + n * a.dy_ns + c0, bytes, full + b, pol);
+                        if (tail) tma_load_1d(buf + m * pitch + bytes, g_zero16, 16u, full + b, pol);
+                    }
+                    for (int s = 0; s < S; ++s) {
+                        const unsigned char* src = static_cast<const unsigned char*>(a.src[s]) + (n * a.src_ld + c0) * 2;
+                        tma_load_1d(buf + (16 + s) * pitch, src, bytes, full + b, pol);
+                        if (tail) tma_load_1d(buf + (16 + s) * pitch + bytes, g_zero16, 16u, full + b, pol);
+                    }
+                    ++issued;
+                    if (++b == B) {
+                        b = 0;
+                        phase ^= 1u;
+                    }
+                }
+            }
+            __syncwarp();
+        }
+        asm volatile("cp.async.wait_all;" ::: "memory");
+        if (lane == 0 && *abort_flag) {
+            for (int c = 0; c < B && c < issued; ++c) {
+                const long long fills = (issued - 1 - c) / B + 1;
+                volatile int no_abort = 0;
+                mbar_wait(full + c, static_cast<uint32_t>((fills - 1) & 1), &no_abort, &g_multi_gen_error, kSiteDrain);
+            }
+        }
+        return;
+    }
+
+    // ---------------------------------------------------------- consumers
+    // warp -> (source tile group, k group): with fewer than eight 8-source
+    // tiles the k steps of a block are split between warps (partial tiles
+    // added afterwards in k-group order); with eight or more every warp owns
+    // whole tiles (tiles w, w + 8, ...).
+    const bool split_k = ntiles < kGenWarps;
+    const int my_tile = split_k ? warp % ntiles : warp;
+    const int my_kg = split_k ? warp / ntiles : 0;
+    const bool active = !split_k || warp < ntiles * kg;
+    const int tile_step = split_k ? ntiles : kGenWarps;  // next tile of this warp (none when split)
+    const uint32_t sbase = smem_u32(smem);
+    const uint32_t ring_s = sbase + L.ring;
+    const uint32_t full_s = sbase + L.full;
+    const uint32_t empty_s = sbase + L.empty;
+    const uint32_t tfull_s = sbase + L.tfull;
+    const uint32_t tempty_s = sbase + L.tempty;
+    // ldmatrix row addresses of this lane (A: dy rows, B: source rows of a tile)
+    const uint32_t a_row = static_cast<uint32_t>((lane & 7) + ((lane >> 3) & 1) * 8) * pitch +
+                           static_cast<uint32_t>((lane >> 4) * 8) * 2u;
+    const uint32_t b_row = static_cast<uint32_t>(16 + (lane & 7)) * pitch + static_cast<uint32_t>(((lane >> 3) & 1) * 8) * 2u;
+    const int g = lane >> 2, t4 = lane & 3;
+    const float inv_r = 1.0f / static_cast<float>(a.R);
+    const int cs = a.cs;
+
+    int b = 0;
+    uint32_t phase = 0;
+    int ts = 0;
+    uint32_t tphase = 0;
+    for (long long n = blockIdx.x; n < N; n += gridDim.x) {
+        float acc[2][4];  // up to two 8-source tiles per warp (s8 <= 128)
+#pragma unroll
+        for (int j = 0; j < 2; ++j)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) acc[j][e] = 0.0f;
+        for (int c = 0; c < nb; ++c) {
+            const int wc = min(dc, D - c * dc);
+            const int ksteps = (wc + 15) >> 4;
+            mbar_wait_s(full_s + 8u * b, phase, abort_flag, &g_multi_gen_error, kSiteBwdConsumer);
+            const uint32_t buf = ring_s + static_cast<uint32_t>(b) * L.buf_bytes;
+            uint32_t dep = 0;
+            if (active) {
+                for (int ks = my_kg; ks < ksteps; ks += kg) {
+                    uint32_t a0, a1, a2, a3;
+                    ldsm_x4(buf + a_row + static_cast<uint32_t>(ks) * 32u, a0, a1, a2, a3);
+                    dep ^= a0;
+#pragma unroll
+                    for (int j = 0; j < 2; ++j) {
+                        const int tile = my_tile + j * tile_step;
+                        if (tile < ntiles && (j == 0 || !split_k)) {
+                            uint32_t b0, b1;
+                            ldsm_x2(buf + b_row + static_cast<uint32_t>(tile * 8) * pitch + static_cast<uint32_t>(ks) * 32u,
+                                    b0, b1);
+                            dep ^= b0;
+                            mma_bf16_16816(acc[j], a0, a1, a2, a3, b0, b1);
+                        }
+                    }
+                }
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive_after(empty_s + 8u * b, dep);
+            if (++b == a.bufs) {
+                b = 0;
+                phase ^= 1u;
+            }
+        }
+        // partial tiles -> red[k group][query][source]; then DA = their sum in k-group order
+        if (active) {
+#pragma unroll
+            for (int j = 0; j < 2; ++j) {
+                const int tile = my_tile + j * tile_step;
+                if (tile < ntiles && (j == 0 || !split_k)) {
+                    float* r = red + (my_kg * 16) * s8;
+                    const int s0 = tile * 8 + 2 * t4;
+                    r[g * s8 + s0] = acc[j][0];
+                    r[g * s8 + s0 + 1] = acc[j][1];
+                    r[(g + 8) * s8 + s0] = acc[j][2];
+                    r[(g + 8) * s8 + s0 + 1] = acc[j][3];
+                }
+            }
+        }
+        named_bar_sync(1, kGenWarps * 32);
+        for (int i = threadIdx.x; i < 16 * s8; i += kGenWarps * 32) {
+            float sum = 0.0f;
+            for (int k = 0; k < kg; ++k) sum += red[k * 16 * s8 + i];
+            da[i] = sum;
+        }
+        mbar_wait_s(tfull_s + 8u * ts, tphase, abort_flag, &g_multi_gen_error, kSiteBwdTokStat);
+        named_bar_sync(1, kGenWarps * 32);
+        // coefficients: one warp per query, lanes over sources
+        const float* tk = tok + ts * tstride;
+        for (int m = warp; m < M; m += kGenWarps) {
+            float p = 0.0f;
+            for (int s = lane; s < S; s += 32) p = fmaf(tk[m * S + s], da[m * s8 + s], p);
+            const float delta = warp_sum(p);
+            for (int s = lane; s < S; s += 32) {
+                const float al = tk[m * S + s];
+                const float dz = al * (da[m * s8 + s] - delta);
+                const float r = tk[2 * MS + s];
+                coef[s * cs + m] = al;
+                coef[s * cs + M + m] = a.scale * r * dz;
+                zr[m * s8 + s] = dz * tk[MS + m * S + s];
+            }
+        }
+        named_bar_sync(1, kGenWarps * 32);
+        for (int s = threadIdx.x; s < S; s += kGenWarps * 32) {
+            float z = 0.0f;
+            for (int m = 0; m < M; ++m) z += zr[m * s8 + s];  // query order
+            const float r = tk[2 * MS + s];
+            coef[s * cs + 2 * M] = -(r * r) * inv_r * z;
+        }
+        named_bar_sync(1, kGenWarps * 32);
+        __syncwarp();
+        if (lane == 0) mbar_arrive_s(tempty_s + 8u * ts);
+        if (++ts == kGenTokSlots) {
+            ts = 0;
+            tphase ^= 1u;
+        }
+        // the token's table -> workspace (16-byte stores; cs is a multiple of 4)
+        float4* out = reinterpret_cast<float4*>(a.coef + n * static_cast<long long>(S) * cs);
+        const float4* in = reinterpret_cast<const float4*>(coef);
+        for (int i = threadIdx.x; i < S * cs / 4; i += kGenWarps * 32) out[i] = in[i];
+        named_bar_sync(1, kGenWarps * 32);  // the table and DA are rewritten by the next token
+    }
+}
+
+// ---------------------------------------------------------------- kernel B
+// Shared memory: token slots [kGenTokSlots] x {coefficient table [S][cs],
+// dy block [M][dcb], ids [M] (selected)}, source chunk ring [chunks][rows]
+// [dcb], barriers, the selected bank's block [(E + 1) pairs of rows] when it
+// is kept in shared memory.
+struct GenBLayout {
+    uint32_t slot, slot_bytes, coef_off, dy_off, ids_off, ring, chunk_bytes, full, empty, tfull, tempty, bank, misc,
+        total;
+};
+
+__host__ __device__ inline GenBLayout gen_b_layout(int S, int cs, int M, int dcb, int rows, int chunks, int bank_rows) {
+    GenBLayout L;
+    const uint32_t row = static_cast<uint32_t>(dcb) * 2u;
+    L.coef_off = 0;
+    L.dy_off = align_up(static_cast<uint32_t>(S * cs) * 4u, 16);
+    L.ids_off = L.dy_off + static_cast<uint32_t>(M) * row;
+    L.slot_bytes = align_up(L.ids_off + static_cast<uint32_t>(M) * 8u, 128);
+    uint32_t off = 0;
+    L.slot = off;
+    off += kGenTokSlots * L.slot_bytes;
+    L.ring = off;
+    L.chunk_bytes = static_cast<uint32_t>(rows) * row;
+    off += static_cast<uint32_t>(chunks) * L.chunk_bytes;
+    off = align_up(off, 16);
+    L.full = off;
+    off += 8u * chunks;
+    L.empty = off;
+    off += 8u * chunks;
+    L.tfull = off;
+    off += 8u * kGenTokSlots;
+    L.tempty = off;
+    off += 8u * kGenTokSlots;
+    off = align_up(off, 16);
+    L.bank = off;
+    off += static_cast<uint32_t>(bank_rows) * row;
+    L.misc = off;
+    off += 16u;
+    L.total = align_up(off, 128);
+    return L;
+}
+
+// MQ: register arrays for up to MQ queries (the run-time M <= MQ).  SEL:
+// per-token queries from the bank rows a.ids selects.
+template <int MQ, bool SEL>
+__global__ void __launch_bounds__(kGenThreads, 1) attnres_multi_grad_kernel(const __grid_constant__ MultiGenArgs a) {
+    extern __shared__ __align__(128) unsigned char smem[];
+    const int S = a.S, M = a.M, cs = a.cs;
+    const int dcb = a.dcb;
+    const int G = a.rows_b;
+    const int K = a.chunks_b;
+    const int E = SEL ? a.E : 0;
+    const bool bank_smem = SEL && a.bank_rows > 0;
+    const GenBLayout L = gen_b_layout(S, cs, M, dcb, G, K, a.bank_rows);
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem + L.full);
+    uint64_t* empty = reinterpret_cast<uint64_t*>(smem + L.empty);
+    uint64_t* tfull = reinterpret_cast<uint64_t*>(smem + L.tfull);
+    uint64_t* tempty = reinterpret_cast<uint64_t*>(smem + L.tempty);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L.misc);
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const long long N = a.N;
+    const int D = a.D;
+    const int nbb = (D + dcb - 1) / dcb;
+    const int cblk = static_cast<int>(blockIdx.x) % nbb;   // this CTA's column block
+    const int grp = static_cast<int>(blockIdx.x) / nbb;    // its token group
+    const int ngrp = static_cast<int>(gridDim.x) / nbb;
+    const int c0 = cblk * dcb;
+    const int wc = min(dcb, D - c0);
+    const uint32_t row_bytes = static_cast<uint32_t>(wc) * 2u;
+    const uint32_t rowp = static_cast<uint32_t>(dcb) * 2u;  // smem row pitch
+    const int QR = SEL ? E : M;
+    float* prow = a.part + static_cast<long long>(grp) * QR * a.R;
+
+    if (threadIdx.x == 0) {
+        for (int k = 0; k < K; ++k) {
+            mbar_init(full + k, 1);
+            mbar_init(empty + k, kGenWarps);
+        }
+        for (int k = 0; k < kGenTokSlots; ++k) {
+            // the TMA copies (one arrival with their bytes); with selected
+            // queries also the producer's cp.async copies of the ids
+            mbar_init(tfull + k, SEL ? 2 : 1);
+            mbar_init(tempty + k, kGenWarps);
+        }
+        *abort_flag = 0;
+        mbar_fence_init();
+    }
+    // the thread's column pair and its key channels
+    const int j0 = c0 + 2 * static_cast<int>(threadIdx.x);  // first column of the pair
+    const bool own = threadIdx.x < kGenWarps * 32 && 2 * static_cast<int>(threadIdx.x) < wc;
+    const int ko = a.ko, kend = a.ko + a.R;
+    const bool kx = own && j0 >= ko && j0 < kend;
+    const bool ky = own && j0 + 1 >= ko && j0 + 1 < kend;
+    if (bank_smem) {
+        // the bank's key values at this block's columns, row e at L.bank + e * rowp
+        // (row E stays zero: it serves an id outside [0, E))
+        uint16_t* bk = reinterpret_cast<uint16_t*>(smem + L.bank);
+        for (int i = threadIdx.x; i < (E + 1) * dcb; i += blockDim.x) {
+            const int e = i / dcb, j = c0 + (i - e * dcb);
+            bk[i] = (e < E && j < D && j >= ko && j < kend) ? a.q[static_cast<long long>(e) * a.R + (j - ko)]
+                                                            : static_cast<uint16_t>(0);
+        }
+    }
+    if (SEL && (kx || ky)) {
+        // this thread's key channels of the group's partial rows start at zero
+        // (the same thread adds to them later, so program order suffices)
+        for (int e = 0; e < E; ++e) {
+            if (kx) prow[static_cast<long long>(e) * a.R + (j0 - ko)] = 0.0f;
+            if (ky) prow[static_cast<long long>(e) * a.R + (j0 + 1 - ko)] = 0.0f;
+        }
+    }
+    __syncthreads();
+
+    if (warp == kGenWarps) {
+        // ------------------------------------------------------ producer
+        const uint64_t pol = policy_evict_first();
+        if (lane == 0) {
+            int k = 0;
+            uint32_t phase = 0;
+            int ts = 0;
+            uint32_t tphase = 0;
+            long long issued = 0, tissued = 0;
+            for (long long n = grp; n < N; n += ngrp) {
+                if (*abort_flag) break;
+                if (!mbar_wait(tempty + ts, tphase ^ 1u, abort_flag, &g_multi_gen_error, kSiteBwdProducer)) break;
+                unsigned char* slot = smem + L.slot + ts * L.slot_bytes;
+                const uint32_t cbytes = static_cast<uint32_t>(S * cs) * 4u;
+                mbar_arrive_expect_tx(tfull + ts, cbytes + static_cast<uint32_t>(M) * row_bytes);
+                tma_load_1d(slot + L.coef_off, a.coef + n * static_cast<long long>(S) * cs, cbytes, tfull + ts, pol);
+                for (int m = 0; m < M; ++m)
+                    tma_load_1d(slot + L.dy_off + m * rowp, a.dy + m * a.dy_ms + n * a.dy_ns + c0, row_bytes,
+                                tfull + ts, pol);
+                if (SEL) {
+                    // ids are 8-byte aligned only: small asynchronous copies
+                    for (int m = 0; m < M; ++m) cp_async_8(slot + L.ids_off + 8 * m, a.ids + n * M + m);
+                    cp_async_arrive_noinc(tfull + ts);
+                }
+                ++tissued;
+                if (++ts == kGenTokSlots) {
+                    ts = 0;
+                    tphase ^= 1u;
+                }
+                bool stop = false;
+                for (int s0 = 0; s0 < S && !stop; s0 += G) {
+                    const int gs = min(G, S - s0);
+                    if (!mbar_wait(empty + k, phase ^ 1u, abort_flag, &g_multi_gen_error, kSiteBwdProducer)) {
+                        stop = true;
+                        break;
+                    }
+                    mbar_arrive_expect_tx(full + k, row_bytes * static_cast<uint32_t>(gs));
+                    for (int r = 0; r < gs; ++r) {
+                        const unsigned char* src =
+                            static_cast<const unsigned char*>(a.src[s0 + r]) + (n * a.src_ld + c0) * 2;
+                        tma_load_1d(smem + L.ring + k * L.chunk_bytes + r * rowp, src, row_bytes, full + k, pol);
+                    }
+                    ++issued;
+                    if (++k == K) {
+                        k = 0;
+                        phase ^= 1u;
+                    }
+                }
+                if (stop) break;
+            }
+            asm volatile("cp.async.wait_all;" ::: "memory");
+            if (*abort_flag) {
+                for (int c = 0; c < K && c < issued; ++c) {
+                    const long long fills = (issued - 1 - c) / K + 1;
+                    volatile int no_abort = 0;
+                    mbar_wait(full + c, static_cast<uint32_t>((fills - 1) & 1), &no_abort, &g_multi_gen_error,
+                              kSiteDrain);
+                }
+                for (int c = 0; c < kGenTokSlots && c < tissued; ++c) {
+                    const long long fills = (tissued - 1 - c) / kGenTokSlots + 1;
+                    volatile int no_abort = 0;
+                    mbar_wait(tfull + c, static_cast<uint32_t>((fills - 1) & 1), &no_abort, &g_multi_gen_error,
+                              kSiteDrain);
+                }
+            }
+        }
+        return;
+    }
+
+    // ---------------------------------------------------------- consumers
+    float2 qv[MQ], dqs[MQ];
+#pragma unroll
+    for (int m = 0; m < MQ; ++m) {
+        float x = 0.0f, y = 0.0f;
+        if (!SEL && m < M) {
+            if (kx) x = bf16_bits_to_float(a.q[static_cast<long long>(m) * a.R + (j0 - ko)]);
+            if (ky) y = bf16_bits_to_float(a.q[static_cast<long long>(m) * a.R + (j0 + 1 - ko)]);
+        }
+        qv[m] = make_float2(x, y);
+        dqs[m] = make_float2(0.0f, 0.0f);
+    }
+    const uint32_t sbase = smem_u32(smem);
+    const uint32_t lane_off = 4u * threadIdx.x;  // this thread's pair within a row
+    const uint32_t full_s = sbase + L.full, empty_s = sbase + L.empty;
+    const uint32_t tfull_s = sbase + L.tfull, tempty_s = sbase + L.tempty;
+    const float2 keep = make_float2(kx ? 1.0f : 0.0f, ky ? 1.0f : 0.0f);
+    int k = 0;
+    uint32_t phase = 0;
+    int ts = 0;
+    uint32_t tphase = 0;
+    for (long long n = grp; n < N; n += ngrp) {
+        mbar_wait_s(tfull_s + 8u * ts, tphase, abort_flag, &g_multi_gen_error, kSiteBwdConsumer);
+        const unsigned char* slot = smem + L.slot + ts * L.slot_bytes;
+        const uint32_t slot_s = sbase + L.slot + ts * L.slot_bytes;
+        const float* ctab = reinterpret_cast<const float*>(slot + L.coef_off);
+        float2 dyv[MQ];
+#pragma unroll
+        for (int m = 0; m < MQ; ++m) {
+            uint32_t w = 0;
+            if (m < M && own) asm volatile("ld.shared.b32 %0, [%1];" : "=r"(w) : "r"(slot_s + L.dy_off + m * rowp + lane_off));
+            dyv[m] = bf2_to_f2(w);
+        }
+        int qrow[MQ];
+        if constexpr (SEL) {
+            const long long* ids = reinterpret_cast<const long long*>(slot + L.ids_off);
+#pragma unroll
+            for (int m = 0; m < MQ; ++m) {
+                qrow[m] = -1;
+                float x = 0.0f, y = 0.0f;
+                if (m < M) {
+                    const long long id = ids[m];
+                    if (id < 0 || id >= E) {
+                        if (threadIdx.x == 0) atomicCAS(&g_multi_gen_error, 0u, static_cast<unsigned>(kSiteBadId));
+                    } else {
+                        qrow[m] = static_cast<int>(id);
+                        if (bank_smem) {
+                            uint32_t w = 0;
+                            if (own)
+                                asm volatile("ld.shared.b32 %0, [%1];"
+                                             : "=r"(w)
+                                             : "r"(sbase + L.bank + static_cast<uint32_t>(id) * rowp + lane_off));
+                            const float2 f = bf2_to_f2(w);
+                            x = f.x;
+                            y = f.y;
+                        } else {
+                            if (kx) x = bf16_bits_to_float(a.q[id * a.R + (j0 - ko)]);
+                            if (ky) y = bf16_bits_to_float(a.q[id * a.R + (j0 + 1 - ko)]);
+                        }
+                    }
+                }
+                qv[m] = make_float2(x, y);
+                dqs[m] = make_float2(0.0f, 0.0f);
+            }
+        }
+        for (int s0 = 0; s0 < S; s0 += G) {
+            const int gs = min(G, S - s0);
+            mbar_wait_s(full_s + 8u * k, phase, abort_flag, &g_multi_gen_error, kSiteBwdConsumer);
+            const uint32_t chunk = sbase + L.ring + static_cast<uint32_t>(k) * L.chunk_bytes + lane_off;
+            uint32_t dep = 0;
+            for (int r = 0; r < gs; ++r) {
+                const int s = s0 + r;
+                uint32_t w = 0;
+                if (own) asm volatile("ld.shared.b32 %0, [%1];" : "=r"(w) : "r"(chunk + static_cast<uint32_t>(r) * rowp));
+                dep ^= w;
+                const float2 t = fmul2(bf2_to_f2(w), keep);  // key channels of the row
+                const float* crow = ctab + s * cs;            // alpha_s0.., b_s0.., c_s (broadcast)
+                float2 o = make_float2(0.0f, 0.0f);
+#pragma unroll
+                for (int m = 0; m < MQ; ++m) {
+                    if (m < M) {
+                        const float al = crow[m];
+                        const float bq = crow[M + m];
+                        o = ffma2(make_float2(al, al), dyv[m], o);
+                        o = ffma2(make_float2(bq, bq), qv[m], o);
+                        dqs[m] = ffma2(make_float2(bq, bq), t, dqs[m]);
+                    }
+                }
+                const float cv = crow[2 * M];
+                o = ffma2(make_float2(cv, cv), t, o);
+                if (own) {
+                    uint16_t* drow = static_cast<uint16_t*>(a.dsrc[s]) + n * a.dsrc_ld + j0;
+                    asm volatile("st.global.cs.b32 [%0], %1;" ::"l"(drow), "r"(pack_f2(o)) : "memory");
+                }
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive_after(empty_s + 8u * k, dep);
+            if (++k == K) {
+                k = 0;
+                phase ^= 1u;
+            }
+        }
+        if constexpr (SEL) {
+            // the token's dq into its bank rows of the group's partial row
+#pragma unroll
+            for (int m = 0; m < MQ; ++m) {
+                if (m < M && qrow[m] >= 0) {
+                    float* p = prow + static_cast<long long>(qrow[m]) * a.R;
+                    if (kx) red_add_f32(p + (j0 - ko), dqs[m].x);
+                    if (ky) red_add_f32(p + (j0 + 1 - ko), dqs[m].y);
+                }
+            }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive_s(tempty_s + 8u * ts);
+        if (++ts == kGenTokSlots) {
+            ts = 0;
+            tphase ^= 1u;
+        }
+    }
+    if constexpr (!SEL) {
+        // this thread's key channels of the group's partial row
+#pragma unroll
+        for (int m = 0; m < MQ; ++m) {
+            if (m < M) {
+                float* p = prow + static_cast<long long>(m) * a.R;
+                if (kx) p[j0 - ko] = dqs[m].x;
+                if (ky) p[j0 + 1 - ko] = dqs[m].y;
+            }
+        }
+    }
+}
+
+template <int MQ, bool SEL>
+cudaError_t launch_grad_t(const MultiPlan& plan, const MultiGenArgs& a, cudaStream_t stream) {
+    auto kern = attnres_multi_grad_kernel<MQ, SEL>;
+    cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                           static_cast<int>(plan.gen_smem_b));
+    if (err != cudaSuccess) return err;
+    kern<<<plan.gen_grid_b, kGenThreads, plan.gen_smem_b, stream>>>(a);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+size_t multi_gen_smem_a(int bufs, int s8, int pitch, int M, int S, int kgroups, int cs) {
+    return gen_a_layout(bufs, s8, static_cast<uint32_t>(pitch), M, S, kgroups, cs).total;
+}
+
+size_t multi_gen_smem_b(int S, int cs, int M, int dcb, int rows, int chunks, int bank_rows) {
+    return gen_b_layout(S, cs, M, dcb, rows, chunks, bank_rows).total;
+}
+
+cudaError_t launch_multi_bwd_general(const MultiPlan& plan, const MultiGenArgs& a, cudaStream_t stream) {
+    cudaError_t err = cudaFuncSetAttribute(attnres_multi_coef_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                           static_cast<int>(plan.gen_smem_a));
+    if (err != cudaSuccess) return err;
+    attnres_multi_coef_kernel<<<plan.gen_grid_a, kGenThreads, plan.gen_smem_a, stream>>>(a);
+    err = cudaGetLastError();
+    if (err != cudaSuccess) return err;
+    const bool sel = a.ids != nullptr;
+    if (a.M <= 4)
+        err = sel ? launch_grad_t<4, true>(plan, a, stream) : launch_grad_t<4, false>(plan, a, stream);
+    else if (a.M <= 8)
+        err = sel ? launch_grad_t<8, true>(plan, a, stream) : launch_grad_t<8, false>(plan, a, stream);
+    else
+        err = sel ? launch_grad_t<16, true>(plan, a, stream) : launch_grad_t<16, false>(plan, a, stream);
+    if (err != cudaSuccess) return err;
+    const int W = (sel ? a.E : a.M) * a.R;
+    return launch_finalize(a.part, plan.gen_groups, W, W, a.dq, a.dq_f32, nullptr, nullptr, stream);
+}
+
+unsigned take_multi_gen_error() {
+    unsigned v = 0, zero = 0;
+    if (cudaMemcpyFromSymbol(&v, g_multi_gen_error, sizeof v) != cudaSuccess) return 0xffffffffu;
+    if (v) cudaMemcpyToSymbol(g_multi_gen_error, &zero, sizeof zero);
+    return v;
+}
+
+}  // namespace attnres

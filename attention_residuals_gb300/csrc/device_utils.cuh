@@ -124,6 +124,11 @@ __device__ __forceinline__ void cp_async_4(void* dst_smem, const void* src_gmem)
                  : "memory");
 }
 
+// 8-byte asynchronous copy global -> shared (both addresses 8-byte aligned).
+__device__ __forceinline__ void cp_async_8(void* dst_smem, const void* src_gmem) {
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 8;" ::"r"(smem_u32(dst_smem)), "l"(src_gmem) : "memory");
+}
+
 // Arrive on `bar` once every cp.async this thread issued so far has landed.
 // The arrival counts against the barrier's expected count (.noinc).
 __device__ __forceinline__ void cp_async_arrive_noinc(uint64_t* bar) {

@@ -327,6 +327,14 @@ __host__ __device__ inline MultiFwdLayout make_multi_fwd_layout(int chunks, int 
 }
 
 struct MultiPlan {
+    // general two-kernel backward (attnres_multi_general.cu): used when the
+    // resident layout does not fit or for more than kMultiResidentMaxM queries
+    int gen;
+    int gen_grid_a, gen_grid_b, gen_groups;   // CTAs of the two kernels, token groups of the second
+    size_t gen_smem_a, gen_smem_b;
+    int gen_s8, gen_kgroups, gen_bufs, gen_dc, gen_pitch, gen_cs;
+    int gen_dcb, gen_rows_b, gen_chunks_b, gen_bank_rows;
+    size_t gen_part_off;                      // workspace: coefficient tables, then partial rows
     int grid;
     int fgrid;             // forward CTAs (multi_fwd_ctas_per_sm per SM)
     int f_group;           // forward softmax group rows (whole chunks, <= kMaxGroup)
@@ -386,6 +394,40 @@ struct MultiBwdArgs {
     int E;                 // bank rows
     int bank_rows;         // E + 1: the bank and a zero row stay in qsm (rows as ids), else 0
 };
+
+// Arguments of the general multi-query backward (attnres_multi_general.cu).
+struct MultiGenArgs {
+    const void* src[ATTNRES_MAX_S];
+    void* dsrc[ATTNRES_MAX_S];
+    long long N, src_ld, dsrc_ld, dy_ms, dy_ns;
+    int S, D, R, ko, M, E;
+    float scale;
+    // coefficient kernel: sources padded to s8, k groups of warps, ring of
+    // `bufs` row blocks of `dc` columns (`pitch` bytes per row), `nblocks`
+    // blocks per row, `cs` floats per source in the coefficient table
+    int s8, kgroups, bufs, nblocks, dc, pitch, cs;
+    // gradient kernel: column blocks of `dcb`, source chunks of `rows_b` rows
+    // in a ring of `chunks_b`, bank rows kept in shared memory (E + 1, or 0)
+    int dcb, rows_b, chunks_b, bank_rows;
+    const uint16_t* q;     // [M][R], or the bank [E][R] with ids
+    const long long* ids;  // [N][M] or NULL
+    const uint16_t* dy;
+    const float* alpha;
+    const float* rstd;
+    const float* logit;
+    float* coef;           // [N][S][cs] workspace
+    float* part;           // [groups][Q * R] workspace
+    uint16_t* dq;
+    float* dq_f32;
+};
+// Queries up to which the resident one-CTA multi-query backward runs (when
+// its layout fits); more queries take the general backward.
+constexpr int kMultiResidentMaxM = 4;
+constexpr int kMultiGenColumns = 512;   // columns per CTA of the gradient kernel
+size_t multi_gen_smem_a(int bufs, int s8, int pitch, int M, int S, int kgroups, int cs);
+size_t multi_gen_smem_b(int S, int cs, int M, int dcb, int rows, int chunks, int bank_rows);
+cudaError_t launch_multi_bwd_general(const MultiPlan& plan, const MultiGenArgs& a, cudaStream_t stream);
+unsigned take_multi_gen_error();
 
 unsigned take_multi_fwd_error();
 unsigned take_multi_bwd_error();

@@ -497,7 +497,7 @@ def attnres_partial_bwd(completed: Sources, partial_new: torch.Tensor, q: torch.
 # Multi-query read ("Fast Attention Residuals", section "Multi-query AttnRes")
 # --------------------------------------------------------------------------
 _MULTI_PLAN_KEYS = ["grid", "consumer_warps", "vectors_per_thread", "query_blocks", "fwd_ring",
-                    "bwd_ring", "dy_slots", "bwd_smem_bytes"]
+                    "bwd_ring", "dy_slots", "bwd_smem_bytes", "bwd_general", "bwd_token_groups"]
 
 
 def make_multi_params(view: _SourceView, M: int, R: int, *, key_offset: Optional[int], eps: float,
@@ -528,7 +528,7 @@ def attnres_multi_plan_info(values: Sources, M: int, R: int, *, key_offset=None)
     view = _source_view(values)
     mp = make_multi_params(view, M, R, key_offset=key_offset, eps=EPS_DEFAULT, scale=1.0,
                            token_major=False)
-    out = (ctypes.c_int64 * 8)()
+    out = (ctypes.c_int64 * 10)()
     _lib.check(_lib.load().attnres_multi_plan_info(ctypes.byref(mp), out), "attnres_multi_plan_info")
     return dict(zip(_MULTI_PLAN_KEYS, list(out)))
 

@@ -4,7 +4,7 @@
 Shapes span every kernel variant (1, 2 or 4 vectors per thread; one or
 several register blocks of queries), ragged token counts, unaligned key
 slices, both output layouts, M from 1 to 16, more sources than a warp has
-lanes, the empty input and shapes the library must refuse.  The long
+lanes and the empty input.  The long
 workload at full size is checked on sampled tokens plus the full dq.
 Tolerances as for the single-query read (parity_utils).
 """
@@ -138,20 +138,15 @@ def test_multi_empty_input():
     assert torch.count_nonzero(g["dq_f32"]).item() == 0 and g["dq"].shape == (2, 128)
 
 
-def test_multi_forward_streams_large_tokens_backward_refuses_them():
-    # 64 rows of 16 KB cannot stay resident in shared memory: the forward
-    # streams them (one pass per query, queries reloaded per pass), the
-    # backward refuses the shape before launching anything
+def test_multi_large_tokens_forward_and_backward():
+    # 64 rows of 16 KB and sixteen queries cannot stay resident in shared
+    # memory: the forward streams the rows (one pass per query block), the
+    # backward takes the general two-kernel path
     wl = make_multi(64, 5, 8192, 8192, 16, key_offset=0, seed=77)
     v, Q = wl.values.cuda(), wl.queries.cuda()
-    fwd = attnres_multi_fwd(v, Q, key_offset=0)
-    torch.cuda.synchronize()
-    attnres_check_device_error()
-    ref = attnres_multi_oracle(wl.values, wl.queries, key_offset=0)
-    _check(wl, fwd, None, ref, False, "S64 D8192 M16 forward")
-    with pytest.raises(AttnresError) as e:
-        attnres_multi_bwd(v, Q, wl.dy.cuda(), fwd, key_offset=0)
-    assert e.value.name == "ATTNRES_ERR_UNSUPPORTED"
+    assert attnres_multi_plan_info(v, 16, 8192, key_offset=0)["bwd_general"] == 1
+    fwd, bwd, ref = run_multi(wl)
+    _check(wl, fwd, bwd, ref, False, "S64 D8192 M16")
 
 
 def test_multi_autograd_compile_and_shared_sources():
