@@ -447,42 +447,66 @@ attnres_status make_multi_plan(const attnres_multi_params* p, MultiPlan* plan, i
         const int s8 = (S + 7) / 8 * 8;
         const int ntiles = s8 / 8;
         pl.gen_s8 = s8;
-        pl.gen_kgroups = ntiles < 8 ? 8 / ntiles : 1;
-        pl.gen_cs = static_cast<int>(align_up(static_cast<uint32_t>(2 * M + 1), 4u));
-        // coefficient kernel: the widest column block (a multiple of 16) whose
-        // ring of two to four row blocks fits
+        pl.gen_kgroups = ntiles < kMultiCoefWarps ? kMultiCoefWarps / ntiles : 1;
+        // coefficient table per source: alpha, b (queries padded to a multiple
+        // of 4, for 16-byte loads) and c, padded to a multiple of 4 floats
+        pl.gen_cs = 2 * ((M + 3) & ~3) + 4;
+        // coefficient kernel: two CTAs per SM when their layouts fit in half of
+        // it, each with the ring of row blocks (column blocks of at least 256, a
+        // multiple of 16, and two to eight buffers) that keeps the most bytes
+        // loading ahead of the block being used
         bool ok_a = false;
-        for (int dc = 512; dc >= 16 && !ok_a; dc /= 2) {
-            const int pitch = dc * 2 + 16;
-            for (int bufs = 4; bufs >= 2 && !ok_a; --bufs) {
-                const size_t sm = multi_gen_smem_a(bufs, s8, pitch, M, S, pl.gen_kgroups, pl.gen_cs);
-                if (sm <= optin) {
-                    ok_a = true;
-                    pl.gen_dc = dc;
-                    pl.gen_pitch = pitch;
-                    pl.gen_bufs = bufs;
-                    pl.gen_smem_a = sm;
+        long long best = -1;
+        int coef_ctas = 2;
+        for (int pass = 0; pass < 4 && !ok_a; ++pass) {
+            coef_ctas = pass < 2 ? 2 : 1;
+            const size_t budget = coef_ctas == 2 ? optin / 2 - 1024 : optin;
+            for (int dc = 1024; dc >= ((pass & 1) == 0 ? 256 : 16); dc /= 2) {
+                const int pitch = dc * 2 + 16;
+                for (int bufs = kMultiGenMaxBufs; bufs >= 2; --bufs) {
+                    const size_t sm = multi_gen_smem_a(bufs, s8, pitch, M, S, pl.gen_kgroups, pl.gen_cs);
+                    if (sm > budget) continue;
+                    const long long ahead = static_cast<long long>(bufs - 1) * (16 + s8) * pitch;
+                    if (ahead > best) {
+                        best = ahead;
+                        ok_a = true;
+                        pl.gen_dc = dc;
+                        pl.gen_pitch = pitch;
+                        pl.gen_bufs = bufs;
+                        pl.gen_smem_a = sm;
+                    }
+                    break;  // the most buffers that fit at this width
                 }
             }
         }
-        // gradient kernel: 512-column blocks, source chunks of up to 8 rows;
-        // a bank of at most 64 KB at these columns stays in shared memory
-        pl.gen_dcb = kMultiGenColumns;
+        // gradient kernel: 512 columns per column pair of a thread (two pairs
+        // when the registers allow, M <= 8), source chunks of up to 8 rows, as
+        // many token slots as leave the ring two tokens of rows; a bank of at
+        // most 64 KB at these columns stays in shared memory
+        const int pairs = (M <= 8 && b.D > kMultiGenColumns) ? 2 : 1;
+        pl.gen_dcb = kMultiGenColumns * pairs;
         pl.gen_rows_b = S < 8 ? S : 8;
         pl.gen_bank_rows = (E > 0 && static_cast<long long>(E + 1) * pl.gen_dcb * 2 <= 65536) ? E + 1 : 0;
+        const int per_token = (S + pl.gen_rows_b - 1) / pl.gen_rows_b;
+        const int want_chunks = 2 * per_token < 16 ? (2 * per_token > 2 ? 2 * per_token : 2) : 16;
         bool ok_b = false;
-        for (int chunks = 8; chunks >= 2 && !ok_b; --chunks) {
-            const size_t sm = multi_gen_smem_b(S, pl.gen_cs, M, pl.gen_dcb, pl.gen_rows_b, chunks, pl.gen_bank_rows);
-            if (sm <= optin) {
+        for (int ts = kMultiGenMaxSlots; ts >= 2 && !ok_b; --ts) {
+            int chunks = 0;
+            while (chunks < 16 && multi_gen_smem_b(S, pl.gen_cs, M, pl.gen_dcb, pl.gen_rows_b, chunks + 1,
+                                                    pl.gen_bank_rows, ts) <= optin)
+                ++chunks;
+            if (chunks >= want_chunks || (ts == 2 && chunks >= 2)) {
                 ok_b = true;
+                pl.gen_tslots_b = ts;
                 pl.gen_chunks_b = chunks;
-                pl.gen_smem_b = sm;
+                pl.gen_smem_b = multi_gen_smem_b(S, pl.gen_cs, M, pl.gen_dcb, pl.gen_rows_b, chunks,
+                                                 pl.gen_bank_rows, ts);
             }
         }
         if (ok_a && ok_b) {
             pl.gen = 1;
             pl.bwd_ok = 1;
-            long long ga = dev.sm_count;
+            long long ga = static_cast<long long>(coef_ctas) * dev.sm_count;
             if (b.N < ga) ga = b.N;
             pl.gen_grid_a = static_cast<int>(ga < 1 ? 1 : ga);
             const int nbb = (b.D + pl.gen_dcb - 1) / pl.gen_dcb;
@@ -957,6 +981,7 @@ static attnres_status multi_bwd_impl(const attnres_multi_params* p, const void* 
         g.rows_b = pl.gen_rows_b;
         g.chunks_b = pl.gen_chunks_b;
         g.bank_rows = ids ? pl.gen_bank_rows : 0;
+        g.tslots_b = pl.gen_tslots_b;
         g.q = static_cast<const uint16_t*>(q);
         g.ids = reinterpret_cast<const long long*>(ids);
         g.dy = static_cast<const uint16_t*>(dy);

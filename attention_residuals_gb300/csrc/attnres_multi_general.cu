@@ -48,9 +48,9 @@ __device__ unsigned int g_multi_gen_error = 0;
 // so the last MMA step reads zeros there.
 __device__ __align__(16) unsigned char g_zero16[16];
 
-constexpr int kGenWarps = 8;                     // consumer warps of both kernels
+constexpr int kGenWarps = 8;                     // consumer warps of the gradient kernel
 constexpr int kGenThreads = (kGenWarps + 1) * 32;
-constexpr int kGenTokSlots = 2;
+constexpr int kGenTokSlots = 2;                  // statistics slots of the coefficient kernel
 
 __device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
     asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
@@ -76,7 +76,9 @@ __device__ __forceinline__ void mma_bf16_16816(float (&d)[4], uint32_t a0, uint3
 // Shared memory: ring of `bufs` row blocks ([16 dy rows][s8 source rows] x
 // pitch bytes; dy rows M..15 and source rows S..s8-1 stay zero), full/empty
 // barriers, statistics ring [kGenTokSlots][2*M*S + S], partial tiles
-// [kgroups][16][s8], DA [16][s8], zr [16][s8], coefficient table [S][cs].
+// [kgroups][16][s8], DA [16][s8], zr [16][s8], coefficient table [S][cs]
+// (queries padded to M4 = M rounded up to 4, for 16-byte loads: alpha at 0,
+// b at M4, c at 2 M4; the padding stays zero).
 struct GenALayout {
     uint32_t ring, full, empty, tfull, tempty, tok, red, da, zr, coef, misc, total;
     uint32_t buf_bytes, tstride;
@@ -117,9 +119,15 @@ __host__ __device__ inline GenALayout gen_a_layout(int bufs, int s8, uint32_t pi
     return L;
 }
 
-__global__ void __launch_bounds__(kGenThreads, 1) attnres_multi_coef_kernel(const __grid_constant__ MultiGenArgs a) {
+// Four consumer warps and a producer warp; two CTAs share an SM, so one
+// CTA's per-token reductions overlap the other's MMAs and copies.
+constexpr int kCoefWarps = kMultiCoefWarps;
+constexpr int kCoefThreads = (kCoefWarps + 1) * 32;
+
+__global__ void __launch_bounds__(kCoefThreads, 2) attnres_multi_coef_kernel(const __grid_constant__ MultiGenArgs a) {
     extern __shared__ __align__(128) unsigned char smem[];
     const int S = a.S, M = a.M, s8 = a.s8;
+    const int M4 = (M + 3) & ~3;
     const int MS = M * S;
     const int ntiles = s8 / 8;
     const int kg = a.kgroups;
@@ -143,32 +151,39 @@ __global__ void __launch_bounds__(kGenThreads, 1) attnres_multi_coef_kernel(cons
     const int D = a.D;
     const uint32_t pitch = a.pitch;
     const int tstride = static_cast<int>(L.tstride);
+    const int cs = a.cs;
+    constexpr int nct = kCoefWarps * 32;
 
     if (threadIdx.x == 0) {
         for (int b = 0; b < B; ++b) {
             mbar_init(full + b, 1);
-            mbar_init(empty + b, kGenWarps);
+            mbar_init(empty + b, kCoefWarps);
         }
         for (int k = 0; k < kGenTokSlots; ++k) {
             mbar_init(tfull + k, 32);
-            mbar_init(tempty + k, kGenWarps);
+            mbar_init(tempty + k, kCoefWarps);
         }
         *abort_flag = 0;
         mbar_fence_init();
     }
-    // the padding rows of every buffer (dy rows M..15, source rows S..s8-1) stay zero
+    // the padding rows of every buffer (dy rows M..15, source rows S..s8-1)
+    // and the coefficient table's padding stay zero
     for (int b = 0; b < B; ++b) {
         unsigned char* buf = smem + L.ring + b * L.buf_bytes;
-        const int pad_rows[2][2] = {{M, 16}, {16 + S, 16 + s8}};
-        for (int p = 0; p < 2; ++p)
-            for (int i = pad_rows[p][0] * static_cast<int>(pitch) / 16 + threadIdx.x;
-                 i < pad_rows[p][1] * static_cast<int>(pitch) / 16; i += blockDim.x)
-                *reinterpret_cast<uint4*>(buf + 16 * i) = make_uint4(0u, 0u, 0u, 0u);
+        const int lo0 = M * static_cast<int>(pitch) / 16, hi0 = 16 * static_cast<int>(pitch) / 16;
+        const int lo1 = (16 + S) * static_cast<int>(pitch) / 16, hi1 = (16 + s8) * static_cast<int>(pitch) / 16;
+        for (int i = lo0 + threadIdx.x; i < hi0; i += blockDim.x)
+            *reinterpret_cast<uint4*>(buf + 16 * i) = make_uint4(0u, 0u, 0u, 0u);
+        for (int i = lo1 + threadIdx.x; i < hi1; i += blockDim.x)
+            *reinterpret_cast<uint4*>(buf + 16 * i) = make_uint4(0u, 0u, 0u, 0u);
     }
+    for (int i = threadIdx.x; i < S * cs; i += blockDim.x) coef[i] = 0.0f;
     __syncthreads();
 
-    if (warp == kGenWarps) {
+    if (warp == kCoefWarps) {
         // ------------------------------------------------------ producer
+        // lane 0 claims a buffer and announces its bytes; all lanes issue the
+        // row copies (one 1-D TMA copy per row, rows spread over the lanes)
         const uint64_t pol = policy_evict_first();
         int b = 0;
         uint32_t phase = 0;
@@ -190,32 +205,38 @@ __global__ void __launch_bounds__(kGenThreads, 1) attnres_multi_coef_kernel(cons
                 ts = 0;
                 tphase ^= 1u;
             }
-            if (lane == 0) {
-                for (int c = 0; c < nb; ++c) {
-                    const int c0 = c * dc;
-                    const int wc = min(dc, D - c0);
-                    const uint32_t bytes = static_cast<uint32_t>(wc) * 2u;
-                    const bool tail = (wc & 15) != 0;  // width 8 mod 16: zeros behind the block
-                    if (!mbar_wait(empty + b, phase ^ 1u, abort_flag, &g_multi_gen_error, kSiteBwdProducer)) break;
-                    mbar_arrive_expect_tx(full + b, (bytes + (tail ? 16u : 0u)) * static_cast<uint32_t>(M + S));
-                    unsigned char* buf = smem + L.ring + b * L.buf_bytes;
-                    for (int m = 0; m < M; ++m) {
-                        tma_load_1d(buf + m * pitch, a.dy + m * a.dy_ms + n * a.dy_ns + c0, bytes, full + b, pol);
-                        if (tail) tma_load_1d(buf + m * pitch + bytes, g_zero16, 16u, full + b, pol);
-                    }
-                    for (int s = 0; s < S; ++s) {
-                        const unsigned char* src = static_cast<const unsigned char*>(a.src[s]) + (n * a.src_ld + c0) * 2;
-                        tma_load_1d(buf + (16 + s) * pitch, src, bytes, full + b, pol);
-                        if (tail) tma_load_1d(buf + (16 + s) * pitch + bytes, g_zero16, 16u, full + b, pol);
-                    }
-                    ++issued;
-                    if (++b == B) {
-                        b = 0;
-                        phase ^= 1u;
-                    }
+            bool stop = false;
+            for (int c = 0; c < nb && !stop; ++c) {
+                const int c0 = c * dc;
+                const int wc = min(dc, D - c0);
+                const uint32_t bytes = static_cast<uint32_t>(wc) * 2u;
+                const bool tail = (wc & 15) != 0;  // width 8 mod 16: zeros behind the block
+                int ok = 1;
+                if (lane == 0) {
+                    ok = mbar_wait(empty + b, phase ^ 1u, abort_flag, &g_multi_gen_error, kSiteBwdProducer) ? 1 : 0;
+                    if (ok) mbar_arrive_expect_tx(full + b, (bytes + (tail ? 16u : 0u)) * static_cast<uint32_t>(M + S));
+                }
+                if (!__shfl_sync(0xffffffffu, ok, 0)) {
+                    stop = true;
+                    break;
+                }
+                unsigned char* buf = smem + L.ring + b * L.buf_bytes;
+                for (int r = lane; r < M + S; r += 32) {
+                    const bool dyrow = r < M;
+                    const int row = dyrow ? r : 16 + (r - M);
+                    const void* src = dyrow ? static_cast<const void*>(a.dy + r * a.dy_ms + n * a.dy_ns + c0)
+                                            : static_cast<const void*>(static_cast<const unsigned char*>(a.src[r - M]) +
+                                                                       (n * a.src_ld + c0) * 2);
+                    tma_load_1d(buf + row * pitch, src, bytes, full + b, pol);
+                    if (tail) tma_load_1d(buf + row * pitch + bytes, g_zero16, 16u, full + b, pol);
+                }
+                ++issued;
+                if (++b == B) {
+                    b = 0;
+                    phase ^= 1u;
                 }
             }
-            __syncwarp();
+            if (stop) break;
         }
         asm volatile("cp.async.wait_all;" ::: "memory");
         if (lane == 0 && *abort_flag) {
@@ -229,15 +250,14 @@ __global__ void __launch_bounds__(kGenThreads, 1) attnres_multi_coef_kernel(cons
     }
 
     // ---------------------------------------------------------- consumers
-    // warp -> (source tile group, k group): with fewer than eight 8-source
-    // tiles the k steps of a block are split between warps (partial tiles
-    // added afterwards in k-group order); with eight or more every warp owns
-    // whole tiles (tiles w, w + 8, ...).
-    const bool split_k = ntiles < kGenWarps;
+    // warp -> (source tile group, k group): with fewer 8-source tiles than
+    // warps the k steps of a block are split between warps (partial tiles
+    // added afterwards in k-group order); otherwise every warp owns whole
+    // tiles (tiles w, w + 4, w + 8, w + 12).
+    const bool split_k = ntiles < kCoefWarps;
     const int my_tile = split_k ? warp % ntiles : warp;
     const int my_kg = split_k ? warp / ntiles : 0;
     const bool active = !split_k || warp < ntiles * kg;
-    const int tile_step = split_k ? ntiles : kGenWarps;  // next tile of this warp (none when split)
     const uint32_t sbase = smem_u32(smem);
     const uint32_t ring_s = sbase + L.ring;
     const uint32_t full_s = sbase + L.full;
@@ -250,16 +270,15 @@ __global__ void __launch_bounds__(kGenThreads, 1) attnres_multi_coef_kernel(cons
     const uint32_t b_row = static_cast<uint32_t>(16 + (lane & 7)) * pitch + static_cast<uint32_t>(((lane >> 3) & 1) * 8) * 2u;
     const int g = lane >> 2, t4 = lane & 3;
     const float inv_r = 1.0f / static_cast<float>(a.R);
-    const int cs = a.cs;
 
     int b = 0;
     uint32_t phase = 0;
     int ts = 0;
     uint32_t tphase = 0;
     for (long long n = blockIdx.x; n < N; n += gridDim.x) {
-        float acc[2][4];  // up to two 8-source tiles per warp (s8 <= 128)
+        float acc[4][4];  // up to four 8-source tiles per warp (s8 <= 128)
 #pragma unroll
-        for (int j = 0; j < 2; ++j)
+        for (int j = 0; j < 4; ++j)
 #pragma unroll
             for (int e = 0; e < 4; ++e) acc[j][e] = 0.0f;
         for (int c = 0; c < nb; ++c) {
@@ -274,9 +293,9 @@ __global__ void __launch_bounds__(kGenThreads, 1) attnres_multi_coef_kernel(cons
                     ldsm_x4(buf + a_row + static_cast<uint32_t>(ks) * 32u, a0, a1, a2, a3);
                     dep ^= a0;
 #pragma unroll
-                    for (int j = 0; j < 2; ++j) {
-                        const int tile = my_tile + j * tile_step;
-                        if (tile < ntiles && (j == 0 || !split_k)) {
+                    for (int j = 0; j < 4; ++j) {
+                        const int tile = my_tile + j * kCoefWarps;
+                        if ((j == 0 || !split_k) && tile < ntiles) {
                             uint32_t b0, b1;
                             ldsm_x2(buf + b_row + static_cast<uint32_t>(tile * 8) * pitch + static_cast<uint32_t>(ks) * 32u,
                                     b0, b1);
@@ -296,9 +315,9 @@ __global__ void __launch_bounds__(kGenThreads, 1) attnres_multi_coef_kernel(cons
         // partial tiles -> red[k group][query][source]; then DA = their sum in k-group order
         if (active) {
 #pragma unroll
-            for (int j = 0; j < 2; ++j) {
-                const int tile = my_tile + j * tile_step;
-                if (tile < ntiles && (j == 0 || !split_k)) {
+            for (int j = 0; j < 4; ++j) {
+                const int tile = my_tile + j * kCoefWarps;
+                if ((j == 0 || !split_k) && tile < ntiles) {
                     float* r = red + (my_kg * 16) * s8;
                     const int s0 = tile * 8 + 2 * t4;
                     r[g * s8 + s0] = acc[j][0];
@@ -308,17 +327,17 @@ __global__ void __launch_bounds__(kGenThreads, 1) attnres_multi_coef_kernel(cons
                 }
             }
         }
-        named_bar_sync(1, kGenWarps * 32);
-        for (int i = threadIdx.x; i < 16 * s8; i += kGenWarps * 32) {
+        named_bar_sync(1, nct);
+        for (int i = threadIdx.x; i < 16 * s8; i += nct) {
             float sum = 0.0f;
             for (int k = 0; k < kg; ++k) sum += red[k * 16 * s8 + i];
             da[i] = sum;
         }
         mbar_wait_s(tfull_s + 8u * ts, tphase, abort_flag, &g_multi_gen_error, kSiteBwdTokStat);
-        named_bar_sync(1, kGenWarps * 32);
+        named_bar_sync(1, nct);
         // coefficients: one warp per query, lanes over sources
         const float* tk = tok + ts * tstride;
-        for (int m = warp; m < M; m += kGenWarps) {
+        for (int m = warp; m < M; m += kCoefWarps) {
             float p = 0.0f;
             for (int s = lane; s < S; s += 32) p = fmaf(tk[m * S + s], da[m * s8 + s], p);
             const float delta = warp_sum(p);
@@ -327,18 +346,18 @@ __global__ void __launch_bounds__(kGenThreads, 1) attnres_multi_coef_kernel(cons
                 const float dz = al * (da[m * s8 + s] - delta);
                 const float r = tk[2 * MS + s];
                 coef[s * cs + m] = al;
-                coef[s * cs + M + m] = a.scale * r * dz;
+                coef[s * cs + M4 + m] = a.scale * r * dz;
                 zr[m * s8 + s] = dz * tk[MS + m * S + s];
             }
         }
-        named_bar_sync(1, kGenWarps * 32);
-        for (int s = threadIdx.x; s < S; s += kGenWarps * 32) {
+        named_bar_sync(1, nct);
+        for (int s = threadIdx.x; s < S; s += nct) {
             float z = 0.0f;
             for (int m = 0; m < M; ++m) z += zr[m * s8 + s];  // query order
             const float r = tk[2 * MS + s];
-            coef[s * cs + 2 * M] = -(r * r) * inv_r * z;
+            coef[s * cs + 2 * M4] = -(r * r) * inv_r * z;
         }
-        named_bar_sync(1, kGenWarps * 32);
+        named_bar_sync(1, nct);
         __syncwarp();
         if (lane == 0) mbar_arrive_s(tempty_s + 8u * ts);
         if (++ts == kGenTokSlots) {
@@ -348,22 +367,23 @@ __global__ void __launch_bounds__(kGenThreads, 1) attnres_multi_coef_kernel(cons
         // the token's table -> workspace (16-byte stores; cs is a multiple of 4)
         float4* out = reinterpret_cast<float4*>(a.coef + n * static_cast<long long>(S) * cs);
         const float4* in = reinterpret_cast<const float4*>(coef);
-        for (int i = threadIdx.x; i < S * cs / 4; i += kGenWarps * 32) out[i] = in[i];
-        named_bar_sync(1, kGenWarps * 32);  // the table and DA are rewritten by the next token
+        for (int i = threadIdx.x; i < S * cs / 4; i += nct) out[i] = in[i];
+        named_bar_sync(1, nct);  // the table and DA are rewritten by the next token
     }
 }
 
 // ---------------------------------------------------------------- kernel B
-// Shared memory: token slots [kGenTokSlots] x {coefficient table [S][cs],
-// dy block [M][dcb], ids [M] (selected)}, source chunk ring [chunks][rows]
-// [dcb], barriers, the selected bank's block [(E + 1) pairs of rows] when it
-// is kept in shared memory.
+// Shared memory: `tslots` token slots x {coefficient table [S][cs], dy block
+// [M][dcb], ids [M] (selected)}, source chunk ring [chunks][rows][dcb],
+// barriers, the selected bank's block [(E + 1) rows] when it is kept in
+// shared memory.
 struct GenBLayout {
     uint32_t slot, slot_bytes, coef_off, dy_off, ids_off, ring, chunk_bytes, full, empty, tfull, tempty, bank, misc,
         total;
 };
 
-__host__ __device__ inline GenBLayout gen_b_layout(int S, int cs, int M, int dcb, int rows, int chunks, int bank_rows) {
+__host__ __device__ inline GenBLayout gen_b_layout(int S, int cs, int M, int dcb, int rows, int chunks, int bank_rows,
+                                                   int tslots) {
     GenBLayout L;
     const uint32_t row = static_cast<uint32_t>(dcb) * 2u;
     L.coef_off = 0;
@@ -372,7 +392,7 @@ __host__ __device__ inline GenBLayout gen_b_layout(int S, int cs, int M, int dcb
     L.slot_bytes = align_up(L.ids_off + static_cast<uint32_t>(M) * 8u, 128);
     uint32_t off = 0;
     L.slot = off;
-    off += kGenTokSlots * L.slot_bytes;
+    off += static_cast<uint32_t>(tslots) * L.slot_bytes;
     L.ring = off;
     L.chunk_bytes = static_cast<uint32_t>(rows) * row;
     off += static_cast<uint32_t>(chunks) * L.chunk_bytes;
@@ -382,9 +402,9 @@ __host__ __device__ inline GenBLayout gen_b_layout(int S, int cs, int M, int dcb
     L.empty = off;
     off += 8u * chunks;
     L.tfull = off;
-    off += 8u * kGenTokSlots;
+    off += 8u * tslots;
     L.tempty = off;
-    off += 8u * kGenTokSlots;
+    off += 8u * tslots;
     off = align_up(off, 16);
     L.bank = off;
     off += static_cast<uint32_t>(bank_rows) * row;
@@ -394,18 +414,22 @@ __host__ __device__ inline GenBLayout gen_b_layout(int S, int cs, int M, int dcb
     return L;
 }
 
-// MQ: register arrays for up to MQ queries (the run-time M <= MQ).  SEL:
-// per-token queries from the bank rows a.ids selects.
-template <int MQ, bool SEL>
+// MQ: register arrays for up to MQ queries (the run-time M <= MQ).  P: column
+// pairs per thread (the CTA's block is 512 * P columns; pair p of thread t is
+// columns 2 (t + 256 p) and the next).  SEL: per-token queries from the bank
+// rows a.ids selects.
+template <int MQ, int P, bool SEL>
 __global__ void __launch_bounds__(kGenThreads, 1) attnres_multi_grad_kernel(const __grid_constant__ MultiGenArgs a) {
     extern __shared__ __align__(128) unsigned char smem[];
     const int S = a.S, M = a.M, cs = a.cs;
-    const int dcb = a.dcb;
+    const int M4 = (M + 3) & ~3;  // queries padded to 4 in the coefficient table
+    const int dcb = a.dcb;        // == kMultiGenColumns * P
     const int G = a.rows_b;
     const int K = a.chunks_b;
+    const int TS = a.tslots_b;
     const int E = SEL ? a.E : 0;
     const bool bank_smem = SEL && a.bank_rows > 0;
-    const GenBLayout L = gen_b_layout(S, cs, M, dcb, G, K, a.bank_rows);
+    const GenBLayout L = gen_b_layout(S, cs, M, dcb, G, K, a.bank_rows, TS);
     uint64_t* full = reinterpret_cast<uint64_t*>(smem + L.full);
     uint64_t* empty = reinterpret_cast<uint64_t*>(smem + L.empty);
     uint64_t* tfull = reinterpret_cast<uint64_t*>(smem + L.tfull);
@@ -431,7 +455,7 @@ __global__ void __launch_bounds__(kGenThreads, 1) attnres_multi_grad_kernel(cons
             mbar_init(full + k, 1);
             mbar_init(empty + k, kGenWarps);
         }
-        for (int k = 0; k < kGenTokSlots; ++k) {
+        for (int k = 0; k < TS; ++k) {
             // the TMA copies (one arrival with their bytes); with selected
             // queries also the producer's cp.async copies of the ids
             mbar_init(tfull + k, SEL ? 2 : 1);
@@ -440,12 +464,18 @@ __global__ void __launch_bounds__(kGenThreads, 1) attnres_multi_grad_kernel(cons
         *abort_flag = 0;
         mbar_fence_init();
     }
-    // the thread's column pair and its key channels
-    const int j0 = c0 + 2 * static_cast<int>(threadIdx.x);  // first column of the pair
-    const bool own = threadIdx.x < kGenWarps * 32 && 2 * static_cast<int>(threadIdx.x) < wc;
+    // the thread's column pairs and their key channels
     const int ko = a.ko, kend = a.ko + a.R;
-    const bool kx = own && j0 >= ko && j0 < kend;
-    const bool ky = own && j0 + 1 >= ko && j0 + 1 < kend;
+    int j0[P];
+    bool own[P], kx[P], ky[P];
+#pragma unroll
+    for (int p = 0; p < P; ++p) {
+        const int pi = static_cast<int>(threadIdx.x) + p * kGenWarps * 32;  // pair index within the block
+        j0[p] = c0 + 2 * pi;
+        own[p] = threadIdx.x < kGenWarps * 32 && 2 * pi < wc;
+        kx[p] = own[p] && j0[p] >= ko && j0[p] < kend;
+        ky[p] = own[p] && j0[p] + 1 >= ko && j0[p] + 1 < kend;
+    }
     if (bank_smem) {
         // the bank's key values at this block's columns, row e at L.bank + e * rowp
         // (row E stays zero: it serves an id outside [0, E))
@@ -456,102 +486,114 @@ __global__ void __launch_bounds__(kGenThreads, 1) attnres_multi_grad_kernel(cons
                                                             : static_cast<uint16_t>(0);
         }
     }
-    if (SEL && (kx || ky)) {
+    if (SEL) {
         // this thread's key channels of the group's partial rows start at zero
         // (the same thread adds to them later, so program order suffices)
-        for (int e = 0; e < E; ++e) {
-            if (kx) prow[static_cast<long long>(e) * a.R + (j0 - ko)] = 0.0f;
-            if (ky) prow[static_cast<long long>(e) * a.R + (j0 + 1 - ko)] = 0.0f;
-        }
+#pragma unroll
+        for (int p = 0; p < P; ++p)
+            for (int e = 0; e < E; ++e) {
+                if (kx[p]) prow[static_cast<long long>(e) * a.R + (j0[p] - ko)] = 0.0f;
+                if (ky[p]) prow[static_cast<long long>(e) * a.R + (j0[p] + 1 - ko)] = 0.0f;
+            }
     }
     __syncthreads();
 
     if (warp == kGenWarps) {
         // ------------------------------------------------------ producer
+        // lane 0 claims a slot or chunk and announces its bytes; all lanes
+        // issue the row copies
         const uint64_t pol = policy_evict_first();
-        if (lane == 0) {
-            int k = 0;
-            uint32_t phase = 0;
-            int ts = 0;
-            uint32_t tphase = 0;
-            long long issued = 0, tissued = 0;
-            for (long long n = grp; n < N; n += ngrp) {
-                if (*abort_flag) break;
-                if (!mbar_wait(tempty + ts, tphase ^ 1u, abort_flag, &g_multi_gen_error, kSiteBwdProducer)) break;
-                unsigned char* slot = smem + L.slot + ts * L.slot_bytes;
-                const uint32_t cbytes = static_cast<uint32_t>(S * cs) * 4u;
-                mbar_arrive_expect_tx(tfull + ts, cbytes + static_cast<uint32_t>(M) * row_bytes);
-                tma_load_1d(slot + L.coef_off, a.coef + n * static_cast<long long>(S) * cs, cbytes, tfull + ts, pol);
-                for (int m = 0; m < M; ++m)
-                    tma_load_1d(slot + L.dy_off + m * rowp, a.dy + m * a.dy_ms + n * a.dy_ns + c0, row_bytes,
-                                tfull + ts, pol);
-                if (SEL) {
-                    // ids are 8-byte aligned only: small asynchronous copies
-                    for (int m = 0; m < M; ++m) cp_async_8(slot + L.ids_off + 8 * m, a.ids + n * M + m);
-                    cp_async_arrive_noinc(tfull + ts);
-                }
-                ++tissued;
-                if (++ts == kGenTokSlots) {
-                    ts = 0;
-                    tphase ^= 1u;
-                }
-                bool stop = false;
-                for (int s0 = 0; s0 < S && !stop; s0 += G) {
-                    const int gs = min(G, S - s0);
-                    if (!mbar_wait(empty + k, phase ^ 1u, abort_flag, &g_multi_gen_error, kSiteBwdProducer)) {
-                        stop = true;
-                        break;
-                    }
-                    mbar_arrive_expect_tx(full + k, row_bytes * static_cast<uint32_t>(gs));
-                    for (int r = 0; r < gs; ++r) {
-                        const unsigned char* src =
-                            static_cast<const unsigned char*>(a.src[s0 + r]) + (n * a.src_ld + c0) * 2;
-                        tma_load_1d(smem + L.ring + k * L.chunk_bytes + r * rowp, src, row_bytes, full + k, pol);
-                    }
-                    ++issued;
-                    if (++k == K) {
-                        k = 0;
-                        phase ^= 1u;
-                    }
-                }
-                if (stop) break;
+        int k = 0;
+        uint32_t phase = 0;
+        int ts = 0;
+        uint32_t tphase = 0;
+        long long issued = 0, tissued = 0;
+        for (long long n = grp; n < N; n += ngrp) {
+            if (__shfl_sync(0xffffffffu, *abort_flag, 0)) break;
+            int ok = 1;
+            const uint32_t cbytes = static_cast<uint32_t>(S * cs) * 4u;
+            if (lane == 0) {
+                ok = mbar_wait(tempty + ts, tphase ^ 1u, abort_flag, &g_multi_gen_error, kSiteBwdProducer) ? 1 : 0;
+                if (ok) mbar_arrive_expect_tx(tfull + ts, cbytes + static_cast<uint32_t>(M) * row_bytes);
             }
-            asm volatile("cp.async.wait_all;" ::: "memory");
-            if (*abort_flag) {
-                for (int c = 0; c < K && c < issued; ++c) {
-                    const long long fills = (issued - 1 - c) / K + 1;
-                    volatile int no_abort = 0;
-                    mbar_wait(full + c, static_cast<uint32_t>((fills - 1) & 1), &no_abort, &g_multi_gen_error,
-                              kSiteDrain);
+            if (!__shfl_sync(0xffffffffu, ok, 0)) break;
+            unsigned char* slot = smem + L.slot + ts * L.slot_bytes;
+            if (lane == 0)
+                tma_load_1d(slot + L.coef_off, a.coef + n * static_cast<long long>(S) * cs, cbytes, tfull + ts, pol);
+            for (int m = lane; m < M; m += 32)
+                tma_load_1d(slot + L.dy_off + m * rowp, a.dy + m * a.dy_ms + n * a.dy_ns + c0, row_bytes, tfull + ts,
+                            pol);
+            if (SEL && lane == 0) {
+                // ids are 8-byte aligned only: small asynchronous copies
+                for (int m = 0; m < M; ++m) cp_async_8(slot + L.ids_off + 8 * m, a.ids + n * M + m);
+                cp_async_arrive_noinc(tfull + ts);
+            }
+            ++tissued;
+            if (++ts == TS) {
+                ts = 0;
+                tphase ^= 1u;
+            }
+            bool stop = false;
+            for (int s0 = 0; s0 < S; s0 += G) {
+                const int gs = min(G, S - s0);
+                if (lane == 0) {
+                    ok = mbar_wait(empty + k, phase ^ 1u, abort_flag, &g_multi_gen_error, kSiteBwdProducer) ? 1 : 0;
+                    if (ok) mbar_arrive_expect_tx(full + k, row_bytes * static_cast<uint32_t>(gs));
                 }
-                for (int c = 0; c < kGenTokSlots && c < tissued; ++c) {
-                    const long long fills = (tissued - 1 - c) / kGenTokSlots + 1;
-                    volatile int no_abort = 0;
-                    mbar_wait(tfull + c, static_cast<uint32_t>((fills - 1) & 1), &no_abort, &g_multi_gen_error,
-                              kSiteDrain);
+                if (!__shfl_sync(0xffffffffu, ok, 0)) {
+                    stop = true;
+                    break;
                 }
+                for (int r = lane; r < gs; r += 32) {
+                    const unsigned char* src = static_cast<const unsigned char*>(a.src[s0 + r]) + (n * a.src_ld + c0) * 2;
+                    tma_load_1d(smem + L.ring + k * L.chunk_bytes + r * rowp, src, row_bytes, full + k, pol);
+                }
+                ++issued;
+                if (++k == K) {
+                    k = 0;
+                    phase ^= 1u;
+                }
+            }
+            if (stop) break;
+        }
+        asm volatile("cp.async.wait_all;" ::: "memory");
+        if (lane == 0 && *abort_flag) {
+            for (int c = 0; c < K && c < issued; ++c) {
+                const long long fills = (issued - 1 - c) / K + 1;
+                volatile int no_abort = 0;
+                mbar_wait(full + c, static_cast<uint32_t>((fills - 1) & 1), &no_abort, &g_multi_gen_error, kSiteDrain);
+            }
+            for (int c = 0; c < TS && c < tissued; ++c) {
+                const long long fills = (tissued - 1 - c) / TS + 1;
+                volatile int no_abort = 0;
+                mbar_wait(tfull + c, static_cast<uint32_t>((fills - 1) & 1), &no_abort, &g_multi_gen_error, kSiteDrain);
             }
         }
         return;
     }
 
     // ---------------------------------------------------------- consumers
-    float2 qv[MQ], dqs[MQ];
+    float2 qv[MQ][P], dqs[MQ][P];
 #pragma unroll
-    for (int m = 0; m < MQ; ++m) {
-        float x = 0.0f, y = 0.0f;
-        if (!SEL && m < M) {
-            if (kx) x = bf16_bits_to_float(a.q[static_cast<long long>(m) * a.R + (j0 - ko)]);
-            if (ky) y = bf16_bits_to_float(a.q[static_cast<long long>(m) * a.R + (j0 + 1 - ko)]);
+    for (int m = 0; m < MQ; ++m)
+#pragma unroll
+        for (int p = 0; p < P; ++p) {
+            float x = 0.0f, y = 0.0f;
+            if (!SEL && m < M) {
+                if (kx[p]) x = bf16_bits_to_float(a.q[static_cast<long long>(m) * a.R + (j0[p] - ko)]);
+                if (ky[p]) y = bf16_bits_to_float(a.q[static_cast<long long>(m) * a.R + (j0[p] + 1 - ko)]);
+            }
+            qv[m][p] = make_float2(x, y);
+            dqs[m][p] = make_float2(0.0f, 0.0f);
         }
-        qv[m] = make_float2(x, y);
-        dqs[m] = make_float2(0.0f, 0.0f);
-    }
     const uint32_t sbase = smem_u32(smem);
-    const uint32_t lane_off = 4u * threadIdx.x;  // this thread's pair within a row
+    const uint32_t lane_off = 4u * threadIdx.x;          // the thread's first pair within a row
+    constexpr uint32_t kPairStep = 4u * kGenWarps * 32;  // bytes between a thread's pairs
     const uint32_t full_s = sbase + L.full, empty_s = sbase + L.empty;
     const uint32_t tfull_s = sbase + L.tfull, tempty_s = sbase + L.tempty;
-    const float2 keep = make_float2(kx ? 1.0f : 0.0f, ky ? 1.0f : 0.0f);
+    float2 keep[P];
+#pragma unroll
+    for (int p = 0; p < P; ++p) keep[p] = make_float2(kx[p] ? 1.0f : 0.0f, ky[p] ? 1.0f : 0.0f);
     int k = 0;
     uint32_t phase = 0;
     int ts = 0;
@@ -560,44 +602,55 @@ __global__ void __launch_bounds__(kGenThreads, 1) attnres_multi_grad_kernel(cons
         mbar_wait_s(tfull_s + 8u * ts, tphase, abort_flag, &g_multi_gen_error, kSiteBwdConsumer);
         const unsigned char* slot = smem + L.slot + ts * L.slot_bytes;
         const uint32_t slot_s = sbase + L.slot + ts * L.slot_bytes;
-        const float* ctab = reinterpret_cast<const float*>(slot + L.coef_off);
-        float2 dyv[MQ];
+        const uint32_t ctab_s = slot_s + L.coef_off;
+        float2 dyv[MQ][P];
 #pragma unroll
-        for (int m = 0; m < MQ; ++m) {
-            uint32_t w = 0;
-            if (m < M && own) asm volatile("ld.shared.b32 %0, [%1];" : "=r"(w) : "r"(slot_s + L.dy_off + m * rowp + lane_off));
-            dyv[m] = bf2_to_f2(w);
-        }
+        for (int m = 0; m < MQ; ++m)
+#pragma unroll
+            for (int p = 0; p < P; ++p) {
+                uint32_t w = 0;
+                if (m < M && own[p])
+                    asm volatile("ld.shared.b32 %0, [%1];"
+                                 : "=r"(w)
+                                 : "r"(slot_s + L.dy_off + m * rowp + lane_off + p * kPairStep));
+                dyv[m][p] = bf2_to_f2(w);
+            }
         int qrow[MQ];
         if constexpr (SEL) {
             const long long* ids = reinterpret_cast<const long long*>(slot + L.ids_off);
 #pragma unroll
             for (int m = 0; m < MQ; ++m) {
-                qrow[m] = -1;
-                float x = 0.0f, y = 0.0f;
+                long long id = -1;
                 if (m < M) {
-                    const long long id = ids[m];
+                    id = ids[m];
                     if (id < 0 || id >= E) {
                         if (threadIdx.x == 0) atomicCAS(&g_multi_gen_error, 0u, static_cast<unsigned>(kSiteBadId));
-                    } else {
-                        qrow[m] = static_cast<int>(id);
+                        id = -1;
+                    }
+                }
+                qrow[m] = static_cast<int>(id);
+#pragma unroll
+                for (int p = 0; p < P; ++p) {
+                    float x = 0.0f, y = 0.0f;
+                    if (id >= 0) {
                         if (bank_smem) {
                             uint32_t w = 0;
-                            if (own)
+                            if (own[p])
                                 asm volatile("ld.shared.b32 %0, [%1];"
                                              : "=r"(w)
-                                             : "r"(sbase + L.bank + static_cast<uint32_t>(id) * rowp + lane_off));
+                                             : "r"(sbase + L.bank + static_cast<uint32_t>(id) * rowp + lane_off +
+                                                   p * kPairStep));
                             const float2 f = bf2_to_f2(w);
                             x = f.x;
                             y = f.y;
                         } else {
-                            if (kx) x = bf16_bits_to_float(a.q[id * a.R + (j0 - ko)]);
-                            if (ky) y = bf16_bits_to_float(a.q[id * a.R + (j0 + 1 - ko)]);
+                            if (kx[p]) x = bf16_bits_to_float(a.q[id * a.R + (j0[p] - ko)]);
+                            if (ky[p]) y = bf16_bits_to_float(a.q[id * a.R + (j0[p] + 1 - ko)]);
                         }
                     }
+                    qv[m][p] = make_float2(x, y);
+                    dqs[m][p] = make_float2(0.0f, 0.0f);
                 }
-                qv[m] = make_float2(x, y);
-                dqs[m] = make_float2(0.0f, 0.0f);
             }
         }
         for (int s0 = 0; s0 < S; s0 += G) {
@@ -607,27 +660,53 @@ __global__ void __launch_bounds__(kGenThreads, 1) attnres_multi_grad_kernel(cons
             uint32_t dep = 0;
             for (int r = 0; r < gs; ++r) {
                 const int s = s0 + r;
-                uint32_t w = 0;
-                if (own) asm volatile("ld.shared.b32 %0, [%1];" : "=r"(w) : "r"(chunk + static_cast<uint32_t>(r) * rowp));
-                dep ^= w;
-                const float2 t = fmul2(bf2_to_f2(w), keep);  // key channels of the row
-                const float* crow = ctab + s * cs;            // alpha_s0.., b_s0.., c_s (broadcast)
-                float2 o = make_float2(0.0f, 0.0f);
+                float2 t[P];
 #pragma unroll
-                for (int m = 0; m < MQ; ++m) {
-                    if (m < M) {
-                        const float al = crow[m];
-                        const float bq = crow[M + m];
-                        o = ffma2(make_float2(al, al), dyv[m], o);
-                        o = ffma2(make_float2(bq, bq), qv[m], o);
-                        dqs[m] = ffma2(make_float2(bq, bq), t, dqs[m]);
+                for (int p = 0; p < P; ++p) {
+                    uint32_t w = 0;
+                    if (own[p])
+                        asm volatile("ld.shared.b32 %0, [%1];"
+                                     : "=r"(w)
+                                     : "r"(chunk + static_cast<uint32_t>(r) * rowp + p * kPairStep));
+                    dep ^= w;
+                    t[p] = fmul2(bf2_to_f2(w), keep[p]);  // key channels of the row
+                }
+                // alpha_s., b_s. and c_s of the row: 16-byte broadcast loads of the
+                // padded table; four independent FMA chains for the dy and query terms
+                const uint32_t crow = ctab_s + static_cast<uint32_t>(s * cs) * 4u;
+                float2 oa[2][P], ob[2][P];
+#pragma unroll
+                for (int h = 0; h < 2; ++h)
+#pragma unroll
+                    for (int p = 0; p < P; ++p) oa[h][p] = ob[h][p] = make_float2(0.0f, 0.0f);
+#pragma unroll
+                for (int g4 = 0; g4 < MQ / 4; ++g4) {
+                    if (4 * g4 < M) {
+                        const float4 av = lds128f(crow + 16u * g4);
+                        const float4 bv = lds128f(crow + 4u * M4 + 16u * g4);
+                        const float al[4] = {av.x, av.y, av.z, av.w};
+                        const float bl[4] = {bv.x, bv.y, bv.z, bv.w};
+#pragma unroll
+                        for (int j = 0; j < 4; ++j) {
+                            const int m = 4 * g4 + j;
+                            const float2 al2 = make_float2(al[j], al[j]), bq2 = make_float2(bl[j], bl[j]);
+#pragma unroll
+                            for (int p = 0; p < P; ++p) {
+                                oa[j & 1][p] = ffma2(al2, dyv[m][p], oa[j & 1][p]);
+                                ob[j & 1][p] = ffma2(bq2, qv[m][p], ob[j & 1][p]);
+                                dqs[m][p] = ffma2(bq2, t[p], dqs[m][p]);
+                            }
+                        }
                     }
                 }
-                const float cv = crow[2 * M];
-                o = ffma2(make_float2(cv, cv), t, o);
-                if (own) {
-                    uint16_t* drow = static_cast<uint16_t*>(a.dsrc[s]) + n * a.dsrc_ld + j0;
-                    asm volatile("st.global.cs.b32 [%0], %1;" ::"l"(drow), "r"(pack_f2(o)) : "memory");
+                float cv;
+                asm volatile("ld.shared.f32 %0, [%1];" : "=f"(cv) : "r"(crow + 8u * M4));
+                const float2 cv2 = make_float2(cv, cv), one = make_float2(1.0f, 1.0f);
+                uint16_t* drow = static_cast<uint16_t*>(a.dsrc[s]) + n * a.dsrc_ld;
+#pragma unroll
+                for (int p = 0; p < P; ++p) {
+                    const float2 o = ffma2(cv2, t[p], ffma2(one, oa[0][p], ffma2(one, oa[1][p], ffma2(one, ob[0][p], ob[1][p]))));
+                    if (own[p]) asm volatile("st.global.cs.b32 [%0], %1;" ::"l"(drow + j0[p]), "r"(pack_f2(o)) : "memory");
                 }
             }
             __syncwarp();
@@ -642,15 +721,18 @@ __global__ void __launch_bounds__(kGenThreads, 1) attnres_multi_grad_kernel(cons
 #pragma unroll
             for (int m = 0; m < MQ; ++m) {
                 if (m < M && qrow[m] >= 0) {
-                    float* p = prow + static_cast<long long>(qrow[m]) * a.R;
-                    if (kx) red_add_f32(p + (j0 - ko), dqs[m].x);
-                    if (ky) red_add_f32(p + (j0 + 1 - ko), dqs[m].y);
+                    float* pq = prow + static_cast<long long>(qrow[m]) * a.R;
+#pragma unroll
+                    for (int p = 0; p < P; ++p) {
+                        if (kx[p]) red_add_f32(pq + (j0[p] - ko), dqs[m][p].x);
+                        if (ky[p]) red_add_f32(pq + (j0[p] + 1 - ko), dqs[m][p].y);
+                    }
                 }
             }
         }
         __syncwarp();
         if (lane == 0) mbar_arrive_s(tempty_s + 8u * ts);
-        if (++ts == kGenTokSlots) {
+        if (++ts == TS) {
             ts = 0;
             tphase ^= 1u;
         }
@@ -660,22 +742,33 @@ __global__ void __launch_bounds__(kGenThreads, 1) attnres_multi_grad_kernel(cons
 #pragma unroll
         for (int m = 0; m < MQ; ++m) {
             if (m < M) {
-                float* p = prow + static_cast<long long>(m) * a.R;
-                if (kx) p[j0 - ko] = dqs[m].x;
-                if (ky) p[j0 + 1 - ko] = dqs[m].y;
+                float* pq = prow + static_cast<long long>(m) * a.R;
+#pragma unroll
+                for (int p = 0; p < P; ++p) {
+                    if (kx[p]) pq[j0[p] - ko] = dqs[m][p].x;
+                    if (ky[p]) pq[j0[p] + 1 - ko] = dqs[m][p].y;
+                }
             }
         }
     }
 }
 
-template <int MQ, bool SEL>
+template <int MQ, int P, bool SEL>
 cudaError_t launch_grad_t(const MultiPlan& plan, const MultiGenArgs& a, cudaStream_t stream) {
-    auto kern = attnres_multi_grad_kernel<MQ, SEL>;
+    auto kern = attnres_multi_grad_kernel<MQ, P, SEL>;
     cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                            static_cast<int>(plan.gen_smem_b));
     if (err != cudaSuccess) return err;
     kern<<<plan.gen_grid_b, kGenThreads, plan.gen_smem_b, stream>>>(a);
     return cudaGetLastError();
+}
+
+template <bool SEL>
+cudaError_t launch_grad_sel(const MultiPlan& plan, const MultiGenArgs& a, cudaStream_t stream) {
+    const int P = a.dcb / kMultiGenColumns;
+    if (a.M <= 4) return P == 2 ? launch_grad_t<4, 2, SEL>(plan, a, stream) : launch_grad_t<4, 1, SEL>(plan, a, stream);
+    if (a.M <= 8) return P == 2 ? launch_grad_t<8, 2, SEL>(plan, a, stream) : launch_grad_t<8, 1, SEL>(plan, a, stream);
+    return launch_grad_t<16, 1, SEL>(plan, a, stream);
 }
 
 }  // namespace
@@ -684,24 +777,19 @@ size_t multi_gen_smem_a(int bufs, int s8, int pitch, int M, int S, int kgroups, 
     return gen_a_layout(bufs, s8, static_cast<uint32_t>(pitch), M, S, kgroups, cs).total;
 }
 
-size_t multi_gen_smem_b(int S, int cs, int M, int dcb, int rows, int chunks, int bank_rows) {
-    return gen_b_layout(S, cs, M, dcb, rows, chunks, bank_rows).total;
+size_t multi_gen_smem_b(int S, int cs, int M, int dcb, int rows, int chunks, int bank_rows, int tslots) {
+    return gen_b_layout(S, cs, M, dcb, rows, chunks, bank_rows, tslots).total;
 }
 
 cudaError_t launch_multi_bwd_general(const MultiPlan& plan, const MultiGenArgs& a, cudaStream_t stream) {
     cudaError_t err = cudaFuncSetAttribute(attnres_multi_coef_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                            static_cast<int>(plan.gen_smem_a));
     if (err != cudaSuccess) return err;
-    attnres_multi_coef_kernel<<<plan.gen_grid_a, kGenThreads, plan.gen_smem_a, stream>>>(a);
+    attnres_multi_coef_kernel<<<plan.gen_grid_a, kCoefThreads, plan.gen_smem_a, stream>>>(a);
     err = cudaGetLastError();
     if (err != cudaSuccess) return err;
     const bool sel = a.ids != nullptr;
-    if (a.M <= 4)
-        err = sel ? launch_grad_t<4, true>(plan, a, stream) : launch_grad_t<4, false>(plan, a, stream);
-    else if (a.M <= 8)
-        err = sel ? launch_grad_t<8, true>(plan, a, stream) : launch_grad_t<8, false>(plan, a, stream);
-    else
-        err = sel ? launch_grad_t<16, true>(plan, a, stream) : launch_grad_t<16, false>(plan, a, stream);
+    err = sel ? launch_grad_sel<true>(plan, a, stream) : launch_grad_sel<false>(plan, a, stream);
     if (err != cudaSuccess) return err;
     const int W = (sel ? a.E : a.M) * a.R;
     return launch_finalize(a.part, plan.gen_groups, W, W, a.dq, a.dq_f32, nullptr, nullptr, stream);

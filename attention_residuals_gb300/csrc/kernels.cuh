@@ -333,7 +333,7 @@ struct MultiPlan {
     int gen_grid_a, gen_grid_b, gen_groups;   // CTAs of the two kernels, token groups of the second
     size_t gen_smem_a, gen_smem_b;
     int gen_s8, gen_kgroups, gen_bufs, gen_dc, gen_pitch, gen_cs;
-    int gen_dcb, gen_rows_b, gen_chunks_b, gen_bank_rows;
+    int gen_dcb, gen_rows_b, gen_chunks_b, gen_bank_rows, gen_tslots_b;
     size_t gen_part_off;                      // workspace: coefficient tables, then partial rows
     int grid;
     int fgrid;             // forward CTAs (multi_fwd_ctas_per_sm per SM)
@@ -408,7 +408,7 @@ struct MultiGenArgs {
     int s8, kgroups, bufs, nblocks, dc, pitch, cs;
     // gradient kernel: column blocks of `dcb`, source chunks of `rows_b` rows
     // in a ring of `chunks_b`, bank rows kept in shared memory (E + 1, or 0)
-    int dcb, rows_b, chunks_b, bank_rows;
+    int dcb, rows_b, chunks_b, bank_rows, tslots_b;
     const uint16_t* q;     // [M][R], or the bank [E][R] with ids
     const long long* ids;  // [N][M] or NULL
     const uint16_t* dy;
@@ -423,9 +423,12 @@ struct MultiGenArgs {
 // Queries up to which the resident one-CTA multi-query backward runs (when
 // its layout fits); more queries take the general backward.
 constexpr int kMultiResidentMaxM = 4;
-constexpr int kMultiGenColumns = 512;   // columns per CTA of the gradient kernel
+constexpr int kMultiGenColumns = 512;   // columns per CTA of the gradient kernel, per column pair of a thread
+constexpr int kMultiGenMaxBufs = 8;     // row-block buffers of the coefficient kernel
+constexpr int kMultiCoefWarps = 4;      // consumer warps of the coefficient kernel
+constexpr int kMultiGenMaxSlots = 8;    // token slots of the gradient kernel
 size_t multi_gen_smem_a(int bufs, int s8, int pitch, int M, int S, int kgroups, int cs);
-size_t multi_gen_smem_b(int S, int cs, int M, int dcb, int rows, int chunks, int bank_rows);
+size_t multi_gen_smem_b(int S, int cs, int M, int dcb, int rows, int chunks, int bank_rows, int tslots);
 cudaError_t launch_multi_bwd_general(const MultiPlan& plan, const MultiGenArgs& a, cudaStream_t stream);
 unsigned take_multi_gen_error();
 
