@@ -951,7 +951,6 @@ static attnres_status multi_bwd_impl(const attnres_multi_params* p, const void* 
     if (!workspace || workspace_bytes < pl.ws_bytes) return ATTNRES_ERR_WORKSPACE;
     if (!aligned16(workspace)) return ATTNRES_ERR_ALIGNMENT;
     if (pl.gen) {
-        if (reinterpret_cast<uintptr_t>(workspace) & 255u) return ATTNRES_ERR_ALIGNMENT;
         MultiGenArgs g;
         std::memset(&g, 0, sizeof g);
         for (int s = 0; s < b.S; ++s) {

@@ -331,11 +331,17 @@ int attnres_jit_kernel_count(void);
  * The forward streams each token's rows once per block of queries it holds
  * in registers (one block for M <= 4 at D <= 2048, M <= 2 at D <= 4096;
  * later blocks re-read the token from L2), so any S and D are served.  The
- * backward keeps a token's S source rows, its M dy rows and the queries' key
- * channels in shared memory; shapes where these do not fit (roughly
- * (S + 2 * M) * D * 2 + M * R * 2 bytes beyond ~220 KB) return
- * ATTNRES_ERR_UNSUPPORTED from attnres_multi_bwd (and from
- * attnres_multi_plan_info) before anything is enqueued.
+ * backward has two forms, both serving every S, D and M the ABI accepts:
+ *  - resident (up to four queries, when a token's S source rows, its M dy
+ *    rows and the queries' key channels fit in shared memory): one kernel
+ *    that reads each row once;
+ *  - general (more queries, or tokens that do not fit): a coefficient kernel
+ *    forms the per-token dots <dy_m, v_s> over blocks of columns with bf16
+ *    tensor-core MMAs and writes every token's coefficients to the
+ *    workspace, then a gradient kernel forms dvalues and dq block by block;
+ *    the sources and dy are read twice.
+ * ATTNRES_MULTI_BWD=general or resident in the environment (read on every
+ * call) forces one form where it fits.
  * ------------------------------------------------------------------------ */
 #define ATTNRES_MAX_M 16
 
@@ -369,7 +375,9 @@ typedef struct {
 attnres_status attnres_multi_fwd(const attnres_multi_params* p, const void* q, void* y,
                                  float* alpha, float* rstd, float* logit, void* stream);
 
-/* Bytes of workspace attnres_multi_bwd needs (grid * M * R * 4; 0 when N == 0). */
+/* Bytes of workspace attnres_multi_bwd needs (0 when N == 0): the per-CTA FP32
+ * partial rows of dq, plus the general form's coefficient tables (N * S *
+ * (2 * M rounded up to 8 + 4) floats). */
 size_t attnres_multi_bwd_workspace_bytes(const attnres_multi_params* p);
 
 /*
@@ -386,15 +394,16 @@ attnres_status attnres_multi_bwd(const attnres_multi_params* p, const void* q, c
                                  void* workspace, size_t workspace_bytes, void* stream);
 
 /*
- * Launch plan of the multi-query kernels (no launch).  out[0..7]: forward
+ * Launch plan of the multi-query kernels (no launch).  out[0..9]: forward
  * CTAs * 1000 + backward CTAs, consumer warps (forward * 1000 + backward),
  * 16-byte vectors per thread (forward * 1000 + backward), queries per
  * register block (forward * 1000 + backward), forward ring (chunks * 1000 +
  * rows per chunk), backward ring (chunks * 1000 + rows per chunk), dy slots,
- * and the backward dynamic shared memory bytes.  UNSUPPORTED when the shape
- * does not fit.
+ * the backward dynamic shared memory bytes (of the gradient kernel in the
+ * general form), the backward form (0 resident, 1 general) and the general
+ * form's token groups (0 otherwise).
  */
-attnres_status attnres_multi_plan_info(const attnres_multi_params* p, int64_t out[8]);
+attnres_status attnres_multi_plan_info(const attnres_multi_params* p, int64_t out[10]);
 
 /* ------------------------------------------------------------------------
  * Selected-query read ("Fast Attention Residuals", section "Multi-query
@@ -407,9 +416,8 @@ attnres_status attnres_multi_plan_info(const attnres_multi_params* p, int64_t ou
  *
  * Gradients: dsrc sums over the K reads of each token; dbank[e] sums the
  * query gradients of every (n, k) with ids[n][k] == e (zero for rows no
- * token selects).  Same kernels, layouts and supported range as the
- * multi-query read with M = K slots per token, plus the bank's dq rows
- * (E * R * 4 bytes of shared memory) in the backward.
+ * token selects).  Same kernels, layouts and range as the multi-query read
+ * with M = K slots per token.
  *   p        as for the multi-query read, M = K (1 <= K <= ATTNRES_MAX_M)
  *   bank     bf16 [E][R] contiguous, E >= 1
  *   ids      int64 [N][K] contiguous, 8-byte aligned; an id outside
