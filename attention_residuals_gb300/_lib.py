@@ -45,6 +45,7 @@ EXPORTED = [
     "attnres_bwd_partial",
     "attnres_step_host",
     "attnres_step_host_workspace_bytes",
+    "attnres_fwd_withhold_for_test",
 ]
 
 
@@ -142,6 +143,8 @@ def load(path: str | None = None):
         lib.attnres_bwd_noalloc.restype = ctypes.c_int
         lib.attnres_bwd_noalloc.argtypes = [P, vp, vp, vp, fp, fp, fp, fp, fp,
                                             ctypes.POINTER(ctypes.c_void_p), i64, vp, fp, vp, fp, vp]
+        lib.attnres_fwd_withhold_for_test.restype = ctypes.c_int
+        lib.attnres_fwd_withhold_for_test.argtypes = [P, vp, vp, vp, fp, fp, fp, fp, i64, ctypes.c_uint32, vp]
         lib.attnres_check_device_error.restype = ctypes.c_int
         lib.attnres_check_device_error.argtypes = []
         lib.attnres_jit_kernel_count.restype = ctypes.c_int

@@ -6,6 +6,7 @@
 #include <mutex>
 
 #include "attnres.h"
+#include "attnres_testing.h"
 #include "kernels.cuh"
 
 namespace attnres {
@@ -567,7 +568,8 @@ attnres_status attnres_plan_info(const attnres_params* p, int64_t out[10]) {
 
 static attnres_status fwd_impl(const attnres_params* p, const void* q, const void* w_o, const void* delta,
                                int64_t delta_ld, void* partial_out, int64_t partial_ld, void* y, float* alpha,
-                               float* rstd, float* logit, float* o_rstd, float* o_pre, void* stream) {
+                               float* rstd, float* logit, float* o_rstd, float* o_pre, void* stream,
+                               long long test_withhold = 0, uint64_t test_wait_ns = 0) {
     attnres_status st = check_shape(p);
     if (st != ATTNRES_OK) return st;
     if (delta) {
@@ -619,8 +621,18 @@ static attnres_status fwd_impl(const attnres_params* p, const void* q, const voi
     a.delta_ld = delta_ld;
     a.partial_out = static_cast<uint16_t*>(partial_out);
     a.partial_ld = partial_ld;
+    a.test_withhold = test_withhold;
+    a.test_wait_ns = test_wait_ns;
     return launch_fwd(pl, a, static_cast<cudaStream_t>(stream)) == cudaSuccess ? ATTNRES_OK
                                                                               : ATTNRES_ERR_CUDA;
+}
+
+attnres_status attnres_fwd_withhold_for_test(const attnres_params* p, const void* q, const void* w_o, void* y,
+                                             float* alpha, float* rstd, float* logit, float* o_rstd,
+                                             int64_t withhold_fill, uint32_t wait_us, void* stream) {
+    if (withhold_fill < 1 || wait_us < 1 || wait_us > 1000000u) return ATTNRES_ERR_INVALID_ARG;
+    return fwd_impl(p, q, w_o, nullptr, 0, nullptr, 0, y, alpha, rstd, logit, o_rstd, nullptr, stream,
+                    withhold_fill, static_cast<uint64_t>(wait_us) * 1000ull);
 }
 
 attnres_status attnres_fwd(const attnres_params* p, const void* q, const void* w_o, void* y,

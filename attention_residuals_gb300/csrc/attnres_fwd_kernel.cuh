@@ -97,6 +97,9 @@ __global__ void __launch_bounds__(kMaxThreads, fwd_ctas_per_sm(VPT)) attnres_fwd
             mbar_init(dempty + k, 1);  // released by the one warp that forms the sum
         }
         *abort_flag = 0;
+        // the consumers' wait limit (microseconds, 0 = the default): nonzero
+        // only in a test of the recovery path
+        abort_flag[2] = static_cast<int>(a.test_wait_ns / 1000ull);
         mbar_fence_init();
     }
     __syncthreads();
@@ -125,9 +128,14 @@ __global__ void __launch_bounds__(kMaxThreads, fwd_ctas_per_sm(VPT)) attnres_fwd
                         dphase ^= 1u;
                     }
                 }
+                bool withheld = false;
                 for (int g0 = 0; g0 < S; g0 += G) {
                     const int gs = min(G, S - g0);
                     if (!mbar_wait(empty + k, phase ^ 1u, abort_flag, &g_fwd_error, kSiteFwdProducer)) break;
+                    if (a.test_withhold > 0 && blockIdx.x == 0 && issued + 1 == a.test_withhold) {
+                        withheld = true;  // test hook: this fill never comes
+                        break;
+                    }
                     mbar_arrive_expect_tx(full + k, bytes * static_cast<uint32_t>(gs));
                     for (int r = 0; r < gs; ++r) {
                         const unsigned char* src =
@@ -140,6 +148,7 @@ __global__ void __launch_bounds__(kMaxThreads, fwd_ctas_per_sm(VPT)) attnres_fwd
                         phase ^= 1u;
                     }
                 }
+                if (withheld) break;
             }
             if (*abort_flag) {
                 // Let every copy this thread started land before the CTA can exit.
@@ -245,7 +254,7 @@ __global__ void __launch_bounds__(kMaxThreads, fwd_ctas_per_sm(VPT)) attnres_fwd
                 int k = ck;
                 uint32_t ph = cphase;
                 for (int r0 = 0; r0 < gs; r0 += G) {
-                    mbar_wait_s(full_s + 8u * k, ph, abort_flag, &g_fwd_error, kSiteFwdConsumer);
+                    mbar_wait_ctl_s(full_s + 8u * k, ph, abort_flag, &g_fwd_error, kSiteFwdConsumer);
                     if (++k == K) {
                         k = 0;
                         ph ^= 1u;

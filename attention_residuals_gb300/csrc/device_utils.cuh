@@ -66,6 +66,10 @@ __device__ __forceinline__ uint64_t global_timer_ns() {
     return t;
 }
 
+// How long a wait on a shared-memory barrier lasts before the kernel gives
+// up on it (nanoseconds).
+constexpr uint64_t kWaitLimitNs = 2000000000ull;
+
 // Wait for the phase with the given parity to complete.  Gives up after
 // about two seconds: records `where` in *err (first failure wins), sets
 // *abort so the calling CTA stops waiting from then on, and returns false.
@@ -79,7 +83,7 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volati
     while (!mbar_try_wait_sleep(bar, parity, 20000u)) {
         if (((++spins) & 15u) == 0u) {
             if (*abort) return false;
-            if (global_timer_ns() - t0 > 2000000000ull) {
+            if (global_timer_ns() - t0 > kWaitLimitNs) {
                 atomicCAS(err, 0u, where);
                 *abort = 1;
                 return false;
@@ -310,15 +314,20 @@ __device__ __forceinline__ bool mbar_test_sleep_s(uint32_t bar, uint32_t parity,
 }
 
 // Bounded wait on a barrier given by its 32-bit shared address (see mbar_wait).
+// `abort` points at the CTA's control words in shared memory: abort[0] is the
+// abort flag; a kernel that sets abort[2] to a nonzero number of microseconds
+// (a test of the recovery path) shortens the limit, read only here, after the
+// first test of the barrier has failed.
 static __device__ __noinline__ bool mbar_wait_slow_s(uint32_t bar, uint32_t parity, volatile int* abort,
-                                              unsigned* err, unsigned where) {
+                                              unsigned* err, unsigned where, bool ctl_limit) {
     if (*abort) return false;
+    const uint64_t limit_ns = (ctl_limit && abort[2] > 0) ? static_cast<uint64_t>(abort[2]) * 1000ull : kWaitLimitNs;
     const uint64_t t0 = global_timer_ns();
     uint32_t spins = 0;
     while (!mbar_test_sleep_s(bar, parity, 20000u)) {
         if (((++spins) & 15u) == 0u) {
             if (*abort) return false;
-            if (global_timer_ns() - t0 > 2000000000ull) {
+            if (global_timer_ns() - t0 > limit_ns) {
                 atomicCAS(err, 0u, where);
                 *abort = 1;
                 return false;
@@ -331,7 +340,14 @@ static __device__ __noinline__ bool mbar_wait_slow_s(uint32_t bar, uint32_t pari
 __device__ __forceinline__ bool mbar_wait_s(uint32_t bar, uint32_t parity, volatile int* abort,
                                             unsigned* err, unsigned where) {
     if (mbar_test_s(bar, parity)) return true;
-    return mbar_wait_slow_s(bar, parity, abort, err, where);
+    return mbar_wait_slow_s(bar, parity, abort, err, where, false);
+}
+
+// As mbar_wait_s, with the limit abort[2] (microseconds) when that word is nonzero.
+__device__ __forceinline__ bool mbar_wait_ctl_s(uint32_t bar, uint32_t parity, volatile int* abort,
+                                                unsigned* err, unsigned where) {
+    if (mbar_test_s(bar, parity)) return true;
+    return mbar_wait_slow_s(bar, parity, abort, err, where, true);
 }
 
 __device__ __forceinline__ uint4 lds128(uint32_t addr) {
@@ -504,7 +520,7 @@ static __device__ __noinline__ bool mbar_wait_cluster_s(uint32_t bar, uint32_t p
     while (!mbar_test_cluster_s(bar, parity, 20000u)) {
         if (((++spins) & 15u) == 0u) {
             if (*abort) return false;
-            if (global_timer_ns() - t0 > 2000000000ull) {
+            if (global_timer_ns() - t0 > kWaitLimitNs) {
                 atomicCAS(err, 0u, where);
                 *abort = 1;
                 return false;

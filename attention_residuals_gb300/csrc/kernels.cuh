@@ -141,6 +141,12 @@ struct FwdArgs {
     long long delta_ld;
     uint16_t* partial_out;
     long long partial_ld;
+    // Test hooks (zero in every ordinary launch): with test_withhold = k > 0
+    // the producer of CTA 0 never issues its k-th chunk fill (and stops), so
+    // that CTA's consumers give up waiting for it after test_wait_ns
+    // nanoseconds (0: the default limit) -- the bounded-wait recovery path.
+    long long test_withhold;
+    uint64_t test_wait_ns;
 };
 constexpr int kDeltaSlots = 2;
 

@@ -1,6 +1,6 @@
 """C-ABI checks that need no GPU: the library builds, loads and exports every
-function include/attnres.h declares, and arguments that break the contract
-are rejected before anything is planned or launched."""
+function the headers in include/ declare, and arguments that break the
+contract are rejected before anything is planned or launched."""
 import ctypes
 import os
 import re
@@ -13,6 +13,8 @@ from attention_residuals_gb300.build import build
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 HEADER = os.path.join(ROOT, "include", "attnres.h")
+HEADERS = sorted(os.path.join(ROOT, "include", f) for f in os.listdir(os.path.join(ROOT, "include"))
+                 if f.endswith(".h"))
 
 
 @pytest.fixture(scope="module")
@@ -22,9 +24,11 @@ def lib():
 
 
 def declared_functions():
-    text = open(HEADER).read()
-    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
-    return sorted(set(re.findall(r"\b(attnres_[a-z_0-9]+)\s*\(", text)))
+    names = set()
+    for h in HEADERS:
+        text = re.sub(r"/\*.*?\*/", "", open(h).read(), flags=re.S)
+        names.update(re.findall(r"\b(attnres_[a-z_0-9]+)\s*\(", text))
+    return sorted(names)
 
 
 def test_header_declares_expected_entry_points():
