@@ -32,6 +32,7 @@ EXPORTED = [
     "attnres_bwd_workspace_bytes",
     "attnres_check_device_error",
     "attnres_jit_kernel_count",
+    "attnres_debug_checks",
     "attnres_status_string",
     "attnres_plan_info",
     "attnres_multi_fwd",
@@ -110,8 +111,10 @@ _lib = None
 
 
 def library_path() -> str:
-    from .build import LIB_PATH
-    return LIB_PATH
+    """The release build, or with ATTNRES_DEBUG_LIB=1 in the environment the
+    bounds-checked build (python -m attention_residuals_gb300.build --debug)."""
+    from .build import DEBUG_LIB_PATH, LIB_PATH
+    return DEBUG_LIB_PATH if os.environ.get("ATTNRES_DEBUG_LIB") == "1" else LIB_PATH
 
 
 def load(path: str | None = None):
@@ -149,6 +152,8 @@ def load(path: str | None = None):
         lib.attnres_check_device_error.argtypes = []
         lib.attnres_jit_kernel_count.restype = ctypes.c_int
         lib.attnres_jit_kernel_count.argtypes = []
+        lib.attnres_debug_checks.restype = ctypes.c_int
+        lib.attnres_debug_checks.argtypes = []
         lib.attnres_status_string.restype = ctypes.c_char_p
         lib.attnres_status_string.argtypes = [ctypes.c_int]
         lib.attnres_plan_info.restype = ctypes.c_int

@@ -5,6 +5,13 @@
 compiles csrc/*.cu in parallel (one -gencode for compute_103a/sm_103a) and
 links attention_residuals_gb300/libattnres_gb300.so against the shared CUDA
 runtime.  No PyTorch headers or libraries are involved.
+
+    python -m attention_residuals_gb300.build --debug
+
+writes libattnres_gb300_debug.so instead, compiled with -DATTNRES_DEBUG:
+every output store is checked against the call's sizes and a bad one is
+skipped and reported by attnres_check_device_error().  ATTNRES_DEBUG_LIB=1
+makes the Python binding load it.
 """
 from __future__ import annotations
 
@@ -21,6 +28,8 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 LIB_NAME = "libattnres_gb300.so"
 LIB_PATH = os.path.join(PKG, LIB_NAME)
+DEBUG_LIB_NAME = "libattnres_gb300_debug.so"
+DEBUG_LIB_PATH = os.path.join(PKG, DEBUG_LIB_NAME)
 SOURCES = ["attnres_fwd.cu", "attnres_bwd.cu", "attnres_bwd_norm.cu", "attnres_bwd_opre.cu", "attnres_bwd_cluster.cu",
            "attnres_multi_fwd.cu", "attnres_multi_bwd.cu", "attnres_multi_general.cu", "attnres_api.cu", "attnres_host.cu", "attnres_jit.cu"]
 # Sources the library compiles again at run time for exact plan shapes
@@ -45,11 +54,12 @@ def _cuda_lib_dir() -> str:
     return os.path.join(cuda, "lib64")
 
 
-def _stale() -> bool:
-    if not os.path.exists(LIB_PATH):
+def _stale(path: str) -> bool:
+    if not os.path.exists(path):
         return True
-    t = os.path.getmtime(LIB_PATH)
-    deps = [os.path.join(CSRC, f) for f in os.listdir(CSRC)] + [os.path.join(INCLUDE, "attnres.h")]
+    t = os.path.getmtime(path)
+    deps = [os.path.join(CSRC, f) for f in os.listdir(CSRC)] + [
+        os.path.join(INCLUDE, f) for f in os.listdir(INCLUDE) if f.endswith(".h")]
     return any(os.path.getmtime(d) > t for d in deps if os.path.isfile(d))
 
 
@@ -68,14 +78,15 @@ def _write_jit_sources(path: str) -> None:
         f.write("\n".join(parts) + "\n")
 
 
-def build(force: bool = False, verbose: bool = False, extra_flags=None) -> str:
-    if not force and not _stale():
-        return LIB_PATH
+def build(force: bool = False, verbose: bool = False, extra_flags=None, debug: bool = False) -> str:
+    lib_path, lib_name = (DEBUG_LIB_PATH, DEBUG_LIB_NAME) if debug else (LIB_PATH, LIB_NAME)
+    if not force and not _stale(lib_path):
+        return lib_path
     nvcc = _nvcc()
     tmp = tempfile.mkdtemp(prefix="attnres_build_")
     libdir = _cuda_lib_dir()
     flags = ["-std=c++17", "-O3", *ARCH, "-lineinfo", "-Xcompiler", "-fPIC", "-I", INCLUDE,
-             "-I", CSRC, "-I", tmp, f'-DATTNRES_CUDA_LIBDIR="{libdir}"'] + list(extra_flags or [])
+             "-I", CSRC, "-I", tmp, f'-DATTNRES_CUDA_LIBDIR="{libdir}"'] + (["-DATTNRES_DEBUG"] if debug else []) + list(extra_flags or [])
     if verbose:
         flags += ["-Xptxas", "-v"]
     try:
@@ -92,18 +103,18 @@ def build(force: bool = False, verbose: bool = False, extra_flags=None) -> str:
 
         with ThreadPoolExecutor(max_workers=len(SOURCES)) as ex:
             objs = list(ex.map(compile_one, SOURCES))
-        out_tmp = os.path.join(tmp, LIB_NAME)
+        out_tmp = os.path.join(tmp, lib_name)
         cmd = [nvcc, *ARCH, "-shared", "-cudart", "shared", *objs, "-o", out_tmp,
                "-Xlinker", f"-rpath={libdir}", "-ldl"]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
             raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
-        shutil.move(out_tmp, LIB_PATH + ".tmp")
-        os.replace(LIB_PATH + ".tmp", LIB_PATH)
+        shutil.move(out_tmp, lib_path + ".tmp")
+        os.replace(lib_path + ".tmp", lib_path)
     finally:
         shutil.rmtree(tmp, ignore_errors=True)
-    return LIB_PATH
+    return lib_path
 
 
 if __name__ == "__main__":
-    print(build(force="--force" in sys.argv, verbose="-v" in sys.argv))
+    print(build(force="--force" in sys.argv, verbose="-v" in sys.argv, debug="--debug" in sys.argv))

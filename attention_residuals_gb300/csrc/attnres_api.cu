@@ -746,6 +746,7 @@ static attnres_status bwd_impl(const attnres_params* p, const void* q, const voi
     unsigned char* ws = static_cast<unsigned char*>(workspace);
     a.tickets = reinterpret_cast<unsigned*>(ws);
     a.part = reinterpret_cast<float*>(ws + pl.ws_part_off);
+    a.part_rows = pl.nparts;
     a.gpart = reinterpret_cast<float*>(ws + pl.ws_gpart_off);
     a.dq = static_cast<uint16_t*>(dq);
     a.dq_f32 = dq_f32;
@@ -835,6 +836,14 @@ attnres_status attnres_check_device_error(void) {
 // Multi-query read.
 // ---------------------------------------------------------------------------
 int attnres_jit_kernel_count(void) { return jit_fwd_kernels(); }
+
+int attnres_debug_checks(void) {
+#ifdef ATTNRES_DEBUG
+    return 1;
+#else
+    return 0;
+#endif
+}
 
 attnres_status attnres_multi_plan_info(const attnres_multi_params* p, int64_t out[10]) {
     attnres_status st = check_multi(p);

@@ -591,6 +591,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1) attnres_bwd_cluster_kernel(con
                                         dq_acc[i][kk] = ffma2(k12, x, dq_acc[i][kk]);
                                     }
                                 }
+                                if (ATTNRES_IN_BOUNDS(n < N && s < S && 8 * (v0 + lcol[i]) + 8 <= D, &g_bwdc_error))
                                 st_global_cs_v4(drow + static_cast<long long>(i) * vstep,
                                                 make_uint4(pack_f2(dv[0]), pack_f2(dv[1]), pack_f2(dv[2]), pack_f2(dv[3])));
                             }
@@ -619,6 +620,9 @@ __global__ void __launch_bounds__(kMaxThreads, 1) attnres_bwd_cluster_kernel(con
                     const int j = 8 * (v0 + lcol[i]) + e;
                     const float dqv = (e & 1) ? dq_acc[i][e >> 1].y : dq_acc[i][e >> 1].x;
                     const float dwv = (e & 1) ? dw_acc[i][e >> 1].y : dw_acc[i][e >> 1].x;
+                    if (!ATTNRES_IN_BOUNDS(cid < a.part_rows && j < D && (!((kmask[i] >> e) & 1u) || (j >= ko && j - ko < R)),
+                                           &g_bwdc_error))
+                        continue;
                     if ((kmask[i] >> e) & 1u) my_part[j - ko] = a.scale * dqv;  // dq = scale * sum_s c1_s t_s
                     if (NORM != 0) my_part[R + j] = dwv;
                 }

@@ -589,6 +589,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1) attnres_bwd_kernel(const __gri
                                 for (int kk = 0; kk < 4; ++kk)
                                     dv[kk] = ffma2(make_float2(1.0f, 1.0f), bf2_to_f2(u4_get(gv, kk)), dv[kk]);
                             }
+                            if (ATTNRES_IN_BOUNDS(n < N && s < S && 8 * col[i] + 8 <= D, &g_bwd_error))
                             st_global_cs_v4(drow + static_cast<long long>(i) * vstep,
                                             make_uint4(pack_f2(dv[0]), pack_f2(dv[1]), pack_f2(dv[2]), pack_f2(dv[3])));
                         }
@@ -623,6 +624,10 @@ __global__ void __launch_bounds__(kMaxThreads, 1) attnres_bwd_kernel(const __gri
                 const float dqv = (e & 1) ? dq_acc[i][e >> 1].y : dq_acc[i][e >> 1].x;
                 const float dwv = (e & 1) ? dw_acc[i][e >> 1].y : dw_acc[i][e >> 1].x;
                 // dq = scale * sum_s dz_s k_s = scale * sum_s c1_s t_s
+                if (!ATTNRES_IN_BOUNDS(static_cast<int>(blockIdx.x) < a.part_rows && j < D &&
+                                           (!((kmask[i] >> e) & 1u) || (j >= ko && j - ko < R)),
+                                       &g_bwd_error))
+                    continue;
                 if ((kmask[i] >> e) & 1u) my_part[j - ko] = a.scale * dqv;
                 if (norm_on) my_part[R + j] = dwv;
             }

@@ -285,7 +285,7 @@ __global__ void __launch_bounds__(kMaxThreads, fwd_ctas_per_sm(VPT)) attnres_fwd
                         ddep ^= dv.x;
                         const uint4 pv = add_bf16x8(lds128(row_raw + 16u * w), dv);
                         sts128(row_raw + 16u * w, pv);
-                        st_global_cs_v4(prow + 8 * w, pv);
+                        if (ATTNRES_IN_BOUNDS(n < N && 8 * w + 8 <= a.D, &g_fwd_error)) st_global_cs_v4(prow + 8 * w, pv);
                     }
                     __syncwarp();  // the sums are visible to every lane of this warp
                     if (lane == 0) mbar_arrive_after(dempty_s + 8u * dslot, ddep);
@@ -420,7 +420,7 @@ __global__ void __launch_bounds__(kMaxThreads, fwd_ctas_per_sm(VPT)) attnres_fwd
         const float2 rho2 = make_float2(rho, rho);
 #pragma unroll
         for (int i = 0; i < VPT; ++i) {
-            if (FULL || col[i] >= 0) {
+            if ((FULL || col[i] >= 0) && ATTNRES_IN_BOUNDS(n < N && 8 * col[i] + 8 <= a.D, &g_fwd_error)) {
                 uint32_t yw[4];
 #pragma unroll
                 for (int kk = 0; kk < 4; ++kk)

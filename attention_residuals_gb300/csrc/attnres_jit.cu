@@ -156,8 +156,12 @@ Entry compile(const Key& k) {
         return e;
     A.addNameExpression(prog, expr);
     A.addNameExpression(prog, err_expr);
+#ifdef ATTNRES_DEBUG
+    const char* opts[] = {"-arch=sm_103a", "-std=c++17", "-lineinfo", "-default-device", "-DATTNRES_DEBUG"};
+#else
     const char* opts[] = {"-arch=sm_103a", "-std=c++17", "-lineinfo", "-default-device"};
-    bool good = A.compileProgram(prog, 4, opts) == NVRTC_SUCCESS;
+#endif
+    bool good = A.compileProgram(prog, static_cast<int>(sizeof opts / sizeof opts[0]), opts) == NVRTC_SUCCESS;
     std::string fn_name, err_name;
     std::vector<char> cubin;
     if (good) {

@@ -610,6 +610,7 @@ __global__ void __launch_bounds__(kMultiBwdThreads, 1) attnres_multi_bwd_kernel(
                                     }
                                 }
                             }
+                            if (ATTNRES_IN_BOUNDS(n < a.N && s < a.S && 8 * col[i] + 8 <= a.D, &g_multi_bwd_error))
                             st_global_cs_v4(drow + 8 * col[i], make_uint4(pack_f2(o[0]), pack_f2(o[1]),
                                                                           pack_f2(o[2]), pack_f2(o[3])));
                         }
@@ -690,6 +691,7 @@ __global__ void __launch_bounds__(kMultiBwdThreads, 1) attnres_multi_bwd_kernel(
                                 for (int kk = 0; kk < 4; ++kk)
                                     o[kk] = ffma2(cs2, key_part(bf2_to_f2(u4_get(xv, kk)), kmask[i], kk), o[kk]);
                             }
+                            if (ATTNRES_IN_BOUNDS(n < a.N && s < a.S && 8 * col[i] + 8 <= a.D, &g_multi_bwd_error))
                             st_global_cs_v4(drow + 8 * col[i], make_uint4(pack_f2(o[0]), pack_f2(o[1]),
                                                                           pack_f2(o[2]), pack_f2(o[3])));
                         }

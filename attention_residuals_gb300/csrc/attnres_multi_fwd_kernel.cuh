@@ -424,7 +424,7 @@ __global__ void __launch_bounds__(kMaxThreads, multi_fwd_ctas_per_sm(VPT))
                     uint16_t* yrow = a.y + static_cast<long long>(m0 + j) * a.y_ms + n * a.y_ns;
 #pragma unroll
                     for (int i = 0; i < VPT; ++i) {
-                        if (col[i] >= 0) {
+                        if (col[i] >= 0 && ATTNRES_IN_BOUNDS(n < a.N && 8 * col[i] + 8 <= a.D, &g_multi_error)) {
                             st_global_cs_v4(yrow + 8 * col[i],
                                             make_uint4(pack_f2(fmul2(acc[j][i][0], il2)), pack_f2(fmul2(acc[j][i][1], il2)),
                                                        pack_f2(fmul2(acc[j][i][2], il2)), pack_f2(fmul2(acc[j][i][3], il2))));

@@ -706,7 +706,8 @@ __global__ void __launch_bounds__(kGenThreads, 1) attnres_multi_grad_kernel(cons
 #pragma unroll
                 for (int p = 0; p < P; ++p) {
                     const float2 o = ffma2(cv2, t[p], ffma2(one, oa[0][p], ffma2(one, oa[1][p], ffma2(one, ob[0][p], ob[1][p]))));
-                    if (own[p]) asm volatile("st.global.cs.b32 [%0], %1;" ::"l"(drow + j0[p]), "r"(pack_f2(o)) : "memory");
+                    if (own[p] && ATTNRES_IN_BOUNDS(n < a.N && s < a.S && j0[p] + 2 <= a.D, &g_multi_gen_error))
+                        asm volatile("st.global.cs.b32 [%0], %1;" ::"l"(drow + j0[p]), "r"(pack_f2(o)) : "memory");
                 }
             }
             __syncwarp();

@@ -32,7 +32,19 @@ enum WaitSite : unsigned {
     kSiteDrain = 6,
     kSiteBadId = 7,  // a selected-query id outside [0, E)
     kSiteBwdExchange = 8,  // a cluster peer's partial sums did not arrive
+    kSiteBounds = 9,       // debug build: a store's indices fell outside the call's sizes
 };
+
+// Debug build (-DATTNRES_DEBUG, a stand-in for a memory checker): a global
+// store whose row, source or column index falls outside the call's sizes is
+// recorded (site kSiteBounds, read by attnres_check_device_error) and skipped
+// instead of made.  The release build evaluates nothing.
+#ifdef ATTNRES_DEBUG
+#define ATTNRES_IN_BOUNDS(cond, errp) \
+    ((cond) ? true : (atomicCAS((errp), 0u, static_cast<unsigned>(::attnres::kSiteBounds)), false))
+#else
+#define ATTNRES_IN_BOUNDS(cond, errp) true
+#endif
 
 // Launch plan: one persistent CTA per SM.  `ncw` consumer warps each own
 // `vpt` 16-byte column vectors of every row.  Source rows stream through a
@@ -169,6 +181,7 @@ struct BwdArgs {
     const float* o_rstd;
     const float* o_pre;  // optional FP32 [N, D]; NULL = recompute o from the sources
     float* part;        // [grid][R + Dw] per-CTA partial sums (Dw = out_norm ? D : 0)
+    int part_rows;      // rows the workspace holds at part (the plan's partial rows)
     float* gpart;       // [ngroups][R + Dw] group sums (in-kernel reduction)
     unsigned* tickets;  // [ngroups + 1] zeroed before launch (in-kernel reduction)
     uint16_t* dq;

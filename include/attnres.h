@@ -280,7 +280,9 @@ attnres_status attnres_step_host(const attnres_params* p, const void* q, const v
  * of time makes the kernel record a nonzero code here and finish without
  * further waiting (its outputs are then garbage); so does a selected-query
  * id outside [0, E) (that query then reads as zero and adds nothing to the
- * bank gradient).  This call synchronises the device, returns
+ * bank gradient), and, in a library built with -DATTNRES_DEBUG, a global
+ * store of an output whose indices fall outside the call's sizes (skipped,
+ * never made).  This call synchronises the device, returns
  * ATTNRES_ERR_DEVICE and clears the record if one was set, ATTNRES_OK
  * otherwise.
  */
@@ -430,7 +432,10 @@ attnres_status attnres_selected_fwd(const attnres_multi_params* p, const void* b
                                     const int64_t* ids, void* y, float* alpha, float* rstd,
                                     float* logit, void* stream);
 
-/* Bytes of workspace attnres_selected_bwd needs (grid * E * R * 4; 0 when N == 0). */
+/* Bytes of workspace attnres_selected_bwd needs (0 when N == 0): FP32
+ * partial rows of dbank (E * R floats per CTA, or per token group in the
+ * general form) plus, in the general form, the coefficient tables as for
+ * attnres_multi_bwd_workspace_bytes. */
 size_t attnres_selected_bwd_workspace_bytes(const attnres_multi_params* p, int32_t E);
 
 attnres_status attnres_selected_bwd(const attnres_multi_params* p, const void* bank, int32_t E,

@@ -32,6 +32,18 @@ attnres_status attnres_fwd_withhold_for_test(const attnres_params* p, const void
                                              float* o_rstd, int64_t withhold_fill, uint32_t wait_us,
                                              void* stream);
 
+/*
+ * 1 when the library was compiled with -DATTNRES_DEBUG (python -m
+ * attention_residuals_gb300.build --debug writes it beside the release
+ * build as libattnres_gb300_debug.so), else 0.  In that build every kernel
+ * checks each global store of an output (y, o_pre, the block partial sum,
+ * every source gradient row, the single-query FP32 partial rows of dq and
+ * dw_o) against the call's sizes before it is made; a store that would fall
+ * outside them is skipped and recorded for attnres_check_device_error(),
+ * never trapped.
+ */
+int attnres_debug_checks(void);
+
 #ifdef __cplusplus
 }
 #endif
