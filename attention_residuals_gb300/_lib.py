@@ -13,7 +13,7 @@ MAX_S = 128
 MAX_D = 8192
 MAX_M = 16
 NOALLOC_SCRATCH_BYTES = 16 << 20
-DEFAULT_SPLIT_N = 16384
+DEFAULT_SPLIT_N = 1
 
 STATUS = {
     0: "ATTNRES_OK",

@@ -649,10 +649,25 @@ __global__ void __launch_bounds__(kMaxThreads, 1) attnres_bwd_kernel(const __gri
     if (!*ticket_flag) return;
     __threadfence();
     float* gsum = a.gpart + static_cast<size_t>(grp) * W;
-    for (int c = threadIdx.x; c < W; c += nct) {
-        float acc = 0.0f;
-        for (int b = 0; b < g_size; ++b) acc += ldcg_f32(a.part + static_cast<size_t>(g_first + b) * W + c);
-        gsum[c] = acc;
+    // four columns at a time, every load of them in flight before the adds
+    // (which keep the CTA order)
+    for (int c0 = threadIdx.x; c0 < W; c0 += 4 * nct) {
+        float v[4][kGroupTicket];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const int c = c0 + u * nct;
+#pragma unroll
+            for (int b = 0; b < kGroupTicket; ++b)
+                v[u][b] = (c < W && b < g_size) ? ldcg_f32(a.part + static_cast<size_t>(g_first + b) * W + c) : 0.0f;
+        }
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            float acc = 0.0f;
+#pragma unroll
+            for (int b = 0; b < kGroupTicket; ++b)
+                if (b < g_size) acc += v[u][b];
+            if (c0 + u * nct < W) gsum[c0 + u * nct] = acc;
+        }
     }
     __threadfence();
     named_bar_sync(1, nct);
@@ -663,37 +678,72 @@ __global__ void __launch_bounds__(kMaxThreads, 1) attnres_bwd_kernel(const __gri
     named_bar_sync(1, nct);
     if (*ticket_flag != 2) return;
     __threadfence();
-    for (int c = threadIdx.x; c < W; c += nct) {
-        float acc = 0.0f;
-        for (int g = 0; g < a.ngroups; ++g) acc += ldcg_f32(a.gpart + static_cast<size_t>(g) * W + c);
-        const uint16_t h = static_cast<uint16_t>(pack_bf16x2(acc, 0.0f) & 0xffffu);
-        if (c < R) {
-            a.dq[c] = h;
-            if (a.dq_f32) a.dq_f32[c] = acc;
-        } else {
-            a.dw_o[c - R] = h;
-            if (a.dw_o_f32) a.dw_o_f32[c - R] = acc;
+    for (int c0 = threadIdx.x; c0 < W; c0 += 4 * nct) {
+        float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+        for (int g0 = 0; g0 < a.ngroups; g0 += 8) {
+            float v[4][8];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const int c = c0 + u * nct;
+#pragma unroll
+                for (int k = 0; k < 8; ++k)
+                    v[u][k] = (c < W && g0 + k < a.ngroups)
+                                  ? ldcg_f32(a.gpart + static_cast<size_t>(g0 + k) * W + c) : 0.0f;
+            }
+#pragma unroll
+            for (int u = 0; u < 4; ++u)
+#pragma unroll
+                for (int k = 0; k < 8; ++k)
+                    if (g0 + k < a.ngroups) acc[u] += v[u][k];
+        }
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const int c = c0 + u * nct;
+            if (c >= W) continue;
+            const uint16_t h = static_cast<uint16_t>(pack_bf16x2(acc[u], 0.0f) & 0xffffu);
+            if (c < R) {
+                a.dq[c] = h;
+                if (a.dq_f32) a.dq_f32[c] = acc[u];
+            } else {
+                a.dw_o[c - R] = h;
+                if (a.dw_o_f32) a.dw_o_f32[c - R] = acc[u];
+            }
         }
     }
 }
 
-// Finalize for the split-N path: column c of dq/dw_o is the sum of the
-// per-CTA partial rows taken in CTA order.
-__global__ void __launch_bounds__(256) attnres_finalize_kernel(const float* __restrict__ part, int P, int R,
-                                                               int W, uint16_t* dq, float* dq_f32,
-                                                               uint16_t* dw_o, float* dw_o_f32) {
-    const int c = blockIdx.x * blockDim.x + threadIdx.x;
-    if (c >= W) return;
+// Finalize for the split-N path: column c of dq/dw_o is the sum of the P
+// partial rows.  A block takes kFinCols columns; its kFinSlices warps of a
+// column group each add one contiguous range of rows (eight loads in flight
+// per thread), then the ranges' sums are added in range order -- a fixed
+// order, so the result does not depend on timing.
+constexpr int kFinCols = 32, kFinSlices = 8;
+
+__global__ void __launch_bounds__(kFinCols * kFinSlices) attnres_finalize_kernel(
+    const float* __restrict__ part, int P, int R, int W, uint16_t* dq, float* dq_f32, uint16_t* dw_o,
+    float* dw_o_f32) {
+    __shared__ float sums[kFinSlices][kFinCols];
+    const int lane = threadIdx.x % kFinCols, sl = threadIdx.x / kFinCols;
+    const int c = blockIdx.x * kFinCols + lane;
+    const int per = (P + kFinSlices - 1) / kFinSlices;
+    const int b0 = sl * per, b1 = min(P, b0 + per);
     float acc = 0.0f;
-    int b = 0;
-    for (; b + 8 <= P; b += 8) {
-        float v[8];
+    if (c < W) {
+        for (int b = b0; b < b1; b += 8) {
+            float v[8];
 #pragma unroll
-        for (int k = 0; k < 8; ++k) v[k] = __ldcg(part + static_cast<size_t>(b + k) * W + c);
+            for (int k = 0; k < 8; ++k) v[k] = b + k < b1 ? __ldcg(part + static_cast<size_t>(b + k) * W + c) : 0.0f;
 #pragma unroll
-        for (int k = 0; k < 8; ++k) acc += v[k];
+            for (int k = 0; k < 8; ++k)
+                if (b + k < b1) acc += v[k];
+        }
     }
-    for (; b < P; ++b) acc += __ldcg(part + static_cast<size_t>(b) * W + c);
+    sums[sl][lane] = acc;
+    __syncthreads();
+    if (sl != 0 || c >= W) return;
+    acc = sums[0][lane];
+#pragma unroll
+    for (int k = 1; k < kFinSlices; ++k) acc += sums[k][lane];
     const uint16_t h = static_cast<uint16_t>(pack_bf16x2(acc, 0.0f) & 0xffffu);
     if (c < R) {
         dq[c] = h;
@@ -714,8 +764,8 @@ cudaError_t launch_bwd_t(const Plan& plan, const BwdArgs& a, cudaStream_t stream
     err = cudaGetLastError();
     if (err != cudaSuccess || !plan.split) return err;
     const int W = a.R + (a.out_norm ? a.D : 0);
-    attnres_finalize_kernel<<<(W + 255) / 256, 256, 0, stream>>>(a.part, plan.grid, a.R, W, a.dq,
-                                                                 a.dq_f32, a.dw_o, a.dw_o_f32);
+    attnres_finalize_kernel<<<(W + kFinCols - 1) / kFinCols, kFinCols * kFinSlices, 0, stream>>>(
+        a.part, plan.grid, a.R, W, a.dq, a.dq_f32, a.dw_o, a.dw_o_f32);
     return cudaGetLastError();
 }
 

@@ -53,7 +53,8 @@ enum WaitSite : unsigned {
 // and releases are per chunk, not per row.  The backward also has a ring of
 // `dy_slots` single-row slots for dy.
 struct Plan {
-    int grid;                // backward CTAs (one per SM)
+    int grid;                // backward CTAs (b_per_sm per SM, or clusters of cl)
+    int b_per_sm;            // backward CTAs that share an SM
     int fgrid;               // forward CTAs (fwd_ctas_per_sm per SM)
     int ncw, vpt;            // forward: consumer warps, 16-byte vectors per thread
     int b_ncw, b_vpt;        // backward

@@ -11,8 +11,8 @@ reduction", Test plan).
 
 The other rows of that table and the pages' other workloads have their own
 lines, each the same contract with its own byte model:
-  `--workload short`   S=8, N=8192, D=2048 (the table's last row; dq and
-                       dw_o reduced inside the backward launch, N < 16384)
+  `--workload short`   S=8, N=8192, D=2048 (the table's last row; narrow
+                       rows: two backward CTAs per SM)
   `--workload sliced`  the Block schedule's sliced read: 8 block sums + the
                        partial sum (S=9), N=16384, D=4096, R=1024, 2% zero
                        rows; one step reads with the key in the first R
@@ -372,11 +372,11 @@ class LongRead(SingleRead):
 
 
 class ShortRead(SingleRead):
-    """S=8, N=8192, D=2048: the in-kernel (single-launch) reduction path."""
+    """S=8, N=8192, D=2048: narrow rows, two backward CTAs per SM."""
     key = "short"
     cfg = 2
-    label = "short, in-kernel reduction"
-    roofline_kernel = "attnres_bwd_kernel (in-kernel reduction)"
+    label = "short"
+    roofline_kernel = "attnres_bwd_kernel (+ finalize)"
     traffic_path = os.path.join(ROOT, "profiles", "attnres_short_bwd_traffic.json")
     traffic_key = "cfg2"
 

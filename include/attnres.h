@@ -21,11 +21,14 @@
  * ("Fast Attention Residuals", section "Sliced LR-AttnRes").
  *
  * The backward returns dvalues, dq and dw_o; dq and dw_o are sums over all N
- * tokens.  For N >= split_n_threshold (default 16384, the page's threshold)
- * the per-CTA FP32 partial sums are combined by a separate finalize kernel;
- * shorter inputs finish the reduction inside the backward kernel (the last
- * CTA of each group, then the last group, add the partials).  Both orders are
- * fixed, so dq and dw_o are bitwise reproducible run to run.
+ * tokens.  For N >= split_n_threshold the per-CTA FP32 partial sums are
+ * combined by a separate finalize kernel; shorter inputs finish the
+ * reduction inside the backward kernel (the last CTA of each group, then the
+ * last group, add the partials).  The page splits at 16384 tokens; on this
+ * GPU the finalize kernel measured as fast or faster at every N, so the
+ * default threshold is 1 (always the finalize kernel) and the in-kernel form
+ * is there for callers that set a larger one.  Both orders are fixed, so dq
+ * and dw_o are bitwise reproducible run to run.
  *
  * A token whose S source rows do not fit in one SM's shared memory (e.g. 64
  * rows of 8192 channels, 1 MB) is shared by a thread-block cluster of 2, 4
@@ -70,7 +73,7 @@ extern "C" {
 
 #define ATTNRES_MAX_S 128      /* most sources one call accepts           */
 #define ATTNRES_MAX_D 8192     /* widest row one call accepts             */
-#define ATTNRES_DEFAULT_SPLIT_N 16384
+#define ATTNRES_DEFAULT_SPLIT_N 1
 
 typedef enum {
     ATTNRES_OK = 0,

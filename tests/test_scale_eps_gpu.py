@@ -41,7 +41,7 @@ def _zero_rows(wl, frac=0.03, seed=0):
 
 SINGLE = [
     # S, N, D, R, ko, out_norm, split_n_threshold, save_o_pre
-    (6, 211, 2048, 2048, 0, True, 0, None),        # resident rows, o rebuilt, in-kernel reduction
+    (6, 211, 2048, 2048, 0, True, 10 ** 9, None),  # resident rows, o rebuilt, in-kernel reduction
     (6, 211, 2048, 2048, 0, True, 1, None),        # same shape, finalize kernel
     (6, 173, 2048, 512, 1536, False, 0, None),     # sliced key in the final R channels
     (9, 97, 8192, 8192, 0, True, 0, False),        # streamed rows (three passes: o, dot, write)

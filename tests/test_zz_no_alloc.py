@@ -39,7 +39,7 @@ def call_noalloc(wl, v, q, w, dy, fwd, thr, outs):
     assert rc == 0, _lib.STATUS.get(rc, rc)
 
 
-@pytest.mark.parametrize("thr", [0, 1])  # in-kernel reduction (tickets) and finalize kernel
+@pytest.mark.parametrize("thr", [10 ** 9, 1])  # in-kernel reduction (tickets) and finalize kernel
 def test_noalloc_matches_workspace_path_twice(thr):
     wl = make_random(6, 301, 2048, out_norm=True, seed=77)
     v = wl.values.cuda()
