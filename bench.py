@@ -815,15 +815,22 @@ def run_ours(args):
         pg.barrier()
     torch.cuda.synchronize()
     sampler.mark("begin")
+    nvtx = torch.cuda.nvtx  # named ranges for a profiler's timeline (no cost without one)
+    nvtx.range_push(f"attnres {args.workload}: {K} timed steps")
     e_start.record(stream)
     for k in range(K):
         ev[k][0].record(stream)
+        nvtx.range_push("forward")
         work.fwd(stream)
+        nvtx.range_pop()
         ev[k][1].record(stream)
+        nvtx.range_push("backward + exchange")
         exchange(work.bwd(stream))
+        nvtx.range_pop()
         ev[k][2].record(stream)
     e_end.record(stream)
     torch.cuda.synchronize()
+    nvtx.range_pop()
     sampler.mark("end")
     if pg is not None:
         pg.barrier()
@@ -865,10 +872,12 @@ def run_ours(args):
         if pg is not None:
             pg.barrier()
         torch.cuda.synchronize()
+        nvtx.range_push(f"attnres {args.workload}: {KE} end-to-end steps from host memory")
         s0.record(stream)
         for _ in range(KE):
             e2e_step()
         s1.record(stream)
+        nvtx.range_pop()
         torch.cuda.synchronize()
         e2e_ms = s0.elapsed_time(s1) / KE
         if pg is not None:
