@@ -48,19 +48,20 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 // The cluster backward's switch, ATTNRES_BWD_CLUSTER (read on every call, so
 // tests can run every form): unset = the planner's choice, "0" = never (the
 // one-CTA streaming backward), "<n>" = clusters of n CTAs with resident rows
-// (n = 2, 4 or 8), "s<n>" = clusters of n CTAs streaming the rows.
+// (n = 2, 4 or 8), "s<n>" = clusters of n CTAs streaming the rows, "h<n>" =
+// the same with two (smaller) CTAs per SM.
 struct ClusterChoice {
-    int mode;  // -1 planner, 0 off, 1 resident, 2 streaming
+    int mode;  // -1 planner, 0 off, 1 resident, 2 streaming, 3 streaming with two CTAs per SM
     int cl;
 };
 ClusterChoice cluster_choice() {
     const char* v = std::getenv("ATTNRES_BWD_CLUSTER");
     if (!v || !v[0]) return {-1, 0};
     if (v[0] == '0' && v[1] == '\0') return {0, 0};
-    const bool strm = v[0] == 's';
-    const int n = std::atoi(strm ? v + 1 : v);
+    const bool strm = v[0] == 's', half = v[0] == 'h';
+    const int n = std::atoi(strm || half ? v + 1 : v);
     if (n != 2 && n != 4 && n != 8) return {-1, 0};
-    return {strm ? 2 : 1, n};
+    return {half ? 3 : (strm ? 2 : 1), n};
 }
 bool aligned4(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
 
@@ -217,25 +218,34 @@ attnres_status make_plan(const attnres_params* p, Plan* plan, bool fused = false
     const long long token_bytes = static_cast<long long>(S) * p->D * 2;
     const bool reuse_overflows = (p->N < pl.grid ? p->N : pl.grid) * token_bytes > dev.l2_bytes / 2;
     if (!pl.resident && !addlast && p->N > 0 && cc.mode != 0 && (cc.mode > 0 || reuse_overflows)) {
-        auto try_cluster = [&](int cl, bool resident, Plan* out) -> bool {
+        auto try_cluster = [&](int cl, bool resident, int per_sm, Plan* out) -> bool {
             if (p->D % (8 * cl) != 0) return false;
             Plan c = pl;
             c.cl = cl;
             c.slice = p->D / cl;
             const int ncv = c.slice / 8;
             if (ncv > 512) return false;
-            c.b_vpt = ncv <= 256 ? 1 : 2;
+            if (per_sm == 1) {
+                c.b_vpt = ncv <= 256 ? 1 : 2;
+            } else {
+                // at most four consumer warps of two vectors: 160 threads at
+                // ~166 registers, two CTAs in one SM's register file
+                if (ncv > 256) return false;
+                c.b_vpt = ncv <= 128 ? 1 : 2;
+            }
             c.b_ncw = (ncv + 32 * c.b_vpt - 1) / (32 * c.b_vpt);
+            c.b_per_sm = per_sm;
             c.b_slot_bytes = static_cast<int>(align_up(static_cast<uint32_t>(c.slice) * 2u, 128u));
             c.dy_slots = c.b_slot_bytes > 8192 ? 2 : 4;
+            const long long budget = per_sm == 1 ? optin : optin / 2 - 1024;
             const long long csb = c.b_slot_bytes;
             const long long cfixed = make_cluster_layout(0, 1, c.b_slot_bytes, c.dy_slots, c.s_pad, cl).total + 64;
-            const long long cavail = optin - cfixed;
+            const long long cavail = budget - cfixed;
             auto chunks_for = [&](int rows) {
                 int k = 0;
                 while (k < kMaxChunks &&
                        make_cluster_layout(k + 1, rows, c.b_slot_bytes, c.dy_slots, c.s_pad, cl).total <=
-                           static_cast<uint32_t>(optin))
+                           static_cast<uint32_t>(budget))
                     ++k;
                 return k;
             };
@@ -248,9 +258,12 @@ attnres_status make_plan(const attnres_params* p, Plan* plan, bool fused = false
                 const int per_token = (S + c.b_rows - 1) / c.b_rows;
                 if (c.b_chunks < (per_token == 1 ? 2 : per_token + (per_token + 1) / 2)) return false;
             } else {
-                // at least four chunks in flight, at most 16 rows each
+                // at least four chunks in flight, at most 16 rows each, a
+                // multiple of four rows when possible (the dot pass reduces
+                // four rows at a time)
                 long long g = cavail / (4 * csb);
                 if (g > 16) g = 16;
+                if (g >= 4) g &= ~3LL;
                 if (g < 1) g = 1;
                 c.b_rows = static_cast<int>(g);
                 c.b_chunks = chunks_for(c.b_rows);
@@ -263,7 +276,7 @@ attnres_status make_plan(const attnres_params* p, Plan* plan, bool fused = false
             if (active < 1) return false;
             long long ncl = active;
             if (p->N < ncl) ncl = p->N;
-            if (!resident && cc.mode != 2 && cl < kClusterMax && ncl * token_bytes > dev.l2_bytes / 4 * 3)
+            if (!resident && cc.mode < 2 && cl < kClusterMax && ncl * token_bytes > dev.l2_bytes / 4 * 3)
                 return false;  // a larger cluster shortens the reuse distance further
             c.nparts = static_cast<int>(ncl);
             c.grid = c.nparts * cl;
@@ -273,9 +286,9 @@ attnres_status make_plan(const attnres_params* p, Plan* plan, bool fused = false
         Plan c;
         bool found = false;
         if (cc.mode > 0) {
-            found = try_cluster(cc.cl, cc.mode == 1, &c);
+            found = try_cluster(cc.cl, cc.mode == 1, cc.mode == 3 ? 2 : 1, &c);
         } else {
-            for (int cl = 2; cl <= kClusterMax && !found; cl *= 2) found = try_cluster(cl, false, &c);
+            for (int cl = 2; cl <= kClusterMax && !found; cl *= 2) found = try_cluster(cl, false, 1, &c);
         }
         if (found) pl = c;
     }

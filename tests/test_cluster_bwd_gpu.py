@@ -8,8 +8,9 @@ Checked against the FP64 oracle: both output-norm modes, R == D and sliced
 keys at both placements, S below and above a warp's 32 lanes, every cluster
 size, token counts below the number of clusters, bitwise run-to-run
 determinism, and agreement with the one-CTA streaming backward that
-ATTNRES_BWD_CLUSTER=0 selects for the same shapes.  ATTNRES_BWD_CLUSTER selects each form: "<n>" resident
-slices on clusters of n, "s<n>" streamed slices, "0" no cluster.
+ATTNRES_BWD_CLUSTER=0 selects for the same shapes.  ATTNRES_BWD_CLUSTER
+selects each form: "<n>" resident slices on clusters of n, "s<n>" streamed
+slices, "h<n>" streamed slices with two CTAs per SM, "0" no cluster.
 """
 import os
 
@@ -38,6 +39,9 @@ CASES = [
     (40, 61, 6144, 1536, 0, True, "s8", 8, 0),       # three vectors' worth of warps per slice
     (24, 70, 8192, 2048, 6144, False, "s2", 2, 0),
     (33, 300, 4096, 1000, 3, False, "s4", 4, 0),
+    (64, 45, 8192, 8192, 0, True, "h4", 4, 0),       # streamed slices, two CTAs per SM
+    (40, 61, 6144, 1536, 0, False, "h8", 8, 0),
+    (33, 300, 4096, 1000, 3, True, "h4", 4, 0),
     (9, 97, 8192, 8192, 0, True, None, 1, 0),        # the planner's own choice: short tokens stream on one CTA,
     (64, 160, 8192, 8192, 0, True, None, 2, 0),      # 1 MB tokens on clusters of two
 ]
