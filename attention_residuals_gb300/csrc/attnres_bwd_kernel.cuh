@@ -152,6 +152,9 @@ __global__ void __launch_bounds__(kMaxThreads, 1) attnres_bwd_kernel(const __gri
                 tphase ^= 1u;
             }
             if (lane == 0) {
+                // the caller's FP32 o of this token: into L2 while the consumers
+                // finish the previous token, so their loads of it hit
+                if (o_saved) prefetch_l2_bulk(a.o_pre + n * D, row_bytes * 2u);
                 if (mbar_wait(dyempty + dk, dphase ^ 1u, abort_flag, &g_bwd_error, kSiteBwdProducer)) {
                     mbar_arrive_expect_tx(dyfull + dk, row_bytes);
                     tma_load_1d(dyring + dk * sb, a.dy + n * D, row_bytes, dyfull + dk, pol);

@@ -230,6 +230,12 @@ __device__ __forceinline__ uint4 ld_global_nc_v4(const void* p) {
 }
 
 // Streaming 16-byte global store (evict-first in L2).
+// Bring `bytes` (a multiple of 16) at a 16-byte aligned global address into
+// L2 ahead of its use (no shared memory, no completion to wait for).
+__device__ __forceinline__ void prefetch_l2_bulk(const void* p, uint32_t bytes) {
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
+}
+
 __device__ __forceinline__ void st_global_cs_v4(void* p, const uint4& v) {
     asm volatile("st.global.cs.v4.u32 [%0], {%1,%2,%3,%4};" ::"l"(p), "r"(v.x), "r"(v.y),
                  "r"(v.z), "r"(v.w)
