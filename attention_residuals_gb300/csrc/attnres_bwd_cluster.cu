@@ -267,6 +267,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1) attnres_bwd_cluster_kernel(con
         const uint32_t red_s = sbase + L.red;
         const uint32_t xbar_s = sbase + XL.xbar;
         const uint32_t xbuf_s = sbase + XL.xbuf;
+        const uint32_t ctab_s = sbase + XL.ctab + static_cast<uint32_t>(warp * s_pad) * 16u;  // this warp's table
         const int red_rows = L.red_rows;
         const int nq = (ncw + 3) >> 2;
         const long long dld_b = a.dsrc_ld * 2;
@@ -502,8 +503,8 @@ __global__ void __launch_bounds__(kMaxThreads, 1) attnres_bwd_cluster_kernel(con
             named_bar_sync(1, nct);
 
             // ---- the cluster's da_s, then the per-source coefficients (every
-            // warp computes them identically; lane l holds sources l, l+32, ...)
-            float cal[NJ], ck1[NJ], ck2[NJ];
+            // warp computes them identically; lane l holds sources l, l+32, ...,
+            // and writes them to the warp's own table for the write pass)
             {
                 const int rb = rbuf;
                 const float* xb = exchange(S, [&](int s) { return red_sum(rb, s); });
@@ -523,15 +524,15 @@ __global__ void __launch_bounds__(kMaxThreads, 1) attnres_bwd_cluster_kernel(con
 #pragma unroll
                 for (int j = 0; j < NJ; ++j) {
                     const int s = lane + 32 * j;
-                    cal[j] = ck1[j] = ck2[j] = 0.0f;
                     if (s < S) {
                         const float al = tk[s];
                         const float r = tk[s_pad + s];
                         const float z = tk[2 * s_pad + s];
                         const float dz = al * (dav[j] - delta);
-                        cal[j] = al;
-                        ck1[j] = r * dz;  // qs carries `scale`
-                        ck2[j] = -(r * r) * dz * z * inv_r;
+                        const float k1 = r * dz;  // qs carries `scale`
+                        const float k2 = -(r * r) * dz * z * inv_r;
+                        sts128(ctab_s + 16u * static_cast<uint32_t>(s),
+                               make_uint4(__float_as_uint(al), __float_as_uint(k1), __float_as_uint(k2), 0u));
                     }
                 }
                 __syncwarp();
@@ -559,19 +560,10 @@ __global__ void __launch_bounds__(kMaxThreads, 1) attnres_bwd_cluster_kernel(con
 #pragma unroll 2
                     for (int r = 0; r < gs; ++r) {
                         const int s = g0 + r;
-                        float al, k1, k2;
-                        if constexpr (NJ == 1) {
-                            al = __shfl_sync(0xffffffffu, cal[0], s);
-                            k1 = __shfl_sync(0xffffffffu, ck1[0], s);
-                            k2 = __shfl_sync(0xffffffffu, ck2[0], s);
-                        } else {
-                            static_assert(NJ == 4, "one or four groups of 32 sources");
-                            const int j = s >> 5;
-                            al = __shfl_sync(0xffffffffu, j == 0 ? cal[0] : j == 1 ? cal[1] : j == 2 ? cal[2] : cal[3], s & 31);
-                            k1 = __shfl_sync(0xffffffffu, j == 0 ? ck1[0] : j == 1 ? ck1[1] : j == 2 ? ck1[2] : ck1[3], s & 31);
-                            k2 = __shfl_sync(0xffffffffu, j == 0 ? ck2[0] : j == 1 ? ck2[1] : j == 2 ? ck2[2] : ck2[3], s & 31);
-                        }
-                        const float2 al2 = make_float2(al, al), k12 = make_float2(k1, k1), k22 = make_float2(k2, k2);
+                        // one broadcast load of the source's three coefficients
+                        const float4 cf = lds128f(ctab_s + 16u * static_cast<uint32_t>(s));
+                        const float2 al2 = make_float2(cf.x, cf.x), k12 = make_float2(cf.y, cf.y),
+                                     k22 = make_float2(cf.z, cf.z);
                         char* drow = dstride ? dnext : static_cast<char*>(a.dsrc[s]) + row_off;
                         dnext += dstride;
 #pragma unroll

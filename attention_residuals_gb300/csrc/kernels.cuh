@@ -197,11 +197,12 @@ struct BwdArgs {
 
 // Backward over a thread-block cluster: the backward layout of one CTA's
 // column slice plus the exchange area, [2 buffers][cl ranks][s_pad] floats
-// that peers write their per-token partial sums into, and two mbarriers
-// (one per buffer) that count the peers' arrivals.
+// that peers write their per-token partial sums into, two mbarriers (one per
+// buffer) that count the peers' arrivals, and each consumer warp's table of
+// the token's per-source coefficients, [warps][s_pad] x {alpha, k1, k2, 0}.
 struct ClusterLayout {
     SmemLayout base;
-    uint32_t xbar, xbuf, total;
+    uint32_t xbar, xbuf, ctab, total;
 };
 
 constexpr int kClusterMax = 8;          // portable cluster size
@@ -216,6 +217,9 @@ __host__ __device__ inline ClusterLayout make_cluster_layout(int chunks, int row
     off += 2u * 8u;
     L.xbuf = off;
     off += 2u * static_cast<uint32_t>(cl) * static_cast<uint32_t>(s_pad) * 4u;
+    off = align_up(off, 16);
+    L.ctab = off;
+    off += static_cast<uint32_t>(kMaxConsumerWarps) * static_cast<uint32_t>(s_pad) * 16u;
     L.total = align_up(off, 128);
     return L;
 }
