@@ -455,44 +455,84 @@ __global__ void __launch_bounds__(kMaxThreads, 1) attnres_bwd_cluster_kernel(con
                     for (int kk = 0; kk < 4; ++kk) dout[i][kk] = bf2_to_f2(u4_get(dyv[i], kk));
             }
 
-            // ---- dot pass: this slice's part of da_s = <do, v_s>, four rows at a time
+            // ---- dot pass: this slice's part of da_s = <do, v_s>
             {
                 int k = res ? tk_ck : ck;
                 uint32_t ph = res ? tk_phase : cphase;
                 uint32_t base = res ? tk_base : cbase;
-                for (int g0 = 0; g0 < S; g0 += G) {
-                    const int gs = min(G, S - g0);
-                    mbar_wait_s(full_s + 8u * k, ph, abort_flag, &g_bwdc_error, kSiteBwdConsumer);
-                    uint32_t dep = 0;
-                    for (int c0 = 0; c0 < gs; c0 += 4) {
-                        float part[4];
+                // one quad of rows: its four partial dots into p[0..3]
+                auto quad = [&](uint32_t rowa0, int nrow, float* p, uint32_t& dep) {
 #pragma unroll
-                        for (int r = 0; r < 4; ++r) {
-                            float2 d2 = make_float2(0.0f, 0.0f);
-                            if (c0 + r < gs) {
-                                const uint32_t rowa = base + static_cast<uint32_t>(c0 + r) * sb;
+                    for (int r = 0; r < 4; ++r) {
+                        float2 d2 = make_float2(0.0f, 0.0f);
+                        if (r < nrow) {
+                            const uint32_t rowa = rowa0 + static_cast<uint32_t>(r) * sb;
 #pragma unroll
-                                for (int i = 0; i < VPT; ++i) {
-                                    if (lcol[i] >= 0) {
-                                        const uint4 xv = lds128(rowa + i * vstep);
-                                        dep ^= xv.x;
+                            for (int i = 0; i < VPT; ++i) {
+                                if (lcol[i] >= 0) {
+                                    const uint4 xv = lds128(rowa + i * vstep);
+                                    dep ^= xv.x;
 #pragma unroll
-                                        for (int kk = 0; kk < 4; ++kk)
-                                            d2 = ffma2(dout[i][kk], bf2_to_f2(u4_get(xv, kk)), d2);
-                                    }
+                                    for (int kk = 0; kk < 4; ++kk)
+                                        d2 = ffma2(dout[i][kk], bf2_to_f2(u4_get(xv, kk)), d2);
                                 }
                             }
-                            part[r] = d2.x + d2.y;
                         }
-                        warp_reduce_scatter<4>(part, lane);
-                        if ((lane & 7) == 0 && c0 + (lane >> 3) < gs)
-                            red[(rbuf * red_rows + g0 + c0 + (lane >> 3)) * kRedPitch + warp] = part[0];
+                        p[r] = d2.x + d2.y;
                     }
-                    if (!res) {
-                        __syncwarp();
-                        if (lane == 0) mbar_arrive_after(empty_s + 8u * k, dep);
+                };
+                if (G % 4 == 0) {
+                    // Streamed chunks of whole quads: two quads (eight rows,
+                    // across chunk boundaries) per warp reduce-scatter, which
+                    // halves the shuffle latency per row; each chunk is released
+                    // as soon as its rows are read.
+                    int crow = 0;  // rows of the current chunk already read
+                    uint32_t dep = 0;
+                    for (int b0 = 0; b0 < S; b0 += 8) {
+                        float part[8];
+#pragma unroll
+                        for (int h = 0; h < 2; ++h) {
+                            const int q0 = b0 + 4 * h;
+                            if (q0 < S) {
+                                if (crow == 0) mbar_wait_s(full_s + 8u * k, ph, abort_flag, &g_bwdc_error, kSiteBwdConsumer);
+                                quad(base + static_cast<uint32_t>(crow) * sb, S - q0, part + 4 * h, dep);
+                                crow += 4;
+                                if (crow == G || q0 + 4 >= S) {
+                                    if (!res) {
+                                        __syncwarp();
+                                        if (lane == 0) mbar_arrive_after(empty_s + 8u * k, dep);
+                                    }
+                                    dep = 0;
+                                    crow = 0;
+                                    next_chunk(k, ph, base);
+                                }
+                            } else {
+#pragma unroll
+                                for (int r = 0; r < 4; ++r) part[4 * h + r] = 0.0f;
+                            }
+                        }
+                        warp_reduce_scatter<8>(part, lane);
+                        if ((lane & 3) == 0 && b0 + (lane >> 2) < S)
+                            red[(rbuf * red_rows + b0 + (lane >> 2)) * kRedPitch + warp] = part[0];
                     }
-                    next_chunk(k, ph, base);
+                } else {
+                    for (int g0 = 0; g0 < S; g0 += G) {
+                        const int gs = min(G, S - g0);
+                        mbar_wait_s(full_s + 8u * k, ph, abort_flag, &g_bwdc_error, kSiteBwdConsumer);
+                        uint32_t dep = 0;
+                        for (int c0 = 0; c0 < gs; c0 += 4) {
+                            float part[4];
+                            quad(base + static_cast<uint32_t>(c0) * sb, gs - c0, part, dep);
+                            warp_reduce_scatter<4>(part, lane);
+                            if ((lane & 7) == 0 && c0 + (lane >> 3) < gs)
+                                red[(rbuf * red_rows + g0 + c0 + (lane >> 3)) * kRedPitch + warp] = part[0];
+                        }
+                        if (!res) {
+                            __syncwarp();
+                            if (lane == 0) mbar_arrive_after(empty_s + 8u * k, dep);
+                        }
+                        next_chunk(k, ph, base);
+                    }
                 }
                 if (!res) {
                     ck = k;
