@@ -586,6 +586,9 @@ __global__ void __launch_bounds__(kMaxThreads, 1) attnres_bwd_cluster_kernel(con
 
             // ---- write pass: dv_s slices and dq contributions; releases the chunks
             {
+                // the gradient rows are not read again here: first out of L2,
+                // so the rows this pass re-reads stay
+                const uint64_t st_pol = policy_evict_first();
                 int k = res ? tk_ck : ck;
                 uint32_t ph = res ? tk_phase : cphase;
                 uint32_t base = res ? tk_base : cbase;
@@ -627,8 +630,9 @@ __global__ void __launch_bounds__(kMaxThreads, 1) attnres_bwd_cluster_kernel(con
                                     }
                                 }
                                 if (ATTNRES_IN_BOUNDS(n < N && s < S && 8 * (v0 + lcol[i]) + 8 <= D, &g_bwdc_error))
-                                st_global_cs_v4(drow + static_cast<long long>(i) * vstep,
-                                                make_uint4(pack_f2(dv[0]), pack_f2(dv[1]), pack_f2(dv[2]), pack_f2(dv[3])));
+                                st_global_v4_policy(drow + static_cast<long long>(i) * vstep,
+                                                    make_uint4(pack_f2(dv[0]), pack_f2(dv[1]), pack_f2(dv[2]), pack_f2(dv[3])),
+                                                    st_pol);
                             }
                         }
                         rowa += sb;
