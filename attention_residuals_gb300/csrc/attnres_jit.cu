@@ -23,7 +23,9 @@
 #include <cstdio>
 #include <cstdlib>
 #include <cstring>
+#include <atomic>
 #include <map>
+#include <memory>
 #include <mutex>
 #include <string>
 #include <tuple>
@@ -111,11 +113,30 @@ struct Entry {
     CUmodule mod = nullptr;
     CUfunction fn = nullptr;
     CUdeviceptr err = 0;  // the module's wait-failure word
-    int smem = 0;         // dynamic shared memory the function is set up for
 };
 
-std::mutex g_mu;
-std::map<Key, Entry> g_cache;
+// A launch shape checked against the device: `block` threads with `smem`
+// bytes of dynamic shared memory, of which at least `ctas` CTAs fit on one SM
+// (ok) or do not (rejected).
+struct Fit {
+    int block, smem, ctas;
+    bool ok;
+};
+
+// One key's slot: compiled once (outside the cache lock, so launches of
+// kernels already compiled never wait for a compile), then the launch shapes
+// checked so far.
+struct Slot {
+    std::once_flag once;
+    std::atomic<bool> compiled{false};
+    Entry e;
+    std::mutex mu;        // guards fits and smem_set
+    std::vector<Fit> fits;
+    int smem_set = 0;     // dynamic shared memory the function is set up for
+};
+
+std::mutex g_mu;  // guards the map only
+std::map<Key, std::shared_ptr<Slot>> g_cache;
 
 bool jit_enabled() {
     const char* e = std::getenv("ATTNRES_JIT");
@@ -195,34 +216,61 @@ Entry compile(const Key& k) {
 // fewer is not used.
 cudaError_t launch_key(const Key& k, unsigned grid, unsigned block, int smem, int ctas_per_sm, const void* args,
                        cudaStream_t stream) {
-    Entry* e = nullptr;
+    std::shared_ptr<Slot> slot;
     {
         std::lock_guard<std::mutex> lock(g_mu);
-        auto it = g_cache.find(k);
-        if (it == g_cache.end()) {
-            // Compiling and loading a module are not stream work: during a
-            // CUDA-graph capture they could invalidate it, so a shape first
-            // seen there runs the precompiled kernel (and compiles later).
-            cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
-            if (cudaStreamIsCapturing(stream, &cap) != cudaSuccess || cap != cudaStreamCaptureStatusNone)
-                return cudaErrorNotSupported;
-            it = g_cache.emplace(k, compile(k)).first;
+        auto& p = g_cache[k];
+        if (!p) p = std::make_shared<Slot>();
+        slot = p;
+    }
+    if (!slot->compiled.load(std::memory_order_acquire)) {
+        // Compiling and loading a module are not stream work: during a
+        // CUDA-graph capture they could invalidate it, so a shape first seen
+        // there runs the precompiled kernel (and compiles later).
+        cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+        if (cudaStreamIsCapturing(stream, &cap) != cudaSuccess || cap != cudaStreamCaptureStatusNone)
+            return cudaErrorNotSupported;
+        std::call_once(slot->once, [&] {
+            slot->e = compile(k);
+            slot->compiled.store(true, std::memory_order_release);
+        });
+    }
+    const Entry& e = slot->e;
+    if (!e.ok) return cudaErrorNotSupported;
+    {
+        // The launch shape must fit as many CTAs per SM as the plan counted
+        // on.  A shape no larger (block, shared memory) and asking no more
+        // CTAs than one already found to fit, fits; one no smaller than a
+        // rejected shape is rejected; anything else is checked now.
+        // Rejections are per shape: other launches of the key still use it.
+        std::lock_guard<std::mutex> lock(slot->mu);
+        int verdict = 0;  // 1 fits, -1 does not, 0 unknown
+        for (const Fit& f : slot->fits) {
+            if (f.ok && static_cast<int>(block) <= f.block && smem <= f.smem && ctas_per_sm <= f.ctas) verdict = 1;
+            if (!f.ok && static_cast<int>(block) >= f.block && smem >= f.smem && ctas_per_sm >= f.ctas) verdict = -1;
+            if (verdict) break;
         }
-        e = &it->second;
-        if (!e->ok) return cudaErrorNotSupported;
-        if (e->smem < smem) {
-            int fit = 0;
-            if (api().funcSetAttribute(e->fn, CU_FUNC_ATTRIBUTE_MAX_DYNAMIC_SHARED_SIZE_BYTES, smem) != CUDA_SUCCESS ||
-                api().occupancy(&fit, e->fn, static_cast<int>(block), static_cast<size_t>(smem)) != CUDA_SUCCESS ||
-                fit < ctas_per_sm) {
-                e->ok = false;  // keep the precompiled kernels for this shape
-                return cudaErrorNotSupported;
+        if (verdict < 0) return cudaErrorNotSupported;
+        if (verdict == 0) {
+            if (smem > slot->smem_set) {
+                if (api().funcSetAttribute(e.fn, CU_FUNC_ATTRIBUTE_MAX_DYNAMIC_SHARED_SIZE_BYTES, smem) != CUDA_SUCCESS)
+                    return cudaErrorNotSupported;
+                slot->smem_set = smem;
             }
-            e->smem = smem;
+            int fit = 0;
+            const bool ok = api().occupancy(&fit, e.fn, static_cast<int>(block), static_cast<size_t>(smem)) ==
+                                CUDA_SUCCESS &&
+                            fit >= ctas_per_sm;
+            slot->fits.push_back(Fit{static_cast<int>(block), smem, ok ? fit : ctas_per_sm, ok});
+            if (!ok) return cudaErrorNotSupported;
+        } else if (smem > slot->smem_set) {
+            if (api().funcSetAttribute(e.fn, CU_FUNC_ATTRIBUTE_MAX_DYNAMIC_SHARED_SIZE_BYTES, smem) != CUDA_SUCCESS)
+                return cudaErrorNotSupported;
+            slot->smem_set = smem;
         }
     }
     void* params[] = {const_cast<void*>(args)};
-    const CUresult r = api().launchKernel(e->fn, grid, 1, 1, block, 1, 1, static_cast<unsigned>(smem),
+    const CUresult r = api().launchKernel(e.fn, grid, 1, 1, block, 1, 1, static_cast<unsigned>(smem),
                                           reinterpret_cast<CUstream>(stream), params, nullptr);
     return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorLaunchFailure;
 }
@@ -265,7 +313,8 @@ unsigned take_jit_error(int kind) {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return 0;
     for (auto& kv : g_cache) {
-        Entry& e = kv.second;
+        if (!kv.second || !kv.second->compiled.load(std::memory_order_acquire)) continue;
+        const Entry& e = kv.second->e;
         if (!e.mod || !e.err || std::get<0>(kv.first) != dev || std::get<1>(kv.first) != kind) continue;
         unsigned v = 0;
         if (api().memcpyDtoH(&v, e.err, sizeof v) != CUDA_SUCCESS) return 0xffffffffu;
@@ -281,7 +330,8 @@ unsigned take_jit_error(int kind) {
 int jit_fwd_kernels() {
     std::lock_guard<std::mutex> lock(g_mu);
     int n = 0;
-    for (auto& kv : g_cache) n += kv.second.ok ? 1 : 0;
+    for (auto& kv : g_cache)
+        n += (kv.second && kv.second->compiled.load(std::memory_order_acquire) && kv.second->e.ok) ? 1 : 0;
     return n;
 }
 
