@@ -774,10 +774,19 @@ cudaError_t launch_bwd_t(const Plan& plan, const BwdArgs& a, cudaStream_t stream
 
 template <int VPT, int NORM, int NJ>
 cudaError_t dispatch_cols(const Plan& plan, const BwdArgs& a, cudaStream_t stream) {
-    if (a.dlast_add)  // the general column form
+    const bool full = (a.D / 8) == VPT * 32 * plan.b_ncw;
+    if (a.dlast_add) {
+        // with an added gradient: whole-vector ownership compiled in for rows
+        // of up to 4096 channels (the block schedule's widths), else the
+        // general column form
+        if constexpr (VPT <= 2) {
+            if (full)
+                return a.R == a.D ? launch_bwd_t<VPT, true, true, true, NORM, NJ>(plan, a, stream)
+                                  : launch_bwd_t<VPT, false, true, true, NORM, NJ>(plan, a, stream);
+        }
         return a.R == a.D ? launch_bwd_t<VPT, true, false, true, NORM, NJ>(plan, a, stream)
                           : launch_bwd_t<VPT, false, false, true, NORM, NJ>(plan, a, stream);
-    const bool full = (a.D / 8) == VPT * 32 * plan.b_ncw;
+    }
     if (a.R == a.D)
         return full ? launch_bwd_t<VPT, true, true, false, NORM, NJ>(plan, a, stream)
                     : launch_bwd_t<VPT, true, false, false, NORM, NJ>(plan, a, stream);
