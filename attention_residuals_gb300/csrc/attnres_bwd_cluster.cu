@@ -61,8 +61,9 @@ __device__ __forceinline__ uint64_t policy_keep_in_l2() {
 // KEYALL: R == D (no per-channel key masks).  NORM: 0 no output norm, 1 o
 // rebuilt from the rows, 2 the caller's FP32 o (a.o_pre).  NJ: groups of 32
 // sources whose coefficients each lane holds (1: S <= 32, 4: up to 128
-// sources).  a.resident selects resident or streaming rows at run time.
-template <int VPT, bool KEYALL, int NORM, int NJ>
+// sources).  FULL: every consumer thread owns whole 16-byte vectors of the
+// slice.  a.resident selects resident or streaming rows at run time.
+template <int VPT, bool KEYALL, int NORM, int NJ, bool FULL>
 __global__ void __launch_bounds__(kMaxThreads, 1) attnres_bwd_cluster_kernel(const __grid_constant__ BwdArgs a) {
     extern __shared__ __align__(128) unsigned char smem[];
     const int ncw = a.ncw;
@@ -341,7 +342,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1) attnres_bwd_cluster_kernel(con
                 uint32_t dep = 0;
 #pragma unroll
                 for (int i = 0; i < VPT; ++i) {
-                    dyv[i] = lcol[i] >= 0 ? lds128(dy_lo + dk * sb + i * vstep) : make_uint4(0u, 0u, 0u, 0u);
+                    dyv[i] = (FULL || lcol[i] >= 0) ? lds128(dy_lo + dk * sb + i * vstep) : make_uint4(0u, 0u, 0u, 0u);
                     dep ^= dyv[i].x;
                 }
                 __syncwarp();
@@ -365,7 +366,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1) attnres_bwd_cluster_kernel(con
                     const float* prow = a.o_pre + n * static_cast<long long>(D);
 #pragma unroll
                     for (int i = 0; i < VPT; ++i) {
-                        if (lcol[i] >= 0) {
+                        if (FULL || lcol[i] >= 0) {
                             const int gc = v0 + lcol[i];
                             const uint4 lo = ld_global_nc_v4(prow + 8 * gc);
                             const uint4 hi = ld_global_nc_v4(prow + 8 * gc + 4);
@@ -396,7 +397,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1) attnres_bwd_cluster_kernel(con
                             const float2 al2 = make_float2(al, al);
 #pragma unroll
                             for (int i = 0; i < VPT; ++i) {
-                                if (lcol[i] >= 0) {
+                                if (FULL || lcol[i] >= 0) {
                                     const uint4 xv = lds128(rowa + i * vstep);
                                     dep ^= xv.x;
 #pragma unroll
@@ -469,7 +470,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1) attnres_bwd_cluster_kernel(con
                             const uint32_t rowa = rowa0 + static_cast<uint32_t>(r) * sb;
 #pragma unroll
                             for (int i = 0; i < VPT; ++i) {
-                                if (lcol[i] >= 0) {
+                                if (FULL || lcol[i] >= 0) {
                                     const uint4 xv = lds128(rowa + i * vstep);
                                     dep ^= xv.x;
 #pragma unroll
@@ -611,7 +612,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1) attnres_bwd_cluster_kernel(con
                         dnext += dstride;
 #pragma unroll
                         for (int i = 0; i < VPT; ++i) {
-                            if (lcol[i] >= 0) {
+                            if (FULL || lcol[i] >= 0) {
                                 float2 dv[4];
 #pragma unroll
                                 for (int kk = 0; kk < 4; ++kk) dv[kk] = fmul2(al2, dout[i][kk]);
@@ -653,7 +654,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1) attnres_bwd_cluster_kernel(con
         float* my_part = a.part + static_cast<size_t>(cid) * W;
 #pragma unroll
         for (int i = 0; i < VPT; ++i) {
-            if (lcol[i] >= 0) {
+            if (FULL || lcol[i] >= 0) {
 #pragma unroll
                 for (int e = 0; e < 8; ++e) {
                     const int j = 8 * (v0 + lcol[i]) + e;
@@ -673,7 +674,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1) attnres_bwd_cluster_kernel(con
     cluster_sync_all();
 }
 
-template <int VPT, bool KEYALL, int NORM, int NJ>
+template <int VPT, bool KEYALL, int NORM, int NJ, bool FULL>
 cudaLaunchConfig_t cluster_config(const Plan& plan, int grid, cudaStream_t stream, cudaLaunchAttribute* attr) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(grid));
@@ -689,15 +690,15 @@ cudaLaunchConfig_t cluster_config(const Plan& plan, int grid, cudaStream_t strea
     return cfg;
 }
 
-template <int VPT, bool KEYALL, int NORM, int NJ>
+template <int VPT, bool KEYALL, int NORM, int NJ, bool FULL>
 struct LaunchFn {
     static cudaError_t run(const Plan& plan, const BwdArgs& a, cudaStream_t stream) {
-        auto kern = attnres_bwd_cluster_kernel<VPT, KEYALL, NORM, NJ>;
+        auto kern = attnres_bwd_cluster_kernel<VPT, KEYALL, NORM, NJ, FULL>;
         cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                                static_cast<int>(plan.smem_bwd));
         if (err != cudaSuccess) return err;
         cudaLaunchAttribute attr[1];
-        cudaLaunchConfig_t cfg = cluster_config<VPT, KEYALL, NORM, NJ>(plan, plan.grid, stream, attr);
+        cudaLaunchConfig_t cfg = cluster_config<VPT, KEYALL, NORM, NJ, FULL>(plan, plan.grid, stream, attr);
         err = cudaLaunchKernelEx(&cfg, kern, a);
         if (err != cudaSuccess) return err;
         const int W = a.R + (a.out_norm ? a.D : 0);
@@ -706,17 +707,17 @@ struct LaunchFn {
     static cudaError_t fail() { return cudaErrorInvalidConfiguration; }
 };
 
-template <int VPT, bool KEYALL, int NORM, int NJ>
+template <int VPT, bool KEYALL, int NORM, int NJ, bool FULL>
 struct OccupancyFn {
     static int run(const Plan& plan) {
-        auto kern = attnres_bwd_cluster_kernel<VPT, KEYALL, NORM, NJ>;
+        auto kern = attnres_bwd_cluster_kernel<VPT, KEYALL, NORM, NJ, FULL>;
         if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  static_cast<int>(plan.smem_bwd)) != cudaSuccess) {
             cudaGetLastError();
             return 0;
         }
         cudaLaunchAttribute attr[1];
-        cudaLaunchConfig_t cfg = cluster_config<VPT, KEYALL, NORM, NJ>(plan, plan.cl, nullptr, attr);
+        cudaLaunchConfig_t cfg = cluster_config<VPT, KEYALL, NORM, NJ, FULL>(plan, plan.cl, nullptr, attr);
         int n = 0;
         if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess) {
             cudaGetLastError();
@@ -729,27 +730,32 @@ struct OccupancyFn {
 
 // One instantiation per (vectors per thread, all channels keys, output-norm
 // mode, source groups); `Fn` launches or queries occupancy.
-template <template <int, bool, int, int> class Fn, int VPT, bool KA, int NM, typename... Args>
-auto pick_nj(bool one, Args&&... args) {
-    return one ? Fn<VPT, KA, NM, 1>::run(args...) : Fn<VPT, KA, NM, 4>::run(args...);
+template <template <int, bool, int, int, bool> class Fn, int VPT, bool KA, int NM, typename... Args>
+auto pick_nj(bool one, bool full, Args&&... args) {
+    if (full) return one ? Fn<VPT, KA, NM, 1, true>::run(args...) : Fn<VPT, KA, NM, 4, true>::run(args...);
+    return one ? Fn<VPT, KA, NM, 1, false>::run(args...) : Fn<VPT, KA, NM, 4, false>::run(args...);
 }
 
-template <template <int, bool, int, int> class Fn, int VPT, bool KA, typename... Args>
-auto pick_norm(int norm, bool one, Args&&... args) {
+template <template <int, bool, int, int, bool> class Fn, int VPT, bool KA, typename... Args>
+auto pick_norm(int norm, bool one, bool full, Args&&... args) {
     switch (norm) {
-        case 0: return pick_nj<Fn, VPT, KA, 0>(one, args...);
-        case 1: return pick_nj<Fn, VPT, KA, 1>(one, args...);
-        case 2: return pick_nj<Fn, VPT, KA, 2>(one, args...);
-        default: return Fn<VPT, KA, 0, 1>::fail();
+        case 0: return pick_nj<Fn, VPT, KA, 0>(one, full, args...);
+        case 1: return pick_nj<Fn, VPT, KA, 1>(one, full, args...);
+        case 2: return pick_nj<Fn, VPT, KA, 2>(one, full, args...);
+        default: return Fn<VPT, KA, 0, 1, false>::fail();
     }
 }
 
-template <template <int, bool, int, int> class Fn, typename... Args>
-auto dispatch(int vpt, bool keyall, int norm, int S, Args&&... args) {
+// full: every consumer thread owns whole 16-byte vectors of the slice (no
+// per-vector ownership checks compiled in).
+template <template <int, bool, int, int, bool> class Fn, typename... Args>
+auto dispatch(int vpt, bool keyall, int norm, int S, bool full, Args&&... args) {
     const bool one = S <= 32;
-    if (vpt == 1) return keyall ? pick_norm<Fn, 1, true>(norm, one, args...) : pick_norm<Fn, 1, false>(norm, one, args...);
-    if (vpt == 2) return keyall ? pick_norm<Fn, 2, true>(norm, one, args...) : pick_norm<Fn, 2, false>(norm, one, args...);
-    return Fn<1, true, 0, 1>::fail();
+    if (vpt == 1)
+        return keyall ? pick_norm<Fn, 1, true>(norm, one, full, args...) : pick_norm<Fn, 1, false>(norm, one, full, args...);
+    if (vpt == 2)
+        return keyall ? pick_norm<Fn, 2, true>(norm, one, full, args...) : pick_norm<Fn, 2, false>(norm, one, full, args...);
+    return Fn<1, true, 0, 1, false>::fail();
 }
 
 }  // namespace
@@ -758,29 +764,31 @@ cudaError_t launch_bwd_cluster(const Plan& plan, const BwdArgs& a, cudaStream_t 
     // output norm: o rebuilt from the rows when they are resident (free) or no
     // saved copy was passed; the caller's FP32 o saves a streamed pass otherwise
     const int norm = !a.out_norm ? 0 : ((a.resident || !a.o_pre) ? 1 : 2);
-    return dispatch<LaunchFn>(plan.b_vpt, a.R == a.D, norm, a.S, plan, a, stream);
+    const bool full = plan.slice / 8 == plan.b_vpt * 32 * plan.b_ncw;
+    return dispatch<LaunchFn>(plan.b_vpt, a.R == a.D, norm, a.S, full, plan, a, stream);
 }
 
 int bwd_cluster_max_active(const Plan& plan, bool keyall, bool norm, int S) {
     // cached per device and launch shape (an occupancy query per call would
     // add host time to every backward)
     struct Entry {
-        int dev, vpt, ncw, cl, smem, keyall, norm, one, n;
+        int dev, vpt, ncw, cl, smem, keyall, norm, one, full, n;
     };
     static std::mutex mu;
     static Entry cache[64];
     static int used = 0;
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return 0;
-    const Entry key{dev, plan.b_vpt, plan.b_ncw, plan.cl, static_cast<int>(plan.smem_bwd), keyall, norm, S <= 32, 0};
+    const bool full = plan.slice / 8 == plan.b_vpt * 32 * plan.b_ncw;
+    const Entry key{dev, plan.b_vpt, plan.b_ncw, plan.cl, static_cast<int>(plan.smem_bwd), keyall, norm, S <= 32, full, 0};
     std::lock_guard<std::mutex> lock(mu);
     for (int i = 0; i < used; ++i) {
         const Entry& e = cache[i];
         if (e.dev == key.dev && e.vpt == key.vpt && e.ncw == key.ncw && e.cl == key.cl && e.smem == key.smem &&
-            e.keyall == key.keyall && e.norm == key.norm && e.one == key.one)
+            e.keyall == key.keyall && e.norm == key.norm && e.one == key.one && e.full == key.full)
             return e.n;
     }
-    const int n = dispatch<OccupancyFn>(plan.b_vpt, keyall, norm ? 1 : 0, S, plan);
+    const int n = dispatch<OccupancyFn>(plan.b_vpt, keyall, norm ? 1 : 0, S, full, plan);
     if (used < 64) {
         cache[used] = key;
         cache[used].n = n;
