@@ -716,11 +716,12 @@ __global__ void __launch_bounds__(kMaxThreads, 1) attnres_bwd_kernel(const __gri
 }
 
 // Finalize for the split-N path: column c of dq/dw_o is the sum of the P
-// partial rows.  A block takes kFinCols columns; its kFinSlices warps of a
-// column group each add one contiguous range of rows (eight loads in flight
-// per thread), then the ranges' sums are added in range order -- a fixed
-// order, so the result does not depend on timing.
-constexpr int kFinCols = 32, kFinSlices = 8;
+// partial rows.  A block takes kFinCols columns; its kFinSlices warps each
+// add one contiguous range of rows for them (eight loads in flight per
+// thread: one or two rounds for up to 512 rows), then the ranges' sums are
+// added in range order -- a fixed order, so the result does not depend on
+// timing.
+constexpr int kFinCols = 32, kFinSlices = 32;
 
 __global__ void __launch_bounds__(kFinCols * kFinSlices) attnres_finalize_kernel(
     const float* __restrict__ part, int P, int R, int W, uint16_t* dq, float* dq_f32, uint16_t* dw_o,

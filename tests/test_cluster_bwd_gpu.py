@@ -39,8 +39,8 @@ CASES = [
     (40, 61, 6144, 1536, 0, True, "s8", 8, 0),       # three vectors' worth of warps per slice
     (24, 70, 8192, 2048, 6144, False, "s2", 2, 0),
     (33, 300, 4096, 1000, 3, False, "s4", 4, 0),
-    (20, 77, 2064, 2064, 0, True, "s2", 2, 0),       # a slice of 129 vectors: not every thread owns one
-    (20, 77, 2064, 512, 1552, False, "2", 2, 1),
+    (64, 77, 2064, 2064, 0, True, "s2", 2, 0),       # a slice of 129 vectors: not every thread owns one
+    (24, 77, 4112, 1024, 3088, False, "2", 2, 1),     # 257 vectors of two per thread
     (64, 45, 8192, 8192, 0, True, "h4", 4, 0),       # streamed slices, two CTAs per SM
     (40, 61, 6144, 1536, 0, False, "h8", 8, 0),
     (33, 300, 4096, 1000, 3, True, "h4", 4, 0),
