@@ -9,9 +9,8 @@ namespace attnres {
 
 cudaError_t launch_finalize(const float* part, int P, int R, int W, uint16_t* dq, float* dq_f32,
                             uint16_t* dw_o, float* dw_o_f32, cudaStream_t stream) {
-    attnres_finalize_kernel<<<(W + kFinCols - 1) / kFinCols, kFinCols * kFinSlices, 0, stream>>>(
-        part, P, R, W, dq, dq_f32, dw_o, dw_o_f32);
-    return cudaGetLastError();
+    return launch_pdl(attnres_finalize_kernel, dim3((W + kFinCols - 1) / kFinCols), dim3(kFinCols * kFinSlices), 0,
+                      stream, part, P, R, W, dq, dq_f32, dw_o, dw_o_f32);
 }
 
 unsigned take_bwd_error() {

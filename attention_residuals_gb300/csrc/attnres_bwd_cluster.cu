@@ -121,6 +121,9 @@ __global__ void __launch_bounds__(kMaxThreads, 1) attnres_bwd_cluster_kernel(con
     __syncthreads();
     // every CTA's exchange barriers are initialised before any peer arrives on them
     cluster_sync_all();
+    // set-up above overlaps the previous kernel's tail; global memory only after it
+    pdl_wait();
+    pdl_launch_dependents();
 
     if (warp == ncw) {
         // ------------------------------------------------------ producer
@@ -697,8 +700,12 @@ struct LaunchFn {
         cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                                static_cast<int>(plan.smem_bwd));
         if (err != cudaSuccess) return err;
-        cudaLaunchAttribute attr[1];
+        cudaLaunchAttribute attr[2];
         cudaLaunchConfig_t cfg = cluster_config<VPT, KEYALL, NORM, NJ, FULL>(plan, plan.grid, stream, attr);
+        // may start during the previous kernel's tail (it waits before any global access)
+        attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[1].val.programmaticStreamSerializationAllowed = 1;
+        cfg.numAttrs = 2;
         err = cudaLaunchKernelEx(&cfg, kern, a);
         if (err != cudaSuccess) return err;
         const int W = a.R + (a.out_norm ? a.D : 0);

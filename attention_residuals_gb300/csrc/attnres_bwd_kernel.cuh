@@ -43,6 +43,7 @@
 
 #include "device_utils.cuh"
 #include "kernels.cuh"
+#include "launch_pdl.cuh"
 
 namespace attnres {
 namespace {
@@ -113,6 +114,9 @@ __global__ void __launch_bounds__(kMaxThreads, 1) attnres_bwd_kernel(const __gri
         mbar_fence_init();
     }
     __syncthreads();
+    // set-up above overlaps the previous kernel's tail; global memory only after it
+    pdl_wait();
+    pdl_launch_dependents();
 
     if (warp == ncw) {
         // ------------------------------------------------------ producer
@@ -727,6 +731,7 @@ __global__ void __launch_bounds__(kFinCols * kFinSlices) attnres_finalize_kernel
     const float* __restrict__ part, int P, int R, int W, uint16_t* dq, float* dq_f32, uint16_t* dw_o,
     float* dw_o_f32) {
     __shared__ float sums[kFinSlices][kFinCols];
+    pdl_wait();  // the partial rows are complete and visible
     const int lane = threadIdx.x % kFinCols, sl = threadIdx.x / kFinCols;
     const int c = blockIdx.x * kFinCols + lane;
     const int per = (P + kFinSlices - 1) / kFinSlices;
@@ -764,13 +769,12 @@ cudaError_t launch_bwd_t(const Plan& plan, const BwdArgs& a, cudaStream_t stream
     cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                            static_cast<int>(plan.smem_bwd));
     if (err != cudaSuccess) return err;
-    kern<<<plan.grid, (plan.b_ncw + 1) * 32, plan.smem_bwd, stream>>>(a);
-    err = cudaGetLastError();
+    err = launch_pdl(kern, dim3(plan.grid), dim3((plan.b_ncw + 1) * 32), plan.smem_bwd, stream, a);
     if (err != cudaSuccess || !plan.split) return err;
     const int W = a.R + (a.out_norm ? a.D : 0);
-    attnres_finalize_kernel<<<(W + kFinCols - 1) / kFinCols, kFinCols * kFinSlices, 0, stream>>>(
-        a.part, plan.grid, a.R, W, a.dq, a.dq_f32, a.dw_o, a.dw_o_f32);
-    return cudaGetLastError();
+    return launch_pdl(attnres_finalize_kernel, dim3((W + kFinCols - 1) / kFinCols), dim3(kFinCols * kFinSlices), 0,
+                      stream, static_cast<const float*>(a.part), plan.grid, a.R, W, a.dq, a.dq_f32, a.dw_o,
+                      a.dw_o_f32);
 }
 
 template <int VPT, int NORM, int NJ>

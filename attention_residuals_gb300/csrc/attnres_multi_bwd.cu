@@ -41,6 +41,7 @@
 
 #include "device_utils.cuh"
 #include "kernels.cuh"
+#include "launch_pdl.cuh"
 
 namespace attnres {
 namespace {
@@ -128,6 +129,9 @@ __global__ void __launch_bounds__(kMultiBwdThreads, 1) attnres_multi_bwd_kernel(
     if (dq_in_smem)
         for (int i = threadIdx.x; i < QR * a.nkv * 8; i += blockDim.x) dqsm[i] = 0.0f;
     __syncthreads();
+    // set-up above overlaps the previous kernel's tail; global memory only after it
+    pdl_wait();
+    pdl_launch_dependents();
 
     if (warp == ncw) {
         // ------------------------------------------------------ producer
@@ -811,8 +815,7 @@ cudaError_t launch_t(const MultiPlan& plan, const MultiBwdArgs& a, cudaStream_t 
     cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                            static_cast<int>(plan.smem_bwd));
     if (err != cudaSuccess) return err;
-    kern<<<plan.grid, (plan.b_ncw + 1) * 32, plan.smem_bwd, stream>>>(a);
-    err = cudaGetLastError();
+    err = launch_pdl(kern, dim3(plan.grid), dim3((plan.b_ncw + 1) * 32), plan.smem_bwd, stream, a);
     if (err != cudaSuccess) return err;
     const int W = (a.ids ? a.E : a.M) * a.R;
     return launch_finalize(a.part, plan.grid, W, W, const_cast<uint16_t*>(a.dq), a.dq_f32, nullptr, nullptr,

@@ -100,6 +100,9 @@ __global__ void __launch_bounds__(kMaxThreads, multi_fwd_ctas_per_sm(VPT))
         mbar_fence_init();
     }
     __syncthreads();
+    // the backward may start launching (it waits for this grid before it
+    // touches global memory)
+    pdl_launch_dependents();
 
     if (warp == ncw) {
         // ------------------------------------------------------ producer

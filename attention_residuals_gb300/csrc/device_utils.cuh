@@ -230,6 +230,15 @@ __device__ __forceinline__ uint4 ld_global_nc_v4(const void* p) {
 }
 
 // Streaming 16-byte global store (evict-first in L2).
+// Programmatic dependent launch.  A kernel launched with programmatic stream
+// serialization may start while the kernel before it on the stream is still
+// running; pdl_wait() then blocks until that kernel has finished and its
+// memory is visible (a no-op for an ordinary launch), so it must come before
+// the kernel's first global memory access.  pdl_launch_dependents() lets the
+// next kernel start launching (its CTAs take SMs as this kernel's CTAs leave).
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 // Bring `bytes` (a multiple of 16) at a 16-byte aligned global address into
 // L2 ahead of its use (no shared memory, no completion to wait for).
 __device__ __forceinline__ void prefetch_l2_bulk(const void* p, uint32_t bytes) {
