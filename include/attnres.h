@@ -32,13 +32,16 @@
  *
  * A token whose S source rows do not fit in one SM's shared memory (e.g. 64
  * rows of 8192 channels, 1 MB) is shared by a thread-block cluster of 2, 4
- * or 8 CTAs in the backward, each holding D/size columns of every row, so
- * that each row is still read from HBM once; the CTAs exchange their partial
- * sums of the two full-width reductions through distributed shared memory.
- * Its partial rows (one per cluster) always go through the finalize kernel.
- * Shapes no cluster can hold stream the rows once per pass instead.
- * ATTNRES_BWD_CLUSTER=0 in the environment (read on every call) keeps the
- * streaming backward for every shape.
+ * or 8 CTAs in the backward, each holding D/size columns of every row: the
+ * rows are streamed once per pass, and with size-times fewer tokens in flight
+ * the later passes find them in L2 instead of HBM; the CTAs exchange their
+ * partial sums of the two full-width reductions through distributed shared
+ * memory.  Its partial rows (one per cluster) always go through the finalize
+ * kernel.  ATTNRES_BWD_CLUSTER in the environment (read on every call)
+ * overrides the choice: "0" one CTA per token for every shape, "2"/"4"/"8"
+ * clusters holding their slices resident, "s2"/"s4"/"s8" clusters streaming
+ * them, "h2"/"h4"/"h8" the same with two CTAs per SM; a form the shape cannot
+ * take falls back to the planner's.
  *
  * Conventions for every entry point:
  *  - All tensor pointers are DEVICE pointers of the current CUDA device,
