@@ -41,7 +41,7 @@
  * overrides the choice: "0" one CTA per token for every shape, "2"/"4"/"8"
  * clusters holding their slices resident, "s2"/"s4"/"s8" clusters streaming
  * them, "h2"/"h4"/"h8" the same with two CTAs per SM; a form the shape cannot
- * take falls back to the planner's.
+ * take falls back to one CTA per token.
  *
  * Conventions for every entry point:
  *  - All tensor pointers are DEVICE pointers of the current CUDA device,
