@@ -281,3 +281,18 @@ def test_autograd_matches_explicit_calls():
     assert torch.equal(qq.grad, g["dq"]) and torch.equal(ww.grad, g["dw_o"])
     check_vec_grad(g["dq"], g["dq_f32"], ref["dq"], {}, "autograd", "dq")
     check_vec_grad(g["dw_o"], g["dw_o_f32"], ref["dw_o"], {}, "autograd", "dw_o")
+
+
+@pytest.mark.parametrize("S,N,D,R,norm", [(8, 700, 2048, 2048, False), (10, 613, 2048, 512, True),
+                                          (16, 900, 1024, 1024, False), (12, 500, 1536, 1536, True),
+                                          (6, 400, 520, 136, True)])
+def test_narrow_rows_two_ctas_per_sm(S, N, D, R, norm):
+    # resident rows of at most 2048 channels: two backward CTAs share each SM
+    wl = make_random(S, N, D, R, key_offset=D - R, out_norm=norm, seed=S + D)
+    info = attnres_plan_info(wl.values.cuda(), R, key_offset=D - R, out_norm=norm)
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    assert info["bwd_resident"] == 1 and info["grid"] == min(N, 2 * sms), info
+    assert info["consumer_warps"] % 1000 <= 4, info
+    fwd, bwd, ref = run_both(wl)
+    check_forward(fwd, ref, out_norm=norm, tag="narrow")
+    print(check_backward(bwd, ref, out_norm=norm, tag=f"narrow S{S} D{D}"))
