@@ -57,7 +57,10 @@
  *    captured into a CUDA graph runs a precompiled kernel instead (see
  *    attnres_jit_kernel_count; ATTNRES_JIT=0 turns the run-time path off).
  *  - Calls are asynchronous on `stream` (a cudaStream_t, NULL = legacy
- *    default stream) and never synchronise the host.
+ *    default stream) and never synchronise the host.  Stream order holds:
+ *    the backward kernels are launched with programmatic dependent launch,
+ *    so they may start their set-up during the previous kernel's tail, but
+ *    they touch no global memory before that kernel has finished.
  *  - Arguments are validated before anything is enqueued; on any error
  *    nothing is launched and the status says why.
  *  - bf16 is IEEE bfloat16 stored as uint16_t bit patterns.
