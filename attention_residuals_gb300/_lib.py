@@ -33,6 +33,7 @@ EXPORTED = [
     "attnres_check_device_error",
     "attnres_jit_kernel_count",
     "attnres_debug_checks",
+    "attnres_multi_fwd_tensor_cores",
     "attnres_status_string",
     "attnres_plan_info",
     "attnres_multi_fwd",
@@ -154,11 +155,13 @@ def load(path: str | None = None):
         lib.attnres_jit_kernel_count.argtypes = []
         lib.attnres_debug_checks.restype = ctypes.c_int
         lib.attnres_debug_checks.argtypes = []
+        lib.attnres_multi_fwd_tensor_cores.restype = ctypes.c_int
         lib.attnres_status_string.restype = ctypes.c_char_p
         lib.attnres_status_string.argtypes = [ctypes.c_int]
         lib.attnres_plan_info.restype = ctypes.c_int
         lib.attnres_plan_info.argtypes = [P, ctypes.POINTER(ctypes.c_int64)]
         MP = ctypes.POINTER(AttnresMultiParams)
+        lib.attnres_multi_fwd_tensor_cores.argtypes = [MP, ctypes.c_int32]
         lib.attnres_multi_fwd.restype = ctypes.c_int
         lib.attnres_multi_fwd.argtypes = [MP, vp, vp, fp, fp, fp, vp]
         lib.attnres_multi_bwd_workspace_bytes.restype = sz

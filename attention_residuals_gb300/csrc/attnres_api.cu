@@ -866,15 +866,25 @@ attnres_status attnres_check_device_error(void) {
     const unsigned mf = take_multi_fwd_error();
     const unsigned mb = take_multi_bwd_error();
     const unsigned mg = take_multi_gen_error();
-    if (f == 0xffffffffu || b == 0xffffffffu || mf == 0xffffffffu || mb == 0xffffffffu || mg == 0xffffffffu)
+    const unsigned mm = take_multi_mma_error();
+    if (f == 0xffffffffu || b == 0xffffffffu || mf == 0xffffffffu || mb == 0xffffffffu || mg == 0xffffffffu ||
+        mm == 0xffffffffu)
         return ATTNRES_ERR_CUDA;
-    return (f || b || mf || mb || mg) ? ATTNRES_ERR_DEVICE : ATTNRES_OK;
+    return (f || b || mf || mb || mg || mm) ? ATTNRES_ERR_DEVICE : ATTNRES_OK;
 }
 
 // ---------------------------------------------------------------------------
 // Multi-query read.
 // ---------------------------------------------------------------------------
 int attnres_jit_kernel_count(void) { return jit_fwd_kernels(); }
+
+int attnres_multi_fwd_tensor_cores(const attnres_multi_params* p, int32_t E) {
+    if (check_multi(p) != ATTNRES_OK) return -1;
+    DeviceInfo dev;
+    if (!device_info(&dev)) return -1;
+    MmaPlan mp;
+    return plan_multi_fwd_mma(p, E > 0 ? E : 0, dev.sm_count, dev.smem_optin, &mp) ? 1 : 0;
+}
 
 int attnres_debug_checks(void) {
 #ifdef ATTNRES_DEBUG
@@ -951,6 +961,12 @@ static attnres_status multi_fwd_impl(const attnres_multi_params* p, const void* 
     a.alpha = alpha;
     a.rstd = rstd;
     a.logit = logit;
+    // several queries over tokens that fit in shared memory: the tensor-core form
+    DeviceInfo dev;
+    MmaPlan mp;
+    if (device_info(&dev) && plan_multi_fwd_mma(p, ids ? E : 0, dev.sm_count, dev.smem_optin, &mp))
+        return launch_multi_fwd_mma(mp, a, static_cast<cudaStream_t>(stream)) == cudaSuccess ? ATTNRES_OK
+                                                                                             : ATTNRES_ERR_CUDA;
     return launch_multi_fwd(pl, a, static_cast<cudaStream_t>(stream)) == cudaSuccess ? ATTNRES_OK
                                                                                     : ATTNRES_ERR_CUDA;
 }

@@ -398,6 +398,18 @@ struct MultiFwdArgs {
     float* logit;          // [N][M][S]
 };
 
+// The tensor-core multi-query forward (attnres_multi_fwd_mma.cu): for reads
+// with several queries whose token's rows fit in shared memory at least
+// twice.  plan_multi_fwd_mma is false when the shape does not qualify (then
+// the kernel of attnres_multi_fwd_kernel.cuh runs).
+struct MmaPlan {
+    int grid, slots, pitch, qpitch, qrows;
+    size_t smem;
+};
+bool plan_multi_fwd_mma(const attnres_multi_params* p, int E, int sm_count, long long smem_optin, MmaPlan* out);
+cudaError_t launch_multi_fwd_mma(const MmaPlan& plan, const MultiFwdArgs& a, cudaStream_t stream);
+unsigned take_multi_mma_error();
+
 struct MultiBwdArgs {
     const void* src[ATTNRES_MAX_S];
     void* dsrc[ATTNRES_MAX_S];

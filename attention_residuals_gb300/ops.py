@@ -529,8 +529,11 @@ def attnres_multi_plan_info(values: Sources, M: int, R: int, *, key_offset=None)
     mp = make_multi_params(view, M, R, key_offset=key_offset, eps=EPS_DEFAULT, scale=1.0,
                            token_major=False)
     out = (ctypes.c_int64 * 10)()
-    _lib.check(_lib.load().attnres_multi_plan_info(ctypes.byref(mp), out), "attnres_multi_plan_info")
-    return dict(zip(_MULTI_PLAN_KEYS, list(out)))
+    lib = _lib.load()
+    _lib.check(lib.attnres_multi_plan_info(ctypes.byref(mp), out), "attnres_multi_plan_info")
+    info = dict(zip(_MULTI_PLAN_KEYS, list(out)))
+    info["fwd_tensor_cores"] = int(lib.attnres_multi_fwd_tensor_cores(ctypes.byref(mp), ctypes.c_int32(0)))
+    return info
 
 
 def attnres_multi_bwd_workspace_bytes(params: _lib.AttnresMultiParams) -> int:

@@ -33,6 +33,14 @@ attnres_status attnres_fwd_withhold_for_test(const attnres_params* p, const void
                                              void* stream);
 
 /*
+ * Which form a multi-query (E = 0) or selected-query (E = bank rows) forward
+ * of these params runs: 1 the tensor-core form, 0 the other, -1 invalid
+ * params or no device.  ATTNRES_MULTI_FWD=mma / simt in the environment
+ * forces the choice where the shape allows it.
+ */
+int attnres_multi_fwd_tensor_cores(const attnres_multi_params* p, int32_t E);
+
+/*
  * 1 when the library was compiled with -DATTNRES_DEBUG (python -m
  * attention_residuals_gb300.build --debug writes it beside the release
  * build as libattnres_gb300_debug.so), else 0.  In that build every kernel
