@@ -30,7 +30,9 @@
 // one softmax group stays in shared memory for every block; a longer token is
 // streamed once per block, all passes but the last asking L2 to keep the rows
 // (evict_last), so the re-reads are served from L2 and HBM sees each row once.
-// Bandwidth-bound per-token reductions: no tensor cores.
+// With a few queries these are bandwidth-bound per-token reductions; nine or
+// more queries make the per-token products dense enough for the tensor-core
+// form (attnres_multi_fwd_mma.cu), which runs instead where it applies.
 #pragma once
 
 #include <cfloat>
