@@ -31,7 +31,7 @@ LIB_PATH = os.path.join(PKG, LIB_NAME)
 DEBUG_LIB_NAME = "libattnres_gb300_debug.so"
 DEBUG_LIB_PATH = os.path.join(PKG, DEBUG_LIB_NAME)
 SOURCES = ["attnres_fwd.cu", "attnres_bwd.cu", "attnres_bwd_norm.cu", "attnres_bwd_opre.cu", "attnres_bwd_cluster.cu",
-           "attnres_multi_fwd.cu", "attnres_multi_fwd_mma.cu", "attnres_multi_bwd.cu", "attnres_multi_general.cu", "attnres_api.cu", "attnres_host.cu", "attnres_jit.cu"]
+           "attnres_multi_fwd.cu", "attnres_multi_fwd_mma.cu", "attnres_multi_bwd.cu", "attnres_multi_general.cu", "attnres_multi_grad_mma.cu", "attnres_api.cu", "attnres_host.cu", "attnres_jit.cu"]
 # Sources the library compiles again at run time for exact plan shapes
 # (attnres_jit.cu): embedded as string literals under their include names.
 JIT_FILES = [("attnres_fwd_kernel.cuh", CSRC), ("attnres_multi_fwd_kernel.cuh", CSRC), ("device_utils.cuh", CSRC),

@@ -506,7 +506,7 @@ attnres_status make_multi_plan(const attnres_multi_params* p, MultiPlan* plan, i
                 for (int bufs = kMultiGenMaxBufs; bufs >= 2; --bufs) {
                     const size_t sm = multi_gen_smem_a(bufs, s8, pitch, M, S, pl.gen_kgroups, pl.gen_cs);
                     if (sm > budget) continue;
-                    const long long ahead = static_cast<long long>(bufs - 1) * (16 + s8) * pitch;
+                    const long long ahead = static_cast<long long>(bufs - 1) * (M + S) * pitch;
                     if (ahead > best) {
                         best = ahead;
                         ok_a = true;
@@ -541,6 +541,28 @@ attnres_status make_multi_plan(const attnres_multi_params* p, MultiPlan* plan, i
                 pl.gen_chunks_b = chunks;
                 pl.gen_smem_b = multi_gen_smem_b(S, pl.gen_cs, M, pl.gen_dcb, pl.gen_rows_b, chunks,
                                                  pl.gen_bank_rows, ts);
+            }
+        }
+        // the gradient kernel on the tensor cores (fixed queries, at most 16
+        // sources: one 16-row MMA tile) with as many token slots as fit, from
+        // kMultiGradMmaMinM queries up (its cost does not grow with the query
+        // count, the SIMT kernel's does); ATTNRES_MULTI_GRAD=mma|simt (read on
+        // every call) forces a form where it fits
+        const char* gform = std::getenv("ATTNRES_MULTI_GRAD");
+        const bool want_simt = gform && std::strcmp(gform, "simt") == 0;
+        const bool want_mma = gform && std::strcmp(gform, "mma") == 0;
+        pl.gen_grad_mma = 0;
+        if (E == 0 && S <= 16 && !want_simt && (want_mma || M >= kMultiGradMmaMinM)) {
+            for (int ts = kMultiGenMaxSlots; ts >= 2; --ts) {
+                const size_t sm = multi_grad_mma_smem(S, pl.gen_cs, M, ts);
+                if (sm <= optin) {
+                    pl.gen_grad_mma = 1;
+                    pl.gen_dcb = kMultiGenColumns;
+                    pl.gen_tslots_b = ts;
+                    pl.gen_smem_b = sm;
+                    ok_b = true;
+                    break;
+                }
             }
         }
         if (ok_a && ok_b) {
@@ -867,10 +889,11 @@ attnres_status attnres_check_device_error(void) {
     const unsigned mb = take_multi_bwd_error();
     const unsigned mg = take_multi_gen_error();
     const unsigned mm = take_multi_mma_error();
+    const unsigned mg2 = take_multi_grad_mma_error();
     if (f == 0xffffffffu || b == 0xffffffffu || mf == 0xffffffffu || mb == 0xffffffffu || mg == 0xffffffffu ||
-        mm == 0xffffffffu)
+        mm == 0xffffffffu || mg2 == 0xffffffffu)
         return ATTNRES_ERR_CUDA;
-    return (f || b || mf || mb || mg || mm) ? ATTNRES_ERR_DEVICE : ATTNRES_OK;
+    return (f || b || mf || mb || mg || mm || mg2) ? ATTNRES_ERR_DEVICE : ATTNRES_OK;
 }
 
 // ---------------------------------------------------------------------------
@@ -910,7 +933,7 @@ attnres_status attnres_multi_plan_info(const attnres_multi_params* p, int64_t ou
     out[5] = pl.b_chunks * 1000 + pl.b_rows;
     out[6] = pl.dy_slots;
     out[7] = static_cast<int64_t>(pl.gen ? pl.gen_smem_b : pl.smem_bwd);
-    out[8] = pl.gen;
+    out[8] = pl.gen ? 1 + pl.gen_grad_mma : 0;
     out[9] = pl.gen ? pl.gen_groups : 0;
     return ATTNRES_OK;
 }

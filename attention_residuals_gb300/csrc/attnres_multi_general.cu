@@ -53,24 +53,34 @@ constexpr int kGenThreads = (kGenWarps + 1) * 32;
 constexpr int kGenTokSlots = 2;                  // statistics slots of the coefficient kernel
 
 // ---------------------------------------------------------------- kernel A
-// Shared memory: ring of `bufs` row blocks ([16 dy rows][s8 source rows] x
-// pitch bytes; dy rows M..15 and source rows S..s8-1 stay zero), full/empty
-// barriers, statistics ring [kGenTokSlots][2*M*S + S], partial tiles
-// [kgroups][16][s8], DA [16][s8], zr [16][s8], coefficient table [S][cs]
+// Shared memory: ring of `bufs` row blocks ([M dy rows][S source rows] x
+// pitch bytes), one zero row that the MMAs read for queries M..15 and
+// sources S..s8-1, full/empty barriers, statistics ring
+// [kGenTokSlots][2*M*S + S], partial tiles [kgroups][16][s8], per-warp
+// parts of the c_s sums [kCoefWarps][s8], coefficient table [S][cs]
 // (queries padded to M4 = M rounded up to 4, for 16-byte loads: alpha at 0,
 // b at M4, c at 2 M4; the padding stays zero).
+//
+// Four consumer warps and a producer warp; two CTAs share an SM, so one
+// CTA's per-token reductions overlap the other's MMAs and copies.
+constexpr int kCoefWarps = kMultiCoefWarps;
+constexpr int kCoefThreads = (kCoefWarps + 1) * 32;
+
 struct GenALayout {
-    uint32_t ring, full, empty, tfull, tempty, tok, red, da, zr, coef, misc, total;
+    uint32_t ring, zero, full, empty, tfull, tempty, tok, red, zr, coef, misc, total;
     uint32_t buf_bytes, tstride;
 };
 
 __host__ __device__ inline GenALayout gen_a_layout(int bufs, int s8, uint32_t pitch, int M, int S, int kgroups,
                                                    int cs) {
     GenALayout L;
-    L.buf_bytes = static_cast<uint32_t>(16 + s8) * pitch;
+    L.buf_bytes = static_cast<uint32_t>(M + S) * pitch;
     uint32_t off = 0;
     L.ring = off;
     off += static_cast<uint32_t>(bufs) * L.buf_bytes;
+    off = align_up(off, 16);
+    L.zero = off;
+    off += pitch;
     off = align_up(off, 16);
     L.full = off;
     off += 8u * bufs;
@@ -86,10 +96,8 @@ __host__ __device__ inline GenALayout gen_a_layout(int bufs, int s8, uint32_t pi
     off += kGenTokSlots * L.tstride * 4u;
     L.red = off;
     off += static_cast<uint32_t>(kgroups) * 16u * static_cast<uint32_t>(s8) * 4u;
-    L.da = off;
-    off += 16u * static_cast<uint32_t>(s8) * 4u;
     L.zr = off;
-    off += 16u * static_cast<uint32_t>(s8) * 4u;
+    off += static_cast<uint32_t>(kCoefWarps) * static_cast<uint32_t>(s8) * 4u;
     off = align_up(off, 16);
     L.coef = off;
     off += static_cast<uint32_t>(S) * static_cast<uint32_t>(cs) * 4u;
@@ -98,11 +106,6 @@ __host__ __device__ inline GenALayout gen_a_layout(int bufs, int s8, uint32_t pi
     L.total = align_up(off, 128);
     return L;
 }
-
-// Four consumer warps and a producer warp; two CTAs share an SM, so one
-// CTA's per-token reductions overlap the other's MMAs and copies.
-constexpr int kCoefWarps = kMultiCoefWarps;
-constexpr int kCoefThreads = (kCoefWarps + 1) * 32;
 
 __global__ void __launch_bounds__(kCoefThreads, 2) attnres_multi_coef_kernel(const __grid_constant__ MultiGenArgs a) {
     extern __shared__ __align__(128) unsigned char smem[];
@@ -118,7 +121,6 @@ __global__ void __launch_bounds__(kCoefThreads, 2) attnres_multi_coef_kernel(con
     uint64_t* tempty = reinterpret_cast<uint64_t*>(smem + L.tempty);
     float* tok = reinterpret_cast<float*>(smem + L.tok);
     float* red = reinterpret_cast<float*>(smem + L.red);
-    float* da = reinterpret_cast<float*>(smem + L.da);
     float* zr = reinterpret_cast<float*>(smem + L.zr);
     float* coef = reinterpret_cast<float*>(smem + L.coef);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L.misc);
@@ -146,17 +148,9 @@ __global__ void __launch_bounds__(kCoefThreads, 2) attnres_multi_coef_kernel(con
         *abort_flag = 0;
         mbar_fence_init();
     }
-    // the padding rows of every buffer (dy rows M..15, source rows S..s8-1)
-    // and the coefficient table's padding stay zero
-    for (int b = 0; b < B; ++b) {
-        unsigned char* buf = smem + L.ring + b * L.buf_bytes;
-        const int lo0 = M * static_cast<int>(pitch) / 16, hi0 = 16 * static_cast<int>(pitch) / 16;
-        const int lo1 = (16 + S) * static_cast<int>(pitch) / 16, hi1 = (16 + s8) * static_cast<int>(pitch) / 16;
-        for (int i = lo0 + threadIdx.x; i < hi0; i += blockDim.x)
-            *reinterpret_cast<uint4*>(buf + 16 * i) = make_uint4(0u, 0u, 0u, 0u);
-        for (int i = lo1 + threadIdx.x; i < hi1; i += blockDim.x)
-            *reinterpret_cast<uint4*>(buf + 16 * i) = make_uint4(0u, 0u, 0u, 0u);
-    }
+    // the zero row and the coefficient table's padding stay zero
+    for (int i = threadIdx.x; i < static_cast<int>(pitch) / 16; i += blockDim.x)
+        *reinterpret_cast<uint4*>(smem + L.zero + 16 * i) = make_uint4(0u, 0u, 0u, 0u);
     for (int i = threadIdx.x; i < S * cs; i += blockDim.x) coef[i] = 0.0f;
     __syncthreads();
 
@@ -203,7 +197,7 @@ __global__ void __launch_bounds__(kCoefThreads, 2) attnres_multi_coef_kernel(con
                 unsigned char* buf = smem + L.ring + b * L.buf_bytes;
                 for (int r = lane; r < M + S; r += 32) {
                     const bool dyrow = r < M;
-                    const int row = dyrow ? r : 16 + (r - M);
+                    const int row = r;
                     const void* src = dyrow ? static_cast<const void*>(a.dy + r * a.dy_ms + n * a.dy_ns + c0)
                                             : static_cast<const void*>(static_cast<const unsigned char*>(a.src[r - M]) +
                                                                        (n * a.src_ld + c0) * 2);
@@ -244,10 +238,18 @@ __global__ void __launch_bounds__(kCoefThreads, 2) attnres_multi_coef_kernel(con
     const uint32_t empty_s = sbase + L.empty;
     const uint32_t tfull_s = sbase + L.tfull;
     const uint32_t tempty_s = sbase + L.tempty;
-    // ldmatrix row addresses of this lane (A: dy rows, B: source rows of a tile)
-    const uint32_t a_row = static_cast<uint32_t>((lane & 7) + ((lane >> 3) & 1) * 8) * pitch +
-                           static_cast<uint32_t>((lane >> 4) * 8) * 2u;
-    const uint32_t b_row = static_cast<uint32_t>(16 + (lane & 7)) * pitch + static_cast<uint32_t>(((lane >> 3) & 1) * 8) * 2u;
+    // ldmatrix row addresses of this lane, relative to a buffer (A: dy row
+    // `ra`; B: source row `rb` of a tile), or absolute at the zero row for
+    // queries past M and sources past S
+    const uint32_t zero_s = sbase + L.zero;
+    const int ra = (lane & 7) + ((lane >> 3) & 1) * 8;
+    const uint32_t a_col = static_cast<uint32_t>((lane >> 4) * 8) * 2u;
+    const uint32_t b_col = static_cast<uint32_t>(((lane >> 3) & 1) * 8) * 2u;
+    auto a_addr = [&](uint32_t buf) { return ra < M ? buf + static_cast<uint32_t>(ra) * pitch + a_col : zero_s + a_col; };
+    auto b_addr = [&](uint32_t buf, int tile) {
+        const int rb = tile * 8 + (lane & 7);
+        return rb < S ? buf + static_cast<uint32_t>(M + rb) * pitch + b_col : zero_s + b_col;
+    };
     const int g = lane >> 2, t4 = lane & 3;
     const float inv_r = 1.0f / static_cast<float>(a.R);
 
@@ -266,21 +268,57 @@ __global__ void __launch_bounds__(kCoefThreads, 2) attnres_multi_coef_kernel(con
             const int ksteps = (wc + 15) >> 4;
             mbar_wait_s(full_s + 8u * b, phase, abort_flag, &g_multi_gen_error, kSiteBwdConsumer);
             const uint32_t buf = ring_s + static_cast<uint32_t>(b) * L.buf_bytes;
+            const uint32_t abuf = a_addr(buf), bbuf = b_addr(buf, my_tile);
             uint32_t dep = 0;
-            if (active) {
-                for (int ks = my_kg; ks < ksteps; ks += kg) {
-                    uint32_t a0, a1, a2, a3;
-                    ldsm_x4(buf + a_row + static_cast<uint32_t>(ks) * 32u, a0, a1, a2, a3);
-                    dep ^= a0;
+            if (active && split_k) {
+                // one tile: the fragments of four k steps are loaded before
+                // their MMAs, which alternate between two accumulators (added
+                // in a fixed order after the token)
+                for (int ks = my_kg; ks < ksteps; ks += 4 * kg) {
+                    uint32_t af[4][4], bf[4][2];
 #pragma unroll
-                    for (int j = 0; j < 4; ++j) {
-                        const int tile = my_tile + j * kCoefWarps;
-                        if ((j == 0 || !split_k) && tile < ntiles) {
-                            uint32_t b0, b1;
-                            ldsm_x2(buf + b_row + static_cast<uint32_t>(tile * 8) * pitch + static_cast<uint32_t>(ks) * 32u,
-                                    b0, b1);
-                            dep ^= b0;
-                            mma_bf16_16816(acc[j], a0, a1, a2, a3, b0, b1);
+                    for (int u = 0; u < 4; ++u) {
+                        const int kk = ks + u * kg;
+                        if (kk < ksteps) {
+                            ldsm_x4(abuf + static_cast<uint32_t>(kk) * 32u, af[u][0], af[u][1], af[u][2], af[u][3]);
+                            ldsm_x2(bbuf + static_cast<uint32_t>(kk) * 32u, bf[u][0], bf[u][1]);
+                            dep ^= af[u][0] ^ bf[u][0];
+                        }
+                    }
+#pragma unroll
+                    for (int u = 0; u < 4; ++u)
+                        if (ks + u * kg < ksteps)
+                            mma_bf16_16816(acc[u & 1], af[u][0], af[u][1], af[u][2], af[u][3], bf[u][0], bf[u][1]);
+                }
+            } else if (active) {
+                // whole tiles (up to four): the fragments of two k steps are
+                // loaded before their MMAs
+                for (int ks = my_kg; ks < ksteps; ks += 2 * kg) {
+                    uint32_t af[2][4], bf[2][4][2];
+#pragma unroll
+                    for (int u = 0; u < 2; ++u) {
+                        const int kk = ks + u * kg;
+                        if (kk < ksteps) {
+                            ldsm_x4(abuf + static_cast<uint32_t>(kk) * 32u, af[u][0], af[u][1], af[u][2], af[u][3]);
+                            dep ^= af[u][0];
+#pragma unroll
+                            for (int j = 0; j < 4; ++j) {
+                                const int tile = my_tile + j * kCoefWarps;
+                                if (tile < ntiles) {
+                                    ldsm_x2(b_addr(buf, tile) + static_cast<uint32_t>(kk) * 32u, bf[u][j][0], bf[u][j][1]);
+                                    dep ^= bf[u][j][0];
+                                }
+                            }
+                        }
+                    }
+#pragma unroll
+                    for (int u = 0; u < 2; ++u) {
+                        if (ks + u * kg < ksteps) {
+#pragma unroll
+                            for (int j = 0; j < 4; ++j)
+                                if (my_tile + j * kCoefWarps < ntiles)
+                                    mma_bf16_16816(acc[j], af[u][0], af[u][1], af[u][2], af[u][3], bf[u][j][0],
+                                                   bf[u][j][1]);
                         }
                     }
                 }
@@ -291,6 +329,10 @@ __global__ void __launch_bounds__(kCoefThreads, 2) attnres_multi_coef_kernel(con
                 b = 0;
                 phase ^= 1u;
             }
+        }
+        if (split_k) {
+#pragma unroll
+            for (int e = 0; e < 4; ++e) acc[0][e] += acc[1][e];
         }
         // partial tiles -> red[k group][query][source]; then DA = their sum in k-group order
         if (active) {
@@ -308,46 +350,113 @@ __global__ void __launch_bounds__(kCoefThreads, 2) attnres_multi_coef_kernel(con
             }
         }
         named_bar_sync(1, nct);
-        for (int i = threadIdx.x; i < 16 * s8; i += nct) {
-            float sum = 0.0f;
-            for (int k = 0; k < kg; ++k) sum += red[k * 16 * s8 + i];
-            da[i] = sum;
-        }
         mbar_wait_s(tfull_s + 8u * ts, tphase, abort_flag, &g_multi_gen_error, kSiteBwdTokStat);
-        named_bar_sync(1, nct);
-        // coefficients: one warp per query, lanes over sources
+        // coefficients: warp w forms those of queries w, w + 4, w + 8, w + 12
+        // together (lanes over sources; da_ms = the k-group partials added in
+        // k-group order), and its part of sum_m dz_ms z_ms per source
         const float* tk = tok + ts * tstride;
-        for (int m = warp; m < M; m += kCoefWarps) {
-            float p = 0.0f;
-            for (int s = lane; s < S; s += 32) p = fmaf(tk[m * S + s], da[m * s8 + s], p);
-            const float delta = warp_sum(p);
-            for (int s = lane; s < S; s += 32) {
-                const float al = tk[m * S + s];
-                const float dz = al * (da[m * s8 + s] - delta);
+        constexpr int kQW = 16 / kCoefWarps;  // queries per warp (M <= 16)
+        auto da_of = [&](int m, int s) {
+            float d = 0.0f;
+            for (int k = 0; k < kg; ++k) d += red[(k * 16 + m) * s8 + s];
+            return d;
+        };
+        if (S <= 32) {
+            // one source per lane: every load of the warp's queries is issued
+            // before the sums that use it
+            const int s = lane;
+            const bool sv = s < S;
+            float al[kQW], lg[kQW], dd[kQW], delta[kQW];
+#pragma unroll
+            for (int i = 0; i < kQW; ++i) {
+                const int m = warp + i * kCoefWarps;
+                const bool v = sv && m < M;
+                al[i] = v ? tk[m * S + s] : 0.0f;
+                lg[i] = v ? tk[MS + m * S + s] : 0.0f;
+                float d = 0.0f;
+#pragma unroll
+                for (int k = 0; k < kCoefWarps; ++k)
+                    if (k < kg) d += v ? red[(k * 16 + m) * s8 + s] : 0.0f;
+                dd[i] = d;
+                delta[i] = al[i] * d;
+            }
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1)
+#pragma unroll
+                for (int i = 0; i < kQW; ++i) delta[i] += __shfl_xor_sync(0xffffffffu, delta[i], o);
+            if (sv) {
                 const float r = tk[2 * MS + s];
-                coef[s * cs + m] = al;
-                coef[s * cs + M4 + m] = a.scale * r * dz;
-                zr[m * s8 + s] = dz * tk[MS + m * S + s];
+                float z = 0.0f;
+#pragma unroll
+                for (int i = 0; i < kQW; ++i) {
+                    const int m = warp + i * kCoefWarps;
+                    if (m < M) {
+                        const float dz = al[i] * (dd[i] - delta[i]);
+                        coef[s * cs + m] = al[i];
+                        coef[s * cs + M4 + m] = a.scale * r * dz;
+                        z = fmaf(dz, lg[i], z);
+                    }
+                }
+                zr[warp * s8 + s] = z;
+            }
+        } else {
+            float delta[kQW];
+#pragma unroll
+            for (int i = 0; i < kQW; ++i) {
+                const int m = warp + i * kCoefWarps;
+                float p = 0.0f;
+                if (m < M)
+                    for (int s = lane; s < S; s += 32) p = fmaf(tk[m * S + s], da_of(m, s), p);
+                delta[i] = p;
+            }
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1)
+#pragma unroll
+                for (int i = 0; i < kQW; ++i) delta[i] += __shfl_xor_sync(0xffffffffu, delta[i], o);
+            for (int s = lane; s < S; s += 32) {
+                const float r = tk[2 * MS + s];
+                float z = 0.0f;
+#pragma unroll
+                for (int i = 0; i < kQW; ++i) {
+                    const int m = warp + i * kCoefWarps;
+                    if (m < M) {
+                        const float al = tk[m * S + s];
+                        const float dz = al * (da_of(m, s) - delta[i]);
+                        coef[s * cs + m] = al;
+                        coef[s * cs + M4 + m] = a.scale * r * dz;
+                        z = fmaf(dz, tk[MS + m * S + s], z);
+                    }
+                }
+                zr[warp * s8 + s] = z;
             }
         }
         named_bar_sync(1, nct);
-        for (int s = threadIdx.x; s < S; s += nct) {
-            float z = 0.0f;
-            for (int m = 0; m < M; ++m) z += zr[m * s8 + s];  // query order
-            const float r = tk[2 * MS + s];
-            coef[s * cs + 2 * M4] = -(r * r) * inv_r * z;
+        // the token's table -> workspace (16-byte stores; cs is a multiple of 4);
+        // the vector holding c_s = -(r_s^2 / R) sum_m dz_ms z_ms (the warps'
+        // parts added in warp order) gets it on the way
+        {
+            float4* out = reinterpret_cast<float4*>(a.coef + n * static_cast<long long>(S) * cs);
+            const float4* in = reinterpret_cast<const float4*>(coef);
+            const int cs4 = cs / 4;
+            for (int i = threadIdx.x; i < S * cs4; i += nct) {
+                float4 v = in[i];
+                const int s = i / cs4;
+                if (4 * (i - s * cs4) == 2 * M4) {
+                    float z = 0.0f;
+#pragma unroll
+                    for (int w = 0; w < kCoefWarps; ++w) z += zr[w * s8 + s];
+                    const float r = tk[2 * MS + s];
+                    v.x = -(r * r) * inv_r * z;
+                }
+                out[i] = v;
+            }
         }
-        named_bar_sync(1, nct);
         __syncwarp();
         if (lane == 0) mbar_arrive_s(tempty_s + 8u * ts);
         if (++ts == kGenTokSlots) {
             ts = 0;
             tphase ^= 1u;
         }
-        // the token's table -> workspace (16-byte stores; cs is a multiple of 4)
-        float4* out = reinterpret_cast<float4*>(a.coef + n * static_cast<long long>(S) * cs);
-        const float4* in = reinterpret_cast<const float4*>(coef);
-        for (int i = threadIdx.x; i < S * cs / 4; i += nct) out[i] = in[i];
         named_bar_sync(1, nct);  // the table and DA are rewritten by the next token
     }
 }
@@ -553,27 +662,45 @@ __global__ void __launch_bounds__(kGenThreads, 1) attnres_multi_grad_kernel(cons
     }
 
     // ---------------------------------------------------------- consumers
-    float2 qv[MQ][P], dqs[MQ][P];
+    // Registers hold the queries in pairs: for query pair i and column c of
+    // the thread (c = 2 p + h over its P column pairs), qp[i][c] = {q_2i,
+    // q_2i+1} at that column; dyp holds the token's dy values and dqp the dq
+    // sums the same way.  A coefficient row stores the four alphas (and the
+    // four b) of a query group contiguously, so each 16-byte load gives two
+    // aligned pairs that enter the packed FMAs as they are: a source row
+    // costs, per group of four queries, two loads and six packed FMAs per
+    // column, and the even and odd queries' partial sums are added at the end.
+    constexpr int MP = MQ / 2;
+    constexpr int C = 2 * P;
+    float2 qp[MP][C], dqp[MP][C];
 #pragma unroll
-    for (int m = 0; m < MQ; ++m)
+    for (int i = 0; i < MP; ++i)
 #pragma unroll
         for (int p = 0; p < P; ++p) {
-            float x = 0.0f, y = 0.0f;
-            if (!SEL && m < M) {
-                if (kx[p]) x = bf16_bits_to_float(a.q[static_cast<long long>(m) * a.R + (j0[p] - ko)]);
-                if (ky[p]) y = bf16_bits_to_float(a.q[static_cast<long long>(m) * a.R + (j0[p] + 1 - ko)]);
+            float q[2][2] = {{0.0f, 0.0f}, {0.0f, 0.0f}};  // [query 2i + e][column]
+            if (!SEL) {
+#pragma unroll
+                for (int e = 0; e < 2; ++e) {
+                    const int m = 2 * i + e;
+                    if (m < M) {
+                        if (kx[p]) q[e][0] = bf16_bits_to_float(a.q[static_cast<long long>(m) * a.R + (j0[p] - ko)]);
+                        if (ky[p]) q[e][1] = bf16_bits_to_float(a.q[static_cast<long long>(m) * a.R + (j0[p] + 1 - ko)]);
+                    }
+                }
             }
-            qv[m][p] = make_float2(x, y);
-            dqs[m][p] = make_float2(0.0f, 0.0f);
+            qp[i][2 * p] = make_float2(q[0][0], q[1][0]);
+            qp[i][2 * p + 1] = make_float2(q[0][1], q[1][1]);
+            dqp[i][2 * p] = dqp[i][2 * p + 1] = make_float2(0.0f, 0.0f);
         }
     const uint32_t sbase = smem_u32(smem);
-    const uint32_t lane_off = 4u * threadIdx.x;          // the thread's first pair within a row
-    constexpr uint32_t kPairStep = 4u * kGenWarps * 32;  // bytes between a thread's pairs
+    constexpr int kPairWords = kGenWarps * 32;  // 4-byte words between a thread's pairs in a row
+    const int rowp_w = static_cast<int>(rowp / 4u);
     const uint32_t full_s = sbase + L.full, empty_s = sbase + L.empty;
     const uint32_t tfull_s = sbase + L.tfull, tempty_s = sbase + L.tempty;
     float2 keep[P];
 #pragma unroll
     for (int p = 0; p < P; ++p) keep[p] = make_float2(kx[p] ? 1.0f : 0.0f, ky[p] ? 1.0f : 0.0f);
+    const float2 one = make_float2(1.0f, 1.0f);
     int k = 0;
     uint32_t phase = 0;
     int ts = 0;
@@ -581,113 +708,126 @@ __global__ void __launch_bounds__(kGenThreads, 1) attnres_multi_grad_kernel(cons
     for (long long n = grp; n < N; n += ngrp) {
         mbar_wait_s(tfull_s + 8u * ts, tphase, abort_flag, &g_multi_gen_error, kSiteBwdConsumer);
         const unsigned char* slot = smem + L.slot + ts * L.slot_bytes;
-        const uint32_t slot_s = sbase + L.slot + ts * L.slot_bytes;
-        const uint32_t ctab_s = slot_s + L.coef_off;
-        float2 dyv[MQ][P];
+        const float* ctab = reinterpret_cast<const float*>(slot + L.coef_off);
+        const uint32_t* dyw = reinterpret_cast<const uint32_t*>(slot + L.dy_off) + threadIdx.x;
+        float2 dyp[MP][C];
 #pragma unroll
-        for (int m = 0; m < MQ; ++m)
+        for (int i = 0; i < MP; ++i)
 #pragma unroll
             for (int p = 0; p < P; ++p) {
-                uint32_t w = 0;
-                if (m < M && own[p])
-                    asm volatile("ld.shared.b32 %0, [%1];"
-                                 : "=r"(w)
-                                 : "r"(slot_s + L.dy_off + m * rowp + lane_off + p * kPairStep));
-                dyv[m][p] = bf2_to_f2(w);
+                uint32_t w0 = 0, w1 = 0;
+                if (2 * i < M && own[p]) w0 = dyw[(2 * i) * rowp_w + p * kPairWords];
+                if (2 * i + 1 < M && own[p]) w1 = dyw[(2 * i + 1) * rowp_w + p * kPairWords];
+                dyp[i][2 * p] = make_float2(__uint_as_float(w0 << 16), __uint_as_float(w1 << 16));
+                dyp[i][2 * p + 1] = make_float2(__uint_as_float(w0 & 0xffff0000u), __uint_as_float(w1 & 0xffff0000u));
             }
-        int qrow[MQ];
+        const long long* ids = reinterpret_cast<const long long*>(slot + L.ids_off);
         if constexpr (SEL) {
-            const long long* ids = reinterpret_cast<const long long*>(slot + L.ids_off);
 #pragma unroll
-            for (int m = 0; m < MQ; ++m) {
-                long long id = -1;
-                if (m < M) {
-                    id = ids[m];
-                    if (id < 0 || id >= E) {
-                        if (threadIdx.x == 0) atomicCAS(&g_multi_gen_error, 0u, static_cast<unsigned>(kSiteBadId));
-                        id = -1;
-                    }
-                }
-                qrow[m] = static_cast<int>(id);
+            for (int i = 0; i < MP; ++i) {
+                float q[2][P][2];  // [query 2i + e][pair][column]: the token's query values
 #pragma unroll
-                for (int p = 0; p < P; ++p) {
-                    float x = 0.0f, y = 0.0f;
-                    if (id >= 0) {
-                        if (bank_smem) {
-                            uint32_t w = 0;
-                            if (own[p])
-                                asm volatile("ld.shared.b32 %0, [%1];"
-                                             : "=r"(w)
-                                             : "r"(sbase + L.bank + static_cast<uint32_t>(id) * rowp + lane_off +
-                                                   p * kPairStep));
-                            const float2 f = bf2_to_f2(w);
-                            x = f.x;
-                            y = f.y;
-                        } else {
-                            if (kx[p]) x = bf16_bits_to_float(a.q[id * a.R + (j0[p] - ko)]);
-                            if (ky[p]) y = bf16_bits_to_float(a.q[id * a.R + (j0[p] + 1 - ko)]);
+                for (int e = 0; e < 2; ++e) {
+                    const int m = 2 * i + e;
+                    long long id = -1;
+                    if (m < M) {
+                        id = ids[m];
+                        if (id < 0 || id >= E) {
+                            if (threadIdx.x == 0) atomicCAS(&g_multi_gen_error, 0u, static_cast<unsigned>(kSiteBadId));
+                            id = -1;
                         }
                     }
-                    qv[m][p] = make_float2(x, y);
-                    dqs[m][p] = make_float2(0.0f, 0.0f);
+#pragma unroll
+                    for (int p = 0; p < P; ++p) {
+                        float x = 0.0f, y = 0.0f;
+                        if (id >= 0) {
+                            if (bank_smem) {
+                                uint32_t w = 0;
+                                if (own[p])
+                                    w = reinterpret_cast<const uint32_t*>(smem + L.bank)[static_cast<int>(id) * rowp_w +
+                                                                                         threadIdx.x + p * kPairWords];
+                                const float2 f = bf2_to_f2(w);
+                                x = f.x;
+                                y = f.y;
+                            } else {
+                                if (kx[p]) x = bf16_bits_to_float(a.q[id * a.R + (j0[p] - ko)]);
+                                if (ky[p]) y = bf16_bits_to_float(a.q[id * a.R + (j0[p] + 1 - ko)]);
+                            }
+                        }
+                        q[e][p][0] = x;
+                        q[e][p][1] = y;
+                    }
+                }
+#pragma unroll
+                for (int p = 0; p < P; ++p) {
+                    qp[i][2 * p] = make_float2(q[0][p][0], q[1][p][0]);
+                    qp[i][2 * p + 1] = make_float2(q[0][p][1], q[1][p][1]);
+                    dqp[i][2 * p] = dqp[i][2 * p + 1] = make_float2(0.0f, 0.0f);
                 }
             }
         }
         for (int s0 = 0; s0 < S; s0 += G) {
             const int gs = min(G, S - s0);
             mbar_wait_s(full_s + 8u * k, phase, abort_flag, &g_multi_gen_error, kSiteBwdConsumer);
-            const uint32_t chunk = sbase + L.ring + static_cast<uint32_t>(k) * L.chunk_bytes + lane_off;
+            const uint32_t* chunk =
+                reinterpret_cast<const uint32_t*>(smem + L.ring + static_cast<uint32_t>(k) * L.chunk_bytes) + threadIdx.x;
             uint32_t dep = 0;
+#pragma unroll 1
             for (int r = 0; r < gs; ++r) {
                 const int s = s0 + r;
-                float2 t[P];
+                float2 t[P], tb[C];
 #pragma unroll
                 for (int p = 0; p < P; ++p) {
-                    uint32_t w = 0;
-                    if (own[p])
-                        asm volatile("ld.shared.b32 %0, [%1];"
-                                     : "=r"(w)
-                                     : "r"(chunk + static_cast<uint32_t>(r) * rowp + p * kPairStep));
+                    const uint32_t w = own[p] ? chunk[r * rowp_w + p * kPairWords] : 0u;
                     dep ^= w;
                     t[p] = fmul2(bf2_to_f2(w), keep[p]);  // key channels of the row
+                    tb[2 * p] = make_float2(t[p].x, t[p].x);
+                    tb[2 * p + 1] = make_float2(t[p].y, t[p].y);
                 }
-                // alpha_s., b_s. and c_s of the row: 16-byte broadcast loads of the
-                // padded table; four independent FMA chains for the dy and query terms
-                const uint32_t crow = ctab_s + static_cast<uint32_t>(s * cs) * 4u;
-                float2 oa[2][P], ob[2][P];
+                // alpha_s., b_s. and c_s of the row (the table's padding queries are zero)
+                const float* crow = ctab + s * cs;
+                // two accumulators per column for the alpha and the b terms (one
+                // when a thread owns two column pairs, to stay within its registers)
+                constexpr int h1 = C > 2 ? 0 : 1;
+                float2 oa[2][C], ob[2][C];
 #pragma unroll
                 for (int h = 0; h < 2; ++h)
 #pragma unroll
-                    for (int p = 0; p < P; ++p) oa[h][p] = ob[h][p] = make_float2(0.0f, 0.0f);
+                    for (int c = 0; c < C; ++c) oa[h][c] = ob[h][c] = make_float2(0.0f, 0.0f);
 #pragma unroll
                 for (int g4 = 0; g4 < MQ / 4; ++g4) {
                     if (4 * g4 < M) {
-                        const float4 av = lds128f(crow + 16u * g4);
-                        const float4 bv = lds128f(crow + 4u * M4 + 16u * g4);
-                        const float al[4] = {av.x, av.y, av.z, av.w};
-                        const float bl[4] = {bv.x, bv.y, bv.z, bv.w};
+                        const float4 av = *reinterpret_cast<const float4*>(crow + 4 * g4);
+                        const float4 bv = *reinterpret_cast<const float4*>(crow + M4 + 4 * g4);
+                        const float2 a01 = make_float2(av.x, av.y), a23 = make_float2(av.z, av.w);
+                        const float2 b01 = make_float2(bv.x, bv.y), b23 = make_float2(bv.z, bv.w);
 #pragma unroll
-                        for (int j = 0; j < 4; ++j) {
-                            const int m = 4 * g4 + j;
-                            const float2 al2 = make_float2(al[j], al[j]), bq2 = make_float2(bl[j], bl[j]);
-#pragma unroll
-                            for (int p = 0; p < P; ++p) {
-                                oa[j & 1][p] = ffma2(al2, dyv[m][p], oa[j & 1][p]);
-                                ob[j & 1][p] = ffma2(bq2, qv[m][p], ob[j & 1][p]);
-                                dqs[m][p] = ffma2(bq2, t[p], dqs[m][p]);
-                            }
+                        for (int c = 0; c < C; ++c) {
+                            oa[0][c] = ffma2(a01, dyp[2 * g4][c], oa[0][c]);
+                            oa[h1][c] = ffma2(a23, dyp[2 * g4 + 1][c], oa[h1][c]);
+                            ob[0][c] = ffma2(b01, qp[2 * g4][c], ob[0][c]);
+                            ob[h1][c] = ffma2(b23, qp[2 * g4 + 1][c], ob[h1][c]);
+                            dqp[2 * g4][c] = ffma2(b01, tb[c], dqp[2 * g4][c]);
+                            dqp[2 * g4 + 1][c] = ffma2(b23, tb[c], dqp[2 * g4 + 1][c]);
                         }
                     }
                 }
-                float cv;
-                asm volatile("ld.shared.f32 %0, [%1];" : "=f"(cv) : "r"(crow + 8u * M4));
-                const float2 cv2 = make_float2(cv, cv), one = make_float2(1.0f, 1.0f);
+                const float cv = crow[2 * M4];
+                const float2 cv2 = make_float2(cv, cv);
                 uint16_t* drow = static_cast<uint16_t*>(a.dsrc[s]) + n * a.dsrc_ld;
 #pragma unroll
                 for (int p = 0; p < P; ++p) {
-                    const float2 o = ffma2(cv2, t[p], ffma2(one, oa[0][p], ffma2(one, oa[1][p], ffma2(one, ob[0][p], ob[1][p]))));
+                    // {even, odd} query sums at the pair's two columns, then their totals
+                    float2 e0 = ffma2(one, oa[0][2 * p], ob[0][2 * p]);
+                    float2 e1 = ffma2(one, oa[0][2 * p + 1], ob[0][2 * p + 1]);
+                    if constexpr (h1 == 1) {
+                        e0 = ffma2(one, e0, ffma2(one, oa[1][2 * p], ob[1][2 * p]));
+                        e1 = ffma2(one, e1, ffma2(one, oa[1][2 * p + 1], ob[1][2 * p + 1]));
+                    }
+                    const float2 o = ffma2(cv2, t[p], ffma2(one, make_float2(e0.x, e1.x), make_float2(e0.y, e1.y)));
+                    // no memory clobber: the next row's shared-memory loads may be issued before it
                     if (own[p] && ATTNRES_IN_BOUNDS(n < a.N && s < a.S && j0[p] + 2 <= a.D, &g_multi_gen_error))
-                        asm volatile("st.global.cs.b32 [%0], %1;" ::"l"(drow + j0[p]), "r"(pack_f2(o)) : "memory");
+                        asm volatile("st.global.cs.b32 [%0], %1;" ::"l"(drow + j0[p]), "r"(pack_f2(o)));
                 }
             }
             __syncwarp();
@@ -698,15 +838,18 @@ __global__ void __launch_bounds__(kGenThreads, 1) attnres_multi_grad_kernel(cons
             }
         }
         if constexpr (SEL) {
-            // the token's dq into its bank rows of the group's partial row
+            // the token's dq into its bank rows of the group's partial row (the
+            // ids are read again from the slot, which is still held)
 #pragma unroll
             for (int m = 0; m < MQ; ++m) {
-                if (m < M && qrow[m] >= 0) {
-                    float* pq = prow + static_cast<long long>(qrow[m]) * a.R;
+                const long long id = m < M ? ids[m] : -1;
+                if (id >= 0 && id < E) {
+                    float* pq = prow + id * a.R;
 #pragma unroll
                     for (int p = 0; p < P; ++p) {
-                        if (kx[p]) red_add_f32(pq + (j0[p] - ko), dqs[m][p].x);
-                        if (ky[p]) red_add_f32(pq + (j0[p] + 1 - ko), dqs[m][p].y);
+                        const float2 d0 = dqp[m >> 1][2 * p], d1 = dqp[m >> 1][2 * p + 1];
+                        if (kx[p]) red_add_f32(pq + (j0[p] - ko), (m & 1) ? d0.y : d0.x);
+                        if (ky[p]) red_add_f32(pq + (j0[p] + 1 - ko), (m & 1) ? d1.y : d1.x);
                     }
                 }
             }
@@ -726,8 +869,9 @@ __global__ void __launch_bounds__(kGenThreads, 1) attnres_multi_grad_kernel(cons
                 float* pq = prow + static_cast<long long>(m) * a.R;
 #pragma unroll
                 for (int p = 0; p < P; ++p) {
-                    if (kx[p]) pq[j0[p] - ko] = dqs[m][p].x;
-                    if (ky[p]) pq[j0[p] + 1 - ko] = dqs[m][p].y;
+                    const float2 d0 = dqp[m >> 1][2 * p], d1 = dqp[m >> 1][2 * p + 1];
+                    if (kx[p]) pq[j0[p] - ko] = (m & 1) ? d0.y : d0.x;
+                    if (ky[p]) pq[j0[p] + 1 - ko] = (m & 1) ? d1.y : d1.x;
                 }
             }
         }
@@ -770,7 +914,8 @@ cudaError_t launch_multi_bwd_general(const MultiPlan& plan, const MultiGenArgs& 
     err = cudaGetLastError();
     if (err != cudaSuccess) return err;
     const bool sel = a.ids != nullptr;
-    err = sel ? launch_grad_sel<true>(plan, a, stream) : launch_grad_sel<false>(plan, a, stream);
+    err = sel ? launch_grad_sel<true>(plan, a, stream)
+              : (plan.gen_grad_mma ? launch_multi_grad_mma(plan, a, stream) : launch_grad_sel<false>(plan, a, stream));
     if (err != cudaSuccess) return err;
     const int W = (sel ? a.E : a.M) * a.R;
     return launch_finalize(a.part, plan.gen_groups, W, W, a.dq, a.dq_f32, nullptr, nullptr, stream);

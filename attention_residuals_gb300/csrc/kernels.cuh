@@ -358,6 +358,7 @@ struct MultiPlan {
     size_t gen_smem_a, gen_smem_b;
     int gen_s8, gen_kgroups, gen_bufs, gen_dc, gen_pitch, gen_cs;
     int gen_dcb, gen_rows_b, gen_chunks_b, gen_bank_rows, gen_tslots_b;
+    int gen_grad_mma;                         // gradient kernel on the tensor cores (attnres_multi_grad_mma.cu)
     size_t gen_part_off;                      // workspace: coefficient tables, then partial rows
     int grid;
     int fgrid;             // forward CTAs (multi_fwd_ctas_per_sm per SM)
@@ -460,13 +461,25 @@ struct MultiGenArgs {
 // its layout fits); more queries take the general backward.
 constexpr int kMultiResidentMaxM = 4;
 constexpr int kMultiGenColumns = 512;   // columns per CTA of the gradient kernel, per column pair of a thread
-constexpr int kMultiGenMaxBufs = 8;     // row-block buffers of the coefficient kernel
+constexpr int kMultiGenMaxBufs = 12;    // row-block buffers of the coefficient kernel
 constexpr int kMultiCoefWarps = 4;      // consumer warps of the coefficient kernel
 constexpr int kMultiGenMaxSlots = 8;    // token slots of the gradient kernel
+// Queries from which the general backward's gradient kernel runs on the
+// tensor cores (measured, S=10 N=32768: M=16 D=1024 1.45 against 2.05 ms for
+// the whole backward, M=16 D=4096 5.53 against 7.92 ms, but M=8 D=4096 4.94
+// against 4.22 ms).
+constexpr int kMultiGradMmaMinM = 9;
 size_t multi_gen_smem_a(int bufs, int s8, int pitch, int M, int S, int kgroups, int cs);
 size_t multi_gen_smem_b(int S, int cs, int M, int dcb, int rows, int chunks, int bank_rows, int tslots);
 cudaError_t launch_multi_bwd_general(const MultiPlan& plan, const MultiGenArgs& a, cudaStream_t stream);
 unsigned take_multi_gen_error();
+// Gradient kernel of the general backward on the tensor cores (fixed
+// queries, at most 16 sources): its shared memory with `slots` token slots,
+// its launch (grid and shared memory from the plan's gen_grid_b,
+// gen_smem_b; token slots in a.tslots_b) and its first failed wait.
+size_t multi_grad_mma_smem(int S, int cs, int M, int slots);
+cudaError_t launch_multi_grad_mma(const MultiPlan& plan, const MultiGenArgs& a, cudaStream_t stream);
+unsigned take_multi_grad_mma_error();
 
 unsigned take_multi_fwd_error();
 unsigned take_multi_bwd_error();

@@ -411,8 +411,9 @@ attnres_status attnres_multi_bwd(const attnres_multi_params* p, const void* q, c
  * register block (forward * 1000 + backward), forward ring (chunks * 1000 +
  * rows per chunk), backward ring (chunks * 1000 + rows per chunk), dy slots,
  * the backward dynamic shared memory bytes (of the gradient kernel in the
- * general form), the backward form (0 resident, 1 general) and the general
- * form's token groups (0 otherwise).
+ * general form), the backward form (0 resident, 1 general, 2 general with
+ * its gradient kernel on the tensor cores) and the general form's token
+ * groups (0 otherwise).
  */
 attnres_status attnres_multi_plan_info(const attnres_multi_params* p, int64_t out[10]);
 

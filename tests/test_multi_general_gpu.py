@@ -8,6 +8,9 @@ general backward serves every shape -- the ones whose token does not fit in
 shared memory (many sources, wide rows, many queries) and, by default, every
 read with more than four queries.  ATTNRES_MULTI_BWD=general forces it on
 any shape, so it is also checked on the shapes of the resident kernels.
+Its gradient kernel runs on the tensor cores for fixed queries and at most
+16 sources; ATTNRES_MULTI_GRAD=simt keeps the SIMT kernel, and both are
+checked.
 """
 import numpy as np
 import pytest
@@ -52,14 +55,23 @@ def _run_multi(wl, twice=False):
     return fwd, bwd, ref
 
 
+def _grad_form(monkeypatch, form, S):
+    """Force the gradient kernel; the plan's backward form it should give
+    (2: tensor-core gradients, for at most 16 sources; 1: SIMT)."""
+    monkeypatch.setenv("ATTNRES_MULTI_GRAD", form)
+    return 2 if form == "mma" and S <= 16 else 1
+
+
+@pytest.mark.parametrize("form", ["mma", "simt"])
 @pytest.mark.parametrize("S,N,D,R,ko,M", MULTI_SHAPES)
-def test_general_on_every_multi_shape(S, N, D, R, ko, M, monkeypatch):
+def test_general_on_every_multi_shape(S, N, D, R, ko, M, form, monkeypatch):
     monkeypatch.setenv("ATTNRES_MULTI_BWD", "general")
+    want = _grad_form(monkeypatch, form, S)
     wl = make_multi(S, N, D, R, M, key_offset=ko, seed=S * 37 + M, src_scale=(0.5, 2.0))
     info = attnres_multi_plan_info(wl.values.cuda(), M, R, key_offset=ko)
-    assert info["bwd_general"] == 1, info
+    assert info["bwd_general"] == want, info
     fwd, bwd, ref = _run_multi(wl)
-    errs = _check_multi(wl, fwd, bwd, ref, f"S{S} N{N} D{D} R{R} ko{ko} M{M}")
+    errs = _check_multi(wl, fwd, bwd, ref, f"S{S} N{N} D{D} R{R} ko{ko} M{M} {form}")
     print(info, errs)
 
 
@@ -77,13 +89,15 @@ WIDE = [
 ]
 
 
+@pytest.mark.parametrize("form", ["mma", "simt"])
 @pytest.mark.parametrize("S,N,D,R,ko,M", WIDE)
-def test_general_wide_shapes(S, N, D, R, ko, M):
+def test_general_wide_shapes(S, N, D, R, ko, M, form, monkeypatch):
+    want = _grad_form(monkeypatch, form, S)
     wl = make_multi(S, N, D, R, M, key_offset=ko, seed=S + D + M, src_scale=(0.5, 2.0), scale=1.7, eps=1e-4)
     info = attnres_multi_plan_info(wl.values.cuda(), M, R, key_offset=ko)
-    assert info["bwd_general"] == 1, info
+    assert info["bwd_general"] == want, info
     fwd, bwd, ref = _run_multi(wl, twice=True)
-    errs = _check_multi(wl, fwd, bwd, ref, f"S{S} N{N} D{D} R{R} ko{ko} M{M}")
+    errs = _check_multi(wl, fwd, bwd, ref, f"S{S} N{N} D{D} R{R} ko{ko} M{M} {form}")
     print(info, errs)
 
 

@@ -144,7 +144,7 @@ def test_multi_large_tokens_forward_and_backward():
     # backward takes the general two-kernel path
     wl = make_multi(64, 5, 8192, 8192, 16, key_offset=0, seed=77)
     v, Q = wl.values.cuda(), wl.queries.cuda()
-    assert attnres_multi_plan_info(v, 16, 8192, key_offset=0)["bwd_general"] == 1
+    assert attnres_multi_plan_info(v, 16, 8192, key_offset=0)["bwd_general"] >= 1
     fwd, bwd, ref = run_multi(wl)
     _check(wl, fwd, bwd, ref, False, "S64 D8192 M16")
 
