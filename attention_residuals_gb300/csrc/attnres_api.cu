@@ -492,29 +492,28 @@ attnres_status make_multi_plan(const attnres_multi_params* p, MultiPlan* plan, i
         // of 4, for 16-byte loads) and c, padded to a multiple of 4 floats
         pl.gen_cs = 2 * ((M + 3) & ~3) + 4;
         // coefficient kernel: two CTAs per SM when their layouts fit in half of
-        // it, each with the ring of row blocks (column blocks of at least 256, a
-        // multiple of 16, and two to eight buffers) that keeps the most bytes
-        // loading ahead of the block being used
+        // it, each with a ring of at least two row blocks of the widest block
+        // width that allows them (1024 columns down to 256, a multiple of 16
+        // below that), holding as many buffers as fit.  Wide blocks first: the
+        // copies are one 1-D bulk copy per row and block, and measured
+        // (S=10, N=32768) 512-byte copies could not keep the SMs fed where
+        // 1-2 KB ones could (M=16 D=1024: 1.28 ms at 256 columns, 1.04 at 512;
+        // M=8 D=4096: 4.23 at 256, 3.30 at 1024).
         bool ok_a = false;
-        long long best = -1;
         int coef_ctas = 2;
         for (int pass = 0; pass < 4 && !ok_a; ++pass) {
             coef_ctas = pass < 2 ? 2 : 1;
             const size_t budget = coef_ctas == 2 ? optin / 2 - 1024 : optin;
-            for (int dc = 1024; dc >= ((pass & 1) == 0 ? 256 : 16); dc /= 2) {
+            for (int dc = 1024; dc >= ((pass & 1) == 0 ? 256 : 16) && !ok_a; dc /= 2) {
                 const int pitch = dc * 2 + 16;
                 for (int bufs = kMultiGenMaxBufs; bufs >= 2; --bufs) {
                     const size_t sm = multi_gen_smem_a(bufs, s8, pitch, M, S, pl.gen_kgroups, pl.gen_cs);
                     if (sm > budget) continue;
-                    const long long ahead = static_cast<long long>(bufs - 1) * (M + S) * pitch;
-                    if (ahead > best) {
-                        best = ahead;
-                        ok_a = true;
-                        pl.gen_dc = dc;
-                        pl.gen_pitch = pitch;
-                        pl.gen_bufs = bufs;
-                        pl.gen_smem_a = sm;
-                    }
+                    ok_a = true;
+                    pl.gen_dc = dc;
+                    pl.gen_pitch = pitch;
+                    pl.gen_bufs = bufs;
+                    pl.gen_smem_a = sm;
                     break;  // the most buffers that fit at this width
                 }
             }

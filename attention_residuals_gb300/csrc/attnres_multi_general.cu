@@ -50,7 +50,7 @@ __device__ __align__(16) unsigned char g_zero16[16];
 
 constexpr int kGenWarps = 8;                     // consumer warps of the gradient kernel
 constexpr int kGenThreads = (kGenWarps + 1) * 32;
-constexpr int kGenTokSlots = 2;                  // statistics slots of the coefficient kernel
+constexpr int kGenTokSlots = 4;                  // statistics slots of the coefficient kernel (tokens the producer may run ahead)
 
 // ---------------------------------------------------------------- kernel A
 // Shared memory: ring of `bufs` row blocks ([M dy rows][S source rows] x

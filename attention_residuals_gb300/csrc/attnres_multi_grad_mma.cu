@@ -5,28 +5,31 @@
 // attnres_multi_general.cu gives the chain rule, "Fast Attention
 // Residuals", sections "Multi-query AttnRes" and "Equation"):
 //   dV [S x D]  = A^T [S x M] . DY [M x D] + B^T [S x M] . Q [M x D]
-//                 + c_s t_s on the key channels
+//                 + C [S x S] . T [S x D]       (C = diag(c_s), key channels)
 //   dQ [M x R] += B [M x S] . T [S x R]                 (summed over tokens)
-// with Q zero off the key channels and T the sources' key channels.  With S
-// and M padded to 16 both are chains of mma.m16n8k16: sources (dV) or
-// queries (dQ) are the A rows, queries (dV) or sources (dQ) the K dimension,
-// 8-channel column tiles the N dimension.  The FP32 coefficients enter as
-// three bf16 terms (hi + mid + lo, the rest below 2^-26 relative; smallest
-// term first); dy, q and t are bf16 and exact, the products exact in FP32
-// and the sums FP32.
+// with Q zero off the key channels and T the sources' rows.  With S and M
+// padded to 16 these are chains of mma.m16n8k16: sources (dV) or queries
+// (dQ) are the A rows, queries or sources the K dimension, 8-channel column
+// tiles the N dimension.  The FP32 coefficients enter as three bf16 terms
+// (hi + mid + lo, the rest below 2^-26 relative; smallest term first); dy, q
+// and t are bf16 and exact, the products exact in FP32 and the sums FP32.
+// A column tile that holds a key boundary adds c_s t_s per element instead.
 //
 // GB300 mapping: one CTA per 512-column block of a token group, as the SIMT
 // gradient kernel.  A producer warp streams each token's coefficient table,
 // its M dy rows and its S source rows (the block's columns, rows padded to
 // 1040 bytes so that ldmatrix reads of 8 consecutive rows fall in different
 // banks) into a ring of token slots with 1-D bulk copies; dy rows past M and
-// source rows past S read one zero row.  Consumer warp w owns 64 columns
-// (eight column tiles).  Per token it forms the three-term A fragments from
-// the table, then per column tile six MMAs for dV (B from the slot's dy rows
+// source rows past S read one zero row.  Per token the consumer threads
+// split the table into bf16 fragment tables in the slot (one element each),
+// and each of the sixteen consumer warps -- four per scheduler, to cover the
+// MMA and shared-memory latencies -- takes its A fragments from them with
+// ldmatrix and runs its four column tiles (32 columns) with their
+// independent chains interleaved: the dV product (B from the slot's dy rows
 // by ldmatrix.trans and from the queries, held in registers for the launch),
-// adds c_s t_s and three MMAs for dQ (B = the slot's source rows).  dV leaves
-// through the warp's staging tile as 16-byte stores; the dQ accumulators stay
-// in registers for all of the CTA's tokens and are written once, as the
+// C . T and the dQ product (B = the slot's source rows).  dV rows leave as
+// bf16 pairs straight from the accumulators; the dQ accumulators stay in
+// registers for all of the CTA's tokens and are written once, as the
 // group's partial row (the finalize kernel adds the groups in order).
 #include "device_utils.cuh"
 #include "kernels.cuh"
@@ -37,38 +40,38 @@ namespace {
 // First failed wait of any launch of this unit (0 = none).
 __device__ unsigned int g_multi_grad_mma_error = 0;
 
-constexpr int kGmWarps = 8;                        // consumer warps
-constexpr int kGmThreads = (kGmWarps + 1) * 32;    // plus the producer warp
-constexpr int kGmCols = kGmWarps * 64;             // columns per CTA
+constexpr int kGmWarps = 16;                       // MMA warps
+constexpr int kGmBuildWarps = 2;                   // warps that split each token's coefficients
+constexpr int kGmThreads = (kGmWarps + kGmBuildWarps + 1) * 32;  // plus the producer warp
+constexpr int kGmCols = kGmWarps * 32;             // columns per CTA
 constexpr int kGmPitch = kGmCols * 2 + 16;         // bytes per row in a slot
-constexpr int kGmStagePitch = 80;                  // bytes per row of a staging tile (32 columns + 16)
-static_assert(kGmCols == kMultiGenColumns, "the MMA gradient kernel keeps the SIMT kernel's column blocks");
-
 constexpr int kGmFragPitch = 48;                   // bytes per row of a fragment table (16 bf16 + 16)
 constexpr int kGmFragBytes = 16 * kGmFragPitch;    // one 16 x 16 bf16 table
+constexpr int kGmTables = 9;                       // {A, B, C} x {hi, mid, lo}
+static_assert(kGmCols == kMultiGenColumns, "the MMA gradient kernel keeps the SIMT kernel's column blocks");
 
 // Shared memory: `slots` token slots {coefficient table [S][cs] FP32, rows
 // [M + S][kGmPitch] bytes: dy rows then source rows (both filled by the
-// copies), fragment tables [2][3][16][kGmFragPitch] (written by the
-// consumers)}, the zero row, the warps' staging tiles, barriers.
+// copies), fragment tables [kGmTables][16][kGmFragPitch] (written by the
+// consumers)}, the zero row, barriers.
 struct GmLayout {
-    uint32_t ring, slot_bytes, rows_off, frag_off, zero, stage, full, empty, misc, total;
+    uint32_t ring, slot_bytes, rows_off, frag_off, zero, full, ready, empty, misc, total;
 };
 
 __host__ __device__ inline GmLayout gm_layout(int S, int cs, int M, int slots) {
     GmLayout L;
     L.rows_off = align_up(static_cast<uint32_t>(S * cs) * 4u, 16);
     L.frag_off = L.rows_off + static_cast<uint32_t>(M + S) * kGmPitch;
-    L.slot_bytes = align_up(L.frag_off + 6u * kGmFragBytes, 128);
+    L.slot_bytes = align_up(L.frag_off + kGmTables * kGmFragBytes, 128);
     uint32_t off = 0;
     L.ring = off;
     off += static_cast<uint32_t>(slots) * L.slot_bytes;
     L.zero = off;
     off += kGmPitch;
-    L.stage = off;
-    off += kGmWarps * 16u * kGmStagePitch;
     off = align_up(off, 8);
     L.full = off;
+    off += 8u * static_cast<uint32_t>(slots);
+    L.ready = off;  // the slot's fragment tables are written
     off += 8u * static_cast<uint32_t>(slots);
     L.empty = off;
     off += 8u * static_cast<uint32_t>(slots);
@@ -90,8 +93,7 @@ __device__ __forceinline__ void split3(float x, uint16_t& hi, uint16_t& mid, uin
 }
 
 // M8: at most eight queries, so alpha and b share one 16-wide K step of the
-// dV product (A = [alpha | b], B = [dy rows 0..7 ; query rows 0..7]): six
-// MMAs per column tile instead of nine.
+// dV product (A = [alpha | b], B = [dy rows 0..7 ; query rows 0..7]).
 template <bool M8>
 __global__ void __launch_bounds__(kGmThreads, 1) attnres_multi_grad_mma_kernel(const __grid_constant__ MultiGenArgs a) {
     extern __shared__ __align__(128) unsigned char smem[];
@@ -116,6 +118,7 @@ __global__ void __launch_bounds__(kGmThreads, 1) attnres_multi_grad_mma_kernel(c
     if (threadIdx.x == 0) {
         for (int k = 0; k < K; ++k) {
             mbar_init(full + k, 1);
+            mbar_init(reinterpret_cast<uint64_t*>(smem + L.ready) + k, kGmBuildWarps);
             mbar_init(empty + k, kGmWarps);
         }
         *abort_flag = 0;
@@ -123,9 +126,14 @@ __global__ void __launch_bounds__(kGmThreads, 1) attnres_multi_grad_mma_kernel(c
     }
     for (int i = threadIdx.x; i < kGmPitch / 16; i += blockDim.x)
         *reinterpret_cast<uint4*>(smem + L.zero + 16 * i) = make_uint4(0u, 0u, 0u, 0u);
+    // every slot's fragment tables start at zero: per token only the entries
+    // of the S sources and the queries (or the diagonal) are rewritten
+    for (int k = 0; k < K; ++k)
+        for (int i = threadIdx.x; i < kGmTables * kGmFragBytes / 16; i += blockDim.x)
+            *reinterpret_cast<uint4*>(smem + L.ring + k * L.slot_bytes + L.frag_off + 16 * i) = make_uint4(0u, 0u, 0u, 0u);
     __syncthreads();
 
-    if (warp == kGmWarps) {
+    if (warp == kGmWarps + kGmBuildWarps) {
         // ------------------------------------------------------ producer
         // lane 0 claims a slot and announces its bytes; the lanes issue the
         // row copies
@@ -168,22 +176,81 @@ __global__ void __launch_bounds__(kGmThreads, 1) attnres_multi_grad_mma_kernel(c
         return;
     }
 
-    // ---------------------------------------------------------- consumers
     const uint32_t sbase = smem_u32(smem);
-    const uint32_t full_s = sbase + L.full, empty_s = sbase + L.empty;
+    const uint32_t full_s = sbase + L.full, ready_s = sbase + L.ready, empty_s = sbase + L.empty;
+    constexpr int tw = kGmFragBytes / 2;  // elements per fragment table
+
+    if (warp >= kGmWarps) {
+        // ------------------------------------------------------ builders
+        // per token, once its copies have landed: the fragment tables in the
+        // slot, [s][column] elements split over the builder threads (the
+        // other entries stay zero): table A (terms at 0..2) the A of the dV
+        // product, alpha_sk (M8: alpha_sk for k < 8, b_s,k-8 above); table B
+        // (3..5) b_sm, the second K step of dV (not M8) and, read transposed,
+        // the A of the dQ product; table C (6..8) diag(c_s).  The MMA warps
+        // wait for them on the slot's `ready` barrier, so the builders run
+        // ahead of them by up to the ring's depth.
+        const int bt_id = static_cast<int>(threadIdx.x) - kGmWarps * 32;
+        constexpr int nbt = kGmBuildWarps * 32;
+        const int wa = M8 ? 8 + M4 : M4;  // live columns of table A
+        const int na = S * wa, nb = S * M4;
+        int k = 0;
+        uint32_t phase = 0;
+        for (long long n = grp; n < N; n += ngrp) {
+            if (!mbar_wait_s(full_s + 8u * k, phase, abort_flag, &g_multi_grad_mma_error, kSiteBwdConsumer)) break;
+            unsigned char* slot = smem + L.ring + k * L.slot_bytes;
+            const float* ctab = reinterpret_cast<const float*>(slot);
+            uint16_t* ft = reinterpret_cast<uint16_t*>(slot + L.frag_off);
+            for (int i = bt_id; i < na + nb + S; i += nbt) {
+                int tb, sr, c;
+                float v;
+                if (i < na) {
+                    tb = 0;
+                    sr = i / wa;
+                    c = i - sr * wa;
+                    if (M8)
+                        v = c < 8 ? (c < M4 ? ctab[sr * cs + c] : 0.0f) : ctab[sr * cs + M4 + c - 8];
+                    else
+                        v = ctab[sr * cs + c];
+                } else if (i < na + nb) {
+                    tb = 1;
+                    sr = (i - na) / M4;
+                    c = (i - na) - sr * M4;
+                    v = ctab[sr * cs + M4 + c];
+                } else {
+                    tb = 2;
+                    sr = c = i - na - nb;
+                    v = ctab[sr * cs + 2 * M4];
+                }
+                const int e = 3 * tb * tw + sr * (kGmFragPitch / 2) + c;
+                split3(v, ft[e], ft[tw + e], ft[2 * tw + e]);
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive_s(ready_s + 8u * k);
+            if (++k == K) {
+                k = 0;
+                phase ^= 1u;
+            }
+        }
+        return;
+    }
+
+    // ---------------------------------------------------------- MMA warps
     const uint32_t zero_s = sbase + L.zero;
-    const uint32_t stage_s = sbase + L.stage + static_cast<uint32_t>(warp) * 16u * kGmStagePitch;
     const int g = lane >> 2, t4 = lane & 3;
-    const int wcol = warp * 64;   // the warp's first column within the block
+    const int wcol = warp * 32;   // the warp's first column within the block
     const bool wact = wcol < wc;  // a warp past the block's width only takes part in the waits
     auto is_key = [&](int col) { return col >= ko && col < ko + R; };
 
     // B fragments of the queries at the warp's column tiles:
     // {q[2 t4][col], q[2 t4 + 1][col]} and {q[2 t4 + 8][col], q[2 t4 + 9][col]}
-    // at col = c0 + wcol + 8 j + g (zero off the key channels and past M)
-    uint32_t bq[8][2];
+    // at col = c0 + wcol + 8 j + g (zero off the key channels and past M);
+    // per tile: wholly on the key (C . T by MMA), holding a key boundary
+    // (c_s t_s per element), or off the key
+    uint32_t bq[4][2];
+    bool kall[4], kmix[4];
 #pragma unroll
-    for (int j = 0; j < 8; ++j) {
+    for (int j = 0; j < 4; ++j) {
         const int col = c0 + wcol + 8 * j + g;
         const bool key = wact && col < D && is_key(col);
         auto qbits = [&](int m) -> uint32_t {
@@ -191,10 +258,13 @@ __global__ void __launch_bounds__(kGmThreads, 1) attnres_multi_grad_mma_kernel(c
         };
         bq[j][0] = qbits(2 * t4) | (qbits(2 * t4 + 1) << 16);
         bq[j][1] = qbits(2 * t4 + 8) | (qbits(2 * t4 + 9) << 16);
+        const int t0 = c0 + wcol + 8 * j;
+        kall[j] = t0 >= ko && t0 + 8 <= ko + R;
+        kmix[j] = !kall[j] && t0 < ko + R && t0 + 8 > ko;
     }
-    float dqa[8][4];
+    float dqa[4][4];
 #pragma unroll
-    for (int j = 0; j < 8; ++j)
+    for (int j = 0; j < 4; ++j)
 #pragma unroll
         for (int e = 0; e < 4; ++e) dqa[j][e] = 0.0f;
 
@@ -205,130 +275,112 @@ __global__ void __launch_bounds__(kGmThreads, 1) attnres_multi_grad_mma_kernel(c
                             static_cast<uint32_t>(lane >> 4) * 16u;
     const uint32_t ft_off = static_cast<uint32_t>((lane & 7) + ((lane >> 4) & 1) * 8) * kGmFragPitch +
                             static_cast<uint32_t>((lane >> 3) & 1) * 16u;
-    constexpr int nct = kGmWarps * 32;
     int k = 0;
     uint32_t phase = 0;
     for (long long n = grp; n < N; n += ngrp) {
+        // the tables are written (after the slot's copies landed)
+        mbar_wait_s(ready_s + 8u * k, phase, abort_flag, &g_multi_grad_mma_error, kSiteBwdConsumer);
         mbar_wait_s(full_s + 8u * k, phase, abort_flag, &g_multi_grad_mma_error, kSiteBwdConsumer);
         unsigned char* slot = smem + L.ring + k * L.slot_bytes;
         const uint32_t rows_s = sbase + L.ring + static_cast<uint32_t>(k) * L.slot_bytes + L.rows_off;
         const uint32_t frag_s = sbase + L.ring + static_cast<uint32_t>(k) * L.slot_bytes + L.frag_off;
         const float* ctab = reinterpret_cast<const float*>(slot);
-        {
-            // the token's fragment tables, one element per consumer thread:
-            // table 0 (term t at 0 + t): A of the dV product, [s][k] = alpha_sk
-            // (M8: alpha_sk for k < 8, b_s,k-8 above); table 1 (term t at 3 + t):
-            // [s][m] = b_sm, the second K step of dV (not M8) and, read
-            // transposed, the A of the dQ product
-            const int i = static_cast<int>(threadIdx.x);
-            const int sr = i >> 4, c = i & 15;
-            float va = 0.0f, vb = 0.0f;
-            if (sr < S) {
-                if (M8)
-                    va = c < 8 ? (c < M4 ? ctab[sr * cs + c] : 0.0f) : (c - 8 < M4 ? ctab[sr * cs + M4 + c - 8] : 0.0f);
-                else
-                    va = c < M4 ? ctab[sr * cs + c] : 0.0f;
-                vb = c < M4 ? ctab[sr * cs + M4 + c] : 0.0f;
-            }
-            uint16_t* ft = reinterpret_cast<uint16_t*>(slot + L.frag_off);
-            const int e = sr * (kGmFragPitch / 2) + c;
-            constexpr int tw = kGmFragBytes / 2;  // elements per table
-            split3(va, ft[e], ft[tw + e], ft[2 * tw + e]);
-            split3(vb, ft[3 * tw + e], ft[4 * tw + e], ft[5 * tw + e]);
-        }
-        named_bar_sync(1, nct);
         if (wact) {
-            uint32_t fa[3][4], fb[3][4], fq[3][4];
-#pragma unroll
-            for (int t = 0; t < 3; ++t) {
-                ldsm_x4(frag_s + t * kGmFragBytes + fa_off, fa[t][0], fa[t][1], fa[t][2], fa[t][3]);
-                if (!M8) ldsm_x4(frag_s + (3 + t) * kGmFragBytes + fa_off, fb[t][0], fb[t][1], fb[t][2], fb[t][3]);
-                ldsm_x4_trans(frag_s + (3 + t) * kGmFragBytes + ft_off, fq[t][0], fq[t][1], fq[t][2], fq[t][3]);
-            }
-            const float cg = g < S ? ctab[g * cs + 2 * M4] : 0.0f;
-            const float cg8 = g + 8 < S ? ctab[(g + 8) * cs + 2 * M4] : 0.0f;
             const uint32_t dyrow = lr < M ? rows_s + static_cast<uint32_t>(lr) * kGmPitch : zero_s;
             const uint32_t trow = lr < S ? rows_s + static_cast<uint32_t>(M + lr) * kGmPitch : zero_s;
-            const uint32_t t_g = rows_s + static_cast<uint32_t>(M + g) * kGmPitch;  // source rows g, g + 8
-            const uint32_t t_g8 = t_g + 8u * kGmPitch;
+            // the B fragments of the warp's four tiles
+            uint32_t bd[4][2], bt[4][2];
 #pragma unroll
-            for (int h = 0; h < 2; ++h) {  // two groups of four column tiles (32 columns)
-                // the group's B fragments first, then its MMAs with the four
-                // tiles' independent chains interleaved
-                uint32_t bd[4][2], bt[4][2];
+            for (int jj = 0; jj < 4; ++jj) {
+                const uint32_t coff = static_cast<uint32_t>(wcol + 8 * jj) * 2u;
+                ldsm_x2_trans(dyrow + coff, bd[jj][0], bd[jj][1]);
+                ldsm_x2_trans(trow + coff, bt[jj][0], bt[jj][1]);
+            }
+            float acc[4][4];
 #pragma unroll
-                for (int jj = 0; jj < 4; ++jj) {
-                    const uint32_t coff = static_cast<uint32_t>(wcol + 32 * h + 8 * jj) * 2u;
-                    ldsm_x2_trans(dyrow + coff, bd[jj][0], bd[jj][1]);
-                    ldsm_x2_trans(trow + coff, bt[jj][0], bt[jj][1]);
-                }
-                float acc[4][4];
+            for (int jj = 0; jj < 4; ++jj)
 #pragma unroll
-                for (int jj = 0; jj < 4; ++jj)
+                for (int e = 0; e < 4; ++e) acc[jj][e] = 0.0f;
+            // dV: the four tiles' chains interleaved, smallest term first
+            {
+                uint32_t fa[3][4];
 #pragma unroll
-                    for (int e = 0; e < 4; ++e) acc[jj][e] = 0.0f;
-                // smallest term first
-                if constexpr (M8) {
-                    // K = [queries 0..7 of dy ; queries 0..7 of q]
+                for (int t = 0; t < 3; ++t) ldsm_x4(frag_s + t * kGmFragBytes + fa_off, fa[t][0], fa[t][1], fa[t][2], fa[t][3]);
 #pragma unroll
-                    for (int tm = 2; tm >= 0; --tm)
-#pragma unroll
-                        for (int jj = 0; jj < 4; ++jj)
-                            mma_bf16_16816(acc[jj], fa[tm][0], fa[tm][1], fa[tm][2], fa[tm][3], bd[jj][0],
-                                           bq[4 * h + jj][0]);
-                } else {
-#pragma unroll
-                    for (int tm = 2; tm >= 0; --tm)
-#pragma unroll
-                        for (int jj = 0; jj < 4; ++jj)
-                            mma_bf16_16816(acc[jj], fa[tm][0], fa[tm][1], fa[tm][2], fa[tm][3], bd[jj][0], bd[jj][1]);
-#pragma unroll
-                    for (int tm = 2; tm >= 0; --tm)
-#pragma unroll
-                        for (int jj = 0; jj < 4; ++jj)
-                            mma_bf16_16816(acc[jj], fb[tm][0], fb[tm][1], fb[tm][2], fb[tm][3], bq[4 * h + jj][0],
-                                           bq[4 * h + jj][1]);
-                }
-#pragma unroll
-                for (int tm = 2; tm >= 0; --tm)
+                for (int t = 2; t >= 0; --t)
 #pragma unroll
                     for (int jj = 0; jj < 4; ++jj)
-                        mma_bf16_16816(dqa[4 * h + jj], fq[tm][0], fq[tm][1], fq[tm][2], fq[tm][3], bt[jj][0], bt[jj][1]);
+                        mma_bf16_16816(acc[jj], fa[t][0], fa[t][1], fa[t][2], fa[t][3], bd[jj][0],
+                                       M8 ? bq[jj][0] : bd[jj][1]);
+            }
+            if constexpr (!M8) {
+                uint32_t fb[3][4];
 #pragma unroll
-                for (int jj = 0; jj < 4; ++jj) {
-                    // + c_s t_s on the key channels, as bf16 pairs into the staging tile
-                    const int cl = wcol + 32 * h + 8 * jj + 2 * t4;  // the pair's first column within the block
+                for (int t = 0; t < 3; ++t)
+                    ldsm_x4(frag_s + (3 + t) * kGmFragBytes + fa_off, fb[t][0], fb[t][1], fb[t][2], fb[t][3]);
+#pragma unroll
+                for (int t = 2; t >= 0; --t)
+#pragma unroll
+                    for (int jj = 0; jj < 4; ++jj)
+                        if (kall[jj] || kmix[jj])
+                            mma_bf16_16816(acc[jj], fb[t][0], fb[t][1], fb[t][2], fb[t][3], bq[jj][0], bq[jj][1]);
+            }
+            {
+                // C . T on the tiles wholly on the key
+                uint32_t fc[3][4];
+#pragma unroll
+                for (int t = 0; t < 3; ++t)
+                    ldsm_x4(frag_s + (6 + t) * kGmFragBytes + fa_off, fc[t][0], fc[t][1], fc[t][2], fc[t][3]);
+#pragma unroll
+                for (int t = 2; t >= 0; --t)
+#pragma unroll
+                    for (int jj = 0; jj < 4; ++jj)
+                        if (kall[jj]) mma_bf16_16816(acc[jj], fc[t][0], fc[t][1], fc[t][2], fc[t][3], bt[jj][0], bt[jj][1]);
+            }
+            {
+                // dQ (tiles with key channels): A = b_sm read transposed, B = the source rows
+                uint32_t fq[3][4];
+#pragma unroll
+                for (int t = 0; t < 3; ++t)
+                    ldsm_x4_trans(frag_s + (3 + t) * kGmFragBytes + ft_off, fq[t][0], fq[t][1], fq[t][2], fq[t][3]);
+#pragma unroll
+                for (int t = 2; t >= 0; --t)
+#pragma unroll
+                    for (int jj = 0; jj < 4; ++jj)
+                        if (kall[jj] || kmix[jj])
+                            mma_bf16_16816(dqa[jj], fq[t][0], fq[t][1], fq[t][2], fq[t][3], bt[jj][0], bt[jj][1]);
+            }
+            // dV rows g and g + 8 of each tile as bf16 pairs; a tile holding a key
+            // boundary adds c_s t_s per element first
+            uint16_t* const d_g = g < S ? static_cast<uint16_t*>(a.dsrc[g]) + n * a.dsrc_ld + c0 : nullptr;
+            uint16_t* const d_g8 = g + 8 < S ? static_cast<uint16_t*>(a.dsrc[g + 8]) + n * a.dsrc_ld + c0 : nullptr;
+#pragma unroll
+            for (int jj = 0; jj < 4; ++jj) {
+                const int cl = wcol + 8 * jj + 2 * t4;  // the pair's first column within the block
+                if (cl >= wc) continue;
+                float2 o0 = make_float2(acc[jj][0], acc[jj][1]), o1 = make_float2(acc[jj][2], acc[jj][3]);
+                if (kmix[jj]) {
                     const float kx = is_key(c0 + cl) ? 1.0f : 0.0f, ky = is_key(c0 + cl + 1) ? 1.0f : 0.0f;
-                    const uint32_t so = static_cast<uint32_t>(jj * 16 + t4 * 4);
+                    const uint32_t t_g = rows_s + static_cast<uint32_t>(M + g) * kGmPitch + static_cast<uint32_t>(cl) * 2u;
                     if (g < S) {
+                        const float cg = ctab[g * cs + 2 * M4];
                         uint32_t w;
-                        asm volatile("ld.shared.b32 %0, [%1];" : "=r"(w) : "r"(t_g + static_cast<uint32_t>(cl) * 2u));
+                        asm volatile("ld.shared.b32 %0, [%1];" : "=r"(w) : "r"(t_g));
                         const float2 t = bf2_to_f2(w);
-                        const float2 o = make_float2(fmaf(cg * kx, t.x, acc[jj][0]), fmaf(cg * ky, t.y, acc[jj][1]));
-                        asm volatile("st.shared.b32 [%0], %1;" ::"r"(stage_s + static_cast<uint32_t>(g) * kGmStagePitch + so),
-                                     "r"(pack_f2(o)));
+                        o0 = make_float2(fmaf(cg * kx, t.x, o0.x), fmaf(cg * ky, t.y, o0.y));
                     }
                     if (g + 8 < S) {
+                        const float cg8 = ctab[(g + 8) * cs + 2 * M4];
                         uint32_t w;
-                        asm volatile("ld.shared.b32 %0, [%1];" : "=r"(w) : "r"(t_g8 + static_cast<uint32_t>(cl) * 2u));
+                        asm volatile("ld.shared.b32 %0, [%1];" : "=r"(w) : "r"(t_g + 8u * kGmPitch));
                         const float2 t = bf2_to_f2(w);
-                        const float2 o = make_float2(fmaf(cg8 * kx, t.x, acc[jj][2]), fmaf(cg8 * ky, t.y, acc[jj][3]));
-                        asm volatile("st.shared.b32 [%0], %1;" ::"r"(stage_s + static_cast<uint32_t>(g + 8) * kGmStagePitch + so),
-                                     "r"(pack_f2(o)));
+                        o1 = make_float2(fmaf(cg8 * kx, t.x, o1.x), fmaf(cg8 * ky, t.y, o1.y));
                     }
                 }
-                __syncwarp();
-                // the group's S rows x 32 columns as 16-byte stores
-                for (int cix = lane; cix < 64; cix += 32) {
-                    const int row = cix >> 2, ch = cix & 3;
-                    const int cb = wcol + 32 * h + 8 * ch;  // within the block
-                    if (row < S && cb < wc &&
-                        ATTNRES_IN_BOUNDS(n < a.N && c0 + cb + 8 <= D, &g_multi_grad_mma_error)) {
-                        const uint4 v = lds128(stage_s + static_cast<uint32_t>(row) * kGmStagePitch + 16u * ch);
-                        st_global_cs_v4(static_cast<uint16_t*>(a.dsrc[row]) + n * a.dsrc_ld + c0 + cb, v);
-                    }
-                }
-                __syncwarp();
+                if (d_g && ATTNRES_IN_BOUNDS(n < a.N && c0 + cl + 2 <= D, &g_multi_grad_mma_error))
+                    asm volatile("st.global.b32 [%0], %1;" ::"l"(d_g + cl), "r"(pack_f2(o0)) : "memory");
+                if (d_g8 && ATTNRES_IN_BOUNDS(n < a.N && c0 + cl + 2 <= D, &g_multi_grad_mma_error))
+                    asm volatile("st.global.b32 [%0], %1;" ::"l"(d_g8 + cl), "r"(pack_f2(o1)) : "memory");
             }
         }
         // this warp is done with the slot
@@ -343,7 +395,7 @@ __global__ void __launch_bounds__(kGmThreads, 1) attnres_multi_grad_mma_kernel(c
     if (wact) {
         float* prow = a.part + static_cast<long long>(grp) * M * R;
 #pragma unroll
-        for (int j = 0; j < 8; ++j) {
+        for (int j = 0; j < 4; ++j) {
             const int col = c0 + wcol + 8 * j + 2 * t4;
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
