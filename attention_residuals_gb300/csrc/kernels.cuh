@@ -458,8 +458,11 @@ struct MultiGenArgs {
     float* dq_f32;
 };
 // Queries up to which the resident one-CTA multi-query backward runs (when
-// its layout fits); more queries take the general backward.
-constexpr int kMultiResidentMaxM = 4;
+// its layout fits); more queries take the general backward (measured, S=10
+// N=32768: M=2 D=4096 0.91 ms resident against 2.29 general, but M=3 D=4096
+// 2.85 against 2.29, M=4 D=1024 0.77 against 0.68, S=16 N=16384 D=2048 M=4
+// 1.50 against 0.84).
+constexpr int kMultiResidentMaxM = 2;
 constexpr int kMultiGenColumns = 512;   // columns per CTA of the gradient kernel, per column pair of a thread
 constexpr int kMultiGenMaxBufs = 12;    // row-block buffers of the coefficient kernel
 constexpr int kMultiCoefWarps = 4;      // consumer warps of the coefficient kernel

@@ -343,16 +343,18 @@ int attnres_jit_kernel_count(void);
  * in registers (one block for M <= 4 at D <= 2048, M <= 2 at D <= 4096;
  * later blocks re-read the token from L2), so any S and D are served.  The
  * backward has two forms, both serving every S, D and M the ABI accepts:
- *  - resident (up to four queries, when a token's S source rows, its M dy
+ *  - resident (up to two queries, when a token's S source rows, its M dy
  *    rows and the queries' key channels fit in shared memory): one kernel
  *    that reads each row once;
  *  - general (more queries, or tokens that do not fit): a coefficient kernel
  *    forms the per-token dots <dy_m, v_s> over blocks of columns with bf16
  *    tensor-core MMAs and writes every token's coefficients to the
- *    workspace, then a gradient kernel forms dvalues and dq block by block;
- *    the sources and dy are read twice.
+ *    workspace, then a gradient kernel forms dvalues and dq block by block
+ *    (on the tensor cores for nine or more fixed queries and at most 16
+ *    sources); the sources and dy are read twice.
  * ATTNRES_MULTI_BWD=general or resident in the environment (read on every
- * call) forces one form where it fits.
+ * call) forces one form where it fits; ATTNRES_MULTI_GRAD=mma or simt the
+ * general form's gradient kernel.
  * ------------------------------------------------------------------------ */
 #define ATTNRES_MAX_M 16
 

@@ -179,7 +179,7 @@ def _multi_call(lib, mp, queries, dy, S, N, D, M, R, E=0, ids=None):
 
 
 @pytest.mark.parametrize("S,N,D,R,ko,M", MULTI)
-@pytest.mark.parametrize("form", [None, "general"])
+@pytest.mark.parametrize("form", [None, "resident", "general"])
 def test_multi_query_stores_stay_inside(S, N, D, R, ko, M, form, monkeypatch):
     if form is not None:
         monkeypatch.setenv("ATTNRES_MULTI_BWD", form)

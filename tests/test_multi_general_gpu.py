@@ -6,7 +6,7 @@ against the FP64 oracle.
 with 1 <= M <= 16, and attnres_selected with K slots per token.  The
 general backward serves every shape -- the ones whose token does not fit in
 shared memory (many sources, wide rows, many queries) and, by default, every
-read with more than four queries.  ATTNRES_MULTI_BWD=general forces it on
+read with more than two queries.  ATTNRES_MULTI_BWD=general forces it on
 any shape, so it is also checked on the shapes of the resident kernels.
 Its gradient kernel runs on the tensor cores for fixed queries and at most
 16 sources; ATTNRES_MULTI_GRAD=simt keeps the SIMT kernel, and both are

@@ -83,8 +83,13 @@ SHAPES = [
 ]
 
 
+@pytest.mark.parametrize("form", [None, "resident"])
 @pytest.mark.parametrize("S,N,D,R,ko,M", SHAPES)
-def test_multi_matches_oracle(S, N, D, R, ko, M):
+def test_multi_matches_oracle(S, N, D, R, ko, M, form, monkeypatch):
+    # default plan, and the resident backward forced wherever a token fits
+    # (by default it serves at most two queries)
+    if form is not None:
+        monkeypatch.setenv("ATTNRES_MULTI_BWD", form)
     wl = make_multi(S, N, D, R, M, key_offset=ko, seed=S * 31 + M, src_scale=(0.5, 2.0))
     fwd, bwd, ref = run_multi(wl)
     errs = _check(wl, fwd, bwd, ref, False, f"S{S} N{N} D{D} R{R} ko{ko} M{M}")
