@@ -165,6 +165,9 @@ MULTI_CONFIGS = {
     # two queries over the long-sequence shapes at quarter rank, key in the
     # final R channels
     "long": dict(S=10, N=32768, D=4096, R=1024, M=2, src_scale=(0.5, 2.0)),
+    # the most queries the page allows (M <= 16) over full-rank keys of
+    # 1024-channel rows: the general backward and the tensor-core kernels
+    "sixteen": dict(S=10, N=32768, D=1024, R=1024, M=16, src_scale=(0.5, 2.0)),
 }
 
 

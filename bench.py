@@ -67,6 +67,7 @@ FALLBACK_HBM_GBS = 6800.0
 NOMINAL_HBM_GBS = 7900.0   # GB300 HBM3e data-sheet bandwidth (context for the measured-peak fraction)
 PROFILE_TRAFFIC = os.path.join(ROOT, "profiles", "attnres_bwd_traffic.json")
 PROFILE_TRAFFIC_MULTI = os.path.join(ROOT, "profiles", "attnres_multi_bwd_traffic.json")
+PROFILE_TRAFFIC_MULTI16 = os.path.join(ROOT, "profiles", "attnres_multi16_bwd_traffic.json")
 PROFILE_TRAFFIC_SELECTED = os.path.join(ROOT, "profiles", "attnres_selected_bwd_traffic.json")
 PROFILE_TRAFFIC_BLOCK = os.path.join(ROOT, "profiles", "attnres_block_bwd_traffic.json")
 
@@ -111,6 +112,8 @@ SINGLE_SOURCES = ["attnres_api.cu", "attnres_bwd.cu", "attnres_bwd_cluster.cu", 
 MULTI_SOURCES = ["attnres_api.cu", "attnres_bwd.cu", "attnres_bwd_kernel.cuh", "attnres_jit.cu",
                  "attnres_multi_bwd.cu", "attnres_multi_fwd.cu", "attnres_multi_fwd_kernel.cuh", "device_utils.cuh",
                  "kernels.cuh"]
+# the sixteen-query read: the tensor-core forward and the general backward
+GENERAL_SOURCES = MULTI_SOURCES + ["attnres_multi_fwd_mma.cu", "attnres_multi_general.cu", "attnres_multi_grad_mma.cu"]
 
 
 def kernel_sources_hash(names=None):
@@ -493,6 +496,41 @@ class MultiRead:
         return time.perf_counter() - t
 
 
+class Multi16Read(MultiRead):
+    """Multi-query read with the most queries the page allows: sixteen
+    full-rank queries over 1024-channel rows (the tensor-core forward; the
+    general backward -- coefficient kernel, then the tensor-core gradient
+    kernel -- whose sources and dy are read twice, though the algorithmic
+    bytes count them once)."""
+    key = "multi16"
+    roofline_kernel = "attnres_multi_coef_kernel + attnres_multi_grad_mma_kernel (+ finalize)"
+    cpu_tokens = 4096
+    ref_tokens = 512
+
+    def __init__(self, tokens=None, seed=0, device="cpu"):
+        from attention_residuals_gb300.workloads import make_multi_workload
+        self.wl = make_multi_workload("sixteen", N=tokens, seed=300 + 1000 * seed, device=device)
+
+    def describe(self):
+        wl = self.wl
+        return (f"multi-query M={wl.M} S={wl.S} N={wl.N} D={wl.D} R={wl.R} key_offset={wl.key_offset} "
+                f"bf16 (sixteen full-rank queries)")
+
+    def prepare(self, dev):
+        import torch
+        from attention_residuals_gb300 import attnres_multi_plan_info
+        wl = self.wl
+        self.info = attnres_multi_plan_info(wl.values, wl.M, wl.R, key_offset=wl.key_offset)
+        # the general form's partial rows: one per token group
+        self.bytes = self.bytes_for(self.info["bwd_token_groups"])
+        self.ws = torch.empty((256 << 20,), dtype=torch.uint8, device=dev)
+        self.launches = 4
+        self.f = None
+
+    def traffic(self):
+        return profiled_traffic("multi16", PROFILE_TRAFFIC_MULTI16, GENERAL_SOURCES)
+
+
 def selected_algorithmic_bytes(S, N, D, R, K, E, P):
     """Selected-query read: as the multi-query read with K slots per token,
     plus the ids [N, K] (int64) read by both kernels and the [P, E*R] FP32
@@ -701,9 +739,10 @@ class BlockRead:
 
 
 WORKLOADS = {"long": LongRead, "short": ShortRead, "sliced": SlicedRead, "deep": DeepRead, "multi": MultiRead,
+             "multi16": Multi16Read,
              "selected": SelectedRead, "block": BlockRead}
-FULL_TOKENS = {"long": 32768, "short": 8192, "sliced": 16384, "deep": 8192, "multi": 32768, "selected": 32768,
-               "block": 16384}
+FULL_TOKENS = {"long": 32768, "short": 8192, "sliced": 16384, "deep": 8192, "multi": 32768, "multi16": 32768,
+               "selected": 32768, "block": 16384}
 
 
 def make_exchange(pg, work):

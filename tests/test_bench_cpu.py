@@ -46,7 +46,7 @@ def test_multi_byte_model():
     assert b["bwd"] == 2 * v + out + stats + 2 * 152 * 2 * 1024 * 4
 
 
-@pytest.mark.parametrize("workload", ["long", "short", "sliced", "deep", "multi", "selected", "block"])
+@pytest.mark.parametrize("workload", ["long", "short", "sliced", "deep", "multi", "multi16", "selected", "block"])
 def test_reference_arm_prints_one_json_line(workload):
     t0 = time.time()
     r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference",
@@ -66,6 +66,13 @@ def test_reference_arm_prints_one_json_line(workload):
     # ms_per_step is what a timed step measured: the steps fit in the run's wall time
     assert d["steps"] * d["ms_per_step"] * 1e-3 < wall
     assert d["config"]["sample_tokens"] == 16
+
+
+def test_sixteen_query_workload():
+    w = bench.Multi16Read(tokens=8)
+    assert (w.wl.S, w.wl.D, w.wl.R, w.wl.M) == (10, 1024, 1024, 16)
+    assert w.bytes_for(76) == bench.multi_algorithmic_bytes(10, 8, 1024, 1024, 16, 76)
+    assert "multi16" in bench.WORKLOADS and bench.FULL_TOKENS["multi16"] == 32768
 
 
 def test_extension_byte_models():
