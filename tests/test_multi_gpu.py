@@ -177,9 +177,17 @@ def test_multi_autograd_compile_and_shared_sources():
     assert yt.shape == (90, 2, 1024)
 
 
-def test_multi_long_full_size_sampled():
-    wl = make_multi_workload("long", device="cuda")
+@pytest.mark.parametrize("key", ["long", "sixteen"])
+def test_multi_full_size_sampled(key):
+    # the bench's multi-query workloads at full size, in its launch
+    # configuration: two quarter-rank queries (resident backward) and sixteen
+    # full-rank queries (tensor-core forward, general backward with the
+    # tensor-core gradient kernel)
+    wl = make_multi_workload(key, device="cuda")
     v, Q, dy = wl.values, wl.queries, wl.dy
+    info = attnres_multi_plan_info(v, wl.M, wl.R, key_offset=wl.key_offset)
+    assert info["bwd_general"] == (2 if key == "sixteen" else 0), info
+    assert info["fwd_tensor_cores"] == (1 if key == "sixteen" else 0), info
     fwd = attnres_multi_fwd(v, Q)
     bwd = attnres_multi_bwd(v, Q, dy, fwd)
     bwd2 = attnres_multi_bwd(v, Q, dy, fwd)
