@@ -12,30 +12,33 @@
 //
 // Kernel A (coefficients) walks a token's rows in blocks of columns: a
 // producer warp copies the block of the M dy rows and the S source rows into
-// a shared-memory ring (1-D TMA, rows padded so ldmatrix is conflict-free),
-// and the consumer warps form DA = DY[M x D] . V[S x D]^T, a contraction over
-// the whole row, with bf16 tensor-core MMAs (mma.sync m16n8k16: the products
-// of bf16 operands are exact, the sums FP32).  After the last block the
-// partial tiles are added in a fixed order, every query's coefficients are
-// formed in FP32 and the token's table [S][alpha_s0..alpha_sM-1,
-// b_s0..b_sM-1, c_s] goes to the workspace.
+// a shared-memory ring (1-D TMA, one copy per row; rows padded so ldmatrix is
+// conflict-free; queries past M and sources past S read one zero row), and
+// the consumer warps form DA = DY[M x D] . V[S x D]^T, a contraction over the
+// whole row, with bf16 tensor-core MMAs (mma.sync m16n8k16: the products of
+// bf16 operands are exact, the sums FP32).  After the last block the partial
+// tiles are added in a fixed order, every query's coefficients are formed in
+// FP32 and the token's table [S][alpha_s0..alpha_sM-1, b_s0..b_sM-1, c_s]
+// goes to the workspace.
 //
-// Kernel B (gradients) gives each CTA one block of 512 columns for a group of
-// tokens.  Thread t owns the column pair (2t, 2t+1) of the block: the token's
-// M dy values there, the M query values (fixed queries: for the whole
-// launch; selected queries: the token's bank rows) and the M dq sums live in
-// registers, so every source row costs one broadcast read of its
-// coefficient row, one read of the row's pair, 3M + 1 packed FMAs and one
-// 4-byte store (a warp stores 128 contiguous bytes).  dq: fixed queries keep
-// the sums in registers for all of the CTA's tokens and write one partial row
-// per token group; selected queries add each token's sums into the bank rows
-// of the group's partial row with L2 reductions (every address has one
-// writer thread, so the order and the result are fixed).  The finalize
-// kernel adds the groups' rows in order: bitwise reproducible.
+// Kernel B (gradients) gives each CTA one block of columns for a group of
+// tokens.  Here the SIMT form: thread t owns column pairs of the block and
+// holds the queries in pairs -- for query pair i and column c, {q_2i,
+// q_2i+1}, the token's dy values and the dq sums the same way -- so each
+// 16-byte load of a coefficient row gives two aligned pairs that feed the
+// packed FMAs directly (per source row and column pair: 3M/2 packed FMAs
+// per column, one read of the row's pair, one 4-byte store).  dq: fixed
+// queries keep the sums in registers for all of the CTA's tokens and write
+// one partial row per token group; selected queries add each token's sums
+// into the bank rows of the group's partial row with L2 reductions (every
+// address has one writer thread, so the order and the result are fixed).
+// The finalize kernel adds the groups' rows in order: bitwise reproducible.
+// With fixed queries, at most 16 sources and nine or more queries the plan
+// takes the tensor-core gradient kernel of attnres_multi_grad_mma.cu instead.
 //
 // The sources and dy are read twice (once per kernel); the resident one-CTA
-// kernels of attnres_multi_bwd.cu read them once and run the shapes they
-// hold with few queries.
+// kernels of attnres_multi_bwd.cu read them once and serve one or two
+// queries when a token fits.
 #include "device_utils.cuh"
 #include "kernels.cuh"
 
